@@ -1,0 +1,525 @@
+// Forward kernel of flexible-mask attention for sm_103a, and the logsumexp
+// merge of split work items.
+//
+// One persistent CTA per SM walks its share of the planner's work items.  An
+// item holds two 128-row halves (two query heads of one kv head, or two
+// consecutive q-tiles of one head) that share every K/V tile load.
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax for half 0 (thread = query row = TMEM lane)
+//   warps 4-7  softmax for half 1
+//   warp  8    TMA producer: Q tiles, then a ring of K/V stages
+//   warp  9    tcgen05 MMA issuer (and TMEM owner)
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
+// P (bf16) is written back over the first 64 columns of S and read from TMEM
+// by the P*V MMA.
+//
+// Per k-tile step j, the MMA order is  PV0(j), S0(j+1), PV1(j), S1(j+1), so
+// one half's softmax overlaps the other half's MMAs.  Because tcgen05 MMAs
+// complete in issue order, the commit that announces S_h(j+1) also tells the
+// softmax warps that PV_h(j) is done, which is when O_h may be rescaled.
+//
+// Online softmax (fp32, base 2): m is the running row maximum of
+// scale*log2(e)*s; it is only raised when a new maximum exceeds it by more
+// than 8 (then O and l are rescaled), so p = 2^(x - m) stays below 256.
+// Masked entries become -inf (only on PARTIAL steps), a row with no visible
+// key keeps l = 0 and is written as out = 0, lse = -inf.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "ffa_internal.cuh"
+#include "ffa_ptx.cuh"
+
+namespace ffa {
+namespace {
+
+constexpr int kFwdThreads = 320;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kChunks = D / 64;          // 128-byte column chunks per row
+  static constexpr int kTileBytes = 128 * D * 2;  // one 128 x D bf16 tile
+  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = 2 * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  // barrier indices
+  static constexpr int kBQFull = 0, kBQEmpty = 1, kBKFull = 2, kBVFull = 2 + kStages,
+                       kBKVEmpty = 2 + 2 * kStages, kBSFull = 2 + 3 * kStages,
+                       kBPFull = kBSFull + 2, kBOFull = kBPFull + 2, kBOEmpty = kBOFull + 2,
+                       kBDrain = kBOEmpty + 2, kNumBars = kBDrain + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + alignment slack
+};
+
+struct FwdParams {
+  const int4* steps;
+  const int* items;
+  const int* order;
+  int n_items;
+  const Slice* slices;
+  int Tq, Hq, g;
+  float scale_log2;
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_o;    // [slot][2][128][D]
+  float* part_lse;  // [slot][2][128], log2 units
+  int* err;
+  uint64_t wait_ns;
+};
+
+__device__ __forceinline__ bool item_at(const FwdParams& P, int r, const int*& it) {
+  const int G = gridDim.x, b = blockIdx.x;
+  const int pos = r * G + ((r & 1) ? (G - 1 - b) : b);
+  if (pos >= P.n_items) return false;
+  it = P.items + (size_t)P.order[pos] * kFiWords;
+  return true;
+}
+
+// Wait that ignores the abort flag (used to drain copies in flight).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_test(bar, parity)) {
+    if (globaltimer_ns() - t0 > ns) return;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    ffa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const FwdParams P) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kBarOff + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  int* abort_flag = reinterpret_cast<int*>(smem + C::kMiscOff + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::kBQFull), 1);
+    mbar_init(bar(C::kBQEmpty), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kBKFull + s), 1);
+      mbar_init(bar(C::kBVFull + s), 1);
+      mbar_init(bar(C::kBKVEmpty + s), 1);
+    }
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar(C::kBSFull + h), 1);
+      mbar_init(bar(C::kBPFull + h), 128);
+      mbar_init(bar(C::kBOFull + h), 1);
+      mbar_init(bar(C::kBOEmpty + h), 128);
+    }
+    mbar_init(bar(C::kBDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{abort_flag, P.err, P.wait_ns};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      uint32_t kv_cnt = 0, q_cnt = 0;
+      bool ok = true;
+      const int* it;
+      for (int r = 0; ok && item_at(P, r, it); ++r) {
+        const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
+        if (se <= sb) continue;
+        const bool act1 = it[kFiQt1] >= 0 && it[kFiH1] >= 0;
+        const int hk = it[kFiH0] / P.g;
+        if (!(ok = mbar_wait(bar(C::kBQEmpty), (q_cnt & 1) ^ 1, ctl, 100))) break;
+        mbar_arrive_expect_tx(bar(C::kBQFull), (act1 ? 2 : 1) * C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_2d(sbase + C::kQOff + c * 16384, &tm_q, bar(C::kBQFull),
+                      it[kFiH0] * D + c * 64, it[kFiQt0] * 128);
+        if (act1)
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_2d(sbase + C::kQOff + C::kTileBytes + c * 16384, &tm_q, bar(C::kBQFull),
+                        it[kFiH1] * D + c * 64, it[kFiQt1] * 128);
+        ++q_cnt;
+        for (int j = sb; j < se; ++j) {
+          const int kt = P.steps[j].x;
+          const int stage = kv_cnt % C::kStages;
+          const uint32_t ph = (kv_cnt / C::kStages) & 1;
+          if (!(ok = mbar_wait(bar(C::kBKVEmpty + stage), ph ^ 1, ctl, 101))) break;
+          mbar_arrive_expect_tx(bar(C::kBKFull + stage), C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_2d(sbase + C::kKOff + stage * C::kTileBytes + c * 16384, &tm_k,
+                        bar(C::kBKFull + stage), hk * D + c * 64, kt * 128);
+          mbar_arrive_expect_tx(bar(C::kBVFull + stage), C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_2d(sbase + C::kVOff + stage * C::kTileBytes + c * 16384, &tm_v,
+                        bar(C::kBVFull + stage), hk * D + c * 64, kt * 128);
+          ++kv_cnt;
+        }
+      }
+      if (!ok) {
+        // Aborted: let the copies already issued land before the CTA exits.
+        if (q_cnt > 0) drain_wait(bar(C::kBQFull), (q_cnt - 1) & 1, P.wait_ns);
+        for (uint32_t i = kv_cnt > (uint32_t)C::kStages ? kv_cnt - C::kStages : 0; i < kv_cnt; ++i) {
+          drain_wait(bar(C::kBKFull + i % C::kStages), (i / C::kStages) & 1, P.wait_ns);
+          drain_wait(bar(C::kBVFull + i % C::kStages), (i / C::kStages) & 1, P.wait_ns);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
+      auto issue_s = [&](int h, int stage) {
+        const uint32_t qa = sbase + C::kQOff + h * C::kTileBytes;
+        const uint32_t ka = sbase + C::kKOff + stage * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + h * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                 kIdS, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int h, int stage, bool acc) {
+        const uint32_t va = sbase + C::kVOff + stage * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + 256 + h * 128, tmem + h * 128 + kk * 8,
+                 sdesc_sw128(va + kk * 2048, 16384, 1024), kIdPV, (acc || kk > 0) ? 1u : 0u);
+      };
+      uint32_t kv_cnt = 0, q_cnt = 0, p_cnt[2] = {0, 0}, oe_cnt[2] = {0, 0};
+      bool ok = true;
+      const int* it;
+      for (int r = 0; ok && item_at(P, r, it); ++r) {
+        const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
+        if (se <= sb) continue;
+        const bool act1 = it[kFiQt1] >= 0 && it[kFiH1] >= 0;
+        if (!(ok = mbar_wait(bar(C::kBQFull), q_cnt & 1, ctl, 200))) break;
+        ++q_cnt;
+        tc_fence_after();
+        bool first_pv[2] = {true, true};
+        int4 cur = P.steps[sb];
+        {
+          const int stage = kv_cnt % C::kStages;
+          if (!(ok = mbar_wait(bar(C::kBKFull + stage), (kv_cnt / C::kStages) & 1, ctl, 201)))
+            break;
+          tc_fence_after();
+          if (cur.y >= 0) {
+            issue_s(0, stage);
+            mma_commit(bar(C::kBSFull + 0));
+          }
+          if (act1 && cur.z >= 0) {
+            issue_s(1, stage);
+            mma_commit(bar(C::kBSFull + 1));
+          }
+        }
+        for (int j = sb; ok && j < se; ++j) {
+          const uint32_t c = kv_cnt + (uint32_t)(j - sb);
+          const int stage = c % C::kStages;
+          const uint32_t ph = (c / C::kStages) & 1;
+          const int stage_n = (c + 1) % C::kStages;
+          const uint32_t ph_n = ((c + 1) / C::kStages) & 1;
+          const bool has_next = j + 1 < se;
+          const int4 nxt = has_next ? P.steps[j + 1] : make_int4(0, -1, -1, 0);
+          bool v_ready = false, k_next_ready = false;
+          for (int h = 0; h < 2; ++h) {
+            const int info = h == 0 ? cur.y : (act1 ? cur.z : -1);
+            if (info >= 0) {
+              if (!(ok = mbar_wait(bar(C::kBPFull + h), p_cnt[h] & 1, ctl, 210 + h))) break;
+              ++p_cnt[h];
+              if (first_pv[h]) {
+                if (!(ok = mbar_wait(bar(C::kBOEmpty + h), (oe_cnt[h] & 1) ^ 1, ctl, 212 + h)))
+                  break;
+                ++oe_cnt[h];
+              }
+              if (!v_ready) {
+                if (!(ok = mbar_wait(bar(C::kBVFull + stage), ph, ctl, 214))) break;
+                v_ready = true;
+              }
+              tc_fence_after();
+              issue_pv(h, stage, !first_pv[h]);
+              first_pv[h] = false;
+            }
+            const int ninfo = h == 0 ? nxt.y : (act1 ? nxt.z : -1);
+            if (has_next && ninfo >= 0) {
+              if (!k_next_ready) {
+                if (!(ok = mbar_wait(bar(C::kBKFull + stage_n), ph_n, ctl, 215))) break;
+                k_next_ready = true;
+                tc_fence_after();
+              }
+              issue_s(h, stage_n);
+              mma_commit(bar(C::kBSFull + h));
+            }
+          }
+          if (!ok) break;
+          mma_commit(bar(C::kBKVEmpty + stage));
+          cur = nxt;
+        }
+        if (!ok) break;
+        for (int h = 0; h < 2; ++h)
+          if (!first_pv[h]) mma_commit(bar(C::kBOFull + h));
+        mma_commit(bar(C::kBQEmpty));
+        kv_cnt += (uint32_t)(se - sb);
+      }
+      // Every MMA issued so far must finish before TMEM is released.
+      mma_commit(bar(C::kBDrain));
+      drain_wait(bar(C::kBDrain), 0, P.wait_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int h = warp >> 2;
+    const int row_in = threadIdx.x & 127;
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + h * 128;
+    const uint32_t tO = tmem + lane_addr + 256 + h * 128;
+    uint32_t s_cnt = 0, o_cnt = 0;
+    bool ok = true;
+    const int* it;
+    for (int r = 0; ok && item_at(P, r, it); ++r) {
+      const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
+      const bool act1 = it[kFiQt1] >= 0 && it[kFiH1] >= 0;
+      if (h == 1 && !act1) continue;
+      const int qt = it[kFiQt0 + h], head = it[kFiH0 + h], slot = it[kFiSlot];
+      const int row = qt * 128 + row_in;
+      float m = -INFINITY, l = 0.f;
+      bool visited = false;
+      for (int j = sb; j < se; ++j) {
+        const int4 st = P.steps[j];
+        const int info = h == 0 ? st.y : st.z;
+        if (info < 0) continue;
+        const bool w = mbar_wait(bar(C::kBSFull + h), s_cnt & 1, ctl, 300 + h);
+        if (!(ok = __all_sync(0xffffffffu, w))) break;
+        ++s_cnt;
+        tc_fence_after();
+        float s[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t u[32];
+          tmem_ld32(tS + 32 * c, u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(u[i]);
+        }
+        if (info & 1) {
+          const Slice sl = P.slices[info >> 1];
+          int lo = 0, hi = 0;
+          if (row >= sl.qs && row < sl.qe) {
+            lo = sl.ks + ((sl.t & 2) ? row - sl.qs : 0) - st.x * 128;
+            hi = sl.ke - ((sl.t & 1) ? sl.qe - 1 - row : 0) - st.x * 128;
+          }
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c < lo || c >= hi) s[c] = -INFINITY;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        const float m_cand = mx * P.scale_log2;
+        const bool raise = m_cand > m + kRescaleThreshold;
+        const bool rescale_o = raise && visited && m > -INFINITY;
+        const float alpha = raise ? exp2f(m - m_cand) : 1.f;
+        if (__any_sync(0xffffffffu, rescale_o)) {
+          const float a = rescale_o ? alpha : 1.f;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t u[32];
+            tmem_ld32(tO + 32 * c, u);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * a);
+            tmem_st32(tO + 32 * c, u);
+          }
+          tmem_st_wait();
+        }
+        if (raise) {
+          l *= alpha;
+          m = m_cand;
+        }
+        const float mu = m == -INFINITY ? 0.f : m;
+        float rs = 0.f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float p0 = ex2_approx(fmaf(s[2 * c], P.scale_log2, -mu));
+          const float p1 = ex2_approx(fmaf(s[2 * c + 1], P.scale_log2, -mu));
+          rs += p0 + p1;
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        l += rs;
+        tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::kBPFull + h));
+        visited = true;
+      }
+      if (!ok) break;
+      // ---- epilogue
+      float o[D];
+      if (visited) {
+        const bool w = mbar_wait(bar(C::kBOFull + h), o_cnt & 1, ctl, 310 + h);
+        if (!(ok = __all_sync(0xffffffffu, w))) break;
+        ++o_cnt;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t u[32];
+          tmem_ld32(tO + 32 * c, u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[32 * c + i] = __uint_as_float(u[i]);
+        }
+        tc_fence_before();
+        mbar_arrive(bar(C::kBOEmpty + h));
+      } else {
+#pragma unroll
+        for (int d = 0; d < D; ++d) o[d] = 0.f;
+      }
+      const bool nonempty = l > 0.f;
+      const float inv_l = nonempty ? 1.f / l : 0.f;
+      if (slot < 0) {
+        if (row < P.Tq) {
+          uint4* dst = reinterpret_cast<uint4*>(P.out + ((size_t)row * P.Hq + head) * D);
+#pragma unroll
+          for (int v = 0; v < D / 8; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(o[8 * v + 0] * inv_l, o[8 * v + 1] * inv_l);
+            w.y = pack_bf16x2(o[8 * v + 2] * inv_l, o[8 * v + 3] * inv_l);
+            w.z = pack_bf16x2(o[8 * v + 4] * inv_l, o[8 * v + 5] * inv_l);
+            w.w = pack_bf16x2(o[8 * v + 6] * inv_l, o[8 * v + 7] * inv_l);
+            dst[v] = w;
+          }
+          P.lse[(size_t)head * P.Tq + row] = nonempty ? (m + log2f(l)) * kLn2 : -INFINITY;
+        }
+      } else {
+        const size_t base = ((size_t)slot * 2 + h) * 128 + row_in;
+        float4* dst = reinterpret_cast<float4*>(P.part_o + base * D);
+#pragma unroll
+        for (int v = 0; v < D / 4; ++v)
+          dst[v] = make_float4(o[4 * v] * inv_l, o[4 * v + 1] * inv_l, o[4 * v + 2] * inv_l,
+                               o[4 * v + 3] * inv_l);
+        P.part_lse[base] = nonempty ? m + log2f(l) : -INFINITY;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Logsumexp merge of split items: one block per (group, half), one thread per row.
+template <int D>
+__global__ void __launch_bounds__(128)
+    ffa_merge_kernel(const int* __restrict__ merges, const float* __restrict__ part_o,
+                     const float* __restrict__ part_lse, int Tq, int Hq,
+                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+  const int grp = blockIdx.x >> 1, h = blockIdx.x & 1;
+  const int* mg = merges + (size_t)grp * kMgWords;
+  const int qt = mg[kMgQt0 + h], head = mg[kMgH0 + h];
+  if (qt < 0 || head < 0) return;
+  const int row_in = threadIdx.x, row = qt * 128 + row_in;
+  if (row >= Tq) return;
+  const int s0 = mg[kMgSlotBeg], ns = mg[kMgSlots];
+  float mx = -INFINITY;
+  for (int s = 0; s < ns; ++s)
+    mx = fmaxf(mx, part_lse[((size_t)(s0 + s) * 2 + h) * 128 + row_in]);
+  float acc[D];
+#pragma unroll
+  for (int d = 0; d < D; ++d) acc[d] = 0.f;
+  float wsum = 0.f;
+  if (mx > -INFINITY) {
+    for (int s = 0; s < ns; ++s) {
+      const size_t base = ((size_t)(s0 + s) * 2 + h) * 128 + row_in;
+      const float w = exp2f(part_lse[base] - mx);
+      wsum += w;
+      const float4* src = reinterpret_cast<const float4*>(part_o + base * D);
+#pragma unroll
+      for (int v = 0; v < D / 4; ++v) {
+        const float4 x = src[v];
+        acc[4 * v] += w * x.x;
+        acc[4 * v + 1] += w * x.y;
+        acc[4 * v + 2] += w * x.z;
+        acc[4 * v + 3] += w * x.w;
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)row * Hq + head) * D);
+#pragma unroll
+  for (int v = 0; v < D / 8; ++v) {
+    uint4 w;
+    w.x = pack_bf16x2(acc[8 * v + 0] * inv, acc[8 * v + 1] * inv);
+    w.y = pack_bf16x2(acc[8 * v + 2] * inv, acc[8 * v + 3] * inv);
+    w.z = pack_bf16x2(acc[8 * v + 4] * inv, acc[8 * v + 5] * inv);
+    w.w = pack_bf16x2(acc[8 * v + 6] * inv, acc[8 * v + 7] * inv);
+    dst[v] = w;
+  }
+  lse[(size_t)head * Tq + row] = wsum > 0.f ? (mx + log2f(wsum)) * kLn2 : -INFINITY;
+}
+
+template <int D>
+ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const void* v, float scale,
+                          void* out, float* lse, void* ws, cudaStream_t st) {
+  using C = FwdCfg<D>;
+  alignas(64) CUtensorMap tq, tk, tv;
+  if (!encode_tile_map(&tq, q, p->Tq, p->Hq * D) || !encode_tile_map(&tk, k, p->Tk, p->Hkv * D) ||
+      !encode_tile_map(&tv, v, p->Tk, p->Hkv * D))
+    return FFA_ERR_INVALID_ARG;
+  FwdParams P;
+  P.steps = p->fwd_steps;
+  P.items = p->fwd_items;
+  P.order = p->fwd_order;
+  P.n_items = (int)p->n_fwd_items;
+  P.slices = p->slices;
+  P.Tq = p->Tq;
+  P.Hq = p->Hq;
+  P.g = p->Hq / p->Hkv;
+  P.scale_log2 = scale * kLog2e;
+  P.out = static_cast<__nv_bfloat16*>(out);
+  P.lse = lse;
+  P.part_o = static_cast<float*>(ws);
+  P.part_lse = P.part_o ? P.part_o + (size_t)p->n_slots * 2 * 128 * D : nullptr;
+  P.err = p->err;
+  P.wait_ns = p->wait_ns;
+  if (cudaFuncSetAttribute(ffa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmemBytes) != cudaSuccess)
+    return FFA_ERR_CUDA;
+  ffa_fwd_kernel<D><<<p->grid_fwd, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, P);
+  if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
+  if (p->n_merges > 0) {
+    ffa_merge_kernel<D><<<(int)(2 * p->n_merges), 128, 0, st>>>(
+        p->merges, P.part_o, P.part_lse, p->Tq, p->Hq, P.out, lse);
+    if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
+  }
+  return FFA_OK;
+}
+
+}  // namespace
+
+size_t fwd_workspace_bytes(const ffa_plan_s* p) {
+  return (size_t)p->n_slots * 2 * 128 * (p->D + 1) * sizeof(float);
+}
+
+ffa_status_t launch_fwd(ffa_plan_s* p, const void* q, const void* k, const void* v, float scale,
+                        void* out, float* lse, void* ws, size_t, cudaStream_t st) {
+  if (p->D == 128) return launch_fwd_d<128>(p, q, k, v, scale, out, lse, ws, st);
+  if (p->D == 64) return launch_fwd_d<64>(p, q, k, v, scale, out, lse, ws, st);
+  return FFA_ERR_UNSUPPORTED;
+}
+
+}  // namespace ffa

@@ -1,0 +1,84 @@
+// Internal layout shared by the planner, forward and backward translation
+// units of libffa.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ffa.h"
+#include "ffa_segments.cuh"
+
+namespace ffa {
+
+constexpr int kTile = 128;  // q rows and k columns per tile
+
+// A slice as stored by the plan: [qs, qe) x [ks, ke), mask type t.
+using Slice = SliceDesc;
+
+// Visit info word: (slice << 1) | partial, or -1 when the half skips the step.
+__host__ __device__ constexpr int visit_info(int slice, bool partial) {
+  return (slice << 1) | (partial ? 1 : 0);
+}
+
+// Forward step (int4): x = k-tile, y = info for half 0, z = info for half 1.
+// Forward item (8 x int32):
+enum FwdItem : int {
+  kFiQt0 = 0,     // q-tile of half 0
+  kFiQt1 = 1,     // q-tile of half 1 (-1: half 1 idle)
+  kFiH0 = 2,      // query head of half 0
+  kFiH1 = 3,      // query head of half 1 (-1: half 1 idle)
+  kFiStepBeg = 4, // first step (index into the step array)
+  kFiStepEnd = 5, // one past the last step
+  kFiSlot = 6,    // -1: write out/lse; else partial-result slot (split items)
+  kFiCost = 7,
+  kFiWords = 8
+};
+// Backward step (int4): x = q-tile, y = info.
+// Backward item (8 x int32):
+enum BwdItem : int {
+  kBiKt = 0, kBiHkv = 1, kBiStepBeg = 2, kBiStepEnd = 3, kBiCost = 4, kBiWords = 8
+};
+// Merge group (8 x int32): halves of one split forward item.
+enum MergeGroup : int {
+  kMgQt0 = 0, kMgQt1 = 1, kMgH0 = 2, kMgH1 = 3, kMgSlotBeg = 4, kMgSlots = 5, kMgWords = 8
+};
+
+}  // namespace ffa
+
+struct ffa_plan_s {
+  int device = 0;
+  int Tq = 0, Tk = 0, Hq = 0, Hkv = 0, D = 0, S = 0;
+  int num_sms = 0;
+  int n_qt = 0, n_kt = 0;
+  ffa::Slice* slices = nullptr;  // device [S]
+  int4* fwd_steps = nullptr;
+  int64_t n_fwd_steps = 0;
+  int* fwd_items = nullptr;
+  int64_t n_fwd_items = 0;
+  int* fwd_order = nullptr;
+  int* merges = nullptr;
+  int64_t n_merges = 0;
+  int n_slots = 0;  // partial-result slots (split forward items)
+  int4* bwd_steps = nullptr;
+  int64_t n_bwd_steps = 0;
+  int* bwd_items = nullptr;
+  int64_t n_bwd_items = 0;
+  int* bwd_order = nullptr;
+  int* err = nullptr;  // device [2]: code, location
+  int grid_fwd = 0, grid_bwd = 0;
+  int64_t area = 0;
+  uint64_t wait_ns = 2000000000ull;
+};
+
+namespace ffa {
+// Implemented in ffa_fwd.cu / ffa_bwd.cu.
+ffa_status_t launch_fwd(ffa_plan_s* p, const void* q, const void* k, const void* v, float scale,
+                        void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t st);
+size_t fwd_workspace_bytes(const ffa_plan_s* p);
+ffa_status_t launch_bwd(ffa_plan_s* p, const void* q, const void* k, const void* v,
+                        const void* out, const void* dout, const float* lse, float scale,
+                        void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, cudaStream_t st);
+size_t bwd_workspace_bytes(const ffa_plan_s* p);
+// Implemented in ffa_plan.cu.
+bool encode_tile_map(void* map128, const void* base, int rows, int cols_elems);
+}  // namespace ffa

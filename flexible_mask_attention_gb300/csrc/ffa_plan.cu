@@ -1,0 +1,784 @@
+// Slice planner and tile scheduler (device kernels) plus the host side of the
+// C ABI declared in include/ffa.h.
+//
+// Work-list specification (all of it computed on the device):
+//   * Forward visits of q-tile qt: every (k-tile kt, slice s) whose tile
+//     holds a visible entry of s, kind FULL when all 128 x 128 entries are
+//     visible, PARTIAL otherwise; ordered by (kt, s).
+//   * Forward units pair two 128-row halves that share K/V tiles:
+//       - grouped-query heads (Hq / Hkv >= 2): one q-tile, two query heads of
+//         the same kv head; the steps are the q-tile's visits;
+//       - otherwise: q-tiles 2u and 2u+1 of one head; the steps merge the two
+//         visit lists on kt (equal kt -> one shared step, in list order).
+//   * Item cost = sum over its steps and busy halves of 4 (FULL) or 5
+//     (PARTIAL).  Items are sorted by (cost descending, index ascending) and
+//     dealt to the persistent CTAs in a snake order.
+//   * While fewer than `split_below` items have work, each such item is cut
+//     into equal runs of steps whose partial results are merged by
+//     logsumexp afterwards.
+//   * Backward visits of k-tile kt: every (q-tile, slice) pair, same kinds,
+//     ordered by (qt, s); one item per (kt, kv head), cost g * visit costs.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "ffa_internal.cuh"
+
+namespace ffa {
+namespace {
+
+constexpr int kFullCost = 4, kPartialCost = 5;
+constexpr int kMaxLocalSegs = 64;
+
+__global__ void k_pack_slices(const int* __restrict__ qr, const int* __restrict__ kr,
+                              const int* __restrict__ ty, int S, Slice* out) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s < S) out[s] = Slice{qr[2 * s], qr[2 * s + 1], kr[2 * s], kr[2 * s + 1], ty[s]};
+}
+
+// flags[0]: bad range/type, flags[1]: overlap.  area: visible pairs per head.
+__global__ void k_check_slices(const Slice* __restrict__ sl, int S, int Tq, int Tk, int* flags,
+                               unsigned long long* area) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= S) return;
+  const Slice x = sl[s];
+  if (x.qs < 0 || x.qs > x.qe || x.qe > Tq || x.ks < 0 || x.ks > x.ke || x.ke > Tk || x.t < 0 ||
+      x.t > 3) {
+    atomicExch(&flags[0], 1);
+    return;
+  }
+  atomicAdd(area, (unsigned long long)slice_area(x));
+}
+
+__global__ void k_check_overlap(const Slice* __restrict__ sl, int S, int* flags) {
+  const long long p = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (p >= (long long)S * S) return;
+  const int i = (int)(p / S), j = (int)(p % S);
+  if (i >= j) return;
+  const Slice a = sl[i], b = sl[j];
+  if (a.qs >= a.qe || a.ks >= a.ke || b.qs >= b.qe || b.ks >= b.ke) return;
+  const bool q_meet = a.qs < b.qe && b.qs < a.qe;
+  const bool k_meet = a.ks < b.ke && b.ks < a.ke;
+  if (q_meet && k_meet) atomicExch(&flags[1], 1);
+}
+
+// Single-block exclusive scan of n int32 counts; total in *total.
+__global__ void k_scan(const int* __restrict__ in, int n, int* __restrict__ out, long long* total) {
+  __shared__ long long part[1024];
+  const int T = blockDim.x, t = threadIdx.x;
+  const int per = (n + T - 1) / T;
+  const int b = t * per, e = min(n, b + per);
+  long long s = 0;
+  for (int i = b; i < e; ++i) s += in[i];
+  part[t] = s;
+  __syncthreads();
+  for (int off = 1; off < T; off <<= 1) {
+    long long v = t >= off ? part[t - off] : 0;
+    __syncthreads();
+    part[t] += v;
+    __syncthreads();
+  }
+  long long run = part[t] - s;
+  for (int i = b; i < e; ++i) {
+    out[i] = (int)run;
+    run += in[i];
+  }
+  if (t == T - 1) *total = part[t];
+}
+
+// ---- forward visits ---------------------------------------------------------
+__global__ void k_fwd_visit_count(const Slice* __restrict__ sl, int S, int n_qt, int* cnt) {
+  const int qt = blockIdx.x * blockDim.x + threadIdx.x;
+  if (qt >= n_qt) return;
+  int c = 0;
+  for (int s = 0; s < S; ++s) {
+    TileRun r;
+    if (fwd_tile_run(sl[s], qt, r)) c += r.e - r.b;
+  }
+  cnt[qt] = c;
+}
+
+// Emits (kt, info) for one tile in (kt, slice) order.  `Run` computes the
+// slice's tile run for this tile index.
+template <bool kFwd>
+__device__ void emit_visits(const Slice* __restrict__ sl, int S, int tile, int2* out) {
+  TileRun local[kMaxLocalSegs];
+  int local_s[kMaxLocalSegs];
+  int nseg = 0, lo = 0x7fffffff, hi = 0;
+  bool overflow = false;
+  for (int s = 0; s < S; ++s) {
+    TileRun r;
+    const bool ok = kFwd ? fwd_tile_run(sl[s], tile, r) : bwd_tile_run(sl[s], tile, r);
+    if (!ok) continue;
+    lo = min(lo, r.b);
+    hi = max(hi, r.e);
+    if (nseg < kMaxLocalSegs) {
+      local[nseg] = r;
+      local_s[nseg] = s;
+    } else {
+      overflow = true;
+    }
+    ++nseg;
+  }
+  int w = 0;
+  for (int x = lo; x < hi; ++x) {
+    if (!overflow) {
+      for (int i = 0; i < nseg; ++i) {
+        const TileRun& r = local[i];
+        if (x >= r.b && x < r.e)
+          out[w++] = make_int2(x, visit_info(local_s[i], !(x >= r.fb && x < r.fe)));
+      }
+    } else {
+      for (int s = 0; s < S; ++s) {
+        TileRun r;
+        const bool ok = kFwd ? fwd_tile_run(sl[s], tile, r) : bwd_tile_run(sl[s], tile, r);
+        if (ok && x >= r.b && x < r.e)
+          out[w++] = make_int2(x, visit_info(s, !(x >= r.fb && x < r.fe)));
+      }
+    }
+  }
+}
+
+__global__ void k_fwd_visit_fill(const Slice* __restrict__ sl, int S, int n_qt,
+                                 const int* __restrict__ off, int2* visits) {
+  const int qt = blockIdx.x * blockDim.x + threadIdx.x;
+  if (qt >= n_qt) return;
+  emit_visits<true>(sl, S, qt, visits + off[qt]);
+}
+
+__device__ __forceinline__ int visit_cost(int info) {
+  return (info & 1) ? kPartialCost : kFullCost;
+}
+
+// Steps of forward unit u.  pair_mode 0: heads share q-tile u.  1: q-tiles
+// 2u and 2u+1 share a head; visits merged on kt.
+__global__ void k_fwd_unit_count(const int2* __restrict__ visits, const int* __restrict__ voff,
+                                 const int* __restrict__ vcnt, int n_qt, int n_units,
+                                 int pair_mode, int* scnt, int* cost_half) {
+  const int u = blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= n_units) return;
+  if (pair_mode == 0) {
+    const int2* a = visits + voff[u];
+    int c = 0;
+    for (int i = 0; i < vcnt[u]; ++i) c += visit_cost(a[i].y);
+    scnt[u] = vcnt[u];
+    cost_half[2 * u] = cost_half[2 * u + 1] = c;
+    return;
+  }
+  const int qa = 2 * u, qb = 2 * u + 1;
+  const int na = vcnt[qa], nb = qb < n_qt ? vcnt[qb] : 0;
+  const int2* a = visits + voff[qa];
+  const int2* b = qb < n_qt ? visits + voff[qb] : nullptr;
+  int i = 0, j = 0, n = 0, ca = 0, cb = 0;
+  while (i < na || j < nb) {
+    if (j >= nb || (i < na && a[i].x < b[j].x)) {
+      ca += visit_cost(a[i].y);
+      ++i;
+    } else if (i >= na || b[j].x < a[i].x) {
+      cb += visit_cost(b[j].y);
+      ++j;
+    } else {
+      ca += visit_cost(a[i].y);
+      cb += visit_cost(b[j].y);
+      ++i;
+      ++j;
+    }
+    ++n;
+  }
+  scnt[u] = n;
+  cost_half[2 * u] = ca;
+  cost_half[2 * u + 1] = cb;
+}
+
+__global__ void k_fwd_unit_fill(const int2* __restrict__ visits, const int* __restrict__ voff,
+                                const int* __restrict__ vcnt, int n_qt, int n_units,
+                                int pair_mode, const int* __restrict__ soff, int4* steps) {
+  const int u = blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= n_units) return;
+  int4* o = steps + soff[u];
+  if (pair_mode == 0) {
+    const int2* a = visits + voff[u];
+    for (int i = 0; i < vcnt[u]; ++i) o[i] = make_int4(a[i].x, a[i].y, a[i].y, 0);
+    return;
+  }
+  const int qa = 2 * u, qb = 2 * u + 1;
+  const int na = vcnt[qa], nb = qb < n_qt ? vcnt[qb] : 0;
+  const int2* a = visits + voff[qa];
+  const int2* b = qb < n_qt ? visits + voff[qb] : nullptr;
+  int i = 0, j = 0, n = 0;
+  while (i < na || j < nb) {
+    if (j >= nb || (i < na && a[i].x < b[j].x)) {
+      o[n] = make_int4(a[i].x, a[i].y, -1, 0);
+      ++i;
+    } else if (i >= na || b[j].x < a[i].x) {
+      o[n] = make_int4(b[j].x, -1, b[j].y, 0);
+      ++j;
+    } else {
+      o[n] = make_int4(a[i].x, a[i].y, b[j].y, 0);
+      ++i;
+      ++j;
+    }
+    ++n;
+  }
+}
+
+__global__ void k_fwd_items(int n_items, int pair_mode, int g, int Hkv, int Hq, int pairs,
+                            int n_qt, const int* __restrict__ soff, const int* __restrict__ scnt,
+                            const int* __restrict__ cost_half, int* items, int* live) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n_items) return;
+  int u, qt0, qt1, h0, h1;
+  if (pair_mode == 0) {
+    u = idx / (Hkv * pairs);
+    const int rem = idx % (Hkv * pairs);
+    const int hk = rem / pairs, p = rem % pairs;
+    qt0 = qt1 = u;
+    h0 = hk * g + 2 * p;
+    h1 = (2 * p + 1 < g) ? h0 + 1 : -1;
+    if (h1 < 0) qt1 = -1;
+  } else {
+    u = idx / Hq;
+    h0 = idx % Hq;
+    qt0 = 2 * u;
+    qt1 = (2 * u + 1 < n_qt) ? 2 * u + 1 : -1;
+    h1 = qt1 >= 0 ? h0 : -1;
+  }
+  int* it = items + (size_t)idx * kFiWords;
+  it[kFiQt0] = qt0;
+  it[kFiQt1] = qt1;
+  it[kFiH0] = h0;
+  it[kFiH1] = h1;
+  it[kFiStepBeg] = soff[u];
+  it[kFiStepEnd] = soff[u] + scnt[u];
+  it[kFiSlot] = -1;
+  it[kFiCost] = cost_half[2 * u] + (h1 >= 0 ? cost_half[2 * u + 1] : 0);
+  if (scnt[u] > 0) atomicAdd(live, 1);
+}
+
+// Split: chunk counts per item, then the chunked item list and merge groups.
+__global__ void k_split_count(const int* __restrict__ items, int n_items, int nsplit, int* chunks,
+                              int* slots, int* groups) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_items) return;
+  const int* it = items + (size_t)i * kFiWords;
+  const int n = it[kFiStepEnd] - it[kFiStepBeg];
+  const int c = max(1, min(nsplit, n));
+  chunks[i] = c;
+  slots[i] = c >= 2 ? c : 0;
+  groups[i] = c >= 2 ? 1 : 0;
+}
+
+__global__ void k_split_fill(const int* __restrict__ items, int n_items,
+                             const int* __restrict__ chunks, const int* __restrict__ coff,
+                             const int* __restrict__ soff, const int* __restrict__ goff,
+                             int* out_items, int* merges) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_items) return;
+  const int* it = items + (size_t)i * kFiWords;
+  const int c = chunks[i];
+  const int b = it[kFiStepBeg], n = it[kFiStepEnd] - b;
+  for (int k = 0; k < c; ++k) {
+    int* o = out_items + (size_t)(coff[i] + k) * kFiWords;
+    for (int w = 0; w < kFiWords; ++w) o[w] = it[w];
+    if (c >= 2) {
+      const int kb = b + (int)((long long)k * n / c), ke = b + (int)((long long)(k + 1) * n / c);
+      o[kFiStepBeg] = kb;
+      o[kFiStepEnd] = ke;
+      o[kFiSlot] = soff[i] + k;
+      o[kFiCost] = (int)((long long)it[kFiCost] * (ke - kb) / max(n, 1));
+    }
+  }
+  if (c >= 2) {
+    int* m = merges + (size_t)goff[i] * kMgWords;
+    m[kMgQt0] = it[kFiQt0];
+    m[kMgQt1] = it[kFiQt1];
+    m[kMgH0] = it[kFiH0];
+    m[kMgH1] = it[kFiH1];
+    m[kMgSlotBeg] = soff[i];
+    m[kMgSlots] = c;
+    m[6] = m[7] = 0;
+  }
+}
+
+// ---- backward visits --------------------------------------------------------
+__global__ void k_bwd_visit_count(const Slice* __restrict__ sl, int S, int n_kt, int* cnt) {
+  const int kt = blockIdx.x * blockDim.x + threadIdx.x;
+  if (kt >= n_kt) return;
+  int c = 0;
+  for (int s = 0; s < S; ++s) {
+    TileRun r;
+    if (bwd_tile_run(sl[s], kt, r)) c += r.e - r.b;
+  }
+  cnt[kt] = c;
+}
+
+__global__ void k_bwd_visit_fill(const Slice* __restrict__ sl, int S, int n_kt,
+                                 const int* __restrict__ off, int2* visits) {
+  const int kt = blockIdx.x * blockDim.x + threadIdx.x;
+  if (kt >= n_kt) return;
+  emit_visits<false>(sl, S, kt, visits + off[kt]);
+}
+
+__global__ void k_bwd_items(int n_kt, int Hkv, int g, const int2* __restrict__ visits,
+                            const int* __restrict__ off, const int* __restrict__ cnt,
+                            int4* steps, int* items) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n_kt * Hkv) return;
+  const int kt = idx / Hkv, hk = idx % Hkv;
+  const int b = off[kt], n = cnt[kt];
+  int c = 0;
+  for (int i = 0; i < n; ++i) {
+    const int2 v = visits[b + i];
+    c += visit_cost(v.y);
+    if (hk == 0) steps[b + i] = make_int4(v.x, v.y, 0, 0);
+  }
+  int* it = items + (size_t)idx * kBiWords;
+  it[kBiKt] = kt;
+  it[kBiHkv] = hk;
+  it[kBiStepBeg] = b;
+  it[kBiStepEnd] = b + n;
+  it[kBiCost] = c * g;
+  it[5] = it[6] = it[7] = 0;
+}
+
+// ---- ordering ---------------------------------------------------------------
+// One block: bitonic sort of (cost desc, index asc) keys in `scratch`
+// (n2 = next power of two >= n entries), then order[r] = index.
+__global__ void k_sort_order(const int* __restrict__ items, int words, int cost_word, int n,
+                             int n2, unsigned long long* scratch, int* order) {
+  for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+    unsigned long long key = ~0ull;
+    if (i < n) {
+      const unsigned int c = (unsigned int)items[(size_t)i * words + cost_word];
+      key = ((unsigned long long)(0x7fffffffu - c) << 32) | (unsigned int)i;
+    }
+    scratch[i] = key;
+  }
+  __syncthreads();
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+        const int l = i ^ j;
+        if (l > i) {
+          const unsigned long long a = scratch[i], b = scratch[l];
+          const bool up = (i & k) == 0;
+          if ((a > b) == up) {
+            scratch[i] = b;
+            scratch[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < n; i += blockDim.x) order[i] = (int)(scratch[i] & 0xffffffffu);
+}
+
+// ---- host helpers -----------------------------------------------------------
+struct DevBuf {
+  void* p = nullptr;
+  ~DevBuf() {
+    if (p) cudaFree(p);
+  }
+  template <class T>
+  T* as() {
+    return static_cast<T*>(p);
+  }
+  cudaError_t alloc(size_t bytes) {
+    return cudaMalloc(&p, bytes > 0 ? bytes : 16);
+  }
+  void* release() {
+    void* q = p;
+    p = nullptr;
+    return q;
+  }
+};
+
+inline int grid_for(long long n, int block) { return (int)std::max(1LL, (n + block - 1) / block); }
+
+#define FFA_CUDA(x)                                      \
+  do {                                                   \
+    cudaError_t e_ = (x);                                \
+    if (e_ != cudaSuccess) {                             \
+      return FFA_ERR_CUDA;                               \
+    }                                                    \
+  } while (0)
+
+ffa_status_t scan(const int* in, int n, int* out, long long* dtot, long long* htot,
+                  cudaStream_t st) {
+  if (n > 0) k_scan<<<1, 1024, 0, st>>>(in, n, out, dtot);
+  else FFA_CUDA(cudaMemsetAsync(dtot, 0, sizeof(long long), st));
+  FFA_CUDA(cudaGetLastError());
+  FFA_CUDA(cudaMemcpyAsync(htot, dtot, sizeof(long long), cudaMemcpyDeviceToHost, st));
+  FFA_CUDA(cudaStreamSynchronize(st));
+  return FFA_OK;
+}
+
+ffa_status_t sort_items(const int* items, int words, int cost_word, int n, int* order,
+                        cudaStream_t st) {
+  if (n <= 0) return FFA_OK;
+  int n2 = 1;
+  while (n2 < n) n2 <<= 1;
+  DevBuf scratch;
+  FFA_CUDA(scratch.alloc(sizeof(unsigned long long) * (size_t)n2));
+  k_sort_order<<<1, 1024, 0, st>>>(items, words, cost_word, n, n2,
+                                   scratch.as<unsigned long long>(), order);
+  FFA_CUDA(cudaGetLastError());
+  FFA_CUDA(cudaStreamSynchronize(st));
+  return FFA_OK;
+}
+
+void free_plan(ffa_plan_s* p) {
+  if (!p) return;
+  void* bufs[] = {p->slices, p->fwd_steps, p->fwd_items, p->fwd_order, p->merges,
+                  p->bwd_steps, p->bwd_items, p->bwd_order, p->err};
+  for (void* b : bufs)
+    if (b) cudaFree(b);
+  delete p;
+}
+
+ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, const int32_t* ty,
+                        int split_below, cudaStream_t st) {
+  const int S = p->S;
+  FFA_CUDA(cudaMalloc(&p->slices, sizeof(Slice) * (size_t)std::max(S, 1)));
+  FFA_CUDA(cudaMalloc(&p->err, 2 * sizeof(int)));
+  FFA_CUDA(cudaMemsetAsync(p->err, 0, 2 * sizeof(int), st));
+  DevBuf flags_area;
+  FFA_CUDA(flags_area.alloc(64));
+  int* flags = flags_area.as<int>();
+  unsigned long long* area = reinterpret_cast<unsigned long long*>(flags + 4);
+  long long* dtot = reinterpret_cast<long long*>(flags + 8);
+  FFA_CUDA(cudaMemsetAsync(flags, 0, 64, st));
+  if (S > 0) {
+    k_pack_slices<<<grid_for(S, 256), 256, 0, st>>>(qr, kr, ty, S, p->slices);
+    k_check_slices<<<grid_for(S, 256), 256, 0, st>>>(p->slices, S, p->Tq, p->Tk, flags, area);
+    k_check_overlap<<<grid_for((long long)S * S, 256), 256, 0, st>>>(p->slices, S, flags);
+    FFA_CUDA(cudaGetLastError());
+  }
+  int hflags[4];
+  unsigned long long harea = 0;
+  FFA_CUDA(cudaMemcpyAsync(hflags, flags, sizeof hflags, cudaMemcpyDeviceToHost, st));
+  FFA_CUDA(cudaMemcpyAsync(&harea, area, sizeof harea, cudaMemcpyDeviceToHost, st));
+  FFA_CUDA(cudaStreamSynchronize(st));
+  if (hflags[0]) return FFA_ERR_RANGE;
+  if (hflags[1]) return FFA_ERR_OVERLAP;
+  p->area = (int64_t)harea;
+
+  const int n_qt = p->n_qt, n_kt = p->n_kt, g = p->Hq / p->Hkv;
+  long long tot = 0;
+  // forward visits
+  DevBuf vcnt, voff, visits;
+  FFA_CUDA(vcnt.alloc(sizeof(int) * n_qt));
+  FFA_CUDA(voff.alloc(sizeof(int) * n_qt));
+  k_fwd_visit_count<<<grid_for(n_qt, 128), 128, 0, st>>>(p->slices, S, n_qt, vcnt.as<int>());
+  FFA_CUDA(cudaGetLastError());
+  ffa_status_t rc = scan(vcnt.as<int>(), n_qt, voff.as<int>(), dtot, &tot, st);
+  if (rc != FFA_OK) return rc;
+  if (tot > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
+  FFA_CUDA(visits.alloc(sizeof(int2) * (size_t)tot));
+  k_fwd_visit_fill<<<grid_for(n_qt, 64), 64, 0, st>>>(p->slices, S, n_qt, voff.as<int>(),
+                                                      visits.as<int2>());
+  FFA_CUDA(cudaGetLastError());
+  // forward units -> steps
+  const int pair_mode = g >= 2 ? 0 : 1;
+  const int n_units = pair_mode == 0 ? n_qt : (n_qt + 1) / 2;
+  DevBuf scnt, soff, cost_half, steps;
+  FFA_CUDA(scnt.alloc(sizeof(int) * n_units));
+  FFA_CUDA(soff.alloc(sizeof(int) * n_units));
+  FFA_CUDA(cost_half.alloc(sizeof(int) * 2 * n_units));
+  k_fwd_unit_count<<<grid_for(n_units, 128), 128, 0, st>>>(visits.as<int2>(), voff.as<int>(),
+                                                           vcnt.as<int>(), n_qt, n_units,
+                                                           pair_mode, scnt.as<int>(),
+                                                           cost_half.as<int>());
+  FFA_CUDA(cudaGetLastError());
+  rc = scan(scnt.as<int>(), n_units, soff.as<int>(), dtot, &tot, st);
+  if (rc != FFA_OK) return rc;
+  p->n_fwd_steps = tot;
+  FFA_CUDA(steps.alloc(sizeof(int4) * (size_t)tot));
+  k_fwd_unit_fill<<<grid_for(n_units, 128), 128, 0, st>>>(visits.as<int2>(), voff.as<int>(),
+                                                          vcnt.as<int>(), n_qt, n_units,
+                                                          pair_mode, soff.as<int>(),
+                                                          steps.as<int4>());
+  FFA_CUDA(cudaGetLastError());
+  // forward items
+  const int pairs = (g + 1) / 2;
+  const long long n_items = pair_mode == 0 ? (long long)n_units * p->Hkv * pairs
+                                           : (long long)n_units * p->Hq;
+  if (n_items > 0x7fffffffLL / kFiWords) return FFA_ERR_UNSUPPORTED;
+  DevBuf items, live;
+  FFA_CUDA(items.alloc(sizeof(int) * kFiWords * (size_t)n_items));
+  FFA_CUDA(live.alloc(sizeof(int)));
+  FFA_CUDA(cudaMemsetAsync(live.p, 0, sizeof(int), st));
+  k_fwd_items<<<grid_for(n_items, 128), 128, 0, st>>>((int)n_items, pair_mode, g, p->Hkv, p->Hq,
+                                                      pairs, n_qt, soff.as<int>(), scnt.as<int>(),
+                                                      cost_half.as<int>(), items.as<int>(),
+                                                      live.as<int>());
+  FFA_CUDA(cudaGetLastError());
+  int hlive = 0;
+  FFA_CUDA(cudaMemcpyAsync(&hlive, live.p, sizeof(int), cudaMemcpyDeviceToHost, st));
+  FFA_CUDA(cudaStreamSynchronize(st));
+  const int threshold = split_below == 0 ? 2 * p->num_sms : split_below;
+  long long final_items = n_items;
+  if (split_below >= 0 && hlive > 0 && hlive < threshold) {
+    const int nsplit = std::min(16, (threshold + hlive - 1) / hlive);
+    DevBuf chunks, coff, slots, sloff, groups, goff, nitems, merges;
+    const size_t nb = sizeof(int) * (size_t)n_items;
+    FFA_CUDA(chunks.alloc(nb));
+    FFA_CUDA(coff.alloc(nb));
+    FFA_CUDA(slots.alloc(nb));
+    FFA_CUDA(sloff.alloc(nb));
+    FFA_CUDA(groups.alloc(nb));
+    FFA_CUDA(goff.alloc(nb));
+    k_split_count<<<grid_for(n_items, 128), 128, 0, st>>>(items.as<int>(), (int)n_items, nsplit,
+                                                          chunks.as<int>(), slots.as<int>(),
+                                                          groups.as<int>());
+    FFA_CUDA(cudaGetLastError());
+    long long n_chunks = 0, n_slots = 0, n_groups = 0;
+    if ((rc = scan(chunks.as<int>(), (int)n_items, coff.as<int>(), dtot, &n_chunks, st))) return rc;
+    if ((rc = scan(slots.as<int>(), (int)n_items, sloff.as<int>(), dtot, &n_slots, st))) return rc;
+    if ((rc = scan(groups.as<int>(), (int)n_items, goff.as<int>(), dtot, &n_groups, st))) return rc;
+    FFA_CUDA(nitems.alloc(sizeof(int) * kFiWords * (size_t)n_chunks));
+    FFA_CUDA(merges.alloc(sizeof(int) * kMgWords * (size_t)std::max(1LL, n_groups)));
+    k_split_fill<<<grid_for(n_items, 128), 128, 0, st>>>(
+        items.as<int>(), (int)n_items, chunks.as<int>(), coff.as<int>(), sloff.as<int>(),
+        goff.as<int>(), nitems.as<int>(), merges.as<int>());
+    FFA_CUDA(cudaGetLastError());
+    FFA_CUDA(cudaStreamSynchronize(st));
+    std::swap(items.p, nitems.p);
+    final_items = n_chunks;
+    p->n_merges = n_groups;
+    p->n_slots = (int)n_slots;
+    p->merges = static_cast<int*>(merges.release());
+  }
+  p->n_fwd_items = final_items;
+  FFA_CUDA(cudaMalloc(&p->fwd_order, sizeof(int) * (size_t)std::max(1LL, final_items)));
+  rc = sort_items(items.as<int>(), kFiWords, kFiCost, (int)final_items, p->fwd_order, st);
+  if (rc != FFA_OK) return rc;
+  p->fwd_items = items.as<int>();
+  items.release();
+  p->fwd_steps = steps.as<int4>();
+  steps.release();
+
+  // backward
+  DevBuf bcnt, boff, bvis;
+  FFA_CUDA(bcnt.alloc(sizeof(int) * n_kt));
+  FFA_CUDA(boff.alloc(sizeof(int) * n_kt));
+  k_bwd_visit_count<<<grid_for(n_kt, 128), 128, 0, st>>>(p->slices, S, n_kt, bcnt.as<int>());
+  FFA_CUDA(cudaGetLastError());
+  if ((rc = scan(bcnt.as<int>(), n_kt, boff.as<int>(), dtot, &tot, st))) return rc;
+  if (tot > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
+  p->n_bwd_steps = tot;
+  FFA_CUDA(bvis.alloc(sizeof(int2) * (size_t)tot));
+  FFA_CUDA(cudaMalloc(&p->bwd_steps, sizeof(int4) * (size_t)std::max(1LL, tot)));
+  k_bwd_visit_fill<<<grid_for(n_kt, 64), 64, 0, st>>>(p->slices, S, n_kt, boff.as<int>(),
+                                                      bvis.as<int2>());
+  const long long nb_items = (long long)n_kt * p->Hkv;
+  p->n_bwd_items = nb_items;
+  FFA_CUDA(cudaMalloc(&p->bwd_items, sizeof(int) * kBiWords * (size_t)std::max(1LL, nb_items)));
+  FFA_CUDA(cudaMalloc(&p->bwd_order, sizeof(int) * (size_t)std::max(1LL, nb_items)));
+  k_bwd_items<<<grid_for(nb_items, 128), 128, 0, st>>>(n_kt, p->Hkv, g, bvis.as<int2>(),
+                                                       boff.as<int>(), bcnt.as<int>(),
+                                                       p->bwd_steps, p->bwd_items);
+  FFA_CUDA(cudaGetLastError());
+  rc = sort_items(p->bwd_items, kBiWords, kBiCost, (int)nb_items, p->bwd_order, st);
+  if (rc != FFA_OK) return rc;
+  p->grid_fwd = (int)std::max(1LL, std::min<long long>(p->num_sms, final_items));
+  p->grid_bwd = (int)std::max(1LL, std::min<long long>(p->num_sms, nb_items));
+  FFA_CUDA(cudaStreamSynchronize(st));
+  return FFA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+// 2-D tensor map over a row-major [rows][cols] bf16 matrix: boxes of
+// 128 rows x 64 columns (128 bytes), 128-byte swizzle, zero fill outside.
+bool encode_tile_map(void* map128, const void* base, int rows, int cols_elems) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols_elems, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols_elems * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(static_cast<CUtensorMap*>(map128), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace ffa
+
+using namespace ffa;
+
+extern "C" {
+
+ffa_status_t ffa_plan_create(ffa_plan_t* plan, const int32_t* q_ranges, const int32_t* k_ranges,
+                             const int32_t* mask_types, int32_t num_slices, int32_t total_q,
+                             int32_t total_k, int32_t num_heads_q, int32_t num_heads_kv,
+                             int32_t head_dim, int32_t num_sms, int32_t split_below,
+                             ffa_stream_t stream) {
+  if (!plan) return FFA_ERR_INVALID_ARG;
+  *plan = nullptr;
+  if (num_slices < 0 || total_q <= 0 || total_k <= 0 || num_heads_q <= 0 || num_heads_kv <= 0 ||
+      split_below < -1 || num_sms < 0)
+    return FFA_ERR_INVALID_ARG;
+  if (num_slices > 0 && (!q_ranges || !k_ranges || !mask_types)) return FFA_ERR_INVALID_ARG;
+  if (num_heads_q % num_heads_kv != 0 || (head_dim != 64 && head_dim != 128))
+    return FFA_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FFA_ERR_CUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FFA_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return FFA_ERR_UNSUPPORTED;
+  ffa_plan_s* p = new ffa_plan_s();
+  p->device = dev;
+  p->Tq = total_q;
+  p->Tk = total_k;
+  p->Hq = num_heads_q;
+  p->Hkv = num_heads_kv;
+  p->D = head_dim;
+  p->S = num_slices;
+  p->num_sms = num_sms > 0 ? num_sms : prop.multiProcessorCount;
+  p->n_qt = (total_q + kTile - 1) / kTile;
+  p->n_kt = (total_k + kTile - 1) / kTile;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  ffa_status_t rc = build_plan(p, q_ranges, k_ranges, mask_types, split_below, st);
+  if (rc != FFA_OK) {
+    cudaStreamSynchronize(st);
+    free_plan(p);
+    return rc;
+  }
+  *plan = p;
+  return FFA_OK;
+}
+
+ffa_status_t ffa_plan_destroy(ffa_plan_t plan) {
+  if (!plan) return FFA_ERR_INVALID_ARG;
+  cudaDeviceSynchronize();
+  free_plan(plan);
+  return FFA_OK;
+}
+
+ffa_status_t ffa_plan_info(ffa_plan_t p, ffa_plan_info_t* info) {
+  if (!p || !info) return FFA_ERR_INVALID_ARG;
+  info->fwd_steps = p->n_fwd_steps;
+  info->fwd_items = p->n_fwd_items;
+  info->bwd_steps = p->n_bwd_steps;
+  info->bwd_items = p->n_bwd_items;
+  info->merges = p->n_merges;
+  info->grid_fwd = p->grid_fwd;
+  info->grid_bwd = p->grid_bwd;
+  info->area = p->area;
+  return FFA_OK;
+}
+
+ffa_status_t ffa_plan_export(ffa_plan_t p, int32_t which, int32_t* dst, int64_t capacity,
+                             int64_t* written) {
+  if (!p || !written || (capacity > 0 && !dst)) return FFA_ERR_INVALID_ARG;
+  const void* src = nullptr;
+  int64_t words = 0;
+  switch (which) {
+    case 0: src = p->fwd_steps; words = 4 * p->n_fwd_steps; break;
+    case 1: src = p->fwd_items; words = kFiWords * p->n_fwd_items; break;
+    case 2: src = p->fwd_order; words = p->n_fwd_items; break;
+    case 3: src = p->bwd_steps; words = 4 * p->n_bwd_steps; break;
+    case 4: src = p->bwd_items; words = kBiWords * p->n_bwd_items; break;
+    case 5: src = p->bwd_order; words = p->n_bwd_items; break;
+    case 6: src = p->merges; words = kMgWords * p->n_merges; break;
+    default: return FFA_ERR_INVALID_ARG;
+  }
+  *written = words;
+  if (words > capacity) return FFA_ERR_INVALID_ARG;
+  if (words > 0 && cudaMemcpy(dst, src, sizeof(int32_t) * words, cudaMemcpyDeviceToHost) !=
+                       cudaSuccess)
+    return FFA_ERR_CUDA;
+  return FFA_OK;
+}
+
+size_t ffa_fwd_workspace_size(ffa_plan_t p) { return p ? fwd_workspace_bytes(p) : 0; }
+size_t ffa_bwd_workspace_size(ffa_plan_t p) { return p ? bwd_workspace_bytes(p) : 0; }
+
+ffa_status_t ffa_fwd(ffa_plan_t p, const void* q, const void* k, const void* v,
+                     float softmax_scale, void* out, float* lse, void* workspace,
+                     size_t workspace_bytes, ffa_stream_t stream) {
+  if (!p || !q || !k || !v || !out || !lse) return FFA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return FFA_ERR_INVALID_ARG;
+  const size_t need = fwd_workspace_bytes(p);
+  if (workspace_bytes < need || (need > 0 && (!workspace || !aligned16(workspace))))
+    return FFA_ERR_WORKSPACE;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)p->D);
+  return launch_fwd(p, q, k, v, scale, out, lse, workspace, workspace_bytes,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+ffa_status_t ffa_bwd(ffa_plan_t p, const void* q, const void* k, const void* v, const void* out,
+                     const void* dout, const float* lse, float softmax_scale, void* dq, void* dk,
+                     void* dv, void* workspace, size_t workspace_bytes, ffa_stream_t stream) {
+  if (!p || !q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv)
+    return FFA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, out, dout, lse, dq, dk, dv};
+  for (const void* x : ptrs)
+    if (!aligned16(x)) return FFA_ERR_INVALID_ARG;
+  const size_t need = bwd_workspace_bytes(p);
+  if (workspace_bytes < need || (need > 0 && (!workspace || !aligned16(workspace))))
+    return FFA_ERR_WORKSPACE;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)p->D);
+  return launch_bwd(p, q, k, v, out, dout, lse, scale, dq, dk, dv, workspace, workspace_bytes,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+ffa_status_t ffa_get_last_device_error(ffa_plan_t p, int32_t* code, int32_t* where,
+                                       ffa_stream_t stream) {
+  if (!p || !code || !where) return FFA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int h[2] = {0, 0};
+  if (cudaMemcpyAsync(h, p->err, sizeof h, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemsetAsync(p->err, 0, sizeof h, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return FFA_ERR_CUDA;
+  *code = h[0];
+  *where = h[1];
+  return FFA_OK;
+}
+
+ffa_status_t ffa_plan_set_wait_limit(ffa_plan_t p, uint64_t ns) {
+  if (!p || ns == 0) return FFA_ERR_INVALID_ARG;
+  p->wait_ns = ns;
+  return FFA_OK;
+}
+
+const char* ffa_status_string(ffa_status_t s) {
+  switch (s) {
+    case FFA_OK: return "ok";
+    case FFA_ERR_INVALID_ARG: return "invalid argument";
+    case FFA_ERR_RANGE: return "slice range out of bounds or bad mask type";
+    case FFA_ERR_OVERLAP: return "slice rectangles overlap";
+    case FFA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FFA_ERR_WORKSPACE: return "workspace too small";
+    case FFA_ERR_TIMEOUT: return "device wait timed out";
+    case FFA_ERR_CUDA: return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,152 @@
+/*
+ * ffa.h -- C ABI of the flexible-mask flash attention library (libffa.so),
+ * built for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (MagiAttention pages, quickstart card "Single-GPU
+ * Flex-Flash-Attention", flex_flash_attn_func): softmax attention over a
+ * packed token stream whose mask is a list of slices.  Slice s is
+ * (q_range [qs, qe), k_range [ks, ke), mask_type); inside it query row i sees
+ * keys [lo, hi) with
+ *     lo = ks + (i - qs)        if mask_type has bit 1 set (inverse causal),
+ *          ks                   otherwise;
+ *     hi = ke - (qe - 1 - i)    if mask_type has bit 0 set (causal),
+ *          ke                   otherwise
+ * (card "Calculate KV Interval Boundaries for Mask Types"), so causal is
+ * bottom-right aligned in the slice's rectangle.  A row sees the union of its
+ * intervals over all slices containing it.  out_i = sum_j softmax_j(scale *
+ * q_i.k_j) v_j, lse_i = log sum_j exp(scale * q_i.k_j) (natural log), and a
+ * row that sees no key gives out = 0, lse = -inf.  Query head h uses key/value
+ * head h / (Hq / Hkv).
+ *
+ * Conventions for every call
+ *   - Tensors are caller-owned DEVICE pointers, contiguous, 16-byte aligned:
+ *       q, out, dout, dq   [Tq][Hq][D]   bf16
+ *       k, v, dk, dv       [Tk][Hkv][D]  bf16
+ *       lse                [Hq][Tq]      fp32 (head-major)
+ *       q_ranges, k_ranges [S][2] int32 (device), mask_types [S] int32 (device)
+ *   - Supported: D in {64, 128}; Hq % Hkv == 0; 0 <= start <= end <= T for
+ *     every range.  Slices with an empty range are allowed and do nothing.
+ *     The (q x k) rectangles of non-empty slices must be pairwise disjoint.
+ *   - Work is queued on `stream` and returns immediately, except
+ *     ffa_plan_create, which synchronises `stream` while it sizes the plan.
+ *   - ffa_fwd / ffa_bwd never allocate: scratch memory is the caller's
+ *     `workspace` of at least the size the *_workspace_size call reports.
+ *   - Errors come back as an ffa_status_t; nothing aborts the process.
+ *     Device-side failures (a bounded wait that ran out) are reported by
+ *     ffa_get_last_device_error.
+ */
+#ifndef FFA_H_
+#define FFA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ffa_stream_t; /* same as cudaStream_t; NULL = legacy default */
+
+typedef enum {
+  FFA_FULL = 0,        /* every (q, k) pair of the rectangle */
+  FFA_CAUSAL = 1,      /* bottom-right aligned lower triangle */
+  FFA_INV_CAUSAL = 2,  /* top-left aligned upper triangle */
+  FFA_BI_CAUSAL = 3    /* both clamps: a band */
+} ffa_mask_t;
+
+typedef enum {
+  FFA_OK = 0,
+  FFA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer */
+  FFA_ERR_RANGE = 2,       /* a range outside [0, T] or start > end, bad mask type */
+  FFA_ERR_OVERLAP = 3,     /* two non-empty slice rectangles intersect */
+  FFA_ERR_UNSUPPORTED = 4, /* head_dim not in {64, 128}, Hq % Hkv != 0, device not sm_103 */
+  FFA_ERR_WORKSPACE = 5,   /* workspace smaller than required */
+  FFA_ERR_TIMEOUT = 6,     /* a kernel's bounded wait ran out (see ffa_get_last_device_error) */
+  FFA_ERR_CUDA = 7         /* a CUDA runtime call failed */
+} ffa_status_t;
+
+/* Opaque plan: the tile work lists derived from one slice table and shape.
+ * It owns device memory for its metadata only and may be reused by any
+ * number of ffa_fwd / ffa_bwd calls on the same device. */
+typedef struct ffa_plan_s* ffa_plan_t;
+
+/* Build a plan (the slice planner and tile scheduler).
+ *   q_ranges, k_ranges: device int32 [num_slices][2]; mask_types: device
+ *   int32 [num_slices] (ffa_mask_t values).  total_q / total_k are Tq / Tk.
+ *   num_sms: CTAs the persistent kernels will use (0 = every SM of the
+ *   current device).  split_below: split forward work items into key chunks
+ *   (merged by logsumexp) while fewer than this many items exist (0 = twice
+ *   num_sms, -1 = never split).
+ * Runs validation and planning kernels on `stream` and synchronises it.
+ * Returns FFA_ERR_RANGE / FFA_ERR_OVERLAP for a bad slice table. */
+ffa_status_t ffa_plan_create(ffa_plan_t* plan, const int32_t* q_ranges, const int32_t* k_ranges,
+                             const int32_t* mask_types, int32_t num_slices, int32_t total_q,
+                             int32_t total_k, int32_t num_heads_q, int32_t num_heads_kv,
+                             int32_t head_dim, int32_t num_sms, int32_t split_below,
+                             ffa_stream_t stream);
+
+/* Free a plan and its device memory (synchronises the device first). */
+ffa_status_t ffa_plan_destroy(ffa_plan_t plan);
+
+/* Sizes of the plan's work lists, in int32 words; see ffa_plan_export. */
+typedef struct {
+  int64_t fwd_steps;  /* 4 words per step */
+  int64_t fwd_items;  /* 8 words per item */
+  int64_t bwd_steps;  /* 4 words per step */
+  int64_t bwd_items;  /* 8 words per item */
+  int64_t merges;     /* 4 words per merge group */
+  int32_t grid_fwd;   /* CTAs of the forward kernel */
+  int32_t grid_bwd;   /* CTAs of the backward kernel */
+  int64_t area;       /* visible (q, k) pairs per head: sum over rows of |keys seen| */
+} ffa_plan_info_t;
+
+ffa_status_t ffa_plan_info(ffa_plan_t plan, ffa_plan_info_t* info);
+
+/* Copy one work list to HOST memory (used to check the planner bit for bit).
+ *   which: 0 fwd steps, 1 fwd items, 2 fwd order, 3 bwd steps, 4 bwd items,
+ *          5 bwd order, 6 merge groups.
+ *   dst: host int32 buffer of `capacity` words; *written receives the count.
+ * Synchronises the plan's stream. */
+ffa_status_t ffa_plan_export(ffa_plan_t plan, int32_t which, int32_t* dst, int64_t capacity,
+                             int64_t* written);
+
+/* Workspace bytes ffa_fwd / ffa_bwd need for this plan (0 is possible). */
+size_t ffa_fwd_workspace_size(ffa_plan_t plan);
+size_t ffa_bwd_workspace_size(ffa_plan_t plan);
+
+/* Forward: out[Tq][Hq][D] (bf16) and lse[Hq][Tq] (fp32, natural log).
+ *   softmax_scale <= 0 selects 1/sqrt(D) (quickstart: "Defaults to
+ *   1/sqrt(head_dim)").  workspace: device memory of ffa_fwd_workspace_size
+ *   bytes (may be NULL when that size is 0), contents need not be set.
+ * Rows that see no key are written as out = 0, lse = -inf. */
+ffa_status_t ffa_fwd(ffa_plan_t plan, const void* q, const void* k, const void* v,
+                     float softmax_scale, void* out, float* lse, void* workspace,
+                     size_t workspace_bytes, ffa_stream_t stream);
+
+/* Backward of ffa_fwd for the loss L with dL/dout = dout.
+ *   out, lse: the forward's results; dq, dk, dv receive the gradients
+ *   (bf16, every element written; keys seen by no query get 0).
+ *   workspace: device memory of ffa_bwd_workspace_size bytes. */
+ffa_status_t ffa_bwd(ffa_plan_t plan, const void* q, const void* k, const void* v,
+                     const void* out, const void* dout, const float* lse, float softmax_scale,
+                     void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                     ffa_stream_t stream);
+
+/* Read and clear the device error word the plan's kernels write:
+ *   *code = 0 none, 1 bounded wait timed out, 2 shared memory misaligned,
+ *   3 bad work item; *where = the location tag of the first failure.
+ * Synchronises `stream`. */
+ffa_status_t ffa_get_last_device_error(ffa_plan_t plan, int32_t* code, int32_t* where,
+                                       ffa_stream_t stream);
+
+/* Bounded-wait limit for the plan's kernels, in nanoseconds (default 2e9).
+ * A wait that runs out makes the kernel stop and report FFA_ERR_TIMEOUT. */
+ffa_status_t ffa_plan_set_wait_limit(ffa_plan_t plan, uint64_t nanoseconds);
+
+/* Human-readable name of a status code (static storage). */
+const char* ffa_status_string(ffa_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FFA_H_ */

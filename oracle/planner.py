@@ -1,0 +1,202 @@
+"""CPU re-derivation of the tile work lists (test infrastructure).
+
+The device planner classifies tiles with closed forms.  This module derives
+the same lists by counting: for every slice it lists each row's visible key
+interval, sums the visible entries of every (q-tile, k-tile) pair, and calls
+a tile FULL when it holds 128 * 128 visible entries and PARTIAL when it holds
+at least one.  The rest (pairing, merging, costs, splitting, ordering) follows
+the work-list specification of the planner:
+
+  * forward visits of a q-tile: (kt, slice) pairs sorted by (kt, slice);
+  * grouped heads (Hq/Hkv >= 2): a unit is one q-tile, items are pairs of
+    query heads of one kv head; otherwise a unit is q-tiles (2u, 2u+1), items
+    one per head, steps merge the two visit lists on kt;
+  * cost = 4 per FULL and 5 per PARTIAL visit over the busy halves;
+  * split (when 0 < items with work < threshold): min(16, ceil(threshold /
+    live)) chunks per item, capped by its step count, step ranges
+    b + k*n//c .. b + (k+1)*n//c, cost scaled by the chunk's share;
+  * order: cost descending, then item index;
+  * backward: per k-tile (qt, slice) visits sorted by (qt, slice), one item
+    per (kt, kv head), cost g * sum of visit costs.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+TILE = 128
+FULL_COST, PARTIAL_COST = 4, 5
+
+
+def row_intervals(qs, qe, ks, ke, t):
+    """Rows of the slice and each row's visible key interval [lo, hi)."""
+    rows = np.arange(qs, qe, dtype=np.int64)
+    lo = ks + ((rows - qs) if (t & 2) else 0)
+    hi = ke - ((qe - 1 - rows) if (t & 1) else 0)
+    lo = np.broadcast_to(np.asarray(lo, np.int64), rows.shape).copy()
+    hi = np.broadcast_to(np.asarray(hi, np.int64), rows.shape).copy()
+    return rows, lo, hi
+
+
+def tile_counts(q_ranges, k_ranges, mask_types):
+    """{slice: {(qt, kt): visible entries}} by summing clipped row intervals."""
+    out = {}
+    for s, ((qs, qe), (ks, ke), t) in enumerate(zip(np.asarray(q_ranges).reshape(-1, 2),
+                                                    np.asarray(k_ranges).reshape(-1, 2),
+                                                    np.asarray(mask_types).reshape(-1))):
+        qs, qe, ks, ke, t = int(qs), int(qe), int(ks), int(ke), int(t)
+        d = {}
+        out[s] = d
+        if qe <= qs or ke <= ks:
+            continue
+        rows, lo, hi = row_intervals(qs, qe, ks, ke, t)
+        ok = hi > lo
+        if not ok.any():
+            continue
+        rows, lo, hi = rows[ok], lo[ok], hi[ok]
+        kts = np.arange(lo.min() // TILE, -(-hi.max() // TILE))
+        qts = rows // TILE
+        for qt in np.unique(qts):
+            sel = qts == qt
+            l, h = lo[sel][:, None], hi[sel][:, None]
+            c = np.clip(np.minimum(h, (kts[None] + 1) * TILE) - np.maximum(l, kts[None] * TILE),
+                        0, None).sum(axis=0)
+            for kt, n in zip(kts, c):
+                if n > 0:
+                    d[(int(qt), int(kt))] = int(n)
+    return out
+
+
+def visible_area(q_ranges, k_ranges, mask_types) -> int:
+    tot = 0
+    for (qs, qe), (ks, ke), t in zip(np.asarray(q_ranges).reshape(-1, 2),
+                                     np.asarray(k_ranges).reshape(-1, 2),
+                                     np.asarray(mask_types).reshape(-1)):
+        if qe <= qs or ke <= ks:
+            continue
+        _, lo, hi = row_intervals(int(qs), int(qe), int(ks), int(ke), int(t))
+        tot += int(np.clip(hi - lo, 0, None).sum())
+    return tot
+
+
+def _info(s, count):
+    return (s << 1) | (0 if count == TILE * TILE else 1)
+
+
+def _cost(info):
+    return PARTIAL_COST if info & 1 else FULL_COST
+
+
+def plan(total_q, total_k, num_heads_q, num_heads_kv, q_ranges, k_ranges, mask_types,
+         num_sms, split_below=0):
+    """Work lists in the export layout of the device planner."""
+    n_qt = -(-total_q // TILE)
+    n_kt = -(-total_k // TILE)
+    g = num_heads_q // num_heads_kv
+    counts = tile_counts(q_ranges, k_ranges, mask_types)
+    fvis = [[] for _ in range(n_qt)]
+    bvis = [[] for _ in range(n_kt)]
+    for s, d in counts.items():
+        for (qt, kt), c in d.items():
+            fvis[qt].append((kt, s, _info(s, c)))
+            bvis[kt].append((qt, s, _info(s, c)))
+    fvis = [[(kt, info) for kt, _, info in sorted(v)] for v in fvis]
+    bvis = [[(qt, info) for qt, _, info in sorted(v)] for v in bvis]
+
+    # forward units and steps
+    pair_mode = 0 if g >= 2 else 1
+    n_units = n_qt if pair_mode == 0 else (n_qt + 1) // 2
+    steps, soff, scnt, cost_half = [], [], [], []
+    for u in range(n_units):
+        soff.append(len(steps))
+        if pair_mode == 0:
+            st = [(kt, i, i, 0) for kt, i in fvis[u]]
+            c = sum(_cost(i) for _, i in fvis[u])
+            cost_half.append((c, c))
+        else:
+            a = fvis[2 * u]
+            b = fvis[2 * u + 1] if 2 * u + 1 < n_qt else []
+            st, i, j, ca, cb = [], 0, 0, 0, 0
+            while i < len(a) or j < len(b):
+                if j >= len(b) or (i < len(a) and a[i][0] < b[j][0]):
+                    st.append((a[i][0], a[i][1], -1, 0)); ca += _cost(a[i][1]); i += 1
+                elif i >= len(a) or b[j][0] < a[i][0]:
+                    st.append((b[j][0], -1, b[j][1], 0)); cb += _cost(b[j][1]); j += 1
+                else:
+                    st.append((a[i][0], a[i][1], b[j][1], 0))
+                    ca += _cost(a[i][1]); cb += _cost(b[j][1]); i += 1; j += 1
+            cost_half.append((ca, cb))
+        steps.extend(st)
+        scnt.append(len(st))
+
+    items = []
+    if pair_mode == 0:
+        pairs = (g + 1) // 2
+        for u in range(n_units):
+            for hk in range(num_heads_kv):
+                for p in range(pairs):
+                    h0 = hk * g + 2 * p
+                    h1 = h0 + 1 if 2 * p + 1 < g else -1
+                    qt1 = u if h1 >= 0 else -1
+                    cost = cost_half[u][0] + (cost_half[u][1] if h1 >= 0 else 0)
+                    items.append([u, qt1, h0, h1, soff[u], soff[u] + scnt[u], -1, cost])
+    else:
+        for u in range(n_units):
+            for h in range(num_heads_q):
+                qt1 = 2 * u + 1 if 2 * u + 1 < n_qt else -1
+                h1 = h if qt1 >= 0 else -1
+                cost = cost_half[u][0] + (cost_half[u][1] if h1 >= 0 else 0)
+                items.append([2 * u, qt1, h, h1, soff[u], soff[u] + scnt[u], -1, cost])
+
+    live = sum(1 for it in items if it[5] > it[4])
+    threshold = 2 * num_sms if split_below == 0 else split_below
+    merges, n_slots = [], 0
+    if split_below >= 0 and 0 < live < threshold:
+        nsplit = min(16, -(-threshold // live))
+        new = []
+        for it in items:
+            b, n = it[4], it[5] - it[4]
+            c = max(1, min(nsplit, n))
+            if c == 1:
+                new.append(list(it))
+                continue
+            for k in range(c):
+                kb, ke = b + k * n // c, b + (k + 1) * n // c
+                x = list(it)
+                x[4], x[5], x[6] = kb, ke, n_slots + k
+                x[7] = it[7] * (ke - kb) // max(n, 1)
+                new.append(x)
+            merges.append([it[0], it[1], it[2], it[3], n_slots, c, 0, 0])
+            n_slots += c
+        items = new
+
+    def order_of(costs):
+        return np.array(sorted(range(len(costs)), key=lambda i: (-costs[i], i)), dtype=np.int32)
+
+    fwd_items = np.array(items, dtype=np.int32).reshape(-1, 8)
+    fwd_order = order_of([it[7] for it in items])
+
+    bsteps, bitems = [], []
+    boff = []
+    for kt in range(n_kt):
+        boff.append(len(bsteps))
+        bsteps.extend((qt, i, 0, 0) for qt, i in bvis[kt])
+    for kt in range(n_kt):
+        c = sum(_cost(i) for _, i in bvis[kt])
+        for hk in range(num_heads_kv):
+            bitems.append([kt, hk, boff[kt], boff[kt] + len(bvis[kt]), c * g, 0, 0, 0])
+    bwd_items = np.array(bitems, dtype=np.int32).reshape(-1, 8)
+    return {
+        "fwd_steps": np.array(steps, dtype=np.int32).reshape(-1, 4),
+        "fwd_items": fwd_items,
+        "fwd_order": fwd_order,
+        "bwd_steps": np.array(bsteps, dtype=np.int32).reshape(-1, 4),
+        "bwd_items": bwd_items,
+        "bwd_order": order_of([it[4] for it in bitems]),
+        "merges": np.array(merges, dtype=np.int32).reshape(-1, 8),
+        "n_slots": n_slots,
+        "grid_fwd": max(1, min(num_sms, len(items))),
+        "grid_bwd": max(1, min(num_sms, len(bitems))),
+        "area": visible_area(q_ranges, k_ranges, mask_types),
+    }

@@ -1,0 +1,156 @@
+"""CPU checks of the planner pieces that do not need a GPU:
+
+* the oracle's counting planner against a dense brute force,
+* the device planner's closed-form tile classification (compiled for the
+  host from the product header) against the counting planner,
+* the seeded workload generators against the values stated in the survey.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+from oracle import dense, planner
+from flexible_mask_attention_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SEG_HEADER = os.path.join(ROOT, "flexible_mask_attention_gb300", "csrc", "ffa_segments.cuh")
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_counts_match_dense(seed):
+    rng = np.random.default_rng(seed)
+    Tq, Tk = int(rng.integers(100, 700)), int(rng.integers(100, 700))
+    qr, kr, ty = W.random_slices(Tq, Tk, int(rng.integers(2, 8)), seed=seed)
+    counts = planner.tile_counts(qr, kr, ty)
+    for s in range(len(ty)):
+        m = dense.dense_mask(Tq, Tk, qr[s:s + 1], kr[s:s + 1], ty[s:s + 1])
+        nq, nk = -(-Tq // 128), -(-Tk // 128)
+        pad = np.zeros((nq * 128, nk * 128), dtype=np.int64)
+        pad[:Tq, :Tk] = m
+        blocks = pad.reshape(nq, 128, nk, 128).sum(axis=(1, 3))
+        got = np.zeros_like(blocks)
+        for (qt, kt), c in counts[s].items():
+            got[qt, kt] = c
+        assert (got == blocks).all()
+    assert planner.visible_area(qr, kr, ty) == dense.dense_mask(Tq, Tk, qr, kr, ty).sum()
+
+
+@pytest.fixture(scope="module")
+def seg_lib(tmp_path_factory):
+    d = tmp_path_factory.mktemp("seg")
+    src = d / "harness.cpp"
+    src.write_text(f"""
+#define __host__
+#define __device__
+#include "{SEG_HEADER}"
+using namespace ffa;
+extern "C" int fwd_run(int qs, int qe, int ks, int ke, int t, int qt, int* o) {{
+  SliceDesc s{{qs, qe, ks, ke, t}}; TileRun r;
+  if (!fwd_tile_run(s, qt, r)) return 0;
+  o[0] = r.b; o[1] = r.fb; o[2] = r.fe; o[3] = r.e; return 1;
+}}
+extern "C" int bwd_run(int qs, int qe, int ks, int ke, int t, int kt, int* o) {{
+  SliceDesc s{{qs, qe, ks, ke, t}}; TileRun r;
+  if (!bwd_tile_run(s, kt, r)) return 0;
+  o[0] = r.b; o[1] = r.fb; o[2] = r.fe; o[3] = r.e; return 1;
+}}
+extern "C" long long area(int qs, int qe, int ks, int ke, int t) {{
+  return slice_area(SliceDesc{{qs, qe, ks, ke, t}});
+}}
+""")
+    so = d / "libseg.so"
+    subprocess.check_call(["g++", "-O1", "-std=c++17", "-shared", "-fPIC", "-o", str(so), str(src)])
+    lib = ctypes.CDLL(str(so))
+    lib.area.restype = ctypes.c_longlong
+    return lib
+
+
+def _closed_form_counts(lib, s, Tq, Tk):
+    """{(qt, kt): 'F'|'P'} from the closed forms, forward and backward views."""
+    o = (ctypes.c_int * 4)()
+    fwd, bwd = {}, {}
+    for qt in range(-(-Tq // 128)):
+        if lib.fwd_run(*s, qt, o):
+            b, fb, fe, e = list(o)
+            for kt in range(b, e):
+                fwd[(qt, kt)] = "F" if fb <= kt < fe else "P"
+    for kt in range(-(-Tk // 128)):
+        if lib.bwd_run(*s, kt, o):
+            b, fb, fe, e = list(o)
+            for qt in range(b, e):
+                bwd[(qt, kt)] = "F" if fb <= qt < fe else "P"
+    return fwd, bwd
+
+
+def _check_slices(lib, qr, kr, ty, Tq, Tk):
+    counts = planner.tile_counts(qr, kr, ty)
+    for s in range(len(ty)):
+        sl = (int(qr[s][0]), int(qr[s][1]), int(kr[s][0]), int(kr[s][1]), int(ty[s]))
+        ref = {key: ("F" if c == 128 * 128 else "P") for key, c in counts[s].items()}
+        fwd, bwd = _closed_form_counts(lib, sl, Tq, Tk)
+        assert fwd == ref, f"forward classification differs for slice {sl}"
+        assert bwd == ref, f"backward classification differs for slice {sl}"
+        assert lib.area(*sl) == planner.visible_area(qr[s:s + 1], kr[s:s + 1], ty[s:s + 1])
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_closed_forms_random(seg_lib, seed):
+    rng = np.random.default_rng(1000 + seed)
+    Tq, Tk = int(rng.integers(50, 1500)), int(rng.integers(50, 1500))
+    qr, kr, ty = W.random_slices(Tq, Tk, int(rng.integers(1, 9)), seed=seed,
+                                 aligned=bool(seed % 3 == 0))
+    _check_slices(seg_lib, qr, kr, ty, Tq, Tk)
+
+
+def test_closed_forms_edge_shapes(seg_lib):
+    cases = []
+    for t in range(4):
+        for qlen, klen in [(1, 1), (1, 300), (300, 1), (128, 128), (129, 127), (127, 129),
+                           (256, 384), (384, 256), (500, 500)]:
+            for qs, ks in [(0, 0), (5, 130), (128, 0), (77, 255)]:
+                cases.append((qs, qs + qlen, ks, ks + klen, t))
+    for c in cases:
+        qr, kr, ty = np.array([[c[0], c[1]]]), np.array([[c[2], c[3]]]), np.array([c[4]])
+        _check_slices(seg_lib, qr, kr, ty, c[1] + 3, c[3] + 3)
+
+
+def test_workload_generators_match_survey_values():
+    assert W.packed_doc_lengths(32768, 2) == [2474, 1214, 1355, 277, 12386, 6430, 1479, 4440, 2713]
+    wl = W.heterogeneous_prefix_docs()
+    assert wl.meta["bounds"] == [4096, 6140, 12656, 14098, 18967, 20502, 21601, 23129, 27005, 29038,
+                                 29636, 31385, 31699, 34519, 35807, 37712, 38846, 47227, 49095,
+                                 50973, 52109, 56750, 64494, 65536]
+    assert wl.meta["doc_types"] == [1, 2, 1, 3, 0, 0, 2, 2, 3, 0, 2, 0, 1, 3, 0, 1, 1, 2, 3, 2, 0, 1, 3]
+    assert wl.num_slices == 47
+    assert W.long_context_docs().num_slices == 64
+
+
+@pytest.mark.parametrize("name,area,full,partial", [
+    ("packed_causal", 1.1678e8, 6773, 727),
+    ("heterogeneous", 4.0434e8, 23296, 2740),
+    ("long_context", 2.8858e9, 175104, 2048),
+])
+def test_config_areas_and_tile_mix(name, area, full, partial):
+    wl = W.CONFIGS[name]()
+    counts = planner.tile_counts(wl.q_ranges, wl.k_ranges, wl.mask_types)
+    nf = sum(1 for d in counts.values() for c in d.values() if c == 128 * 128)
+    npart = sum(1 for d in counts.values() for c in d.values() if c < 128 * 128)
+    a = planner.visible_area(wl.q_ranges, wl.k_ranges, wl.mask_types)
+    assert abs(a - area) / area < 1e-4
+    assert (nf, npart) == (full, partial)
+
+
+def test_plan_split_and_order_rules():
+    wl = W.tiny_causal_docs()
+    p = planner.plan(256, 256, 1, 1, wl.q_ranges, wl.k_ranges, wl.mask_types, num_sms=152)
+    # one unit (q-tiles 0, 1), two steps, split into two single-step chunks
+    assert p["fwd_steps"].tolist() == [[0, 1, -1, 0], [1, -1, 3, 0]]
+    assert p["fwd_items"].tolist() == [[0, 1, 0, 0, 0, 1, 0, 5], [0, 1, 0, 0, 1, 2, 1, 5]]
+    assert p["merges"].tolist() == [[0, 1, 0, 0, 0, 2, 0, 0]]
+    q = planner.plan(256, 256, 1, 1, wl.q_ranges, wl.k_ranges, wl.mask_types, num_sms=152,
+                     split_below=-1)
+    assert q["fwd_items"].tolist() == [[0, 1, 0, 0, 0, 2, -1, 10]]
+    assert q["bwd_items"].tolist() == [[0, 0, 0, 1, 5, 0, 0, 0], [1, 0, 1, 2, 5, 0, 0, 0]]
