@@ -1,0 +1,392 @@
+#!/usr/bin/env python
+"""Benchmark of the flexible-mask attention hot path on GB300.
+
+One step = the whole path on one batch: the slice planner, the forward
+(out, lse) and the backward (dq, dk, dv), on the 64K-token heterogeneous
+mask (a shared 4096-token prefix plus 23 documents of mixed mask types,
+47 slices, 16 heads, head_dim 128, bf16).  The metric is effective TFLOPS
+over the unmasked area: forward 4*D*area*Hq, backward 2.5x that.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ffa|reference]
+
+Under torchrun every rank runs its own replica of the workload (the path
+has no cross-GPU exchange), ranks meet at a barrier around the timed loop,
+and rank 0 prints one JSON line with the max time over ranks.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective TFLOPS (unmasked area) fwd/bwd on 1 GB300; % of BF16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ffa", "reference"], default="ffa")
+    ap.add_argument("--config", default="heterogeneous")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(use_cuda: bool):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend="nccl" if use_cuda else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "flexible_mask_attention_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile(kernel: str):
+    """DRAM bytes per launch recorded by an ncu capture of the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == kernel and parts[1] == want:
+            return float(parts[2])
+    return None
+
+
+def oracle_sample(wl, q, k, v, do, seconds: float, seed: int = 0):
+    """Time the fp64 oracle on a seeded row sample (forward + dq of those rows).
+
+    The credit is the full effective fwd+bwd work of the sampled rows
+    (14*D*Hq per visible pair) although the oracle's dK/dV part is not run,
+    so the figure is an upper bound on the oracle's throughput."""
+    import numpy as np
+
+    import oracle
+    from oracle import planner
+    rng = np.random.default_rng(seed)
+    D, Hq = wl.head_dim, wl.num_heads_q
+    # per-row visible counts, to credit the work
+    counts = np.zeros(wl.total_q, dtype=np.int64)
+    for (qs, qe), (ks, ke), t in zip(wl.q_ranges, wl.k_ranges, wl.mask_types):
+        if qe > qs and ke > ks:
+            rows, lo, hi = planner.row_intervals(int(qs), int(qe), int(ks), int(ke), int(t))
+            counts[rows] += np.clip(hi - lo, 0, None)
+    # calibrate on a small sample, then size the real one
+    probe = rng.choice(wl.total_q, 8, replace=False)
+    t0 = time.perf_counter()
+    oracle.fwd(q, k, v, wl.q_ranges, wl.k_ranges, wl.mask_types, rows=probe)
+    oracle.bwd(q, k, v, do, wl.q_ranges, wl.k_ranges, wl.mask_types, dq_rows=probe, dkv_keys=[])
+    dt = max(time.perf_counter() - t0, 1e-4)
+    per_pair = dt / max(1, counts[probe].sum())
+    n = int(np.clip(seconds / max(per_pair * counts.mean(), 1e-9), 8, wl.total_q))
+    rows = np.sort(rng.choice(wl.total_q, n, replace=False))
+    t0 = time.perf_counter()
+    oracle.fwd(q, k, v, wl.q_ranges, wl.k_ranges, wl.mask_types, rows=rows)
+    oracle.bwd(q, k, v, do, wl.q_ranges, wl.k_ranges, wl.mask_types, dq_rows=rows, dkv_keys=[])
+    t = time.perf_counter() - t0
+    flops = 14.0 * D * Hq * float(counts[rows].sum())
+    return {"value": flops / t / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": (f"{n} seeded query rows of {wl.total_q} x all {Hq} heads: fp64 forward + dq; "
+                       f"credited 14*D*Hq per visible pair (dK/dV credited, not run); "
+                       f"{t:.1f} s on the host")}, t
+
+
+def run_reference(args, wl, world, rank):
+    """The oracle as the reference arm: each step a bounded CPU sample."""
+    import torch
+    if rank != 0:
+        return
+    q, k, v, do = __import__("flexible_mask_attention_gb300.workloads",
+                             fromlist=["x"]).make_tensors(wl, with_dout=True)
+    per_step = max(1.0, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(wl, q, k, v, do, per_step / 4, seed=1)
+    vals, total_t = [], 0.0
+    last = None
+    for s in range(args.steps):
+        last, t = oracle_sample(wl, q, k, v, do, per_step, seed=100 + s)
+        vals.append(last["value"])
+        total_t += t
+    value = statistics.mean(vals)
+    line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": wl.name, "slices": wl.num_slices, "tokens": wl.total_q,
+                       "heads_q": wl.num_heads_q, "heads_kv": wl.num_heads_kv,
+                       "head_dim": wl.head_dim},
+            "cpu_baseline": dict(last, value=value),
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ffa(args, wl, world, rank, local):
+    import numpy as np
+    import torch
+
+    import flexible_mask_attention_gb300 as ffa
+    from flexible_mask_attention_gb300 import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q, k, v, do = W.make_tensors(wl, with_dout=True)
+    host = [t.pin_memory() for t in (q, k, v, do)]
+    qd, kd, vd, dod = (t.to(dev) for t in host)
+    qr = torch.as_tensor(wl.q_ranges, dtype=torch.int32)
+    kr = torch.as_tensor(wl.k_ranges, dtype=torch.int32)
+    ty = torch.as_tensor(wl.mask_types, dtype=torch.int32)
+    qr_d, kr_d, ty_d = qr.to(dev), kr.to(dev), ty.to(dev)
+    Tq, Tk, Hq, Hkv, D = wl.total_q, wl.total_k, wl.num_heads_q, wl.num_heads_kv, wl.head_dim
+    out = torch.empty_like(qd)
+    lse = torch.empty(Hq, Tq, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    plan0 = ffa.ffa_plan_create(qr_d, kr_d, ty_d, Tq, Tk, Hq, Hkv, D)
+    info = ffa.ffa_plan_info(plan0)
+    ws_f = torch.empty(max(16, ffa.ffa_fwd_workspace_size(plan0)), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(max(16, ffa.ffa_bwd_workspace_size(plan0)), dtype=torch.uint8, device=dev)
+    plan0.destroy()
+    area = info["area"]
+    f_fwd = 4.0 * D * area * Hq
+    f_bwd = 2.5 * f_fwd
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    def step(qa, ka, va, doa, record=None):
+        if record is not None:
+            record[0].record(stream)
+        plan = ffa.ffa_plan_create(qr_d, kr_d, ty_d, Tq, Tk, Hq, Hkv, D)
+        if record is not None:
+            record[1].record(stream)
+        ffa.ffa_fwd(plan, qa, ka, va, out=out, lse=lse, workspace=ws_f)
+        if record is not None:
+            record[2].record(stream)
+        ffa.ffa_bwd(plan, qa, ka, va, out, doa, lse, dq=dq, dk=dk, dv=dv, workspace=ws_b)
+        if record is not None:
+            record[3].record(stream)
+        return plan
+
+    for _ in range(args.warmup):
+        step(qd, kd, vd, dod).destroy()
+    torch.cuda.synchronize()
+    # correctness guard: no device error, finite results
+    p = step(qd, kd, vd, dod)
+    torch.cuda.synchronize()
+    err = ffa.ffa_get_last_device_error(p)
+    p.destroy()
+    if err != (0, 0):
+        raise RuntimeError(f"device error {err}")
+
+    sampler = ClockSampler(local)
+    launches0 = ffa.ffa_kernel_launch_count()
+    t_plan, t_fwd, t_bwd = [], [], []
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    plans = []
+    for _ in range(args.steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        plans.append((step(qd, kd, vd, dod, evs), evs))
+    end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier(world)
+    launches = ffa.ffa_kernel_launch_count() - launches0
+    elapsed_ms = start.elapsed_time(end)
+    for pl, evs in plans:
+        t_plan.append(evs[0].elapsed_time(evs[1]))
+        t_fwd.append(evs[1].elapsed_time(evs[2]))
+        t_bwd.append(evs[2].elapsed_time(evs[3]))
+        pl.destroy()
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    ms_step = elapsed_ms / args.steps
+    value = world * args.steps * (f_fwd + f_bwd) / (elapsed_ms / 1e3) / 1e12
+
+    # end to end through the public API with host buffers
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dq_h, dk_h, dv_h = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv))
+    h2d = sum(t.numel() * t.element_size() for t in host) + 3 * qr.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in (out_h, lse_h, dq_h, dk_h, dv_h))
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        qa, ka, va, doa = (t.to(dev, non_blocking=True) for t in host)
+        pl = step(qa, ka, va, doa)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        dq_h.copy_(dq, non_blocking=True)
+        dk_h.copy_(dk, non_blocking=True)
+        dv_h.copy_(dv, non_blocking=True)
+        pl.destroy()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = world * args.steps * (f_fwd + f_bwd) / (e2e_ms / 1e3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    fwd_ms, bwd_ms, plan_ms = (statistics.mean(x) for x in (t_fwd, t_bwd, t_plan))
+    dom = "bwd" if bwd_ms >= fwd_ms else "fwd"
+    dom_ms = bwd_ms if dom == "bwd" else fwd_ms
+    dom_flops = f_bwd if dom == "bwd" else f_fwd
+    achieved = dom_flops / (dom_ms / 1e3) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "traffic": traffic_from_profile("ffa_bwd_kernel" if dom == "bwd" else "ffa_fwd_kernel"),
+                "kernel": "backward (preprocess + main + dq convert)" if dom == "bwd" else "forward",
+                "peak_source": f"{peak_src} bf16_tflops_sustained",
+                "frac_of_burst_peak": achieved / peaks["bf16_tflops"]}
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "slices": wl.num_slices, "tokens": Tq,
+                   "heads_q": Hq, "heads_kv": Hkv, "head_dim": D,
+                   "visible_pairs_per_head": area, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (q, k, v, dout 268 MB each)"},
+        "phases_ms": {"plan": plan_ms, "fwd": fwd_ms, "bwd": bwd_ms},
+        "fwd_tflops": f_fwd / (fwd_ms / 1e3) / 1e12,
+        "bwd_tflops": f_bwd / (bwd_ms / 1e3) / 1e12,
+        "fwd_frac_of_peak": f_fwd / (fwd_ms / 1e3) / 1e12 / peak,
+        "bwd_frac_of_peak": f_bwd / (bwd_ms / 1e3) / 1e12 / peak,
+        "roofline": roofline,
+        "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"], _ = oracle_sample(wl, q, k, v, do, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    from flexible_mask_attention_gb300 import workloads as W
+    wl = W.CONFIGS[args.config]()
+    if args.impl == "reference":
+        world, rank, _ = dist_setup(use_cuda=False)
+        run_reference(args, wl, world, rank)
+    else:
+        world, rank, local = dist_setup(use_cuda=True)
+        run_ffa(args, wl, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -18,7 +18,8 @@ __all__ = [
     "FFA_FULL", "FFA_CAUSAL", "FFA_INV_CAUSAL", "FFA_BI_CAUSAL", "FFAError", "Plan",
     "library_path", "load_library", "ffa_plan_create", "ffa_plan_destroy", "ffa_plan_info",
     "ffa_plan_export", "ffa_fwd_workspace_size", "ffa_bwd_workspace_size", "ffa_fwd", "ffa_bwd",
-    "ffa_get_last_device_error", "ffa_plan_set_wait_limit", "EXPORTED_SYMBOLS",
+    "ffa_get_last_device_error", "ffa_plan_set_wait_limit", "ffa_kernel_launch_count",
+    "EXPORTED_SYMBOLS",
 ]
 
 FFA_FULL, FFA_CAUSAL, FFA_INV_CAUSAL, FFA_BI_CAUSAL = 0, 1, 2, 3
@@ -32,6 +33,7 @@ EXPORTED_SYMBOLS = [
     "ffa_plan_create", "ffa_plan_destroy", "ffa_plan_info", "ffa_plan_export",
     "ffa_fwd_workspace_size", "ffa_bwd_workspace_size", "ffa_fwd", "ffa_bwd",
     "ffa_get_last_device_error", "ffa_plan_set_wait_limit", "ffa_status_string",
+    "ffa_kernel_launch_count",
 ]
 
 
@@ -82,9 +84,11 @@ def load_library():
     lib.ffa_plan_set_wait_limit.argtypes = [P, U64]
     lib.ffa_status_string.argtypes = [I32]
     lib.ffa_status_string.restype = ctypes.c_char_p
+    lib.ffa_kernel_launch_count.argtypes = []
+    lib.ffa_kernel_launch_count.restype = U64
     for name in EXPORTED_SYMBOLS:
-        if name != "ffa_fwd_workspace_size" and name != "ffa_bwd_workspace_size" \
-                and name != "ffa_status_string":
+        if name not in ("ffa_fwd_workspace_size", "ffa_bwd_workspace_size", "ffa_status_string",
+                        "ffa_kernel_launch_count"):
             getattr(lib, name).restype = I32
     _lib = lib
     return lib
@@ -264,6 +268,11 @@ def ffa_get_last_device_error(plan: Plan, stream=None):
 def ffa_plan_set_wait_limit(plan: Plan, nanoseconds: int):
     _check("ffa_plan_set_wait_limit",
            load_library().ffa_plan_set_wait_limit(plan.handle, int(nanoseconds)))
+
+
+def ffa_kernel_launch_count() -> int:
+    """Kernels the library has launched in this process."""
+    return int(load_library().ffa_kernel_launch_count())
 
 
 def default_scale(head_dim: int) -> float:

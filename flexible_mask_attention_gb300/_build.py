@@ -54,7 +54,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
     tmp = LIB + f".tmp{os.getpid()}"
-    subprocess.check_call([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"])
+    subprocess.check_call([nvcc, *ARCH, "-shared", "--cudart", "static", "-o", tmp, *objs])
     os.replace(tmp, LIB)
     return LIB
 

@@ -503,6 +503,7 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     ffa_bwd_pre_kernel<D><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse,
         p->Tq, p->Hq, qpad, lse2, delta, dq_acc);
+    note_launches(1);
     if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   }
   alignas(64) CUtensorMap tq, tk, tv, tdo;
@@ -533,10 +534,12 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
                            C::kSmemBytes) != cudaSuccess)
     return FFA_ERR_CUDA;
   ffa_bwd_kernel<D><<<p->grid_bwd, kBwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, P);
+  note_launches(1);
   if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   const long long n8 = (long long)p->Tq * p->Hq * D / 8;
   ffa_dq_convert_kernel<D><<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(
       dq_acc, static_cast<__nv_bfloat16*>(dq), n8);
+  note_launches(1);
   if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   return FFA_OK;
 }

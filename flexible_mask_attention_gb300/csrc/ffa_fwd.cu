@@ -500,10 +500,12 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
                            C::kSmemBytes) != cudaSuccess)
     return FFA_ERR_CUDA;
   ffa_fwd_kernel<D><<<p->grid_fwd, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, P);
+  note_launches(1);
   if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   if (p->n_merges > 0) {
     ffa_merge_kernel<D><<<(int)(2 * p->n_merges), 128, 0, st>>>(
         p->merges, P.part_o, P.part_lse, p->Tq, p->Hq, P.out, lse);
+    note_launches(1);
     if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   }
   return FFA_OK;

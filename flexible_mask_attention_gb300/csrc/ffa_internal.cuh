@@ -81,4 +81,5 @@ ffa_status_t launch_bwd(ffa_plan_s* p, const void* q, const void* k, const void*
 size_t bwd_workspace_bytes(const ffa_plan_s* p);
 // Implemented in ffa_plan.cu.
 bool encode_tile_map(void* map128, const void* base, int rows, int cols_elems);
+void note_launches(int n);  // adds to the count reported by ffa_kernel_launch_count
 }  // namespace ffa

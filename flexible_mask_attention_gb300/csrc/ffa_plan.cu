@@ -24,6 +24,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <vector>
 
 #include "ffa_internal.cuh"
@@ -410,8 +411,10 @@ inline int grid_for(long long n, int block) { return (int)std::max(1LL, (n + blo
 
 ffa_status_t scan(const int* in, int n, int* out, long long* dtot, long long* htot,
                   cudaStream_t st) {
-  if (n > 0) k_scan<<<1, 1024, 0, st>>>(in, n, out, dtot);
-  else FFA_CUDA(cudaMemsetAsync(dtot, 0, sizeof(long long), st));
+  if (n > 0) {
+    k_scan<<<1, 1024, 0, st>>>(in, n, out, dtot);
+    note_launches(1);
+  } else FFA_CUDA(cudaMemsetAsync(dtot, 0, sizeof(long long), st));
   FFA_CUDA(cudaGetLastError());
   FFA_CUDA(cudaMemcpyAsync(htot, dtot, sizeof(long long), cudaMemcpyDeviceToHost, st));
   FFA_CUDA(cudaStreamSynchronize(st));
@@ -427,6 +430,7 @@ ffa_status_t sort_items(const int* items, int words, int cost_word, int n, int* 
   FFA_CUDA(scratch.alloc(sizeof(unsigned long long) * (size_t)n2));
   k_sort_order<<<1, 1024, 0, st>>>(items, words, cost_word, n, n2,
                                    scratch.as<unsigned long long>(), order);
+  note_launches(1);
   FFA_CUDA(cudaGetLastError());
   FFA_CUDA(cudaStreamSynchronize(st));
   return FFA_OK;
@@ -455,8 +459,11 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   FFA_CUDA(cudaMemsetAsync(flags, 0, 64, st));
   if (S > 0) {
     k_pack_slices<<<grid_for(S, 256), 256, 0, st>>>(qr, kr, ty, S, p->slices);
+    note_launches(1);
     k_check_slices<<<grid_for(S, 256), 256, 0, st>>>(p->slices, S, p->Tq, p->Tk, flags, area);
+    note_launches(1);
     k_check_overlap<<<grid_for((long long)S * S, 256), 256, 0, st>>>(p->slices, S, flags);
+    note_launches(1);
     FFA_CUDA(cudaGetLastError());
   }
   int hflags[4];
@@ -475,6 +482,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   FFA_CUDA(vcnt.alloc(sizeof(int) * n_qt));
   FFA_CUDA(voff.alloc(sizeof(int) * n_qt));
   k_fwd_visit_count<<<grid_for(n_qt, 128), 128, 0, st>>>(p->slices, S, n_qt, vcnt.as<int>());
+  note_launches(1);
   FFA_CUDA(cudaGetLastError());
   ffa_status_t rc = scan(vcnt.as<int>(), n_qt, voff.as<int>(), dtot, &tot, st);
   if (rc != FFA_OK) return rc;
@@ -482,6 +490,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   FFA_CUDA(visits.alloc(sizeof(int2) * (size_t)tot));
   k_fwd_visit_fill<<<grid_for(n_qt, 64), 64, 0, st>>>(p->slices, S, n_qt, voff.as<int>(),
                                                       visits.as<int2>());
+  note_launches(1);
   FFA_CUDA(cudaGetLastError());
   // forward units -> steps
   const int pair_mode = g >= 2 ? 0 : 1;
@@ -494,6 +503,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
                                                            vcnt.as<int>(), n_qt, n_units,
                                                            pair_mode, scnt.as<int>(),
                                                            cost_half.as<int>());
+  note_launches(1);
   FFA_CUDA(cudaGetLastError());
   rc = scan(scnt.as<int>(), n_units, soff.as<int>(), dtot, &tot, st);
   if (rc != FFA_OK) return rc;
@@ -503,6 +513,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
                                                           vcnt.as<int>(), n_qt, n_units,
                                                           pair_mode, soff.as<int>(),
                                                           steps.as<int4>());
+  note_launches(1);
   FFA_CUDA(cudaGetLastError());
   // forward items
   const int pairs = (g + 1) / 2;
@@ -517,6 +528,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
                                                       pairs, n_qt, soff.as<int>(), scnt.as<int>(),
                                                       cost_half.as<int>(), items.as<int>(),
                                                       live.as<int>());
+  note_launches(1);
   FFA_CUDA(cudaGetLastError());
   int hlive = 0;
   FFA_CUDA(cudaMemcpyAsync(&hlive, live.p, sizeof(int), cudaMemcpyDeviceToHost, st));
@@ -536,6 +548,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
     k_split_count<<<grid_for(n_items, 128), 128, 0, st>>>(items.as<int>(), (int)n_items, nsplit,
                                                           chunks.as<int>(), slots.as<int>(),
                                                           groups.as<int>());
+    note_launches(1);
     FFA_CUDA(cudaGetLastError());
     long long n_chunks = 0, n_slots = 0, n_groups = 0;
     if ((rc = scan(chunks.as<int>(), (int)n_items, coff.as<int>(), dtot, &n_chunks, st))) return rc;
@@ -546,6 +559,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
     k_split_fill<<<grid_for(n_items, 128), 128, 0, st>>>(
         items.as<int>(), (int)n_items, chunks.as<int>(), coff.as<int>(), sloff.as<int>(),
         goff.as<int>(), nitems.as<int>(), merges.as<int>());
+    note_launches(1);
     FFA_CUDA(cudaGetLastError());
     FFA_CUDA(cudaStreamSynchronize(st));
     std::swap(items.p, nitems.p);
@@ -568,6 +582,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   FFA_CUDA(bcnt.alloc(sizeof(int) * n_kt));
   FFA_CUDA(boff.alloc(sizeof(int) * n_kt));
   k_bwd_visit_count<<<grid_for(n_kt, 128), 128, 0, st>>>(p->slices, S, n_kt, bcnt.as<int>());
+  note_launches(1);
   FFA_CUDA(cudaGetLastError());
   if ((rc = scan(bcnt.as<int>(), n_kt, boff.as<int>(), dtot, &tot, st))) return rc;
   if (tot > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
@@ -576,6 +591,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   FFA_CUDA(cudaMalloc(&p->bwd_steps, sizeof(int4) * (size_t)std::max(1LL, tot)));
   k_bwd_visit_fill<<<grid_for(n_kt, 64), 64, 0, st>>>(p->slices, S, n_kt, boff.as<int>(),
                                                       bvis.as<int2>());
+  note_launches(1);
   const long long nb_items = (long long)n_kt * p->Hkv;
   p->n_bwd_items = nb_items;
   FFA_CUDA(cudaMalloc(&p->bwd_items, sizeof(int) * kBiWords * (size_t)std::max(1LL, nb_items)));
@@ -583,6 +599,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   k_bwd_items<<<grid_for(nb_items, 128), 128, 0, st>>>(n_kt, p->Hkv, g, bvis.as<int2>(),
                                                        boff.as<int>(), bcnt.as<int>(),
                                                        p->bwd_steps, p->bwd_items);
+  note_launches(1);
   FFA_CUDA(cudaGetLastError());
   rc = sort_items(p->bwd_items, kBiWords, kBiCost, (int)nb_items, p->bwd_order, st);
   if (rc != FFA_OK) return rc;
@@ -607,7 +624,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+std::atomic<uint64_t> g_launches{0};
+
 }  // namespace
+
+void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+uint64_t g_launches_total() { return g_launches.load(std::memory_order_relaxed); }
 
 // 2-D tensor map over a row-major [rows][cols] bf16 matrix: boxes of
 // 128 rows x 64 columns (128 bytes), 128-byte swizzle, zero fill outside.
@@ -766,6 +788,8 @@ ffa_status_t ffa_plan_set_wait_limit(ffa_plan_t p, uint64_t ns) {
   p->wait_ns = ns;
   return FFA_OK;
 }
+
+uint64_t ffa_kernel_launch_count(void) { return ffa::g_launches_total(); }
 
 const char* ffa_status_string(ffa_status_t s) {
   switch (s) {

@@ -94,7 +94,7 @@ typedef struct {
   int64_t fwd_items;  /* 8 words per item */
   int64_t bwd_steps;  /* 4 words per step */
   int64_t bwd_items;  /* 8 words per item */
-  int64_t merges;     /* 4 words per merge group */
+  int64_t merges;     /* 8 words per merge group */
   int32_t grid_fwd;   /* CTAs of the forward kernel */
   int32_t grid_bwd;   /* CTAs of the backward kernel */
   int64_t area;       /* visible (q, k) pairs per head: sum over rows of |keys seen| */
@@ -115,8 +115,8 @@ size_t ffa_fwd_workspace_size(ffa_plan_t plan);
 size_t ffa_bwd_workspace_size(ffa_plan_t plan);
 
 /* Forward: out[Tq][Hq][D] (bf16) and lse[Hq][Tq] (fp32, natural log).
- *   softmax_scale <= 0 selects 1/sqrt(D) (quickstart: "Defaults to
- *   1/sqrt(head_dim)").  workspace: device memory of ffa_fwd_workspace_size
+ *   softmax_scale <= 0 selects 1/sqrt(D), the default the quickstart
+ *   card gives.  workspace: device memory of ffa_fwd_workspace_size
  *   bytes (may be NULL when that size is 0), contents need not be set.
  * Rows that see no key are written as out = 0, lse = -inf. */
 ffa_status_t ffa_fwd(ffa_plan_t plan, const void* q, const void* k, const void* v,
@@ -145,6 +145,10 @@ ffa_status_t ffa_plan_set_wait_limit(ffa_plan_t plan, uint64_t nanoseconds);
 
 /* Human-readable name of a status code (static storage). */
 const char* ffa_status_string(ffa_status_t status);
+
+/* Number of CUDA kernels this library has launched in the calling process
+ * (planner, forward, merge and backward kernels).  For instrumentation. */
+uint64_t ffa_kernel_launch_count(void);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,57 @@
+"""The device planner's work lists equal the CPU re-derivation bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import flexible_mask_attention_gb300 as ffa
+from flexible_mask_attention_gb300 import workloads as W
+from oracle import planner
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ["fwd_steps", "fwd_items", "fwd_order", "bwd_steps", "bwd_items", "bwd_order", "merges"]
+
+
+def compare(qr, kr, ty, Tq, Tk, Hq, Hkv, D, split_below=0):
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = ffa.ffa_plan_create(qr, kr, ty, Tq, Tk, Hq, Hkv, D, split_below=split_below)
+    ref = planner.plan(Tq, Tk, Hq, Hkv, qr, kr, ty, num_sms=nsm, split_below=split_below)
+    for which, name in enumerate(NAMES):
+        got = ffa.ffa_plan_export(plan, which)
+        exp = ref[name].reshape(got.shape) if ref[name].size == got.size else ref[name]
+        assert got.shape == exp.shape and np.array_equal(got, exp), f"{name} differs"
+    info = ffa.ffa_plan_info(plan)
+    assert info["area"] == ref["area"]
+    assert info["grid_fwd"] == ref["grid_fwd"] and info["grid_bwd"] == ref["grid_bwd"]
+    plan.destroy()
+
+
+@pytest.mark.parametrize("name", ["tiny", "packed_causal", "heterogeneous", "long_context"])
+def test_configs(name):
+    wl = W.CONFIGS[name]()
+    compare(wl.q_ranges, wl.k_ranges, wl.mask_types, wl.total_q, wl.total_k, wl.num_heads_q,
+            wl.num_heads_kv, wl.head_dim)
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("heads", [(4, 2), (2, 2), (3, 1)])
+def test_random(seed, heads):
+    rng = np.random.default_rng(seed)
+    Tq, Tk = int(rng.integers(100, 3000)), int(rng.integers(100, 3000))
+    qr, kr, ty = W.random_slices(Tq, Tk, int(rng.integers(1, 12)), seed=seed)
+    compare(qr, kr, ty, Tq, Tk, heads[0], heads[1], 128, split_below=[0, -1, 400][seed % 3])
+
+
+def test_rejects_bad_slices():
+    with pytest.raises(ffa.FFAError) as e:
+        ffa.ffa_plan_create([[0, 10], [5, 20]], [[0, 10], [5, 20]], [0, 0], 32, 32, 1, 1, 128)
+    assert e.value.status == 3
+    with pytest.raises(ffa.FFAError) as e:
+        ffa.ffa_plan_create([[0, 40]], [[0, 10]], [0], 32, 32, 1, 1, 128)
+    assert e.value.status == 2
+    with pytest.raises(ffa.FFAError) as e:
+        ffa.ffa_plan_create([[0, 10]], [[0, 10]], [5], 32, 32, 1, 1, 128)
+    assert e.value.status == 2
+    with pytest.raises(ffa.FFAError) as e:
+        ffa.ffa_plan_create([[0, 10]], [[0, 10]], [0], 32, 32, 1, 1, 96)
+    assert e.value.status == 4
