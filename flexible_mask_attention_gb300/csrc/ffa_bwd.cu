@@ -1,7 +1,7 @@
 // Backward kernels of flexible-mask attention for sm_103a.
 //
-//   1. preprocess: delta[h][q] = <dO, O> (fp32), lse2 = lse * log2(e), and
-//      dQaccum = 0;
+//   1. preprocess: -delta[h][q] = -<dO, O> (fp32), -lse * log2(e), and
+//      dQaccum = 0 (stored negated so the main kernel adds them with FMAs);
 //   2. main: one work item per (k-tile, kv head).  The 128 x D tiles of K and
 //      V stay in shared memory; the item loops over every (q-tile, query head
 //      of the group) that sees the k-tile:
@@ -11,7 +11,8 @@
 //          dS^T = P^T * (dP^T - delta)
 //          dV  += P^T dO          (tcgen05, A = P^T from TMEM)
 //          dK  += dS^T Q          (tcgen05, A = dS^T from TMEM)
-//          dQ   = dS K            (tcgen05, A = dS from shared memory)
+//          dQ^T = K^T dS^T        (tcgen05, both operands from shared memory;
+//                                  dQ = dS K when D = 64)
 //      dK and dV accumulate in TMEM and are written once per item (no
 //      atomics); each dQ tile is added into the fp32 dQaccum.
 //   3. convert: dq = bf16(dQaccum).
@@ -47,7 +48,9 @@ struct BwdCfg {
   static constexpr int kQOff = 2 * kTileBytes;
   static constexpr int kDOOff = kQOff + kStages * kTileBytes;
   static constexpr int kDSOff = kDOOff + kStages * kTileBytes;  // 128 x 128 bf16
-  static constexpr int kBarOff = kDSOff + 128 * 128 * 2;
+  static constexpr int kLseOff = kDSOff + 128 * 128 * 2;         // per stage: -lse2[128], -delta[128]
+  static constexpr int kLseStageBytes = 2 * 128 * 4;
+  static constexpr int kBarOff = kLseOff + kStages * kLseStageBytes;
   static constexpr int kBKVFull = 0, kBKVEmpty = 1, kBQFull = 2, kBQEmpty = 2 + kStages,
                        kBDOFull = 2 + 2 * kStages, kBDOEmpty = 2 + 3 * kStages,
                        kBSdpFull = 2 + 4 * kStages, kBPFull = kBSdpFull + 1,
@@ -55,7 +58,8 @@ struct BwdCfg {
                        kBDkvEmpty = kBDkvFull + 1, kBDrain = kBDkvEmpty + 1,
                        kNumBars = kBDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
+  // The dynamic shared memory base must be 1024-byte aligned (checked on entry).
+  static constexpr int kSmemBytes = kMiscOff + 64;
   // TMEM columns
   static constexpr int kTdV = 0, kTdK = D, kTS = 2 * D, kTdP = 2 * D + 128;
 };
@@ -68,8 +72,8 @@ struct BwdParams {
   const Slice* slices;
   int Tq, Tk, Hq, g, qpad;
   float scale, scale_log2;
-  const float* lse2;   // [Hq][qpad] log2-scaled lse
-  const float* delta;  // [Hq][qpad]
+  const float* nlse2;   // [Hq][qpad] -lse * log2(e)
+  const float* ndelta;  // [Hq][qpad] -rowsum(dO * O)
   float* dq_acc;       // [Tq][Hq][D]
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -106,15 +110,70 @@ __device__ __forceinline__ void key_query_window(const Slice& sl, int key, int q
   hi = b - qt * 128;
 }
 
+// P^T and dS^T for one key row j over the 128 queries of the step:
+//   p = 2^(s * scale * log2e - lse2), ds = p * (dp - delta)
+// written as bf16 pairs to TMEM (over the first 64 columns of S^T and dP^T)
+// and dS to the 128-byte swizzled shared-memory tile (row j, query chunks).
+template <bool kPartial>
+__device__ __forceinline__ void pds_tile(uint32_t tS, uint32_t tP, const float* nl,
+                                         const float* nd, float scale_log2, int lo, int hi, int j,
+                                         uint8_t* ds_row) {
+  const float2 sc2 = make_float2(scale_log2, scale_log2);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t r[64];  // r[0..32): S^T, r[32..64): dP^T
+    tmem_ld32x2(tS + 32 * c, tP + 32 * c, r);
+    uint32_t pp[16], dd[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      const float4 l4 = *reinterpret_cast<const float4*>(nl + 32 * c + e);
+      const float4 d4 = *reinterpret_cast<const float4*>(nd + 32 * c + e);
+#pragma unroll
+      for (int u = 0; u < 4; u += 2) {
+        const int col = 32 * c + e + u;
+        const float2 nlp = u == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
+        const float2 ndp = u == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
+        const float2 x = __ffma2_rn(
+            make_float2(__uint_as_float(r[e + u]), __uint_as_float(r[e + u + 1])), sc2, nlp);
+        float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        if (kPartial) {
+          p.x = (col >= lo && col < hi) ? p.x : 0.f;
+          p.y = (col + 1 >= lo && col + 1 < hi) ? p.y : 0.f;
+        }
+        const float2 dpd = __fadd2_rn(
+            make_float2(__uint_as_float(r[32 + e + u]), __uint_as_float(r[32 + e + u + 1])), ndp);
+        const float2 ds = __fmul2_rn(p, dpd);
+        pp[(e + u) >> 1] = pack_bf16x2(p.x, p.y);
+        dd[(e + u) >> 1] = pack_bf16x2(ds.x, ds.y);
+      }
+    }
+    tmem_st16(tS + 16 * c, pp);
+    tmem_st16(tP + 16 * c, dd);
+    // dS row j, queries [32c, 32c+32): four 16-byte units of the swizzled row
+    // of query chunk c/2.
+    uint8_t* base = ds_row + (c >> 1) * 16384;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int unit = (c & 1) * 4 + u;
+      *reinterpret_cast<uint4*>(base + ((unit ^ (j & 7)) << 4)) =
+          make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     ffa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const BwdParams P) {
   using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if ((smem_u32(smem) & 1023u) != 0) {
+    // The swizzled tile layout needs a 1024-byte aligned base; refuse to run.
+    if (threadIdx.x == 0) record_error(P.err, kDevBadSmemAlign, 1);
+    return;
+  }
   const uint32_t sbase = smem_u32(smem);
   auto bar = [&](int i) -> uint32_t { return sbase + C::kBarOff + 8 * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
@@ -159,7 +218,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_do);
       uint32_t kv_cnt = 0, q_cnt = 0;
-      bool ok = true;
+      bool ok = true, q_only = false;  // q_only: Q of iteration q_cnt issued, its dO not yet
       const int* it;
       for (int r = 0; ok && bwd_item_at(P, r, it); ++r) {
         const int sb = it[kBiStepBeg], se = it[kBiStepEnd];
@@ -181,11 +240,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int stage = q_cnt % C::kStages;
           const uint32_t ph = (q_cnt / C::kStages) & 1;
           if (!(ok = mbar_wait(bar(C::kBQEmpty + stage), ph ^ 1, ctl, 401))) break;
-          mbar_arrive_expect_tx(bar(C::kBQFull + stage), C::kTileBytes);
+          mbar_arrive_expect_tx(bar(C::kBQFull + stage), C::kTileBytes + C::kLseStageBytes);
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_2d(sbase + C::kQOff + stage * C::kTileBytes + c * 16384, &tm_q,
                         bar(C::kBQFull + stage), h * D + c * 64, qt * 128);
+          const uint32_t ls = sbase + C::kLseOff + stage * C::kLseStageBytes;
+          bulk_load(ls, P.nlse2 + (size_t)h * P.qpad + qt * 128, 512, bar(C::kBQFull + stage));
+          bulk_load(ls + 512, P.ndelta + (size_t)h * P.qpad + qt * 128, 512,
+                    bar(C::kBQFull + stage));
+          q_only = true;
           if (!(ok = mbar_wait(bar(C::kBDOEmpty + stage), ph ^ 1, ctl, 402))) break;
+          q_only = false;
           mbar_arrive_expect_tx(bar(C::kBDOFull + stage), C::kTileBytes);
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_2d(sbase + C::kDOOff + stage * C::kTileBytes + c * 16384, &tm_do,
@@ -194,11 +259,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       if (!ok) {
-        if (kv_cnt > 0) drain_wait_b(bar(C::kBKVFull), (kv_cnt - 1) & 1, P.wait_ns);
+        if (kv_cnt > 0) drain_wait_b(bar(C::kBKVFull), (kv_cnt - 1) & 1, kDrainNs);
         for (uint32_t i = q_cnt > (uint32_t)C::kStages ? q_cnt - C::kStages : 0; i < q_cnt; ++i) {
-          drain_wait_b(bar(C::kBQFull + i % C::kStages), (i / C::kStages) & 1, P.wait_ns);
-          drain_wait_b(bar(C::kBDOFull + i % C::kStages), (i / C::kStages) & 1, P.wait_ns);
+          drain_wait_b(bar(C::kBQFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
+          drain_wait_b(bar(C::kBDOFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
         }
+        if (q_only)
+          drain_wait_b(bar(C::kBQFull + q_cnt % C::kStages), (q_cnt / C::kStages) & 1, kDrainNs);
       }
     }
   } else if (warp == 9) {
@@ -206,7 +273,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdAcc = idesc_bf16(128, D, false, true);   // A from TMEM, B MN-major
-      constexpr uint32_t kIdDq = idesc_bf16(128, D, true, true);     // A and B MN-major
+      constexpr uint32_t kIdDq = idesc_bf16(128, D == 128 ? 128 : D, true, true);  // both MN-major
       const uint32_t kA = sbase + C::kKOff, vA = sbase + C::kVOff, dsA = sbase + C::kDSOff;
       uint32_t kv_cnt = 0, q_cnt = 0, p_cnt = 0, dqf_cnt = 0, dkv_cnt = 0;
       bool ok = true, dq_pending = false;
@@ -263,10 +330,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           mma_commit(bar(C::kBDOEmpty + stage));
           mma_commit(bar(C::kBQEmpty + stage));
+          if constexpr (D == 128) {
+            // dQ^T = K^T dS^T: lanes = head dim, columns = queries, so the dQ
+            // warps reduce whole 128-byte row segments.
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + C::kTS, sdesc_sw128(dsA + kk * 2048, 16384, 1024),
-                   sdesc_sw128(kA + kk * 2048, 16384, 1024), kIdDq, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tmem + C::kTS, sdesc_sw128(kA + kk * 2048, 16384, 1024),
+                     sdesc_sw128(dsA + kk * 2048, 16384, 1024), kIdDq, kk > 0 ? 1u : 0u);
+          } else {
+            // dQ = dS K: lanes = queries.
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tmem + C::kTS, sdesc_sw128(dsA + kk * 2048, 16384, 1024),
+                     sdesc_sw128(kA + kk * 2048, 16384, 1024), kIdDq, kk > 0 ? 1u : 0u);
+          }
           mma_commit(bar(C::kBDqFull));
           dq_pending = true;
           ++q_cnt;
@@ -276,7 +353,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_commit(bar(C::kBKVEmpty));
       }
       mma_commit(bar(C::kBDrain));
-      drain_wait_b(bar(C::kBDrain), 0, P.wait_ns);
+      drain_wait_b(bar(C::kBDrain), 0, kDrainNs);
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ P / dS warps
@@ -299,50 +376,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int h = hk * g + i % g;
         int lo = 0, hi = 128;
         if (info & 1) key_query_window(P.slices[info >> 1], key, qt, lo, hi);
-        const float* lse_row = P.lse2 + (size_t)h * P.qpad + qt * 128;
-        const float* dl_row = P.delta + (size_t)h * P.qpad + qt * 128;
+        const float* nl = reinterpret_cast<const float*>(smem + C::kLseOff +
+                                                         (sdp_cnt % C::kStages) * C::kLseStageBytes);
+        const float* nd = nl + 128;
         bool w = mbar_wait(bar(C::kBSdpFull), sdp_cnt & 1, ctl, 600);
         if (!(ok = __all_sync(0xffffffffu, w))) break;
         ++sdp_cnt;
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sv[32], dv[32];
-          tmem_ld32(tS + 32 * c, sv);
-          tmem_ld32(tP + 32 * c, dv);
-          uint32_t pp[16], dd[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(lse_row + 32 * c + e);
-            const float4 d4 = *reinterpret_cast<const float4*>(dl_row + 32 * c + e);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-            const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
-            float p[4], ds[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int col = 32 * c + e + u;
-              const float x = fmaf(__uint_as_float(sv[e + u]), P.scale_log2, -lv[u]);
-              const float pe = ex2_approx(x);
-              p[u] = (col >= lo && col < hi) ? pe : 0.f;
-              ds[u] = p[u] * (__uint_as_float(dv[e + u]) - dl[u]);
-            }
-            pp[e / 2] = pack_bf16x2(p[0], p[1]);
-            pp[e / 2 + 1] = pack_bf16x2(p[2], p[3]);
-            dd[e / 2] = pack_bf16x2(ds[0], ds[1]);
-            dd[e / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
-          }
-          tmem_st16(tS + 16 * c, pp);
-          tmem_st16(tP + 16 * c, dd);
-          // dS row j, queries [32c, 32c+32): four 16-byte units of the 128-byte
-          // swizzled row of column chunk c/2.
-          uint8_t* base = ds_row + (c >> 1) * 16384;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int unit = (c & 1) * 4 + u;
-            *reinterpret_cast<uint4*>(base + ((unit ^ (j & 7)) << 4)) =
-                make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
-          }
-        }
+        if (info & 1) pds_tile<true>(tS, tP, nl, nd, P.scale_log2, lo, hi, j, ds_row);
+        else pds_tile<false>(tS, tP, nl, nd, P.scale_log2, 0, 128, j, ds_row);
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
@@ -350,47 +392,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!ok) break;
       // ---- dK / dV epilogue (written once per item; zeros when no query sees the tile)
-      float dvv[D], dkv[D];
+      uint4* pv = reinterpret_cast<uint4*>(P.dv + ((size_t)key * (P.Hq / g) + hk) * D);
+      uint4* pk = reinterpret_cast<uint4*>(P.dk + ((size_t)key * (P.Hq / g) + hk) * D);
+      const bool store = key < P.Tk;
       if (n_it > 0) {
         bool w = mbar_wait(bar(C::kBDkvFull), dkv_cnt & 1, ctl, 610);
         if (!(ok = __all_sync(0xffffffffu, w))) break;
         ++dkv_cnt;
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+#pragma unroll 1
+        for (int c = 0; c < 2 * (D / 32); ++c) {
+          const bool is_k = c >= D / 32;
+          const int cc = is_k ? c - D / 32 : c;
           uint32_t u[32];
-          tmem_ld32(tmem + lane_addr + C::kTdV + 32 * c, u);
+          tmem_ld32(tmem + lane_addr + (is_k ? C::kTdK : C::kTdV) + 32 * cc, u);
+          if (c == 2 * (D / 32) - 1) {
+            tc_fence_before();
+            mbar_arrive(bar(C::kBDkvEmpty));
+          }
+          const float sc = is_k ? P.scale : 1.f;
+          uint4* dst = (is_k ? pk : pv) + cc * 4;
+          if (store) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) dvv[32 * c + e] = __uint_as_float(u[e]);
-          tmem_ld32(tmem + lane_addr + C::kTdK + 32 * c, u);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) dkv[32 * c + e] = __uint_as_float(u[e]) * P.scale;
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(
+                  pack_bf16x2(__uint_as_float(u[8 * v]) * sc, __uint_as_float(u[8 * v + 1]) * sc),
+                  pack_bf16x2(__uint_as_float(u[8 * v + 2]) * sc, __uint_as_float(u[8 * v + 3]) * sc),
+                  pack_bf16x2(__uint_as_float(u[8 * v + 4]) * sc, __uint_as_float(u[8 * v + 5]) * sc),
+                  pack_bf16x2(__uint_as_float(u[8 * v + 6]) * sc, __uint_as_float(u[8 * v + 7]) * sc));
+          }
         }
-        tc_fence_before();
-        mbar_arrive(bar(C::kBDkvEmpty));
-      } else {
+      } else if (store) {
 #pragma unroll
-        for (int d = 0; d < D; ++d) dvv[d] = dkv[d] = 0.f;
-      }
-      if (key < P.Tk) {
-        uint4* pv = reinterpret_cast<uint4*>(P.dv + ((size_t)key * (P.Hq / g) + hk) * D);
-        uint4* pk = reinterpret_cast<uint4*>(P.dk + ((size_t)key * (P.Hq / g) + hk) * D);
-#pragma unroll
-        for (int v = 0; v < D / 8; ++v) {
-          pv[v] = make_uint4(pack_bf16x2(dvv[8 * v], dvv[8 * v + 1]),
-                             pack_bf16x2(dvv[8 * v + 2], dvv[8 * v + 3]),
-                             pack_bf16x2(dvv[8 * v + 4], dvv[8 * v + 5]),
-                             pack_bf16x2(dvv[8 * v + 6], dvv[8 * v + 7]));
-          pk[v] = make_uint4(pack_bf16x2(dkv[8 * v], dkv[8 * v + 1]),
-                             pack_bf16x2(dkv[8 * v + 2], dkv[8 * v + 3]),
-                             pack_bf16x2(dkv[8 * v + 4], dkv[8 * v + 5]),
-                             pack_bf16x2(dkv[8 * v + 6], dkv[8 * v + 7]));
-        }
+        for (int v = 0; v < D / 8; ++v) pv[v] = pk[v] = make_uint4(0, 0, 0, 0);
       }
     }
   } else {
     // ------------------------------------------------------------ dQ warps
-    const int rq = threadIdx.x - 128;  // query row of the tile
+    const int t = threadIdx.x - 128;  // TMEM lane: head-dim index (D = 128) or query row
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t dq_cnt = 0;
     bool ok = true;
@@ -403,32 +442,54 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int4 st = P.steps[sb + i / g];
         const int qt = st.x, info = st.y;
         const int h = hk * g + i % g;
-        const int q = qt * 128 + rq;
-        bool add = q < P.Tq;
+        // rows of this q-tile that can receive a non-zero dQ
+        int q_lo = qt * 128, q_hi = min(P.Tq, qt * 128 + 128);
         if (info & 1) {
           const Slice sl = P.slices[info >> 1];
-          add = add && q >= sl.qs && q < sl.qe;
+          q_lo = max(q_lo, sl.qs);
+          q_hi = min(q_hi, sl.qe);
         }
         bool w = mbar_wait(bar(C::kBDqFull), dq_cnt & 1, ctl, 700);
         if (!(ok = __all_sync(0xffffffffu, w))) break;
         ++dq_cnt;
         tc_fence_after();
-        float acc[D];
+        if constexpr (D == 128) {
+          // lane t = head-dim index; columns = queries of the tile.  Read the
+          // whole tile, hand the columns back to the MMA warp, then reduce.
+          uint32_t u[128];
+          tmem_ld128(tmem + lane_addr + C::kTS, u);
+          tc_fence_before();
+          mbar_arrive(bar(C::kBDqFree));
+          float* col = P.dq_acc + ((size_t)qt * 128 * P.Hq + h) * D + t;
+          const size_t row_stride = (size_t)P.Hq * D;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t u[32];
-          tmem_ld32(tmem + lane_addr + C::kTS + 32 * c, u);
+          for (int e = 0; e < 128; ++e) {
+            const int q = qt * 128 + e;
+            if (q >= q_lo && q < q_hi)
+              red_add_f32(col + (size_t)e * row_stride, __uint_as_float(u[e]) * P.scale);
+          }
+        } else {
+          // lane t = query row; columns = head dim
+          const int q = qt * 128 + t;
+          const bool add = q >= q_lo && q < q_hi;
+          float* dst = P.dq_acc + ((size_t)q * P.Hq + h) * D;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t u[32];
+            tmem_ld32(tmem + lane_addr + C::kTS + 32 * c, u);
+            if (c == D / 32 - 1) {
+              tc_fence_before();
+              mbar_arrive(bar(C::kBDqFree));
+            }
+            if (add) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) acc[32 * c + e] = __uint_as_float(u[e]);
-        }
-        tc_fence_before();
-        mbar_arrive(bar(C::kBDqFree));
-        if (add) {
-          float4* dst = reinterpret_cast<float4*>(P.dq_acc + ((size_t)q * P.Hq + h) * D);
-#pragma unroll
-          for (int v = 0; v < D / 4; ++v)
-            atomicAdd(dst + v, make_float4(acc[4 * v] * P.scale, acc[4 * v + 1] * P.scale,
-                                           acc[4 * v + 2] * P.scale, acc[4 * v + 3] * P.scale));
+              for (int v = 0; v < 8; ++v)
+                red_add_v4(dst + 32 * c + 4 * v, __uint_as_float(u[4 * v]) * P.scale,
+                           __uint_as_float(u[4 * v + 1]) * P.scale,
+                           __uint_as_float(u[4 * v + 2]) * P.scale,
+                           __uint_as_float(u[4 * v + 3]) * P.scale);
+            }
+          }
         }
       }
     }
@@ -442,7 +503,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-// delta = rowsum(dO * O), lse2 = lse * log2(e) (padded rows: 0), dQaccum = 0.
+// -delta = -rowsum(dO * O), -lse2 = -lse * log2(e) (padded rows: 0), dQaccum = 0.
 template <int D>
 __global__ void ffa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
                                    const __nv_bfloat16* __restrict__ dout,
@@ -474,8 +535,8 @@ __global__ void ffa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
     const float lv = lse[(size_t)h * Tq + q];
     l2 = lv * kLog2e;  // -inf stays -inf: such rows have no visible key
   }
-  lse2[(size_t)h * qpad + q] = l2;
-  delta[(size_t)h * qpad + q] = dsum;
+  lse2[(size_t)h * qpad + q] = -l2;
+  delta[(size_t)h * qpad + q] = -dsum;
 }
 
 template <int D>
@@ -523,8 +584,8 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   P.qpad = qpad;
   P.scale = scale;
   P.scale_log2 = scale * kLog2e;
-  P.lse2 = lse2;
-  P.delta = delta;
+  P.nlse2 = lse2;
+  P.ndelta = delta;
   P.dq_acc = dq_acc;
   P.dk = static_cast<__nv_bfloat16*>(dk);
   P.dv = static_cast<__nv_bfloat16*>(dv);

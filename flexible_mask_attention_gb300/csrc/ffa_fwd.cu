@@ -49,9 +49,9 @@ struct FwdCfg {
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
   // barrier indices
   static constexpr int kBQFull = 0, kBQEmpty = 1, kBKFull = 2, kBVFull = 2 + kStages,
-                       kBKVEmpty = 2 + 2 * kStages, kBSFull = 2 + 3 * kStages,
-                       kBPFull = kBSFull + 2, kBOFull = kBPFull + 2, kBOEmpty = kBOFull + 2,
-                       kBDrain = kBOEmpty + 2, kNumBars = kBDrain + 1;
+                       kBKEmpty = 2 + 2 * kStages, kBVEmpty = 2 + 3 * kStages,
+                       kBSFull = 2 + 4 * kStages, kBPFull = kBSFull + 2, kBOFull = kBPFull + 2,
+                       kBOEmpty = kBOFull + 2, kBDrain = kBOEmpty + 2, kNumBars = kBDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + alignment slack
 };
@@ -112,7 +112,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar(C::kBKFull + s), 1);
       mbar_init(bar(C::kBVFull + s), 1);
-      mbar_init(bar(C::kBKVEmpty + s), 1);
+      mbar_init(bar(C::kBKEmpty + s), 1);
+      mbar_init(bar(C::kBVEmpty + s), 1);
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(bar(C::kBSFull + h), 1);
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       uint32_t kv_cnt = 0, q_cnt = 0;
-      bool ok = true;
+      bool ok = true, k_only = false;  // k_only: K of step kv_cnt issued, its V not yet
       const int* it;
       for (int r = 0; ok && item_at(P, r, it); ++r) {
         const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
@@ -158,11 +159,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const int kt = P.steps[j].x;
           const int stage = kv_cnt % C::kStages;
           const uint32_t ph = (kv_cnt / C::kStages) & 1;
-          if (!(ok = mbar_wait(bar(C::kBKVEmpty + stage), ph ^ 1, ctl, 101))) break;
+          if (!(ok = mbar_wait(bar(C::kBKEmpty + stage), ph ^ 1, ctl, 101))) break;
           mbar_arrive_expect_tx(bar(C::kBKFull + stage), C::kTileBytes);
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_2d(sbase + C::kKOff + stage * C::kTileBytes + c * 16384, &tm_k,
                         bar(C::kBKFull + stage), hk * D + c * 64, kt * 128);
+          k_only = true;
+          if (!(ok = mbar_wait(bar(C::kBVEmpty + stage), ph ^ 1, ctl, 102))) break;
+          k_only = false;
           mbar_arrive_expect_tx(bar(C::kBVFull + stage), C::kTileBytes);
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_2d(sbase + C::kVOff + stage * C::kTileBytes + c * 16384, &tm_v,
@@ -172,11 +176,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (!ok) {
         // Aborted: let the copies already issued land before the CTA exits.
-        if (q_cnt > 0) drain_wait(bar(C::kBQFull), (q_cnt - 1) & 1, P.wait_ns);
+        if (q_cnt > 0) drain_wait(bar(C::kBQFull), (q_cnt - 1) & 1, kDrainNs);
         for (uint32_t i = kv_cnt > (uint32_t)C::kStages ? kv_cnt - C::kStages : 0; i < kv_cnt; ++i) {
-          drain_wait(bar(C::kBKFull + i % C::kStages), (i / C::kStages) & 1, P.wait_ns);
-          drain_wait(bar(C::kBVFull + i % C::kStages), (i / C::kStages) & 1, P.wait_ns);
+          drain_wait(bar(C::kBKFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
+          drain_wait(bar(C::kBVFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
         }
+        if (k_only)
+          drain_wait(bar(C::kBKFull + kv_cnt % C::kStages), (kv_cnt / C::kStages) & 1, kDrainNs);
       }
     }
   } else if (warp == 9) {
@@ -226,6 +232,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             issue_s(1, stage);
             mma_commit(bar(C::kBSFull + 1));
           }
+          mma_commit(bar(C::kBKEmpty + stage));  // every S of this step is issued
         }
         for (int j = sb; ok && j < se; ++j) {
           const uint32_t c = kv_cnt + (uint32_t)(j - sb);
@@ -236,6 +243,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const bool has_next = j + 1 < se;
           const int4 nxt = has_next ? P.steps[j + 1] : make_int4(0, -1, -1, 0);
           bool v_ready = false, k_next_ready = false;
+#pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int info = h == 0 ? cur.y : (act1 ? cur.z : -1);
             if (info >= 0) {
@@ -266,10 +274,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             }
           }
           if (!ok) break;
-          mma_commit(bar(C::kBKVEmpty + stage));
+          mma_commit(bar(C::kBVEmpty + stage));
+          if (has_next) mma_commit(bar(C::kBKEmpty + stage_n));  // S of step j+1 issued
           cur = nxt;
         }
         if (!ok) break;
+#pragma unroll
         for (int h = 0; h < 2; ++h)
           if (!first_pv[h]) mma_commit(bar(C::kBOFull + h));
         mma_commit(bar(C::kBQEmpty));
@@ -277,9 +287,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       // Every MMA issued so far must finish before TMEM is released.
       mma_commit(bar(C::kBDrain));
-      drain_wait(bar(C::kBDrain), 0, P.wait_ns);
+      drain_wait(bar(C::kBDrain), 0, kDrainNs);
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
     const int h = warp >> 2;
     const int row_in = threadIdx.x & 127;
@@ -297,23 +307,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int row = qt * 128 + row_in;
       float m = -INFINITY, l = 0.f;
       bool visited = false;
+      int4 st_next = sb < se ? P.steps[sb] : make_int4(0, -1, -1, 0);
       for (int j = sb; j < se; ++j) {
-        const int4 st = P.steps[j];
+        const int4 st = st_next;
+        if (j + 1 < se) st_next = P.steps[j + 1];  // prefetch the next step descriptor
         const int info = h == 0 ? st.y : st.z;
         if (info < 0) continue;
         const bool w = mbar_wait(bar(C::kBSFull + h), s_cnt & 1, ctl, 300 + h);
         if (!(ok = __all_sync(0xffffffffu, w))) break;
         ++s_cnt;
         tc_fence_after();
-        float s[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t u[32];
-          tmem_ld32(tS + 32 * c, u);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(u[i]);
-        }
+        uint32_t u[128];
+        tmem_ld128(tS, u);
         if (info & 1) {
+          // PARTIAL step: keep this row's visible window [lo, hi) of the tile.
           const Slice sl = P.slices[info >> 1];
           int lo = 0, hi = 0;
           if (row >= sl.qs && row < sl.qe) {
@@ -322,24 +329,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
 #pragma unroll
           for (int c = 0; c < 128; ++c)
-            if (c < lo || c >= hi) s[c] = -INFINITY;
+            if (c < lo || c >= hi) u[c] = 0xff800000u;  // -inf
         }
-        float mx = s[0];
+        // Row maximum: four independent chains of 3-input max.
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        for (int c = 0; c < 128; c += 8) {
+          mx0 = fmax3(mx0, __uint_as_float(u[c]), __uint_as_float(u[c + 1]));
+          mx1 = fmax3(mx1, __uint_as_float(u[c + 2]), __uint_as_float(u[c + 3]));
+          mx2 = fmax3(mx2, __uint_as_float(u[c + 4]), __uint_as_float(u[c + 5]));
+          mx3 = fmax3(mx3, __uint_as_float(u[c + 6]), __uint_as_float(u[c + 7]));
+        }
+        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
         const float m_cand = mx * P.scale_log2;
         const bool raise = m_cand > m + kRescaleThreshold;
         const bool rescale_o = raise && visited && m > -INFINITY;
         const float alpha = raise ? exp2f(m - m_cand) : 1.f;
         if (__any_sync(0xffffffffu, rescale_o)) {
           const float a = rescale_o ? alpha : 1.f;
-#pragma unroll
+#pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
-            uint32_t u[32];
-            tmem_ld32(tO + 32 * c, u);
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * a);
-            tmem_st32(tO + 32 * c, u);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+            tmem_st32(tO + 32 * c, o);
           }
           tmem_st_wait();
         }
@@ -348,68 +362,81 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           m = m_cand;
         }
         const float mu = m == -INFINITY ? 0.f : m;
-        float rs = 0.f;
-        uint32_t pk[64];
+        // p = 2^(s * scale * log2e - m) two lanes at a time; four partial row sums.
+        const float2 sc2 = make_float2(P.scale_log2, P.scale_log2);
+        const float2 nm2 = make_float2(-mu, -mu);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+        // P (bf16 pairs) goes over S columns [0, 64); every S value is in registers.
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float p0 = ex2_approx(fmaf(s[2 * c], P.scale_log2, -mu));
-          const float p1 = ex2_approx(fmaf(s[2 * c + 1], P.scale_log2, -mu));
-          rs += p0 + p1;
-          pk[c] = pack_bf16x2(p0, p1);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = 32 * q4 + 2 * i;
+            const float2 t = __ffma2_rn(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])),
+                                        sc2, nm2);
+            const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+            acc[i & 3] = __fadd2_rn(acc[i & 3], p);
+            pk[i] = pack_bf16x2(p.x, p.y);
+          }
+          tmem_st16(tS + 16 * q4, pk);
         }
-        l += rs;
-        tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+        l += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) +
+             (acc[3].x + acc[3].y);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(C::kBPFull + h));
         visited = true;
       }
       if (!ok) break;
-      // ---- epilogue
-      float o[D];
+      // ---- epilogue: O / l -> out (bf16) or a partial slot (fp32), 32 columns at a time
+      const bool nonempty = l > 0.f;
+      const float inv_l = nonempty ? 1.f / l : 0.f;
+      const bool store = slot >= 0 || row < P.Tq;
+      const size_t pbase = slot >= 0 ? ((size_t)slot * 2 + h) * 128 + row_in : 0;
+      uint4* dst_b = reinterpret_cast<uint4*>(P.out + ((size_t)row * P.Hq + head) * D);
+      float4* dst_f = slot >= 0 ? reinterpret_cast<float4*>(P.part_o + pbase * D) : nullptr;
       if (visited) {
         const bool w = mbar_wait(bar(C::kBOFull + h), o_cnt & 1, ctl, 310 + h);
         if (!(ok = __all_sync(0xffffffffu, w))) break;
         ++o_cnt;
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t u[32];
-          tmem_ld32(tO + 32 * c, u);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[32 * c + i] = __uint_as_float(u[i]);
-        }
-        tc_fence_before();
-        mbar_arrive(bar(C::kBOEmpty + h));
-      } else {
-#pragma unroll
-        for (int d = 0; d < D; ++d) o[d] = 0.f;
       }
-      const bool nonempty = l > 0.f;
-      const float inv_l = nonempty ? 1.f / l : 0.f;
-      if (slot < 0) {
-        if (row < P.Tq) {
-          uint4* dst = reinterpret_cast<uint4*>(P.out + ((size_t)row * P.Hq + head) * D);
-#pragma unroll
-          for (int v = 0; v < D / 8; ++v) {
-            uint4 w;
-            w.x = pack_bf16x2(o[8 * v + 0] * inv_l, o[8 * v + 1] * inv_l);
-            w.y = pack_bf16x2(o[8 * v + 2] * inv_l, o[8 * v + 3] * inv_l);
-            w.z = pack_bf16x2(o[8 * v + 4] * inv_l, o[8 * v + 5] * inv_l);
-            w.w = pack_bf16x2(o[8 * v + 6] * inv_l, o[8 * v + 7] * inv_l);
-            dst[v] = w;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        if (visited) {
+          tmem_ld32(tO + 32 * c, u);
+          if (c == D / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(bar(C::kBOEmpty + h));
           }
-          P.lse[(size_t)head * P.Tq + row] = nonempty ? (m + log2f(l)) * kLn2 : -INFINITY;
-        }
-      } else {
-        const size_t base = ((size_t)slot * 2 + h) * 128 + row_in;
-        float4* dst = reinterpret_cast<float4*>(P.part_o + base * D);
+        } else {
 #pragma unroll
-        for (int v = 0; v < D / 4; ++v)
-          dst[v] = make_float4(o[4 * v] * inv_l, o[4 * v + 1] * inv_l, o[4 * v + 2] * inv_l,
-                               o[4 * v + 3] * inv_l);
-        P.part_lse[base] = nonempty ? m + log2f(l) : -INFINITY;
+          for (int i = 0; i < 32; ++i) u[i] = 0u;
+        }
+        if (!store) continue;
+        if (slot < 0) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst_b[4 * c + v] = make_uint4(
+                pack_bf16x2(__uint_as_float(u[8 * v]) * inv_l, __uint_as_float(u[8 * v + 1]) * inv_l),
+                pack_bf16x2(__uint_as_float(u[8 * v + 2]) * inv_l, __uint_as_float(u[8 * v + 3]) * inv_l),
+                pack_bf16x2(__uint_as_float(u[8 * v + 4]) * inv_l, __uint_as_float(u[8 * v + 5]) * inv_l),
+                pack_bf16x2(__uint_as_float(u[8 * v + 6]) * inv_l, __uint_as_float(u[8 * v + 7]) * inv_l));
+        } else {
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst_f[8 * c + v] = make_float4(
+                __uint_as_float(u[4 * v]) * inv_l, __uint_as_float(u[4 * v + 1]) * inv_l,
+                __uint_as_float(u[4 * v + 2]) * inv_l, __uint_as_float(u[4 * v + 3]) * inv_l);
+        }
+      }
+      if (slot < 0) {
+        if (row < P.Tq) P.lse[(size_t)head * P.Tq + row] = nonempty ? (m + log2f(l)) * kLn2 : -INFINITY;
+      } else {
+        P.part_lse[pbase] = nonempty ? m + log2f(l) : -INFINITY;
       }
     }
   }
@@ -499,6 +526,7 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   if (cudaFuncSetAttribute(ffa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
     return FFA_ERR_CUDA;
+
   ffa_fwd_kernel<D><<<p->grid_fwd, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, P);
   note_launches(1);
   if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;

@@ -11,7 +11,7 @@
 //       - otherwise: q-tiles 2u and 2u+1 of one head; the steps merge the two
 //         visit lists on kt (equal kt -> one shared step, in list order).
 //   * Item cost = sum over its steps and busy halves of 4 (FULL) or 5
-//     (PARTIAL).  Items are sorted by (cost descending, index ascending) and
+//     (PARTIAL).  Items are sorted by (kv head, cost descending, index) and
 //     dealt to the persistent CTAs in a snake order.
 //   * While fewer than `split_below` items have work, each such item is cut
 //     into equal runs of steps whose partial results are merged by
@@ -103,52 +103,84 @@ __global__ void k_fwd_visit_count(const Slice* __restrict__ sl, int S, int n_qt,
   cnt[qt] = c;
 }
 
-// Emits (kt, info) for one tile in (kt, slice) order.  `Run` computes the
-// slice's tile run for this tile index.
-template <bool kFwd>
-__device__ void emit_visits(const Slice* __restrict__ sl, int S, int tile, int2* out) {
-  TileRun local[kMaxLocalSegs];
-  int local_s[kMaxLocalSegs];
-  int nseg = 0, lo = 0x7fffffff, hi = 0;
-  bool overflow = false;
-  for (int s = 0; s < S; ++s) {
-    TileRun r;
-    const bool ok = kFwd ? fwd_tile_run(sl[s], tile, r) : bwd_tile_run(sl[s], tile, r);
-    if (!ok) continue;
-    lo = min(lo, r.b);
-    hi = max(hi, r.e);
-    if (nseg < kMaxLocalSegs) {
-      local[nseg] = r;
-      local_s[nseg] = s;
-    } else {
-      overflow = true;
-    }
-    ++nseg;
-  }
-  int w = 0;
-  for (int x = lo; x < hi; ++x) {
-    if (!overflow) {
-      for (int i = 0; i < nseg; ++i) {
-        const TileRun& r = local[i];
-        if (x >= r.b && x < r.e)
-          out[w++] = make_int2(x, visit_info(local_s[i], !(x >= r.fb && x < r.fe)));
-      }
-    } else {
-      for (int s = 0; s < S; ++s) {
-        TileRun r;
-        const bool ok = kFwd ? fwd_tile_run(sl[s], tile, r) : bwd_tile_run(sl[s], tile, r);
-        if (ok && x >= r.b && x < r.e)
-          out[w++] = make_int2(x, visit_info(s, !(x >= r.fb && x < r.fe)));
-      }
-    }
-  }
-}
+// Emits the (tile index, info) visits of one tile in (index, slice) order,
+// one warp per tile: the lanes collect the
+// tile's slice runs (kept in shared memory, in slice order), then walk the
+// visited range 32 positions at a time; a warp scan of the per-position
+// counts gives every lane its output offset.
+constexpr int kFillWarps = 4;
 
-__global__ void k_fwd_visit_fill(const Slice* __restrict__ sl, int S, int n_qt,
-                                 const int* __restrict__ off, int2* visits) {
-  const int qt = blockIdx.x * blockDim.x + threadIdx.x;
-  if (qt >= n_qt) return;
-  emit_visits<true>(sl, S, qt, visits + off[qt]);
+template <bool kFwd>
+__global__ void __launch_bounds__(32 * kFillWarps)
+    k_visit_fill_warp(const Slice* __restrict__ sl, int S, int n_tiles,
+                      const int* __restrict__ off, int2* visits) {
+  __shared__ TileRun seg[kFillWarps][kMaxLocalSegs];
+  __shared__ int seg_s[kFillWarps][kMaxLocalSegs];
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x * kFillWarps + wib;
+  if (tile >= n_tiles) return;  // whole warp leaves together
+  int nseg = 0, lo = 0x7fffffff, hi = 0;
+  for (int s0 = 0; s0 < S; s0 += 32) {
+    const int s = s0 + lane;
+    TileRun r;
+    const bool ok = s < S && (kFwd ? fwd_tile_run(sl[s], tile, r) : bwd_tile_run(sl[s], tile, r));
+    const unsigned m = __ballot_sync(0xffffffffu, ok);
+    if (ok) {
+      const int pos = nseg + __popc(m & ((1u << lane) - 1u));
+      if (pos < kMaxLocalSegs) {
+        seg[wib][pos] = r;
+        seg_s[wib][pos] = s;
+      }
+      lo = min(lo, r.b);
+      hi = max(hi, r.e);
+    }
+    nseg += __popc(m);
+  }
+  for (int d = 16; d > 0; d >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, d));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, d));
+  }
+  __syncwarp();
+  const bool overflow = nseg > kMaxLocalSegs;
+  int base = off[tile];
+  for (int x0 = lo; x0 < hi; x0 += 32) {
+    const int x = x0 + lane;
+    int cnt = 0;
+    if (x < hi) {
+      if (!overflow) {
+        for (int i = 0; i < nseg; ++i) cnt += (x >= seg[wib][i].b && x < seg[wib][i].e) ? 1 : 0;
+      } else {
+        for (int s = 0; s < S; ++s) {
+          TileRun r;
+          const bool ok = kFwd ? fwd_tile_run(sl[s], tile, r) : bwd_tile_run(sl[s], tile, r);
+          cnt += (ok && x >= r.b && x < r.e) ? 1 : 0;
+        }
+      }
+    }
+    int incl = cnt;
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    if (cnt > 0) {
+      int w = base + incl - cnt;
+      if (!overflow) {
+        for (int i = 0; i < nseg; ++i) {
+          const TileRun r = seg[wib][i];
+          if (x >= r.b && x < r.e)
+            visits[w++] = make_int2(x, visit_info(seg_s[wib][i], !(x >= r.fb && x < r.fe)));
+        }
+      } else {
+        for (int s = 0; s < S; ++s) {
+          TileRun r;
+          const bool ok = kFwd ? fwd_tile_run(sl[s], tile, r) : bwd_tile_run(sl[s], tile, r);
+          if (ok && x >= r.b && x < r.e)
+            visits[w++] = make_int2(x, visit_info(s, !(x >= r.fb && x < r.fe)));
+        }
+      }
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
 }
 
 __device__ __forceinline__ int visit_cost(int info) {
@@ -317,12 +349,6 @@ __global__ void k_bwd_visit_count(const Slice* __restrict__ sl, int S, int n_kt,
   cnt[kt] = c;
 }
 
-__global__ void k_bwd_visit_fill(const Slice* __restrict__ sl, int S, int n_kt,
-                                 const int* __restrict__ off, int2* visits) {
-  const int kt = blockIdx.x * blockDim.x + threadIdx.x;
-  if (kt >= n_kt) return;
-  emit_visits<false>(sl, S, kt, visits + off[kt]);
-}
 
 __global__ void k_bwd_items(int n_kt, int Hkv, int g, const int2* __restrict__ visits,
                             const int* __restrict__ off, const int* __restrict__ cnt,
@@ -347,15 +373,20 @@ __global__ void k_bwd_items(int n_kt, int Hkv, int g, const int2* __restrict__ v
 }
 
 // ---- ordering ---------------------------------------------------------------
-// One block: bitonic sort of (cost desc, index asc) keys in `scratch`
-// (n2 = next power of two >= n entries), then order[r] = index.
-__global__ void k_sort_order(const int* __restrict__ items, int words, int cost_word, int n,
-                             int n2, unsigned long long* scratch, int* order) {
+// One block: bitonic sort of (kv head asc, cost desc, index asc) keys in
+// `scratch` (n2 = next power of two >= n entries), then order[r] = index.
+// Grouping by kv head keeps one head's K/V (and dQ accumulator) hot in L2.
+// Key bits: [50,64) kv head, [24,50) 2^26-1-cost, [0,24) index.
+__global__ void k_sort_order(const int* __restrict__ items, int words, int cost_word,
+                             int head_word, int head_div, int n, int n2,
+                             unsigned long long* scratch, int* order) {
   for (int i = threadIdx.x; i < n2; i += blockDim.x) {
     unsigned long long key = ~0ull;
     if (i < n) {
-      const unsigned int c = (unsigned int)items[(size_t)i * words + cost_word];
-      key = ((unsigned long long)(0x7fffffffu - c) << 32) | (unsigned int)i;
+      const int* it = items + (size_t)i * words;
+      const unsigned long long c = (unsigned int)it[cost_word];
+      const unsigned long long hk = (unsigned int)(it[head_word] / head_div);
+      key = (hk << 50) | ((0x3ffffffull - c) << 24) | (unsigned long long)i;
     }
     scratch[i] = key;
   }
@@ -376,21 +407,24 @@ __global__ void k_sort_order(const int* __restrict__ items, int words, int cost_
       __syncthreads();
     }
   }
-  for (int i = threadIdx.x; i < n; i += blockDim.x) order[i] = (int)(scratch[i] & 0xffffffffu);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) order[i] = (int)(scratch[i] & 0xffffffu);
 }
 
 // ---- host helpers -----------------------------------------------------------
+// Stream-ordered scratch memory for the planner (freed on the same stream).
 struct DevBuf {
   void* p = nullptr;
+  cudaStream_t st = nullptr;
+  explicit DevBuf(cudaStream_t s = nullptr) : st(s) {}
   ~DevBuf() {
-    if (p) cudaFree(p);
+    if (p) cudaFreeAsync(p, st);
   }
   template <class T>
   T* as() {
     return static_cast<T*>(p);
   }
   cudaError_t alloc(size_t bytes) {
-    return cudaMalloc(&p, bytes > 0 ? bytes : 16);
+    return cudaMallocAsync(&p, bytes > 0 ? bytes : 16, st);
   }
   void* release() {
     void* q = p;
@@ -421,14 +455,15 @@ ffa_status_t scan(const int* in, int n, int* out, long long* dtot, long long* ht
   return FFA_OK;
 }
 
-ffa_status_t sort_items(const int* items, int words, int cost_word, int n, int* order,
-                        cudaStream_t st) {
+ffa_status_t sort_items(const int* items, int words, int cost_word, int head_word, int head_div,
+                        int n, int* order, cudaStream_t st) {
   if (n <= 0) return FFA_OK;
+  if (n >= (1 << 24)) return FFA_ERR_UNSUPPORTED;
   int n2 = 1;
   while (n2 < n) n2 <<= 1;
-  DevBuf scratch;
+  DevBuf scratch(st);
   FFA_CUDA(scratch.alloc(sizeof(unsigned long long) * (size_t)n2));
-  k_sort_order<<<1, 1024, 0, st>>>(items, words, cost_word, n, n2,
+  k_sort_order<<<1, 1024, 0, st>>>(items, words, cost_word, head_word, head_div, n, n2,
                                    scratch.as<unsigned long long>(), order);
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
@@ -451,7 +486,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   FFA_CUDA(cudaMalloc(&p->slices, sizeof(Slice) * (size_t)std::max(S, 1)));
   FFA_CUDA(cudaMalloc(&p->err, 2 * sizeof(int)));
   FFA_CUDA(cudaMemsetAsync(p->err, 0, 2 * sizeof(int), st));
-  DevBuf flags_area;
+  DevBuf flags_area(st);
   FFA_CUDA(flags_area.alloc(64));
   int* flags = flags_area.as<int>();
   unsigned long long* area = reinterpret_cast<unsigned long long*>(flags + 4);
@@ -478,7 +513,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   const int n_qt = p->n_qt, n_kt = p->n_kt, g = p->Hq / p->Hkv;
   long long tot = 0;
   // forward visits
-  DevBuf vcnt, voff, visits;
+  DevBuf vcnt(st), voff(st), visits(st);
   FFA_CUDA(vcnt.alloc(sizeof(int) * n_qt));
   FFA_CUDA(voff.alloc(sizeof(int) * n_qt));
   k_fwd_visit_count<<<grid_for(n_qt, 128), 128, 0, st>>>(p->slices, S, n_qt, vcnt.as<int>());
@@ -488,14 +523,14 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   if (rc != FFA_OK) return rc;
   if (tot > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
   FFA_CUDA(visits.alloc(sizeof(int2) * (size_t)tot));
-  k_fwd_visit_fill<<<grid_for(n_qt, 64), 64, 0, st>>>(p->slices, S, n_qt, voff.as<int>(),
-                                                      visits.as<int2>());
+  k_visit_fill_warp<true><<<grid_for(n_qt, kFillWarps), 32 * kFillWarps, 0, st>>>(
+      p->slices, S, n_qt, voff.as<int>(), visits.as<int2>());
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
   // forward units -> steps
   const int pair_mode = g >= 2 ? 0 : 1;
   const int n_units = pair_mode == 0 ? n_qt : (n_qt + 1) / 2;
-  DevBuf scnt, soff, cost_half, steps;
+  DevBuf scnt(st), soff(st), cost_half(st), steps(st);
   FFA_CUDA(scnt.alloc(sizeof(int) * n_units));
   FFA_CUDA(soff.alloc(sizeof(int) * n_units));
   FFA_CUDA(cost_half.alloc(sizeof(int) * 2 * n_units));
@@ -520,7 +555,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   const long long n_items = pair_mode == 0 ? (long long)n_units * p->Hkv * pairs
                                            : (long long)n_units * p->Hq;
   if (n_items > 0x7fffffffLL / kFiWords) return FFA_ERR_UNSUPPORTED;
-  DevBuf items, live;
+  DevBuf items(st), live(st);
   FFA_CUDA(items.alloc(sizeof(int) * kFiWords * (size_t)n_items));
   FFA_CUDA(live.alloc(sizeof(int)));
   FFA_CUDA(cudaMemsetAsync(live.p, 0, sizeof(int), st));
@@ -537,7 +572,8 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   long long final_items = n_items;
   if (split_below >= 0 && hlive > 0 && hlive < threshold) {
     const int nsplit = std::min(16, (threshold + hlive - 1) / hlive);
-    DevBuf chunks, coff, slots, sloff, groups, goff, nitems, merges;
+    DevBuf chunks(st), coff(st), slots(st), sloff(st), groups(st), goff(st), nitems(st),
+        merges(st);
     const size_t nb = sizeof(int) * (size_t)n_items;
     FFA_CUDA(chunks.alloc(nb));
     FFA_CUDA(coff.alloc(nb));
@@ -570,7 +606,8 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   }
   p->n_fwd_items = final_items;
   FFA_CUDA(cudaMalloc(&p->fwd_order, sizeof(int) * (size_t)std::max(1LL, final_items)));
-  rc = sort_items(items.as<int>(), kFiWords, kFiCost, (int)final_items, p->fwd_order, st);
+  rc = sort_items(items.as<int>(), kFiWords, kFiCost, kFiH0, g, (int)final_items, p->fwd_order,
+                  st);
   if (rc != FFA_OK) return rc;
   p->fwd_items = items.as<int>();
   items.release();
@@ -578,7 +615,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   steps.release();
 
   // backward
-  DevBuf bcnt, boff, bvis;
+  DevBuf bcnt(st), boff(st), bvis(st);
   FFA_CUDA(bcnt.alloc(sizeof(int) * n_kt));
   FFA_CUDA(boff.alloc(sizeof(int) * n_kt));
   k_bwd_visit_count<<<grid_for(n_kt, 128), 128, 0, st>>>(p->slices, S, n_kt, bcnt.as<int>());
@@ -589,8 +626,8 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   p->n_bwd_steps = tot;
   FFA_CUDA(bvis.alloc(sizeof(int2) * (size_t)tot));
   FFA_CUDA(cudaMalloc(&p->bwd_steps, sizeof(int4) * (size_t)std::max(1LL, tot)));
-  k_bwd_visit_fill<<<grid_for(n_kt, 64), 64, 0, st>>>(p->slices, S, n_kt, boff.as<int>(),
-                                                      bvis.as<int2>());
+  k_visit_fill_warp<false><<<grid_for(n_kt, kFillWarps), 32 * kFillWarps, 0, st>>>(
+      p->slices, S, n_kt, boff.as<int>(), bvis.as<int2>());
   note_launches(1);
   const long long nb_items = (long long)n_kt * p->Hkv;
   p->n_bwd_items = nb_items;
@@ -601,7 +638,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
                                                        p->bwd_steps, p->bwd_items);
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
-  rc = sort_items(p->bwd_items, kBiWords, kBiCost, (int)nb_items, p->bwd_order, st);
+  rc = sort_items(p->bwd_items, kBiWords, kBiCost, kBiHkv, 1, (int)nb_items, p->bwd_order, st);
   if (rc != FFA_OK) return rc;
   p->grid_fwd = (int)std::max(1LL, std::min<long long>(p->num_sms, final_items));
   p->grid_bwd = (int)std::max(1LL, std::min<long long>(p->num_sms, nb_items));
