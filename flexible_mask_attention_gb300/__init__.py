@@ -19,7 +19,7 @@ __all__ = [
     "library_path", "load_library", "ffa_plan_create", "ffa_plan_destroy", "ffa_plan_info",
     "ffa_plan_export", "ffa_fwd_workspace_size", "ffa_bwd_workspace_size", "ffa_fwd", "ffa_bwd",
     "ffa_get_last_device_error", "ffa_plan_set_wait_limit", "ffa_kernel_launch_count",
-    "EXPORTED_SYMBOLS",
+    "ffa_bwd_noalloc", "EXPORTED_SYMBOLS",
 ]
 
 FFA_FULL, FFA_CAUSAL, FFA_INV_CAUSAL, FFA_BI_CAUSAL = 0, 1, 2, 3
@@ -33,7 +33,7 @@ EXPORTED_SYMBOLS = [
     "ffa_plan_create", "ffa_plan_destroy", "ffa_plan_info", "ffa_plan_export",
     "ffa_fwd_workspace_size", "ffa_bwd_workspace_size", "ffa_fwd", "ffa_bwd",
     "ffa_get_last_device_error", "ffa_plan_set_wait_limit", "ffa_status_string",
-    "ffa_kernel_launch_count",
+    "ffa_kernel_launch_count", "ffa_bwd_noalloc", "ffa_bwd_noalloc_max_workspace",
 ]
 
 
@@ -86,9 +86,12 @@ def load_library():
     lib.ffa_status_string.restype = ctypes.c_char_p
     lib.ffa_kernel_launch_count.argtypes = []
     lib.ffa_kernel_launch_count.restype = U64
+    lib.ffa_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, F, P, P, P, P]
+    lib.ffa_bwd_noalloc_max_workspace.argtypes = []
+    lib.ffa_bwd_noalloc_max_workspace.restype = S
     for name in EXPORTED_SYMBOLS:
         if name not in ("ffa_fwd_workspace_size", "ffa_bwd_workspace_size", "ffa_status_string",
-                        "ffa_kernel_launch_count"):
+                        "ffa_kernel_launch_count", "ffa_bwd_noalloc_max_workspace"):
             getattr(lib, name).restype = I32
     _lib = lib
     return lib
@@ -254,6 +257,24 @@ def ffa_bwd(plan: Plan, q, k, v, out, dout, lse, dq=None, dk=None, dv=None, soft
     _check("ffa_bwd", load_library().ffa_bwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out),
                                              _ptr(dout), _ptr(lse), scale, _ptr(dq), _ptr(dk),
                                              _ptr(dv), _ptr(ws), nbytes, _stream(stream)))
+    return dq, dk, dv
+
+
+def ffa_bwd_noalloc(plan: Plan, q, k, v, out, dout, lse, dq, dk, dv, softmax_scale=None,
+                    stream=None):
+    """ffa_bwd with the library's fixed scratch array: passes no workspace and
+    makes the library allocate nothing (outputs must be given)."""
+    Tq, Tk, Hq, Hkv, D = (plan.total_q, plan.total_k, plan.num_heads_q, plan.num_heads_kv,
+                          plan.head_dim)
+    for t, n, s in ((q, "q", (Tq, Hq, D)), (k, "k", (Tk, Hkv, D)), (v, "v", (Tk, Hkv, D)),
+                    (out, "out", (Tq, Hq, D)), (dout, "dout", (Tq, Hq, D)),
+                    (dq, "dq", (Tq, Hq, D)), (dk, "dk", (Tk, Hkv, D)), (dv, "dv", (Tk, Hkv, D))):
+        _need(t, n, torch.bfloat16, s)
+    _need(lse, "lse", torch.float32, (Hq, Tq))
+    scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    _check("ffa_bwd_noalloc", load_library().ffa_bwd_noalloc(
+        plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), scale,
+        _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
     return dq, dk, dv
 
 

@@ -29,6 +29,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "ffa_internal.cuh"
 #include "ffa_ptx.cuh"
 
@@ -621,3 +623,68 @@ ffa_status_t launch_bwd(ffa_plan_s* p, const void* q, const void* k, const void*
 }
 
 }  // namespace ffa
+
+// ---------------------------------------------------------------------------
+// Allocation-free backward.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// backward: code running while a stream is being captured into a graph,
+// runtimes that forbid allocation after start-up, or hosts whose memory
+// manager owns every allocation.  ffa_bwd_noalloc serves them: its scratch
+// (log2-scaled lse, delta and the fp32 dQ accumulator) lives in the array
+// below, which every GPU that loads this library holds until the process
+// exits.  All calls share it, so calls whose kernels overlap on the GPU race.
+namespace ffa {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 64ull << 20;  // 64 MiB
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array for the current device.  Host code
+// cannot use the array's name as a device address; the runtime resolves it
+// once per device (with that device current).
+ffa_status_t noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FFA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FFA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return FFA_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return FFA_OK;
+}
+
+bool aligned16_b(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace ffa
+
+extern "C" size_t ffa_bwd_noalloc_max_workspace(void) { return ffa::kNoAllocScratchBytes; }
+
+extern "C" ffa_status_t ffa_bwd_noalloc(ffa_plan_t p, const void* q, const void* k, const void* v,
+                                        const void* out, const void* dout, const float* lse,
+                                        float softmax_scale, void* dq, void* dk, void* dv,
+                                        ffa_stream_t stream) {
+  using namespace ffa;
+  if (!p || !q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv)
+    return FFA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, out, dout, lse, dq, dk, dv};
+  for (const void* x : ptrs)
+    if (!aligned16_b(x)) return FFA_ERR_INVALID_ARG;
+  const size_t need = bwd_workspace_bytes(p);
+  if (need > kNoAllocScratchBytes) return FFA_ERR_WORKSPACE;
+  void* ws = nullptr;
+  const ffa_status_t rc = noalloc_scratch(&ws);
+  if (rc != FFA_OK) return rc;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)p->D);
+  return launch_bwd(p, q, k, v, out, dout, lse, scale, dq, dk, dv, ws, need,
+                    reinterpret_cast<cudaStream_t>(stream));
+}

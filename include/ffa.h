@@ -132,6 +132,28 @@ ffa_status_t ffa_bwd(ffa_plan_t plan, const void* q, const void* k, const void* 
                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                      ffa_stream_t stream);
 
+/* Backward without any allocation: the same computation as ffa_bwd, with its
+ * scratch memory taken from a fixed array inside the library instead of a
+ * caller workspace.  (No counterpart in the MagiAttention pages.)  For callers
+ * that cannot allocate device memory when they run the backward: code running
+ * during stream capture into a CUDA graph, runtimes that forbid allocation
+ * after start-up, or hosts whose memory manager owns every allocation.
+ *   - The array holds ffa_bwd_noalloc_max_workspace() bytes (64 MiB) on every
+ *     GPU that loads this library, until the process exits.  A plan whose
+ *     ffa_bwd_workspace_size exceeds it gets FFA_ERR_WORKSPACE.
+ *   - The first call on a device resolves the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the array and re-initialises what must start at zero;
+ *     calls whose kernels overlap on the GPU (other streams) race.
+ *   - Arguments as for ffa_bwd; nothing is allocated or freed. */
+ffa_status_t ffa_bwd_noalloc(ffa_plan_t plan, const void* q, const void* k, const void* v,
+                             const void* out, const void* dout, const float* lse,
+                             float softmax_scale, void* dq, void* dk, void* dv,
+                             ffa_stream_t stream);
+
+/* Size in bytes of the fixed scratch array ffa_bwd_noalloc uses. */
+size_t ffa_bwd_noalloc_max_workspace(void);
+
 /* Read and clear the device error word the plan's kernels write:
  *   *code = 0 none, 1 bounded wait timed out, 2 shared memory misaligned,
  *   3 bad work item; *where = the location tag of the first failure.
