@@ -261,6 +261,7 @@ def run_ffa(args, wl, world, rank, local):
             record[0].record(stream)
         plan = ffa.ffa_plan_create(qr_d, kr_d, ty_d, Tq, Tk, Hq, Hkv, D)
         if record is not None:
+            ffa.ffa_plan_set_events(plan, record[4:10])
             record[1].record(stream)
         ffa.ffa_fwd(plan, qa, ka, va, out=out, lse=lse, workspace=ws_f)
         if record is not None:
@@ -292,7 +293,7 @@ def run_ffa(args, wl, world, rank, local):
     start.record(stream)
     plans = []
     for _ in range(args.steps):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
         plans.append((step(qd, kd, vd, dod, evs), evs))
     end.record(stream)
     torch.cuda.synchronize()
@@ -300,10 +301,16 @@ def run_ffa(args, wl, world, rank, local):
     barrier(world)
     launches = ffa.ffa_kernel_launch_count() - launches0
     elapsed_ms = start.elapsed_time(end)
+    t_kern = {"ffa_fwd_kernel": [], "ffa_bwd_pre_kernel": [], "ffa_bwd_dkdv_kernel": [],
+              "ffa_bwd_dq_kernel": []}
     for pl, evs in plans:
         t_plan.append(evs[0].elapsed_time(evs[1]))
         t_fwd.append(evs[1].elapsed_time(evs[2]))
         t_bwd.append(evs[2].elapsed_time(evs[3]))
+        t_kern["ffa_fwd_kernel"].append(evs[4].elapsed_time(evs[5]))
+        t_kern["ffa_bwd_pre_kernel"].append(evs[6].elapsed_time(evs[7]))
+        t_kern["ffa_bwd_dkdv_kernel"].append(evs[7].elapsed_time(evs[8]))
+        t_kern["ffa_bwd_dq_kernel"].append(evs[8].elapsed_time(evs[9]))
         pl.destroy()
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
 
@@ -314,7 +321,7 @@ def run_ffa(args, wl, world, rank, local):
                       f_fwd + f_bwd)
     peaks, peak_src = load_peaks()
     return finish(args, wl, world, rank, elapsed_ms, t_plan, t_fwd, t_bwd, f_fwd, f_bwd, area,
-                  launches, clocks, e2e, peaks, peak_src, q, k, v, do)
+                  launches, clocks, e2e, peaks, peak_src, q, k, v, do, t_kern)
 
 
 def run_e2e(args, world, dev, stream, step, host, out, lse, dq, dk, dv, qr, flops):
@@ -346,22 +353,31 @@ def run_e2e(args, world, dev, stream, step, host, out, lse, dq, dk, dv, qr, flop
             "d2h_bytes_per_step": d2h}
 
 
+# FLOP credited to each tensor-core kernel per visible (q, k, head), in units
+# of D: the forward's two products; of the backward's five (S, dP, dV, dK, dQ)
+# the dK/dV pass computes four and the dQ pass one (it also recomputes S and
+# dP, which is not credited).
+KERNEL_CREDIT = {"ffa_fwd_kernel": 4.0, "ffa_bwd_dkdv_kernel": 8.0, "ffa_bwd_dq_kernel": 2.0}
+
+
 def finish(args, wl, world, rank, elapsed_ms, t_plan, t_fwd, t_bwd, f_fwd, f_bwd, area,
-           launches, clocks, e2e, peaks, peak_src, q, k, v, do):
+           launches, clocks, e2e, peaks, peak_src, q, k, v, do, t_kern):
     Tq, Hq, Hkv, D = wl.total_q, wl.num_heads_q, wl.num_heads_kv, wl.head_dim
     ms_step = elapsed_ms / args.steps
     value = world * args.steps * (f_fwd + f_bwd) / (elapsed_ms / 1e3) / 1e12
     fwd_ms, bwd_ms, plan_ms = (statistics.mean(x) for x in (t_fwd, t_bwd, t_plan))
-    dom = "bwd" if bwd_ms >= fwd_ms else "fwd"
-    dom_ms = bwd_ms if dom == "bwd" else fwd_ms
-    dom_flops = f_bwd if dom == "bwd" else f_fwd
-    achieved = dom_flops / (dom_ms / 1e3) / 1e12
+    kern_ms = {k: statistics.mean(v) for k, v in t_kern.items()}
+    dom = max(KERNEL_CREDIT, key=lambda k: kern_ms[k])
+    dom_flops = KERNEL_CREDIT[dom] * D * area * Hq
+    achieved = dom_flops / (kern_ms[dom] / 1e3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
+    traffic = traffic_from_profile(dom)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak,
-                "traffic": traffic_from_profile("ffa_bwd_kernel" if dom == "bwd" else "ffa_fwd_kernel"),
-                "kernel": "backward (preprocess + main + dq convert)" if dom == "bwd" else "forward",
-                "peak_source": f"{peak_src} bf16_tflops_sustained",
+                "frac": achieved / peak, "traffic": traffic, "kernel": dom,
+                "kernel_ms": kern_ms[dom],
+                "credited_flop_per_visible_pair_head": f"{KERNEL_CREDIT[dom]:.0f}*D",
+                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a "
+                               f"multi-second step loop)",
                 "frac_of_burst_peak": achieved / peaks["bf16_tflops"]}
     if rank != 0:
         return
@@ -376,6 +392,7 @@ def finish(args, wl, world, rank, elapsed_ms, t_plan, t_fwd, t_bwd, f_fwd, f_bwd
                    "l2": f"inputs larger than L2: q and dout {Tq * Hq * D * 2 / 1e6:.0f} MB each, "
                          f"k and v {wl.total_k * Hkv * D * 2 / 1e6:.0f} MB each, no flush"},
         "phases_ms": {"plan": plan_ms, "fwd": fwd_ms, "bwd": bwd_ms},
+        "kernels_ms": kern_ms,
         "fwd_tflops": f_fwd / (fwd_ms / 1e3) / 1e12,
         "bwd_tflops": f_bwd / (bwd_ms / 1e3) / 1e12,
         "fwd_frac_of_peak": f_fwd / (fwd_ms / 1e3) / 1e12 / peak,

@@ -19,7 +19,7 @@ __all__ = [
     "library_path", "load_library", "ffa_plan_create", "ffa_plan_destroy", "ffa_plan_info",
     "ffa_plan_export", "ffa_fwd_workspace_size", "ffa_bwd_workspace_size", "ffa_fwd", "ffa_bwd",
     "ffa_get_last_device_error", "ffa_plan_set_wait_limit", "ffa_kernel_launch_count",
-    "ffa_bwd_noalloc", "EXPORTED_SYMBOLS",
+    "ffa_bwd_noalloc", "ffa_plan_set_events", "EXPORTED_SYMBOLS",
 ]
 
 FFA_FULL, FFA_CAUSAL, FFA_INV_CAUSAL, FFA_BI_CAUSAL = 0, 1, 2, 3
@@ -34,6 +34,7 @@ EXPORTED_SYMBOLS = [
     "ffa_fwd_workspace_size", "ffa_bwd_workspace_size", "ffa_fwd", "ffa_bwd",
     "ffa_get_last_device_error", "ffa_plan_set_wait_limit", "ffa_status_string",
     "ffa_kernel_launch_count", "ffa_bwd_noalloc", "ffa_bwd_noalloc_max_workspace",
+    "ffa_plan_set_events",
 ]
 
 
@@ -82,6 +83,7 @@ def load_library():
     lib.ffa_bwd.argtypes = [P, P, P, P, P, P, P, F, P, P, P, P, S, P]
     lib.ffa_get_last_device_error.argtypes = [P, ctypes.POINTER(I32), ctypes.POINTER(I32), P]
     lib.ffa_plan_set_wait_limit.argtypes = [P, U64]
+    lib.ffa_plan_set_events.argtypes = [P, ctypes.POINTER(P), I32]
     lib.ffa_status_string.argtypes = [I32]
     lib.ffa_status_string.restype = ctypes.c_char_p
     lib.ffa_kernel_launch_count.argtypes = []
@@ -284,6 +286,23 @@ def ffa_get_last_device_error(plan: Plan, stream=None):
     _check("ffa_get_last_device_error", load_library().ffa_get_last_device_error(
         plan.handle, ctypes.byref(code), ctypes.byref(where), _stream(stream)))
     return code.value, where.value
+
+
+def ffa_plan_set_events(plan: Plan, events):
+    """Phase events (six torch.cuda.Event with timing) recorded by the library
+    around its forward and backward kernels; None stops recording."""
+    if events is None:
+        _check("ffa_plan_set_events", load_library().ffa_plan_set_events(plan.handle, None, 0))
+        plan._events = None
+        return
+    if len(events) != 6:
+        raise ValueError("six events are required")
+    for e in events:
+        if not e.cuda_event:  # torch creates the event on its first record
+            e.record()
+    arr = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    plan._events = (events, arr)  # keep the handles alive with the plan
+    _check("ffa_plan_set_events", load_library().ffa_plan_set_events(plan.handle, arr, 6))
 
 
 def ffa_plan_set_wait_limit(plan: Plan, nanoseconds: int):

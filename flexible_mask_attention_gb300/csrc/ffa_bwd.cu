@@ -1,31 +1,28 @@
-// Backward kernels of flexible-mask attention for sm_103a.
+// Backward kernels of flexible-mask attention for sm_103a, in two passes
+// without atomics:
 //
-//   1. preprocess: -delta[h][q] = -<dO, O> (fp32), -lse * log2(e), and
-//      dQaccum = 0 (stored negated so the main kernel adds them with FMAs);
-//   2. main: one work item per (k-tile, kv head).  The 128 x D tiles of K and
-//      V stay in shared memory; the item loops over every (q-tile, query head
-//      of the group) that sees the k-tile:
-//          S^T  = K Q^T           (tcgen05, SS)      -> TMEM
-//          dP^T = V dO^T          (tcgen05, SS)      -> TMEM
+//   1. preprocess: -lse * log2(e) and -delta = -<dO, O> per (head, row), fp32,
+//      stored negated so the kernels add them with FMAs;
+//   2. dK/dV pass, one work item per (k-tile, kv head).  K and V stay in
+//      shared memory; the item loops over every (q-tile, query head of the
+//      group) that sees the k-tile:
+//          S^T  = K Q^T                (tcgen05, SS)  -> TMEM
+//          dP^T = V dO^T               (tcgen05, SS)  -> TMEM
 //          P^T  = 2^(S^T*scale*log2e - lse2), masked on PARTIAL steps
 //          dS^T = P^T * (dP^T - delta)
-//          dV  += P^T dO          (tcgen05, A = P^T from TMEM)
-//          dK  += dS^T Q          (tcgen05, A = dS^T from TMEM)
-//          dQ^T = K^T dS^T        (tcgen05, both operands from shared memory;
-//                                  dQ = dS K when D = 64)
-//      dK and dV accumulate in TMEM and are written once per item (no
-//      atomics); each dQ tile is added into the fp32 dQaccum.
-//   3. convert: dq = bf16(dQaccum).
+//          dV  += P^T dO               (tcgen05, A = P^T from shared memory)
+//          dK  += dS^T Q               (tcgen05, A = dS^T from TMEM)
+//      dK, dV accumulate in TMEM and are written once per item;
+//   3. dQ pass, one work unit per (q-tile, query head), over the k-tiles the
+//      q-tile sees (the forward's visits):
+//          S  = Q K^T, dP = dO V^T     (tcgen05, SS)  -> TMEM
+//          dS = 2^(S*scale*log2e - lse2) * (dP - delta), masked
+//          dQ += dS K                  (tcgen05, A = dS from TMEM)
+//      dQ accumulates in TMEM and is written once (bf16) per unit.
 // This is the standard softmax-attention gradient; the mask only decides
-// which entries of P are zero.
-//
-// Warp roles of the main kernel (320 threads):
-//   warps 0-3  P/dS warps (thread = key = TMEM lane), dK/dV epilogue
-//   warps 4-7  dQ warps (thread = query row = TMEM lane): TMEM -> fp32 atomics
-//   warp  8    TMA producer (K, V per item; Q, dO two-stage rings)
-//   warp  9    MMA issuer, TMEM owner
-// TMEM columns: dV [0,D), dK [D,2D), S^T [2D,2D+128), dP^T [2D+128,2D+256);
-// the dQ tile reuses the S^T columns once P^T has been consumed.
+// which entries of P are zero.  Recomputing S and dP in the dQ pass costs two
+// extra MMAs per tile pair but removes the fp32 dQ reductions, which on this
+// part cost more than the recomputation, and makes dQ deterministic.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -37,59 +34,7 @@
 namespace ffa {
 namespace {
 
-constexpr int kBwdThreads = 320;
 constexpr float kLog2e = 1.4426950408889634f;
-
-template <int D>
-struct BwdCfg {
-  static constexpr int kChunks = D / 64;
-  static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kStages = 2;
-  static constexpr int kKOff = 0;
-  static constexpr int kVOff = kTileBytes;
-  static constexpr int kQOff = 2 * kTileBytes;
-  static constexpr int kDOOff = kQOff + kStages * kTileBytes;
-  static constexpr int kDSOff = kDOOff + kStages * kTileBytes;  // 128 x 128 bf16
-  static constexpr int kLseOff = kDSOff + 128 * 128 * 2;         // per stage: -lse2[128], -delta[128]
-  static constexpr int kLseStageBytes = 2 * 128 * 4;
-  static constexpr int kBarOff = kLseOff + kStages * kLseStageBytes;
-  static constexpr int kBKVFull = 0, kBKVEmpty = 1, kBQFull = 2, kBQEmpty = 2 + kStages,
-                       kBDOFull = 2 + 2 * kStages, kBDOEmpty = 2 + 3 * kStages,
-                       kBSdpFull = 2 + 4 * kStages, kBPFull = kBSdpFull + 1,
-                       kBDqFull = kBPFull + 1, kBDqFree = kBDqFull + 1, kBDkvFull = kBDqFree + 1,
-                       kBDkvEmpty = kBDkvFull + 1, kBDrain = kBDkvEmpty + 1,
-                       kNumBars = kBDrain + 1;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  // The dynamic shared memory base must be 1024-byte aligned (checked on entry).
-  static constexpr int kSmemBytes = kMiscOff + 64;
-  // TMEM columns
-  static constexpr int kTdV = 0, kTdK = D, kTS = 2 * D, kTdP = 2 * D + 128;
-};
-
-struct BwdParams {
-  const int4* steps;
-  const int* items;
-  const int* order;
-  int n_items;
-  const Slice* slices;
-  int Tq, Tk, Hq, g, qpad;
-  float scale, scale_log2;
-  const float* nlse2;   // [Hq][qpad] -lse * log2(e)
-  const float* ndelta;  // [Hq][qpad] -rowsum(dO * O)
-  float* dq_acc;       // [Tq][Hq][D]
-  __nv_bfloat16* dk;
-  __nv_bfloat16* dv;
-  int* err;
-  uint64_t wait_ns;
-};
-
-__device__ __forceinline__ bool bwd_item_at(const BwdParams& P, int r, const int*& it) {
-  const int G = gridDim.x, b = blockIdx.x;
-  const int pos = r * G + ((r & 1) ? (G - 1 - b) : b);
-  if (pos >= P.n_items) return false;
-  it = P.items + (size_t)P.order[pos] * kBiWords;
-  return true;
-}
 
 __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity, uint64_t ns) {
   const uint64_t t0 = globaltimer_ns();
@@ -98,7 +43,62 @@ __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity, uint
   }
 }
 
-// Query rows of this step visible to key `key` under a PARTIAL step's slice,
+// ============================================================================
+// dK / dV pass
+// Warp roles (192 threads): warps 0-3 P/dS (thread = key = TMEM lane) and
+// the dK/dV epilogue, warp 4 TMA producer, warp 5 MMA issuer (TMEM owner).
+// TMEM columns: dV [0,D), dK [D,2D), S^T [2D,2D+128), dP^T [2D+128,2D+256).
+template <int D>
+struct KvCfg {
+  static constexpr int kThreads = 192;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kStages = 2;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kTileBytes;
+  static constexpr int kQOff = 2 * kTileBytes;
+  static constexpr int kDOOff = kQOff + kStages * kTileBytes;
+  static constexpr int kPOff = kDOOff + kStages * kTileBytes;  // P^T, 128 keys x 128 queries bf16
+  static constexpr int kLseOff = kPOff + 128 * 128 * 2;        // per stage: -lse2[128], -delta[128]
+  static constexpr int kLseStageBytes = 2 * 128 * 4;
+  static constexpr int kBarOff = kLseOff + kStages * kLseStageBytes;
+  static constexpr int kBKVFull = 0, kBKVEmpty = 1, kBQFull = 2, kBQEmpty = 2 + kStages,
+                       kBDOFull = 2 + 2 * kStages, kBDOEmpty = 2 + 3 * kStages,
+                       kBSdpFull = 2 + 4 * kStages, kBSFree = kBSdpFull + 1,
+                       kBPFull = kBSFree + 1, kBDkvFull = kBPFull + 1,
+                       kBDkvEmpty = kBDkvFull + 1, kBDrain = kBDkvEmpty + 1,
+                       kNumBars = kBDrain + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  // The dynamic shared memory base must be 1024-byte aligned (checked on entry).
+  static constexpr int kSmemBytes = kMiscOff + 64;
+  static constexpr int kTdV = 0, kTdK = D, kTS = 2 * D, kTdP = 2 * D + 128;
+};
+
+struct KvParams {
+  const int4* steps;
+  const int* items;
+  const int* order;
+  int n_items;
+  const Slice* slices;
+  int Tk, Hkv, g, qpad;
+  float scale, scale_log2;
+  const float* nlse2;   // [Hq][qpad] -lse * log2(e)
+  const float* ndelta;  // [Hq][qpad] -rowsum(dO * O)
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int* err;
+  uint64_t wait_ns;
+};
+
+__device__ __forceinline__ bool kv_item_at(const KvParams& P, int r, const int*& it) {
+  const int G = gridDim.x, b = blockIdx.x;
+  const int pos = r * G + ((r & 1) ? (G - 1 - b) : b);
+  if (pos >= P.n_items) return false;
+  it = P.items + (size_t)P.order[pos] * kBiWords;
+  return true;
+}
+
+// Query rows of the step visible to key `key` under a PARTIAL step's slice,
 // in local coordinates [lo, hi) of the q-tile.
 __device__ __forceinline__ void key_query_window(const Slice& sl, int key, int qt, int& lo,
                                                  int& hi) {
@@ -112,19 +112,20 @@ __device__ __forceinline__ void key_query_window(const Slice& sl, int key, int q
   hi = b - qt * 128;
 }
 
-// P^T and dS^T for one key row j over the 128 queries of the step:
-//   p = 2^(s * scale * log2e - lse2), ds = p * (dp - delta)
-// written as bf16 pairs to TMEM (over the first 64 columns of S^T and dP^T)
-// and dS to the 128-byte swizzled shared-memory tile (row j, query chunks).
+// P^T and dS^T for key row j over the 128 queries of the step, from the S^T
+// row already in registers (s) and the dP^T row read from TMEM here:
+//   p = 2^(s * scale * log2e - lse2), ds = p * (dp - delta).
+// dS^T goes to TMEM as bf16 pairs over dP^T columns [0, 64); P^T goes to the
+// 128-byte swizzled shared-memory tile (row j, K-major for the dV MMA).
 template <bool kPartial>
-__device__ __forceinline__ void pds_tile(uint32_t tS, uint32_t tP, const float* nl,
-                                         const float* nd, float scale_log2, int lo, int hi, int j,
-                                         uint8_t* ds_row) {
+__device__ __forceinline__ void pds_row(const uint32_t (&s)[128], uint32_t tP, const float* nl,
+                                        const float* nd, float scale_log2, int lo, int hi, int j,
+                                        uint8_t* p_row) {
   const float2 sc2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    uint32_t r[64];  // r[0..32): S^T, r[32..64): dP^T
-    tmem_ld32x2(tS + 32 * c, tP + 32 * c, r);
+    uint32_t dp[32];
+    tmem_ld32(tP + 32 * c, dp);
     uint32_t pp[16], dd[16];
 #pragma unroll
     for (int e = 0; e < 32; e += 4) {
@@ -136,43 +137,42 @@ __device__ __forceinline__ void pds_tile(uint32_t tS, uint32_t tP, const float* 
         const float2 nlp = u == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
         const float2 ndp = u == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
         const float2 x = __ffma2_rn(
-            make_float2(__uint_as_float(r[e + u]), __uint_as_float(r[e + u + 1])), sc2, nlp);
+            make_float2(__uint_as_float(s[col]), __uint_as_float(s[col + 1])), sc2, nlp);
         float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
         if (kPartial) {
           p.x = (col >= lo && col < hi) ? p.x : 0.f;
           p.y = (col + 1 >= lo && col + 1 < hi) ? p.y : 0.f;
         }
         const float2 dpd = __fadd2_rn(
-            make_float2(__uint_as_float(r[32 + e + u]), __uint_as_float(r[32 + e + u + 1])), ndp);
+            make_float2(__uint_as_float(dp[e + u]), __uint_as_float(dp[e + u + 1])), ndp);
         const float2 ds = __fmul2_rn(p, dpd);
         pp[(e + u) >> 1] = pack_bf16x2(p.x, p.y);
         dd[(e + u) >> 1] = pack_bf16x2(ds.x, ds.y);
       }
     }
-    tmem_st16(tS + 16 * c, pp);
+    // chunk c writes dP^T columns [16c, 16c + 16), all read by this or an
+    // earlier chunk
     tmem_st16(tP + 16 * c, dd);
-    // dS row j, queries [32c, 32c+32): four 16-byte units of the swizzled row
-    // of query chunk c/2.
-    uint8_t* base = ds_row + (c >> 1) * 16384;
+    uint8_t* base = p_row + (c >> 1) * 16384;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int unit = (c & 1) * 4 + u;
       *reinterpret_cast<uint4*>(base + ((unit ^ (j & 7)) << 4)) =
-          make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+          make_uint4(pp[4 * u], pp[4 * u + 1], pp[4 * u + 2], pp[4 * u + 3]);
     }
   }
 }
 
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    ffa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                   const BwdParams P) {
-  using C = BwdCfg<D>;
+__global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
+    ffa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_do, const KvParams P) {
+  using C = KvCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
   if ((smem_u32(smem) & 1023u) != 0) {
-    // The swizzled tile layout needs a 1024-byte aligned base; refuse to run.
     if (threadIdx.x == 0) record_error(P.err, kDevBadSmemAlign, 1);
     return;
   }
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   int* abort_flag = reinterpret_cast<int*>(smem + C::kMiscOff + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == 9) {
+  if (warp == 5) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -196,9 +196,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar(C::kBDOEmpty + s), 1);
     }
     mbar_init(bar(C::kBSdpFull), 1);
+    mbar_init(bar(C::kBSFree), 128);
     mbar_init(bar(C::kBPFull), 128);
-    mbar_init(bar(C::kBDqFull), 1);
-    mbar_init(bar(C::kBDqFree), 128);
     mbar_init(bar(C::kBDkvFull), 1);
     mbar_init(bar(C::kBDkvEmpty), 128);
     mbar_init(bar(C::kBDrain), 1);
@@ -212,7 +211,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const WaitCtl ctl{abort_flag, P.err, P.wait_ns};
   const int g = P.g;
 
-  if (warp == 8) {
+  if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tm_q);
@@ -222,7 +221,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t kv_cnt = 0, q_cnt = 0;
       bool ok = true, q_only = false;  // q_only: Q of iteration q_cnt issued, its dO not yet
       const int* it;
-      for (int r = 0; ok && bwd_item_at(P, r, it); ++r) {
+      for (int r = 0; ok && kv_item_at(P, r, it); ++r) {
         const int sb = it[kBiStepBeg], se = it[kBiStepEnd];
         if (se <= sb) continue;
         const int kt = it[kBiKt], hk = it[kBiHkv];
@@ -270,104 +269,104 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           drain_wait_b(bar(C::kBQFull + q_cnt % C::kStages), (q_cnt / C::kStages) & 1, kDrainNs);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t kIdAcc = idesc_bf16(128, D, false, true);   // A from TMEM, B MN-major
-      constexpr uint32_t kIdDq = idesc_bf16(128, D == 128 ? 128 : D, true, true);  // both MN-major
-      const uint32_t kA = sbase + C::kKOff, vA = sbase + C::kVOff, dsA = sbase + C::kDSOff;
-      uint32_t kv_cnt = 0, q_cnt = 0, p_cnt = 0, dqf_cnt = 0, dkv_cnt = 0;
-      bool ok = true, dq_pending = false;
+      constexpr uint32_t kIdAcc = idesc_bf16(128, D, false, true);  // A K-major, B MN-major
+      const uint32_t kA = sbase + C::kKOff, vA = sbase + C::kVOff, pA = sbase + C::kPOff;
+      auto issue_st = [&](uint32_t qA) {  // S^T = K Q^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + C::kTS, sdesc_sw128(kA + off, 16, 1024), sdesc_sw128(qA + off, 16, 1024),
+                 kIdS, kk > 0 ? 1u : 0u);
+        }
+      };
+      uint32_t kv_cnt = 0, q_cnt = 0, sf_cnt = 0, p_cnt = 0, dkv_cnt = 0;
+      bool ok = true;
       const int* it;
-      for (int r = 0; ok && bwd_item_at(P, r, it); ++r) {
+      for (int r = 0; ok && kv_item_at(P, r, it); ++r) {
         const int sb = it[kBiStepBeg], se = it[kBiStepEnd];
         if (se <= sb) continue;
         if (!(ok = mbar_wait(bar(C::kBKVFull), kv_cnt & 1, ctl, 500))) break;
         ++kv_cnt;
+        tc_fence_after();
         const int n_it = (se - sb) * g;
-        for (int i = 0; i < n_it; ++i) {
+        {  // S^T of the first iteration
           const int stage = q_cnt % C::kStages;
-          const uint32_t ph = (q_cnt / C::kStages) & 1;
+          if (!(ok = mbar_wait(bar(C::kBQFull + stage), (q_cnt / C::kStages) & 1, ctl, 501))) break;
+          tc_fence_after();
+          issue_st(sbase + C::kQOff + stage * C::kTileBytes);
+        }
+        for (int i = 0; i < n_it; ++i) {
+          const uint32_t c = q_cnt + (uint32_t)i;
+          const int stage = c % C::kStages;
+          const uint32_t ph = (c / C::kStages) & 1;
           const uint32_t qA = sbase + C::kQOff + stage * C::kTileBytes;
           const uint32_t doA = sbase + C::kDOOff + stage * C::kTileBytes;
-          if (!(ok = mbar_wait(bar(C::kBQFull + stage), ph, ctl, 501))) break;
           if (!(ok = mbar_wait(bar(C::kBDOFull + stage), ph, ctl, 502))) break;
           tc_fence_after();
-          // dP^T = V dO^T first: its columns were freed by the previous dK MMA.
+          // dP^T = V dO^T; its columns were last read by the previous dK MMA.
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tmem + C::kTdP, sdesc_sw128(vA + off, 16, 1024), sdesc_sw128(doA + off, 16, 1024),
-                   kIdS, kk > 0 ? 1u : 0u);
-          }
-          // S^T = K Q^T reuses the previous dQ tile's columns.
-          if (dq_pending) {
-            if (!(ok = mbar_wait(bar(C::kBDqFree), dqf_cnt & 1, ctl, 503))) break;
-            ++dqf_cnt;
-            tc_fence_after();
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tmem + C::kTS, sdesc_sw128(kA + off, 16, 1024), sdesc_sw128(qA + off, 16, 1024),
-                   kIdS, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + C::kTdP, sdesc_sw128(vA + off, 16, 1024),
+                   sdesc_sw128(doA + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(C::kBSdpFull));
-          if (!(ok = mbar_wait(bar(C::kBPFull), p_cnt & 1, ctl, 504))) break;
+          if (i + 1 < n_it) {
+            // S^T of the next iteration as soon as this S^T is in registers.
+            const uint32_t c1 = c + 1;
+            const int st1 = c1 % C::kStages;
+            if (!(ok = mbar_wait(bar(C::kBSFree), sf_cnt & 1, ctl, 503))) break;
+            ++sf_cnt;
+            if (!(ok = mbar_wait(bar(C::kBQFull + st1), (c1 / C::kStages) & 1, ctl, 504))) break;
+            tc_fence_after();
+            issue_st(sbase + C::kQOff + st1 * C::kTileBytes);
+          }
+          if (!(ok = mbar_wait(bar(C::kBPFull), p_cnt & 1, ctl, 505))) break;
           ++p_cnt;
           tc_fence_after();
           if (i == 0) {
-            if (!(ok = mbar_wait(bar(C::kBDkvEmpty), (dkv_cnt & 1) ^ 1, ctl, 505))) break;
+            if (!(ok = mbar_wait(bar(C::kBDkvEmpty), (dkv_cnt & 1) ^ 1, ctl, 506))) break;
             ++dkv_cnt;
             tc_fence_after();
           }
           const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            mma_ts(tmem + C::kTdV, tmem + C::kTS + kk * 8, sdesc_sw128(doA + kk * 2048, 16384, 1024),
-                   kIdAcc, (acc0 || kk > 0) ? 1u : 0u);
-            mma_ts(tmem + C::kTdK, tmem + C::kTdP + kk * 8, sdesc_sw128(qA + kk * 2048, 16384, 1024),
-                   kIdAcc, (acc0 || kk > 0) ? 1u : 0u);
+            const uint32_t poff = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_ss(tmem + C::kTdV, sdesc_sw128(pA + poff, 16, 1024),
+                   sdesc_sw128(doA + kk * 2048, 16384, 1024), kIdAcc, (acc0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + C::kTdK, tmem + C::kTdP + kk * 8,
+                   sdesc_sw128(qA + kk * 2048, 16384, 1024), kIdAcc, (acc0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(bar(C::kBDOEmpty + stage));
           mma_commit(bar(C::kBQEmpty + stage));
-          if constexpr (D == 128) {
-            // dQ^T = K^T dS^T: lanes = head dim, columns = queries, so the dQ
-            // warps reduce whole 128-byte row segments.
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tmem + C::kTS, sdesc_sw128(kA + kk * 2048, 16384, 1024),
-                     sdesc_sw128(dsA + kk * 2048, 16384, 1024), kIdDq, kk > 0 ? 1u : 0u);
-          } else {
-            // dQ = dS K: lanes = queries.
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tmem + C::kTS, sdesc_sw128(dsA + kk * 2048, 16384, 1024),
-                     sdesc_sw128(kA + kk * 2048, 16384, 1024), kIdDq, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(C::kBDqFull));
-          dq_pending = true;
-          ++q_cnt;
         }
         if (!ok) break;
+        // a pending S-free arrival of the last iteration is consumed here
+        if (!(ok = mbar_wait(bar(C::kBSFree), sf_cnt & 1, ctl, 507))) break;
+        ++sf_cnt;
+        q_cnt += (uint32_t)n_it;
         mma_commit(bar(C::kBDkvFull));
         mma_commit(bar(C::kBKVEmpty));
       }
       mma_commit(bar(C::kBDrain));
       drain_wait_b(bar(C::kBDrain), 0, kDrainNs);
     }
-  } else if (warp < 4) {
+  } else {
     // ------------------------------------------------------------ P / dS warps
     const int j = threadIdx.x;  // key lane
     const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t tS = tmem + lane_addr + C::kTS;
     const uint32_t tP = tmem + lane_addr + C::kTdP;
-    uint8_t* ds_row = smem + C::kDSOff + j * 128;
+    uint8_t* p_row = smem + C::kPOff + j * 128;
     uint32_t sdp_cnt = 0, dkv_cnt = 0;
     bool ok = true;
     const int* it;
-    for (int r = 0; ok && bwd_item_at(P, r, it); ++r) {
+    for (int r = 0; ok && kv_item_at(P, r, it); ++r) {
       const int sb = it[kBiStepBeg], se = it[kBiStepEnd];
       const int kt = it[kBiKt], hk = it[kBiHkv];
       const int key = kt * 128 + j;
@@ -375,18 +374,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int i = 0; i < n_it; ++i) {
         const int4 st = P.steps[sb + i / g];
         const int qt = st.x, info = st.y;
-        const int h = hk * g + i % g;
         int lo = 0, hi = 128;
         if (info & 1) key_query_window(P.slices[info >> 1], key, qt, lo, hi);
         const float* nl = reinterpret_cast<const float*>(smem + C::kLseOff +
                                                          (sdp_cnt % C::kStages) * C::kLseStageBytes);
         const float* nd = nl + 128;
-        bool w = mbar_wait(bar(C::kBSdpFull), sdp_cnt & 1, ctl, 600);
+        const bool w = mbar_wait(bar(C::kBSdpFull), sdp_cnt & 1, ctl, 600);
         if (!(ok = __all_sync(0xffffffffu, w))) break;
         ++sdp_cnt;
         tc_fence_after();
-        if (info & 1) pds_tile<true>(tS, tP, nl, nd, P.scale_log2, lo, hi, j, ds_row);
-        else pds_tile<false>(tS, tP, nl, nd, P.scale_log2, 0, 128, j, ds_row);
+        uint32_t s[128];
+        tmem_ld128(tS, s);
+        tc_fence_before();
+        mbar_arrive(bar(C::kBSFree));
+        if (info & 1) pds_row<true>(s, tP, nl, nd, P.scale_log2, lo, hi, j, p_row);
+        else pds_row<false>(s, tP, nl, nd, P.scale_log2, 0, 128, j, p_row);
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
@@ -394,11 +396,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!ok) break;
       // ---- dK / dV epilogue (written once per item; zeros when no query sees the tile)
-      uint4* pv = reinterpret_cast<uint4*>(P.dv + ((size_t)key * (P.Hq / g) + hk) * D);
-      uint4* pk = reinterpret_cast<uint4*>(P.dk + ((size_t)key * (P.Hq / g) + hk) * D);
+      uint4* pv = reinterpret_cast<uint4*>(P.dv + ((size_t)key * P.Hkv + hk) * D);
+      uint4* pk = reinterpret_cast<uint4*>(P.dk + ((size_t)key * P.Hkv + hk) * D);
       const bool store = key < P.Tk;
       if (n_it > 0) {
-        bool w = mbar_wait(bar(C::kBDkvFull), dkv_cnt & 1, ctl, 610);
+        const bool w = mbar_wait(bar(C::kBDkvFull), dkv_cnt & 1, ctl, 610);
         if (!(ok = __all_sync(0xffffffffu, w))) break;
         ++dkv_cnt;
         tc_fence_after();
@@ -429,89 +431,396 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int v = 0; v < D / 8; ++v) pv[v] = pk[v] = make_uint4(0, 0, 0, 0);
       }
     }
-  } else {
-    // ------------------------------------------------------------ dQ warps
-    const int t = threadIdx.x - 128;  // TMEM lane: head-dim index (D = 128) or query row
-    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t dq_cnt = 0;
-    bool ok = true;
-    const int* it;
-    for (int r = 0; ok && bwd_item_at(P, r, it); ++r) {
-      const int sb = it[kBiStepBeg], se = it[kBiStepEnd];
-      const int hk = it[kBiHkv];
-      const int n_it = (se - sb) * g;
-      for (int i = 0; i < n_it; ++i) {
-        const int4 st = P.steps[sb + i / g];
-        const int qt = st.x, info = st.y;
-        const int h = hk * g + i % g;
-        // rows of this q-tile that can receive a non-zero dQ
-        int q_lo = qt * 128, q_hi = min(P.Tq, qt * 128 + 128);
-        if (info & 1) {
-          const Slice sl = P.slices[info >> 1];
-          q_lo = max(q_lo, sl.qs);
-          q_hi = min(q_hi, sl.qe);
-        }
-        bool w = mbar_wait(bar(C::kBDqFull), dq_cnt & 1, ctl, 700);
-        if (!(ok = __all_sync(0xffffffffu, w))) break;
-        ++dq_cnt;
-        tc_fence_after();
-        if constexpr (D == 128) {
-          // lane t = head-dim index; columns = queries of the tile.  Read the
-          // whole tile, hand the columns back to the MMA warp, then reduce.
-          uint32_t u[128];
-          tmem_ld128(tmem + lane_addr + C::kTS, u);
-          tc_fence_before();
-          mbar_arrive(bar(C::kBDqFree));
-          float* col = P.dq_acc + ((size_t)qt * 128 * P.Hq + h) * D + t;
-          const size_t row_stride = (size_t)P.Hq * D;
-#pragma unroll
-          for (int e = 0; e < 128; ++e) {
-            const int q = qt * 128 + e;
-            if (q >= q_lo && q < q_hi)
-              red_add_f32(col + (size_t)e * row_stride, __uint_as_float(u[e]) * P.scale);
-          }
-        } else {
-          // lane t = query row; columns = head dim
-          const int q = qt * 128 + t;
-          const bool add = q >= q_lo && q < q_hi;
-          float* dst = P.dq_acc + ((size_t)q * P.Hq + h) * D;
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t u[32];
-            tmem_ld32(tmem + lane_addr + C::kTS + 32 * c, u);
-            if (c == D / 32 - 1) {
-              tc_fence_before();
-              mbar_arrive(bar(C::kBDqFree));
-            }
-            if (add) {
-#pragma unroll
-              for (int v = 0; v < 8; ++v)
-                red_add_v4(dst + 32 * c + 4 * v, __uint_as_float(u[4 * v]) * P.scale,
-                           __uint_as_float(u[4 * v + 1]) * P.scale,
-                           __uint_as_float(u[4 * v + 2]) * P.scale,
-                           __uint_as_float(u[4 * v + 3]) * P.scale);
-            }
-          }
-        }
-      }
-    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 5) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
-// -delta = -rowsum(dO * O), -lse2 = -lse * log2(e) (padded rows: 0), dQaccum = 0.
+// ============================================================================
+// dQ pass
+// Work units: the halves of the planner's unsplit forward items, i.e. one
+// (q-tile, query head) with its visits in k-tile order.
+// Warp roles (192 threads): warps 0-3 dS warps (thread = query row = TMEM
+// lane) and the dQ epilogue, warp 4 TMA producer, warp 5 MMA issuer.
+// TMEM columns: S of even steps [0,128), of odd steps [128,256), dP
+// [256,384), dQ [384,384+D).  dS (bf16) is written over the first 64 columns
+// of its step's S buffer and read from TMEM by the dQ MMA.
+template <int D>
+struct DqCfg {
+  static constexpr int kThreads = 192;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kStages = 2;
+  static constexpr int kQOff = 0;
+  static constexpr int kDOOff = kTileBytes;
+  static constexpr int kKOff = 2 * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kBQFull = 0, kBQEmpty = 1, kBKFull = 2, kBKEmpty = 2 + kStages,
+                       kBVFull = 2 + 2 * kStages, kBVEmpty = 2 + 3 * kStages,
+                       kBSdFull = 2 + 4 * kStages, kBDpFree = kBSdFull + 1,
+                       kBDsFull = kBDpFree + 1, kBDqFull = kBDsFull + 1,
+                       kBDqEmpty = kBDqFull + 1, kBDrain = kBDqEmpty + 1, kNumBars = kBDrain + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 64;
+  static constexpr int kTS0 = 0, kTdP = 256, kTdQ = 384;
+};
+
+struct DqParams {
+  const int4* steps;
+  const int* items;
+  const int* order;
+  int n_items;
+  const Slice* slices;
+  int Tq, Hq, g, qpad;
+  float scale, scale_log2;
+  const float* nlse2;
+  const float* ndelta;
+  __nv_bfloat16* dq;
+  int* err;
+  uint64_t wait_ns;
+};
+
+__device__ __forceinline__ bool dq_item_at(const DqParams& P, int r, const int*& it) {
+  const int G = gridDim.x, b = blockIdx.x;
+  const int pos = r * G + ((r & 1) ? (G - 1 - b) : b);
+  if (pos >= P.n_items) return false;
+  it = P.items + (size_t)P.order[pos] * kFiWords;
+  return true;
+}
+
+__device__ __forceinline__ bool half_active(const int* it, int h) {
+  return it[kFiQt0 + h] >= 0 && it[kFiH0 + h] >= 0;
+}
+
+__device__ __forceinline__ int half_info(const int4& st, int h) { return h == 0 ? st.y : st.z; }
+
+template <int D>
+__global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
+    ffa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_do, const DqParams P) {
+  using C = DqCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) record_error(P.err, kDevBadSmemAlign, 2);
+    return;
+  }
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kBarOff + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  int* abort_flag = reinterpret_cast<int*>(smem + C::kMiscOff + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::kBQFull), 1);
+    mbar_init(bar(C::kBQEmpty), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kBKFull + s), 1);
+      mbar_init(bar(C::kBKEmpty + s), 1);
+      mbar_init(bar(C::kBVFull + s), 1);
+      mbar_init(bar(C::kBVEmpty + s), 1);
+    }
+    mbar_init(bar(C::kBSdFull), 1);
+    mbar_init(bar(C::kBDpFree), 128);
+    mbar_init(bar(C::kBDsFull), 128);
+    mbar_init(bar(C::kBDqFull), 1);
+    mbar_init(bar(C::kBDqEmpty), 128);
+    mbar_init(bar(C::kBDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{abort_flag, P.err, P.wait_ns};
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_do);
+      uint32_t kv_cnt = 0, q_cnt = 0;
+      bool ok = true, k_only = false;
+      const int* it;
+      for (int r = 0; ok && dq_item_at(P, r, it); ++r) {
+        const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
+        if (se <= sb) continue;
+        for (int h = 0; ok && h < 2; ++h) {
+          if (!half_active(it, h)) continue;
+          int n = 0;
+          for (int j = sb; j < se; ++j) n += half_info(P.steps[j], h) >= 0 ? 1 : 0;
+          if (n == 0) continue;
+          const int qt = it[kFiQt0 + h], head = it[kFiH0 + h], hk = head / P.g;
+          if (!(ok = mbar_wait(bar(C::kBQEmpty), (q_cnt & 1) ^ 1, ctl, 800))) break;
+          mbar_arrive_expect_tx(bar(C::kBQFull), 2 * C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c) {
+            tma_load_2d(sbase + C::kQOff + c * 16384, &tm_q, bar(C::kBQFull), head * D + c * 64,
+                        qt * 128);
+            tma_load_2d(sbase + C::kDOOff + c * 16384, &tm_do, bar(C::kBQFull),
+                        head * D + c * 64, qt * 128);
+          }
+          ++q_cnt;
+          for (int j = sb; j < se; ++j) {
+            const int4 st = P.steps[j];
+            if (half_info(st, h) < 0) continue;
+            const int stage = kv_cnt % C::kStages;
+            const uint32_t ph = (kv_cnt / C::kStages) & 1;
+            if (!(ok = mbar_wait(bar(C::kBKEmpty + stage), ph ^ 1, ctl, 801))) break;
+            mbar_arrive_expect_tx(bar(C::kBKFull + stage), C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_2d(sbase + C::kKOff + stage * C::kTileBytes + c * 16384, &tm_k,
+                          bar(C::kBKFull + stage), hk * D + c * 64, st.x * 128);
+            k_only = true;
+            if (!(ok = mbar_wait(bar(C::kBVEmpty + stage), ph ^ 1, ctl, 802))) break;
+            k_only = false;
+            mbar_arrive_expect_tx(bar(C::kBVFull + stage), C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_2d(sbase + C::kVOff + stage * C::kTileBytes + c * 16384, &tm_v,
+                          bar(C::kBVFull + stage), hk * D + c * 64, st.x * 128);
+            ++kv_cnt;
+          }
+        }
+      }
+      if (!ok) {
+        if (q_cnt > 0) drain_wait_b(bar(C::kBQFull), (q_cnt - 1) & 1, kDrainNs);
+        for (uint32_t i = kv_cnt > (uint32_t)C::kStages ? kv_cnt - C::kStages : 0; i < kv_cnt; ++i) {
+          drain_wait_b(bar(C::kBKFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
+          drain_wait_b(bar(C::kBVFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
+        }
+        if (k_only)
+          drain_wait_b(bar(C::kBKFull + kv_cnt % C::kStages), (kv_cnt / C::kStages) & 1, kDrainNs);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);  // A from TMEM, B MN-major
+      const uint32_t qA = sbase + C::kQOff, doA = sbase + C::kDOOff;
+      auto issue_s = [&](int buf, int stage) {  // S = Q K^T
+        const uint32_t ka = sbase + C::kKOff + stage * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + C::kTS0 + 128 * buf, sdesc_sw128(qA + off, 16, 1024),
+                 sdesc_sw128(ka + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_dp = [&](int stage) {  // dP = dO V^T
+        const uint32_t va = sbase + C::kVOff + stage * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + C::kTdP, sdesc_sw128(doA + off, 16, 1024),
+                 sdesc_sw128(va + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+        }
+      };
+      uint32_t kv_cnt = 0, q_cnt = 0, dpf_cnt = 0, ds_cnt = 0, dqe_cnt = 0;
+      bool ok = true;
+      const int* it;
+      for (int r = 0; ok && dq_item_at(P, r, it); ++r) {
+        const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
+        if (se <= sb) continue;
+        for (int h = 0; ok && h < 2; ++h) {
+          if (!half_active(it, h)) continue;
+          int n = 0;
+          for (int j = sb; j < se; ++j) n += half_info(P.steps[j], h) >= 0 ? 1 : 0;
+          if (n == 0) continue;
+          if (!(ok = mbar_wait(bar(C::kBQFull), q_cnt & 1, ctl, 900))) break;
+          ++q_cnt;
+          tc_fence_after();
+          {  // step 0: S and dP
+            const int stage = kv_cnt % C::kStages;
+            const uint32_t ph = (kv_cnt / C::kStages) & 1;
+            if (!(ok = mbar_wait(bar(C::kBKFull + stage), ph, ctl, 901))) break;
+            tc_fence_after();
+            issue_s(0, stage);
+            if (!(ok = mbar_wait(bar(C::kBVFull + stage), ph, ctl, 902))) break;
+            tc_fence_after();
+            issue_dp(stage);
+            mma_commit(bar(C::kBSdFull));
+          }
+          for (int v = 0; v < n; ++v) {
+            const uint32_t c = kv_cnt + (uint32_t)v;
+            const int stage = c % C::kStages;
+            if (v + 1 < n) {
+              const uint32_t c1 = c + 1;
+              const int st1 = c1 % C::kStages;
+              const uint32_t ph1 = (c1 / C::kStages) & 1;
+              if (!(ok = mbar_wait(bar(C::kBKFull + st1), ph1, ctl, 903))) break;
+              tc_fence_after();
+              issue_s((v + 1) & 1, st1);
+              if (!(ok = mbar_wait(bar(C::kBDpFree), dpf_cnt & 1, ctl, 904))) break;
+              ++dpf_cnt;
+              if (!(ok = mbar_wait(bar(C::kBVFull + st1), ph1, ctl, 905))) break;
+              tc_fence_after();
+              issue_dp(st1);
+              mma_commit(bar(C::kBSdFull));
+            }
+            if (!(ok = mbar_wait(bar(C::kBDsFull), ds_cnt & 1, ctl, 906))) break;
+            ++ds_cnt;
+            tc_fence_after();
+            if (v == 0) {
+              if (!(ok = mbar_wait(bar(C::kBDqEmpty), (dqe_cnt & 1) ^ 1, ctl, 907))) break;
+              ++dqe_cnt;
+              tc_fence_after();
+            }
+            const uint32_t ka = sbase + C::kKOff + stage * C::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tmem + C::kTdQ, tmem + C::kTS0 + 128 * (v & 1) + kk * 8,
+                     sdesc_sw128(ka + kk * 2048, 16384, 1024), kIdQ, (v > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(bar(C::kBKEmpty + stage));
+            mma_commit(bar(C::kBVEmpty + stage));
+          }
+          if (!ok) break;
+          // the dS warps' dP-free arrival of the last step
+          if (!(ok = mbar_wait(bar(C::kBDpFree), dpf_cnt & 1, ctl, 908))) break;
+          ++dpf_cnt;
+          kv_cnt += (uint32_t)n;
+          mma_commit(bar(C::kBDqFull));
+          mma_commit(bar(C::kBQEmpty));
+        }
+      }
+      mma_commit(bar(C::kBDrain));
+      drain_wait_b(bar(C::kBDrain), 0, kDrainNs);
+    }
+  } else {
+    // ------------------------------------------------------------ dS warps
+    const int t = threadIdx.x;  // query row within the tile = TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    uint32_t sd_cnt = 0, dq_cnt = 0;
+    bool ok = true;
+    const int* it;
+    const float2 sc2 = make_float2(P.scale_log2, P.scale_log2);
+    for (int r = 0; ok && dq_item_at(P, r, it); ++r) {
+      const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
+      for (int h = 0; ok && h < 2; ++h) {
+        if (!half_active(it, h)) continue;
+        const int qt = it[kFiQt0 + h], head = it[kFiH0 + h];
+        const int row = qt * 128 + t;
+        const float nl = P.nlse2[(size_t)head * P.qpad + row];
+        const float nd = P.ndelta[(size_t)head * P.qpad + row];
+        const float2 nl2 = make_float2(nl, nl);
+        int v = 0;
+        for (int j = sb; j < se; ++j) {
+          const int4 st = P.steps[j];
+          const int info = half_info(st, h);
+          if (info < 0) continue;
+          const bool w = mbar_wait(bar(C::kBSdFull), sd_cnt & 1, ctl, 1000);
+          if (!(ok = __all_sync(0xffffffffu, w))) break;
+          ++sd_cnt;
+          tc_fence_after();
+          uint32_t dp[128];
+          tmem_ld128(tmem + lane_addr + C::kTdP, dp);
+          tc_fence_before();
+          mbar_arrive(bar(C::kBDpFree));
+          int lo = 0, hi = 128;
+          if (info & 1) {
+            const Slice sl = P.slices[info >> 1];
+            lo = hi = 0;
+            if (row >= sl.qs && row < sl.qe) {
+              lo = sl.ks + ((sl.t & 2) ? row - sl.qs : 0) - st.x * 128;
+              hi = sl.ke - ((sl.t & 1) ? sl.qe - 1 - row : 0) - st.x * 128;
+            }
+          }
+          const uint32_t tSb = tmem + lane_addr + C::kTS0 + 128 * (v & 1);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t s[32];
+            tmem_ld32(tSb + 32 * c, s);
+            uint32_t dd[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const int col = 32 * c + e;
+              const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])),
+                                          sc2, nl2);
+              float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              if (info & 1) {
+                p.x = (col >= lo && col < hi) ? p.x : 0.f;
+                p.y = (col + 1 >= lo && col + 1 < hi) ? p.y : 0.f;
+              }
+              const float2 ds = __fmul2_rn(
+                  p, __fadd2_rn(make_float2(__uint_as_float(dp[col]), __uint_as_float(dp[col + 1])),
+                                make_float2(nd, nd)));
+              dd[e >> 1] = pack_bf16x2(ds.x, ds.y);
+            }
+            // chunk c writes S columns [16c, 16c + 16), read by this or an earlier chunk
+            tmem_st16(tSb + 16 * c, dd);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(C::kBDsFull));
+          ++v;
+        }
+        if (!ok) break;
+        // ---- epilogue: dQ * scale -> bf16, every row of the tile written once
+        uint4* dst = reinterpret_cast<uint4*>(P.dq + ((size_t)row * P.Hq + head) * D);
+        const bool store = row < P.Tq;
+        if (v > 0) {
+          const bool w = mbar_wait(bar(C::kBDqFull), dq_cnt & 1, ctl, 1010);
+          if (!(ok = __all_sync(0xffffffffu, w))) break;
+          ++dq_cnt;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t u[32];
+            tmem_ld32(tmem + lane_addr + C::kTdQ + 32 * c, u);
+            if (c == D / 32 - 1) {
+              tc_fence_before();
+              mbar_arrive(bar(C::kBDqEmpty));
+            }
+            if (store) {
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4)
+                dst[4 * c + q4] = make_uint4(
+                    pack_bf16x2(__uint_as_float(u[8 * q4]) * P.scale,
+                                __uint_as_float(u[8 * q4 + 1]) * P.scale),
+                    pack_bf16x2(__uint_as_float(u[8 * q4 + 2]) * P.scale,
+                                __uint_as_float(u[8 * q4 + 3]) * P.scale),
+                    pack_bf16x2(__uint_as_float(u[8 * q4 + 4]) * P.scale,
+                                __uint_as_float(u[8 * q4 + 5]) * P.scale),
+                    pack_bf16x2(__uint_as_float(u[8 * q4 + 6]) * P.scale,
+                                __uint_as_float(u[8 * q4 + 7]) * P.scale));
+            }
+          }
+        } else if (store) {
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// -delta = -rowsum(dO * O), -lse2 = -lse * log2(e); padded rows get 0.
 template <int D>
 __global__ void ffa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
                                    const __nv_bfloat16* __restrict__ dout,
                                    const float* __restrict__ lse, int Tq, int Hq, int qpad,
-                                   float* __restrict__ lse2, float* __restrict__ delta,
-                                   float* __restrict__ dq_acc) {
+                                   float* __restrict__ nlse2, float* __restrict__ ndelta) {
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // (q, h)
   if (idx >= (long long)qpad * Hq) return;
   const int q = (int)(idx / Hq), h = (int)(idx % Hq);
@@ -519,7 +828,6 @@ __global__ void ffa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
   if (q < Tq) {
     const uint4* o4 = reinterpret_cast<const uint4*>(out + ((size_t)q * Hq + h) * D);
     const uint4* d4 = reinterpret_cast<const uint4*>(dout + ((size_t)q * Hq + h) * D);
-    float4* z = reinterpret_cast<float4*>(dq_acc + ((size_t)q * Hq + h) * D);
 #pragma unroll
     for (int v = 0; v < D / 8; ++v) {
       const uint4 a = o4[v], b = d4[v];
@@ -532,40 +840,25 @@ __global__ void ffa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
         dsum = fmaf(fa.y, fb.y, dsum);
       }
     }
-#pragma unroll
-    for (int v = 0; v < D / 4; ++v) z[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float lv = lse[(size_t)h * Tq + q];
-    l2 = lv * kLog2e;  // -inf stays -inf: such rows have no visible key
+    l2 = lse[(size_t)h * Tq + q] * kLog2e;  // -inf stays -inf: such rows see no key
   }
-  lse2[(size_t)h * qpad + q] = -l2;
-  delta[(size_t)h * qpad + q] = -dsum;
-}
-
-template <int D>
-__global__ void ffa_dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
-                                      long long n8) {
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n8) return;
-  const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
-  const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
-  reinterpret_cast<uint4*>(dq)[i] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
-                                               pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+  nlse2[(size_t)h * qpad + q] = -l2;
+  ndelta[(size_t)h * qpad + q] = -dsum;
 }
 
 template <int D>
 ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const void* v,
                           const void* out, const void* dout, const float* lse, float scale,
                           void* dq, void* dk, void* dv, void* ws, cudaStream_t st) {
-  using C = BwdCfg<D>;
   const int qpad = p->n_qt * 128;
-  float* lse2 = static_cast<float*>(ws);
-  float* delta = lse2 + (size_t)p->Hq * qpad;
-  float* dq_acc = delta + (size_t)p->Hq * qpad;
+  float* nlse2 = static_cast<float*>(ws);
+  float* ndelta = nlse2 + (size_t)p->Hq * qpad;
   {
     const long long n = (long long)qpad * p->Hq;
+    record_phase(p, 2, st);
     ffa_bwd_pre_kernel<D><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse,
-        p->Tq, p->Hq, qpad, lse2, delta, dq_acc);
+        p->Tq, p->Hq, qpad, nlse2, ndelta);
     note_launches(1);
     if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   }
@@ -573,37 +866,63 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   if (!encode_tile_map(&tq, q, p->Tq, p->Hq * D) || !encode_tile_map(&tk, k, p->Tk, p->Hkv * D) ||
       !encode_tile_map(&tv, v, p->Tk, p->Hkv * D) || !encode_tile_map(&tdo, dout, p->Tq, p->Hq * D))
     return FFA_ERR_INVALID_ARG;
-  BwdParams P;
-  P.steps = p->bwd_steps;
-  P.items = p->bwd_items;
-  P.order = p->bwd_order;
-  P.n_items = (int)p->n_bwd_items;
-  P.slices = p->slices;
-  P.Tq = p->Tq;
-  P.Tk = p->Tk;
-  P.Hq = p->Hq;
-  P.g = p->Hq / p->Hkv;
-  P.qpad = qpad;
-  P.scale = scale;
-  P.scale_log2 = scale * kLog2e;
-  P.nlse2 = lse2;
-  P.ndelta = delta;
-  P.dq_acc = dq_acc;
-  P.dk = static_cast<__nv_bfloat16*>(dk);
-  P.dv = static_cast<__nv_bfloat16*>(dv);
-  P.err = p->err;
-  P.wait_ns = p->wait_ns;
-  if (cudaFuncSetAttribute(ffa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::kSmemBytes) != cudaSuccess)
-    return FFA_ERR_CUDA;
-  ffa_bwd_kernel<D><<<p->grid_bwd, kBwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, P);
-  note_launches(1);
-  if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
-  const long long n8 = (long long)p->Tq * p->Hq * D / 8;
-  ffa_dq_convert_kernel<D><<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(
-      dq_acc, static_cast<__nv_bfloat16*>(dq), n8);
-  note_launches(1);
-  if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
+  const float scale_log2 = scale * kLog2e;
+  {
+    using C = KvCfg<D>;
+    KvParams P;
+    P.steps = p->bwd_steps;
+    P.items = p->bwd_items;
+    P.order = p->bwd_order;
+    P.n_items = (int)p->n_bwd_items;
+    P.slices = p->slices;
+    P.Tk = p->Tk;
+    P.Hkv = p->Hkv;
+    P.g = p->Hq / p->Hkv;
+    P.qpad = qpad;
+    P.scale = scale;
+    P.scale_log2 = scale_log2;
+    P.nlse2 = nlse2;
+    P.ndelta = ndelta;
+    P.dk = static_cast<__nv_bfloat16*>(dk);
+    P.dv = static_cast<__nv_bfloat16*>(dv);
+    P.err = p->err;
+    P.wait_ns = p->wait_ns;
+    if (cudaFuncSetAttribute(ffa_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
+      return FFA_ERR_CUDA;
+    record_phase(p, 3, st);
+    ffa_bwd_dkdv_kernel<D><<<p->grid_bwd, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, P);
+    note_launches(1);
+    if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
+  }
+  {
+    using C = DqCfg<D>;
+    DqParams P;
+    P.steps = p->fwd_steps;
+    P.items = p->dq_items;
+    P.order = p->dq_order;
+    P.n_items = (int)p->n_dq_items;
+    P.slices = p->slices;
+    P.Tq = p->Tq;
+    P.Hq = p->Hq;
+    P.g = p->Hq / p->Hkv;
+    P.qpad = qpad;
+    P.scale = scale;
+    P.scale_log2 = scale_log2;
+    P.nlse2 = nlse2;
+    P.ndelta = ndelta;
+    P.dq = static_cast<__nv_bfloat16*>(dq);
+    P.err = p->err;
+    P.wait_ns = p->wait_ns;
+    if (cudaFuncSetAttribute(ffa_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
+      return FFA_ERR_CUDA;
+    record_phase(p, 4, st);
+    ffa_bwd_dq_kernel<D><<<p->grid_dq, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, P);
+    note_launches(1);
+    if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
+  }
+  record_phase(p, 5, st);
   return FFA_OK;
 }
 
@@ -611,7 +930,7 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
 
 size_t bwd_workspace_bytes(const ffa_plan_s* p) {
   const size_t qpad = (size_t)p->n_qt * 128;
-  return (2 * qpad * p->Hq + (size_t)p->Tq * p->Hq * p->D) * sizeof(float);
+  return 2 * qpad * p->Hq * sizeof(float);
 }
 
 ffa_status_t launch_bwd(ffa_plan_s* p, const void* q, const void* k, const void* v,
@@ -631,7 +950,7 @@ ffa_status_t launch_bwd(ffa_plan_s* p, const void* q, const void* k, const void*
 // backward: code running while a stream is being captured into a graph,
 // runtimes that forbid allocation after start-up, or hosts whose memory
 // manager owns every allocation.  ffa_bwd_noalloc serves them: its scratch
-// (log2-scaled lse, delta and the fp32 dQ accumulator) lives in the array
+// (log2-scaled lse and delta) lives in the array
 // below, which every GPU that loads this library holds until the process
 // exits.  All calls share it, so calls whose kernels overlap on the GPU race.
 namespace ffa {

@@ -527,6 +527,7 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
                            C::kSmemBytes) != cudaSuccess)
     return FFA_ERR_CUDA;
 
+  record_phase(p, 0, st);
   ffa_fwd_kernel<D><<<p->grid_fwd, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, P);
   note_launches(1);
   if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
@@ -536,6 +537,7 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     note_launches(1);
     if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   }
+  record_phase(p, 1, st);
   return FFA_OK;
 }
 

@@ -64,8 +64,16 @@ struct ffa_plan_s {
   int* bwd_items = nullptr;
   int64_t n_bwd_items = 0;
   int* bwd_order = nullptr;
+  // Unsplit forward items for the dQ pass of the backward (aliases the
+  // forward list when no item was split).
+  int* dq_items = nullptr;
+  int* dq_order = nullptr;
+  int64_t n_dq_items = 0;
+  bool dq_alias = true;
   int* err = nullptr;  // device [2]: code, location
-  int grid_fwd = 0, grid_bwd = 0;
+  int grid_fwd = 0, grid_bwd = 0, grid_dq = 0;
+  cudaEvent_t events[6] = {};  // optional phase events (ffa_plan_set_events)
+  bool use_events = false;
   int64_t area = 0;
   uint64_t wait_ns = 2000000000ull;
 };
@@ -82,4 +90,8 @@ size_t bwd_workspace_bytes(const ffa_plan_s* p);
 // Implemented in ffa_plan.cu.
 bool encode_tile_map(void* map128, const void* base, int rows, int cols_elems);
 void note_launches(int n);  // adds to the count reported by ffa_kernel_launch_count
+// Records phase event i of the plan on `st` when the caller asked for them.
+inline void record_phase(const ffa_plan_s* p, int i, cudaStream_t st) {
+  if (p->use_events) cudaEventRecord(p->events[i], st);
+}
 }  // namespace ffa

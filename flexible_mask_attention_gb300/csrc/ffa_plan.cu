@@ -477,6 +477,10 @@ void free_plan(ffa_plan_s* p) {
                   p->bwd_steps, p->bwd_items, p->bwd_order, p->err};
   for (void* b : bufs)
     if (b) cudaFree(b);
+  if (!p->dq_alias) {
+    if (p->dq_items) cudaFree(p->dq_items);
+    if (p->dq_order) cudaFree(p->dq_order);
+  }
   delete p;
 }
 
@@ -599,6 +603,10 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
     FFA_CUDA(cudaGetLastError());
     FFA_CUDA(cudaStreamSynchronize(st));
     std::swap(items.p, nitems.p);
+    // the unsplit list stays for the dQ pass of the backward
+    p->dq_items = static_cast<int*>(nitems.release());
+    p->n_dq_items = n_items;
+    p->dq_alias = false;
     final_items = n_chunks;
     p->n_merges = n_groups;
     p->n_slots = (int)n_slots;
@@ -613,6 +621,16 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   items.release();
   p->fwd_steps = steps.as<int4>();
   steps.release();
+  if (p->dq_alias) {
+    p->dq_items = p->fwd_items;
+    p->dq_order = p->fwd_order;
+    p->n_dq_items = p->n_fwd_items;
+  } else {
+    FFA_CUDA(cudaMalloc(&p->dq_order, sizeof(int) * (size_t)std::max<int64_t>(1, p->n_dq_items)));
+    rc = sort_items(p->dq_items, kFiWords, kFiCost, kFiH0, g, (int)p->n_dq_items, p->dq_order, st);
+    if (rc != FFA_OK) return rc;
+  }
+  p->grid_dq = (int)std::max<int64_t>(1, std::min<int64_t>(p->num_sms, p->n_dq_items));
 
   // backward
   DevBuf bcnt(st), boff(st), bvis(st);
@@ -817,6 +835,13 @@ ffa_status_t ffa_get_last_device_error(ffa_plan_t p, int32_t* code, int32_t* whe
     return FFA_ERR_CUDA;
   *code = h[0];
   *where = h[1];
+  return FFA_OK;
+}
+
+ffa_status_t ffa_plan_set_events(ffa_plan_t p, void* const* events, int32_t n) {
+  if (!p || (n != 0 && n != 6) || (n == 6 && !events)) return FFA_ERR_INVALID_ARG;
+  p->use_events = n == 6;
+  for (int i = 0; i < 6; ++i) p->events[i] = n == 6 ? static_cast<cudaEvent_t>(events[i]) : nullptr;
   return FFA_OK;
 }
 

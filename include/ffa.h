@@ -165,6 +165,15 @@ ffa_status_t ffa_get_last_device_error(ffa_plan_t plan, int32_t* code, int32_t* 
  * A wait that runs out makes the kernel stop and report FFA_ERR_TIMEOUT. */
 ffa_status_t ffa_plan_set_wait_limit(ffa_plan_t plan, uint64_t nanoseconds);
 
+/* Instrumentation: CUDA events (cudaEvent_t values, created by the caller)
+ * that ffa_fwd / ffa_bwd record on their stream around their kernels:
+ *   events[0], events[1]: before / after the forward kernel (and merge);
+ *   events[2], events[3], events[4], events[5]: before the backward
+ *   preprocess, before the dK/dV pass, before the dQ pass, after the dQ pass.
+ * n_events must be 6, or 0 to stop recording.  The plan keeps the handles
+ * only; the caller owns and destroys the events. */
+ffa_status_t ffa_plan_set_events(ffa_plan_t plan, void* const* events, int32_t n_events);
+
 /* Human-readable name of a status code (static storage). */
 const char* ffa_status_string(ffa_status_t status);
 
