@@ -45,12 +45,15 @@ __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity, uint
 
 // ============================================================================
 // dK / dV pass
-// Warp roles (192 threads): warps 0-3 P/dS (thread = key = TMEM lane) and
-// the dK/dV epilogue, warp 4 TMA producer, warp 5 MMA issuer (TMEM owner).
+// Warp roles (320 threads): warps 0-7 P/dS in two warpgroups (thread = key =
+// TMEM lane; warpgroup w owns query columns [64w, 64w+64)) and the dK/dV
+// epilogue, warp 8 TMA producer, warp 9 MMA issuer (TMEM owner).
 // TMEM columns: dV [0,D), dK [D,2D), S^T [2D,2D+128), dP^T [2D+128,2D+256).
+// Warpgroup w writes its dS^T pairs over dP^T columns [64w, 64w+32), inside
+// the range it read itself.
 template <int D>
 struct KvCfg {
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 320;
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kStages = 2;
@@ -112,32 +115,34 @@ __device__ __forceinline__ void key_query_window(const Slice& sl, int key, int q
   hi = b - qt * 128;
 }
 
-// P^T and dS^T for key row j over the 128 queries of the step, from the S^T
-// row already in registers (s) and the dP^T row read from TMEM here:
+// P^T and dS^T for key row j over the 64 queries [q0, q0+64) of the step
+// owned by this warpgroup, from the S^T values already in registers (s) and
+// the dP^T values read from TMEM here:
 //   p = 2^(s * scale * log2e - lse2), ds = p * (dp - delta).
-// dS^T goes to TMEM as bf16 pairs over dP^T columns [0, 64); P^T goes to the
-// 128-byte swizzled shared-memory tile (row j, K-major for the dV MMA).
+// dS^T goes to TMEM as bf16 pairs over dP^T columns [q0, q0+32); P^T goes to
+// query chunk q0/64 of the 128-byte swizzled shared-memory tile (row j).
 template <bool kPartial>
-__device__ __forceinline__ void pds_row(const uint32_t (&s)[128], uint32_t tP, const float* nl,
-                                        const float* nd, float scale_log2, int lo, int hi, int j,
-                                        uint8_t* p_row) {
+__device__ __forceinline__ void pds_half(const uint32_t (&s)[64], uint32_t tP, int q0,
+                                         const float* nl, const float* nd, float scale_log2,
+                                         int lo, int hi, int j, uint8_t* p_row) {
   const float2 sc2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
+  for (int c = 0; c < 2; ++c) {
     uint32_t dp[32];
-    tmem_ld32(tP + 32 * c, dp);
+    tmem_ld32(tP + q0 + 32 * c, dp);
     uint32_t pp[16], dd[16];
 #pragma unroll
     for (int e = 0; e < 32; e += 4) {
-      const float4 l4 = *reinterpret_cast<const float4*>(nl + 32 * c + e);
-      const float4 d4 = *reinterpret_cast<const float4*>(nd + 32 * c + e);
+      const float4 l4 = *reinterpret_cast<const float4*>(nl + q0 + 32 * c + e);
+      const float4 d4 = *reinterpret_cast<const float4*>(nd + q0 + 32 * c + e);
 #pragma unroll
       for (int u = 0; u < 4; u += 2) {
-        const int col = 32 * c + e + u;
+        const int lc = 32 * c + e + u;  // column within this warpgroup's half
+        const int col = q0 + lc;
         const float2 nlp = u == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
         const float2 ndp = u == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
         const float2 x = __ffma2_rn(
-            make_float2(__uint_as_float(s[col]), __uint_as_float(s[col + 1])), sc2, nlp);
+            make_float2(__uint_as_float(s[lc]), __uint_as_float(s[lc + 1])), sc2, nlp);
         float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
         if (kPartial) {
           p.x = (col >= lo && col < hi) ? p.x : 0.f;
@@ -150,14 +155,12 @@ __device__ __forceinline__ void pds_row(const uint32_t (&s)[128], uint32_t tP, c
         dd[(e + u) >> 1] = pack_bf16x2(ds.x, ds.y);
       }
     }
-    // chunk c writes dP^T columns [16c, 16c + 16), all read by this or an
-    // earlier chunk
-    tmem_st16(tP + 16 * c, dd);
-    uint8_t* base = p_row + (c >> 1) * 16384;
+    // chunk c writes dP^T columns [q0 + 16c, q0 + 16c + 16), read by chunk 0
+    tmem_st16(tP + q0 + 16 * c, dd);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int unit = (c & 1) * 4 + u;
-      *reinterpret_cast<uint4*>(base + ((unit ^ (j & 7)) << 4)) =
+      const int unit = c * 4 + u;
+      *reinterpret_cast<uint4*>(p_row + ((unit ^ (j & 7)) << 4)) =
           make_uint4(pp[4 * u], pp[4 * u + 1], pp[4 * u + 2], pp[4 * u + 3]);
     }
   }
@@ -182,7 +185,7 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
   int* abort_flag = reinterpret_cast<int*>(smem + C::kMiscOff + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -196,10 +199,10 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
       mbar_init(bar(C::kBDOEmpty + s), 1);
     }
     mbar_init(bar(C::kBSdpFull), 1);
-    mbar_init(bar(C::kBSFree), 128);
-    mbar_init(bar(C::kBPFull), 128);
+    mbar_init(bar(C::kBSFree), 256);
+    mbar_init(bar(C::kBPFull), 256);
     mbar_init(bar(C::kBDkvFull), 1);
-    mbar_init(bar(C::kBDkvEmpty), 128);
+    mbar_init(bar(C::kBDkvEmpty), 256);
     mbar_init(bar(C::kBDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
   const WaitCtl ctl{abort_flag, P.err, P.wait_ns};
   const int g = P.g;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tm_q);
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
           drain_wait_b(bar(C::kBQFull + q_cnt % C::kStages), (q_cnt / C::kStages) & 1, kDrainNs);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
@@ -339,7 +342,9 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
             const uint32_t poff = (kk >> 2) * 16384 + (kk & 3) * 32;
             mma_ss(tmem + C::kTdV, sdesc_sw128(pA + poff, 16, 1024),
                    sdesc_sw128(doA + kk * 2048, 16384, 1024), kIdAcc, (acc0 || kk > 0) ? 1u : 0u);
-            mma_ts(tmem + C::kTdK, tmem + C::kTdP + kk * 8,
+            // dS^T pairs of queries [16kk, 16kk+16): warpgroup kk/4 wrote them at
+            // dP^T column 64*(kk/4) + 8*(kk%4)
+            mma_ts(tmem + C::kTdK, tmem + C::kTdP + 64 * (kk >> 2) + 8 * (kk & 3),
                    sdesc_sw128(qA + kk * 2048, 16384, 1024), kIdAcc, (acc0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(bar(C::kBDOEmpty + stage));
@@ -356,13 +361,14 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
       mma_commit(bar(C::kBDrain));
       drain_wait_b(bar(C::kBDrain), 0, kDrainNs);
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ P / dS warps
-    const int j = threadIdx.x;  // key lane
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_addr + C::kTS;
+    const int wg = warp >> 2;             // query columns [64wg, 64wg+64)
+    const int j = threadIdx.x & 127;      // key lane
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + C::kTS + 64 * wg;
     const uint32_t tP = tmem + lane_addr + C::kTdP;
-    uint8_t* p_row = smem + C::kPOff + j * 128;
+    uint8_t* p_row = smem + C::kPOff + wg * 16384 + j * 128;
     uint32_t sdp_cnt = 0, dkv_cnt = 0;
     bool ok = true;
     const int* it;
@@ -383,21 +389,22 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
         if (!(ok = __all_sync(0xffffffffu, w))) break;
         ++sdp_cnt;
         tc_fence_after();
-        uint32_t s[128];
-        tmem_ld128(tS, s);
+        uint32_t s[64];
+        tmem_ld64(tS, s);
         tc_fence_before();
         mbar_arrive(bar(C::kBSFree));
-        if (info & 1) pds_row<true>(s, tP, nl, nd, P.scale_log2, lo, hi, j, p_row);
-        else pds_row<false>(s, tP, nl, nd, P.scale_log2, 0, 128, j, p_row);
+        if (info & 1) pds_half<true>(s, tP, 64 * wg, nl, nd, P.scale_log2, lo, hi, j, p_row);
+        else pds_half<false>(s, tP, 64 * wg, nl, nd, P.scale_log2, 0, 128, j, p_row);
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(C::kBPFull));
       }
       if (!ok) break;
-      // ---- dK / dV epilogue (written once per item; zeros when no query sees the tile)
-      uint4* pv = reinterpret_cast<uint4*>(P.dv + ((size_t)key * P.Hkv + hk) * D);
-      uint4* pk = reinterpret_cast<uint4*>(P.dk + ((size_t)key * P.Hkv + hk) * D);
+      // ---- dK / dV epilogue: warpgroup wg writes columns [wg*D/2, (wg+1)*D/2)
+      constexpr int kHalf = D / 2;
+      uint4* pv = reinterpret_cast<uint4*>(P.dv + ((size_t)key * P.Hkv + hk) * D + wg * kHalf);
+      uint4* pk = reinterpret_cast<uint4*>(P.dk + ((size_t)key * P.Hkv + hk) * D + wg * kHalf);
       const bool store = key < P.Tk;
       if (n_it > 0) {
         const bool w = mbar_wait(bar(C::kBDkvFull), dkv_cnt & 1, ctl, 610);
@@ -405,12 +412,12 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
         ++dkv_cnt;
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 2 * (D / 32); ++c) {
-          const bool is_k = c >= D / 32;
-          const int cc = is_k ? c - D / 32 : c;
+        for (int c = 0; c < 2 * (kHalf / 32); ++c) {
+          const bool is_k = c >= kHalf / 32;
+          const int cc = is_k ? c - kHalf / 32 : c;
           uint32_t u[32];
-          tmem_ld32(tmem + lane_addr + (is_k ? C::kTdK : C::kTdV) + 32 * cc, u);
-          if (c == 2 * (D / 32) - 1) {
+          tmem_ld32(tmem + lane_addr + (is_k ? C::kTdK : C::kTdV) + wg * kHalf + 32 * cc, u);
+          if (c == 2 * (kHalf / 32) - 1) {
             tc_fence_before();
             mbar_arrive(bar(C::kBDkvEmpty));
           }
@@ -428,13 +435,13 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
         }
       } else if (store) {
 #pragma unroll
-        for (int v = 0; v < D / 8; ++v) pv[v] = pk[v] = make_uint4(0, 0, 0, 0);
+        for (int v = 0; v < kHalf / 8; ++v) pv[v] = pk[v] = make_uint4(0, 0, 0, 0);
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -445,14 +452,16 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
 // dQ pass
 // Work units: the halves of the planner's unsplit forward items, i.e. one
 // (q-tile, query head) with its visits in k-tile order.
-// Warp roles (192 threads): warps 0-3 dS warps (thread = query row = TMEM
-// lane) and the dQ epilogue, warp 4 TMA producer, warp 5 MMA issuer.
+// Warp roles (320 threads): warps 0-7 dS warps in two warpgroups (thread =
+// query row = TMEM lane; warpgroup w owns key columns [64w, 64w+64)) and the
+// dQ epilogue, warp 8 TMA producer, warp 9 MMA issuer.
 // TMEM columns: S of even steps [0,128), of odd steps [128,256), dP
-// [256,384), dQ [384,384+D).  dS (bf16) is written over the first 64 columns
-// of its step's S buffer and read from TMEM by the dQ MMA.
+// [256,384), dQ [384,384+D).  Warpgroup w writes its dS pairs over columns
+// [64w, 64w+32) of its step's S buffer (read by itself first); the dQ MMA
+// reads them from TMEM.
 template <int D>
 struct DqCfg {
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 320;
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kStages = 2;
@@ -519,7 +528,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   int* abort_flag = reinterpret_cast<int*>(smem + C::kMiscOff + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -533,10 +542,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       mbar_init(bar(C::kBVEmpty + s), 1);
     }
     mbar_init(bar(C::kBSdFull), 1);
-    mbar_init(bar(C::kBDpFree), 128);
-    mbar_init(bar(C::kBDsFull), 128);
+    mbar_init(bar(C::kBDpFree), 256);
+    mbar_init(bar(C::kBDsFull), 256);
     mbar_init(bar(C::kBDqFull), 1);
-    mbar_init(bar(C::kBDqEmpty), 128);
+    mbar_init(bar(C::kBDqEmpty), 256);
     mbar_init(bar(C::kBDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -547,7 +556,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, P.err, P.wait_ns};
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tm_q);
@@ -606,7 +615,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           drain_wait_b(bar(C::kBKFull + kv_cnt % C::kStages), (kv_cnt / C::kStages) & 1, kDrainNs);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
@@ -682,8 +691,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
             }
             const uint32_t ka = sbase + C::kKOff + stage * C::kTileBytes;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ts(tmem + C::kTdQ, tmem + C::kTS0 + 128 * (v & 1) + kk * 8,
+            for (int kk = 0; kk < 8; ++kk)  // dS pairs of keys [16kk, 16kk+16)
+              mma_ts(tmem + C::kTdQ, tmem + C::kTS0 + 128 * (v & 1) + 64 * (kk >> 2) + 8 * (kk & 3),
                      sdesc_sw128(ka + kk * 2048, 16384, 1024), kIdQ, (v > 0 || kk > 0) ? 1u : 0u);
             mma_commit(bar(C::kBKEmpty + stage));
             mma_commit(bar(C::kBVEmpty + stage));
@@ -700,10 +709,11 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       mma_commit(bar(C::kBDrain));
       drain_wait_b(bar(C::kBDrain), 0, kDrainNs);
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ dS warps
-    const int t = threadIdx.x;  // query row within the tile = TMEM lane
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const int wg = warp >> 2;         // key columns [64wg, 64wg+64)
+    const int t = threadIdx.x & 127;  // query row within the tile = TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t sd_cnt = 0, dq_cnt = 0;
     bool ok = true;
     const int* it;
@@ -726,8 +736,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           if (!(ok = __all_sync(0xffffffffu, w))) break;
           ++sd_cnt;
           tc_fence_after();
-          uint32_t dp[128];
-          tmem_ld128(tmem + lane_addr + C::kTdP, dp);
+          uint32_t dp[64];
+          tmem_ld64(tmem + lane_addr + C::kTdP + 64 * wg, dp);
           tc_fence_before();
           mbar_arrive(bar(C::kBDpFree));
           int lo = 0, hi = 128;
@@ -739,15 +749,16 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
               hi = sl.ke - ((sl.t & 1) ? sl.qe - 1 - row : 0) - st.x * 128;
             }
           }
-          const uint32_t tSb = tmem + lane_addr + C::kTS0 + 128 * (v & 1);
+          const uint32_t tSb = tmem + lane_addr + C::kTS0 + 128 * (v & 1) + 64 * wg;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t s[32];
             tmem_ld32(tSb + 32 * c, s);
             uint32_t dd[16];
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
-              const int col = 32 * c + e;
+              const int lc = 32 * c + e;
+              const int col = 64 * wg + lc;
               const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])),
                                           sc2, nl2);
               float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
@@ -756,11 +767,11 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
                 p.y = (col + 1 >= lo && col + 1 < hi) ? p.y : 0.f;
               }
               const float2 ds = __fmul2_rn(
-                  p, __fadd2_rn(make_float2(__uint_as_float(dp[col]), __uint_as_float(dp[col + 1])),
+                  p, __fadd2_rn(make_float2(__uint_as_float(dp[lc]), __uint_as_float(dp[lc + 1])),
                                 make_float2(nd, nd)));
               dd[e >> 1] = pack_bf16x2(ds.x, ds.y);
             }
-            // chunk c writes S columns [16c, 16c + 16), read by this or an earlier chunk
+            // chunk c writes columns [64wg + 16c, 64wg + 16c + 16), read by chunk 0
             tmem_st16(tSb + 16 * c, dd);
           }
           tmem_st_wait();
@@ -769,8 +780,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           ++v;
         }
         if (!ok) break;
-        // ---- epilogue: dQ * scale -> bf16, every row of the tile written once
-        uint4* dst = reinterpret_cast<uint4*>(P.dq + ((size_t)row * P.Hq + head) * D);
+        // ---- epilogue: dQ * scale -> bf16; warpgroup wg writes columns [wg*D/2, (wg+1)*D/2)
+        constexpr int kHalf = D / 2;
+        uint4* dst = reinterpret_cast<uint4*>(P.dq + ((size_t)row * P.Hq + head) * D + wg * kHalf);
         const bool store = row < P.Tq;
         if (v > 0) {
           const bool w = mbar_wait(bar(C::kBDqFull), dq_cnt & 1, ctl, 1010);
@@ -778,10 +790,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           ++dq_cnt;
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < kHalf / 32; ++c) {
             uint32_t u[32];
-            tmem_ld32(tmem + lane_addr + C::kTdQ + 32 * c, u);
-            if (c == D / 32 - 1) {
+            tmem_ld32(tmem + lane_addr + C::kTdQ + wg * kHalf + 32 * c, u);
+            if (c == kHalf / 32 - 1) {
               tc_fence_before();
               mbar_arrive(bar(C::kBDqEmpty));
             }
@@ -801,14 +813,14 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           }
         } else if (store) {
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < kHalf / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
         }
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
