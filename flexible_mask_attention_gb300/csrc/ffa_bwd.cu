@@ -45,15 +45,16 @@ __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity, uint
 
 // ============================================================================
 // dK / dV pass
-// Warp roles (320 threads): warps 0-7 P/dS in two warpgroups (thread = key =
+// Warp roles (384 threads): warps 0-7 P/dS in two warpgroups (thread = key =
 // TMEM lane; warpgroup w owns query columns [64w, 64w+64)) and the dK/dV
-// epilogue, warp 8 TMA producer, warp 9 MMA issuer (TMEM owner).
+// epilogue, warp 8 TMA producer, warp 9 MMA issuer (TMEM owner), warps 10-11
+// idle; registers split 200 / 104 between them (ffa_ptx.cuh).
 // TMEM columns: dV [0,D), dK [D,2D), S^T [2D,2D+128), dP^T [2D+128,2D+256).
 // Warpgroup w writes its dS^T pairs over dP^T columns [64w, 64w+32), inside
 // the range it read itself.
 template <int D>
 struct KvCfg {
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = kSplitThreads;
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kStages = 2;
@@ -214,6 +215,8 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
   const WaitCtl ctl{abort_flag, P.err, P.wait_ns};
   const int g = P.g;
 
+  if (warp >= 8) {
+  reg_dealloc<kSplitNarrowRegs>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -361,7 +364,9 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
       mma_commit(bar(C::kBDrain));
       drain_wait_b(bar(C::kBDrain), 0, kDrainNs);
     }
-  } else if (warp < 8) {
+  }
+  } else {
+    reg_alloc<kSplitWideRegs>();
     // ------------------------------------------------------------ P / dS warps
     const int wg = warp >> 2;             // query columns [64wg, 64wg+64)
     const int j = threadIdx.x & 127;      // key lane
@@ -452,16 +457,17 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
 // dQ pass
 // Work units: the halves of the planner's unsplit forward items, i.e. one
 // (q-tile, query head) with its visits in k-tile order.
-// Warp roles (320 threads): warps 0-7 dS warps in two warpgroups (thread =
+// Warp roles (384 threads): warps 0-7 dS warps in two warpgroups (thread =
 // query row = TMEM lane; warpgroup w owns key columns [64w, 64w+64)) and the
-// dQ epilogue, warp 8 TMA producer, warp 9 MMA issuer.
+// dQ epilogue, warp 8 TMA producer, warp 9 MMA issuer, warps 10-11 idle;
+// registers split 200 / 104 as in the dK/dV pass.
 // TMEM columns: S of even steps [0,128), of odd steps [128,256), dP
 // [256,384), dQ [384,384+D).  Warpgroup w writes its dS pairs over columns
 // [64w, 64w+32) of its step's S buffer (read by itself first); the dQ MMA
 // reads them from TMEM.
 template <int D>
 struct DqCfg {
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = kSplitThreads;
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kStages = 2;
@@ -556,6 +562,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, P.err, P.wait_ns};
 
+  if (warp >= 8) {
+  reg_dealloc<kSplitNarrowRegs>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -709,7 +717,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       mma_commit(bar(C::kBDrain));
       drain_wait_b(bar(C::kBDrain), 0, kDrainNs);
     }
-  } else if (warp < 8) {
+  }
+  } else {
+    reg_alloc<kSplitWideRegs>();
     // ------------------------------------------------------------ dS warps
     const int wg = warp >> 2;         // key columns [64wg, 64wg+64)
     const int t = threadIdx.x & 127;  // query row within the tile = TMEM lane
@@ -902,6 +912,7 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     if (cudaFuncSetAttribute(ffa_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return FFA_ERR_CUDA;
+    if (!split_regs_ok<ffa_bwd_dkdv_kernel<D>>()) return FFA_ERR_UNSUPPORTED;
     record_phase(p, 3, st);
     ffa_bwd_dkdv_kernel<D><<<p->grid_bwd, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, P);
     note_launches(1);
@@ -929,6 +940,7 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     if (cudaFuncSetAttribute(ffa_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return FFA_ERR_CUDA;
+    if (!split_regs_ok<ffa_bwd_dq_kernel<D>>()) return FFA_ERR_UNSUPPORTED;
     record_phase(p, 4, st);
     ffa_bwd_dq_kernel<D><<<p->grid_dq, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, P);
     note_launches(1);

@@ -5,25 +5,14 @@
 // item holds two 128-row halves (two query heads of one kv head, or two
 // consecutive q-tiles of one head) that share every K/V tile load.
 //
-// Warp roles (320 threads):
+// Warp roles (384 threads, three warpgroups):
 //   warps 0-3  softmax for half 0 (thread = query row = TMEM lane)
 //   warps 4-7  softmax for half 1
 //   warp  8    TMA producer: Q tiles, then a ring of K/V stages
 //   warp  9    tcgen05 MMA issuer (and TMEM owner)
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
-// P (bf16) is written back over the first 64 columns of S and read from TMEM
-// by the P*V MMA.
-//
-// Per k-tile step j, the MMA order is  PV0(j), S0(j+1), PV1(j), S1(j+1), so
-// one half's softmax overlaps the other half's MMAs.  Because tcgen05 MMAs
-// complete in issue order, the commit that announces S_h(j+1) also tells the
-// softmax warps that PV_h(j) is done, which is when O_h may be rescaled.
-//
-// Online softmax (fp32, base 2): m is the running row maximum of
-// scale*log2(e)*s; it is only raised when a new maximum exceeds it by more
-// than 8 (then O and l are rescaled), so p = 2^(x - m) stays below 256.
-// Masked entries become -inf (only on PARTIAL steps), a row with no visible
-// key keeps l = 0 and is written as out = 0, lse = -inf.
+//   warps 10-11 idle
+// Registers: the control warpgroup (warps 8-11) shrinks to 104 per thread
+// and the softmax warpgroups grow to 200 (the split in ffa_ptx.cuh).
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -33,7 +22,7 @@
 namespace ffa {
 namespace {
 
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = kSplitThreads;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
@@ -131,6 +120,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, P.err, P.wait_ns};
 
+  if (warp >= 8) {
+  reg_dealloc<kSplitNarrowRegs>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -289,7 +280,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mma_commit(bar(C::kBDrain));
       drain_wait(bar(C::kBDrain), 0, kDrainNs);
     }
-  } else if (warp < 8) {
+  }
+  } else {
+    reg_alloc<kSplitWideRegs>();
     // ------------------------------------------------------------ softmax
     const int h = warp >> 2;
     const int row_in = threadIdx.x & 127;
@@ -526,7 +519,7 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   if (cudaFuncSetAttribute(ffa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
     return FFA_ERR_CUDA;
-
+  if (!split_regs_ok<ffa_fwd_kernel<D>>()) return FFA_ERR_UNSUPPORTED;
   record_phase(p, 0, st);
   ffa_fwd_kernel<D><<<p->grid_fwd, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, P);
   note_launches(1);

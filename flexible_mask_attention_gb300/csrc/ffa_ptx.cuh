@@ -303,6 +303,30 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Register split of the 384-thread kernels (three warpgroups, one CTA per
+// SM).  They compile to 168 registers per thread (65536 / 384, rounded down
+// to a multiple of 8); the control warpgroup (producer, MMA issuer, two idle
+// warps) shrinks to 104 and the two elementwise warpgroups grow to 200:
+// 2 * 128 * 200 + 128 * 104 = 384 * 168, so the exchange always completes.
+constexpr int kSplitThreads = 384;
+constexpr int kSplitLaunchRegs = 168;
+constexpr int kSplitWideRegs = 200;
+constexpr int kSplitNarrowRegs = 104;
+static_assert(2 * 128 * kSplitWideRegs + 128 * kSplitNarrowRegs == kSplitThreads * kSplitLaunchRegs,
+              "register exchange between warpgroups must balance");
+
+// True when the kernel was built with exactly kSplitLaunchRegs registers per
+// thread; otherwise the register exchange above could block forever and the
+// kernel must not be launched.
+template <auto Kernel>
+inline bool split_regs_ok() {
+  static const int regs = [] {
+    cudaFuncAttributes fa;
+    return cudaFuncGetAttributes(&fa, Kernel) == cudaSuccess ? fa.numRegs : -1;
+  }();
+  return regs == kSplitLaunchRegs;
+}
+
 // Per-warpgroup register rebalancing; every warp of the warpgroup executes it.
 template <int N>
 __device__ __forceinline__ void reg_dealloc() {
