@@ -280,13 +280,21 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdAcc = idesc_bf16(128, D, false, true);  // A K-major, B MN-major
-      const uint32_t kA = sbase + C::kKOff, vA = sbase + C::kVOff, pA = sbase + C::kPOff;
-      auto issue_st = [&](uint32_t qA) {  // S^T = K Q^T
+      constexpr uint32_t kTile16 = C::kTileBytes >> 4;
+      // Base descriptors: K-major (k) and MN-major (m) views of each buffer.
+      const uint64_t dKk = sdesc_sw128(sbase + C::kKOff, 16, 1024);
+      const uint64_t dVk = sdesc_sw128(sbase + C::kVOff, 16, 1024);
+      const uint64_t dPk = sdesc_sw128(sbase + C::kPOff, 16, 1024);
+      const uint64_t dQk = sdesc_sw128(sbase + C::kQOff, 16, 1024);
+      const uint64_t dQm = sdesc_sw128(sbase + C::kQOff, 16384, 1024);
+      const uint64_t dDOk = sdesc_sw128(sbase + C::kDOOff, 16, 1024);
+      const uint64_t dDOm = sdesc_sw128(sbase + C::kDOOff, 16384, 1024);
+      auto issue_st = [&](int qstage) {  // S^T = K Q^T
+        const uint64_t qd = dQk + qstage * kTile16;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + C::kTS, sdesc_sw128(kA + off, 16, 1024), sdesc_sw128(qA + off, 16, 1024),
-                 kIdS, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;  // 16-byte units
+          mma_ss_at(tmem + C::kTS, dKk, off, qd, off, kIdS, kk > 0 ? 1u : 0u);
         }
       };
       uint32_t kv_cnt = 0, q_cnt = 0, sf_cnt = 0, p_cnt = 0, dkv_cnt = 0;
@@ -303,22 +311,22 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
           const int stage = q_cnt % C::kStages;
           if (!(ok = mbar_wait(bar(C::kBQFull + stage), (q_cnt / C::kStages) & 1, ctl, 501))) break;
           tc_fence_after();
-          issue_st(sbase + C::kQOff + stage * C::kTileBytes);
+          issue_st(stage);
         }
         for (int i = 0; i < n_it; ++i) {
           const uint32_t c = q_cnt + (uint32_t)i;
           const int stage = c % C::kStages;
           const uint32_t ph = (c / C::kStages) & 1;
-          const uint32_t qA = sbase + C::kQOff + stage * C::kTileBytes;
-          const uint32_t doA = sbase + C::kDOOff + stage * C::kTileBytes;
           if (!(ok = mbar_wait(bar(C::kBDOFull + stage), ph, ctl, 502))) break;
           tc_fence_after();
           // dP^T = V dO^T; its columns were last read by the previous dK MMA.
+          {
+            const uint64_t dod = dDOk + stage * kTile16;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tmem + C::kTdP, sdesc_sw128(vA + off, 16, 1024),
-                   sdesc_sw128(doA + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
+              mma_ss_at(tmem + C::kTdP, dVk, off, dod, off, kIdS, kk > 0 ? 1u : 0u);
+            }
           }
           mma_commit(bar(C::kBSdpFull));
           if (i + 1 < n_it) {
@@ -329,7 +337,7 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
             ++sf_cnt;
             if (!(ok = mbar_wait(bar(C::kBQFull + st1), (c1 / C::kStages) & 1, ctl, 504))) break;
             tc_fence_after();
-            issue_st(sbase + C::kQOff + st1 * C::kTileBytes);
+            issue_st(st1);
           }
           if (!(ok = mbar_wait(bar(C::kBPFull), p_cnt & 1, ctl, 505))) break;
           ++p_cnt;
@@ -340,15 +348,16 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
             tc_fence_after();
           }
           const uint32_t acc0 = i > 0 ? 1u : 0u;
+          const uint64_t dom = dDOm + stage * kTile16;
+          const uint64_t qm = dQm + stage * kTile16;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t poff = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tmem + C::kTdV, sdesc_sw128(pA + poff, 16, 1024),
-                   sdesc_sw128(doA + kk * 2048, 16384, 1024), kIdAcc, (acc0 || kk > 0) ? 1u : 0u);
+            const uint32_t poff = (kk >> 2) * 1024 + (kk & 3) * 2;
+            mma_ss_at(tmem + C::kTdV, dPk, poff, dom, kk * 128, kIdAcc, (acc0 || kk > 0) ? 1u : 0u);
             // dS^T pairs of queries [16kk, 16kk+16): warpgroup kk/4 wrote them at
             // dP^T column 64*(kk/4) + 8*(kk%4)
-            mma_ts(tmem + C::kTdK, tmem + C::kTdP + 64 * (kk >> 2) + 8 * (kk & 3),
-                   sdesc_sw128(qA + kk * 2048, 16384, 1024), kIdAcc, (acc0 || kk > 0) ? 1u : 0u);
+            mma_ts_at(tmem + C::kTdK, tmem + C::kTdP + 64 * (kk >> 2) + 8 * (kk & 3), qm, kk * 128,
+                      kIdAcc, (acc0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(bar(C::kBDOEmpty + stage));
           mma_commit(bar(C::kBQEmpty + stage));
@@ -628,23 +637,26 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);  // A from TMEM, B MN-major
-      const uint32_t qA = sbase + C::kQOff, doA = sbase + C::kDOOff;
+      constexpr uint32_t kTile16 = C::kTileBytes >> 4;
+      const uint64_t dQk = sdesc_sw128(sbase + C::kQOff, 16, 1024);
+      const uint64_t dDOk = sdesc_sw128(sbase + C::kDOOff, 16, 1024);
+      const uint64_t dKk = sdesc_sw128(sbase + C::kKOff, 16, 1024);
+      const uint64_t dKm = sdesc_sw128(sbase + C::kKOff, 16384, 1024);
+      const uint64_t dVk = sdesc_sw128(sbase + C::kVOff, 16, 1024);
       auto issue_s = [&](int buf, int stage) {  // S = Q K^T
-        const uint32_t ka = sbase + C::kKOff + stage * C::kTileBytes;
+        const uint64_t kd = dKk + stage * kTile16;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + C::kTS0 + 128 * buf, sdesc_sw128(qA + off, 16, 1024),
-                 sdesc_sw128(ka + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;  // 16-byte units
+          mma_ss_at(tmem + C::kTS0 + 128 * buf, dQk, off, kd, off, kIdS, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_dp = [&](int stage) {  // dP = dO V^T
-        const uint32_t va = sbase + C::kVOff + stage * C::kTileBytes;
+        const uint64_t vd = dVk + stage * kTile16;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + C::kTdP, sdesc_sw128(doA + off, 16, 1024),
-                 sdesc_sw128(va + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
+          mma_ss_at(tmem + C::kTdP, dDOk, off, vd, off, kIdS, kk > 0 ? 1u : 0u);
         }
       };
       uint32_t kv_cnt = 0, q_cnt = 0, dpf_cnt = 0, ds_cnt = 0, dqe_cnt = 0;
@@ -697,11 +709,11 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
               ++dqe_cnt;
               tc_fence_after();
             }
-            const uint32_t ka = sbase + C::kKOff + stage * C::kTileBytes;
+            const uint64_t km = dKm + stage * kTile16;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)  // dS pairs of keys [16kk, 16kk+16)
-              mma_ts(tmem + C::kTdQ, tmem + C::kTS0 + 128 * (v & 1) + 64 * (kk >> 2) + 8 * (kk & 3),
-                     sdesc_sw128(ka + kk * 2048, 16384, 1024), kIdQ, (v > 0 || kk > 0) ? 1u : 0u);
+              mma_ts_at(tmem + C::kTdQ, tmem + C::kTS0 + 128 * (v & 1) + 64 * (kk >> 2) + 8 * (kk & 3),
+                        km, kk * 128, kIdQ, (v > 0 || kk > 0) ? 1u : 0u);
             mma_commit(bar(C::kBKEmpty + stage));
             mma_commit(bar(C::kBVEmpty + stage));
           }

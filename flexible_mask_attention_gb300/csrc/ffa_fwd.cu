@@ -13,6 +13,20 @@
 //   warps 10-11 idle
 // Registers: the control warpgroup (warps 8-11) shrinks to 104 per thread
 // and the softmax warpgroups grow to 200 (the split in ffa_ptx.cuh).
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
+// P (bf16) is written back over the first 64 columns of S and read from TMEM
+// by the P*V MMA.
+//
+// Per k-tile step j, the MMA order is  PV0(j), S0(j+1), PV1(j), S1(j+1), so
+// one half's softmax overlaps the other half's MMAs.  Because tcgen05 MMAs
+// complete in issue order, the commit that announces S_h(j+1) also tells the
+// softmax warps that PV_h(j) is done, which is when O_h may be rescaled.
+//
+// Online softmax (fp32, base 2): m is the running row maximum of
+// scale*log2(e)*s; it is only raised when a new maximum exceeds it by more
+// than 8 (then O and l are rescaled), so p = 2^(x - m) stays below 256.
+// Masked entries become -inf (only on PARTIAL steps), a row with no visible
+// key keeps l = 0 and is written as out = 0, lse = -inf.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -181,22 +195,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
+      constexpr uint32_t kTile16 = C::kTileBytes >> 4;
+      const uint64_t dQ = sdesc_sw128(sbase + C::kQOff, 16, 1024);     // K-major
+      const uint64_t dK = sdesc_sw128(sbase + C::kKOff, 16, 1024);     // K-major
+      const uint64_t dV = sdesc_sw128(sbase + C::kVOff, 16384, 1024);  // MN-major
       auto issue_s = [&](int h, int stage) {
-        const uint32_t qa = sbase + C::kQOff + h * C::kTileBytes;
-        const uint32_t ka = sbase + C::kKOff + stage * C::kTileBytes;
+        const uint64_t qd = dQ + h * kTile16, kd = dK + stage * kTile16;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + h * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                 kIdS, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;  // 16-byte units
+          mma_ss_at(tmem + h * 128, qd, off, kd, off, kIdS, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int h, int stage, bool acc) {
-        const uint32_t va = sbase + C::kVOff + stage * C::kTileBytes;
+        const uint64_t vd = dV + stage * kTile16;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + 256 + h * 128, tmem + h * 128 + kk * 8,
-                 sdesc_sw128(va + kk * 2048, 16384, 1024), kIdPV, (acc || kk > 0) ? 1u : 0u);
+          mma_ts_at(tmem + 256 + h * 128, tmem + h * 128 + kk * 8, vd, kk * 128, kIdPV,
+                    (acc || kk > 0) ? 1u : 0u);
       };
       uint32_t kv_cnt = 0, q_cnt = 0, p_cnt[2] = {0, 0}, oe_cnt[2] = {0, 0};
       bool ok = true;

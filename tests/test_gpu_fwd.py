@@ -71,3 +71,20 @@ def test_large_scores_rescale():
     _, out, lse = run_fwd(q, k, v, qr, kr, ty)
     ro, rl = oracle.fwd(q, k, v, qr, kr, ty)
     check_fwd(out, lse, ro, rl)
+
+
+def test_scores_far_below_zero():
+    """Every visible score lies far below 0 (q ~ +1, k ~ -1): the running
+    maximum starts far under the scale of the first tile's values, and the
+    result must not underflow to an empty row."""
+    import torch
+    T, H, D = 700, 2, 128
+    g = torch.Generator().manual_seed(11)
+    q = (1.0 + 0.1 * torch.randn(T, H, D, generator=g)).to(torch.bfloat16)
+    k = (-1.0 + 0.1 * torch.randn(T, H, D, generator=g)).to(torch.bfloat16)
+    v = bf16(T, H, D, seed=12)
+    qr, kr, ty = [[0, 400], [400, T]], [[0, 400], [0, T]], [1, 0]
+    _, out, lse = run_fwd(q, k, v, qr, kr, ty)
+    ro, rl = oracle.fwd(q, k, v, qr, kr, ty)
+    assert np.isfinite(lse).all() and (lse < -3).all()
+    check_fwd(out, lse, ro, rl)
