@@ -6,7 +6,9 @@ the product package: the two share only the seeded input generators.
 
 Contents
   * ``fwd`` / ``bwd``: the fp64 C oracle (``ffa_oracle.c``), the
-    masked-softmax definition written out, on all rows/keys or a subset.
+    masked-softmax definition written out, on all rows/keys or a subset,
+    optionally with attention-sink logits in the normaliser; ``dsink`` their
+    gradient.
   * ``lse_merge``: combination of partial (out, lse) pairs with a global
     logsumexp (FlagAttention user guide, "Split-KV and paged attention").
   * ``dense``: a numpy brute force over an explicit Tq x Tk mask built from a
@@ -50,11 +52,13 @@ def load_library(path: str):
     L = ctypes.c_long
     I = ctypes.c_int
     D = ctypes.c_double
-    lib.ffa_oracle_fwd.argtypes = [P, P, P, L, L, I, I, I, P, P, P, I, D, P, L, P, P]
+    lib.ffa_oracle_fwd.argtypes = [P, P, P, L, L, I, I, I, P, P, P, I, D, P, I, I, P, L, P, P]
     lib.ffa_oracle_fwd.restype = I
-    lib.ffa_oracle_bwd.argtypes = [P, P, P, P, L, L, I, I, I, P, P, P, I, D,
+    lib.ffa_oracle_bwd.argtypes = [P, P, P, P, L, L, I, I, I, P, P, P, I, D, P, I, I,
                                    P, L, P, P, L, P, P]
     lib.ffa_oracle_bwd.restype = I
+    lib.ffa_oracle_dsink.argtypes = [P, P, P, P, L, L, I, I, I, P, P, P, I, D, P, I, I, P, L, P]
+    lib.ffa_oracle_dsink.restype = I
     lib.ffa_oracle_num_threads.restype = I
     return lib
 
@@ -89,8 +93,27 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
-def fwd(q, k, v, q_ranges, k_ranges, mask_types, softmax_scale=None, rows=None, lib=None):
-    """fp64 forward. Returns (out[n, Hq, D], lse[Hq, n]) for ``rows`` (all by default)."""
+_LAYOUTS = {"sh": 0, "ssh": 1}
+
+
+def _sink(sink, sink_layout, Tq, Hq):
+    """(fp64 array or None, n_sink, layout code) for an optional sink tensor."""
+    if sink is None:
+        return None, 0, 0
+    code = _LAYOUTS[sink_layout]
+    a = np.ascontiguousarray(np.asarray(sink.detach().cpu() if hasattr(sink, "detach") else sink,
+                                        dtype=np.float64))
+    if code == 0 and (a.ndim != 2 or a.shape[1] != Hq):
+        raise ValueError("sink layout 'sh' wants [n_sink, Hq]")
+    if code == 1 and (a.ndim != 3 or a.shape[0] != Tq or a.shape[2] != Hq):
+        raise ValueError("sink layout 'ssh' wants [Tq, n_sink, Hq]")
+    return a, a.shape[-2], code
+
+
+def fwd(q, k, v, q_ranges, k_ranges, mask_types, softmax_scale=None, rows=None, lib=None, *,
+        sink=None, sink_layout="sh"):
+    """fp64 forward. Returns (out[n, Hq, D], lse[Hq, n]) for ``rows`` (all by default).
+    ``sink``: optional fp32 sink logits, [n_sink, Hq] ("sh") or [Tq, n_sink, Hq] ("ssh")."""
     qn, kn, vn = _u16(q), _u16(k), _u16(v)
     Tq, Hq, D = qn.shape
     Tk, Hkv, _ = kn.shape
@@ -98,10 +121,12 @@ def fwd(q, k, v, q_ranges, k_ranges, mask_types, softmax_scale=None, rows=None, 
     qr, kr, ty = _i32(q_ranges).reshape(-1, 2), _i32(k_ranges).reshape(-1, 2), _i32(mask_types)
     rows_a = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     n = Tq if rows_a is None else rows_a.shape[0]
+    sk, ns, lay = _sink(sink, sink_layout, Tq, Hq)
     out = np.zeros((n, Hq, D), np.float64)
     lse = np.zeros((Hq, n), np.float64)
     rc = (lib or _load()).ffa_oracle_fwd(_ptr(qn), _ptr(kn), _ptr(vn), Tq, Tk, Hq, Hkv, D, _ptr(qr),
                                 _ptr(kr), _ptr(ty), ty.shape[0], scale,
+                                None if sk is None else _ptr(sk), ns, lay,
                                 None if rows_a is None else _ptr(rows_a), n, _ptr(out), _ptr(lse))
     if rc != 0:
         raise ValueError("oracle: bad arguments")
@@ -109,7 +134,7 @@ def fwd(q, k, v, q_ranges, k_ranges, mask_types, softmax_scale=None, rows=None, 
 
 
 def bwd(q, k, v, dout, q_ranges, k_ranges, mask_types, softmax_scale=None,
-        dq_rows=None, dkv_keys=None, lib=None):
+        dq_rows=None, dkv_keys=None, lib=None, *, sink=None, sink_layout="sh"):
     """fp64 backward. Returns (dq[nq, Hq, D], dk[nk, Hkv, D], dv[nk, Hkv, D])."""
     qn, kn, vn, dn = _u16(q), _u16(k), _u16(v), _u16(dout)
     Tq, Hq, D = qn.shape
@@ -123,13 +148,36 @@ def bwd(q, k, v, dout, q_ranges, k_ranges, mask_types, softmax_scale=None,
     dq = np.zeros((nq, Hq, D), np.float64)
     dk = np.zeros((nk, Hkv, D), np.float64)
     dv = np.zeros((nk, Hkv, D), np.float64)
+    sk, ns, lay = _sink(sink, sink_layout, Tq, Hq)
     rc = (lib or _load()).ffa_oracle_bwd(_ptr(qn), _ptr(kn), _ptr(vn), _ptr(dn), Tq, Tk, Hq, Hkv, D,
                                 _ptr(qr), _ptr(kr), _ptr(ty), ty.shape[0], scale,
+                                None if sk is None else _ptr(sk), ns, lay,
                                 None if rq is None else _ptr(rq), nq, _ptr(dq),
                                 None if rk is None else _ptr(rk), nk, _ptr(dk), _ptr(dv))
     if rc != 0:
         raise ValueError("oracle: bad arguments")
     return dq, dk, dv
+
+
+def dsink(q, k, v, dout, q_ranges, k_ranges, mask_types, sink, sink_layout="sh",
+          softmax_scale=None, rows=None, lib=None):
+    """fp64 gradient of the sink logits: [n_sink, Hq] ("sh", summed over all
+    rows) or [n, n_sink, Hq] for ``rows`` ("ssh", all rows by default)."""
+    qn, kn, vn, dn = _u16(q), _u16(k), _u16(v), _u16(dout)
+    Tq, Hq, D = qn.shape
+    Tk, Hkv, _ = kn.shape
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    qr, kr, ty = _i32(q_ranges).reshape(-1, 2), _i32(k_ranges).reshape(-1, 2), _i32(mask_types)
+    sk, ns, lay = _sink(sink, sink_layout, Tq, Hq)
+    rows_a = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = Tq if rows_a is None else rows_a.shape[0]
+    out = np.zeros((ns, Hq) if lay == 0 else (n, ns, Hq), np.float64)
+    rc = (lib or _load()).ffa_oracle_dsink(_ptr(qn), _ptr(kn), _ptr(vn), _ptr(dn), Tq, Tk, Hq, Hkv,
+                                  D, _ptr(qr), _ptr(kr), _ptr(ty), ty.shape[0], scale, _ptr(sk),
+                                  ns, lay, None if rows_a is None else _ptr(rows_a), n, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle: bad arguments")
+    return out
 
 
 def lse_merge(lse_parts, out_parts):

@@ -28,6 +28,19 @@
  * delta_i = <dO_i, O_i>, dS = P (dP - delta), dQ_i = scale sum_j dS_ij k_j,
  * dK_j = scale sum_i dS_ij q_i, summed over the query heads of a kv head.
  *
+ * Attention sink (quickstart card "Single-GPU Flex-Flash-Attention", the
+ * `sink` argument, and the FlashAttention-with-sink cards, layouts "sh"
+ * [n_sink][Hq] and "ssh" [Tq][n_sink][Hq], fp32).  The pages show the
+ * argument but not its formula; the reading used here: each sink value
+ * sigma_s is a logit, not multiplied by the softmax scale, that joins the
+ * row's normaliser only,
+ *     lse_i = log( sum_j exp(x_j) + sum_s exp(sigma_s) ),
+ *     out_i = sum_j exp(x_j - lse_i) v_j,
+ * so a row that sees no key gets out = 0 and lse = log sum_s exp(sigma_s).
+ * Its gradient follows from that definition:
+ *     dsink_s = - sum_i exp(sigma_s - lse_i) delta_i
+ * (summed over the rows of the head for "sh", one value per row for "ssh").
+ *
  * Every loop below is the definition written out, with no blocking, fusion or
  * reordering.  OpenMP only splits independent (head, row) or (head, key)
  * pairs across threads.
@@ -98,7 +111,16 @@ typedef struct {
   const slice_t* sl;
   int ns;
   double scale;
+  const double* sink; /* NULL: no sink */
+  int n_sink;
+  int sink_layout;    /* 0: [n_sink][Hq], 1: [Tq][n_sink][Hq] */
 } problem_t;
+
+/* Sink logit s of (head h, row i). */
+static double sink_value(const problem_t* P, int h, long i, int s) {
+  if (P->sink_layout == 0) return P->sink[(size_t)s * P->Hq + h];
+  return P->sink[((size_t)i * P->n_sink + s) * P->Hq + h];
+}
 
 /* Forward for one (head, row): fills out_row[D] and returns lse.
  * xbuf holds Tk doubles (scores of the visible keys), vis holds Tk flags. */
@@ -122,12 +144,20 @@ static double row_forward(const problem_t* P, int h, long i, double* out_row, do
     if (xbuf[j] > m) m = xbuf[j];
     ++cnt;
   }
+  /* sink logits join the normaliser (and its maximum, for a stable sum) */
+  const int ns = P->sink ? P->n_sink : 0;
+  for (int s = 0; s < ns; ++s) {
+    const double sv = sink_value(P, h, i, s);
+    if (sv > m) m = sv;
+  }
   for (int t = 0; t < D; ++t) out_row[t] = 0.0;
-  if (cnt == 0) return -INFINITY;
+  if (m == -INFINITY) return -INFINITY; /* no visible key and no (finite) sink */
   double sum = 0.0;
   for (long j = 0; j < P->Tk; ++j)
     if (vis[j]) sum += exp(xbuf[j] - m);
+  for (int s = 0; s < ns; ++s) sum += exp(sink_value(P, h, i, s) - m);
   const double lse = m + log(sum);
+  if (cnt == 0) return lse;
   for (long j = 0; j < P->Tk; ++j) {
     if (!vis[j]) continue;
     const double p = exp(xbuf[j] - lse);
@@ -149,11 +179,13 @@ int ffa_oracle_num_threads(void) {
  * out: [n_rows][Hq][D], lse: [Hq][n_rows]. */
 int ffa_oracle_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, long Tq, long Tk,
                    int Hq, int Hkv, int D, const int* q_ranges, const int* k_ranges,
-                   const int* mask_types, int num_slices, double scale, const long* rows,
-                   long n_rows, double* out, double* lse) {
+                   const int* mask_types, int num_slices, double scale, const double* sink,
+                   int n_sink, int sink_layout, const long* rows, long n_rows, double* out,
+                   double* lse) {
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0) return 1;
+  if (n_sink < 0 || (n_sink > 0 && !sink) || sink_layout < 0 || sink_layout > 1) return 1;
   slice_t* sl = read_slices(q_ranges, k_ranges, mask_types, num_slices);
-  problem_t P = {q, k, v, Tq, Tk, Hq, Hkv, D, sl, num_slices, scale};
+  problem_t P = {q, k, v, Tq, Tk, Hq, Hkv, D, sl, num_slices, scale, sink, n_sink, sink_layout};
   const long n = rows ? n_rows : Tq;
 #pragma omp parallel
   {
@@ -179,11 +211,13 @@ int ffa_oracle_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, long
 int ffa_oracle_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
                    long Tq, long Tk, int Hq, int Hkv, int D, const int* q_ranges,
                    const int* k_ranges, const int* mask_types, int num_slices, double scale,
-                   const long* dq_rows, long n_dq_rows, double* dq, const long* dkv_keys,
-                   long n_keys, double* dk, double* dv) {
+                   const double* sink, int n_sink, int sink_layout, const long* dq_rows,
+                   long n_dq_rows, double* dq, const long* dkv_keys, long n_keys, double* dk,
+                   double* dv) {
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0) return 1;
+  if (n_sink < 0 || (n_sink > 0 && !sink) || sink_layout < 0 || sink_layout > 1) return 1;
   slice_t* sl = read_slices(q_ranges, k_ranges, mask_types, num_slices);
-  problem_t P = {q, k, v, Tq, Tk, Hq, Hkv, D, sl, num_slices, scale};
+  problem_t P = {q, k, v, Tq, Tk, Hq, Hkv, D, sl, num_slices, scale, sink, n_sink, sink_layout};
   const int g = Hq / Hkv;
   const long nq = dq_rows ? n_dq_rows : Tq;
   const long nk = dkv_keys ? n_keys : Tk;
@@ -288,6 +322,59 @@ int ffa_oracle_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
     free(lse_all);
     free(delta_all);
   }
+  free(sl);
+  return 0;
+}
+
+/* Gradient of the sink logits: dsink_s = - sum_i exp(sigma_s - lse_i) delta_i,
+ * with the oracle's own lse and O.  Layout 0 ([n_sink][Hq]): summed over all
+ * rows of the head, in row order; layout 1 ([Tq][n_sink][Hq]): one value per
+ * row, for the rows in `rows` (NULL: all) -> dsink[n][n_sink][Hq]. */
+int ffa_oracle_dsink(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     const uint16_t* dout, long Tq, long Tk, int Hq, int Hkv, int D,
+                     const int* q_ranges, const int* k_ranges, const int* mask_types,
+                     int num_slices, double scale, const double* sink, int n_sink,
+                     int sink_layout, const long* rows, long n_rows, double* dsink) {
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0) return 1;
+  if (n_sink <= 0 || !sink || sink_layout < 0 || sink_layout > 1) return 1;
+  if (sink_layout == 0 && rows) return 1; /* a per-head sum needs every row */
+  slice_t* sl = read_slices(q_ranges, k_ranges, mask_types, num_slices);
+  problem_t P = {q, k, v, Tq, Tk, Hq, Hkv, D, sl, num_slices, scale, sink, n_sink, sink_layout};
+  const long n = rows ? n_rows : Tq;
+  /* per (row, head, sink) term, then the sums in a fixed order */
+  double* term = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * Hq * n_sink);
+#pragma omp parallel
+  {
+    double* xbuf = (double*)malloc(sizeof(double) * (size_t)(Tk > 0 ? Tk : 1));
+    unsigned char* vis = (unsigned char*)malloc((size_t)(Tk > 0 ? Tk : 1));
+    double* o = (double*)malloc(sizeof(double) * D);
+#pragma omp for schedule(dynamic, 4)
+    for (long w = 0; w < n * Hq; ++w) {
+      const long r = w / Hq;
+      const int h = (int)(w % Hq);
+      const long i = rows ? rows[r] : r;
+      const double lse = row_forward(&P, h, i, o, xbuf, vis);
+      const uint16_t* doi = dout + ((size_t)i * Hq + h) * D;
+      double delta = 0.0;
+      for (int t = 0; t < D; ++t) delta += bf16_to_double(doi[t]) * o[t];
+      for (int s = 0; s < n_sink; ++s)
+        term[((size_t)r * n_sink + s) * Hq + h] = -exp(sink_value(&P, h, i, s) - lse) * delta;
+    }
+    free(xbuf);
+    free(vis);
+    free(o);
+  }
+  if (sink_layout == 0) {
+    for (int s = 0; s < n_sink; ++s)
+      for (int h = 0; h < Hq; ++h) {
+        double acc = 0.0;
+        for (long r = 0; r < n; ++r) acc += term[((size_t)r * n_sink + s) * Hq + h];
+        dsink[(size_t)s * Hq + h] = acc;
+      }
+  } else {
+    memcpy(dsink, term, sizeof(double) * (size_t)n * Hq * n_sink);
+  }
+  free(term);
   free(sl);
   return 0;
 }
