@@ -19,10 +19,14 @@ __all__ = [
     "library_path", "load_library", "ffa_plan_create", "ffa_plan_destroy", "ffa_plan_info",
     "ffa_plan_export", "ffa_fwd_workspace_size", "ffa_bwd_workspace_size", "ffa_fwd", "ffa_bwd",
     "ffa_get_last_device_error", "ffa_plan_set_wait_limit", "ffa_kernel_launch_count",
-    "ffa_bwd_noalloc", "ffa_plan_set_events", "EXPORTED_SYMBOLS",
+    "ffa_bwd_noalloc", "ffa_plan_set_events", "ffa_fwd_ex", "ffa_bwd_ex", "FFA_SINK_SH",
+    "FFA_SINK_SSH", "FFA_MAX_SINK", "EXPORTED_SYMBOLS",
 ]
 
 FFA_FULL, FFA_CAUSAL, FFA_INV_CAUSAL, FFA_BI_CAUSAL = 0, 1, 2, 3
+FFA_SINK_SH, FFA_SINK_SSH = 0, 1  # sink layouts [n_sink, Hq] and [Tq, n_sink, Hq]
+FFA_MAX_SINK = 64
+_SINK_LAYOUTS = {"sh": FFA_SINK_SH, "ssh": FFA_SINK_SSH}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _STATUS = {0: "ok", 1: "invalid argument", 2: "slice range out of bounds or bad mask type",
@@ -34,7 +38,7 @@ EXPORTED_SYMBOLS = [
     "ffa_fwd_workspace_size", "ffa_bwd_workspace_size", "ffa_fwd", "ffa_bwd",
     "ffa_get_last_device_error", "ffa_plan_set_wait_limit", "ffa_status_string",
     "ffa_kernel_launch_count", "ffa_bwd_noalloc", "ffa_bwd_noalloc_max_workspace",
-    "ffa_plan_set_events",
+    "ffa_plan_set_events", "ffa_fwd_ex", "ffa_bwd_ex",
 ]
 
 
@@ -81,6 +85,8 @@ def load_library():
     lib.ffa_bwd_workspace_size.restype = S
     lib.ffa_fwd.argtypes = [P, P, P, P, F, P, P, P, S, P]
     lib.ffa_bwd.argtypes = [P, P, P, P, P, P, P, F, P, P, P, P, S, P]
+    lib.ffa_fwd_ex.argtypes = [P, P, P, P, P, I32, I32, F, P, P, P, S, P]
+    lib.ffa_bwd_ex.argtypes = [P, P, P, P, P, P, P, P, I32, I32, F, P, P, P, P, P, S, P]
     lib.ffa_get_last_device_error.argtypes = [P, ctypes.POINTER(I32), ctypes.POINTER(I32), P]
     lib.ffa_plan_set_wait_limit.argtypes = [P, U64]
     lib.ffa_plan_set_events.argtypes = [P, ctypes.POINTER(P), I32]
@@ -260,6 +266,75 @@ def ffa_bwd(plan: Plan, q, k, v, out, dout, lse, dq=None, dk=None, dv=None, soft
                                              _ptr(dout), _ptr(lse), scale, _ptr(dq), _ptr(dk),
                                              _ptr(dv), _ptr(ws), nbytes, _stream(stream)))
     return dq, dk, dv
+
+
+def _sink_args(plan: Plan, sink, sink_layout):
+    """(pointer, num_sink, layout code) of an optional fp32 sink tensor."""
+    if sink is None:
+        return None, 0, FFA_SINK_SH
+    if sink_layout not in _SINK_LAYOUTS:
+        raise ValueError("sink_layout must be 'sh' or 'ssh'")
+    code = _SINK_LAYOUTS[sink_layout]
+    Tq, Hq = plan.total_q, plan.num_heads_q
+    if not (sink.is_cuda and sink.dtype == torch.float32 and sink.is_contiguous()):
+        raise ValueError("sink must be a contiguous fp32 CUDA tensor")
+    if code == FFA_SINK_SH and (sink.dim() != 2 or sink.shape[1] != Hq):
+        raise ValueError(f"sink layout 'sh' wants [n_sink, {Hq}], got {tuple(sink.shape)}")
+    if code == FFA_SINK_SSH and (sink.dim() != 3 or sink.shape[0] != Tq or sink.shape[2] != Hq):
+        raise ValueError(f"sink layout 'ssh' wants [{Tq}, n_sink, {Hq}], got {tuple(sink.shape)}")
+    return _ptr(sink), int(sink.shape[-2]), code
+
+
+def ffa_fwd_ex(plan: Plan, q, k, v, sink=None, sink_layout="sh", out=None, lse=None,
+               softmax_scale=None, workspace=None, stream=None):
+    """ffa_fwd with optional attention-sink logits (fp32, [n_sink, Hq] for
+    "sh" or [Tq, n_sink, Hq] for "ssh"); lse includes the sink term."""
+    Tq, Tk, Hq, Hkv, D = (plan.total_q, plan.total_k, plan.num_heads_q, plan.num_heads_kv,
+                          plan.head_dim)
+    _need(q, "q", torch.bfloat16, (Tq, Hq, D))
+    _need(k, "k", torch.bfloat16, (Tk, Hkv, D))
+    _need(v, "v", torch.bfloat16, (Tk, Hkv, D))
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty(Hq, Tq, dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(out, "out", torch.bfloat16, (Tq, Hq, D))
+    _need(lse, "lse", torch.float32, (Hq, Tq))
+    sp, ns, lay = _sink_args(plan, sink, sink_layout)
+    nbytes = ffa_fwd_workspace_size(plan)
+    ws = _workspace(nbytes, q.device, workspace)
+    scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    _check("ffa_fwd_ex", load_library().ffa_fwd_ex(plan.handle, _ptr(q), _ptr(k), _ptr(v), sp, ns,
+                                                   lay, scale, _ptr(out), _ptr(lse), _ptr(ws),
+                                                   nbytes, _stream(stream)))
+    return out, lse
+
+
+def ffa_bwd_ex(plan: Plan, q, k, v, out, dout, lse, sink=None, sink_layout="sh", dq=None,
+               dk=None, dv=None, dsink=None, softmax_scale=None, workspace=None, stream=None):
+    """Backward of ffa_fwd_ex: (dq, dk, dv, dsink); dsink is None without a sink."""
+    Tq, Tk, Hq, Hkv, D = (plan.total_q, plan.total_k, plan.num_heads_q, plan.num_heads_kv,
+                          plan.head_dim)
+    for t, n, s in ((q, "q", (Tq, Hq, D)), (k, "k", (Tk, Hkv, D)), (v, "v", (Tk, Hkv, D)),
+                    (out, "out", (Tq, Hq, D)), (dout, "dout", (Tq, Hq, D))):
+        _need(t, n, torch.bfloat16, s)
+    _need(lse, "lse", torch.float32, (Hq, Tq))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, n, s in ((dq, "dq", (Tq, Hq, D)), (dk, "dk", (Tk, Hkv, D)), (dv, "dv", (Tk, Hkv, D))):
+        _need(t, n, torch.bfloat16, s)
+    sp, ns, lay = _sink_args(plan, sink, sink_layout)
+    if ns > 0 and dsink is None:
+        dsink = torch.empty_like(sink)
+    if dsink is not None:
+        _need(dsink, "dsink", torch.float32, tuple(sink.shape))
+    nbytes = ffa_bwd_workspace_size(plan)
+    ws = _workspace(nbytes, q.device, workspace)
+    scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    _check("ffa_bwd_ex", load_library().ffa_bwd_ex(
+        plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), sp, ns, lay,
+        scale, _ptr(dq), _ptr(dk), _ptr(dv), None if dsink is None else _ptr(dsink), _ptr(ws),
+        nbytes, _stream(stream)))
+    return dq, dk, dv, (dsink if ns > 0 else None)
 
 
 def ffa_bwd_noalloc(plan: Plan, q, k, v, out, dout, lse, dq, dk, dv, softmax_scale=None,

@@ -880,10 +880,49 @@ __global__ void ffa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
   ndelta[(size_t)h * qpad + q] = -dsum;
 }
 
+// Gradient of the attention-sink logits, which enter only the normaliser:
+//   dsink_s = -sum_i exp(sink_s - lse_i) delta_i = sum_i 2^(sink_s log2 e + nlse2_i) ndelta_i
+// over the rows i of the head (nlse2 = -lse log2 e and ndelta = -delta from
+// the preprocess kernel).  Layout 0 ([n][Hq]): one block per (s, head), each
+// thread sums a fixed stride of rows and the block adds the partial sums in a
+// fixed tree, so the result does not depend on scheduling.  Layout 1
+// ([Tq][n][Hq]): one thread per element, no sum.
+__global__ void __launch_bounds__(256)
+    ffa_dsink_kernel(const float* __restrict__ sink, int n, int layout, int Tq, int Hq, int qpad,
+                     const float* __restrict__ nlse2, const float* __restrict__ ndelta,
+                     float* __restrict__ dsink) {
+  if (layout == 0) {
+    __shared__ float red[256];
+    const int s = blockIdx.x / Hq, h = blockIdx.x % Hq;
+    const float sg = sink[(size_t)s * Hq + h] * kLog2e;
+    const float* nl = nlse2 + (size_t)h * qpad;
+    const float* nd = ndelta + (size_t)h * qpad;
+    float acc = 0.f;
+    for (int i = threadIdx.x; i < Tq; i += 256) {
+      const float e = sg + nl[i];
+      if (e > -INFINITY && e < INFINITY) acc = fmaf(exp2f(e), nd[i], acc);
+    }
+    red[threadIdx.x] = acc;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+      if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) dsink[(size_t)s * Hq + h] = red[0];
+  } else {
+    const long long idx = (long long)blockIdx.x * 256 + threadIdx.x;  // (row * n + s) * Hq + h
+    if (idx >= (long long)Tq * n * Hq) return;
+    const int h = (int)(idx % Hq), i = (int)(idx / Hq / n);
+    const float e = sink[idx] * kLog2e + nlse2[(size_t)h * qpad + i];
+    dsink[idx] = (e > -INFINITY && e < INFINITY) ? exp2f(e) * ndelta[(size_t)h * qpad + i] : 0.f;
+  }
+}
+
 template <int D>
 ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const void* v,
                           const void* out, const void* dout, const float* lse, float scale,
-                          void* dq, void* dk, void* dv, void* ws, cudaStream_t st) {
+                          void* dq, void* dk, void* dv, void* ws, cudaStream_t st,
+                          const SinkArgs& sk, float* dsink) {
   const int qpad = p->n_qt * 128;
   float* nlse2 = static_cast<float*>(ws);
   float* ndelta = nlse2 + (size_t)p->Hq * qpad;
@@ -895,6 +934,17 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
         p->Tq, p->Hq, qpad, nlse2, ndelta);
     note_launches(1);
     if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
+  }
+  if (sk.n > 0 && dsink) {
+    const unsigned blocks =
+        sk.layout == 0 ? (unsigned)(sk.n * p->Hq)
+                       : (unsigned)(((long long)p->Tq * sk.n * p->Hq + 255) / 256);
+    if (blocks > 0) {
+      ffa_dsink_kernel<<<blocks, 256, 0, st>>>(sk.sink, sk.n, sk.layout, p->Tq, p->Hq, qpad, nlse2,
+                                               ndelta, dsink);
+      note_launches(1);
+      if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
+    }
   }
   alignas(64) CUtensorMap tq, tk, tv, tdo;
   if (!encode_tile_map(&tq, q, p->Tq, p->Hq * D) || !encode_tile_map(&tk, k, p->Tk, p->Hkv * D) ||
@@ -971,9 +1021,12 @@ size_t bwd_workspace_bytes(const ffa_plan_s* p) {
 
 ffa_status_t launch_bwd(ffa_plan_s* p, const void* q, const void* k, const void* v,
                         const void* out, const void* dout, const float* lse, float scale,
-                        void* dq, void* dk, void* dv, void* ws, size_t, cudaStream_t st) {
-  if (p->D == 128) return launch_bwd_d<128>(p, q, k, v, out, dout, lse, scale, dq, dk, dv, ws, st);
-  if (p->D == 64) return launch_bwd_d<64>(p, q, k, v, out, dout, lse, scale, dq, dk, dv, ws, st);
+                        void* dq, void* dk, void* dv, void* ws, size_t, cudaStream_t st,
+                        const SinkArgs& sink, float* dsink) {
+  if (p->D == 128)
+    return launch_bwd_d<128>(p, q, k, v, out, dout, lse, scale, dq, dk, dv, ws, st, sink, dsink);
+  if (p->D == 64)
+    return launch_bwd_d<64>(p, q, k, v, out, dout, lse, scale, dq, dk, dv, ws, st, sink, dsink);
   return FFA_ERR_UNSUPPORTED;
 }
 

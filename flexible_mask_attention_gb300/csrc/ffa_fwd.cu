@@ -27,6 +27,12 @@
 // than 8 (then O and l are rescaled), so p = 2^(x - m) stays below 256.
 // Masked entries become -inf (only on PARTIAL steps), a row with no visible
 // key keeps l = 0 and is written as out = 0, lse = -inf.
+//
+// Attention sink (optional): the sink logits of a row join its normaliser
+// only.  The epilogue of an unsplit item (or the merge of a split one) adds
+// log2 sum_s 2^(sink_s log2 e) to the keys' log-normaliser and scales out by
+// the keys' share of the total, so a row with no visible key gets out = 0
+// and lse = logsumexp(sink).
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -73,7 +79,30 @@ struct FwdParams {
   float* part_lse;  // [slot][2][128], log2 units
   int* err;
   uint64_t wait_ns;
+  const float* sink;  // optional sink logits
+  int n_sink, sink_layout;
 };
+
+// log2 of sum_s exp(sink_s) for (row, head) (-inf without sinks); sink logits
+// are natural-log values.  layout 0: sink[s][Hq], layout 1: sink[row][s][Hq].
+__device__ __forceinline__ float sink_log2(const float* sink, int n, int layout, int row, int head,
+                                           int Hq) {
+  if (n <= 0) return -INFINITY;
+  const float* b = layout == 0 ? sink + head : sink + (size_t)row * n * Hq + head;
+  float mx = -INFINITY;
+  for (int s = 0; s < n; ++s) mx = fmaxf(mx, b[(size_t)s * Hq] * kLog2e);
+  if (mx == -INFINITY) return -INFINITY;
+  float sum = 0.f;
+  for (int s = 0; s < n; ++s) sum += exp2f(b[(size_t)s * Hq] * kLog2e - mx);
+  return mx + log2f(sum);
+}
+
+// log2(2^a + 2^b), -inf when both are -inf.
+__device__ __forceinline__ float log2_add(float a, float b) {
+  const float mx = fmaxf(a, b);
+  if (mx == -INFINITY) return -INFINITY;
+  return mx + log2f(exp2f(a - mx) + exp2f(b - mx));
+}
 
 __device__ __forceinline__ bool item_at(const FwdParams& P, int r, const int*& it) {
   const int G = gridDim.x, b = blockIdx.x;
@@ -401,7 +430,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (!ok) break;
       // ---- epilogue: O / l -> out (bf16) or a partial slot (fp32), 32 columns at a time
       const bool nonempty = l > 0.f;
-      const float inv_l = nonempty ? 1.f / l : 0.f;
+      float inv_l = nonempty ? 1.f / l : 0.f;
+      // Row log2-normaliser: the keys', plus the sink's for an unsplit item
+      // (split items leave the sink to the merge).
+      float lse2 = nonempty ? m + log2f(l) : -INFINITY;
+      if (P.n_sink > 0 && slot < 0 && row < P.Tq) {
+        const float tot = log2_add(lse2, sink_log2(P.sink, P.n_sink, P.sink_layout, row, head, P.Hq));
+        if (nonempty) inv_l *= exp2f(lse2 - tot);
+        lse2 = tot;
+      }
       const bool store = slot >= 0 || row < P.Tq;
       const size_t pbase = slot >= 0 ? ((size_t)slot * 2 + h) * 128 + row_in : 0;
       uint4* dst_b = reinterpret_cast<uint4*>(P.out + ((size_t)row * P.Hq + head) * D);
@@ -443,9 +480,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       }
       if (slot < 0) {
-        if (row < P.Tq) P.lse[(size_t)head * P.Tq + row] = nonempty ? (m + log2f(l)) * kLn2 : -INFINITY;
+        if (row < P.Tq) P.lse[(size_t)head * P.Tq + row] = lse2 * kLn2;
       } else {
-        P.part_lse[pbase] = nonempty ? m + log2f(l) : -INFINITY;
+        P.part_lse[pbase] = lse2;
       }
     }
   }
@@ -463,7 +500,8 @@ template <int D>
 __global__ void __launch_bounds__(128)
     ffa_merge_kernel(const int* __restrict__ merges, const float* __restrict__ part_o,
                      const float* __restrict__ part_lse, int Tq, int Hq,
-                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                     const float* __restrict__ sink, int n_sink, int sink_layout) {
   const int grp = blockIdx.x >> 1, h = blockIdx.x & 1;
   const int* mg = merges + (size_t)grp * kMgWords;
   const int qt = mg[kMgQt0 + h], head = mg[kMgH0 + h];
@@ -494,7 +532,13 @@ __global__ void __launch_bounds__(128)
       }
     }
   }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  float lse2 = wsum > 0.f ? mx + log2f(wsum) : -INFINITY;
+  if (n_sink > 0) {  // the sink joins the merged normaliser once
+    const float tot = log2_add(lse2, sink_log2(sink, n_sink, sink_layout, row, head, Hq));
+    if (wsum > 0.f) inv *= exp2f(lse2 - tot);
+    lse2 = tot;
+  }
   uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)row * Hq + head) * D);
 #pragma unroll
   for (int v = 0; v < D / 8; ++v) {
@@ -505,12 +549,12 @@ __global__ void __launch_bounds__(128)
     w.w = pack_bf16x2(acc[8 * v + 6] * inv, acc[8 * v + 7] * inv);
     dst[v] = w;
   }
-  lse[(size_t)head * Tq + row] = wsum > 0.f ? (mx + log2f(wsum)) * kLn2 : -INFINITY;
+  lse[(size_t)head * Tq + row] = lse2 * kLn2;
 }
 
 template <int D>
 ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const void* v, float scale,
-                          void* out, float* lse, void* ws, cudaStream_t st) {
+                          void* out, float* lse, void* ws, cudaStream_t st, const SinkArgs& sk) {
   using C = FwdCfg<D>;
   alignas(64) CUtensorMap tq, tk, tv;
   if (!encode_tile_map(&tq, q, p->Tq, p->Hq * D) || !encode_tile_map(&tk, k, p->Tk, p->Hkv * D) ||
@@ -532,6 +576,9 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   P.part_lse = P.part_o ? P.part_o + (size_t)p->n_slots * 2 * 128 * D : nullptr;
   P.err = p->err;
   P.wait_ns = p->wait_ns;
+  P.sink = sk.sink;
+  P.n_sink = sk.n;
+  P.sink_layout = sk.layout;
   if (cudaFuncSetAttribute(ffa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
     return FFA_ERR_CUDA;
@@ -542,7 +589,7 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   if (p->n_merges > 0) {
     ffa_merge_kernel<D><<<(int)(2 * p->n_merges), 128, 0, st>>>(
-        p->merges, P.part_o, P.part_lse, p->Tq, p->Hq, P.out, lse);
+        p->merges, P.part_o, P.part_lse, p->Tq, p->Hq, P.out, lse, sk.sink, sk.n, sk.layout);
     note_launches(1);
     if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   }
@@ -557,9 +604,10 @@ size_t fwd_workspace_bytes(const ffa_plan_s* p) {
 }
 
 ffa_status_t launch_fwd(ffa_plan_s* p, const void* q, const void* k, const void* v, float scale,
-                        void* out, float* lse, void* ws, size_t, cudaStream_t st) {
-  if (p->D == 128) return launch_fwd_d<128>(p, q, k, v, scale, out, lse, ws, st);
-  if (p->D == 64) return launch_fwd_d<64>(p, q, k, v, scale, out, lse, ws, st);
+                        void* out, float* lse, void* ws, size_t, cudaStream_t st,
+                        const SinkArgs& sink) {
+  if (p->D == 128) return launch_fwd_d<128>(p, q, k, v, scale, out, lse, ws, st, sink);
+  if (p->D == 64) return launch_fwd_d<64>(p, q, k, v, scale, out, lse, ws, st, sink);
   return FFA_ERR_UNSUPPORTED;
 }
 

@@ -79,13 +79,24 @@ struct ffa_plan_s {
 };
 
 namespace ffa {
+// Optional attention-sink logits (fp32): layout 0 is [n][Hq], layout 1 is
+// [Tq][n][Hq]; n == 0 means no sink.
+struct SinkArgs {
+  const float* sink = nullptr;
+  int n = 0;
+  int layout = 0;
+};
 // Implemented in ffa_fwd.cu / ffa_bwd.cu.
 ffa_status_t launch_fwd(ffa_plan_s* p, const void* q, const void* k, const void* v, float scale,
-                        void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t st);
+                        void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t st,
+                        const SinkArgs& sink = SinkArgs());
 size_t fwd_workspace_bytes(const ffa_plan_s* p);
+// dsink (when non-null and sink.n > 0) receives the sink gradient, in the
+// sink's own layout, overwritten.
 ffa_status_t launch_bwd(ffa_plan_s* p, const void* q, const void* k, const void* v,
                         const void* out, const void* dout, const float* lse, float scale,
-                        void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, cudaStream_t st);
+                        void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, cudaStream_t st,
+                        const SinkArgs& sink = SinkArgs(), float* dsink = nullptr);
 size_t bwd_workspace_bytes(const ffa_plan_s* p);
 // Implemented in ffa_plan.cu.
 bool encode_tile_map(void* map128, const void* base, int rows, int cols_elems);

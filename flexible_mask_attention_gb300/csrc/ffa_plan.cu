@@ -679,6 +679,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Sink arguments: none (num_sink == 0), or fp32 logits in a known layout.
+bool sink_args_ok(const float* sink, int32_t n, int32_t layout) {
+  if (n < 0 || n > FFA_MAX_SINK) return false;
+  if (layout != FFA_SINK_SH && layout != FFA_SINK_SSH) return false;
+  if (n > 0 && (!sink || (reinterpret_cast<uintptr_t>(sink) & 3u))) return false;
+  return true;
+}
+
 std::atomic<uint64_t> g_launches{0};
 
 }  // namespace
@@ -794,34 +802,62 @@ ffa_status_t ffa_plan_export(ffa_plan_t p, int32_t which, int32_t* dst, int64_t 
 size_t ffa_fwd_workspace_size(ffa_plan_t p) { return p ? fwd_workspace_bytes(p) : 0; }
 size_t ffa_bwd_workspace_size(ffa_plan_t p) { return p ? bwd_workspace_bytes(p) : 0; }
 
-ffa_status_t ffa_fwd(ffa_plan_t p, const void* q, const void* k, const void* v,
-                     float softmax_scale, void* out, float* lse, void* workspace,
-                     size_t workspace_bytes, ffa_stream_t stream) {
+ffa_status_t ffa_fwd_ex(ffa_plan_t p, const void* q, const void* k, const void* v,
+                        const float* sink, int32_t num_sink, int32_t sink_layout,
+                        float softmax_scale, void* out, float* lse, void* workspace,
+                        size_t workspace_bytes, ffa_stream_t stream) {
   if (!p || !q || !k || !v || !out || !lse) return FFA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
     return FFA_ERR_INVALID_ARG;
+  if (!sink_args_ok(sink, num_sink, sink_layout)) return FFA_ERR_INVALID_ARG;
   const size_t need = fwd_workspace_bytes(p);
   if (workspace_bytes < need || (need > 0 && (!workspace || !aligned16(workspace))))
     return FFA_ERR_WORKSPACE;
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)p->D);
+  SinkArgs sk;
+  sk.sink = sink;
+  sk.n = num_sink;
+  sk.layout = sink_layout;
   return launch_fwd(p, q, k, v, scale, out, lse, workspace, workspace_bytes,
-                    reinterpret_cast<cudaStream_t>(stream));
+                    reinterpret_cast<cudaStream_t>(stream), sk);
 }
 
-ffa_status_t ffa_bwd(ffa_plan_t p, const void* q, const void* k, const void* v, const void* out,
-                     const void* dout, const float* lse, float softmax_scale, void* dq, void* dk,
-                     void* dv, void* workspace, size_t workspace_bytes, ffa_stream_t stream) {
+ffa_status_t ffa_fwd(ffa_plan_t p, const void* q, const void* k, const void* v,
+                     float softmax_scale, void* out, float* lse, void* workspace,
+                     size_t workspace_bytes, ffa_stream_t stream) {
+  return ffa_fwd_ex(p, q, k, v, nullptr, 0, FFA_SINK_SH, softmax_scale, out, lse, workspace,
+                    workspace_bytes, stream);
+}
+
+ffa_status_t ffa_bwd_ex(ffa_plan_t p, const void* q, const void* k, const void* v, const void* out,
+                        const void* dout, const float* lse, const float* sink, int32_t num_sink,
+                        int32_t sink_layout, float softmax_scale, void* dq, void* dk, void* dv,
+                        float* dsink, void* workspace, size_t workspace_bytes,
+                        ffa_stream_t stream) {
   if (!p || !q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv)
     return FFA_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, out, dout, lse, dq, dk, dv};
   for (const void* x : ptrs)
     if (!aligned16(x)) return FFA_ERR_INVALID_ARG;
+  if (!sink_args_ok(sink, num_sink, sink_layout)) return FFA_ERR_INVALID_ARG;
+  if (dsink && (reinterpret_cast<uintptr_t>(dsink) & 3u)) return FFA_ERR_INVALID_ARG;
   const size_t need = bwd_workspace_bytes(p);
   if (workspace_bytes < need || (need > 0 && (!workspace || !aligned16(workspace))))
     return FFA_ERR_WORKSPACE;
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)p->D);
+  SinkArgs sk;
+  sk.sink = sink;
+  sk.n = num_sink;
+  sk.layout = sink_layout;
   return launch_bwd(p, q, k, v, out, dout, lse, scale, dq, dk, dv, workspace, workspace_bytes,
-                    reinterpret_cast<cudaStream_t>(stream));
+                    reinterpret_cast<cudaStream_t>(stream), sk, dsink);
+}
+
+ffa_status_t ffa_bwd(ffa_plan_t p, const void* q, const void* k, const void* v, const void* out,
+                     const void* dout, const float* lse, float softmax_scale, void* dq, void* dk,
+                     void* dv, void* workspace, size_t workspace_bytes, ffa_stream_t stream) {
+  return ffa_bwd_ex(p, q, k, v, out, dout, lse, nullptr, 0, FFA_SINK_SH, softmax_scale, dq, dk,
+                    dv, nullptr, workspace, workspace_bytes, stream);
 }
 
 ffa_status_t ffa_get_last_device_error(ffa_plan_t p, int32_t* code, int32_t* where,

@@ -123,6 +123,32 @@ ffa_status_t ffa_fwd(ffa_plan_t plan, const void* q, const void* k, const void* 
                      float softmax_scale, void* out, float* lse, void* workspace,
                      size_t workspace_bytes, ffa_stream_t stream);
 
+/* Attention sink (MagiAttention pages: the `sink` argument of
+ * flex_flash_attn_func in the quickstart card, and the FlashAttention
+ * "with sink" cards, which give its two layouts).  The pages do not state the
+ * formula; this library reads it as: each sink value s is a logit in natural
+ * log units, NOT multiplied by softmax_scale, that joins only the row's
+ * normaliser,
+ *     lse_i = log( sum_j exp(scale * q_i.k_j) + sum_s exp(sink_s) ),
+ *     out_i = sum_j exp(scale * q_i.k_j - lse_i) v_j,
+ * so a row that sees no key gets out = 0 and lse = log sum_s exp(sink_s), and
+ *     dsink_s = - sum_i exp(sink_s - lse_i) <dout_i, out_i>.
+ * Layouts of the fp32 DEVICE array (4-byte aligned):
+ *     FFA_SINK_SH   [num_sink][Hq]      one set per query head (dsink sums over rows)
+ *     FFA_SINK_SSH  [Tq][num_sink][Hq]  one set per (row, query head)
+ * A sink value of -inf contributes nothing. */
+typedef enum { FFA_SINK_SH = 0, FFA_SINK_SSH = 1 } ffa_sink_layout_t;
+#define FFA_MAX_SINK 64 /* largest num_sink accepted */
+
+/* ffa_fwd with optional sink logits (num_sink = 0: none, sink may be NULL;
+ * identical to ffa_fwd).  Returns FFA_ERR_INVALID_ARG for num_sink outside
+ * [0, FFA_MAX_SINK], an unknown layout, or a NULL / misaligned sink when
+ * num_sink > 0.  lse includes the sink term. */
+ffa_status_t ffa_fwd_ex(ffa_plan_t plan, const void* q, const void* k, const void* v,
+                        const float* sink, int32_t num_sink, int32_t sink_layout,
+                        float softmax_scale, void* out, float* lse, void* workspace,
+                        size_t workspace_bytes, ffa_stream_t stream);
+
 /* Backward of ffa_fwd for the loss L with dL/dout = dout.
  *   out, lse: the forward's results; dq, dk, dv receive the gradients
  *   (bf16, every element written; keys seen by no query get 0).
@@ -131,6 +157,17 @@ ffa_status_t ffa_bwd(ffa_plan_t plan, const void* q, const void* k, const void* 
                      const void* out, const void* dout, const float* lse, float softmax_scale,
                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                      ffa_stream_t stream);
+
+/* Backward of ffa_fwd_ex.  out and lse are ffa_fwd_ex's results for the same
+ * sink (the sink acts on dq, dk, dv only through lse).  dsink: fp32 DEVICE
+ * array in the sink's layout, overwritten with the sink gradient, or NULL to
+ * skip it; ignored when num_sink = 0.  The per-head sums of the "sh" layout
+ * are taken in a fixed order, so repeated calls give identical results. */
+ffa_status_t ffa_bwd_ex(ffa_plan_t plan, const void* q, const void* k, const void* v,
+                        const void* out, const void* dout, const float* lse, const float* sink,
+                        int32_t num_sink, int32_t sink_layout, float softmax_scale, void* dq,
+                        void* dk, void* dv, float* dsink, void* workspace,
+                        size_t workspace_bytes, ffa_stream_t stream);
 
 /* Backward without any allocation: the same computation as ffa_bwd, with its
  * scratch memory taken from a fixed array inside the library instead of a
