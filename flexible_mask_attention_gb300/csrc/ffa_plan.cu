@@ -55,16 +55,62 @@ __global__ void k_check_slices(const Slice* __restrict__ sl, int S, int Tq, int 
   atomicAdd(area, (unsigned long long)slice_area(x));
 }
 
-__global__ void k_check_overlap(const Slice* __restrict__ sl, int S, int* flags) {
-  const long long p = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (p >= (long long)S * S) return;
-  const int i = (int)(p / S), j = (int)(p % S);
-  if (i >= j) return;
-  const Slice a = sl[i], b = sl[j];
-  if (a.qs >= a.qe || a.ks >= a.ke || b.qs >= b.qe || b.ks >= b.ke) return;
-  const bool q_meet = a.qs < b.qe && b.qs < a.qe;
-  const bool k_meet = a.ks < b.ke && b.ks < a.ke;
-  if (q_meet && k_meet) atomicExch(&flags[1], 1);
+// ---- per-tile slice lists ---------------------------------------------------
+// List of tile t: the non-empty slices whose q range (kQ) or k range meets
+// rows/keys [128t, 128t+128), in slice order.  One block per tile walks the
+// slices 256 at a time; a block scan of the hit flags places each hit, so the
+// order never depends on scheduling.  Count mode (list == nullptr) writes the
+// list lengths to cnt.
+constexpr int kListThreads = 256;
+
+template <bool kQ>
+__global__ void __launch_bounds__(kListThreads)
+    k_tile_slices(const Slice* __restrict__ sl, int S, const int* __restrict__ off,
+                  int* __restrict__ cnt, int* __restrict__ list) {
+  __shared__ int warp_tot[kListThreads / 32];
+  const int t = blockIdx.x, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int lo = t * 128, hi = lo + 128;
+  int base = list ? off[t] : 0;
+  for (int s0 = 0; s0 < S; s0 += kListThreads) {
+    const int s = s0 + threadIdx.x;
+    bool hit = false;
+    if (s < S) {
+      const Slice x = sl[s];
+      if (x.qs < x.qe && x.ks < x.ke)
+        hit = kQ ? (x.qs < hi && x.qe > lo) : (x.ks < hi && x.ke > lo);
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, hit);
+    if (lane == 0) warp_tot[w] = __popc(m);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int i = 0; i < kListThreads / 32; ++i) {
+      before += i < w ? warp_tot[i] : 0;
+      total += warp_tot[i];
+    }
+    if (hit && list) list[base + before + __popc(m & ((1u << lane) - 1u))] = s;
+    base += total;
+    __syncthreads();
+  }
+  if (!list && threadIdx.x == 0) cnt[t] = base;
+}
+
+// Two non-empty slices overlap iff their rectangles meet; then they share a
+// row, hence a q-tile, so only pairs within one q-tile's list are compared.
+__global__ void __launch_bounds__(kListThreads)
+    k_check_overlap(const Slice* __restrict__ sl, const int* __restrict__ list,
+                    const int* __restrict__ off, const int* __restrict__ cnt, int* flags) {
+  const int* L = list + off[blockIdx.x];
+  const int n = cnt[blockIdx.x];
+  for (int i = threadIdx.x; i < n; i += kListThreads) {
+    const Slice a = sl[L[i]];
+    for (int j = i + 1; j < n; ++j) {
+      const Slice b = sl[L[j]];
+      if (a.qs < b.qe && b.qs < a.qe && a.ks < b.ke && b.ks < a.ke) {
+        atomicExch(&flags[1], 1);
+        return;
+      }
+    }
+  }
 }
 
 // Single-block exclusive scan of n int32 counts; total in *total.
@@ -92,38 +138,44 @@ __global__ void k_scan(const int* __restrict__ in, int n, int* __restrict__ out,
 }
 
 // ---- forward visits ---------------------------------------------------------
-__global__ void k_fwd_visit_count(const Slice* __restrict__ sl, int S, int n_qt, int* cnt) {
+__global__ void k_fwd_visit_count(const Slice* __restrict__ sl, const int* __restrict__ list,
+                                  const int* __restrict__ loff, const int* __restrict__ lcnt,
+                                  int n_qt, int* cnt) {
   const int qt = blockIdx.x * blockDim.x + threadIdx.x;
   if (qt >= n_qt) return;
   int c = 0;
-  for (int s = 0; s < S; ++s) {
+  for (int i = 0; i < lcnt[qt]; ++i) {
     TileRun r;
-    if (fwd_tile_run(sl[s], qt, r)) c += r.e - r.b;
+    if (fwd_tile_run(sl[list[loff[qt] + i]], qt, r)) c += r.e - r.b;
   }
   cnt[qt] = c;
 }
 
 // Emits the (tile index, info) visits of one tile in (index, slice) order,
-// one warp per tile: the lanes collect the
-// tile's slice runs (kept in shared memory, in slice order), then walk the
-// visited range 32 positions at a time; a warp scan of the per-position
-// counts gives every lane its output offset.
+// one warp per tile: the lanes collect the runs of the slices in the tile's
+// list (kept in shared memory, in slice order), then walk the visited range
+// 32 positions at a time; a warp scan of the per-position counts gives every
+// lane its output offset.  Tiles with more than kMaxLocalSegs runs re-read
+// the list for every position instead.
 constexpr int kFillWarps = 4;
 
 template <bool kFwd>
 __global__ void __launch_bounds__(32 * kFillWarps)
-    k_visit_fill_warp(const Slice* __restrict__ sl, int S, int n_tiles,
+    k_visit_fill_warp(const Slice* __restrict__ sl, const int* __restrict__ list,
+                      const int* __restrict__ loff, const int* __restrict__ lcnt, int n_tiles,
                       const int* __restrict__ off, int2* visits) {
   __shared__ TileRun seg[kFillWarps][kMaxLocalSegs];
   __shared__ int seg_s[kFillWarps][kMaxLocalSegs];
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x * kFillWarps + wib;
   if (tile >= n_tiles) return;  // whole warp leaves together
+  const int* L = list + loff[tile];
+  const int S = lcnt[tile];
   int nseg = 0, lo = 0x7fffffff, hi = 0;
   for (int s0 = 0; s0 < S; s0 += 32) {
-    const int s = s0 + lane;
+    const int s = s0 + lane < S ? L[s0 + lane] : -1;
     TileRun r;
-    const bool ok = s < S && (kFwd ? fwd_tile_run(sl[s], tile, r) : bwd_tile_run(sl[s], tile, r));
+    const bool ok = s >= 0 && (kFwd ? fwd_tile_run(sl[s], tile, r) : bwd_tile_run(sl[s], tile, r));
     const unsigned m = __ballot_sync(0xffffffffu, ok);
     if (ok) {
       const int pos = nseg + __popc(m & ((1u << lane) - 1u));
@@ -150,8 +202,9 @@ __global__ void __launch_bounds__(32 * kFillWarps)
       if (!overflow) {
         for (int i = 0; i < nseg; ++i) cnt += (x >= seg[wib][i].b && x < seg[wib][i].e) ? 1 : 0;
       } else {
-        for (int s = 0; s < S; ++s) {
+        for (int i = 0; i < S; ++i) {
           TileRun r;
+          const int s = L[i];
           const bool ok = kFwd ? fwd_tile_run(sl[s], tile, r) : bwd_tile_run(sl[s], tile, r);
           cnt += (ok && x >= r.b && x < r.e) ? 1 : 0;
         }
@@ -171,8 +224,9 @@ __global__ void __launch_bounds__(32 * kFillWarps)
             visits[w++] = make_int2(x, visit_info(seg_s[wib][i], !(x >= r.fb && x < r.fe)));
         }
       } else {
-        for (int s = 0; s < S; ++s) {
+        for (int i = 0; i < S; ++i) {
           TileRun r;
+          const int s = L[i];
           const bool ok = kFwd ? fwd_tile_run(sl[s], tile, r) : bwd_tile_run(sl[s], tile, r);
           if (ok && x >= r.b && x < r.e)
             visits[w++] = make_int2(x, visit_info(s, !(x >= r.fb && x < r.fe)));
@@ -338,13 +392,15 @@ __global__ void k_split_fill(const int* __restrict__ items, int n_items,
 }
 
 // ---- backward visits --------------------------------------------------------
-__global__ void k_bwd_visit_count(const Slice* __restrict__ sl, int S, int n_kt, int* cnt) {
+__global__ void k_bwd_visit_count(const Slice* __restrict__ sl, const int* __restrict__ list,
+                                  const int* __restrict__ loff, const int* __restrict__ lcnt,
+                                  int n_kt, int* cnt) {
   const int kt = blockIdx.x * blockDim.x + threadIdx.x;
   if (kt >= n_kt) return;
   int c = 0;
-  for (int s = 0; s < S; ++s) {
+  for (int i = 0; i < lcnt[kt]; ++i) {
     TileRun r;
-    if (bwd_tile_run(sl[s], kt, r)) c += r.e - r.b;
+    if (bwd_tile_run(sl[list[loff[kt] + i]], kt, r)) c += r.e - r.b;
   }
   cnt[kt] = c;
 }
@@ -501,7 +557,48 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
     note_launches(1);
     k_check_slices<<<grid_for(S, 256), 256, 0, st>>>(p->slices, S, p->Tq, p->Tk, flags, area);
     note_launches(1);
-    k_check_overlap<<<grid_for((long long)S * S, 256), 256, 0, st>>>(p->slices, S, flags);
+    FFA_CUDA(cudaGetLastError());
+  }
+  // per-tile slice lists (q-tiles for the forward and the overlap check,
+  // k-tiles for the backward)
+  const int n_qt = p->n_qt, n_kt = p->n_kt, g = p->Hq / p->Hkv;
+  long long tot = 0;
+  ffa_status_t rc = FFA_OK;
+  DevBuf qlcnt(st), qloff(st), qlist(st), klcnt(st), kloff(st), klist(st);
+  FFA_CUDA(qlcnt.alloc(sizeof(int) * n_qt));
+  FFA_CUDA(qloff.alloc(sizeof(int) * n_qt));
+  FFA_CUDA(klcnt.alloc(sizeof(int) * n_kt));
+  FFA_CUDA(kloff.alloc(sizeof(int) * n_kt));
+  if (n_qt > 0) {
+    k_tile_slices<true><<<n_qt, kListThreads, 0, st>>>(p->slices, S, nullptr, qlcnt.as<int>(),
+                                                       nullptr);
+    note_launches(1);
+    FFA_CUDA(cudaGetLastError());
+  }
+  if ((rc = scan(qlcnt.as<int>(), n_qt, qloff.as<int>(), dtot, &tot, st))) return rc;
+  if (tot > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
+  FFA_CUDA(qlist.alloc(sizeof(int) * (size_t)tot));
+  if (n_qt > 0) {
+    k_tile_slices<true><<<n_qt, kListThreads, 0, st>>>(p->slices, S, qloff.as<int>(), nullptr,
+                                                       qlist.as<int>());
+    note_launches(1);
+    k_check_overlap<<<n_qt, kListThreads, 0, st>>>(p->slices, qlist.as<int>(), qloff.as<int>(),
+                                                   qlcnt.as<int>(), flags);
+    note_launches(1);
+    FFA_CUDA(cudaGetLastError());
+  }
+  if (n_kt > 0) {
+    k_tile_slices<false><<<n_kt, kListThreads, 0, st>>>(p->slices, S, nullptr, klcnt.as<int>(),
+                                                        nullptr);
+    note_launches(1);
+    FFA_CUDA(cudaGetLastError());
+  }
+  if ((rc = scan(klcnt.as<int>(), n_kt, kloff.as<int>(), dtot, &tot, st))) return rc;
+  if (tot > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
+  FFA_CUDA(klist.alloc(sizeof(int) * (size_t)tot));
+  if (n_kt > 0) {
+    k_tile_slices<false><<<n_kt, kListThreads, 0, st>>>(p->slices, S, kloff.as<int>(), nullptr,
+                                                        klist.as<int>());
     note_launches(1);
     FFA_CUDA(cudaGetLastError());
   }
@@ -514,21 +611,22 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   if (hflags[1]) return FFA_ERR_OVERLAP;
   p->area = (int64_t)harea;
 
-  const int n_qt = p->n_qt, n_kt = p->n_kt, g = p->Hq / p->Hkv;
-  long long tot = 0;
   // forward visits
   DevBuf vcnt(st), voff(st), visits(st);
   FFA_CUDA(vcnt.alloc(sizeof(int) * n_qt));
   FFA_CUDA(voff.alloc(sizeof(int) * n_qt));
-  k_fwd_visit_count<<<grid_for(n_qt, 128), 128, 0, st>>>(p->slices, S, n_qt, vcnt.as<int>());
+  k_fwd_visit_count<<<grid_for(n_qt, 128), 128, 0, st>>>(p->slices, qlist.as<int>(),
+                                                         qloff.as<int>(), qlcnt.as<int>(), n_qt,
+                                                         vcnt.as<int>());
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
-  ffa_status_t rc = scan(vcnt.as<int>(), n_qt, voff.as<int>(), dtot, &tot, st);
+  rc = scan(vcnt.as<int>(), n_qt, voff.as<int>(), dtot, &tot, st);
   if (rc != FFA_OK) return rc;
   if (tot > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
   FFA_CUDA(visits.alloc(sizeof(int2) * (size_t)tot));
   k_visit_fill_warp<true><<<grid_for(n_qt, kFillWarps), 32 * kFillWarps, 0, st>>>(
-      p->slices, S, n_qt, voff.as<int>(), visits.as<int2>());
+      p->slices, qlist.as<int>(), qloff.as<int>(), qlcnt.as<int>(), n_qt, voff.as<int>(),
+      visits.as<int2>());
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
   // forward units -> steps
@@ -636,7 +734,9 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   DevBuf bcnt(st), boff(st), bvis(st);
   FFA_CUDA(bcnt.alloc(sizeof(int) * n_kt));
   FFA_CUDA(boff.alloc(sizeof(int) * n_kt));
-  k_bwd_visit_count<<<grid_for(n_kt, 128), 128, 0, st>>>(p->slices, S, n_kt, bcnt.as<int>());
+  k_bwd_visit_count<<<grid_for(n_kt, 128), 128, 0, st>>>(p->slices, klist.as<int>(),
+                                                         kloff.as<int>(), klcnt.as<int>(), n_kt,
+                                                         bcnt.as<int>());
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
   if ((rc = scan(bcnt.as<int>(), n_kt, boff.as<int>(), dtot, &tot, st))) return rc;
@@ -645,7 +745,8 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   FFA_CUDA(bvis.alloc(sizeof(int2) * (size_t)tot));
   FFA_CUDA(cudaMalloc(&p->bwd_steps, sizeof(int4) * (size_t)std::max(1LL, tot)));
   k_visit_fill_warp<false><<<grid_for(n_kt, kFillWarps), 32 * kFillWarps, 0, st>>>(
-      p->slices, S, n_kt, boff.as<int>(), bvis.as<int2>());
+      p->slices, klist.as<int>(), kloff.as<int>(), klcnt.as<int>(), n_kt, boff.as<int>(),
+      bvis.as<int2>());
   note_launches(1);
   const long long nb_items = (long long)n_kt * p->Hkv;
   p->n_bwd_items = nb_items;

@@ -9,7 +9,11 @@ packed variable-length documents with one causal slice each (varlen key,
 "magi_attn_varlen_key" card), a shared prefix visible to later documents
 (quickstart "Single-GPU Flex-Flash-Attention" mask picture and the block-causal
 example), and long-context block sliding windows built from consecutive
-causal/full slices.  No dataset is involved; every value is synthetic.
+causal/full slices, and uniform block-sparse masks given by a (q block,
+k block) size pair ("Configure ... Block Sizes for Sparse Attention" cards:
+64/128 square blocks, q blocks of 32..8 against k blocks of 64, k blocks of
+32..1 against q blocks of 64).  No dataset is involved; every value is
+synthetic.
 
 Mask-type codes: 0 = full, 1 = causal (bottom-right aligned), 2 = inverse
 causal (top-left aligned), 3 = bidirectional causal (both clamps).
@@ -183,6 +187,32 @@ def random_slices(total_q: int, total_k: int, n: int, seed: int,
             np.asarray(ty, np.int32))
 
 
+def block_sparse(total: int = 16384, hq: int = 16, hkv: int = 4, d: int = 128,
+                 q_block: int = 64, k_block: int = 64, density: float = 0.125,
+                 seed: int = 6) -> Workload:
+    """Uniform block-sparse attention: the sequence is cut into q blocks of
+    ``q_block`` rows and k blocks of ``k_block`` keys; every q block attends
+    to ``round(density * n_k_blocks)`` (at least one) k blocks drawn without
+    replacement, and every selected (q block, k block) pair is one full
+    slice.  Slices are listed q block by q block, k blocks ascending, so the
+    table holds many tiny slices (the density is this module's choice: the
+    pages give the block sizes only).
+    """
+    rng = np.random.default_rng(seed)
+    nq, nk = -(-total // q_block), -(-total // k_block)
+    per = max(1, int(round(density * nk)))
+    qr, kr = [], []
+    for qb in range(nq):
+        q0, q1 = qb * q_block, min(total, (qb + 1) * q_block)
+        for kb in np.sort(rng.choice(nk, per, replace=False)):
+            k0, k1 = int(kb) * k_block, min(total, (int(kb) + 1) * k_block)
+            qr.append([q0, q1]); kr.append([k0, k1])
+    ty = [FULL] * len(qr)
+    return _pack(f"block_sparse_T{total}_Hq{hq}_Hkv{hkv}_D{d}_q{q_block}_k{k_block}", total,
+                 total, hq, hkv, d, qr, kr, ty, seed=seed, q_block=q_block, k_block=k_block,
+                 density=density)
+
+
 def make_tensors(wl: Workload, with_dout: bool = False):
     """bf16 q, k, v (and dout) ~ N(0, 1) from a seeded CPU torch generator."""
     import torch
@@ -203,4 +233,9 @@ CONFIGS = {
     "packed_causal": packed_causal_docs,
     "heterogeneous": heterogeneous_prefix_docs,
     "long_context": long_context_docs,
+    "block_sparse_64x64": lambda: block_sparse(q_block=64, k_block=64),
+    "block_sparse_128x128": lambda: block_sparse(q_block=128, k_block=128),
+    "block_sparse_16x64": lambda: block_sparse(q_block=16, k_block=64),
+    "block_sparse_64x8": lambda: block_sparse(q_block=64, k_block=8),
+    "block_sparse_64x1": lambda: block_sparse(q_block=64, k_block=1),
 }

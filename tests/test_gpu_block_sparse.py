@@ -1,0 +1,72 @@
+"""Uniform block-sparse masks (many tiny full slices): forward and backward of
+the CUDA path against the fp64 oracle, on small cases in full and on the
+benchmark-size tables on sampled rows and keys."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import flexible_mask_attention_gb300 as ffa
+from flexible_mask_attention_gb300 import workloads as W
+from gpu_helpers import bf16, check_fwd, check_grad
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+BLOCKS = [(64, 64), (128, 128), (32, 64), (16, 64), (8, 64), (64, 32), (64, 16), (64, 8), (64, 1)]
+
+
+def run(wl, q, k, v, do=None):
+    plan = ffa.ffa_plan_create(wl.q_ranges, wl.k_ranges, wl.mask_types, wl.total_q, wl.total_k,
+                               wl.num_heads_q, wl.num_heads_kv, wl.head_dim)
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    out, lse = ffa.ffa_fwd(plan, qd, kd, vd)
+    res = [out, lse]
+    if do is not None:
+        res += list(ffa.ffa_bwd(plan, qd, kd, vd, out, do.to(DEV), lse))
+    torch.cuda.synchronize()
+    assert ffa.ffa_get_last_device_error(plan) == (0, 0)
+    return [t.float().cpu().numpy() for t in res]
+
+
+@pytest.mark.parametrize("blocks", BLOCKS, ids=[f"q{a}_k{b}" for a, b in BLOCKS])
+def test_block_sparse_small(blocks):
+    wl = W.block_sparse(total=2048, hq=4, hkv=2, d=128, q_block=blocks[0], k_block=blocks[1],
+                        seed=17)
+    q, k, v, do = W.make_tensors(wl, with_dout=True)
+    out, lse, dq, dk, dv = run(wl, q, k, v, do)
+    ro, rl = oracle.fwd(q, k, v, wl.q_ranges, wl.k_ranges, wl.mask_types)
+    check_fwd(out, lse, ro, rl)
+    rq, rk, rv = oracle.bwd(q, k, v, do, wl.q_ranges, wl.k_ranges, wl.mask_types)
+    check_grad(dq, rq, "dq"); check_grad(dk, rk, "dk"); check_grad(dv, rv, "dv")
+
+
+def test_block_sparse_d64_gqa():
+    wl = W.block_sparse(total=1500, hq=6, hkv=2, d=64, q_block=64, k_block=16, seed=23)
+    q, k, v, do = W.make_tensors(wl, with_dout=True)
+    out, lse, dq, dk, dv = run(wl, q, k, v, do)
+    ro, rl = oracle.fwd(q, k, v, wl.q_ranges, wl.k_ranges, wl.mask_types)
+    check_fwd(out, lse, ro, rl)
+    rq, rk, rv = oracle.bwd(q, k, v, do, wl.q_ranges, wl.k_ranges, wl.mask_types)
+    check_grad(dq, rq, "dq"); check_grad(dk, rk, "dk"); check_grad(dv, rv, "dv")
+
+
+@pytest.mark.parametrize("name,with_dkv", [("block_sparse_64x64", True), ("block_sparse_16x64", True),
+                                           ("block_sparse_64x1", False)])
+def test_block_sparse_full_size_sampled(name, with_dkv):
+    """Benchmark-size tables: forward on a sample of rows, dq on fewer rows,
+    dk/dv on a few keys (skipped for the half-million-slice table, where the
+    oracle's per-key pass alone takes half a minute)."""
+    wl = W.CONFIGS[name]()
+    q, k, v, do = W.make_tensors(wl, with_dout=True)
+    out, lse, dq, dk, dv = run(wl, q, k, v, do)
+    rng = np.random.default_rng(5)
+    rows = np.sort(rng.choice(wl.total_q, 48, replace=False))
+    ro, rl = oracle.fwd(q, k, v, wl.q_ranges, wl.k_ranges, wl.mask_types, rows=rows)
+    check_fwd(out, lse, ro, rl, rows=rows)
+    keys = np.sort(rng.choice(wl.total_k, 4, replace=False)) if with_dkv else np.zeros(0, np.int64)
+    rq, rk, rv = oracle.bwd(q, k, v, do, wl.q_ranges, wl.k_ranges, wl.mask_types,
+                            dq_rows=rows[:12], dkv_keys=keys)
+    check_grad(dq[rows[:12]], rq, "dq")
+    if with_dkv:
+        check_grad(dk[keys], rk, "dk"); check_grad(dv[keys], rv, "dv")

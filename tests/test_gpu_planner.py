@@ -55,3 +55,22 @@ def test_rejects_bad_slices():
     with pytest.raises(ffa.FFAError) as e:
         ffa.ffa_plan_create([[0, 10]], [[0, 10]], [0], 32, 32, 1, 1, 96)
     assert e.value.status == 4
+
+
+@pytest.mark.parametrize("blocks", [(64, 64), (128, 128), (16, 64), (8, 64), (64, 8), (64, 1)])
+def test_block_sparse(blocks):
+    """Many tiny slices (uniform block-sparse masks): same lists as the CPU derivation."""
+    wl = W.block_sparse(total=4096, hq=4, hkv=2, q_block=blocks[0], k_block=blocks[1], seed=9)
+    compare(wl.q_ranges, wl.k_ranges, wl.mask_types, wl.total_q, wl.total_k, wl.num_heads_q,
+            wl.num_heads_kv, wl.head_dim)
+
+
+def test_overlap_found_between_tiny_slices():
+    """The tile-local overlap check still sees an overlap hidden among many slices."""
+    wl = W.block_sparse(total=4096, hq=2, hkv=2, q_block=64, k_block=8, seed=3)
+    qr, kr = wl.q_ranges.copy(), wl.k_ranges.copy()
+    qr[-1] = [qr[5][0] + 3, qr[5][0] + 9]   # rows inside q block 0
+    kr[-1] = [kr[5][0] + 1, kr[5][0] + 2]   # a key of slice 5
+    with pytest.raises(ffa.FFAError) as e:
+        ffa.ffa_plan_create(qr, kr, wl.mask_types, 4096, 4096, 2, 2, 128)
+    assert e.value.status == 3
