@@ -84,6 +84,7 @@ struct KvParams {
   const int* order;
   int n_items;
   const Slice* slices;
+  const int* masks;  // slice lists of multi-slice visits
   int Tk, Hkv, g, qpad;
   float scale, scale_log2;
   const float* nlse2;   // [Hq][qpad] -lse * log2(e)
@@ -102,20 +103,6 @@ __device__ __forceinline__ bool kv_item_at(const KvParams& P, int r, const int*&
   return true;
 }
 
-// Query rows of the step visible to key `key` under a PARTIAL step's slice,
-// in local coordinates [lo, hi) of the q-tile.
-__device__ __forceinline__ void key_query_window(const Slice& sl, int key, int qt, int& lo,
-                                                 int& hi) {
-  lo = hi = 0;
-  if (key < sl.ks || key >= sl.ke) return;
-  int a = (sl.t & 1) ? key + sl.qe - sl.ke : sl.qs;
-  a = a > sl.qs ? a : sl.qs;
-  int b = (sl.t & 2) ? key - sl.ks + sl.qs + 1 : sl.qe;
-  b = b < sl.qe ? b : sl.qe;
-  lo = a - qt * 128;
-  hi = b - qt * 128;
-}
-
 // P^T and dS^T for key row j over the 64 queries [q0, q0+64) of the step
 // owned by this warpgroup, from the S^T values already in registers (s) and
 // the dP^T values read from TMEM here:
@@ -125,7 +112,7 @@ __device__ __forceinline__ void key_query_window(const Slice& sl, int key, int q
 template <bool kPartial>
 __device__ __forceinline__ void pds_half(const uint32_t (&s)[64], uint32_t tP, int q0,
                                          const float* nl, const float* nd, float scale_log2,
-                                         int lo, int hi, int j, uint8_t* p_row) {
+                                         uint32_t m_lo, uint32_t m_hi, int j, uint8_t* p_row) {
   const float2 sc2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
@@ -139,15 +126,15 @@ __device__ __forceinline__ void pds_half(const uint32_t (&s)[64], uint32_t tP, i
 #pragma unroll
       for (int u = 0; u < 4; u += 2) {
         const int lc = 32 * c + e + u;  // column within this warpgroup's half
-        const int col = q0 + lc;
         const float2 nlp = u == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
         const float2 ndp = u == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
         const float2 x = __ffma2_rn(
             make_float2(__uint_as_float(s[lc]), __uint_as_float(s[lc + 1])), sc2, nlp);
         float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-        if (kPartial) {
-          p.x = (col >= lo && col < hi) ? p.x : 0.f;
-          p.y = (col + 1 >= lo && col + 1 < hi) ? p.y : 0.f;
+        if (kPartial) {  // bits of this warpgroup's 64 columns: m_lo (0-31), m_hi (32-63)
+          const uint32_t mw = lc < 32 ? m_lo : m_hi;
+          p.x = ((mw >> (lc & 31)) & 1u) ? p.x : 0.f;
+          p.y = ((mw >> ((lc + 1) & 31)) & 1u) ? p.y : 0.f;
         }
         const float2 dpd = __fadd2_rn(
             make_float2(__uint_as_float(dp[e + u]), __uint_as_float(dp[e + u + 1])), ndp);
@@ -394,8 +381,8 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
       for (int i = 0; i < n_it; ++i) {
         const int4 st = P.steps[sb + i / g];
         const int qt = st.x, info = st.y;
-        int lo = 0, hi = 128;
-        if (info & 1) key_query_window(P.slices[info >> 1], key, qt, lo, hi);
+        uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
+        if (info & 1) step_mask<false>(info, P.slices, P.masks, key, qt, vb);
         const float* nl = reinterpret_cast<const float*>(smem + C::kLseOff +
                                                          (sdp_cnt % C::kStages) * C::kLseStageBytes);
         const float* nd = nl + 128;
@@ -407,8 +394,9 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
         tmem_ld64(tS, s);
         tc_fence_before();
         mbar_arrive(bar(C::kBSFree));
-        if (info & 1) pds_half<true>(s, tP, 64 * wg, nl, nd, P.scale_log2, lo, hi, j, p_row);
-        else pds_half<false>(s, tP, 64 * wg, nl, nd, P.scale_log2, 0, 128, j, p_row);
+        const uint32_t m_lo = wg ? vb[2] : vb[0], m_hi = wg ? vb[3] : vb[1];
+        if (info & 1) pds_half<true>(s, tP, 64 * wg, nl, nd, P.scale_log2, m_lo, m_hi, j, p_row);
+        else pds_half<false>(s, tP, 64 * wg, nl, nd, P.scale_log2, m_lo, m_hi, j, p_row);
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
@@ -501,6 +489,7 @@ struct DqParams {
   const int* order;
   int n_items;
   const Slice* slices;
+  const int* masks;  // slice lists of multi-slice visits
   int Tq, Hq, g, qpad;
   float scale, scale_log2;
   const float* nlse2;
@@ -762,15 +751,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           tmem_ld64(tmem + lane_addr + C::kTdP + 64 * wg, dp);
           tc_fence_before();
           mbar_arrive(bar(C::kBDpFree));
-          int lo = 0, hi = 128;
-          if (info & 1) {
-            const Slice sl = P.slices[info >> 1];
-            lo = hi = 0;
-            if (row >= sl.qs && row < sl.qe) {
-              lo = sl.ks + ((sl.t & 2) ? row - sl.qs : 0) - st.x * 128;
-              hi = sl.ke - ((sl.t & 1) ? sl.qe - 1 - row : 0) - st.x * 128;
-            }
-          }
+          uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
+          if (info & 1) step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
+          const uint32_t m_lo = wg ? vb[2] : vb[0], m_hi = wg ? vb[3] : vb[1];
           const uint32_t tSb = tmem + lane_addr + C::kTS0 + 128 * (v & 1) + 64 * wg;
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
@@ -780,13 +763,13 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
               const int lc = 32 * c + e;
-              const int col = 64 * wg + lc;
               const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])),
                                           sc2, nl2);
               float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-              if (info & 1) {
-                p.x = (col >= lo && col < hi) ? p.x : 0.f;
-                p.y = (col + 1 >= lo && col + 1 < hi) ? p.y : 0.f;
+              if (info & 1) {  // lc is this warpgroup's column: m_lo (0-31), m_hi (32-63)
+                const uint32_t mw = lc < 32 ? m_lo : m_hi;
+                p.x = ((mw >> (lc & 31)) & 1u) ? p.x : 0.f;
+                p.y = ((mw >> ((lc + 1) & 31)) & 1u) ? p.y : 0.f;
               }
               const float2 ds = __fmul2_rn(
                   p, __fadd2_rn(make_float2(__uint_as_float(dp[lc]), __uint_as_float(dp[lc + 1])),
@@ -959,6 +942,7 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     P.order = p->bwd_order;
     P.n_items = (int)p->n_bwd_items;
     P.slices = p->slices;
+    P.masks = p->bwd_masks;
     P.Tk = p->Tk;
     P.Hkv = p->Hkv;
     P.g = p->Hq / p->Hkv;
@@ -988,6 +972,7 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     P.order = p->dq_order;
     P.n_items = (int)p->n_dq_items;
     P.slices = p->slices;
+    P.masks = p->fwd_masks;
     P.Tq = p->Tq;
     P.Hq = p->Hq;
     P.g = p->Hq / p->Hkv;

@@ -71,6 +71,7 @@ struct FwdParams {
   const int* order;
   int n_items;
   const Slice* slices;
+  const int* masks;  // slice lists of multi-slice visits
   int Tq, Hq, g;
   float scale_log2;
   __nv_bfloat16* out;
@@ -358,16 +359,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         uint32_t u[128];
         tmem_ld128(tS, u);
         if (info & 1) {
-          // PARTIAL step: keep this row's visible window [lo, hi) of the tile.
-          const Slice sl = P.slices[info >> 1];
-          int lo = 0, hi = 0;
-          if (row >= sl.qs && row < sl.qe) {
-            lo = sl.ks + ((sl.t & 2) ? row - sl.qs : 0) - st.x * 128;
-            hi = sl.ke - ((sl.t & 1) ? sl.qe - 1 - row : 0) - st.x * 128;
-          }
+          // PARTIAL step: keep the keys this row sees under the step's slice(s).
+          uint32_t vb[4];
+          step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
 #pragma unroll
           for (int c = 0; c < 128; ++c)
-            if (c < lo || c >= hi) u[c] = 0xff800000u;  // -inf
+            if (!mask_bit(vb, c)) u[c] = 0xff800000u;  // -inf
         }
         // Row maximum: four independent chains of 3-input max.
         float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
@@ -566,6 +563,7 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   P.order = p->fwd_order;
   P.n_items = (int)p->n_fwd_items;
   P.slices = p->slices;
+  P.masks = p->fwd_masks;
   P.Tq = p->Tq;
   P.Hq = p->Hq;
   P.g = p->Hq / p->Hkv;

@@ -15,10 +15,77 @@ constexpr int kTile = 128;  // q rows and k columns per tile
 // A slice as stored by the plan: [qs, qe) x [ks, ke), mask type t.
 using Slice = SliceDesc;
 
-// Visit info word: (slice << 1) | partial, or -1 when the half skips the step.
+// Visit info of one (q-tile, k-tile) pair (-1 in a step: the half skips it):
+//   (s << 2) | partial   one slice s sees the tile (FULL when bit 0 is clear);
+//   (m << 2) | 3         several slices see parts of it: masks[m] = n and
+//                        masks[m+1 .. m+n] are their indices, ascending.
+// Slices are disjoint, so a FULL tile always has exactly one slice.
 __host__ __device__ constexpr int visit_info(int slice, bool partial) {
-  return (slice << 1) | (partial ? 1 : 0);
+  return (slice << 2) | (partial ? 1 : 0);
 }
+__host__ __device__ constexpr int visit_list_info(int m) { return (m << 2) | 3; }
+
+#ifdef __CUDACC__
+// Adds [lo, hi) (tile-local, any range) to a 128-bit mask of tile columns.
+__device__ __forceinline__ void add_window(int lo, int hi, uint32_t (&b)[4]) {
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int a = max(lo - 32 * w, 0), e = min(hi - 32 * w, 32);
+    if (e > a) b[w] |= (e == 32 ? 0xffffffffu : ((1u << e) - 1u)) & ~((1u << a) - 1u);
+  }
+}
+
+// Keys of k-tile kt that query row `row` sees under slice sl, tile-local.
+__device__ __forceinline__ void row_window(const Slice& sl, int row, int kt, int& lo, int& hi) {
+  lo = hi = 0;
+  if (row >= sl.qs && row < sl.qe) {
+    lo = sl.ks + ((sl.t & 2) ? row - sl.qs : 0) - kt * kTile;
+    hi = sl.ke - ((sl.t & 1) ? sl.qe - 1 - row : 0) - kt * kTile;
+  }
+}
+
+// Query rows of q-tile qt that key `key` is seen by under slice sl, tile-local.
+__device__ __forceinline__ void key_window(const Slice& sl, int key, int qt, int& lo, int& hi) {
+  lo = hi = 0;
+  if (key < sl.ks || key >= sl.ke) return;
+  int a = (sl.t & 1) ? key + sl.qe - sl.ke : sl.qs;
+  a = a > sl.qs ? a : sl.qs;
+  int b = (sl.t & 2) ? key - sl.ks + sl.qs + 1 : sl.qe;
+  b = b < sl.qe ? b : sl.qe;
+  lo = a - qt * kTile;
+  hi = b - qt * kTile;
+}
+
+// Visible columns of one PARTIAL step for one thread's row (kRow: window of
+// query row `pos` over the keys of tile t) or key (window of key `pos` over
+// the queries of tile t): the union over the step's slice or slice list.
+template <bool kRow>
+__device__ __forceinline__ void step_mask(int info, const Slice* __restrict__ slices,
+                                          const int* __restrict__ masks, int pos, int t,
+                                          uint32_t (&b)[4]) {
+  b[0] = b[1] = b[2] = b[3] = 0u;
+  int lo, hi;
+  if ((info & 3) != 3) {
+    const Slice sl = slices[info >> 2];
+    if (kRow) row_window(sl, pos, t, lo, hi);
+    else key_window(sl, pos, t, lo, hi);
+    add_window(lo, hi, b);
+    return;
+  }
+  const int* ml = masks + (info >> 2);
+  const int n = ml[0];
+  for (int i = 0; i < n; ++i) {
+    const Slice sl = slices[ml[1 + i]];
+    if (kRow) row_window(sl, pos, t, lo, hi);
+    else key_window(sl, pos, t, lo, hi);
+    add_window(lo, hi, b);
+  }
+}
+
+__device__ __forceinline__ bool mask_bit(const uint32_t (&b)[4], int c) {
+  return (b[c >> 5] >> (c & 31)) & 1u;
+}
+#endif
 
 // Forward step (int4): x = k-tile, y = info for half 0, z = info for half 1.
 // Forward item (8 x int32):
@@ -59,8 +126,12 @@ struct ffa_plan_s {
   int* merges = nullptr;
   int64_t n_merges = 0;
   int n_slots = 0;  // partial-result slots (split forward items)
+  int* fwd_masks = nullptr;  // slice lists of multi-slice forward visits
+  int64_t n_fwd_masks = 0;
   int4* bwd_steps = nullptr;
   int64_t n_bwd_steps = 0;
+  int* bwd_masks = nullptr;  // slice lists of multi-slice backward visits
+  int64_t n_bwd_masks = 0;
   int* bwd_items = nullptr;
   int64_t n_bwd_items = 0;
   int* bwd_order = nullptr;

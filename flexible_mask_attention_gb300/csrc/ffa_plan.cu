@@ -137,33 +137,26 @@ __global__ void k_scan(const int* __restrict__ in, int n, int* __restrict__ out,
   if (t == T - 1) *total = part[t];
 }
 
-// ---- forward visits ---------------------------------------------------------
-__global__ void k_fwd_visit_count(const Slice* __restrict__ sl, const int* __restrict__ list,
-                                  const int* __restrict__ loff, const int* __restrict__ lcnt,
-                                  int n_qt, int* cnt) {
-  const int qt = blockIdx.x * blockDim.x + threadIdx.x;
-  if (qt >= n_qt) return;
-  int c = 0;
-  for (int i = 0; i < lcnt[qt]; ++i) {
-    TileRun r;
-    if (fwd_tile_run(sl[list[loff[qt] + i]], qt, r)) c += r.e - r.b;
-  }
-  cnt[qt] = c;
-}
-
-// Emits the (tile index, info) visits of one tile in (index, slice) order,
-// one warp per tile: the lanes collect the runs of the slices in the tile's
-// list (kept in shared memory, in slice order), then walk the visited range
-// 32 positions at a time; a warp scan of the per-position counts gives every
-// lane its output offset.  Tiles with more than kMaxLocalSegs runs re-read
-// the list for every position instead.
+// ---- visits -----------------------------------------------------------------
+// One warp per tile: the lanes collect the runs of the slices in the tile's
+// list (kept in shared memory, in slice order), then walk the tile's visited
+// range 32 positions at a time.  A position seen by one slice becomes one
+// visit with that slice's info; a position seen by several (all PARTIAL,
+// since slices are disjoint) becomes one visit whose info points at a slice
+// list [n, s_0 .. s_n-1] in `masks`.  Warp scans of the per-position counts
+// place visits and list entries, so the output never depends on scheduling.
+// Count mode (kCount) only stores the tile's visit and list-word totals.
+// Tiles with more than kMaxLocalSegs runs re-read the slice list for every
+// position instead of shared memory.
 constexpr int kFillWarps = 4;
 
-template <bool kFwd>
+template <bool kFwd, bool kCount>
 __global__ void __launch_bounds__(32 * kFillWarps)
-    k_visit_fill_warp(const Slice* __restrict__ sl, const int* __restrict__ list,
-                      const int* __restrict__ loff, const int* __restrict__ lcnt, int n_tiles,
-                      const int* __restrict__ off, int2* visits) {
+    k_visit_warp(const Slice* __restrict__ sl, const int* __restrict__ list,
+                 const int* __restrict__ loff, const int* __restrict__ lcnt, int n_tiles,
+                 int* __restrict__ vcnt, int* __restrict__ mcnt, const int* __restrict__ voff,
+                 const int* __restrict__ moff, int2* __restrict__ visits,
+                 int* __restrict__ masks) {
   __shared__ TileRun seg[kFillWarps][kMaxLocalSegs];
   __shared__ int seg_s[kFillWarps][kMaxLocalSegs];
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -194,46 +187,64 @@ __global__ void __launch_bounds__(32 * kFillWarps)
   }
   __syncwarp();
   const bool overflow = nseg > kMaxLocalSegs;
-  int base = off[tile];
+  const int n_src = overflow ? S : nseg;
+  // run i of this tile (slice index in *s); false when the slice has none
+  auto run_of = [&](int i, TileRun& r, int& s) -> bool {
+    if (!overflow) {
+      r = seg[wib][i];
+      s = seg_s[wib][i];
+      return true;
+    }
+    s = L[i];
+    return kFwd ? fwd_tile_run(sl[s], tile, r) : bwd_tile_run(sl[s], tile, r);
+  };
+  int vbase = kCount ? 0 : voff[tile], mbase = kCount ? 0 : moff[tile];
   for (int x0 = lo; x0 < hi; x0 += 32) {
     const int x = x0 + lane;
-    int cnt = 0;
+    int cnt = 0, first_s = 0;
+    bool first_partial = false;
     if (x < hi) {
-      if (!overflow) {
-        for (int i = 0; i < nseg; ++i) cnt += (x >= seg[wib][i].b && x < seg[wib][i].e) ? 1 : 0;
-      } else {
-        for (int i = 0; i < S; ++i) {
-          TileRun r;
-          const int s = L[i];
-          const bool ok = kFwd ? fwd_tile_run(sl[s], tile, r) : bwd_tile_run(sl[s], tile, r);
-          cnt += (ok && x >= r.b && x < r.e) ? 1 : 0;
+      for (int i = 0; i < n_src; ++i) {
+        TileRun r;
+        int s;
+        if (run_of(i, r, s) && x >= r.b && x < r.e) {
+          if (cnt == 0) {
+            first_s = s;
+            first_partial = !(x >= r.fb && x < r.fe);
+          }
+          ++cnt;
         }
       }
     }
-    int incl = cnt;
+    const int vis = cnt > 0 ? 1 : 0, msz = cnt >= 2 ? cnt + 1 : 0;
+    int vi = vis, mi = msz;
     for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += v;
-    }
-    if (cnt > 0) {
-      int w = base + incl - cnt;
-      if (!overflow) {
-        for (int i = 0; i < nseg; ++i) {
-          const TileRun r = seg[wib][i];
-          if (x >= r.b && x < r.e)
-            visits[w++] = make_int2(x, visit_info(seg_s[wib][i], !(x >= r.fb && x < r.fe)));
-        }
-      } else {
-        for (int i = 0; i < S; ++i) {
-          TileRun r;
-          const int s = L[i];
-          const bool ok = kFwd ? fwd_tile_run(sl[s], tile, r) : bwd_tile_run(sl[s], tile, r);
-          if (ok && x >= r.b && x < r.e)
-            visits[w++] = make_int2(x, visit_info(s, !(x >= r.fb && x < r.fe)));
-        }
+      const int a = __shfl_up_sync(0xffffffffu, vi, d), b = __shfl_up_sync(0xffffffffu, mi, d);
+      if (lane >= d) {
+        vi += a;
+        mi += b;
       }
     }
-    base += __shfl_sync(0xffffffffu, incl, 31);
+    if (!kCount && cnt > 0) {
+      int info = visit_info(first_s, first_partial);
+      if (cnt >= 2) {
+        int m = mbase + mi - msz;
+        info = visit_list_info(m);
+        masks[m++] = cnt;
+        for (int i = 0; i < n_src; ++i) {
+          TileRun r;
+          int s;
+          if (run_of(i, r, s) && x >= r.b && x < r.e) masks[m++] = s;
+        }
+      }
+      visits[vbase + vi - vis] = make_int2(x, info);
+    }
+    vbase += __shfl_sync(0xffffffffu, vi, 31);
+    mbase += __shfl_sync(0xffffffffu, mi, 31);
+  }
+  if (kCount && lane == 0) {
+    vcnt[tile] = vbase;
+    mcnt[tile] = mbase;
   }
 }
 
@@ -391,21 +402,7 @@ __global__ void k_split_fill(const int* __restrict__ items, int n_items,
   }
 }
 
-// ---- backward visits --------------------------------------------------------
-__global__ void k_bwd_visit_count(const Slice* __restrict__ sl, const int* __restrict__ list,
-                                  const int* __restrict__ loff, const int* __restrict__ lcnt,
-                                  int n_kt, int* cnt) {
-  const int kt = blockIdx.x * blockDim.x + threadIdx.x;
-  if (kt >= n_kt) return;
-  int c = 0;
-  for (int i = 0; i < lcnt[kt]; ++i) {
-    TileRun r;
-    if (bwd_tile_run(sl[list[loff[kt] + i]], kt, r)) c += r.e - r.b;
-  }
-  cnt[kt] = c;
-}
-
-
+// ---- backward items ---------------------------------------------------------
 __global__ void k_bwd_items(int n_kt, int Hkv, int g, const int2* __restrict__ visits,
                             const int* __restrict__ off, const int* __restrict__ cnt,
                             int4* steps, int* items) {
@@ -530,7 +527,8 @@ ffa_status_t sort_items(const int* items, int words, int cost_word, int head_wor
 void free_plan(ffa_plan_s* p) {
   if (!p) return;
   void* bufs[] = {p->slices, p->fwd_steps, p->fwd_items, p->fwd_order, p->merges,
-                  p->bwd_steps, p->bwd_items, p->bwd_order, p->err};
+                  p->bwd_steps, p->bwd_items, p->bwd_order, p->err, p->fwd_masks,
+                  p->bwd_masks};
   for (void* b : bufs)
     if (b) cudaFree(b);
   if (!p->dq_alias) {
@@ -612,21 +610,28 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   p->area = (int64_t)harea;
 
   // forward visits
-  DevBuf vcnt(st), voff(st), visits(st);
+  DevBuf vcnt(st), voff(st), visits(st), fmcnt(st), fmoff(st);
   FFA_CUDA(vcnt.alloc(sizeof(int) * n_qt));
   FFA_CUDA(voff.alloc(sizeof(int) * n_qt));
-  k_fwd_visit_count<<<grid_for(n_qt, 128), 128, 0, st>>>(p->slices, qlist.as<int>(),
-                                                         qloff.as<int>(), qlcnt.as<int>(), n_qt,
-                                                         vcnt.as<int>());
+  FFA_CUDA(fmcnt.alloc(sizeof(int) * n_qt));
+  FFA_CUDA(fmoff.alloc(sizeof(int) * n_qt));
+  k_visit_warp<true, true><<<grid_for(n_qt, kFillWarps), 32 * kFillWarps, 0, st>>>(
+      p->slices, qlist.as<int>(), qloff.as<int>(), qlcnt.as<int>(), n_qt, vcnt.as<int>(),
+      fmcnt.as<int>(), nullptr, nullptr, nullptr, nullptr);
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
   rc = scan(vcnt.as<int>(), n_qt, voff.as<int>(), dtot, &tot, st);
   if (rc != FFA_OK) return rc;
   if (tot > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
   FFA_CUDA(visits.alloc(sizeof(int2) * (size_t)tot));
-  k_visit_fill_warp<true><<<grid_for(n_qt, kFillWarps), 32 * kFillWarps, 0, st>>>(
-      p->slices, qlist.as<int>(), qloff.as<int>(), qlcnt.as<int>(), n_qt, voff.as<int>(),
-      visits.as<int2>());
+  long long mtot = 0;
+  if ((rc = scan(fmcnt.as<int>(), n_qt, fmoff.as<int>(), dtot, &mtot, st))) return rc;
+  if (mtot > (1LL << 29)) return FFA_ERR_UNSUPPORTED;
+  p->n_fwd_masks = mtot;
+  FFA_CUDA(cudaMalloc(&p->fwd_masks, sizeof(int) * (size_t)std::max(1LL, mtot)));
+  k_visit_warp<true, false><<<grid_for(n_qt, kFillWarps), 32 * kFillWarps, 0, st>>>(
+      p->slices, qlist.as<int>(), qloff.as<int>(), qlcnt.as<int>(), n_qt, nullptr, nullptr,
+      voff.as<int>(), fmoff.as<int>(), visits.as<int2>(), p->fwd_masks);
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
   // forward units -> steps
@@ -731,12 +736,14 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   p->grid_dq = (int)std::max<int64_t>(1, std::min<int64_t>(p->num_sms, p->n_dq_items));
 
   // backward
-  DevBuf bcnt(st), boff(st), bvis(st);
+  DevBuf bcnt(st), boff(st), bvis(st), bmcnt(st), bmoff(st);
   FFA_CUDA(bcnt.alloc(sizeof(int) * n_kt));
   FFA_CUDA(boff.alloc(sizeof(int) * n_kt));
-  k_bwd_visit_count<<<grid_for(n_kt, 128), 128, 0, st>>>(p->slices, klist.as<int>(),
-                                                         kloff.as<int>(), klcnt.as<int>(), n_kt,
-                                                         bcnt.as<int>());
+  FFA_CUDA(bmcnt.alloc(sizeof(int) * n_kt));
+  FFA_CUDA(bmoff.alloc(sizeof(int) * n_kt));
+  k_visit_warp<false, true><<<grid_for(n_kt, kFillWarps), 32 * kFillWarps, 0, st>>>(
+      p->slices, klist.as<int>(), kloff.as<int>(), klcnt.as<int>(), n_kt, bcnt.as<int>(),
+      bmcnt.as<int>(), nullptr, nullptr, nullptr, nullptr);
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
   if ((rc = scan(bcnt.as<int>(), n_kt, boff.as<int>(), dtot, &tot, st))) return rc;
@@ -744,9 +751,14 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   p->n_bwd_steps = tot;
   FFA_CUDA(bvis.alloc(sizeof(int2) * (size_t)tot));
   FFA_CUDA(cudaMalloc(&p->bwd_steps, sizeof(int4) * (size_t)std::max(1LL, tot)));
-  k_visit_fill_warp<false><<<grid_for(n_kt, kFillWarps), 32 * kFillWarps, 0, st>>>(
-      p->slices, klist.as<int>(), kloff.as<int>(), klcnt.as<int>(), n_kt, boff.as<int>(),
-      bvis.as<int2>());
+  long long bmtot = 0;
+  if ((rc = scan(bmcnt.as<int>(), n_kt, bmoff.as<int>(), dtot, &bmtot, st))) return rc;
+  if (bmtot > (1LL << 29)) return FFA_ERR_UNSUPPORTED;
+  p->n_bwd_masks = bmtot;
+  FFA_CUDA(cudaMalloc(&p->bwd_masks, sizeof(int) * (size_t)std::max(1LL, bmtot)));
+  k_visit_warp<false, false><<<grid_for(n_kt, kFillWarps), 32 * kFillWarps, 0, st>>>(
+      p->slices, klist.as<int>(), kloff.as<int>(), klcnt.as<int>(), n_kt, nullptr, nullptr,
+      boff.as<int>(), bmoff.as<int>(), bvis.as<int2>(), p->bwd_masks);
   note_launches(1);
   const long long nb_items = (long long)n_kt * p->Hkv;
   p->n_bwd_items = nb_items;
@@ -874,6 +886,8 @@ ffa_status_t ffa_plan_info(ffa_plan_t p, ffa_plan_info_t* info) {
   info->grid_fwd = p->grid_fwd;
   info->grid_bwd = p->grid_bwd;
   info->area = p->area;
+  info->fwd_masks = p->n_fwd_masks;
+  info->bwd_masks = p->n_bwd_masks;
   return FFA_OK;
 }
 
@@ -890,6 +904,8 @@ ffa_status_t ffa_plan_export(ffa_plan_t p, int32_t which, int32_t* dst, int64_t 
     case 4: src = p->bwd_items; words = kBiWords * p->n_bwd_items; break;
     case 5: src = p->bwd_order; words = p->n_bwd_items; break;
     case 6: src = p->merges; words = kMgWords * p->n_merges; break;
+    case 7: src = p->fwd_masks; words = p->n_fwd_masks; break;
+    case 8: src = p->bwd_masks; words = p->n_bwd_masks; break;
     default: return FFA_ERR_INVALID_ARG;
   }
   *written = words;

@@ -7,7 +7,10 @@ a tile FULL when it holds 128 * 128 visible entries and PARTIAL when it holds
 at least one.  The rest (pairing, merging, costs, splitting, ordering) follows
 the work-list specification of the planner:
 
-  * forward visits of a q-tile: (kt, slice) pairs sorted by (kt, slice);
+  * forward visits of a q-tile: one per k-tile seen, in kt order; info is
+    (slice << 2) | partial when one slice sees the tile pair, else
+    (m << 2) | 3 with a slice list [n, s_0, ..] (ascending) at offset m of
+    the direction's list array (lists appended in tile, then kt order);
   * grouped heads (Hq/Hkv >= 2): a unit is one q-tile, items are pairs of
     query heads of one kv head; otherwise a unit is q-tiles (2u, 2u+1), items
     one per head, steps merge the two visit lists on kt;
@@ -16,8 +19,8 @@ the work-list specification of the planner:
     live)) chunks per item, capped by its step count, step ranges
     b + k*n//c .. b + (k+1)*n//c, cost scaled by the chunk's share;
   * order: kv head ascending, then cost descending, then item index;
-  * backward: per k-tile (qt, slice) visits sorted by (qt, slice), one item
-    per (kt, kv head), cost g * sum of visit costs.
+  * backward: per k-tile one visit per q-tile seen, merged the same way, one
+    item per (kt, kv head), cost g * sum of visit costs.
 """
 from __future__ import annotations
 
@@ -81,7 +84,25 @@ def visible_area(q_ranges, k_ranges, mask_types) -> int:
 
 
 def _info(s, count):
-    return (s << 1) | (0 if count == TILE * TILE else 1)
+    return (s << 2) | (0 if count == TILE * TILE else 1)
+
+
+def _merge(visits, masks):
+    """Sorted (x, slice, info) visits of one tile -> one (x, info) per x;
+    x seen by several slices gets a slice list appended to ``masks``."""
+    out, i = [], 0
+    while i < len(visits):
+        j = i
+        while j < len(visits) and visits[j][0] == visits[i][0]:
+            j += 1
+        if j - i == 1:
+            out.append((visits[i][0], visits[i][2]))
+        else:
+            out.append((visits[i][0], (len(masks) << 2) | 3))
+            masks.append(j - i)
+            masks.extend(v[1] for v in visits[i:j])
+        i = j
+    return out
 
 
 def _cost(info):
@@ -101,8 +122,9 @@ def plan(total_q, total_k, num_heads_q, num_heads_kv, q_ranges, k_ranges, mask_t
         for (qt, kt), c in d.items():
             fvis[qt].append((kt, s, _info(s, c)))
             bvis[kt].append((qt, s, _info(s, c)))
-    fvis = [[(kt, info) for kt, _, info in sorted(v)] for v in fvis]
-    bvis = [[(qt, info) for qt, _, info in sorted(v)] for v in bvis]
+    fmasks, bmasks = [], []
+    fvis = [_merge(sorted(v), fmasks) for v in fvis]
+    bvis = [_merge(sorted(v), bmasks) for v in bvis]
 
     # forward units and steps
     pair_mode = 0 if g >= 2 else 1
@@ -196,6 +218,8 @@ def plan(total_q, total_k, num_heads_q, num_heads_kv, q_ranges, k_ranges, mask_t
         "bwd_items": bwd_items,
         "bwd_order": order_of([it[4] for it in bitems], [it[1] for it in bitems]),
         "merges": np.array(merges, dtype=np.int32).reshape(-1, 8),
+        "fwd_masks": np.array(fmasks, dtype=np.int32).reshape(-1, 1),
+        "bwd_masks": np.array(bmasks, dtype=np.int32).reshape(-1, 1),
         "n_slots": n_slots,
         "grid_fwd": max(1, min(num_sms, len(items))),
         "grid_bwd": max(1, min(num_sms, len(bitems))),

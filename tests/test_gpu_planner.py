@@ -9,7 +9,8 @@ from oracle import planner
 
 pytestmark = pytest.mark.gpu
 
-NAMES = ["fwd_steps", "fwd_items", "fwd_order", "bwd_steps", "bwd_items", "bwd_order", "merges"]
+NAMES = ["fwd_steps", "fwd_items", "fwd_order", "bwd_steps", "bwd_items", "bwd_order", "merges",
+         "fwd_masks", "bwd_masks"]
 
 
 def compare(qr, kr, ty, Tq, Tk, Hq, Hkv, D, split_below=0):

@@ -147,7 +147,8 @@ def test_plan_split_and_order_rules():
     wl = W.tiny_causal_docs()
     p = planner.plan(256, 256, 1, 1, wl.q_ranges, wl.k_ranges, wl.mask_types, num_sms=152)
     # one unit (q-tiles 0, 1), two steps, split into two single-step chunks
-    assert p["fwd_steps"].tolist() == [[0, 1, -1, 0], [1, -1, 3, 0]]
+    # info = (slice << 2) | partial
+    assert p["fwd_steps"].tolist() == [[0, 1, -1, 0], [1, -1, 5, 0]]
     assert p["fwd_items"].tolist() == [[0, 1, 0, 0, 0, 1, 0, 5], [0, 1, 0, 0, 1, 2, 1, 5]]
     assert p["merges"].tolist() == [[0, 1, 0, 0, 0, 2, 0, 0]]
     q = planner.plan(256, 256, 1, 1, wl.q_ranges, wl.k_ranges, wl.mask_types, num_sms=152,
