@@ -170,7 +170,14 @@ def oracle_sample(wl, q, k, v, do, seconds: float, seed: int = 0):
     D, Hq = wl.head_dim, wl.num_heads_q
     # per-row visible counts, to credit the work
     counts = np.zeros(wl.total_q, dtype=np.int64)
-    for (qs, qe), (ks, ke), t in zip(wl.q_ranges, wl.k_ranges, wl.mask_types):
+    qr, kr, ty = (np.asarray(a, dtype=np.int64) for a in (wl.q_ranges, wl.k_ranges,
+                                                          wl.mask_types))
+    full = (ty == 0) & (qr[:, 1] > qr[:, 0]) & (kr[:, 1] > kr[:, 0])
+    diff = np.zeros(wl.total_q + 1, dtype=np.int64)  # full slices: one add per range end
+    np.add.at(diff, qr[full, 0], kr[full, 1] - kr[full, 0])
+    np.add.at(diff, qr[full, 1], -(kr[full, 1] - kr[full, 0]))
+    counts += np.cumsum(diff)[:-1]
+    for (qs, qe), (ks, ke), t in zip(qr[~full], kr[~full], ty[~full]):
         if qe > qs and ke > ks:
             rows, lo, hi = planner.row_intervals(int(qs), int(qe), int(ks), int(ke), int(t))
             counts[rows] += np.clip(hi - lo, 0, None)

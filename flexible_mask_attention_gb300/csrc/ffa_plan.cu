@@ -96,16 +96,56 @@ __global__ void __launch_bounds__(kListThreads)
 
 // Two non-empty slices overlap iff their rectangles meet; then they share a
 // row, hence a q-tile, so only pairs within one q-tile's list are compared.
+// Lists of up to kSweepMax slices are sorted by k start in shared memory and
+// swept: slice i is compared only with the following slices that start
+// before its k end (the only ones whose k range can meet it).  Longer lists
+// compare every pair.
+constexpr int kSweepMax = 4096;
+
 __global__ void __launch_bounds__(kListThreads)
     k_check_overlap(const Slice* __restrict__ sl, const int* __restrict__ list,
                     const int* __restrict__ off, const int* __restrict__ cnt, int* flags) {
+  __shared__ unsigned long long key[kSweepMax];  // (k start << 32) | list position
   const int* L = list + off[blockIdx.x];
   const int n = cnt[blockIdx.x];
+  if (n > kSweepMax) {
+    for (int i = threadIdx.x; i < n; i += kListThreads) {
+      const Slice a = sl[L[i]];
+      for (int j = i + 1; j < n; ++j) {
+        const Slice b = sl[L[j]];
+        if (a.qs < b.qe && b.qs < a.qe && a.ks < b.ke && b.ks < a.ke) {
+          atomicExch(&flags[1], 1);
+          return;
+        }
+      }
+    }
+    return;
+  }
+  int n2 = 1;
+  while (n2 < n) n2 <<= 1;
+  for (int i = threadIdx.x; i < n2; i += kListThreads)
+    key[i] = i < n ? ((unsigned long long)(unsigned)sl[L[i]].ks << 32) | (unsigned)i : ~0ull;
+  __syncthreads();
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n2; i += kListThreads) {
+        const int l = i ^ j;
+        if (l > i) {
+          const unsigned long long a = key[i], b = key[l];
+          if ((a > b) == ((i & k) == 0)) {
+            key[i] = b;
+            key[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
   for (int i = threadIdx.x; i < n; i += kListThreads) {
-    const Slice a = sl[L[i]];
-    for (int j = i + 1; j < n; ++j) {
-      const Slice b = sl[L[j]];
-      if (a.qs < b.qe && b.qs < a.qe && a.ks < b.ke && b.ks < a.ke) {
+    const Slice a = sl[L[key[i] & 0xffffffffu]];
+    for (int j = i + 1; j < n && (int)(key[j] >> 32) < a.ke; ++j) {
+      const Slice b = sl[L[key[j] & 0xffffffffu]];
+      if (a.qs < b.qe && b.qs < a.qe) {  // k ranges meet: b.ks in [a.ks, a.ke)
         atomicExch(&flags[1], 1);
         return;
       }
