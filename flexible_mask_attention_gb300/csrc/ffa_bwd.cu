@@ -71,11 +71,12 @@ struct KvCfg {
                        kBSdpFull = 2 + 4 * kStages, kBSFree = kBSdpFull + 1,
                        kBPFull = kBSFree + 1, kBDkvFull = kBPFull + 1,
                        kBDkvEmpty = kBDkvFull + 1, kBDrain = kBDkvEmpty + 1,
-                       kNumBars = kBDrain + 1;
+                       kBSFull = kBDrain + 1, kNumBars = kBSFull + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   // The dynamic shared memory base must be 1024-byte aligned (checked on entry).
   static constexpr int kSmemBytes = kMiscOff + 64;
   static constexpr int kTdV = 0, kTdK = D, kTS = 2 * D, kTdP = 2 * D + 128;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
 struct KvParams {
@@ -187,6 +188,7 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
       mbar_init(bar(C::kBDOEmpty + s), 1);
     }
     mbar_init(bar(C::kBSdpFull), 1);
+    mbar_init(bar(C::kBSFull), 1);
     mbar_init(bar(C::kBSFree), 256);
     mbar_init(bar(C::kBPFull), 256);
     mbar_init(bar(C::kBDkvFull), 1);
@@ -299,6 +301,7 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
           if (!(ok = mbar_wait(bar(C::kBQFull + stage), (q_cnt / C::kStages) & 1, ctl, 501))) break;
           tc_fence_after();
           issue_st(stage);
+          mma_commit(bar(C::kBSFull));
         }
         for (int i = 0; i < n_it; ++i) {
           const uint32_t c = q_cnt + (uint32_t)i;
@@ -325,6 +328,7 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
             if (!(ok = mbar_wait(bar(C::kBQFull + st1), (c1 / C::kStages) & 1, ctl, 504))) break;
             tc_fence_after();
             issue_st(st1);
+            mma_commit(bar(C::kBSFull));
           }
           if (!(ok = mbar_wait(bar(C::kBPFull), p_cnt & 1, ctl, 505))) break;
           ++p_cnt;
@@ -378,22 +382,29 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
       const int kt = it[kBiKt], hk = it[kBiHkv];
       const int key = kt * 128 + j;
       const int n_it = (se - sb) * g;
+      int4 st_next = n_it > 0 ? P.steps[sb] : make_int4(0, -1, -1, 0);
       for (int i = 0; i < n_it; ++i) {
-        const int4 st = P.steps[sb + i / g];
+        const int4 st = st_next;
+        if (i + 1 < n_it) st_next = P.steps[sb + (i + 1) / g];  // prefetch the next descriptor
         const int qt = st.x, info = st.y;
         uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
         if (info & 1) step_mask<false>(info, P.slices, P.masks, key, qt, vb);
         const float* nl = reinterpret_cast<const float*>(smem + C::kLseOff +
                                                          (sdp_cnt % C::kStages) * C::kLseStageBytes);
         const float* nd = nl + 128;
-        const bool w = mbar_wait(bar(C::kBSdpFull), sdp_cnt & 1, ctl, 600);
+        // S^T first: its buffer is released before dP^T is even complete, so
+        // the next S^T can follow dP^T on the tensor pipe at once.
+        const bool w = mbar_wait(bar(C::kBSFull), sdp_cnt & 1, ctl, 600);
         if (!(ok = __all_sync(0xffffffffu, w))) break;
-        ++sdp_cnt;
         tc_fence_after();
         uint32_t s[64];
         tmem_ld64(tS, s);
         tc_fence_before();
         mbar_arrive(bar(C::kBSFree));
+        const bool w2 = mbar_wait(bar(C::kBSdpFull), sdp_cnt & 1, ctl, 601);
+        if (!(ok = __all_sync(0xffffffffu, w2))) break;
+        ++sdp_cnt;
+        tc_fence_after();
         const uint32_t m_lo = wg ? vb[2] : vb[0], m_hi = wg ? vb[3] : vb[1];
         if (info & 1) pds_half<true>(s, tP, 64 * wg, nl, nd, P.scale_log2, m_lo, m_hi, j, p_row);
         else pds_half<false>(s, tP, 64 * wg, nl, nd, P.scale_log2, m_lo, m_hi, j, p_row);
@@ -467,26 +478,32 @@ struct DqCfg {
   static constexpr int kThreads = kSplitThreads;
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kStages = 2;
+  // K is read by the S MMA of a step and again by its dQ MMA at the end, so
+  // it gets the deeper ring; V (read by the dP MMA only) is released as soon
+  // as that MMA completes.
+  static constexpr int kKStages = D == 128 ? 3 : 4;
+  static constexpr int kVStages = D == 128 ? 2 : 4;
   static constexpr int kQOff = 0;
   static constexpr int kDOOff = kTileBytes;
   static constexpr int kKOff = 2 * kTileBytes;
-  static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-  static constexpr int kBQFull = 0, kBQEmpty = 1, kBKFull = 2, kBKEmpty = 2 + kStages,
-                       kBVFull = 2 + 2 * kStages, kBVEmpty = 2 + 3 * kStages,
-                       kBSdFull = 2 + 4 * kStages, kBDpFree = kBSdFull + 1,
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+  static constexpr int kBQFull = 0, kBQEmpty = 1, kBKFull = 2, kBKEmpty = kBKFull + kKStages,
+                       kBVFull = kBKEmpty + kKStages, kBVEmpty = kBVFull + kVStages,
+                       kBSdFull = kBVEmpty + kVStages, kBDpFree = kBSdFull + 1,
                        kBDsFull = kBDpFree + 1, kBDqFull = kBDsFull + 1,
                        kBDqEmpty = kBDqFull + 1, kBDrain = kBDqEmpty + 1, kNumBars = kBDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64;
   static constexpr int kTS0 = 0, kTdP = 256, kTdQ = 384;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
 struct DqParams {
   const int4* steps;
   const int* items;
   const int* order;
+  const int* counts;  // visits of each half of an item
   int n_items;
   const Slice* slices;
   const int* masks;  // slice lists of multi-slice visits
@@ -499,11 +516,12 @@ struct DqParams {
   uint64_t wait_ns;
 };
 
-__device__ __forceinline__ bool dq_item_at(const DqParams& P, int r, const int*& it) {
+__device__ __forceinline__ bool dq_item_at(const DqParams& P, int r, const int*& it, int& idx) {
   const int G = gridDim.x, b = blockIdx.x;
   const int pos = r * G + ((r & 1) ? (G - 1 - b) : b);
   if (pos >= P.n_items) return false;
-  it = P.items + (size_t)P.order[pos] * kFiWords;
+  idx = P.order[pos];
+  it = P.items + (size_t)idx * kFiWords;
   return true;
 }
 
@@ -539,9 +557,11 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(C::kBQFull), 1);
     mbar_init(bar(C::kBQEmpty), 1);
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(bar(C::kBKFull + s), 1);
       mbar_init(bar(C::kBKEmpty + s), 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
       mbar_init(bar(C::kBVFull + s), 1);
       mbar_init(bar(C::kBVEmpty + s), 1);
     }
@@ -572,13 +592,13 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       uint32_t kv_cnt = 0, q_cnt = 0;
       bool ok = true, k_only = false;
       const int* it;
-      for (int r = 0; ok && dq_item_at(P, r, it); ++r) {
+      int idx = 0;
+      for (int r = 0; ok && dq_item_at(P, r, it, idx); ++r) {
         const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
         if (se <= sb) continue;
         for (int h = 0; ok && h < 2; ++h) {
           if (!half_active(it, h)) continue;
-          int n = 0;
-          for (int j = sb; j < se; ++j) n += half_info(P.steps[j], h) >= 0 ? 1 : 0;
+          const int n = P.counts[2 * idx + h];
           if (n == 0) continue;
           const int qt = it[kFiQt0 + h], head = it[kFiH0 + h], hk = head / P.g;
           if (!(ok = mbar_wait(bar(C::kBQEmpty), (q_cnt & 1) ^ 1, ctl, 800))) break;
@@ -593,32 +613,32 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           for (int j = sb; j < se; ++j) {
             const int4 st = P.steps[j];
             if (half_info(st, h) < 0) continue;
-            const int stage = kv_cnt % C::kStages;
-            const uint32_t ph = (kv_cnt / C::kStages) & 1;
-            if (!(ok = mbar_wait(bar(C::kBKEmpty + stage), ph ^ 1, ctl, 801))) break;
-            mbar_arrive_expect_tx(bar(C::kBKFull + stage), C::kTileBytes);
+            const int ks = kv_cnt % C::kKStages, vs = kv_cnt % C::kVStages;
+            const uint32_t kph = (kv_cnt / C::kKStages) & 1, vph = (kv_cnt / C::kVStages) & 1;
+            if (!(ok = mbar_wait(bar(C::kBKEmpty + ks), kph ^ 1, ctl, 801))) break;
+            mbar_arrive_expect_tx(bar(C::kBKFull + ks), C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c)
-              tma_load_2d(sbase + C::kKOff + stage * C::kTileBytes + c * 16384, &tm_k,
-                          bar(C::kBKFull + stage), hk * D + c * 64, st.x * 128);
+              tma_load_2d(sbase + C::kKOff + ks * C::kTileBytes + c * 16384, &tm_k,
+                          bar(C::kBKFull + ks), hk * D + c * 64, st.x * 128);
             k_only = true;
-            if (!(ok = mbar_wait(bar(C::kBVEmpty + stage), ph ^ 1, ctl, 802))) break;
+            if (!(ok = mbar_wait(bar(C::kBVEmpty + vs), vph ^ 1, ctl, 802))) break;
             k_only = false;
-            mbar_arrive_expect_tx(bar(C::kBVFull + stage), C::kTileBytes);
+            mbar_arrive_expect_tx(bar(C::kBVFull + vs), C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c)
-              tma_load_2d(sbase + C::kVOff + stage * C::kTileBytes + c * 16384, &tm_v,
-                          bar(C::kBVFull + stage), hk * D + c * 64, st.x * 128);
+              tma_load_2d(sbase + C::kVOff + vs * C::kTileBytes + c * 16384, &tm_v,
+                          bar(C::kBVFull + vs), hk * D + c * 64, st.x * 128);
             ++kv_cnt;
           }
         }
       }
       if (!ok) {
         if (q_cnt > 0) drain_wait_b(bar(C::kBQFull), (q_cnt - 1) & 1, kDrainNs);
-        for (uint32_t i = kv_cnt > (uint32_t)C::kStages ? kv_cnt - C::kStages : 0; i < kv_cnt; ++i) {
-          drain_wait_b(bar(C::kBKFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
-          drain_wait_b(bar(C::kBVFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
-        }
+        for (uint32_t i = kv_cnt > (uint32_t)C::kKStages ? kv_cnt - C::kKStages : 0; i < kv_cnt; ++i)
+          drain_wait_b(bar(C::kBKFull + i % C::kKStages), (i / C::kKStages) & 1, kDrainNs);
+        for (uint32_t i = kv_cnt > (uint32_t)C::kVStages ? kv_cnt - C::kVStages : 0; i < kv_cnt; ++i)
+          drain_wait_b(bar(C::kBVFull + i % C::kVStages), (i / C::kVStages) & 1, kDrainNs);
         if (k_only)
-          drain_wait_b(bar(C::kBKFull + kv_cnt % C::kStages), (kv_cnt / C::kStages) & 1, kDrainNs);
+          drain_wait_b(bar(C::kBKFull + kv_cnt % C::kKStages), (kv_cnt / C::kKStages) & 1, kDrainNs);
       }
     }
   } else if (warp == 9) {
@@ -651,44 +671,44 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       uint32_t kv_cnt = 0, q_cnt = 0, dpf_cnt = 0, ds_cnt = 0, dqe_cnt = 0;
       bool ok = true;
       const int* it;
-      for (int r = 0; ok && dq_item_at(P, r, it); ++r) {
+      int idx = 0;
+      for (int r = 0; ok && dq_item_at(P, r, it, idx); ++r) {
         const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
         if (se <= sb) continue;
         for (int h = 0; ok && h < 2; ++h) {
           if (!half_active(it, h)) continue;
-          int n = 0;
-          for (int j = sb; j < se; ++j) n += half_info(P.steps[j], h) >= 0 ? 1 : 0;
+          const int n = P.counts[2 * idx + h];
           if (n == 0) continue;
           if (!(ok = mbar_wait(bar(C::kBQFull), q_cnt & 1, ctl, 900))) break;
           ++q_cnt;
           tc_fence_after();
           {  // step 0: S and dP
-            const int stage = kv_cnt % C::kStages;
-            const uint32_t ph = (kv_cnt / C::kStages) & 1;
-            if (!(ok = mbar_wait(bar(C::kBKFull + stage), ph, ctl, 901))) break;
+            const int ks = kv_cnt % C::kKStages, vs = kv_cnt % C::kVStages;
+            if (!(ok = mbar_wait(bar(C::kBKFull + ks), (kv_cnt / C::kKStages) & 1, ctl, 901))) break;
             tc_fence_after();
-            issue_s(0, stage);
-            if (!(ok = mbar_wait(bar(C::kBVFull + stage), ph, ctl, 902))) break;
+            issue_s(0, ks);
+            if (!(ok = mbar_wait(bar(C::kBVFull + vs), (kv_cnt / C::kVStages) & 1, ctl, 902))) break;
             tc_fence_after();
-            issue_dp(stage);
+            issue_dp(vs);
             mma_commit(bar(C::kBSdFull));
+            mma_commit(bar(C::kBVEmpty + vs));  // V is read by the dP MMA only
           }
           for (int v = 0; v < n; ++v) {
             const uint32_t c = kv_cnt + (uint32_t)v;
-            const int stage = c % C::kStages;
+            const int stage = c % C::kKStages;  // K of this step (read by its dQ MMA)
             if (v + 1 < n) {
               const uint32_t c1 = c + 1;
-              const int st1 = c1 % C::kStages;
-              const uint32_t ph1 = (c1 / C::kStages) & 1;
-              if (!(ok = mbar_wait(bar(C::kBKFull + st1), ph1, ctl, 903))) break;
+              const int k1 = c1 % C::kKStages, v1 = c1 % C::kVStages;
+              if (!(ok = mbar_wait(bar(C::kBKFull + k1), (c1 / C::kKStages) & 1, ctl, 903))) break;
               tc_fence_after();
-              issue_s((v + 1) & 1, st1);
+              issue_s((v + 1) & 1, k1);
               if (!(ok = mbar_wait(bar(C::kBDpFree), dpf_cnt & 1, ctl, 904))) break;
               ++dpf_cnt;
-              if (!(ok = mbar_wait(bar(C::kBVFull + st1), ph1, ctl, 905))) break;
+              if (!(ok = mbar_wait(bar(C::kBVFull + v1), (c1 / C::kVStages) & 1, ctl, 905))) break;
               tc_fence_after();
-              issue_dp(st1);
+              issue_dp(v1);
               mma_commit(bar(C::kBSdFull));
+              mma_commit(bar(C::kBVEmpty + v1));
             }
             if (!(ok = mbar_wait(bar(C::kBDsFull), ds_cnt & 1, ctl, 906))) break;
             ++ds_cnt;
@@ -704,7 +724,6 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
               mma_ts_at(tmem + C::kTdQ, tmem + C::kTS0 + 128 * (v & 1) + 64 * (kk >> 2) + 8 * (kk & 3),
                         km, kk * 128, kIdQ, (v > 0 || kk > 0) ? 1u : 0u);
             mma_commit(bar(C::kBKEmpty + stage));
-            mma_commit(bar(C::kBVEmpty + stage));
           }
           if (!ok) break;
           // the dS warps' dP-free arrival of the last step
@@ -728,8 +747,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     uint32_t sd_cnt = 0, dq_cnt = 0;
     bool ok = true;
     const int* it;
+    int idx = 0;
     const float2 sc2 = make_float2(P.scale_log2, P.scale_log2);
-    for (int r = 0; ok && dq_item_at(P, r, it); ++r) {
+    for (int r = 0; ok && dq_item_at(P, r, it, idx); ++r) {
       const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
       for (int h = 0; ok && h < 2; ++h) {
         if (!half_active(it, h)) continue;
@@ -739,8 +759,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         const float nd = P.ndelta[(size_t)head * P.qpad + row];
         const float2 nl2 = make_float2(nl, nl);
         int v = 0;
+        int4 st_next = sb < se ? P.steps[sb] : make_int4(0, -1, -1, 0);
         for (int j = sb; j < se; ++j) {
-          const int4 st = P.steps[j];
+          const int4 st = st_next;
+          if (j + 1 < se) st_next = P.steps[j + 1];  // prefetch the next step descriptor
           const int info = half_info(st, h);
           if (info < 0) continue;
           const bool w = mbar_wait(bar(C::kBSdFull), sd_cnt & 1, ctl, 1000);
@@ -970,6 +992,7 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     P.steps = p->fwd_steps;
     P.items = p->dq_items;
     P.order = p->dq_order;
+    P.counts = p->dq_counts;
     P.n_items = (int)p->n_dq_items;
     P.slices = p->slices;
     P.masks = p->fwd_masks;

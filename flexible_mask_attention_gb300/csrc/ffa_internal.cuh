@@ -139,6 +139,7 @@ struct ffa_plan_s {
   // forward list when no item was split).
   int* dq_items = nullptr;
   int* dq_order = nullptr;
+  int* dq_counts = nullptr;  // [n_dq_items][2]: visits of each half of a dQ item
   int64_t n_dq_items = 0;
   bool dq_alias = true;
   int* err = nullptr;  // device [2]: code, location

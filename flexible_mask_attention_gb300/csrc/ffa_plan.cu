@@ -465,6 +465,23 @@ __global__ void k_bwd_items(int n_kt, int Hkv, int g, const int2* __restrict__ v
   it[5] = it[6] = it[7] = 0;
 }
 
+// Visits of each half of the (unsplit) forward items the dQ pass walks: a
+// half skips the steps whose info for it is -1.
+__global__ void k_dq_counts(const int* __restrict__ items, int n_items,
+                            const int4* __restrict__ steps, int* __restrict__ counts) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_items) return;
+  const int* it = items + (size_t)i * kFiWords;
+  int n0 = 0, n1 = 0;
+  for (int j = it[kFiStepBeg]; j < it[kFiStepEnd]; ++j) {
+    const int4 s = steps[j];
+    n0 += s.y >= 0 ? 1 : 0;
+    n1 += s.z >= 0 ? 1 : 0;
+  }
+  counts[2 * i] = n0;
+  counts[2 * i + 1] = n1;
+}
+
 // ---- ordering ---------------------------------------------------------------
 // One block: bitonic sort of (kv head asc, cost desc, index asc) keys in
 // `scratch` (n2 = next power of two >= n entries), then order[r] = index.
@@ -568,7 +585,7 @@ void free_plan(ffa_plan_s* p) {
   if (!p) return;
   void* bufs[] = {p->slices, p->fwd_steps, p->fwd_items, p->fwd_order, p->merges,
                   p->bwd_steps, p->bwd_items, p->bwd_order, p->err, p->fwd_masks,
-                  p->bwd_masks};
+                  p->bwd_masks, p->dq_counts};
   for (void* b : bufs)
     if (b) cudaFree(b);
   if (!p->dq_alias) {
@@ -774,6 +791,13 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
     if (rc != FFA_OK) return rc;
   }
   p->grid_dq = (int)std::max<int64_t>(1, std::min<int64_t>(p->num_sms, p->n_dq_items));
+  FFA_CUDA(cudaMalloc(&p->dq_counts, sizeof(int) * 2 * (size_t)std::max<int64_t>(1, p->n_dq_items)));
+  if (p->n_dq_items > 0) {
+    k_dq_counts<<<grid_for(p->n_dq_items, 128), 128, 0, st>>>(p->dq_items, (int)p->n_dq_items,
+                                                             p->fwd_steps, p->dq_counts);
+    note_launches(1);
+    FFA_CUDA(cudaGetLastError());
+  }
 
   // backward
   DevBuf bcnt(st), boff(st), bvis(st), bmcnt(st), bmoff(st);
