@@ -71,10 +71,12 @@ struct KvCfg {
                        kBSdpFull = 2 + 4 * kStages, kBSFree = kBSdpFull + 1,
                        kBPFull = kBSFree + 1, kBDkvFull = kBPFull + 1,
                        kBDkvEmpty = kBDkvFull + 1, kBDrain = kBDkvEmpty + 1,
-                       kBSFull = kBDrain + 1, kNumBars = kBSFull + 1;
+                       kBSFull = kBDrain + 1, kBItemFull = kBSFull + 1,
+                       kBItemEmpty = kBItemFull + kItemRing, kNumBars = kBItemEmpty + kItemRing;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   // The dynamic shared memory base must be 1024-byte aligned (checked on entry).
-  static constexpr int kSmemBytes = kMiscOff + 64;
+  static constexpr int kSlotOff = kMiscOff + 64;  // work-queue slots
+  static constexpr int kSmemBytes = kSlotOff + 4 * kItemRing;
   static constexpr int kTdV = 0, kTdK = D, kTS = 2 * D, kTdP = 2 * D + 128;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
@@ -83,6 +85,7 @@ struct KvParams {
   const int4* steps;
   const int* items;
   const int* order;
+  int* ticket;  // work-queue counter, zero at launch
   int n_items;
   const Slice* slices;
   const int* masks;  // slice lists of multi-slice visits
@@ -95,14 +98,6 @@ struct KvParams {
   int* err;
   uint64_t wait_ns;
 };
-
-__device__ __forceinline__ bool kv_item_at(const KvParams& P, int r, const int*& it) {
-  const int G = gridDim.x, b = blockIdx.x;
-  const int pos = r * G + ((r & 1) ? (G - 1 - b) : b);
-  if (pos >= P.n_items) return false;
-  it = P.items + (size_t)P.order[pos] * kBiWords;
-  return true;
-}
 
 // P^T and dS^T for key row j over the 64 queries [q0, q0+64) of the step
 // owned by this warpgroup, from the S^T values already in registers (s) and
@@ -189,6 +184,10 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
     }
     mbar_init(bar(C::kBSdpFull), 1);
     mbar_init(bar(C::kBSFull), 1);
+    for (int s = 0; s < kItemRing; ++s) {
+      mbar_init(bar(C::kBItemFull + s), 1);
+      mbar_init(bar(C::kBItemEmpty + s), 1 + 256);  // MMA thread + elementwise threads
+    }
     mbar_init(bar(C::kBSFree), 256);
     mbar_init(bar(C::kBPFull), 256);
     mbar_init(bar(C::kBDkvFull), 1);
@@ -203,6 +202,8 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, P.err, P.wait_ns};
   const int g = P.g;
+  const ItemQueue queue{reinterpret_cast<int*>(smem + C::kSlotOff), bar(C::kBItemFull),
+                        bar(C::kBItemEmpty)};
 
   if (warp >= 8) {
   reg_dealloc<kSplitNarrowRegs>();
@@ -215,8 +216,11 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
       prefetch_tmap(&tm_do);
       uint32_t kv_cnt = 0, q_cnt = 0;
       bool ok = true, q_only = false;  // q_only: Q of iteration q_cnt issued, its dO not yet
-      const int* it;
-      for (int r = 0; ok && kv_item_at(P, r, it); ++r) {
+      for (int r = 0; ok; ++r) {
+        const int pos = atomicAdd(P.ticket, 1);
+        const int idx = pos < P.n_items ? P.order[pos] : -1;
+        if (!(ok = queue_publish(queue, r, idx, ctl, 409)) || idx < 0) break;
+        const int* it = P.items + (size_t)idx * kBiWords;
         const int sb = it[kBiStepBeg], se = it[kBiStepEnd];
         if (se <= sb) continue;
         const int kt = it[kBiKt], hk = it[kBiHkv];
@@ -288,8 +292,10 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
       };
       uint32_t kv_cnt = 0, q_cnt = 0, sf_cnt = 0, p_cnt = 0, dkv_cnt = 0;
       bool ok = true;
-      const int* it;
-      for (int r = 0; ok && kv_item_at(P, r, it); ++r) {
+      for (int r = 0; ok; ++r) {
+        int idx;
+        if (!(ok = queue_take(queue, r, idx, ctl, 509)) || idx < 0) break;
+        const int* it = P.items + (size_t)idx * kBiWords;
         const int sb = it[kBiStepBeg], se = it[kBiStepEnd];
         if (se <= sb) continue;
         if (!(ok = mbar_wait(bar(C::kBKVFull), kv_cnt & 1, ctl, 500))) break;
@@ -376,8 +382,11 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
     uint8_t* p_row = smem + C::kPOff + wg * 16384 + j * 128;
     uint32_t sdp_cnt = 0, dkv_cnt = 0;
     bool ok = true;
-    const int* it;
-    for (int r = 0; ok && kv_item_at(P, r, it); ++r) {
+    for (int r = 0; ok; ++r) {
+      int idx = -1;
+      const bool w = queue_take(queue, r, idx, ctl, 609);
+      if (!(ok = __all_sync(0xffffffffu, w)) || idx < 0) break;
+      const int* it = P.items + (size_t)idx * kBiWords;
       const int sb = it[kBiStepBeg], se = it[kBiStepEnd];
       const int kt = it[kBiKt], hk = it[kBiHkv];
       const int key = kt * 128 + j;
@@ -962,6 +971,7 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     P.steps = p->bwd_steps;
     P.items = p->bwd_items;
     P.order = p->bwd_order;
+    P.ticket = p->tickets + 1;
     P.n_items = (int)p->n_bwd_items;
     P.slices = p->slices;
     P.masks = p->bwd_masks;
@@ -981,6 +991,7 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
                              C::kSmemBytes) != cudaSuccess)
       return FFA_ERR_CUDA;
     if (!split_regs_ok<ffa_bwd_dkdv_kernel<D>>()) return FFA_ERR_UNSUPPORTED;
+    if (cudaMemsetAsync(P.ticket, 0, sizeof(int), st) != cudaSuccess) return FFA_ERR_CUDA;
     record_phase(p, 3, st);
     ffa_bwd_dkdv_kernel<D><<<p->grid_bwd, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, P);
     note_launches(1);

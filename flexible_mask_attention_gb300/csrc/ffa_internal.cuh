@@ -143,6 +143,7 @@ struct ffa_plan_s {
   int64_t n_dq_items = 0;
   bool dq_alias = true;
   int* err = nullptr;  // device [2]: code, location
+  int* tickets = nullptr;  // device [3]: work-queue counters (forward, dK/dV, dQ)
   int grid_fwd = 0, grid_bwd = 0, grid_dq = 0;
   cudaEvent_t events[6] = {};  // optional phase events (ffa_plan_set_events)
   bool use_events = false;

@@ -586,7 +586,7 @@ void free_plan(ffa_plan_s* p) {
   if (!p) return;
   void* bufs[] = {p->slices, p->fwd_steps, p->fwd_items, p->fwd_order, p->merges,
                   p->bwd_steps, p->bwd_items, p->bwd_order, p->err, p->fwd_masks,
-                  p->bwd_masks, p->dq_counts};
+                  p->bwd_masks, p->dq_counts, p->tickets};
   for (void* b : bufs)
     if (b) cudaFree(b);
   if (!p->dq_alias) {
@@ -601,6 +601,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   const int S = p->S;
   FFA_CUDA(cudaMalloc(&p->slices, sizeof(Slice) * (size_t)std::max(S, 1)));
   FFA_CUDA(cudaMalloc(&p->err, 2 * sizeof(int)));
+  FFA_CUDA(cudaMalloc(&p->tickets, 4 * sizeof(int)));
   FFA_CUDA(cudaMemsetAsync(p->err, 0, 2 * sizeof(int), st));
   DevBuf flags_area(st);
   FFA_CUDA(flags_area.alloc(64));

@@ -96,6 +96,41 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 }
 
 // ----------------------------------------------------------------------------
+// Dynamic work queue of a persistent kernel.  One producer thread draws item
+// positions from a global ticket counter (zeroed before the launch) and
+// publishes the item index through a ring of kItemRing shared-memory slots,
+// -1 once the list is exhausted; every consumer thread reads every slot.  The
+// slot's "full" barrier counts the producer's arrival, its "empty" barrier
+// the consumers' (mbarrier arrive/wait order the slot write before the reads).
+// Items are drawn in cost-descending order, so each CTA takes the next
+// heaviest item whenever it runs out of work (greedy assignment at run time).
+constexpr int kItemRing = 4;
+
+struct ItemQueue {
+  int* slot;        // shared [kItemRing]
+  uint32_t full0;   // mbarrier of slot 0; slot s's barrier is at + 8 s
+  uint32_t empty0;
+};
+
+__device__ __forceinline__ bool queue_publish(const ItemQueue& q, int r, int value,
+                                              const WaitCtl& ctl, int where) {
+  const int s = r % kItemRing;
+  if (!mbar_wait(q.empty0 + 8 * s, ((r / kItemRing) & 1) ^ 1, ctl, where)) return false;
+  q.slot[s] = value;
+  mbar_arrive(q.full0 + 8 * s);
+  return true;
+}
+
+__device__ __forceinline__ bool queue_take(const ItemQueue& q, int r, int& value,
+                                           const WaitCtl& ctl, int where) {
+  const int s = r % kItemRing;
+  if (!mbar_wait(q.full0 + 8 * s, (r / kItemRing) & 1, ctl, where)) return false;
+  value = *reinterpret_cast<volatile int*>(q.slot + s);
+  mbar_arrive(q.empty0 + 8 * s);
+  return true;
+}
+
+// ----------------------------------------------------------------------------
 // TMA (tiled, 2-D) and bulk copies, completing on an mbarrier.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int x, int y) {
