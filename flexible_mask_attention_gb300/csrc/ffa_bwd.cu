@@ -501,8 +501,10 @@ struct DqCfg {
                        kBVFull = kBKEmpty + kKStages, kBVEmpty = kBVFull + kVStages,
                        kBSdFull = kBVEmpty + kVStages, kBDpFree = kBSdFull + 1,
                        kBDsFull = kBDpFree + 1, kBDqFull = kBDsFull + 1,
-                       kBDqEmpty = kBDqFull + 1, kBDrain = kBDqEmpty + 1, kNumBars = kBDrain + 1;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+                       kBDqEmpty = kBDqFull + 1, kBDrain = kBDqEmpty + 1,
+                       kBItemFull = kBDrain + 1, kBItemEmpty = kBItemFull + kItemRing,
+                       kNumBars = kBItemEmpty + kItemRing;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag, queue slots
   static constexpr int kSmemBytes = kMiscOff + 64;
   static constexpr int kTS0 = 0, kTdP = 256, kTdQ = 384;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -512,6 +514,7 @@ struct DqParams {
   const int4* steps;
   const int* items;
   const int* order;
+  int* ticket;  // work-queue counter, zero at launch
   const int* counts;  // visits of each half of an item
   int n_items;
   const Slice* slices;
@@ -524,15 +527,6 @@ struct DqParams {
   int* err;
   uint64_t wait_ns;
 };
-
-__device__ __forceinline__ bool dq_item_at(const DqParams& P, int r, const int*& it, int& idx) {
-  const int G = gridDim.x, b = blockIdx.x;
-  const int pos = r * G + ((r & 1) ? (G - 1 - b) : b);
-  if (pos >= P.n_items) return false;
-  idx = P.order[pos];
-  it = P.items + (size_t)idx * kFiWords;
-  return true;
-}
 
 __device__ __forceinline__ bool half_active(const int* it, int h) {
   return it[kFiQt0 + h] >= 0 && it[kFiH0 + h] >= 0;
@@ -580,6 +574,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     mbar_init(bar(C::kBDqFull), 1);
     mbar_init(bar(C::kBDqEmpty), 256);
     mbar_init(bar(C::kBDrain), 1);
+    for (int s = 0; s < kItemRing; ++s) {
+      mbar_init(bar(C::kBItemFull + s), 1);
+      mbar_init(bar(C::kBItemEmpty + s), 1 + 256);  // MMA thread + dS threads
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -588,6 +586,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, P.err, P.wait_ns};
+  const ItemQueue queue{reinterpret_cast<int*>(smem + C::kMiscOff + 16), bar(C::kBItemFull),
+                        bar(C::kBItemEmpty)};
 
   if (warp >= 8) {
   reg_dealloc<kSplitNarrowRegs>();
@@ -600,9 +600,11 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       prefetch_tmap(&tm_do);
       uint32_t kv_cnt = 0, q_cnt = 0;
       bool ok = true, k_only = false;
-      const int* it;
-      int idx = 0;
-      for (int r = 0; ok && dq_item_at(P, r, it, idx); ++r) {
+      for (int r = 0; ok; ++r) {
+        const int pos = atomicAdd(P.ticket, 1);
+        const int idx = pos < P.n_items ? P.order[pos] : -1;
+        if (!(ok = queue_publish(queue, r, idx, ctl, 809)) || idx < 0) break;
+        const int* it = P.items + (size_t)idx * kFiWords;
         const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
         if (se <= sb) continue;
         for (int h = 0; ok && h < 2; ++h) {
@@ -679,9 +681,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       };
       uint32_t kv_cnt = 0, q_cnt = 0, dpf_cnt = 0, ds_cnt = 0, dqe_cnt = 0;
       bool ok = true;
-      const int* it;
-      int idx = 0;
-      for (int r = 0; ok && dq_item_at(P, r, it, idx); ++r) {
+      for (int r = 0; ok; ++r) {
+        int idx;
+        if (!(ok = queue_take(queue, r, idx, ctl, 909)) || idx < 0) break;
+        const int* it = P.items + (size_t)idx * kFiWords;
         const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
         if (se <= sb) continue;
         for (int h = 0; ok && h < 2; ++h) {
@@ -755,10 +758,12 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t sd_cnt = 0, dq_cnt = 0;
     bool ok = true;
-    const int* it;
-    int idx = 0;
     const float2 sc2 = make_float2(P.scale_log2, P.scale_log2);
-    for (int r = 0; ok && dq_item_at(P, r, it, idx); ++r) {
+    for (int r = 0; ok; ++r) {
+      int idx = -1;
+      const bool w = queue_take(queue, r, idx, ctl, 1009);
+      if (!(ok = __all_sync(0xffffffffu, w)) || idx < 0) break;
+      const int* it = P.items + (size_t)idx * kFiWords;
       const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
       for (int h = 0; ok && h < 2; ++h) {
         if (!half_active(it, h)) continue;
@@ -1003,6 +1008,7 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     P.steps = p->fwd_steps;
     P.items = p->dq_items;
     P.order = p->dq_order;
+    P.ticket = p->tickets + 2;
     P.counts = p->dq_counts;
     P.n_items = (int)p->n_dq_items;
     P.slices = p->slices;
@@ -1022,6 +1028,7 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
                              C::kSmemBytes) != cudaSuccess)
       return FFA_ERR_CUDA;
     if (!split_regs_ok<ffa_bwd_dq_kernel<D>>()) return FFA_ERR_UNSUPPORTED;
+    if (cudaMemsetAsync(P.ticket, 0, sizeof(int), st) != cudaSuccess) return FFA_ERR_CUDA;
     record_phase(p, 4, st);
     ffa_bwd_dq_kernel<D><<<p->grid_dq, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, P);
     note_launches(1);

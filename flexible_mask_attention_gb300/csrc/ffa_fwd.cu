@@ -60,8 +60,10 @@ struct FwdCfg {
   static constexpr int kBQFull = 0, kBQEmpty = 1, kBKFull = 2, kBVFull = 2 + kStages,
                        kBKEmpty = 2 + 2 * kStages, kBVEmpty = 2 + 3 * kStages,
                        kBSFull = 2 + 4 * kStages, kBPFull = kBSFull + 2, kBOFull = kBPFull + 2,
-                       kBOEmpty = kBOFull + 2, kBDrain = kBOEmpty + 2, kNumBars = kBDrain + 1;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+                       kBOEmpty = kBOFull + 2, kBDrain = kBOEmpty + 2,
+                       kBItemFull = kBDrain + 1, kBItemEmpty = kBItemFull + kItemRing,
+                       kNumBars = kBItemEmpty + kItemRing;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag, queue slots
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + alignment slack
 };
 
@@ -69,6 +71,7 @@ struct FwdParams {
   const int4* steps;
   const int* items;
   const int* order;
+  int* ticket;  // work-queue counter, zero at launch
   int n_items;
   const Slice* slices;
   const int* masks;  // slice lists of multi-slice visits
@@ -103,14 +106,6 @@ __device__ __forceinline__ float log2_add(float a, float b) {
   const float mx = fmaxf(a, b);
   if (mx == -INFINITY) return -INFINITY;
   return mx + log2f(exp2f(a - mx) + exp2f(b - mx));
-}
-
-__device__ __forceinline__ bool item_at(const FwdParams& P, int r, const int*& it) {
-  const int G = gridDim.x, b = blockIdx.x;
-  const int pos = r * G + ((r & 1) ? (G - 1 - b) : b);
-  if (pos >= P.n_items) return false;
-  it = P.items + (size_t)P.order[pos] * kFiWords;
-  return true;
 }
 
 // Wait that ignores the abort flag (used to drain copies in flight).
@@ -155,6 +150,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(bar(C::kBOEmpty + h), 128);
     }
     mbar_init(bar(C::kBDrain), 1);
+    for (int s = 0; s < kItemRing; ++s) {
+      mbar_init(bar(C::kBItemFull + s), 1);
+      mbar_init(bar(C::kBItemEmpty + s), 1 + 256);  // MMA thread + softmax threads
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -163,6 +162,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, P.err, P.wait_ns};
+  const ItemQueue queue{reinterpret_cast<int*>(smem + C::kMiscOff + 16), bar(C::kBItemFull),
+                        bar(C::kBItemEmpty)};
 
   if (warp >= 8) {
   reg_dealloc<kSplitNarrowRegs>();
@@ -174,8 +175,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       prefetch_tmap(&tm_v);
       uint32_t kv_cnt = 0, q_cnt = 0;
       bool ok = true, k_only = false;  // k_only: K of step kv_cnt issued, its V not yet
-      const int* it;
-      for (int r = 0; ok && item_at(P, r, it); ++r) {
+      for (int r = 0; ok; ++r) {
+        const int pos = atomicAdd(P.ticket, 1);
+        const int idx = pos < P.n_items ? P.order[pos] : -1;
+        if (!(ok = queue_publish(queue, r, idx, ctl, 109)) || idx < 0) break;
+        const int* it = P.items + (size_t)idx * kFiWords;
         const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
         if (se <= sb) continue;
         const bool act1 = it[kFiQt1] >= 0 && it[kFiH1] >= 0;
@@ -246,8 +250,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       };
       uint32_t kv_cnt = 0, q_cnt = 0, p_cnt[2] = {0, 0}, oe_cnt[2] = {0, 0};
       bool ok = true;
-      const int* it;
-      for (int r = 0; ok && item_at(P, r, it); ++r) {
+      for (int r = 0; ok; ++r) {
+        int idx;
+        if (!(ok = queue_take(queue, r, idx, ctl, 209)) || idx < 0) break;
+        const int* it = P.items + (size_t)idx * kFiWords;
         const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
         if (se <= sb) continue;
         const bool act1 = it[kFiQt1] >= 0 && it[kFiH1] >= 0;
@@ -337,8 +343,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tO = tmem + lane_addr + 256 + h * 128;
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
-    const int* it;
-    for (int r = 0; ok && item_at(P, r, it); ++r) {
+    for (int r = 0; ok; ++r) {
+      int idx = -1;
+      const bool w = queue_take(queue, r, idx, ctl, 309);
+      if (!(ok = __all_sync(0xffffffffu, w)) || idx < 0) break;
+      const int* it = P.items + (size_t)idx * kFiWords;
       const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
       const bool act1 = it[kFiQt1] >= 0 && it[kFiH1] >= 0;
       if (h == 1 && !act1) continue;
@@ -561,6 +570,7 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   P.steps = p->fwd_steps;
   P.items = p->fwd_items;
   P.order = p->fwd_order;
+  P.ticket = p->tickets;
   P.n_items = (int)p->n_fwd_items;
   P.slices = p->slices;
   P.masks = p->fwd_masks;
@@ -581,6 +591,7 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
                            C::kSmemBytes) != cudaSuccess)
     return FFA_ERR_CUDA;
   if (!split_regs_ok<ffa_fwd_kernel<D>>()) return FFA_ERR_UNSUPPORTED;
+  if (cudaMemsetAsync(P.ticket, 0, sizeof(int), st) != cudaSuccess) return FFA_ERR_CUDA;
   record_phase(p, 0, st);
   ffa_fwd_kernel<D><<<p->grid_fwd, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, P);
   note_launches(1);
