@@ -2,22 +2,23 @@
 // C ABI declared in include/ffa.h.
 //
 // Work-list specification (all of it computed on the device):
-//   * Forward visits of q-tile qt: every (k-tile kt, slice s) whose tile
-//     holds a visible entry of s, kind FULL when all 128 x 128 entries are
-//     visible, PARTIAL otherwise; ordered by (kt, s).
+//   * Forward visits of q-tile qt: one per k-tile kt that holds a visible
+//     entry, in kt order; kind FULL when one slice makes all 128 x 128
+//     entries visible, PARTIAL otherwise; a tile seen by several slices
+//     carries the list of those slices (masked by the union of their windows).
 //   * Forward units pair two 128-row halves that share K/V tiles:
 //       - grouped-query heads (Hq / Hkv >= 2): one q-tile, two query heads of
 //         the same kv head; the steps are the q-tile's visits;
 //       - otherwise: q-tiles 2u and 2u+1 of one head; the steps merge the two
 //         visit lists on kt (equal kt -> one shared step, in list order).
 //   * Item cost = sum over its steps and busy halves of 4 (FULL) or 5
-//     (PARTIAL).  Items are sorted by (kv head, cost descending, index) and
-//     dealt to the persistent CTAs in a snake order.
+//     (PARTIAL).  Items are sorted by (cost descending, index); the
+//     persistent kernels draw them in that order from a work queue.
 //   * While fewer than `split_below` items have work, each such item is cut
 //     into equal runs of steps whose partial results are merged by
 //     logsumexp afterwards.
-//   * Backward visits of k-tile kt: every (q-tile, slice) pair, same kinds,
-//     ordered by (qt, s); one item per (kt, kv head), cost g * visit costs.
+//   * Backward visits of k-tile kt: one per q-tile, merged the same way, in
+//     qt order; one item per (kt, kv head), cost g * visit costs.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <stdio.h>
@@ -485,10 +486,10 @@ __global__ void k_dq_counts(const int* __restrict__ items, int n_items,
 // ---- ordering ---------------------------------------------------------------
 // One block: bitonic sort of (cost desc, index asc) keys in `scratch`
 // (n2 = next power of two >= n entries), then order[r] = index.  The
-// persistent kernels deal the sorted items out in snake order, so the heavy
-// items go first and the light ones even out the tail.  (Grouping the items
-// by kv head first, for L2 reuse of one head's tiles, measured slower on
-// GB300: balance matters more than locality at these sizes.)
+// persistent kernels draw the items in this order from a work queue, so the
+// heavy items go first and the light ones even out the tail.  (Grouping the
+// items by kv head first, for L2 reuse of one head's tiles, measured slower
+// on GB300: balance matters more than locality at these sizes.)
 // Key bits: [24,50) 2^26-1-cost, [0,24) index.
 __global__ void k_sort_order(const int* __restrict__ items, int words, int cost_word, int n,
                              int n2, unsigned long long* scratch, int* order) {
