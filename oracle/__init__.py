@@ -52,12 +52,12 @@ def load_library(path: str):
     L = ctypes.c_long
     I = ctypes.c_int
     D = ctypes.c_double
-    lib.ffa_oracle_fwd.argtypes = [P, P, P, L, L, I, I, I, P, P, P, I, D, P, I, I, P, L, P, P]
+    lib.ffa_oracle_fwd.argtypes = [P, P, P, L, L, I, I, I, P, P, P, I, D, D, P, I, I, P, L, P, P]
     lib.ffa_oracle_fwd.restype = I
-    lib.ffa_oracle_bwd.argtypes = [P, P, P, P, L, L, I, I, I, P, P, P, I, D, P, I, I,
+    lib.ffa_oracle_bwd.argtypes = [P, P, P, P, L, L, I, I, I, P, P, P, I, D, D, P, I, I,
                                    P, L, P, P, L, P, P]
     lib.ffa_oracle_bwd.restype = I
-    lib.ffa_oracle_dsink.argtypes = [P, P, P, P, L, L, I, I, I, P, P, P, I, D, P, I, I, P, L, P]
+    lib.ffa_oracle_dsink.argtypes = [P, P, P, P, L, L, I, I, I, P, P, P, I, D, D, P, I, I, P, L, P]
     lib.ffa_oracle_dsink.restype = I
     lib.ffa_oracle_num_threads.restype = I
     return lib
@@ -111,9 +111,10 @@ def _sink(sink, sink_layout, Tq, Hq):
 
 
 def fwd(q, k, v, q_ranges, k_ranges, mask_types, softmax_scale=None, rows=None, lib=None, *,
-        sink=None, sink_layout="sh"):
+        sink=None, sink_layout="sh", softcap=0.0):
     """fp64 forward. Returns (out[n, Hq, D], lse[Hq, n]) for ``rows`` (all by default).
-    ``sink``: optional fp32 sink logits, [n_sink, Hq] ("sh") or [Tq, n_sink, Hq] ("ssh")."""
+    ``sink``: optional fp32 sink logits, [n_sink, Hq] ("sh") or [Tq, n_sink, Hq] ("ssh").
+    ``softcap`` c > 0 caps every score to c * tanh(score / c)."""
     qn, kn, vn = _u16(q), _u16(k), _u16(v)
     Tq, Hq, D = qn.shape
     Tk, Hkv, _ = kn.shape
@@ -125,7 +126,7 @@ def fwd(q, k, v, q_ranges, k_ranges, mask_types, softmax_scale=None, rows=None, 
     out = np.zeros((n, Hq, D), np.float64)
     lse = np.zeros((Hq, n), np.float64)
     rc = (lib or _load()).ffa_oracle_fwd(_ptr(qn), _ptr(kn), _ptr(vn), Tq, Tk, Hq, Hkv, D, _ptr(qr),
-                                _ptr(kr), _ptr(ty), ty.shape[0], scale,
+                                _ptr(kr), _ptr(ty), ty.shape[0], scale, float(softcap),
                                 None if sk is None else _ptr(sk), ns, lay,
                                 None if rows_a is None else _ptr(rows_a), n, _ptr(out), _ptr(lse))
     if rc != 0:
@@ -134,7 +135,7 @@ def fwd(q, k, v, q_ranges, k_ranges, mask_types, softmax_scale=None, rows=None, 
 
 
 def bwd(q, k, v, dout, q_ranges, k_ranges, mask_types, softmax_scale=None,
-        dq_rows=None, dkv_keys=None, lib=None, *, sink=None, sink_layout="sh"):
+        dq_rows=None, dkv_keys=None, lib=None, *, sink=None, sink_layout="sh", softcap=0.0):
     """fp64 backward. Returns (dq[nq, Hq, D], dk[nk, Hkv, D], dv[nk, Hkv, D])."""
     qn, kn, vn, dn = _u16(q), _u16(k), _u16(v), _u16(dout)
     Tq, Hq, D = qn.shape
@@ -150,7 +151,7 @@ def bwd(q, k, v, dout, q_ranges, k_ranges, mask_types, softmax_scale=None,
     dv = np.zeros((nk, Hkv, D), np.float64)
     sk, ns, lay = _sink(sink, sink_layout, Tq, Hq)
     rc = (lib or _load()).ffa_oracle_bwd(_ptr(qn), _ptr(kn), _ptr(vn), _ptr(dn), Tq, Tk, Hq, Hkv, D,
-                                _ptr(qr), _ptr(kr), _ptr(ty), ty.shape[0], scale,
+                                _ptr(qr), _ptr(kr), _ptr(ty), ty.shape[0], scale, float(softcap),
                                 None if sk is None else _ptr(sk), ns, lay,
                                 None if rq is None else _ptr(rq), nq, _ptr(dq),
                                 None if rk is None else _ptr(rk), nk, _ptr(dk), _ptr(dv))
@@ -160,7 +161,7 @@ def bwd(q, k, v, dout, q_ranges, k_ranges, mask_types, softmax_scale=None,
 
 
 def dsink(q, k, v, dout, q_ranges, k_ranges, mask_types, sink, sink_layout="sh",
-          softmax_scale=None, rows=None, lib=None):
+          softmax_scale=None, rows=None, lib=None, softcap=0.0):
     """fp64 gradient of the sink logits: [n_sink, Hq] ("sh", summed over all
     rows) or [n, n_sink, Hq] for ``rows`` ("ssh", all rows by default)."""
     qn, kn, vn, dn = _u16(q), _u16(k), _u16(v), _u16(dout)
@@ -173,7 +174,8 @@ def dsink(q, k, v, dout, q_ranges, k_ranges, mask_types, sink, sink_layout="sh",
     n = Tq if rows_a is None else rows_a.shape[0]
     out = np.zeros((ns, Hq) if lay == 0 else (n, ns, Hq), np.float64)
     rc = (lib or _load()).ffa_oracle_dsink(_ptr(qn), _ptr(kn), _ptr(vn), _ptr(dn), Tq, Tk, Hq, Hkv,
-                                  D, _ptr(qr), _ptr(kr), _ptr(ty), ty.shape[0], scale, _ptr(sk),
+                                  D, _ptr(qr), _ptr(kr), _ptr(ty), ty.shape[0], scale,
+                                  float(softcap), _ptr(sk),
                                   ns, lay, None if rows_a is None else _ptr(rows_a), n, _ptr(out))
     if rc != 0:
         raise ValueError("oracle: bad arguments")

@@ -41,6 +41,13 @@
  *     dsink_s = - sum_i exp(sigma_s - lse_i) delta_i
  * (summed over the rows of the head for "sh", one value per row for "ssh").
  *
+ * Softcap (quickstart card: the `softcap` argument, default 0; no formula on
+ * the pages).  Reading: for c > 0 every score is capped smoothly,
+ *     x_j = c * tanh(scale * <q_i, k_j> / c),
+ * and the backward carries the chain-rule factor 1 - tanh^2 into dS:
+ *     dS = P (dP - delta) (1 - (x / c)^2),  dQ = scale dS K,  dK = scale dS^T Q.
+ * c <= 0 means no cap.
+ *
  * Every loop below is the definition written out, with no blocking, fusion or
  * reordering.  OpenMP only splits independent (head, row) or (head, key)
  * pairs across threads.
@@ -111,10 +118,24 @@ typedef struct {
   const slice_t* sl;
   int ns;
   double scale;
+  double softcap;     /* <= 0: no cap */
   const double* sink; /* NULL: no sink */
   int n_sink;
   int sink_layout;    /* 0: [n_sink][Hq], 1: [Tq][n_sink][Hq] */
 } problem_t;
+
+/* Score of a (row, key) pair from its dot product: scale * dot, capped. */
+static double score(const problem_t* P, double dot) {
+  const double x = P->scale * dot;
+  return P->softcap > 0.0 ? P->softcap * tanh(x / P->softcap) : x;
+}
+
+/* d score / d(scale * dot) at score x: 1 - tanh^2 under a cap, else 1. */
+static double score_grad(const problem_t* P, double x) {
+  if (P->softcap <= 0.0) return 1.0;
+  const double t = x / P->softcap;
+  return 1.0 - t * t;
+}
 
 /* Sink logit s of (head h, row i). */
 static double sink_value(const problem_t* P, int h, long i, int s) {
@@ -140,7 +161,7 @@ static double row_forward(const problem_t* P, int h, long i, double* out_row, do
   long cnt = 0;
   for (long j = 0; j < P->Tk; ++j) {
     if (!vis[j]) continue;
-    xbuf[j] = P->scale * dot_bf16(qi, P->k + ((size_t)j * P->Hkv + hk) * D, D);
+    xbuf[j] = score(P, dot_bf16(qi, P->k + ((size_t)j * P->Hkv + hk) * D, D));
     if (xbuf[j] > m) m = xbuf[j];
     ++cnt;
   }
@@ -179,13 +200,14 @@ int ffa_oracle_num_threads(void) {
  * out: [n_rows][Hq][D], lse: [Hq][n_rows]. */
 int ffa_oracle_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, long Tq, long Tk,
                    int Hq, int Hkv, int D, const int* q_ranges, const int* k_ranges,
-                   const int* mask_types, int num_slices, double scale, const double* sink,
-                   int n_sink, int sink_layout, const long* rows, long n_rows, double* out,
-                   double* lse) {
+                   const int* mask_types, int num_slices, double scale, double softcap,
+                   const double* sink, int n_sink, int sink_layout, const long* rows, long n_rows,
+                   double* out, double* lse) {
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0) return 1;
   if (n_sink < 0 || (n_sink > 0 && !sink) || sink_layout < 0 || sink_layout > 1) return 1;
   slice_t* sl = read_slices(q_ranges, k_ranges, mask_types, num_slices);
-  problem_t P = {q, k, v, Tq, Tk, Hq, Hkv, D, sl, num_slices, scale, sink, n_sink, sink_layout};
+  problem_t P = {q, k, v, Tq, Tk, Hq, Hkv, D, sl, num_slices, scale, softcap, sink, n_sink,
+                 sink_layout};
   const long n = rows ? n_rows : Tq;
 #pragma omp parallel
   {
@@ -211,13 +233,15 @@ int ffa_oracle_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, long
 int ffa_oracle_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
                    long Tq, long Tk, int Hq, int Hkv, int D, const int* q_ranges,
                    const int* k_ranges, const int* mask_types, int num_slices, double scale,
-                   const double* sink, int n_sink, int sink_layout, const long* dq_rows,
+                   double softcap, const double* sink, int n_sink, int sink_layout,
+                   const long* dq_rows,
                    long n_dq_rows, double* dq, const long* dkv_keys, long n_keys, double* dk,
                    double* dv) {
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0) return 1;
   if (n_sink < 0 || (n_sink > 0 && !sink) || sink_layout < 0 || sink_layout > 1) return 1;
   slice_t* sl = read_slices(q_ranges, k_ranges, mask_types, num_slices);
-  problem_t P = {q, k, v, Tq, Tk, Hq, Hkv, D, sl, num_slices, scale, sink, n_sink, sink_layout};
+  problem_t P = {q, k, v, Tq, Tk, Hq, Hkv, D, sl, num_slices, scale, softcap, sink, n_sink,
+                 sink_layout};
   const int g = Hq / Hkv;
   const long nq = dq_rows ? n_dq_rows : Tq;
   const long nk = dkv_keys ? n_keys : Tk;
@@ -245,7 +269,7 @@ int ffa_oracle_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
         if (!vis[j]) continue;
         const double p = exp(xbuf[j] - lse);
         const double dp = dot_bf16(doi, v + ((size_t)j * Hkv + hk) * D, D);
-        const double ds = p * (dp - delta);
+        const double ds = p * (dp - delta) * score_grad(&P, xbuf[j]);
         const uint16_t* kj = k + ((size_t)j * Hkv + hk) * D;
         for (int t = 0; t < D; ++t) dqi[t] += scale * ds * bf16_to_double(kj[t]);
       }
@@ -307,9 +331,10 @@ int ffa_oracle_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
         for (int h = hk * g; h < (hk + 1) * g; ++h) {
           const uint16_t* qi = q + ((size_t)i * Hq + h) * D;
           const uint16_t* doi = dout + ((size_t)i * Hq + h) * D;
-          const double p = exp(scale * dot_bf16(qi, kj, D) - lse_all[(size_t)h * Tq + i]);
+          const double x = score(&P, dot_bf16(qi, kj, D));
+          const double p = exp(x - lse_all[(size_t)h * Tq + i]);
           const double dp = dot_bf16(doi, vj, D);
-          const double ds = p * (dp - delta_all[(size_t)h * Tq + i]);
+          const double ds = p * (dp - delta_all[(size_t)h * Tq + i]) * score_grad(&P, x);
           for (int t = 0; t < D; ++t) {
             dvj[t] += p * bf16_to_double(doi[t]);
             dkj[t] += scale * ds * bf16_to_double(qi[t]);
@@ -333,13 +358,14 @@ int ffa_oracle_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
 int ffa_oracle_dsink(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                      const uint16_t* dout, long Tq, long Tk, int Hq, int Hkv, int D,
                      const int* q_ranges, const int* k_ranges, const int* mask_types,
-                     int num_slices, double scale, const double* sink, int n_sink,
-                     int sink_layout, const long* rows, long n_rows, double* dsink) {
+                     int num_slices, double scale, double softcap, const double* sink,
+                     int n_sink, int sink_layout, const long* rows, long n_rows, double* dsink) {
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0) return 1;
   if (n_sink <= 0 || !sink || sink_layout < 0 || sink_layout > 1) return 1;
   if (sink_layout == 0 && rows) return 1; /* a per-head sum needs every row */
   slice_t* sl = read_slices(q_ranges, k_ranges, mask_types, num_slices);
-  problem_t P = {q, k, v, Tq, Tk, Hq, Hkv, D, sl, num_slices, scale, sink, n_sink, sink_layout};
+  problem_t P = {q, k, v, Tq, Tk, Hq, Hkv, D, sl, num_slices, scale, softcap, sink, n_sink,
+                 sink_layout};
   const long n = rows ? n_rows : Tq;
   /* per (row, head, sink) term, then the sums in a fixed order */
   double* term = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * Hq * n_sink);

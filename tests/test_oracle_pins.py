@@ -320,7 +320,8 @@ MUTANTS = {
     "gqa_mapping": (r"const int hk = h / \(P->Hq / P->Hkv\);", "const int hk = h % P->Hkv;"),
     "dropped_max": (r"const double lse = m \+ log\(sum\);", "const double lse = log(sum);"),
     "dq_dropped_scale": (r"dqi\[t\] \+= scale \* ds", "dqi[t] += ds"),
-    "dropped_delta": (r"const double ds = p \* \(dp - delta\);", "const double ds = p * dp;"),
+    "dropped_delta": (r"const double ds = p \* \(dp - delta\) \* score_grad\(&P, xbuf\[j\]\);",
+                      "const double ds = p * dp * score_grad(&P, xbuf[j]);"),
     "dk_transposed_operand": (r"dkj\[t\] \+= scale \* ds \* bf16_to_double\(qi\[t\]\)",
                               "dkj[t] += scale * ds * bf16_to_double(kj[t])"),
 }
