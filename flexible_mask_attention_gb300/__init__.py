@@ -86,8 +86,8 @@ def load_library():
     lib.ffa_bwd_workspace_size.restype = S
     lib.ffa_fwd.argtypes = [P, P, P, P, F, P, P, P, S, P]
     lib.ffa_bwd.argtypes = [P, P, P, P, P, P, P, F, P, P, P, P, S, P]
-    lib.ffa_fwd_ex.argtypes = [P, P, P, P, P, I32, I32, F, P, P, P, S, P]
-    lib.ffa_bwd_ex.argtypes = [P, P, P, P, P, P, P, P, I32, I32, F, P, P, P, P, P, S, P]
+    lib.ffa_fwd_ex.argtypes = [P, P, P, P, P, I32, I32, F, F, P, P, P, S, P]
+    lib.ffa_bwd_ex.argtypes = [P, P, P, P, P, P, P, P, I32, I32, F, F, P, P, P, P, P, S, P]
     lib.ffa_get_last_device_error.argtypes = [P, ctypes.POINTER(I32), ctypes.POINTER(I32), P]
     lib.ffa_plan_set_wait_limit.argtypes = [P, U64]
     lib.ffa_plan_set_events.argtypes = [P, ctypes.POINTER(P), I32]
@@ -287,9 +287,10 @@ def _sink_args(plan: Plan, sink, sink_layout):
 
 
 def ffa_fwd_ex(plan: Plan, q, k, v, sink=None, sink_layout="sh", out=None, lse=None,
-               softmax_scale=None, workspace=None, stream=None):
+               softmax_scale=None, softcap=0.0, workspace=None, stream=None):
     """ffa_fwd with optional attention-sink logits (fp32, [n_sink, Hq] for
-    "sh" or [Tq, n_sink, Hq] for "ssh"); lse includes the sink term."""
+    "sh" or [Tq, n_sink, Hq] for "ssh"; lse includes the sink term) and an
+    optional softcap c > 0 (scores become c * tanh(score / c))."""
     Tq, Tk, Hq, Hkv, D = (plan.total_q, plan.total_k, plan.num_heads_q, plan.num_heads_kv,
                           plan.head_dim)
     _need(q, "q", torch.bfloat16, (Tq, Hq, D))
@@ -304,13 +305,14 @@ def ffa_fwd_ex(plan: Plan, q, k, v, sink=None, sink_layout="sh", out=None, lse=N
     ws = _workspace(nbytes, q.device, workspace)
     scale = 0.0 if softmax_scale is None else float(softmax_scale)
     _check("ffa_fwd_ex", load_library().ffa_fwd_ex(plan.handle, _ptr(q), _ptr(k), _ptr(v), sp, ns,
-                                                   lay, scale, _ptr(out), _ptr(lse), _ptr(ws),
-                                                   nbytes, _stream(stream)))
+                                                   lay, scale, float(softcap), _ptr(out), _ptr(lse),
+                                                   _ptr(ws), nbytes, _stream(stream)))
     return out, lse
 
 
 def ffa_bwd_ex(plan: Plan, q, k, v, out, dout, lse, sink=None, sink_layout="sh", dq=None,
-               dk=None, dv=None, dsink=None, softmax_scale=None, workspace=None, stream=None):
+               dk=None, dv=None, dsink=None, softmax_scale=None, softcap=0.0, workspace=None,
+               stream=None):
     """Backward of ffa_fwd_ex: (dq, dk, dv, dsink); dsink is None without a sink."""
     Tq, Tk, Hq, Hkv, D = (plan.total_q, plan.total_k, plan.num_heads_q, plan.num_heads_kv,
                           plan.head_dim)
@@ -333,8 +335,8 @@ def ffa_bwd_ex(plan: Plan, q, k, v, out, dout, lse, sink=None, sink_layout="sh",
     scale = 0.0 if softmax_scale is None else float(softmax_scale)
     _check("ffa_bwd_ex", load_library().ffa_bwd_ex(
         plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), sp, ns, lay,
-        scale, _ptr(dq), _ptr(dk), _ptr(dv), None if dsink is None else _ptr(dsink), _ptr(ws),
-        nbytes, _stream(stream)))
+        scale, float(softcap), _ptr(dq), _ptr(dk), _ptr(dv), None if dsink is None else _ptr(dsink),
+        _ptr(ws), nbytes, _stream(stream)))
     return dq, dk, dv, (dsink if ns > 0 else None)
 
 

@@ -97,6 +97,7 @@ struct KvParams {
   __nv_bfloat16* dv;
   int* err;
   uint64_t wait_ns;
+  CapConsts cap;  // used by the softcap instantiation only
 };
 
 // P^T and dS^T for key row j over the 64 queries [q0, q0+64) of the step
@@ -105,10 +106,13 @@ struct KvParams {
 //   p = 2^(s * scale * log2e - lse2), ds = p * (dp - delta).
 // dS^T goes to TMEM as bf16 pairs over dP^T columns [q0, q0+32); P^T goes to
 // query chunk q0/64 of the 128-byte swizzled shared-memory tile (row j).
-template <bool kPartial>
+// kCap: scores capped to c tanh(scale s / c); then x = c log2e tanh(..) - lse2
+// and dS also carries the factor 1 - tanh^2.
+template <bool kPartial, bool kCap>
 __device__ __forceinline__ void pds_half(const uint32_t (&s)[64], uint32_t tP, int q0,
                                          const float* nl, const float* nd, float scale_log2,
-                                         uint32_t m_lo, uint32_t m_hi, int j, uint8_t* p_row) {
+                                         const CapConsts& cap, uint32_t m_lo, uint32_t m_hi, int j,
+                                         uint8_t* p_row) {
   const float2 sc2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
@@ -124,8 +128,14 @@ __device__ __forceinline__ void pds_half(const uint32_t (&s)[64], uint32_t tP, i
         const int lc = 32 * c + e + u;  // column within this warpgroup's half
         const float2 nlp = u == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
         const float2 ndp = u == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
-        const float2 x = __ffma2_rn(
-            make_float2(__uint_as_float(s[lc]), __uint_as_float(s[lc + 1])), sc2, nlp);
+        float2 th = make_float2(0.f, 0.f);
+        if (kCap)
+          th = make_float2(tanhf(__uint_as_float(s[lc]) * cap.a),
+                           tanhf(__uint_as_float(s[lc + 1]) * cap.a));
+        const float2 x =
+            kCap ? __ffma2_rn(th, make_float2(cap.c2, cap.c2), nlp)
+                 : __ffma2_rn(make_float2(__uint_as_float(s[lc]), __uint_as_float(s[lc + 1])), sc2,
+                              nlp);
         float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
         if (kPartial) {  // bits of this warpgroup's 64 columns: m_lo (0-31), m_hi (32-63)
           const uint32_t mw = lc < 32 ? m_lo : m_hi;
@@ -134,7 +144,8 @@ __device__ __forceinline__ void pds_half(const uint32_t (&s)[64], uint32_t tP, i
         }
         const float2 dpd = __fadd2_rn(
             make_float2(__uint_as_float(dp[e + u]), __uint_as_float(dp[e + u + 1])), ndp);
-        const float2 ds = __fmul2_rn(p, dpd);
+        float2 ds = __fmul2_rn(p, dpd);
+        if (kCap) ds = __fmul2_rn(ds, make_float2(1.f - th.x * th.x, 1.f - th.y * th.y));
         pp[(e + u) >> 1] = pack_bf16x2(p.x, p.y);
         dd[(e + u) >> 1] = pack_bf16x2(ds.x, ds.y);
       }
@@ -150,7 +161,7 @@ __device__ __forceinline__ void pds_half(const uint32_t (&s)[64], uint32_t tP, i
   }
 }
 
-template <int D>
+template <int D, bool kCap>
 __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
     ffa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -415,8 +426,10 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
         ++sdp_cnt;
         tc_fence_after();
         const uint32_t m_lo = wg ? vb[2] : vb[0], m_hi = wg ? vb[3] : vb[1];
-        if (info & 1) pds_half<true>(s, tP, 64 * wg, nl, nd, P.scale_log2, m_lo, m_hi, j, p_row);
-        else pds_half<false>(s, tP, 64 * wg, nl, nd, P.scale_log2, m_lo, m_hi, j, p_row);
+        if (info & 1)
+          pds_half<true, kCap>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, m_hi, j, p_row);
+        else
+          pds_half<false, kCap>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, m_hi, j, p_row);
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
@@ -526,6 +539,7 @@ struct DqParams {
   __nv_bfloat16* dq;
   int* err;
   uint64_t wait_ns;
+  CapConsts cap;  // used by the softcap instantiation only
 };
 
 __device__ __forceinline__ bool half_active(const int* it, int h) {
@@ -534,7 +548,7 @@ __device__ __forceinline__ bool half_active(const int* it, int h) {
 
 __device__ __forceinline__ int half_info(const int4& st, int h) { return h == 0 ? st.y : st.z; }
 
-template <int D>
+template <int D, bool kCap>
 __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     ffa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -799,17 +813,24 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
               const int lc = 32 * c + e;
-              const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])),
-                                          sc2, nl2);
+              float2 th = make_float2(0.f, 0.f);
+              if (kCap)
+                th = make_float2(tanhf(__uint_as_float(s[e]) * P.cap.a),
+                                 tanhf(__uint_as_float(s[e + 1]) * P.cap.a));
+              const float2 x =
+                  kCap ? __ffma2_rn(th, make_float2(P.cap.c2, P.cap.c2), nl2)
+                       : __ffma2_rn(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])),
+                                    sc2, nl2);
               float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
               if (info & 1) {  // lc is this warpgroup's column: m_lo (0-31), m_hi (32-63)
                 const uint32_t mw = lc < 32 ? m_lo : m_hi;
                 p.x = ((mw >> (lc & 31)) & 1u) ? p.x : 0.f;
                 p.y = ((mw >> ((lc + 1) & 31)) & 1u) ? p.y : 0.f;
               }
-              const float2 ds = __fmul2_rn(
+              float2 ds = __fmul2_rn(
                   p, __fadd2_rn(make_float2(__uint_as_float(dp[lc]), __uint_as_float(dp[lc + 1])),
                                 make_float2(nd, nd)));
+              if (kCap) ds = __fmul2_rn(ds, make_float2(1.f - th.x * th.x, 1.f - th.y * th.y));
               dd[e >> 1] = pack_bf16x2(ds.x, ds.y);
             }
             // chunk c writes columns [64wg + 16c, 64wg + 16c + 16), read by chunk 0
@@ -937,11 +958,16 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-template <int D>
+template <int D, bool kCap>
 ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const void* v,
                           const void* out, const void* dout, const float* lse, float scale,
                           void* dq, void* dk, void* dv, void* ws, cudaStream_t st,
-                          const SinkArgs& sk, float* dsink) {
+                          const SinkArgs& sk, float* dsink, float softcap) {
+  CapConsts cap;
+  if (kCap) {
+    cap.a = scale / softcap;
+    cap.c2 = softcap * kLog2e;
+  }
   const int qpad = p->n_qt * 128;
   float* nlse2 = static_cast<float*>(ws);
   float* ndelta = nlse2 + (size_t)p->Hq * qpad;
@@ -989,16 +1015,17 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     P.nlse2 = nlse2;
     P.ndelta = ndelta;
     P.dk = static_cast<__nv_bfloat16*>(dk);
+    P.cap = cap;
     P.dv = static_cast<__nv_bfloat16*>(dv);
     P.err = p->err;
     P.wait_ns = p->wait_ns;
-    if (cudaFuncSetAttribute(ffa_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(ffa_bwd_dkdv_kernel<D, kCap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return FFA_ERR_CUDA;
-    if (!split_regs_ok<ffa_bwd_dkdv_kernel<D>>()) return FFA_ERR_UNSUPPORTED;
+    if (!split_regs_ok<ffa_bwd_dkdv_kernel<D, kCap>>()) return FFA_ERR_UNSUPPORTED;
     if (cudaMemsetAsync(P.ticket, 0, sizeof(int), st) != cudaSuccess) return FFA_ERR_CUDA;
     record_phase(p, 3, st);
-    ffa_bwd_dkdv_kernel<D><<<p->grid_bwd, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, P);
+    ffa_bwd_dkdv_kernel<D, kCap><<<p->grid_bwd, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, P);
     note_launches(1);
     if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   }
@@ -1022,15 +1049,16 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     P.nlse2 = nlse2;
     P.ndelta = ndelta;
     P.dq = static_cast<__nv_bfloat16*>(dq);
+    P.cap = cap;
     P.err = p->err;
     P.wait_ns = p->wait_ns;
-    if (cudaFuncSetAttribute(ffa_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(ffa_bwd_dq_kernel<D, kCap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return FFA_ERR_CUDA;
-    if (!split_regs_ok<ffa_bwd_dq_kernel<D>>()) return FFA_ERR_UNSUPPORTED;
+    if (!split_regs_ok<ffa_bwd_dq_kernel<D, kCap>>()) return FFA_ERR_UNSUPPORTED;
     if (cudaMemsetAsync(P.ticket, 0, sizeof(int), st) != cudaSuccess) return FFA_ERR_CUDA;
     record_phase(p, 4, st);
-    ffa_bwd_dq_kernel<D><<<p->grid_dq, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, P);
+    ffa_bwd_dq_kernel<D, kCap><<<p->grid_dq, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, P);
     note_launches(1);
     if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   }
@@ -1048,11 +1076,18 @@ size_t bwd_workspace_bytes(const ffa_plan_s* p) {
 ffa_status_t launch_bwd(ffa_plan_s* p, const void* q, const void* k, const void* v,
                         const void* out, const void* dout, const float* lse, float scale,
                         void* dq, void* dk, void* dv, void* ws, size_t, cudaStream_t st,
-                        const SinkArgs& sink, float* dsink) {
+                        const SinkArgs& sink, float* dsink, float softcap) {
+  const bool c = softcap > 0.f;
   if (p->D == 128)
-    return launch_bwd_d<128>(p, q, k, v, out, dout, lse, scale, dq, dk, dv, ws, st, sink, dsink);
+    return c ? launch_bwd_d<128, true>(p, q, k, v, out, dout, lse, scale, dq, dk, dv, ws, st, sink,
+                                       dsink, softcap)
+             : launch_bwd_d<128, false>(p, q, k, v, out, dout, lse, scale, dq, dk, dv, ws, st,
+                                        sink, dsink, softcap);
   if (p->D == 64)
-    return launch_bwd_d<64>(p, q, k, v, out, dout, lse, scale, dq, dk, dv, ws, st, sink, dsink);
+    return c ? launch_bwd_d<64, true>(p, q, k, v, out, dout, lse, scale, dq, dk, dv, ws, st, sink,
+                                      dsink, softcap)
+             : launch_bwd_d<64, false>(p, q, k, v, out, dout, lse, scale, dq, dk, dv, ws, st, sink,
+                                       dsink, softcap);
   return FFA_ERR_UNSUPPORTED;
 }
 

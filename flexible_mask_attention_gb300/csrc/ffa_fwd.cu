@@ -28,6 +28,10 @@
 // Masked entries become -inf (only on PARTIAL steps), a row with no visible
 // key keeps l = 0 and is written as out = 0, lse = -inf.
 //
+// Softcap (optional, a separate instantiation): scores become
+// c * tanh(scale * s / c) before the softmax; the tile maximum is capped the
+// same way (tanh is increasing) and masked entries stay -inf.
+//
 // Attention sink (optional): the sink logits of a row join its normaliser
 // only.  The epilogue of an unsplit item (or the merge of a split one) adds
 // log2 sum_s 2^(sink_s log2 e) to the keys' log-normaliser and scales out by
@@ -85,7 +89,13 @@ struct FwdParams {
   uint64_t wait_ns;
   const float* sink;  // optional sink logits
   int n_sink, sink_layout;
+  CapConsts cap;      // used by the softcap instantiation only
 };
+
+// Capped score in base-2 units for raw score x (-inf stays -inf).
+__device__ __forceinline__ float capped2(float x, const CapConsts& c) {
+  return x == -INFINITY ? -INFINITY : c.c2 * tanhf(x * c.a);
+}
 
 // log2 of sum_s exp(sink_s) for (row, head) (-inf without sinks); sink logits
 // are natural-log values.  layout 0: sink[s][Hq], layout 1: sink[row][s][Hq].
@@ -116,7 +126,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-template <int D>
+template <int D, bool kCap>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     ffa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams P) {
@@ -385,7 +395,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mx3 = fmax3(mx3, __uint_as_float(u[c + 6]), __uint_as_float(u[c + 7]));
         }
         const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-        const float m_cand = mx * P.scale_log2;
+        const float m_cand = kCap ? capped2(mx, P.cap) : mx * P.scale_log2;
         const bool raise = m_cand > m + kRescaleThreshold;
         const bool rescale_o = raise && visited && m > -INFINITY;
         const float alpha = raise ? exp2f(m - m_cand) : 1.f;
@@ -418,8 +428,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int c = 32 * q4 + 2 * i;
-            const float2 t = __ffma2_rn(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])),
-                                        sc2, nm2);
+            const float2 t =
+                kCap ? make_float2(capped2(__uint_as_float(u[c]), P.cap) - mu,
+                                   capped2(__uint_as_float(u[c + 1]), P.cap) - mu)
+                     : __ffma2_rn(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])),
+                                  sc2, nm2);
             const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
             acc[i & 3] = __fadd2_rn(acc[i & 3], p);
             pk[i] = pack_bf16x2(p.x, p.y);
@@ -558,9 +571,10 @@ __global__ void __launch_bounds__(128)
   lse[(size_t)head * Tq + row] = lse2 * kLn2;
 }
 
-template <int D>
+template <int D, bool kCap>
 ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const void* v, float scale,
-                          void* out, float* lse, void* ws, cudaStream_t st, const SinkArgs& sk) {
+                          void* out, float* lse, void* ws, cudaStream_t st, const SinkArgs& sk,
+                          float softcap) {
   using C = FwdCfg<D>;
   alignas(64) CUtensorMap tq, tk, tv;
   if (!encode_tile_map(&tq, q, p->Tq, p->Hq * D) || !encode_tile_map(&tk, k, p->Tk, p->Hkv * D) ||
@@ -587,13 +601,17 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   P.sink = sk.sink;
   P.n_sink = sk.n;
   P.sink_layout = sk.layout;
-  if (cudaFuncSetAttribute(ffa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (kCap) {
+    P.cap.a = scale / softcap;
+    P.cap.c2 = softcap * kLog2e;
+  }
+  if (cudaFuncSetAttribute(ffa_fwd_kernel<D, kCap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
     return FFA_ERR_CUDA;
-  if (!split_regs_ok<ffa_fwd_kernel<D>>()) return FFA_ERR_UNSUPPORTED;
+  if (!split_regs_ok<ffa_fwd_kernel<D, kCap>>()) return FFA_ERR_UNSUPPORTED;
   if (cudaMemsetAsync(P.ticket, 0, sizeof(int), st) != cudaSuccess) return FFA_ERR_CUDA;
   record_phase(p, 0, st);
-  ffa_fwd_kernel<D><<<p->grid_fwd, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, P);
+  ffa_fwd_kernel<D, kCap><<<p->grid_fwd, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, P);
   note_launches(1);
   if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   if (p->n_merges > 0) {
@@ -614,9 +632,14 @@ size_t fwd_workspace_bytes(const ffa_plan_s* p) {
 
 ffa_status_t launch_fwd(ffa_plan_s* p, const void* q, const void* k, const void* v, float scale,
                         void* out, float* lse, void* ws, size_t, cudaStream_t st,
-                        const SinkArgs& sink) {
-  if (p->D == 128) return launch_fwd_d<128>(p, q, k, v, scale, out, lse, ws, st, sink);
-  if (p->D == 64) return launch_fwd_d<64>(p, q, k, v, scale, out, lse, ws, st, sink);
+                        const SinkArgs& sink, float softcap) {
+  const bool cap = softcap > 0.f;
+  if (p->D == 128)
+    return cap ? launch_fwd_d<128, true>(p, q, k, v, scale, out, lse, ws, st, sink, softcap)
+               : launch_fwd_d<128, false>(p, q, k, v, scale, out, lse, ws, st, sink, softcap);
+  if (p->D == 64)
+    return cap ? launch_fwd_d<64, true>(p, q, k, v, scale, out, lse, ws, st, sink, softcap)
+               : launch_fwd_d<64, false>(p, q, k, v, scale, out, lse, ws, st, sink, softcap);
   return FFA_ERR_UNSUPPORTED;
 }
 

@@ -162,14 +162,21 @@ struct SinkArgs {
 // Implemented in ffa_fwd.cu / ffa_bwd.cu.
 ffa_status_t launch_fwd(ffa_plan_s* p, const void* q, const void* k, const void* v, float scale,
                         void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t st,
-                        const SinkArgs& sink = SinkArgs());
+                        const SinkArgs& sink = SinkArgs(), float softcap = 0.f);
 size_t fwd_workspace_bytes(const ffa_plan_s* p);
 // dsink (when non-null and sink.n > 0) receives the sink gradient, in the
 // sink's own layout, overwritten.
 ffa_status_t launch_bwd(ffa_plan_s* p, const void* q, const void* k, const void* v,
                         const void* out, const void* dout, const float* lse, float scale,
                         void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, cudaStream_t st,
-                        const SinkArgs& sink = SinkArgs(), float* dsink = nullptr);
+                        const SinkArgs& sink = SinkArgs(), float* dsink = nullptr,
+                        float softcap = 0.f);
+// Softcap c > 0: every score x = scale * q.k becomes c * tanh(x / c).  In
+// base-2 units the kernels use x2 = c log2(e) tanh(raw * scale / c).
+struct CapConsts {
+  float a = 0.f;   // scale / c
+  float c2 = 0.f;  // c * log2(e)
+};
 size_t bwd_workspace_bytes(const ffa_plan_s* p);
 // Implemented in ffa_plan.cu.
 bool encode_tile_map(void* map128, const void* base, int rows, int cols_elems);

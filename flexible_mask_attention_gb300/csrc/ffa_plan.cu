@@ -988,12 +988,13 @@ size_t ffa_bwd_workspace_size(ffa_plan_t p) { return p ? bwd_workspace_bytes(p) 
 
 ffa_status_t ffa_fwd_ex(ffa_plan_t p, const void* q, const void* k, const void* v,
                         const float* sink, int32_t num_sink, int32_t sink_layout,
-                        float softmax_scale, void* out, float* lse, void* workspace,
-                        size_t workspace_bytes, ffa_stream_t stream) {
+                        float softmax_scale, float softcap, void* out, float* lse,
+                        void* workspace, size_t workspace_bytes, ffa_stream_t stream) {
   if (!p || !q || !k || !v || !out || !lse) return FFA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
     return FFA_ERR_INVALID_ARG;
   if (!sink_args_ok(sink, num_sink, sink_layout)) return FFA_ERR_INVALID_ARG;
+  if (!(softcap >= 0.f && softcap <= 3.0e38f)) return FFA_ERR_INVALID_ARG;  // also rejects NaN
   const size_t need = fwd_workspace_bytes(p);
   if (workspace_bytes < need || (need > 0 && (!workspace || !aligned16(workspace))))
     return FFA_ERR_WORKSPACE;
@@ -1003,20 +1004,20 @@ ffa_status_t ffa_fwd_ex(ffa_plan_t p, const void* q, const void* k, const void* 
   sk.n = num_sink;
   sk.layout = sink_layout;
   return launch_fwd(p, q, k, v, scale, out, lse, workspace, workspace_bytes,
-                    reinterpret_cast<cudaStream_t>(stream), sk);
+                    reinterpret_cast<cudaStream_t>(stream), sk, softcap);
 }
 
 ffa_status_t ffa_fwd(ffa_plan_t p, const void* q, const void* k, const void* v,
                      float softmax_scale, void* out, float* lse, void* workspace,
                      size_t workspace_bytes, ffa_stream_t stream) {
-  return ffa_fwd_ex(p, q, k, v, nullptr, 0, FFA_SINK_SH, softmax_scale, out, lse, workspace,
+  return ffa_fwd_ex(p, q, k, v, nullptr, 0, FFA_SINK_SH, softmax_scale, 0.f, out, lse, workspace,
                     workspace_bytes, stream);
 }
 
 ffa_status_t ffa_bwd_ex(ffa_plan_t p, const void* q, const void* k, const void* v, const void* out,
                         const void* dout, const float* lse, const float* sink, int32_t num_sink,
-                        int32_t sink_layout, float softmax_scale, void* dq, void* dk, void* dv,
-                        float* dsink, void* workspace, size_t workspace_bytes,
+                        int32_t sink_layout, float softmax_scale, float softcap, void* dq, void* dk,
+                        void* dv, float* dsink, void* workspace, size_t workspace_bytes,
                         ffa_stream_t stream) {
   if (!p || !q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv)
     return FFA_ERR_INVALID_ARG;
@@ -1025,6 +1026,7 @@ ffa_status_t ffa_bwd_ex(ffa_plan_t p, const void* q, const void* k, const void* 
     if (!aligned16(x)) return FFA_ERR_INVALID_ARG;
   if (!sink_args_ok(sink, num_sink, sink_layout)) return FFA_ERR_INVALID_ARG;
   if (dsink && (reinterpret_cast<uintptr_t>(dsink) & 3u)) return FFA_ERR_INVALID_ARG;
+  if (!(softcap >= 0.f && softcap <= 3.0e38f)) return FFA_ERR_INVALID_ARG;  // also rejects NaN
   const size_t need = bwd_workspace_bytes(p);
   if (workspace_bytes < need || (need > 0 && (!workspace || !aligned16(workspace))))
     return FFA_ERR_WORKSPACE;
@@ -1034,14 +1036,14 @@ ffa_status_t ffa_bwd_ex(ffa_plan_t p, const void* q, const void* k, const void* 
   sk.n = num_sink;
   sk.layout = sink_layout;
   return launch_bwd(p, q, k, v, out, dout, lse, scale, dq, dk, dv, workspace, workspace_bytes,
-                    reinterpret_cast<cudaStream_t>(stream), sk, dsink);
+                    reinterpret_cast<cudaStream_t>(stream), sk, dsink, softcap);
 }
 
 ffa_status_t ffa_bwd(ffa_plan_t p, const void* q, const void* k, const void* v, const void* out,
                      const void* dout, const float* lse, float softmax_scale, void* dq, void* dk,
                      void* dv, void* workspace, size_t workspace_bytes, ffa_stream_t stream) {
-  return ffa_bwd_ex(p, q, k, v, out, dout, lse, nullptr, 0, FFA_SINK_SH, softmax_scale, dq, dk,
-                    dv, nullptr, workspace, workspace_bytes, stream);
+  return ffa_bwd_ex(p, q, k, v, out, dout, lse, nullptr, 0, FFA_SINK_SH, softmax_scale, 0.f, dq,
+                    dk, dv, nullptr, workspace, workspace_bytes, stream);
 }
 
 ffa_status_t ffa_get_last_device_error(ffa_plan_t p, int32_t* code, int32_t* where,

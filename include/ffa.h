@@ -146,14 +146,21 @@ ffa_status_t ffa_fwd(ffa_plan_t plan, const void* q, const void* k, const void* 
 typedef enum { FFA_SINK_SH = 0, FFA_SINK_SSH = 1 } ffa_sink_layout_t;
 #define FFA_MAX_SINK 64 /* largest num_sink accepted */
 
-/* ffa_fwd with optional sink logits (num_sink = 0: none, sink may be NULL;
- * identical to ffa_fwd).  Returns FFA_ERR_INVALID_ARG for num_sink outside
- * [0, FFA_MAX_SINK], an unknown layout, or a NULL / misaligned sink when
- * num_sink > 0.  lse includes the sink term. */
+/* Softcap (MagiAttention quickstart card: the `softcap` argument of
+ * flex_flash_attn_func, default 0; the pages give no formula).  This library
+ * reads it as the usual smooth cap: for softcap = c > 0 every score
+ * x = scale * q_i.k_j becomes c * tanh(x / c) before the softmax (the
+ * backward carries the factor 1 - tanh^2 into dS); c = 0 means no cap.
+ *
+ * ffa_fwd with optional sink logits and softcap (num_sink = 0 and
+ * softcap = 0: identical to ffa_fwd; sink may then be NULL).  Returns
+ * FFA_ERR_INVALID_ARG for num_sink outside [0, FFA_MAX_SINK], an unknown
+ * layout, a NULL / misaligned sink when num_sink > 0, or a negative or
+ * non-finite softcap.  lse includes the sink term. */
 ffa_status_t ffa_fwd_ex(ffa_plan_t plan, const void* q, const void* k, const void* v,
                         const float* sink, int32_t num_sink, int32_t sink_layout,
-                        float softmax_scale, void* out, float* lse, void* workspace,
-                        size_t workspace_bytes, ffa_stream_t stream);
+                        float softmax_scale, float softcap, void* out, float* lse,
+                        void* workspace, size_t workspace_bytes, ffa_stream_t stream);
 
 /* Backward of ffa_fwd for the loss L with dL/dout = dout.
  *   out, lse: the forward's results; dq, dk, dv receive the gradients
@@ -165,14 +172,14 @@ ffa_status_t ffa_bwd(ffa_plan_t plan, const void* q, const void* k, const void* 
                      ffa_stream_t stream);
 
 /* Backward of ffa_fwd_ex.  out and lse are ffa_fwd_ex's results for the same
- * sink (the sink acts on dq, dk, dv only through lse).  dsink: fp32 DEVICE
+ * sink and softcap (the sink acts on dq, dk, dv only through lse).  dsink: fp32 DEVICE
  * array in the sink's layout, overwritten with the sink gradient, or NULL to
  * skip it; ignored when num_sink = 0.  The per-head sums of the "sh" layout
  * are taken in a fixed order, so repeated calls give identical results. */
 ffa_status_t ffa_bwd_ex(ffa_plan_t plan, const void* q, const void* k, const void* v,
                         const void* out, const void* dout, const float* lse, const float* sink,
-                        int32_t num_sink, int32_t sink_layout, float softmax_scale, void* dq,
-                        void* dk, void* dv, float* dsink, void* workspace,
+                        int32_t num_sink, int32_t sink_layout, float softmax_scale, float softcap,
+                        void* dq, void* dk, void* dv, float* dsink, void* workspace,
                         size_t workspace_bytes, ffa_stream_t stream);
 
 /* Backward without any allocation: the same computation as ffa_bwd, with its

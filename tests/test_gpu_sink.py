@@ -123,11 +123,13 @@ def test_sink_argument_checks():
     out, lse = torch.empty_like(q), torch.empty(H, T, device=DEV)
     big = torch.zeros(ffa.FFA_MAX_SINK + 1, H, device=DEV)
     P = ffa._ptr
-    args = lambda sink, n, lay: (plan.handle, P(q), P(k), P(v), sink, n, lay, 0.0, P(out), P(lse),
-                                 None, 0, None)
+    args = lambda sink, n, lay, cap=0.0: (plan.handle, P(q), P(k), P(v), sink, n, lay, 0.0, cap,
+                                          P(out), P(lse), None, 0, None)
     assert lib.ffa_fwd_ex(*args(P(big), ffa.FFA_MAX_SINK + 1, 0)) == 1
     assert lib.ffa_fwd_ex(*args(None, 2, 0)) == 1
     assert lib.ffa_fwd_ex(*args(P(big), 2, 7)) == 1
     assert lib.ffa_fwd_ex(*args(P(big), -1, 0)) == 1
+    assert lib.ffa_fwd_ex(*args(None, 0, 0, -1.0)) == 1
+    assert lib.ffa_fwd_ex(*args(None, 0, 0, float("nan"))) == 1
     assert lib.ffa_fwd_ex(*args(None, 0, 0)) == 0
     torch.cuda.synchronize()
