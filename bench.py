@@ -45,6 +45,9 @@ def parse_args():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
+    ap.add_argument("--sink", type=int, default=0,
+                    help="attention-sink logits per query head (seeded fp32 [n, Hq]); 0 = none")
+    ap.add_argument("--softcap", type=float, default=0.0, help="score cap c (0 = none)")
     return ap.parse_args()
 
 
@@ -258,6 +261,12 @@ def run_ffa(args, wl, world, rank, local):
     ws_b = torch.empty(max(16, ffa.ffa_bwd_workspace_size(plan0)), dtype=torch.uint8, device=dev)
     plan0.destroy()
     area = info["area"]
+    sink = dsink = None
+    if args.sink > 0:
+        g = torch.Generator().manual_seed(wl.seed + 1000)
+        sink = (2.0 * torch.randn(args.sink, Hq, generator=g)).float().to(dev)
+        dsink = torch.empty_like(sink)
+    extended = sink is not None or args.softcap > 0
     f_fwd = 4.0 * D * area * Hq
     f_bwd = 2.5 * f_fwd
     stream = torch.cuda.current_stream()
@@ -270,10 +279,18 @@ def run_ffa(args, wl, world, rank, local):
         if record is not None:
             ffa.ffa_plan_set_events(plan, record[4:10])
             record[1].record(stream)
-        ffa.ffa_fwd(plan, qa, ka, va, out=out, lse=lse, workspace=ws_f)
+        if extended:
+            ffa.ffa_fwd_ex(plan, qa, ka, va, sink=sink, out=out, lse=lse, softcap=args.softcap,
+                           workspace=ws_f)
+        else:
+            ffa.ffa_fwd(plan, qa, ka, va, out=out, lse=lse, workspace=ws_f)
         if record is not None:
             record[2].record(stream)
-        ffa.ffa_bwd(plan, qa, ka, va, out, doa, lse, dq=dq, dk=dk, dv=dv, workspace=ws_b)
+        if extended:
+            ffa.ffa_bwd_ex(plan, qa, ka, va, out, doa, lse, sink=sink, dq=dq, dk=dk, dv=dv,
+                           dsink=dsink, softcap=args.softcap, workspace=ws_b)
+        else:
+            ffa.ffa_bwd(plan, qa, ka, va, out, doa, lse, dq=dq, dk=dk, dv=dv, workspace=ws_b)
         if record is not None:
             record[3].record(stream)
         return plan
@@ -395,6 +412,7 @@ def finish(args, wl, world, rank, elapsed_ms, t_plan, t_fwd, t_bwd, f_fwd, f_bwd
         "data": "synthetic",
         "config": {"workload": wl.name, "slices": wl.num_slices, "tokens": Tq,
                    "heads_q": Hq, "heads_kv": Hkv, "head_dim": D,
+                   "sink": args.sink, "softcap": args.softcap,
                    "visible_pairs_per_head": area, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: q and dout {Tq * Hq * D * 2 / 1e6:.0f} MB each, "
                          f"k and v {wl.total_k * Hkv * D * 2 / 1e6:.0f} MB each, no flush"},

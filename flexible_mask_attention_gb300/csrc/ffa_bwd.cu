@@ -130,8 +130,8 @@ __device__ __forceinline__ void pds_half(const uint32_t (&s)[64], uint32_t tP, i
         const float2 ndp = u == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
         float2 th = make_float2(0.f, 0.f);
         if (kCap)
-          th = make_float2(tanhf(__uint_as_float(s[lc]) * cap.a),
-                           tanhf(__uint_as_float(s[lc + 1]) * cap.a));
+          th = make_float2(tanh_exp(__uint_as_float(s[lc]) * cap.a),
+                           tanh_exp(__uint_as_float(s[lc + 1]) * cap.a));
         const float2 x =
             kCap ? __ffma2_rn(th, make_float2(cap.c2, cap.c2), nlp)
                  : __ffma2_rn(make_float2(__uint_as_float(s[lc]), __uint_as_float(s[lc + 1])), sc2,
@@ -815,8 +815,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
               const int lc = 32 * c + e;
               float2 th = make_float2(0.f, 0.f);
               if (kCap)
-                th = make_float2(tanhf(__uint_as_float(s[e]) * P.cap.a),
-                                 tanhf(__uint_as_float(s[e + 1]) * P.cap.a));
+                th = make_float2(tanh_exp(__uint_as_float(s[e]) * P.cap.a),
+                                 tanh_exp(__uint_as_float(s[e + 1]) * P.cap.a));
               const float2 x =
                   kCap ? __ffma2_rn(th, make_float2(P.cap.c2, P.cap.c2), nl2)
                        : __ffma2_rn(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])),

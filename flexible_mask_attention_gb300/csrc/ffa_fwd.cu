@@ -94,7 +94,7 @@ struct FwdParams {
 
 // Capped score in base-2 units for raw score x (-inf stays -inf).
 __device__ __forceinline__ float capped2(float x, const CapConsts& c) {
-  return x == -INFINITY ? -INFINITY : c.c2 * tanhf(x * c.a);
+  return x == -INFINITY ? -INFINITY : c.c2 * tanh_exp(x * c.a);
 }
 
 // log2 of sum_s exp(sink_s) for (row, head) (-inf without sinks); sink logits

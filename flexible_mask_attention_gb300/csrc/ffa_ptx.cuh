@@ -349,6 +349,21 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// tanh from the identity tanh(u) = 1 - 2 / (e^(2u) + 1), with the hardware
+// base-2 exponential and reciprocal: absolute error of a few 1e-7, exactly
+// +-1 once e^(2u) overflows or underflows.  (Used for the softcap, where
+// only absolute errors of the capped score matter.)
+__device__ __forceinline__ float tanh_exp(float u) {
+  const float e = ex2_approx(u * 2.8853900817779268f);  // 2 log2(e)
+  return 1.f - 2.f * rcp_approx(e + 1.f);
+}
+
 // Register split of the 384-thread kernels (three warpgroups, one CTA per
 // SM).  They compile to 168 registers per thread (65536 / 384, rounded down
 // to a multiple of 8); the control warpgroup (producer, MMA issuer, two idle
