@@ -10,7 +10,7 @@
 //          dP^T = V dO^T               (tcgen05, SS)  -> TMEM
 //          P^T  = 2^(S^T*scale*log2e - lse2), masked on PARTIAL steps
 //          dS^T = P^T * (dP^T - delta)
-//          dV  += P^T dO               (tcgen05, A = P^T from shared memory)
+//          dV  += P^T dO               (tcgen05, A = P^T from TMEM)
 //          dK  += dS^T Q               (tcgen05, A = dS^T from TMEM)
 //      dK, dV accumulate in TMEM and are written once per item;
 //   3. dQ pass, one work unit per (q-tile, query head), over the k-tiles the
@@ -50,25 +50,29 @@ __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity, uint
 // epilogue, warp 8 TMA producer, warp 9 MMA issuer (TMEM owner), warps 10-11
 // idle; registers split 200 / 104 between them (ffa_ptx.cuh).
 // TMEM columns: dV [0,D), dK [D,2D), S^T [2D,2D+128), dP^T [2D+128,2D+256).
-// Warpgroup w writes its dS^T pairs over dP^T columns [64w, 64w+32), inside
-// the range it read itself.
+// Warpgroup w owns dP^T columns [64w, 64w+64) of that range and, once it has
+// read a 32-column chunk, overwrites the chunk with bf16 pairs: dS^T in its
+// first 16 columns, P^T in its last 16.  Both later MMAs take their A operand
+// from there, so shared memory carries only the four bf16 tiles.
 template <int D>
 struct KvCfg {
   static constexpr int kThreads = kSplitThreads;
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kStages = 2;
+  // Q is read first (by the S^T MMA), so it gets the deeper ring; -lse2 and
+  // -delta (read with dP^T) travel with dO.
+  static constexpr int kQStages = D == 128 ? 3 : 4;
+  static constexpr int kDOStages = D == 128 ? 2 : 4;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kTileBytes;
   static constexpr int kQOff = 2 * kTileBytes;
-  static constexpr int kDOOff = kQOff + kStages * kTileBytes;
-  static constexpr int kPOff = kDOOff + kStages * kTileBytes;  // P^T, 128 keys x 128 queries bf16
-  static constexpr int kLseOff = kPOff + 128 * 128 * 2;        // per stage: -lse2[128], -delta[128]
+  static constexpr int kDOOff = kQOff + kQStages * kTileBytes;
+  static constexpr int kLseOff = kDOOff + kDOStages * kTileBytes;  // per dO stage: -lse2, -delta
   static constexpr int kLseStageBytes = 2 * 128 * 4;
-  static constexpr int kBarOff = kLseOff + kStages * kLseStageBytes;
-  static constexpr int kBKVFull = 0, kBKVEmpty = 1, kBQFull = 2, kBQEmpty = 2 + kStages,
-                       kBDOFull = 2 + 2 * kStages, kBDOEmpty = 2 + 3 * kStages,
-                       kBSdpFull = 2 + 4 * kStages, kBSFree = kBSdpFull + 1,
+  static constexpr int kBarOff = kLseOff + kDOStages * kLseStageBytes;
+  static constexpr int kBKVFull = 0, kBKVEmpty = 1, kBQFull = 2, kBQEmpty = 2 + kQStages,
+                       kBDOFull = 2 + 2 * kQStages, kBDOEmpty = kBDOFull + kDOStages,
+                       kBSdpFull = kBDOEmpty + kDOStages, kBSFree = kBSdpFull + 1,
                        kBPFull = kBSFree + 1, kBDkvFull = kBPFull + 1,
                        kBDkvEmpty = kBDkvFull + 1, kBDrain = kBDkvEmpty + 1,
                        kBSFull = kBDrain + 1, kBItemFull = kBSFull + 1,
@@ -100,19 +104,18 @@ struct KvParams {
   CapConsts cap;  // used by the softcap instantiation only
 };
 
-// P^T and dS^T for key row j over the 64 queries [q0, q0+64) of the step
-// owned by this warpgroup, from the S^T values already in registers (s) and
-// the dP^T values read from TMEM here:
+// P^T and dS^T for one key row (TMEM lane) over the 64 queries [q0, q0+64)
+// of the step owned by this warpgroup, from the S^T values already in
+// registers (s) and the dP^T values read from TMEM here:
 //   p = 2^(s * scale * log2e - lse2), ds = p * (dp - delta).
-// dS^T goes to TMEM as bf16 pairs over dP^T columns [q0, q0+32); P^T goes to
-// query chunk q0/64 of the 128-byte swizzled shared-memory tile (row j).
+// Queries [q0+32c, q0+32c+32) go back, as bf16 pairs, over the dP^T chunk
+// they were read from: dS^T in columns [q0+32c, +16), P^T in [q0+32c+16, +16).
 // kCap: scores capped to c tanh(scale s / c); then x = c log2e tanh(..) - lse2
 // and dS also carries the factor 1 - tanh^2.
 template <bool kPartial, bool kCap>
 __device__ __forceinline__ void pds_half(const uint32_t (&s)[64], uint32_t tP, int q0,
                                          const float* nl, const float* nd, float scale_log2,
-                                         const CapConsts& cap, uint32_t m_lo, uint32_t m_hi, int j,
-                                         uint8_t* p_row) {
+                                         const CapConsts& cap, uint32_t m_lo, uint32_t m_hi) {
   const float2 sc2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
@@ -150,14 +153,8 @@ __device__ __forceinline__ void pds_half(const uint32_t (&s)[64], uint32_t tP, i
         dd[(e + u) >> 1] = pack_bf16x2(ds.x, ds.y);
       }
     }
-    // chunk c writes dP^T columns [q0 + 16c, q0 + 16c + 16), read by chunk 0
-    tmem_st16(tP + q0 + 16 * c, dd);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int unit = c * 4 + u;
-      *reinterpret_cast<uint4*>(p_row + ((unit ^ (j & 7)) << 4)) =
-          make_uint4(pp[4 * u], pp[4 * u + 1], pp[4 * u + 2], pp[4 * u + 3]);
-    }
+    tmem_st16(tP + q0 + 32 * c, dd);
+    tmem_st16(tP + q0 + 32 * c + 16, pp);
   }
 }
 
@@ -187,9 +184,11 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(C::kBKVFull), 1);
     mbar_init(bar(C::kBKVEmpty), 1);
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < C::kQStages; ++s) {
       mbar_init(bar(C::kBQFull + s), 1);
       mbar_init(bar(C::kBQEmpty + s), 1);
+    }
+    for (int s = 0; s < C::kDOStages; ++s) {
       mbar_init(bar(C::kBDOFull + s), 1);
       mbar_init(bar(C::kBDOEmpty + s), 1);
     }
@@ -225,8 +224,8 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_do);
-      uint32_t kv_cnt = 0, q_cnt = 0;
-      bool ok = true, q_only = false;  // q_only: Q of iteration q_cnt issued, its dO not yet
+      uint32_t kv_cnt = 0, q_cnt = 0, do_cnt = 0;  // tiles issued
+      bool ok = true;
       for (int r = 0; ok; ++r) {
         const int pos = atomicAdd(P.ticket, 1);
         const int idx = pos < P.n_items ? P.order[pos] : -1;
@@ -248,35 +247,36 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
         for (int i = 0; i < n_it; ++i) {
           const int qt = P.steps[sb + i / g].x;
           const int h = hk * g + i % g;
-          const int stage = q_cnt % C::kStages;
-          const uint32_t ph = (q_cnt / C::kStages) & 1;
-          if (!(ok = mbar_wait(bar(C::kBQEmpty + stage), ph ^ 1, ctl, 401))) break;
-          mbar_arrive_expect_tx(bar(C::kBQFull + stage), C::kTileBytes + C::kLseStageBytes);
+          const int qs = q_cnt % C::kQStages;
+          if (!(ok = mbar_wait(bar(C::kBQEmpty + qs), ((q_cnt / C::kQStages) & 1) ^ 1, ctl, 401)))
+            break;
+          mbar_arrive_expect_tx(bar(C::kBQFull + qs), C::kTileBytes);
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_2d(sbase + C::kQOff + stage * C::kTileBytes + c * 16384, &tm_q,
-                        bar(C::kBQFull + stage), h * D + c * 64, qt * 128);
-          const uint32_t ls = sbase + C::kLseOff + stage * C::kLseStageBytes;
-          bulk_load(ls, P.nlse2 + (size_t)h * P.qpad + qt * 128, 512, bar(C::kBQFull + stage));
-          bulk_load(ls + 512, P.ndelta + (size_t)h * P.qpad + qt * 128, 512,
-                    bar(C::kBQFull + stage));
-          q_only = true;
-          if (!(ok = mbar_wait(bar(C::kBDOEmpty + stage), ph ^ 1, ctl, 402))) break;
-          q_only = false;
-          mbar_arrive_expect_tx(bar(C::kBDOFull + stage), C::kTileBytes);
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_2d(sbase + C::kDOOff + stage * C::kTileBytes + c * 16384, &tm_do,
-                        bar(C::kBDOFull + stage), h * D + c * 64, qt * 128);
+            tma_load_2d(sbase + C::kQOff + qs * C::kTileBytes + c * 16384, &tm_q,
+                        bar(C::kBQFull + qs), h * D + c * 64, qt * 128);
           ++q_cnt;
+          const int ds = do_cnt % C::kDOStages;
+          if (!(ok = mbar_wait(bar(C::kBDOEmpty + ds), ((do_cnt / C::kDOStages) & 1) ^ 1, ctl,
+                               402)))
+            break;
+          mbar_arrive_expect_tx(bar(C::kBDOFull + ds), C::kTileBytes + C::kLseStageBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_2d(sbase + C::kDOOff + ds * C::kTileBytes + c * 16384, &tm_do,
+                        bar(C::kBDOFull + ds), h * D + c * 64, qt * 128);
+          const uint32_t ls = sbase + C::kLseOff + ds * C::kLseStageBytes;
+          bulk_load(ls, P.nlse2 + (size_t)h * P.qpad + qt * 128, 512, bar(C::kBDOFull + ds));
+          bulk_load(ls + 512, P.ndelta + (size_t)h * P.qpad + qt * 128, 512,
+                    bar(C::kBDOFull + ds));
+          ++do_cnt;
         }
       }
       if (!ok) {
         if (kv_cnt > 0) drain_wait_b(bar(C::kBKVFull), (kv_cnt - 1) & 1, kDrainNs);
-        for (uint32_t i = q_cnt > (uint32_t)C::kStages ? q_cnt - C::kStages : 0; i < q_cnt; ++i) {
-          drain_wait_b(bar(C::kBQFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
-          drain_wait_b(bar(C::kBDOFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
-        }
-        if (q_only)
-          drain_wait_b(bar(C::kBQFull + q_cnt % C::kStages), (q_cnt / C::kStages) & 1, kDrainNs);
+        for (uint32_t i = q_cnt > (uint32_t)C::kQStages ? q_cnt - C::kQStages : 0; i < q_cnt; ++i)
+          drain_wait_b(bar(C::kBQFull + i % C::kQStages), (i / C::kQStages) & 1, kDrainNs);
+        for (uint32_t i = do_cnt > (uint32_t)C::kDOStages ? do_cnt - C::kDOStages : 0; i < do_cnt;
+             ++i)
+          drain_wait_b(bar(C::kBDOFull + i % C::kDOStages), (i / C::kDOStages) & 1, kDrainNs);
       }
     }
   } else if (warp == 9) {
@@ -288,7 +288,6 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
       // Base descriptors: K-major (k) and MN-major (m) views of each buffer.
       const uint64_t dKk = sdesc_sw128(sbase + C::kKOff, 16, 1024);
       const uint64_t dVk = sdesc_sw128(sbase + C::kVOff, 16, 1024);
-      const uint64_t dPk = sdesc_sw128(sbase + C::kPOff, 16, 1024);
       const uint64_t dQk = sdesc_sw128(sbase + C::kQOff, 16, 1024);
       const uint64_t dQm = sdesc_sw128(sbase + C::kQOff, 16384, 1024);
       const uint64_t dDOk = sdesc_sw128(sbase + C::kDOOff, 16, 1024);
@@ -314,21 +313,20 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
         tc_fence_after();
         const int n_it = (se - sb) * g;
         {  // S^T of the first iteration
-          const int stage = q_cnt % C::kStages;
-          if (!(ok = mbar_wait(bar(C::kBQFull + stage), (q_cnt / C::kStages) & 1, ctl, 501))) break;
+          const int qs = q_cnt % C::kQStages;
+          if (!(ok = mbar_wait(bar(C::kBQFull + qs), (q_cnt / C::kQStages) & 1, ctl, 501))) break;
           tc_fence_after();
-          issue_st(stage);
+          issue_st(qs);
           mma_commit(bar(C::kBSFull));
         }
         for (int i = 0; i < n_it; ++i) {
           const uint32_t c = q_cnt + (uint32_t)i;
-          const int stage = c % C::kStages;
-          const uint32_t ph = (c / C::kStages) & 1;
-          if (!(ok = mbar_wait(bar(C::kBDOFull + stage), ph, ctl, 502))) break;
+          const int qs = c % C::kQStages, ds = c % C::kDOStages;
+          if (!(ok = mbar_wait(bar(C::kBDOFull + ds), (c / C::kDOStages) & 1, ctl, 502))) break;
           tc_fence_after();
-          // dP^T = V dO^T; its columns were last read by the previous dK MMA.
+          // dP^T = V dO^T; its columns were last read by the previous dV / dK MMAs.
           {
-            const uint64_t dod = dDOk + stage * kTile16;
+            const uint64_t dod = dDOk + ds * kTile16;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
@@ -339,10 +337,10 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
           if (i + 1 < n_it) {
             // S^T of the next iteration as soon as this S^T is in registers.
             const uint32_t c1 = c + 1;
-            const int st1 = c1 % C::kStages;
+            const int st1 = c1 % C::kQStages;
             if (!(ok = mbar_wait(bar(C::kBSFree), sf_cnt & 1, ctl, 503))) break;
             ++sf_cnt;
-            if (!(ok = mbar_wait(bar(C::kBQFull + st1), (c1 / C::kStages) & 1, ctl, 504))) break;
+            if (!(ok = mbar_wait(bar(C::kBQFull + st1), (c1 / C::kQStages) & 1, ctl, 504))) break;
             tc_fence_after();
             issue_st(st1);
             mma_commit(bar(C::kBSFull));
@@ -356,19 +354,18 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
             tc_fence_after();
           }
           const uint32_t acc0 = i > 0 ? 1u : 0u;
-          const uint64_t dom = dDOm + stage * kTile16;
-          const uint64_t qm = dQm + stage * kTile16;
+          const uint64_t dom = dDOm + ds * kTile16;
+          const uint64_t qm = dQm + qs * kTile16;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t poff = (kk >> 2) * 1024 + (kk & 3) * 2;
-            mma_ss_at(tmem + C::kTdV, dPk, poff, dom, kk * 128, kIdAcc, (acc0 || kk > 0) ? 1u : 0u);
-            // dS^T pairs of queries [16kk, 16kk+16): warpgroup kk/4 wrote them at
-            // dP^T column 64*(kk/4) + 8*(kk%4)
-            mma_ts_at(tmem + C::kTdK, tmem + C::kTdP + 64 * (kk >> 2) + 8 * (kk & 3), qm, kk * 128,
-                      kIdAcc, (acc0 || kk > 0) ? 1u : 0u);
+            // queries [16kk, 16kk+16): warpgroup kk/4, chunk (kk%4)/2, half kk%2 of
+            // the chunk's dS^T (and, 16 columns on, P^T) pairs
+            const uint32_t ta = tmem + C::kTdP + 64 * (kk >> 2) + 32 * ((kk & 3) >> 1) + 8 * (kk & 1);
+            mma_ts_at(tmem + C::kTdV, ta + 16, dom, kk * 128, kIdAcc, (acc0 || kk > 0) ? 1u : 0u);
+            mma_ts_at(tmem + C::kTdK, ta, qm, kk * 128, kIdAcc, (acc0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(bar(C::kBDOEmpty + stage));
-          mma_commit(bar(C::kBQEmpty + stage));
+          mma_commit(bar(C::kBDOEmpty + ds));
+          mma_commit(bar(C::kBQEmpty + qs));
         }
         if (!ok) break;
         // a pending S-free arrival of the last iteration is consumed here
@@ -390,7 +387,6 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_addr + C::kTS + 64 * wg;
     const uint32_t tP = tmem + lane_addr + C::kTdP;
-    uint8_t* p_row = smem + C::kPOff + wg * 16384 + j * 128;
     uint32_t sdp_cnt = 0, dkv_cnt = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
@@ -409,8 +405,8 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
         const int qt = st.x, info = st.y;
         uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
         if (info & 1) step_mask<false>(info, P.slices, P.masks, key, qt, vb);
-        const float* nl = reinterpret_cast<const float*>(smem + C::kLseOff +
-                                                         (sdp_cnt % C::kStages) * C::kLseStageBytes);
+        const float* nl = reinterpret_cast<const float*>(
+            smem + C::kLseOff + (sdp_cnt % C::kDOStages) * C::kLseStageBytes);
         const float* nd = nl + 128;
         // S^T first: its buffer is released before dP^T is even complete, so
         // the next S^T can follow dP^T on the tensor pipe at once.
@@ -427,11 +423,10 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
         tc_fence_after();
         const uint32_t m_lo = wg ? vb[2] : vb[0], m_hi = wg ? vb[3] : vb[1];
         if (info & 1)
-          pds_half<true, kCap>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, m_hi, j, p_row);
+          pds_half<true, kCap>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, m_hi);
         else
-          pds_half<false, kCap>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, m_hi, j, p_row);
+          pds_half<false, kCap>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, m_hi);
         tmem_st_wait();
-        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(C::kBPFull));
       }
