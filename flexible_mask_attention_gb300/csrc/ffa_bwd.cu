@@ -73,7 +73,7 @@ struct KvCfg {
   static constexpr int kBKVFull = 0, kBKVEmpty = 1, kBQFull = 2, kBQEmpty = 2 + kQStages,
                        kBDOFull = 2 + 2 * kQStages, kBDOEmpty = kBDOFull + kDOStages,
                        kBSdpFull = kBDOEmpty + kDOStages, kBSFree = kBSdpFull + 1,
-                       kBPFull = kBSFree + 1, kBDkvFull = kBPFull + 1,
+                       kBPFull = kBSFree + 1, kBDkvFull = kBPFull + 2,
                        kBDkvEmpty = kBDkvFull + 1, kBDrain = kBDkvEmpty + 1,
                        kBSFull = kBDrain + 1, kBItemFull = kBSFull + 1,
                        kBItemEmpty = kBItemFull + kItemRing, kNumBars = kBItemEmpty + kItemRing;
@@ -104,21 +104,20 @@ struct KvParams {
   CapConsts cap;  // used by the softcap instantiation only
 };
 
-// P^T and dS^T for one key row (TMEM lane) over the 64 queries [q0, q0+64)
-// of the step owned by this warpgroup, from the S^T values already in
-// registers (s) and the dP^T values read from TMEM here:
+// P^T and dS^T for one key row (TMEM lane) over the 32 queries
+// [q0+32c, q0+32c+32) of the step (chunk c of this warpgroup's 64), from the
+// S^T values already in registers (s) and the dP^T values read from TMEM here:
 //   p = 2^(s * scale * log2e - lse2), ds = p * (dp - delta).
-// Queries [q0+32c, q0+32c+32) go back, as bf16 pairs, over the dP^T chunk
-// they were read from: dS^T in columns [q0+32c, +16), P^T in [q0+32c+16, +16).
+// They go back, as bf16 pairs, over the dP^T chunk they were read from:
+// dS^T in columns [q0+32c, +16), P^T in [q0+32c+16, +16).
 // kCap: scores capped to c tanh(scale s / c); then x = c log2e tanh(..) - lse2
 // and dS also carries the factor 1 - tanh^2.
-template <bool kPartial, bool kCap>
-__device__ __forceinline__ void pds_half(const uint32_t (&s)[64], uint32_t tP, int q0,
-                                         const float* nl, const float* nd, float scale_log2,
-                                         const CapConsts& cap, uint32_t m_lo, uint32_t m_hi) {
+template <bool kPartial, bool kCap, int c>
+__device__ __forceinline__ void pds_chunk(const uint32_t (&s)[64], uint32_t tP, int q0,
+                                          const float* nl, const float* nd, float scale_log2,
+                                          const CapConsts& cap, uint32_t m_lo, uint32_t m_hi) {
   const float2 sc2 = make_float2(scale_log2, scale_log2);
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
+  {
     uint32_t dp[32];
     tmem_ld32(tP + q0 + 32 * c, dp);
     uint32_t pp[16], dd[16];
@@ -141,7 +140,7 @@ __device__ __forceinline__ void pds_half(const uint32_t (&s)[64], uint32_t tP, i
                               nlp);
         float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
         if (kPartial) {  // bits of this warpgroup's 64 columns: m_lo (0-31), m_hi (32-63)
-          const uint32_t mw = lc < 32 ? m_lo : m_hi;
+          const uint32_t mw = c == 0 ? m_lo : m_hi;
           p.x = ((mw >> (lc & 31)) & 1u) ? p.x : 0.f;
           p.y = ((mw >> ((lc + 1) & 31)) & 1u) ? p.y : 0.f;
         }
@@ -200,6 +199,7 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
     }
     mbar_init(bar(C::kBSFree), 256);
     mbar_init(bar(C::kBPFull), 256);
+    mbar_init(bar(C::kBPFull + 1), 256);
     mbar_init(bar(C::kBDkvFull), 1);
     mbar_init(bar(C::kBDkvEmpty), 256);
     mbar_init(bar(C::kBDrain), 1);
@@ -346,7 +346,6 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
             mma_commit(bar(C::kBSFull));
           }
           if (!(ok = mbar_wait(bar(C::kBPFull), p_cnt & 1, ctl, 505))) break;
-          ++p_cnt;
           tc_fence_after();
           if (i == 0) {
             if (!(ok = mbar_wait(bar(C::kBDkvEmpty), (dkv_cnt & 1) ^ 1, ctl, 506))) break;
@@ -356,14 +355,29 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
           const uint32_t acc0 = i > 0 ? 1u : 0u;
           const uint64_t dom = dDOm + ds * kTile16;
           const uint64_t qm = dQm + qs * kTile16;
+          // queries [16kk, 16kk+16) with kk = 4w + 2c + h: warpgroup w, chunk c,
+          // half h of the chunk's dS^T (and, 16 columns on, P^T) pairs.  Chunk 0
+          // of both warpgroups first (kk = 0 is issued first: it starts the sum).
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            // queries [16kk, 16kk+16): warpgroup kk/4, chunk (kk%4)/2, half kk%2 of
-            // the chunk's dS^T (and, 16 columns on, P^T) pairs
-            const uint32_t ta = tmem + C::kTdP + 64 * (kk >> 2) + 32 * ((kk & 3) >> 1) + 8 * (kk & 1);
-            mma_ts_at(tmem + C::kTdV, ta + 16, dom, kk * 128, kIdAcc, (acc0 || kk > 0) ? 1u : 0u);
-            mma_ts_at(tmem + C::kTdK, ta, qm, kk * 128, kIdAcc, (acc0 || kk > 0) ? 1u : 0u);
+          for (int c = 0; c < 2; ++c) {
+            if (c == 1) {
+              if (!(ok = mbar_wait(bar(C::kBPFull + 1), p_cnt & 1, ctl, 508))) break;
+              tc_fence_after();
+            }
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int kk = 4 * w + 2 * c + h;
+                const uint32_t ta = tmem + C::kTdP + 64 * w + 32 * c + 8 * h;
+                const uint32_t acc = (acc0 || kk > 0) ? 1u : 0u;
+                mma_ts_at(tmem + C::kTdV, ta + 16, dom, kk * 128, kIdAcc, acc);
+                mma_ts_at(tmem + C::kTdK, ta, qm, kk * 128, kIdAcc, acc);
+              }
+            }
           }
+          if (!ok) break;
+          ++p_cnt;
           mma_commit(bar(C::kBDOEmpty + ds));
           mma_commit(bar(C::kBQEmpty + qs));
         }
@@ -422,13 +436,22 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
         ++sdp_cnt;
         tc_fence_after();
         const uint32_t m_lo = wg ? vb[2] : vb[0], m_hi = wg ? vb[3] : vb[1];
+        // Each 32-query chunk is signalled on its own, so the dV / dK MMAs of
+        // the first chunk run while the second is computed.
         if (info & 1)
-          pds_half<true, kCap>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, m_hi);
+          pds_chunk<true, kCap, 0>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, m_hi);
         else
-          pds_half<false, kCap>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, m_hi);
+          pds_chunk<false, kCap, 0>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, m_hi);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(C::kBPFull));
+        if (info & 1)
+          pds_chunk<true, kCap, 1>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, m_hi);
+        else
+          pds_chunk<false, kCap, 1>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, m_hi);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::kBPFull + 1));
       }
       if (!ok) break;
       // ---- dK / dV epilogue: warpgroup wg writes columns [wg*D/2, (wg+1)*D/2)
