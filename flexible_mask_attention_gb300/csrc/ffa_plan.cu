@@ -484,21 +484,25 @@ __global__ void k_dq_counts(const int* __restrict__ items, int n_items,
 }
 
 // ---- ordering ---------------------------------------------------------------
-// One block: bitonic sort of (cost desc, index asc) keys in `scratch`
-// (n2 = next power of two >= n entries), then order[r] = index.  The
-// persistent kernels draw the items in this order from a work queue, so the
-// heavy items go first and the light ones even out the tail.  (Grouping the
-// items by kv head first, for L2 reuse of one head's tiles, measured slower
-// on GB300: balance matters more than locality at these sizes.)
-// Key bits: [24,50) 2^26-1-cost, [0,24) index.
+// One block: bitonic sort of keys in `scratch` (n2 = next power of two >= n
+// entries), then order[r] = index.  The persistent kernels draw the items in
+// this order from a work queue, so the heavy items go first and the light
+// ones even out the tail.  The order is by cost octave (descending), then kv
+// head, then cost (descending), then index: within an octave the CTAs
+// running at one time share few heads, so their K/V (or Q/dO) tiles stay in
+// L2.  (Pure kv-head order measured slower: balance comes first.)
+// Key bits: [58,64) 63-octave, [50,58) kv head, [24,50) 2^26-1-cost, [0,24) index.
 __global__ void k_sort_order(const int* __restrict__ items, int words, int cost_word, int n,
-                             int n2, unsigned long long* scratch, int* order) {
+                             int n2, unsigned long long* scratch, int* order, int head_word,
+                             int head_div) {
   for (int i = threadIdx.x; i < n2; i += blockDim.x) {
     unsigned long long key = ~0ull;
     if (i < n) {
       const int* it = items + (size_t)i * words;
-      const unsigned long long c = (unsigned int)it[cost_word];
-      key = ((0x3ffffffull - c) << 24) | (unsigned long long)i;
+      const unsigned long long c = (unsigned int)it[cost_word] & 0x3ffffffu;
+      const unsigned long long hk = (unsigned int)(max(it[head_word], 0) / head_div) & 0xffu;
+      const unsigned long long oct = 63u - min(63u, (unsigned int)(63 - __clzll((long long)c + 1)));
+      key = (oct << 58) | (hk << 50) | ((0x3ffffffull - c) << 24) | (unsigned long long)i;
     }
     scratch[i] = key;
   }
@@ -567,8 +571,9 @@ ffa_status_t scan(const int* in, int n, int* out, long long* dtot, long long* ht
   return FFA_OK;
 }
 
-ffa_status_t sort_items(const int* items, int words, int cost_word, int n, int* order,
-                        cudaStream_t st) {
+// head_word: the item word holding a head, head_div: divisor to its kv head.
+ffa_status_t sort_items(const int* items, int words, int cost_word, int head_word, int head_div,
+                        int n, int* order, cudaStream_t st) {
   if (n <= 0) return FFA_OK;
   if (n >= (1 << 24)) return FFA_ERR_UNSUPPORTED;
   int n2 = 1;
@@ -576,7 +581,7 @@ ffa_status_t sort_items(const int* items, int words, int cost_word, int n, int* 
   DevBuf scratch(st);
   FFA_CUDA(scratch.alloc(sizeof(unsigned long long) * (size_t)n2));
   k_sort_order<<<1, 1024, 0, st>>>(items, words, cost_word, n, n2,
-                                   scratch.as<unsigned long long>(), order);
+                                   scratch.as<unsigned long long>(), order, head_word, head_div);
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
   FFA_CUDA(cudaStreamSynchronize(st));
@@ -777,8 +782,8 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   }
   p->n_fwd_items = final_items;
   FFA_CUDA(cudaMalloc(&p->fwd_order, sizeof(int) * (size_t)std::max(1LL, final_items)));
-  rc = sort_items(items.as<int>(), kFiWords, kFiCost, (int)final_items, p->fwd_order,
-                  st);
+  rc = sort_items(items.as<int>(), kFiWords, kFiCost, kFiH0, p->Hq / p->Hkv, (int)final_items,
+                  p->fwd_order, st);
   if (rc != FFA_OK) return rc;
   p->fwd_items = items.as<int>();
   items.release();
@@ -790,7 +795,8 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
     p->n_dq_items = p->n_fwd_items;
   } else {
     FFA_CUDA(cudaMalloc(&p->dq_order, sizeof(int) * (size_t)std::max<int64_t>(1, p->n_dq_items)));
-    rc = sort_items(p->dq_items, kFiWords, kFiCost, (int)p->n_dq_items, p->dq_order, st);
+    rc = sort_items(p->dq_items, kFiWords, kFiCost, kFiH0, p->Hq / p->Hkv, (int)p->n_dq_items,
+                    p->dq_order, st);
     if (rc != FFA_OK) return rc;
   }
   p->grid_dq = (int)std::max<int64_t>(1, std::min<int64_t>(p->num_sms, p->n_dq_items));
@@ -836,7 +842,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
                                                        p->bwd_steps, p->bwd_items);
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
-  rc = sort_items(p->bwd_items, kBiWords, kBiCost, (int)nb_items, p->bwd_order, st);
+  rc = sort_items(p->bwd_items, kBiWords, kBiCost, kBiHkv, 1, (int)nb_items, p->bwd_order, st);
   if (rc != FFA_OK) return rc;
   p->grid_fwd = (int)std::max(1LL, std::min<long long>(p->num_sms, final_items));
   p->grid_bwd = (int)std::max(1LL, std::min<long long>(p->num_sms, nb_items));

@@ -18,7 +18,8 @@ the work-list specification of the planner:
   * split (when 0 < items with work < threshold): min(16, ceil(threshold /
     live)) chunks per item, capped by its step count, step ranges
     b + k*n//c .. b + (k+1)*n//c, cost scaled by the chunk's share;
-  * order: cost descending, then item index;
+  * order: cost octave floor(log2(cost + 1)) descending, then kv head, then
+    cost descending, then item index;
   * backward: per k-tile one visit per q-tile seen, merged the same way, one
     item per (kt, kv head), cost g * sum of visit costs.
 """
@@ -193,11 +194,12 @@ def plan(total_q, total_k, num_heads_q, num_heads_kv, q_ranges, k_ranges, mask_t
             n_slots += c
         items = new
 
-    def order_of(costs):
-        return np.array(sorted(range(len(costs)), key=lambda i: (-costs[i], i)), dtype=np.int32)
+    def order_of(costs, heads):
+        key = lambda i: (-int(costs[i] + 1).bit_length(), heads[i], -costs[i], i)
+        return np.array(sorted(range(len(costs)), key=key), dtype=np.int32)
 
     fwd_items = np.array(items, dtype=np.int32).reshape(-1, 8)
-    fwd_order = order_of([it[7] for it in items])
+    fwd_order = order_of([it[7] for it in items], [max(it[2], 0) // g for it in items])
 
     bsteps, bitems = [], []
     boff = []
@@ -215,7 +217,7 @@ def plan(total_q, total_k, num_heads_q, num_heads_kv, q_ranges, k_ranges, mask_t
         "fwd_order": fwd_order,
         "bwd_steps": np.array(bsteps, dtype=np.int32).reshape(-1, 4),
         "bwd_items": bwd_items,
-        "bwd_order": order_of([it[4] for it in bitems]),
+        "bwd_order": order_of([it[4] for it in bitems], [it[1] for it in bitems]),
         "merges": np.array(merges, dtype=np.int32).reshape(-1, 8),
         "fwd_masks": np.array(fmasks, dtype=np.int32).reshape(-1, 1),
         "bwd_masks": np.array(bmasks, dtype=np.int32).reshape(-1, 1),
