@@ -559,6 +559,58 @@ inline int grid_for(long long n, int block) { return (int)std::max(1LL, (n + blo
     }                                                    \
   } while (0)
 
+// ---- small device -> host reads ----------------------------------------------
+// The planner reads a few counts back to size its lists.  A copy-engine read
+// (cudaMemcpyAsync) would queue behind any large transfer the caller has in
+// flight on another stream (e.g. the previous call's results going to the
+// host) and wait for all of it; instead a one-block kernel writes the words
+// into mapped pinned host memory, one small buffer per host thread, allocated
+// on first use and kept for the thread's life.
+__global__ void k_to_host(const unsigned int* __restrict__ src, int words,
+                          volatile unsigned int* dst) {
+  for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
+}
+
+constexpr int kMailboxWords = 64;
+
+unsigned int* host_mailbox(unsigned int** dev_view) {
+  thread_local unsigned int* box = nullptr;
+  thread_local unsigned int* dbox = nullptr;
+  if (!box) {
+    unsigned int* b = nullptr;
+    if (cudaHostAlloc(&b, kMailboxWords * sizeof(unsigned int), cudaHostAllocMapped) != cudaSuccess)
+      return nullptr;
+    unsigned int* d = nullptr;
+    if (cudaHostGetDevicePointer(&d, b, 0) != cudaSuccess) {
+      cudaFreeHost(b);
+      return nullptr;
+    }
+    box = b;
+    dbox = d;
+  }
+  *dev_view = dbox;
+  return box;
+}
+
+// Copies `bytes` (a multiple of 4, at most 256) from device memory to `dst`
+// and waits for the stream; falls back to a copy-engine read when no mapped
+// buffer could be had.
+ffa_status_t read_to_host(void* dst, const void* src, size_t bytes, cudaStream_t st) {
+  unsigned int* dview = nullptr;
+  unsigned int* box = bytes % 4 == 0 && bytes <= kMailboxWords * 4 ? host_mailbox(&dview) : nullptr;
+  if (!box) {
+    FFA_CUDA(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, st));
+    FFA_CUDA(cudaStreamSynchronize(st));
+    return FFA_OK;
+  }
+  k_to_host<<<1, 64, 0, st>>>(static_cast<const unsigned int*>(src), (int)(bytes / 4), dview);
+  note_launches(1);
+  FFA_CUDA(cudaGetLastError());
+  FFA_CUDA(cudaStreamSynchronize(st));
+  memcpy(dst, box, bytes);
+  return FFA_OK;
+}
+
 ffa_status_t scan(const int* in, int n, int* out, long long* dtot, long long* htot,
                   cudaStream_t st) {
   if (n > 0) {
@@ -566,9 +618,7 @@ ffa_status_t scan(const int* in, int n, int* out, long long* dtot, long long* ht
     note_launches(1);
   } else FFA_CUDA(cudaMemsetAsync(dtot, 0, sizeof(long long), st));
   FFA_CUDA(cudaGetLastError());
-  FFA_CUDA(cudaMemcpyAsync(htot, dtot, sizeof(long long), cudaMemcpyDeviceToHost, st));
-  FFA_CUDA(cudaStreamSynchronize(st));
-  return FFA_OK;
+  return read_to_host(htot, dtot, sizeof(long long), st);
 }
 
 // head_word: the item word holding a head, head_div: divisor to its kv head.
@@ -602,12 +652,16 @@ void free_plan(ffa_plan_s* p) {
   delete p;
 }
 
+// The plan's lists are stream-ordered allocations on the planning stream (a
+// plain cudaMalloc may stop work on other streams from overlapping, e.g. a
+// caller's copies of the previous call's results); the planner synchronizes
+// that stream before it returns, so they are ready for any stream after.
 ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, const int32_t* ty,
                         int split_below, cudaStream_t st) {
   const int S = p->S;
-  FFA_CUDA(cudaMalloc(&p->slices, sizeof(Slice) * (size_t)std::max(S, 1)));
-  FFA_CUDA(cudaMalloc(&p->err, 2 * sizeof(int)));
-  FFA_CUDA(cudaMalloc(&p->tickets, 4 * sizeof(int)));
+  FFA_CUDA(cudaMallocAsync(&p->slices, sizeof(Slice) * (size_t)std::max(S, 1), st));
+  FFA_CUDA(cudaMallocAsync(&p->err, 2 * sizeof(int), st));
+  FFA_CUDA(cudaMallocAsync(&p->tickets, 4 * sizeof(int), st));
   FFA_CUDA(cudaMemsetAsync(p->err, 0, 2 * sizeof(int), st));
   DevBuf flags_area(st);
   FFA_CUDA(flags_area.alloc(64));
@@ -667,9 +721,10 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   }
   int hflags[4];
   unsigned long long harea = 0;
-  FFA_CUDA(cudaMemcpyAsync(hflags, flags, sizeof hflags, cudaMemcpyDeviceToHost, st));
-  FFA_CUDA(cudaMemcpyAsync(&harea, area, sizeof harea, cudaMemcpyDeviceToHost, st));
-  FFA_CUDA(cudaStreamSynchronize(st));
+  ffa_status_t rc_read = read_to_host(hflags, flags, sizeof hflags, st);
+  if (rc_read != FFA_OK) return rc_read;
+  rc_read = read_to_host(&harea, area, sizeof harea, st);
+  if (rc_read != FFA_OK) return rc_read;
   if (hflags[0]) return FFA_ERR_RANGE;
   if (hflags[1]) return FFA_ERR_OVERLAP;
   p->area = (int64_t)harea;
@@ -693,7 +748,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   if ((rc = scan(fmcnt.as<int>(), n_qt, fmoff.as<int>(), dtot, &mtot, st))) return rc;
   if (mtot > (1LL << 29)) return FFA_ERR_UNSUPPORTED;
   p->n_fwd_masks = mtot;
-  FFA_CUDA(cudaMalloc(&p->fwd_masks, sizeof(int) * (size_t)std::max(1LL, mtot)));
+  FFA_CUDA(cudaMallocAsync(&p->fwd_masks, sizeof(int) * (size_t)std::max(1LL, mtot), st));
   k_visit_warp<true, false><<<grid_for(n_qt, kFillWarps), 32 * kFillWarps, 0, st>>>(
       p->slices, qlist.as<int>(), qloff.as<int>(), qlcnt.as<int>(), n_qt, nullptr, nullptr,
       voff.as<int>(), fmoff.as<int>(), visits.as<int2>(), p->fwd_masks);
@@ -738,8 +793,10 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
   int hlive = 0;
-  FFA_CUDA(cudaMemcpyAsync(&hlive, live.p, sizeof(int), cudaMemcpyDeviceToHost, st));
-  FFA_CUDA(cudaStreamSynchronize(st));
+  {
+    const ffa_status_t rc_live = read_to_host(&hlive, live.p, sizeof(int), st);
+    if (rc_live != FFA_OK) return rc_live;
+  }
   const int threshold = split_below == 0 ? 2 * p->num_sms : split_below;
   long long final_items = n_items;
   if (split_below >= 0 && hlive > 0 && hlive < threshold) {
@@ -781,7 +838,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
     p->merges = static_cast<int*>(merges.release());
   }
   p->n_fwd_items = final_items;
-  FFA_CUDA(cudaMalloc(&p->fwd_order, sizeof(int) * (size_t)std::max(1LL, final_items)));
+  FFA_CUDA(cudaMallocAsync(&p->fwd_order, sizeof(int) * (size_t)std::max(1LL, final_items), st));
   rc = sort_items(items.as<int>(), kFiWords, kFiCost, kFiH0, p->Hq / p->Hkv, (int)final_items,
                   p->fwd_order, st);
   if (rc != FFA_OK) return rc;
@@ -794,13 +851,13 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
     p->dq_order = p->fwd_order;
     p->n_dq_items = p->n_fwd_items;
   } else {
-    FFA_CUDA(cudaMalloc(&p->dq_order, sizeof(int) * (size_t)std::max<int64_t>(1, p->n_dq_items)));
+    FFA_CUDA(cudaMallocAsync(&p->dq_order, sizeof(int) * (size_t)std::max<int64_t>(1, p->n_dq_items), st));
     rc = sort_items(p->dq_items, kFiWords, kFiCost, kFiH0, p->Hq / p->Hkv, (int)p->n_dq_items,
                     p->dq_order, st);
     if (rc != FFA_OK) return rc;
   }
   p->grid_dq = (int)std::max<int64_t>(1, std::min<int64_t>(p->num_sms, p->n_dq_items));
-  FFA_CUDA(cudaMalloc(&p->dq_counts, sizeof(int) * 2 * (size_t)std::max<int64_t>(1, p->n_dq_items)));
+  FFA_CUDA(cudaMallocAsync(&p->dq_counts, sizeof(int) * 2 * (size_t)std::max<int64_t>(1, p->n_dq_items), st));
   if (p->n_dq_items > 0) {
     k_dq_counts<<<grid_for(p->n_dq_items, 128), 128, 0, st>>>(p->dq_items, (int)p->n_dq_items,
                                                              p->fwd_steps, p->dq_counts);
@@ -823,20 +880,20 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   if (tot > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
   p->n_bwd_steps = tot;
   FFA_CUDA(bvis.alloc(sizeof(int2) * (size_t)tot));
-  FFA_CUDA(cudaMalloc(&p->bwd_steps, sizeof(int4) * (size_t)std::max(1LL, tot)));
+  FFA_CUDA(cudaMallocAsync(&p->bwd_steps, sizeof(int4) * (size_t)std::max(1LL, tot), st));
   long long bmtot = 0;
   if ((rc = scan(bmcnt.as<int>(), n_kt, bmoff.as<int>(), dtot, &bmtot, st))) return rc;
   if (bmtot > (1LL << 29)) return FFA_ERR_UNSUPPORTED;
   p->n_bwd_masks = bmtot;
-  FFA_CUDA(cudaMalloc(&p->bwd_masks, sizeof(int) * (size_t)std::max(1LL, bmtot)));
+  FFA_CUDA(cudaMallocAsync(&p->bwd_masks, sizeof(int) * (size_t)std::max(1LL, bmtot), st));
   k_visit_warp<false, false><<<grid_for(n_kt, kFillWarps), 32 * kFillWarps, 0, st>>>(
       p->slices, klist.as<int>(), kloff.as<int>(), klcnt.as<int>(), n_kt, nullptr, nullptr,
       boff.as<int>(), bmoff.as<int>(), bvis.as<int2>(), p->bwd_masks);
   note_launches(1);
   const long long nb_items = (long long)n_kt * p->Hkv;
   p->n_bwd_items = nb_items;
-  FFA_CUDA(cudaMalloc(&p->bwd_items, sizeof(int) * kBiWords * (size_t)std::max(1LL, nb_items)));
-  FFA_CUDA(cudaMalloc(&p->bwd_order, sizeof(int) * (size_t)std::max(1LL, nb_items)));
+  FFA_CUDA(cudaMallocAsync(&p->bwd_items, sizeof(int) * kBiWords * (size_t)std::max(1LL, nb_items), st));
+  FFA_CUDA(cudaMallocAsync(&p->bwd_order, sizeof(int) * (size_t)std::max(1LL, nb_items), st));
   k_bwd_items<<<grid_for(nb_items, 128), 128, 0, st>>>(n_kt, p->Hkv, g, bvis.as<int2>(),
                                                        boff.as<int>(), bcnt.as<int>(),
                                                        p->bwd_steps, p->bwd_items);
