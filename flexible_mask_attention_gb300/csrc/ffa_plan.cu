@@ -492,9 +492,16 @@ __global__ void k_dq_counts(const int* __restrict__ items, int n_items,
 // running at one time share few heads, so their K/V (or Q/dO) tiles stay in
 // L2.  (Pure kv-head order measured slower: balance comes first.)
 // Key bits: [58,64) 63-octave, [50,58) kv head, [24,50) 2^26-1-cost, [0,24) index.
+// The keys live in shared memory when they fit (kSortSmemKeys), else in the
+// global `scratch`: the network's ~log2(n2)^2/2 passes then cost shared- rather
+// than L2-memory latency each.
+constexpr int kSortSmemKeys = 16384;
+
 __global__ void k_sort_order(const int* __restrict__ items, int words, int cost_word, int n,
                              int n2, unsigned long long* scratch, int* order, int head_word,
                              int head_div) {
+  extern __shared__ unsigned long long sort_keys[];
+  unsigned long long* keys = n2 <= kSortSmemKeys ? sort_keys : scratch;
   for (int i = threadIdx.x; i < n2; i += blockDim.x) {
     unsigned long long key = ~0ull;
     if (i < n) {
@@ -504,7 +511,7 @@ __global__ void k_sort_order(const int* __restrict__ items, int words, int cost_
       const unsigned long long oct = 63u - min(63u, (unsigned int)(63 - __clzll((long long)c + 1)));
       key = (oct << 58) | (hk << 50) | ((0x3ffffffull - c) << 24) | (unsigned long long)i;
     }
-    scratch[i] = key;
+    keys[i] = key;
   }
   __syncthreads();
   for (int k = 2; k <= n2; k <<= 1) {
@@ -512,18 +519,18 @@ __global__ void k_sort_order(const int* __restrict__ items, int words, int cost_
       for (int i = threadIdx.x; i < n2; i += blockDim.x) {
         const int l = i ^ j;
         if (l > i) {
-          const unsigned long long a = scratch[i], b = scratch[l];
+          const unsigned long long a = keys[i], b = keys[l];
           const bool up = (i & k) == 0;
           if ((a > b) == up) {
-            scratch[i] = b;
-            scratch[l] = a;
+            keys[i] = b;
+            keys[l] = a;
           }
         }
       }
       __syncthreads();
     }
   }
-  for (int i = threadIdx.x; i < n; i += blockDim.x) order[i] = (int)(scratch[i] & 0xffffffu);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) order[i] = (int)(keys[i] & 0xffffffu);
 }
 
 // ---- host helpers -----------------------------------------------------------
@@ -611,13 +618,21 @@ ffa_status_t read_to_host(void* dst, const void* src, size_t bytes, cudaStream_t
   return FFA_OK;
 }
 
-ffa_status_t scan(const int* in, int n, int* out, long long* dtot, long long* htot,
-                  cudaStream_t st) {
+// Exclusive scan of in[0, n) into out, total into *dtot (device), no read back:
+// independent scans are launched back to back and their totals read at once.
+ffa_status_t scan_launch(const int* in, int n, int* out, long long* dtot, cudaStream_t st) {
   if (n > 0) {
     k_scan<<<1, 1024, 0, st>>>(in, n, out, dtot);
     note_launches(1);
   } else FFA_CUDA(cudaMemsetAsync(dtot, 0, sizeof(long long), st));
   FFA_CUDA(cudaGetLastError());
+  return FFA_OK;
+}
+
+ffa_status_t scan(const int* in, int n, int* out, long long* dtot, long long* htot,
+                  cudaStream_t st) {
+  const ffa_status_t rc = scan_launch(in, n, out, dtot, st);
+  if (rc != FFA_OK) return rc;
   return read_to_host(htot, dtot, sizeof(long long), st);
 }
 
@@ -629,13 +644,15 @@ ffa_status_t sort_items(const int* items, int words, int cost_word, int head_wor
   int n2 = 1;
   while (n2 < n) n2 <<= 1;
   DevBuf scratch(st);
-  FFA_CUDA(scratch.alloc(sizeof(unsigned long long) * (size_t)n2));
-  k_sort_order<<<1, 1024, 0, st>>>(items, words, cost_word, n, n2,
-                                   scratch.as<unsigned long long>(), order, head_word, head_div);
+  if (n2 > kSortSmemKeys) FFA_CUDA(scratch.alloc(sizeof(unsigned long long) * (size_t)n2));
+  const size_t smem = n2 <= kSortSmemKeys ? sizeof(unsigned long long) * (size_t)n2 : 0;
+  FFA_CUDA(cudaFuncSetAttribute(k_sort_order, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)(sizeof(unsigned long long) * kSortSmemKeys)));
+  k_sort_order<<<1, 1024, smem, st>>>(items, words, cost_word, n, n2,
+                                      scratch.as<unsigned long long>(), order, head_word, head_div);
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
-  FFA_CUDA(cudaStreamSynchronize(st));
-  return FFA_OK;
+  return FFA_OK;  // consumed by later work on `st`; the planner synchronizes before returning
 }
 
 void free_plan(ffa_plan_s* p) {
@@ -692,8 +709,18 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
     note_launches(1);
     FFA_CUDA(cudaGetLastError());
   }
-  if ((rc = scan(qlcnt.as<int>(), n_qt, qloff.as<int>(), dtot, &tot, st))) return rc;
-  if (tot > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
+  if (n_kt > 0) {
+    k_tile_slices<false><<<n_kt, kListThreads, 0, st>>>(p->slices, S, nullptr, klcnt.as<int>(),
+                                                        nullptr);
+    note_launches(1);
+    FFA_CUDA(cudaGetLastError());
+  }
+  long long lt[2];  // list lengths: q-tile lists, k-tile lists
+  if ((rc = scan_launch(qlcnt.as<int>(), n_qt, qloff.as<int>(), dtot, st))) return rc;
+  if ((rc = scan_launch(klcnt.as<int>(), n_kt, kloff.as<int>(), dtot + 1, st))) return rc;
+  if ((rc = read_to_host(lt, dtot, sizeof lt, st))) return rc;
+  tot = lt[0];
+  if (tot > 0x7fffffffLL || lt[1] > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
   FFA_CUDA(qlist.alloc(sizeof(int) * (size_t)tot));
   if (n_qt > 0) {
     k_tile_slices<true><<<n_qt, kListThreads, 0, st>>>(p->slices, S, qloff.as<int>(), nullptr,
@@ -704,14 +731,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
     note_launches(1);
     FFA_CUDA(cudaGetLastError());
   }
-  if (n_kt > 0) {
-    k_tile_slices<false><<<n_kt, kListThreads, 0, st>>>(p->slices, S, nullptr, klcnt.as<int>(),
-                                                        nullptr);
-    note_launches(1);
-    FFA_CUDA(cudaGetLastError());
-  }
-  if ((rc = scan(klcnt.as<int>(), n_kt, kloff.as<int>(), dtot, &tot, st))) return rc;
-  if (tot > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
+  tot = lt[1];
   FFA_CUDA(klist.alloc(sizeof(int) * (size_t)tot));
   if (n_kt > 0) {
     k_tile_slices<false><<<n_kt, kListThreads, 0, st>>>(p->slices, S, kloff.as<int>(), nullptr,
@@ -719,14 +739,12 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
     note_launches(1);
     FFA_CUDA(cudaGetLastError());
   }
-  int hflags[4];
+  int hfa[6];  // flags[4], then the area (64-bit) right after them
+  if ((rc = read_to_host(hfa, flags, sizeof hfa, st))) return rc;
+  if (hfa[0]) return FFA_ERR_RANGE;
+  if (hfa[1]) return FFA_ERR_OVERLAP;
   unsigned long long harea = 0;
-  ffa_status_t rc_read = read_to_host(hflags, flags, sizeof hflags, st);
-  if (rc_read != FFA_OK) return rc_read;
-  rc_read = read_to_host(&harea, area, sizeof harea, st);
-  if (rc_read != FFA_OK) return rc_read;
-  if (hflags[0]) return FFA_ERR_RANGE;
-  if (hflags[1]) return FFA_ERR_OVERLAP;
+  memcpy(&harea, hfa + 4, sizeof harea);
   p->area = (int64_t)harea;
 
   // forward visits
@@ -740,12 +758,14 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
       fmcnt.as<int>(), nullptr, nullptr, nullptr, nullptr);
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
-  rc = scan(vcnt.as<int>(), n_qt, voff.as<int>(), dtot, &tot, st);
-  if (rc != FFA_OK) return rc;
+  long long vm[2];  // visits, slice-list words
+  if ((rc = scan_launch(vcnt.as<int>(), n_qt, voff.as<int>(), dtot, st))) return rc;
+  if ((rc = scan_launch(fmcnt.as<int>(), n_qt, fmoff.as<int>(), dtot + 1, st))) return rc;
+  if ((rc = read_to_host(vm, dtot, sizeof vm, st))) return rc;
+  tot = vm[0];
   if (tot > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
   FFA_CUDA(visits.alloc(sizeof(int2) * (size_t)tot));
-  long long mtot = 0;
-  if ((rc = scan(fmcnt.as<int>(), n_qt, fmoff.as<int>(), dtot, &mtot, st))) return rc;
+  const long long mtot = vm[1];
   if (mtot > (1LL << 29)) return FFA_ERR_UNSUPPORTED;
   p->n_fwd_masks = mtot;
   FFA_CUDA(cudaMallocAsync(&p->fwd_masks, sizeof(int) * (size_t)std::max(1LL, mtot), st));
@@ -876,13 +896,16 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
       bmcnt.as<int>(), nullptr, nullptr, nullptr, nullptr);
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
-  if ((rc = scan(bcnt.as<int>(), n_kt, boff.as<int>(), dtot, &tot, st))) return rc;
+  long long bm[2];  // visits, slice-list words
+  if ((rc = scan_launch(bcnt.as<int>(), n_kt, boff.as<int>(), dtot, st))) return rc;
+  if ((rc = scan_launch(bmcnt.as<int>(), n_kt, bmoff.as<int>(), dtot + 1, st))) return rc;
+  if ((rc = read_to_host(bm, dtot, sizeof bm, st))) return rc;
+  tot = bm[0];
   if (tot > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
   p->n_bwd_steps = tot;
   FFA_CUDA(bvis.alloc(sizeof(int2) * (size_t)tot));
   FFA_CUDA(cudaMallocAsync(&p->bwd_steps, sizeof(int4) * (size_t)std::max(1LL, tot), st));
-  long long bmtot = 0;
-  if ((rc = scan(bmcnt.as<int>(), n_kt, bmoff.as<int>(), dtot, &bmtot, st))) return rc;
+  const long long bmtot = bm[1];
   if (bmtot > (1LL << 29)) return FFA_ERR_UNSUPPORTED;
   p->n_bwd_masks = bmtot;
   FFA_CUDA(cudaMallocAsync(&p->bwd_masks, sizeof(int) * (size_t)std::max(1LL, bmtot), st));
