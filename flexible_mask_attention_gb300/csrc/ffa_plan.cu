@@ -572,7 +572,8 @@ inline int grid_for(long long n, int block) { return (int)std::max(1LL, (n + blo
 // flight on another stream (e.g. the previous call's results going to the
 // host) and wait for all of it; instead a one-block kernel writes the words
 // into mapped pinned host memory, one small buffer per host thread, allocated
-// on first use and kept for the thread's life.
+// on first use and kept for the thread's life (unified addressing gives it
+// the same address on every device).
 __global__ void k_to_host(const unsigned int* __restrict__ src, int words,
                           volatile unsigned int* dst) {
   for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
@@ -585,7 +586,9 @@ unsigned int* host_mailbox(unsigned int** dev_view) {
   thread_local unsigned int* dbox = nullptr;
   if (!box) {
     unsigned int* b = nullptr;
-    if (cudaHostAlloc(&b, kMailboxWords * sizeof(unsigned int), cudaHostAllocMapped) != cudaSuccess)
+    // portable: a host thread may plan on several devices
+    if (cudaHostAlloc(&b, kMailboxWords * sizeof(unsigned int),
+                      cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess)
       return nullptr;
     unsigned int* d = nullptr;
     if (cudaHostGetDevicePointer(&d, b, 0) != cudaSuccess) {
