@@ -1115,12 +1115,14 @@ ffa_status_t launch_bwd(ffa_plan_s* p, const void* q, const void* k, const void*
 // Allocation-free backward.
 //
 // Some callers cannot allocate device memory at the point where they run the
-// backward: code running while a stream is being captured into a graph,
-// runtimes that forbid allocation after start-up, or hosts whose memory
-// manager owns every allocation.  ffa_bwd_noalloc serves them: its scratch
-// (log2-scaled lse and delta) lives in the array
-// below, which every GPU that loads this library holds until the process
-// exits.  All calls share it, so calls whose kernels overlap on the GPU race.
+// backward: runtimes that forbid allocation once they have started, hosts
+// whose own memory manager owns every byte of the GPU, or latency-critical
+// loops that must not pay for (or synchronise on) an allocation.
+// ffa_bwd_noalloc serves them: its scratch (log2-scaled lse and delta) lives
+// in the array below, which every GPU that loads this library holds until the
+// process exits.  All calls share it, so calls whose kernels overlap on the
+// GPU race.  The first call on a device resolves the array's address for
+// that device; make that first call before any stream capture.
 namespace ffa {
 namespace {
 
@@ -1163,6 +1165,9 @@ extern "C" ffa_status_t ffa_bwd_noalloc(ffa_plan_t p, const void* q, const void*
   using namespace ffa;
   if (!p || !q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv)
     return FFA_ERR_INVALID_ARG;
+  // The scratch address below is resolved for the current device, and the
+  // plan's lists live on the plan's device: both must be the same GPU.
+  if (!on_plan_device(p)) return FFA_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, out, dout, lse, dq, dk, dv};
   for (const void* x : ptrs)
     if (!aligned16_b(x)) return FFA_ERR_INVALID_ARG;

@@ -179,6 +179,7 @@ struct CapConsts {
 };
 size_t bwd_workspace_bytes(const ffa_plan_s* p);
 // Implemented in ffa_plan.cu.
+bool on_plan_device(const ffa_plan_s* p);  // current device == the plan's device
 bool encode_tile_map(void* map128, const void* base, int rows, int cols_elems);
 void note_launches(int n);  // adds to the count reported by ffa_kernel_launch_count
 // Records phase event i of the plan on `st` when the caller asked for them.

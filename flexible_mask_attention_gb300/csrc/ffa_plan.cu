@@ -12,7 +12,8 @@
 //       - otherwise: q-tiles 2u and 2u+1 of one head; the steps merge the two
 //         visit lists on kt (equal kt -> one shared step, in list order).
 //   * Item cost = sum over its steps and busy halves of 4 (FULL) or 5
-//     (PARTIAL).  Items are sorted by (cost descending, index); the
+//     (PARTIAL).  Items are sorted by cost octave floor(log2(cost + 1))
+//     (descending), then kv head, then cost (descending), then index; the
 //     persistent kernels draw them in that order from a work queue.
 //   * While fewer than `split_below` items have work, each such item is cut
 //     into equal runs of steps whose partial results are merged by
@@ -960,6 +961,13 @@ std::atomic<uint64_t> g_launches{0};
 
 }  // namespace
 
+// True when the calling thread's current device is the one the plan was
+// built on (its lists, tickets and error word live there).
+bool on_plan_device(const ffa_plan_s* p) {
+  int dev = -1;
+  return cudaGetDevice(&dev) == cudaSuccess && dev == p->device;
+}
+
 void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 uint64_t g_launches_total() { return g_launches.load(std::memory_order_relaxed); }
 
@@ -1027,8 +1035,14 @@ ffa_status_t ffa_plan_create(ffa_plan_t* plan, const int32_t* q_ranges, const in
 
 ffa_status_t ffa_plan_destroy(ffa_plan_t plan) {
   if (!plan) return FFA_ERR_INVALID_ARG;
+  // Work using the plan runs on the plan's device: wait for that device, free
+  // there, and give the caller back its own current device.
+  int cur = -1;
+  const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+  const bool switched = have_cur && cur != plan->device && cudaSetDevice(plan->device) == cudaSuccess;
   cudaDeviceSynchronize();
   free_plan(plan);
+  if (switched) cudaSetDevice(cur);
   return FFA_OK;
 }
 
@@ -1050,6 +1064,7 @@ ffa_status_t ffa_plan_info(ffa_plan_t p, ffa_plan_info_t* info) {
 ffa_status_t ffa_plan_export(ffa_plan_t p, int32_t which, int32_t* dst, int64_t capacity,
                              int64_t* written) {
   if (!p || !written || (capacity > 0 && !dst)) return FFA_ERR_INVALID_ARG;
+  if (!on_plan_device(p)) return FFA_ERR_INVALID_ARG;
   const void* src = nullptr;
   int64_t words = 0;
   switch (which) {
@@ -1080,6 +1095,7 @@ ffa_status_t ffa_fwd_ex(ffa_plan_t p, const void* q, const void* k, const void* 
                         float softmax_scale, float softcap, void* out, float* lse,
                         void* workspace, size_t workspace_bytes, ffa_stream_t stream) {
   if (!p || !q || !k || !v || !out || !lse) return FFA_ERR_INVALID_ARG;
+  if (!on_plan_device(p)) return FFA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
     return FFA_ERR_INVALID_ARG;
   if (!sink_args_ok(sink, num_sink, sink_layout)) return FFA_ERR_INVALID_ARG;
@@ -1110,6 +1126,7 @@ ffa_status_t ffa_bwd_ex(ffa_plan_t p, const void* q, const void* k, const void* 
                         ffa_stream_t stream) {
   if (!p || !q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv)
     return FFA_ERR_INVALID_ARG;
+  if (!on_plan_device(p)) return FFA_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, out, dout, lse, dq, dk, dv};
   for (const void* x : ptrs)
     if (!aligned16(x)) return FFA_ERR_INVALID_ARG;
@@ -1138,6 +1155,7 @@ ffa_status_t ffa_bwd(ffa_plan_t p, const void* q, const void* k, const void* v, 
 ffa_status_t ffa_get_last_device_error(ffa_plan_t p, int32_t* code, int32_t* where,
                                        ffa_stream_t stream) {
   if (!p || !code || !where) return FFA_ERR_INVALID_ARG;
+  if (!on_plan_device(p)) return FFA_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int h[2] = {0, 0};
   if (cudaMemcpyAsync(h, p->err, sizeof h, cudaMemcpyDeviceToHost, st) != cudaSuccess ||

@@ -31,6 +31,10 @@
  *     ffa_plan_create, which synchronises `stream` while it sizes the plan.
  *   - ffa_fwd / ffa_bwd never allocate: scratch memory is the caller's
  *     `workspace` of at least the size the *_workspace_size call reports.
+ *   - Every call that takes a plan must run with the plan's device current
+ *     (the one current at ffa_plan_create); otherwise it returns
+ *     FFA_ERR_INVALID_ARG before touching the GPU (ffa_plan_destroy switches
+ *     to the plan's device itself).
  *   - Errors come back as an ffa_status_t; nothing aborts the process.
  *     Device-side failures (a bounded wait that ran out) are reported by
  *     ffa_get_last_device_error.
@@ -85,7 +89,8 @@ ffa_status_t ffa_plan_create(ffa_plan_t* plan, const int32_t* q_ranges, const in
                              int32_t head_dim, int32_t num_sms, int32_t split_below,
                              ffa_stream_t stream);
 
-/* Free a plan and its device memory (synchronises the device first). */
+/* Free a plan and its device memory (synchronises the plan's device first;
+ * the caller's current device is unchanged afterwards). */
 ffa_status_t ffa_plan_destroy(ffa_plan_t plan);
 
 /* Sizes of the plan's work lists, in int32 words; see ffa_plan_export. */
@@ -185,15 +190,16 @@ ffa_status_t ffa_bwd_ex(ffa_plan_t plan, const void* q, const void* k, const voi
 /* Backward without any allocation: the same computation as ffa_bwd, with its
  * scratch memory taken from a fixed array inside the library instead of a
  * caller workspace.  (No counterpart in the MagiAttention pages.)  For callers
- * that cannot allocate device memory when they run the backward: code running
- * during stream capture into a CUDA graph, runtimes that forbid allocation
- * after start-up, or hosts whose memory manager owns every allocation.
+ * that cannot allocate device memory when they run the backward: runtimes
+ * that forbid allocation once they have started, hosts whose own memory
+ * manager owns every byte of the GPU, or latency-critical loops that must not
+ * pay for (or synchronise on) an allocation.
  *   - The array holds ffa_bwd_noalloc_max_workspace() bytes (64 MiB) on every
  *     GPU that loads this library, until the process exits.  A plan whose
  *     ffa_bwd_workspace_size exceeds it gets FFA_ERR_WORKSPACE.
  *   - The first call on a device resolves the array's device address (with
  *     that device current); make that first call before any stream capture.
- *   - Every call shares the array and re-initialises what must start at zero;
+ *   - Every call shares the array and rewrites all of the scratch it reads;
  *     calls whose kernels overlap on the GPU (other streams) race.
  *   - Arguments as for ffa_bwd; nothing is allocated or freed. */
 ffa_status_t ffa_bwd_noalloc(ffa_plan_t plan, const void* q, const void* k, const void* v,
