@@ -105,9 +105,11 @@ def heterogeneous_prefix_docs(total: int = 65536, h: int = 16, d: int = 128,
     ``default_rng(seed)``: ``n_docs - 1`` distinct cut points drawn with
     ``choice(arange(prefix + 256, total - 256), n_docs - 1, replace=False)``,
     redrawn until every document has at least ``min_doc`` tokens.  The
-    documents' self-slice types are then ``permutation`` of
-    {full x6, causal x6, inverse-causal x6, bi-causal x5} from the same
-    generator.  Slices: the prefix's own full block, one self-slice per
+    documents' self-slice types are then ``permutation`` of a multiset that
+    splits ``n_docs`` as evenly as possible over {full, causal,
+    inverse-causal, bi-causal}, the first types taking the remainder (23
+    documents: full x6, causal x6, inverse-causal x6, bi-causal x5) from the
+    same generator.  Slices: the prefix's own full block, one self-slice per
     document, and one full slice per document over the prefix keys.
     """
     rng = np.random.default_rng(seed)
@@ -117,7 +119,8 @@ def heterogeneous_prefix_docs(total: int = 65536, h: int = 16, d: int = 128,
         bounds = [prefix] + sorted(int(c) for c in cuts) + [total]
         if len(set(bounds)) == len(bounds) and min(np.diff(bounds)) >= min_doc:
             break
-    base = [FULL] * 6 + [CAUSAL] * 6 + [INV_CAUSAL] * 6 + [BI_CAUSAL] * 5
+    per = [n_docs // 4 + (1 if i < n_docs % 4 else 0) for i in range(4)]
+    base = [FULL] * per[0] + [CAUSAL] * per[1] + [INV_CAUSAL] * per[2] + [BI_CAUSAL] * per[3]
     assert len(base) == n_docs
     types = [int(t) for t in rng.permutation(base)]
     qr, kr, ty = [[0, prefix]], [[0, prefix]], [FULL]
@@ -130,6 +133,26 @@ def heterogeneous_prefix_docs(total: int = 65536, h: int = 16, d: int = 128,
     return _pack(f"heterogeneous_prefix_T{total}_H{h}_D{d}", total, total, h, h, d,
                  qr, kr, ty, seed=seed, dout_seed=dout_seed, bounds=bounds,
                  doc_types=types)
+
+
+def short_causal_docs(total: int = 32768, h: int = 8, d: int = 128, lo: int = 128,
+                      hi: int = 512, seed: int = 8) -> Workload:
+    """Packed short documents (the memory-bound regime): lengths drawn one at a
+    time from ``default_rng(seed).integers(lo, hi + 1)`` until they reach
+    ``total`` (the last one takes the remainder, folded into the previous
+    document when shorter than ``lo``), one causal self-slice each."""
+    rng = np.random.default_rng(seed)
+    lens: list[int] = []
+    while sum(lens) < total:
+        lens.append(int(rng.integers(lo, hi + 1)))
+    lens[-1] = total - sum(lens[:-1])
+    if lens[-1] < lo and len(lens) > 1:
+        rem = lens.pop()
+        lens[-1] += rem
+    b = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    qr = np.stack([b[:-1], b[1:]], axis=1)
+    return _pack(f"short_causal_T{total}_H{h}_D{d}_L{lo}-{hi}", total, total, h, h, d, qr, qr,
+                 [CAUSAL] * len(lens), seed=seed, doc_lens=lens)
 
 
 def long_context_docs(total: int = 262144, hq: int = 16, hkv: int = 4, d: int = 128,
@@ -232,7 +255,12 @@ CONFIGS = {
     "tiny": tiny_causal_docs,
     "packed_causal": packed_causal_docs,
     "heterogeneous": heterogeneous_prefix_docs,
+    # the same structure at a quarter of the length (4096-token prefix, 11
+    # documents of all four types), small enough for a full oracle backward
+    "heterogeneous_mid": lambda: heterogeneous_prefix_docs(total=16384, h=2, n_docs=11, seed=13,
+                                                           dout_seed=17),
     "long_context": long_context_docs,
+    "short_docs": short_causal_docs,
     "block_sparse_64x64": lambda: block_sparse(q_block=64, k_block=64),
     "block_sparse_128x128": lambda: block_sparse(q_block=128, k_block=128),
     "block_sparse_16x64": lambda: block_sparse(q_block=16, k_block=64),
