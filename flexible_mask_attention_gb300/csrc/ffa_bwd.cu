@@ -982,10 +982,7 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
                           void* dq, void* dk, void* dv, void* ws, cudaStream_t st,
                           const SinkArgs& sk, float* dsink, float softcap) {
   CapConsts cap;
-  if (kCap) {
-    cap.a = scale / softcap;
-    cap.c2 = softcap * kLog2e;
-  }
+  if (kCap) cap = make_cap_consts(scale, softcap);
   const int qpad = p->n_qt * 128;
   float* nlse2 = static_cast<float*>(ws);
   float* ndelta = nlse2 + (size_t)p->Hq * qpad;

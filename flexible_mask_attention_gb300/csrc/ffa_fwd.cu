@@ -30,7 +30,11 @@
 //
 // Softcap (optional, a separate instantiation): scores become
 // c * tanh(scale * s / c) before the softmax; the tile maximum is capped the
-// same way (tanh is increasing) and masked entries stay -inf.
+// same way (tanh is increasing) and masked entries stay -inf.  When every
+// score of a warp's 32 rows lies in the range of the odd tanh polynomial
+// (|scale * s / c| <= 1), the capped scores come from that polynomial on the
+// FMA pipe (one MUFU operation per score, the exponential); otherwise from
+// tanh(u) = 1 - 2 / (e^(2u) + 1), which costs two more.
 //
 // Attention sink (optional): the sink logits of a row join its normaliser
 // only.  The epilogue of an unsplit item (or the merge of a split one) adds
@@ -95,6 +99,76 @@ struct FwdParams {
 // Capped score in base-2 units for raw score x (-inf stays -inf).
 __device__ __forceinline__ float capped2(float x, const CapConsts& c) {
   return x == -INFINITY ? -INFINITY : c.c2 * tanh_exp(x * c.a);
+}
+
+// The same on the polynomial's range |x| <= c.smax (-inf stays -inf).
+__device__ __forceinline__ float capped2_poly(float x, const CapConsts& c) {
+  if (x == -INFINITY) return -INFINITY;
+  const float w = x * x;
+  float r = c.r[kTanhPolyTerms - 1];
+#pragma unroll
+  for (int k = kTanhPolyTerms - 2; k >= 0; --k) r = fmaf(r, w, c.r[k]);
+  return x * r;
+}
+
+// Exponent modes of one softmax tile (see exp_tile).
+enum ExpMode : int {
+  kExpPlain = 0,    // p = 2^(s * scale * log2e - m)
+  kExpCapExp = 1,   // capped score from the exponential identity of tanh
+  kExpCapPoly = 2,  // capped score from the tanh polynomial (every score in range)
+  kExpCapPolyMask = 3  // the same on a PARTIAL step: masked columns forced to p = 0
+};
+
+// p = 2^(x - mu) for the 128 scores of one row (x the base-2 score, capped
+// or not), written as bf16 pairs over S columns [0, 64); returns their sum.
+// Masked scores arrive as -inf.  The polynomial modes first turn the raw
+// scores into x - mu in place (the polynomial of -inf is not -inf, so in
+// kExpCapPolyMask the row's column mask puts -inf back), then exponentiate.
+template <int kMode>
+__device__ __forceinline__ float exp_tile(uint32_t (&u)[128], uint32_t tS, float mu,
+                                          float scale_log2, const CapConsts& cap,
+                                          const uint32_t (&vb)[4]) {
+  const float2 sc2 = make_float2(scale_log2, scale_log2);
+  const float2 nm2 = make_float2(-mu, -mu);
+  if (kMode >= kExpCapPoly) {
+    // capped base-2 scores minus mu, in place
+#pragma unroll
+    for (int c = 0; c < 128; c += 2) {
+      const float2 sv = make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1]));
+      const float2 w = __fmul2_rn(sv, sv);
+      float2 r = cap.r2[kTanhPolyTerms - 1];
+#pragma unroll
+      for (int k = kTanhPolyTerms - 2; k >= 0; --k) r = __ffma2_rn(r, w, cap.r2[k]);
+      float2 t = __ffma2_rn(sv, r, nm2);
+      if (kMode == kExpCapPolyMask) {
+        t.x = mask_bit(vb, c) ? t.x : -INFINITY;
+        t.y = mask_bit(vb, c + 1) ? t.y : -INFINITY;
+      }
+      u[c] = __float_as_uint(t.x);
+      u[c + 1] = __float_as_uint(t.y);
+    }
+  }
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                   make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int c = 32 * q4 + 2 * i;
+      const float2 sv = make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1]));
+      float2 t;
+      if (kMode == kExpPlain) t = __ffma2_rn(sv, sc2, nm2);
+      else if (kMode == kExpCapExp) t = make_float2(capped2(sv.x, cap) - mu, capped2(sv.y, cap) - mu);
+      else t = sv;
+      const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+      acc[i & 3] = __fadd2_rn(acc[i & 3], p);
+      pk[i] = pack_bf16x2(p.x, p.y);
+    }
+    tmem_st16(tS + 16 * q4, pk);
+  }
+  return (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) +
+         (acc[3].x + acc[3].y);
 }
 
 // log2 of sum_s exp(sink_s) for (row, head) (-inf without sinks); sink logits
@@ -377,9 +451,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_after();
         uint32_t u[128];
         tmem_ld128(tS, u);
+        float mn = INFINITY;
+        if (kCap) {
+          // Smallest raw score of the row, masked columns included: with the
+          // masked maximum below it bounds every score the row sees.
+          float mn0 = INFINITY, mn1 = INFINITY, mn2 = INFINITY, mn3 = INFINITY;
+#pragma unroll
+          for (int c = 0; c < 128; c += 8) {
+            mn0 = fmin3(mn0, __uint_as_float(u[c]), __uint_as_float(u[c + 1]));
+            mn1 = fmin3(mn1, __uint_as_float(u[c + 2]), __uint_as_float(u[c + 3]));
+            mn2 = fmin3(mn2, __uint_as_float(u[c + 4]), __uint_as_float(u[c + 5]));
+            mn3 = fmin3(mn3, __uint_as_float(u[c + 6]), __uint_as_float(u[c + 7]));
+          }
+          mn = fminf(fminf(mn0, mn1), fminf(mn2, mn3));
+        }
+        const bool lo_in_range = -mn <= P.cap.smax;
+        uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
         if (info & 1) {
           // PARTIAL step: keep the keys this row sees under the step's slice(s).
-          uint32_t vb[4];
           step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
 #pragma unroll
           for (int c = 0; c < 128; ++c)
@@ -395,7 +484,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mx3 = fmax3(mx3, __uint_as_float(u[c + 6]), __uint_as_float(u[c + 7]));
         }
         const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-        const float m_cand = kCap ? capped2(mx, P.cap) : mx * P.scale_log2;
+        // Softcap: the polynomial serves when every score of the warp's rows
+        // lies in its range (a warp-uniform choice), else the exponential form.
+        const bool poly = kCap && __all_sync(0xffffffffu, lo_in_range && mx <= P.cap.smax);
+        const float m_cand = kCap ? (poly ? capped2_poly(mx, P.cap) : capped2(mx, P.cap))
+                                  : mx * P.scale_log2;
         const bool raise = m_cand > m + kRescaleThreshold;
         const bool rescale_o = raise && visited && m > -INFINITY;
         const float alpha = raise ? exp2f(m - m_cand) : 1.f;
@@ -416,31 +509,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           m = m_cand;
         }
         const float mu = m == -INFINITY ? 0.f : m;
-        // p = 2^(s * scale * log2e - m) two lanes at a time; four partial row sums.
-        const float2 sc2 = make_float2(P.scale_log2, P.scale_log2);
-        const float2 nm2 = make_float2(-mu, -mu);
-        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                         make_float2(0.f, 0.f)};
-        // P (bf16 pairs) goes over S columns [0, 64); every S value is in registers.
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int c = 32 * q4 + 2 * i;
-            const float2 t =
-                kCap ? make_float2(capped2(__uint_as_float(u[c]), P.cap) - mu,
-                                   capped2(__uint_as_float(u[c + 1]), P.cap) - mu)
-                     : __ffma2_rn(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])),
-                                  sc2, nm2);
-            const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-            acc[i & 3] = __fadd2_rn(acc[i & 3], p);
-            pk[i] = pack_bf16x2(p.x, p.y);
-          }
-          tmem_st16(tS + 16 * q4, pk);
-        }
-        l += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) +
-             (acc[3].x + acc[3].y);
+        // p = 2^(x - m) two lanes at a time, four partial row sums; P (bf16
+        // pairs) goes over S columns [0, 64): every S value is in registers.
+        if (!kCap)
+          l += exp_tile<kExpPlain>(u, tS, mu, P.scale_log2, P.cap, vb);
+        else if (!poly)
+          l += exp_tile<kExpCapExp>(u, tS, mu, P.scale_log2, P.cap, vb);
+        else if (info & 1)
+          l += exp_tile<kExpCapPolyMask>(u, tS, mu, P.scale_log2, P.cap, vb);
+        else
+          l += exp_tile<kExpCapPoly>(u, tS, mu, P.scale_log2, P.cap, vb);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(C::kBPFull + h));
@@ -601,10 +679,7 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   P.sink = sk.sink;
   P.n_sink = sk.n;
   P.sink_layout = sk.layout;
-  if (kCap) {
-    P.cap.a = scale / softcap;
-    P.cap.c2 = softcap * kLog2e;
-  }
+  if (kCap) P.cap = make_cap_consts(scale, softcap);
   if (cudaFuncSetAttribute(ffa_fwd_kernel<D, kCap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
     return FFA_ERR_CUDA;

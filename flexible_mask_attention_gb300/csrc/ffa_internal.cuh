@@ -173,10 +173,48 @@ ffa_status_t launch_bwd(ffa_plan_s* p, const void* q, const void* k, const void*
                         float softcap = 0.f);
 // Softcap c > 0: every score x = scale * q.k becomes c * tanh(x / c).  In
 // base-2 units the kernels use x2 = c log2(e) tanh(raw * scale / c).
+//
+// tanh(u) ~ u * sum_k kTanhPoly[k] * u^(2k) on |u| <= kTanhPolyRange: the odd
+// minimax polynomial of degree 11 (max error 2.9e-7 in fp64, 3.6e-7 when
+// evaluated by Horner in fp32), written by tanh_poly.py in this package.
+constexpr int kTanhPolyTerms = 6;
+constexpr double kTanhPolyRange = 1.0;
+constexpr double kTanhPoly[kTanhPolyTerms] = {
+    9.99996966051127645e-01,
+    -3.33241060355627228e-01,
+    1.32541111570184694e-01,
+    -5.09893659390155130e-02,
+    1.61341877872809153e-02,
+    -2.84789341630459431e-03};
 struct CapConsts {
   float a = 0.f;   // scale / c
   float c2 = 0.f;  // c * log2(e)
+  // Fast path: for |raw| <= smax (u = raw * a within the polynomial's range)
+  // the capped base-2 score is raw * R(raw^2), R(z) = sum_k r[k] z^k with
+  // r[k] = log2(e) * scale * kTanhPoly[k] * a^(2k); r2 holds each r[k]
+  // twice, the operand form of the packed two-lane FMAs, which then read it
+  // from the kernel's parameters instead of holding it in registers.
+  float r[kTanhPolyTerms] = {};
+  float2 r2[kTanhPolyTerms] = {};
+  float smax = 0.f;
 };
+// Fills CapConsts for softmax scale `scale` and cap c > 0 (host side, in
+// double so that c log2(e) and the powers of a neither overflow nor flush).
+inline CapConsts make_cap_consts(float scale, float c) {
+  CapConsts k;
+  const double a = (double)scale / (double)c;
+  k.a = (float)a;
+  k.c2 = (float)((double)c * 1.4426950408889634);
+  double apow = 1.0;
+  for (int i = 0; i < kTanhPolyTerms; ++i) {
+    k.r[i] = (float)(1.4426950408889634 * (double)scale * kTanhPoly[i] * apow);
+    k.r2[i] = make_float2(k.r[i], k.r[i]);
+    apow *= a * a;
+  }
+  const double sm = kTanhPolyRange / a;
+  k.smax = sm < 3.0e38 ? (float)sm : 3.0e38f;
+  return k;
+}
 size_t bwd_workspace_bytes(const ffa_plan_s* p);
 // Implemented in ffa_plan.cu.
 bool on_plan_device(const ffa_plan_s* p);  // current device == the plan's device

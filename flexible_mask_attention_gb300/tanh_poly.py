@@ -1,0 +1,79 @@
+"""Coefficients of the odd polynomial the softcap kernels use for tanh.
+
+The kernels cap a score x to c * tanh(x / c).  Where every argument
+u = x / c of a tile lies in [-U, U] they evaluate tanh(u) as
+u * Q(u^2) with Q(w) = q_0 + q_1 w + ... + q_5 w^5 (an odd polynomial of
+degree 11), on the FMA pipe; elsewhere they fall back to the exponential
+identity tanh(u) = 1 - 2 / (exp(2u) + 1).
+
+Q is the minimax (best uniform) approximation of tanh on [-U, U]: the
+polynomial whose largest absolute error is smallest, i.e. the one whose
+error equioscillates (Chebyshev's alternation theorem).  It is found here as
+a linear program over a dense grid (minimise t subject to |p(u_i) -
+tanh(u_i)| <= t), with p written in the odd Chebyshev polynomials
+T_1, T_3, ..., T_11 of u / U so that the program is well conditioned, and
+then converted to the monomial coefficients q_k.
+
+    python -m flexible_mask_attention_gb300.tanh_poly   # prints the C table
+
+The printed table is pasted into csrc/ffa_internal.cuh (kTanhPoly).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+U = 1.0        # range of the polynomial: |u| <= U
+N_TERMS = 6    # q_0 .. q_5 (degree 11)
+
+
+def fit(U: float = U, n_terms: int = N_TERMS, n_grid: int = 20001):
+    from numpy.polynomial import chebyshev as C
+    from scipy.optimize import linprog
+
+    t = np.linspace(0.0, 1.0, n_grid)[1:]      # u / U on (0, 1]; the error is odd
+    y = np.tanh(U * t)
+    basis = np.stack([C.chebval(t, [0] * (2 * k + 1) + [1]) for k in range(n_terms)], axis=1)
+    nv = n_terms + 1
+    cost = np.zeros(nv)
+    cost[-1] = 1.0
+    ones = np.ones((t.shape[0], 1))
+    a_ub = np.vstack([np.hstack([basis, -ones]), np.hstack([-basis, -ones])])
+    b_ub = np.concatenate([y, -y])
+    res = linprog(cost, A_ub=a_ub, b_ub=b_ub, bounds=[(None, None)] * nv, method="highs")
+    if not res.success:
+        raise RuntimeError(res.message)
+    cheb = np.zeros(2 * n_terms)
+    cheb[1::2] = res.x[:n_terms]
+    mono_t = C.cheb2poly(cheb)                  # coefficients of t^0 .. t^(2n-1)
+    # p(u) = sum_j m_j (u / U)^j, odd j only  ->  q_k = m_(2k+1) / U^(2k+1)
+    q = np.array([mono_t[2 * k + 1] / U ** (2 * k + 1) for k in range(n_terms)])
+    return q
+
+
+def max_error(q, U: float = U, fp32: bool = False, n: int = 400001) -> float:
+    u = np.linspace(-U, U, n)
+    if fp32:
+        u32 = u.astype(np.float32)
+        w = u32 * u32
+        p = np.float32(q[-1])
+        for c in q[-2::-1]:
+            p = (p * w + np.float32(c)).astype(np.float32)
+        approx = (u32 * p).astype(np.float64)
+        return float(np.abs(approx - np.tanh(u32.astype(np.float64))).max())
+    w = u * u
+    p = np.zeros_like(u) + q[-1]
+    for c in q[-2::-1]:
+        p = p * w + c
+    return float(np.abs(u * p - np.tanh(u)).max())
+
+
+def main():
+    q = fit()
+    print(f"// tanh(u) ~ u * sum_k kTanhPoly[k] * u^(2k) on |u| <= {U}: "
+          f"max error {max_error(q):.2e} (fp64), {max_error(q, fp32=True):.2e} (fp32 Horner)")
+    print("constexpr double kTanhPoly[%d] = {" % len(q))
+    print(",\n".join(f"    {c:.17e}" for c in q) + "};")
+
+
+if __name__ == "__main__":
+    main()

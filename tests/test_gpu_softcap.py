@@ -69,3 +69,40 @@ def test_softcap_with_sink():
     check_grad(dv.float().cpu().numpy(), rv, "dv")
     rs = oracle.dsink(q, k, v, do, qr, kr, ty, sink, "sh", softcap=cap)
     check_grad(ds.cpu().numpy(), rs, "dsink")
+
+
+# Scores of unit-scale inputs stay well inside the tanh polynomial's range
+# (|score / c| <= 1) for these caps, so every warp takes the polynomial path;
+# in the mixed case a few query rows are scaled up so that the warps holding
+# them fall back to the exponential form inside the same launch.
+POLY_CASES = [
+    # (Tq, Tk, Hq, Hkv, D, n_segments, seed, cap, rows scaled up)
+    (1000, 1000, 4, 2, 128, 5, 81, 30.0, 0),
+    (640, 900, 3, 1, 64, 6, 82, 8.0, 0),
+    (1100, 1100, 2, 2, 128, 5, 83, 8.0, 12),
+    (700, 700, 2, 1, 128, 4, 84, 1.0e6, 0),
+]
+
+
+@pytest.mark.parametrize("case", POLY_CASES,
+                         ids=[f"T{c[0]}_D{c[4]}_cap{c[7]:g}_big{c[8]}" for c in POLY_CASES])
+def test_softcap_polynomial_path(case):
+    Tq, Tk, Hq, Hkv, D, nseg, seed, cap, n_big = case
+    qr, kr, ty = W.random_slices(Tq, Tk, nseg, seed=seed)
+    q, k = bf16(Tq, Hq, D, seed=seed), bf16(Tk, Hkv, D, seed=seed + 1)
+    v, do = bf16(Tk, Hkv, D, seed=seed + 2), bf16(Tq, Hq, D, seed=seed + 3)
+    if n_big:
+        rows = np.random.default_rng(seed).choice(Tq, n_big, replace=False)
+        q[rows] = (q[rows].float() * 6.0).to(torch.bfloat16)
+    plan = ffa.ffa_plan_create(qr, kr, ty, Tq, Tk, Hq, Hkv, D)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    out, lse = ffa.ffa_fwd_ex(plan, qd, kd, vd, softcap=cap)
+    dq, dk, dv, _ = ffa.ffa_bwd_ex(plan, qd, kd, vd, out, dod, lse, softcap=cap)
+    torch.cuda.synchronize()
+    assert ffa.ffa_get_last_device_error(plan) == (0, 0)
+    ro, rl = oracle.fwd(q, k, v, qr, kr, ty, softcap=cap)
+    check_fwd(out.float().cpu().numpy(), lse.cpu().numpy(), ro, rl)
+    rq, rk, rv = oracle.bwd(q, k, v, do, qr, kr, ty, softcap=cap)
+    check_grad(dq.float().cpu().numpy(), rq, "dq")
+    check_grad(dk.float().cpu().numpy(), rk, "dk")
+    check_grad(dv.float().cpu().numpy(), rv, "dv")
