@@ -110,9 +110,38 @@ struct KvParams {
 //   p = 2^(s * scale * log2e - lse2), ds = p * (dp - delta).
 // They go back, as bf16 pairs, over the dP^T chunk they were read from:
 // dS^T in columns [q0+32c, +16), P^T in [q0+32c+16, +16).
-// kCap: scores capped to c tanh(scale s / c); then x = c log2e tanh(..) - lse2
-// and dS also carries the factor 1 - tanh^2.
-template <bool kPartial, bool kCap, int c>
+// Softcap (kCapMode > 0): scores capped to c tanh(scale s / c); then
+// x = c log2e tanh(..) - lse2 and dS also carries the factor 1 - tanh^2.
+// tanh comes from the exponential identity (kCapExp) or, when every score of
+// the warp is in its range, from the odd polynomial (kCapPoly).
+enum CapMode : int { kCapNone = 0, kCapExp = 1, kCapPoly = 2 };
+
+// tanh(s * a) of two raw scores by the polynomial (their |s| <= cap.smax).
+__device__ __forceinline__ float2 tanh_poly2(float2 sv, const CapConsts& cap) {
+  const float2 w = __fmul2_rn(sv, sv);
+  float2 r = cap.t2[kTanhPolyTerms - 1];
+#pragma unroll
+  for (int k = kTanhPolyTerms - 2; k >= 0; --k) r = __ffma2_rn(r, w, cap.t2[k]);
+  return __fmul2_rn(sv, r);
+}
+
+// True for every lane when all n raw scores of every lane of the warp lie in
+// the tanh polynomial's range (warp-uniform).
+template <int n>
+__device__ __forceinline__ bool scores_in_poly_range(const uint32_t* s, float smax) {
+  float mx0 = -INFINITY, mx1 = -INFINITY, mn0 = INFINITY, mn1 = INFINITY;
+#pragma unroll
+  for (int c = 0; c + 3 < n; c += 4) {
+    mx0 = fmax3(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+    mx1 = fmax3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+    mn0 = fmin3(mn0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+    mn1 = fmin3(mn1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+  }
+  const float big = fmaxf(fmaxf(mx0, mx1), -fminf(mn0, mn1));
+  return __all_sync(0xffffffffu, big <= smax);
+}
+
+template <bool kPartial, int kCapMode, int c>
 __device__ __forceinline__ void pds_chunk(const uint32_t (&s)[64], uint32_t tP, int q0,
                                           const float* nl, const float* nd, float scale_log2,
                                           const CapConsts& cap, uint32_t m_lo, uint32_t m_hi) {
@@ -130,14 +159,13 @@ __device__ __forceinline__ void pds_chunk(const uint32_t (&s)[64], uint32_t tP, 
         const int lc = 32 * c + e + u;  // column within this warpgroup's half
         const float2 nlp = u == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
         const float2 ndp = u == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
+        const float2 sv = make_float2(__uint_as_float(s[lc]), __uint_as_float(s[lc + 1]));
         float2 th = make_float2(0.f, 0.f);
-        if (kCap)
-          th = make_float2(tanh_exp(__uint_as_float(s[lc]) * cap.a),
-                           tanh_exp(__uint_as_float(s[lc + 1]) * cap.a));
-        const float2 x =
-            kCap ? __ffma2_rn(th, make_float2(cap.c2, cap.c2), nlp)
-                 : __ffma2_rn(make_float2(__uint_as_float(s[lc]), __uint_as_float(s[lc + 1])), sc2,
-                              nlp);
+        if (kCapMode == kCapExp) th = make_float2(tanh_exp(sv.x * cap.a), tanh_exp(sv.y * cap.a));
+        if (kCapMode == kCapPoly) th = tanh_poly2(sv, cap);
+        const float2 x = kCapMode != kCapNone
+                             ? __ffma2_rn(th, make_float2(cap.c2, cap.c2), nlp)
+                             : __ffma2_rn(sv, sc2, nlp);
         float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
         if (kPartial) {  // bits of this warpgroup's 64 columns: m_lo (0-31), m_hi (32-63)
           const uint32_t mw = c == 0 ? m_lo : m_hi;
@@ -147,7 +175,8 @@ __device__ __forceinline__ void pds_chunk(const uint32_t (&s)[64], uint32_t tP, 
         const float2 dpd = __fadd2_rn(
             make_float2(__uint_as_float(dp[e + u]), __uint_as_float(dp[e + u + 1])), ndp);
         float2 ds = __fmul2_rn(p, dpd);
-        if (kCap) ds = __fmul2_rn(ds, make_float2(1.f - th.x * th.x, 1.f - th.y * th.y));
+        if (kCapMode != kCapNone)
+          ds = __fmul2_rn(ds, __ffma2_rn(make_float2(-th.x, -th.y), th, make_float2(1.f, 1.f)));
         pp[(e + u) >> 1] = pack_bf16x2(p.x, p.y);
         dd[(e + u) >> 1] = pack_bf16x2(ds.x, ds.y);
       }
@@ -436,19 +465,40 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
         ++sdp_cnt;
         tc_fence_after();
         const uint32_t m_lo = wg ? vb[2] : vb[0], m_hi = wg ? vb[3] : vb[1];
+        const bool poly = kCap && scores_in_poly_range<64>(s, P.cap.smax);
         // Each 32-query chunk is signalled on its own, so the dV / dK MMAs of
         // the first chunk run while the second is computed.
-        if (info & 1)
-          pds_chunk<true, kCap, 0>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, m_hi);
-        else
-          pds_chunk<false, kCap, 0>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, m_hi);
+#define FFA_PDS(chunk)                                                                       \
+  do {                                                                                       \
+    if (!kCap) {                                                                             \
+      if (info & 1)                                                                          \
+        pds_chunk<true, kCapNone, chunk>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo,  \
+                                         m_hi);                                              \
+      else                                                                                   \
+        pds_chunk<false, kCapNone, chunk>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, \
+                                          m_hi);                                             \
+    } else if (poly) {                                                                       \
+      if (info & 1)                                                                          \
+        pds_chunk<true, kCapPoly, chunk>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo,  \
+                                         m_hi);                                              \
+      else                                                                                   \
+        pds_chunk<false, kCapPoly, chunk>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, \
+                                          m_hi);                                             \
+    } else {                                                                                 \
+      if (info & 1)                                                                          \
+        pds_chunk<true, kCapExp, chunk>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo,   \
+                                        m_hi);                                               \
+      else                                                                                   \
+        pds_chunk<false, kCapExp, chunk>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo,  \
+                                         m_hi);                                              \
+    }                                                                                        \
+  } while (0)
+        FFA_PDS(0);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(C::kBPFull));
-        if (info & 1)
-          pds_chunk<true, kCap, 1>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, m_hi);
-        else
-          pds_chunk<false, kCap, 1>(s, tP, 64 * wg, nl, nd, P.scale_log2, P.cap, m_lo, m_hi);
+        FFA_PDS(1);
+#undef FFA_PDS
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(C::kBPFull + 1));
@@ -559,6 +609,37 @@ struct DqParams {
   uint64_t wait_ns;
   CapConsts cap;  // used by the softcap instantiation only
 };
+
+// dS = 2^(x - lse2) * (dP - delta) for 32 columns of one query row (x the
+// base-2 score, capped by kCapMode as in pds_chunk), masked by the bits mw of
+// the chunk when `partial`, as bf16 pairs.  c0: the chunk's first column in dp.
+template <int kCapMode>
+__device__ __forceinline__ void dq_ds_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[64],
+                                            int c0, uint32_t mw, bool partial, float2 nl2,
+                                            float nd, float2 sc2, const CapConsts& cap,
+                                            uint32_t (&dd)[16]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    const int lc = c0 + e;
+    const float2 sv = make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1]));
+    float2 th = make_float2(0.f, 0.f);
+    if (kCapMode == kCapExp) th = make_float2(tanh_exp(sv.x * cap.a), tanh_exp(sv.y * cap.a));
+    if (kCapMode == kCapPoly) th = tanh_poly2(sv, cap);
+    const float2 x = kCapMode != kCapNone ? __ffma2_rn(th, make_float2(cap.c2, cap.c2), nl2)
+                                          : __ffma2_rn(sv, sc2, nl2);
+    float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+    if (partial) {
+      p.x = ((mw >> (e & 31)) & 1u) ? p.x : 0.f;
+      p.y = ((mw >> ((e + 1) & 31)) & 1u) ? p.y : 0.f;
+    }
+    float2 ds = __fmul2_rn(
+        p, __fadd2_rn(make_float2(__uint_as_float(dp[lc]), __uint_as_float(dp[lc + 1])),
+                      make_float2(nd, nd)));
+    if (kCapMode != kCapNone)
+      ds = __fmul2_rn(ds, __ffma2_rn(make_float2(-th.x, -th.y), th, make_float2(1.f, 1.f)));
+    dd[e >> 1] = pack_bf16x2(ds.x, ds.y);
+  }
+}
 
 __device__ __forceinline__ bool half_active(const int* it, int h) {
   return it[kFiQt0 + h] >= 0 && it[kFiH0 + h] >= 0;
@@ -827,30 +908,14 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           for (int c = 0; c < 2; ++c) {
             uint32_t s[32];
             tmem_ld32(tSb + 32 * c, s);
+            const uint32_t mw = c == 0 ? m_lo : m_hi;
             uint32_t dd[16];
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const int lc = 32 * c + e;
-              float2 th = make_float2(0.f, 0.f);
-              if (kCap)
-                th = make_float2(tanh_exp(__uint_as_float(s[e]) * P.cap.a),
-                                 tanh_exp(__uint_as_float(s[e + 1]) * P.cap.a));
-              const float2 x =
-                  kCap ? __ffma2_rn(th, make_float2(P.cap.c2, P.cap.c2), nl2)
-                       : __ffma2_rn(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])),
-                                    sc2, nl2);
-              float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-              if (info & 1) {  // lc is this warpgroup's column: m_lo (0-31), m_hi (32-63)
-                const uint32_t mw = lc < 32 ? m_lo : m_hi;
-                p.x = ((mw >> (lc & 31)) & 1u) ? p.x : 0.f;
-                p.y = ((mw >> ((lc + 1) & 31)) & 1u) ? p.y : 0.f;
-              }
-              float2 ds = __fmul2_rn(
-                  p, __fadd2_rn(make_float2(__uint_as_float(dp[lc]), __uint_as_float(dp[lc + 1])),
-                                make_float2(nd, nd)));
-              if (kCap) ds = __fmul2_rn(ds, make_float2(1.f - th.x * th.x, 1.f - th.y * th.y));
-              dd[e >> 1] = pack_bf16x2(ds.x, ds.y);
-            }
+            if (!kCap)
+              dq_ds_chunk<kCapNone>(s, dp, 32 * c, mw, info & 1, nl2, nd, sc2, P.cap, dd);
+            else if (scores_in_poly_range<32>(s, P.cap.smax))
+              dq_ds_chunk<kCapPoly>(s, dp, 32 * c, mw, info & 1, nl2, nd, sc2, P.cap, dd);
+            else
+              dq_ds_chunk<kCapExp>(s, dp, 32 * c, mw, info & 1, nl2, nd, sc2, P.cap, dd);
             // chunk c writes columns [64wg + 16c, 64wg + 16c + 16), read by chunk 0
             tmem_st16(tSb + 16 * c, dd);
           }
@@ -908,34 +973,61 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
 }
 
 // -delta = -rowsum(dO * O), -lse2 = -lse * log2(e); padded rows get 0.
+// HBM-bound (it reads out and dout once).  A block covers 64 consecutive rows
+// of one head: each warp takes 8 of them, D / 8 lanes per row reading 16
+// bytes each (a warp's load covers 2 or 4 whole rows, 512 contiguous bytes
+// when Hq = 1 and full 32-byte sectors always), issues all of its loads
+// before using any, and sums each row with a shuffle tree in a fixed order;
+// the block's lse reads and scratch writes are contiguous.
+constexpr int kPreRows = 64;  // rows per block (8 warps x 8 rows)
+
 template <int D>
-__global__ void ffa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
-                                   const __nv_bfloat16* __restrict__ dout,
-                                   const float* __restrict__ lse, int Tq, int Hq, int qpad,
-                                   float* __restrict__ nlse2, float* __restrict__ ndelta) {
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // (q, h)
-  if (idx >= (long long)qpad * Hq) return;
-  const int q = (int)(idx / Hq), h = (int)(idx % Hq);
-  float dsum = 0.f, l2 = 0.f;
-  if (q < Tq) {
-    const uint4* o4 = reinterpret_cast<const uint4*>(out + ((size_t)q * Hq + h) * D);
-    const uint4* d4 = reinterpret_cast<const uint4*>(dout + ((size_t)q * Hq + h) * D);
+__global__ void __launch_bounds__(256)
+    ffa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
+                       const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
+                       int Tq, int Hq, int qpad, float* __restrict__ nlse2,
+                       float* __restrict__ ndelta) {
+  constexpr int kLanes = D / 8;              // lanes per row, 16 bytes each
+  constexpr int kRowsPerLoad = 32 / kLanes;  // rows one warp-wide load covers
+  constexpr int kIters = 8 / kRowsPerLoad;   // loads per lane and tensor
+  const int h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane / kLanes, li = lane % kLanes;
+  const int q_base = blockIdx.x * kPreRows + warp * 8;
+  uint4 a[kIters], b[kIters];
 #pragma unroll
-    for (int v = 0; v < D / 8; ++v) {
-      const uint4 a = o4[v], b = d4[v];
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[t]));
-        const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[t]));
-        dsum = fmaf(fa.x, fb.x, dsum);
-        dsum = fmaf(fa.y, fb.y, dsum);
-      }
+  for (int it = 0; it < kIters; ++it) {
+    const int q = q_base + it * kRowsPerLoad + sub;
+    if (q < Tq) {
+      const size_t off = ((size_t)q * Hq + h) * D + li * 8;
+      a[it] = *reinterpret_cast<const uint4*>(out + off);
+      b[it] = *reinterpret_cast<const uint4*>(dout + off);
+    } else {
+      a[it] = b[it] = make_uint4(0, 0, 0, 0);
     }
-    l2 = lse[(size_t)h * Tq + q] * kLog2e;  // -inf stays -inf: such rows see no key
   }
-  nlse2[(size_t)h * qpad + q] = -l2;
-  ndelta[(size_t)h * qpad + q] = -dsum;
+#pragma unroll
+  for (int it = 0; it < kIters; ++it) {
+    const uint32_t aw[4] = {a[it].x, a[it].y, a[it].z, a[it].w};
+    const uint32_t bw[4] = {b[it].x, b[it].y, b[it].z, b[it].w};
+    float dsum = 0.f;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[t]));
+      const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[t]));
+      dsum = fmaf(fa.x, fb.x, dsum);
+      dsum = fmaf(fa.y, fb.y, dsum);
+    }
+#pragma unroll
+    for (int o = kLanes / 2; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+    const int q = q_base + it * kRowsPerLoad + sub;
+    if (li == 0 && q < qpad) {
+      // -inf stays -inf (such rows see no key); padded rows get 0
+      const float l2 = q < Tq ? lse[(size_t)h * Tq + q] * kLog2e : 0.f;
+      nlse2[(size_t)h * qpad + q] = -l2;
+      ndelta[(size_t)h * qpad + q] = -dsum;
+    }
+  }
 }
 
 // Gradient of the attention-sink logits, which enter only the normaliser:
@@ -987,9 +1079,9 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   float* nlse2 = static_cast<float*>(ws);
   float* ndelta = nlse2 + (size_t)p->Hq * qpad;
   {
-    const long long n = (long long)qpad * p->Hq;
     record_phase(p, 2, st);
-    ffa_bwd_pre_kernel<D><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(
+    const dim3 grid((unsigned)(qpad / kPreRows), (unsigned)p->Hq);
+    ffa_bwd_pre_kernel<D><<<grid, 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse,
         p->Tq, p->Hq, qpad, nlse2, ndelta);
     note_launches(1);

@@ -175,17 +175,19 @@ ffa_status_t launch_bwd(ffa_plan_s* p, const void* q, const void* k, const void*
 // base-2 units the kernels use x2 = c log2(e) tanh(raw * scale / c).
 //
 // tanh(u) ~ u * sum_k kTanhPoly[k] * u^(2k) on |u| <= kTanhPolyRange: the odd
-// minimax polynomial of degree 11 (max error 2.9e-7 in fp64, 3.6e-7 when
-// evaluated by Horner in fp32), written by tanh_poly.py in this package.
+// polynomial of degree 11 with the smallest largest error relative to tanh
+// (1.3e-6 in fp64, 1.4e-6 when evaluated by Horner in fp32), so a capped
+// score c tanh(x / c) is off by at most 1.4e-6 |x| whatever the cap;
+// written by tanh_poly.py in this package.
 constexpr int kTanhPolyTerms = 6;
 constexpr double kTanhPolyRange = 1.0;
 constexpr double kTanhPoly[kTanhPolyTerms] = {
-    9.99996966051127645e-01,
-    -3.33241060355627228e-01,
-    1.32541111570184694e-01,
-    -5.09893659390155130e-02,
-    1.61341877872809153e-02,
-    -2.84789341630459431e-03};
+    9.99998715205285826e-01,
+    -3.33276316555438212e-01,
+    1.32733617778814705e-01,
+    -5.14167687820982905e-02,
+    1.65506712346618519e-02,
+    -2.99609548713972596e-03};
 struct CapConsts {
   float a = 0.f;   // scale / c
   float c2 = 0.f;  // c * log2(e)
@@ -196,6 +198,10 @@ struct CapConsts {
   // from the kernel's parameters instead of holding it in registers.
   float r[kTanhPolyTerms] = {};
   float2 r2[kTanhPolyTerms] = {};
+  // tanh itself (the backward also needs 1 - tanh^2): tanh(raw * a) =
+  // raw * T(raw^2), T(z) = sum_k t[k] z^k, t[k] = kTanhPoly[k] * a^(2k+1),
+  // as pairs.
+  float2 t2[kTanhPolyTerms] = {};
   float smax = 0.f;
 };
 // Fills CapConsts for softmax scale `scale` and cap c > 0 (host side, in
@@ -209,6 +215,8 @@ inline CapConsts make_cap_consts(float scale, float c) {
   for (int i = 0; i < kTanhPolyTerms; ++i) {
     k.r[i] = (float)(1.4426950408889634 * (double)scale * kTanhPoly[i] * apow);
     k.r2[i] = make_float2(k.r[i], k.r[i]);
+    const float t = (float)(kTanhPoly[i] * apow * a);
+    k.t2[i] = make_float2(t, t);
     apow *= a * a;
   }
   const double sm = kTanhPolyRange / a;

@@ -1,7 +1,8 @@
 """The softcap kernels' tanh polynomial: the table compiled into the CUDA
 sources is the one the committed generator produces, and its error against
-numpy's tanh stays within the bound the kernels rely on (a few 1e-7, the
-accuracy of the exponential form it replaces)."""
+numpy's tanh stays within the bound the kernels rely on (1.4e-6 relative
+to tanh, so that a capped score is accurate relative to the score for any
+cap)."""
 import os
 import re
 
@@ -31,9 +32,11 @@ def test_table_matches_generator():
 def test_error_bound():
     from flexible_mask_attention_gb300 import tanh_poly
     q, rng = header_table()
-    assert tanh_poly.max_error(q, rng) < 3.0e-7
-    assert tanh_poly.max_error(q, rng, fp32=True) < 4.0e-7
+    # relative to tanh(u): the capped score c tanh(x / c) is then accurate
+    # relative to the score for every cap c
+    assert tanh_poly.max_error(q, rng) < 1.4e-6
+    assert tanh_poly.max_error(q, rng, fp32=True) < 1.5e-6
     # odd and close to the identity near zero
     u = np.linspace(1e-4, 1e-2, 50)
     p = u * np.polyval(q[::-1], u * u)
-    assert np.abs(p - np.tanh(u)).max() < 1e-7
+    assert (np.abs(p - np.tanh(u)) / np.tanh(u)).max() < 1.4e-6
