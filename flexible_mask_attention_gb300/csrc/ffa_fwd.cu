@@ -32,7 +32,7 @@
 // c * tanh(scale * s / c) before the softmax; the tile maximum is capped the
 // same way (tanh is increasing) and masked entries stay -inf.  When every
 // score of a warp's 32 rows lies in the range of the odd tanh polynomial
-// (|scale * s / c| <= 1), the capped scores come from that polynomial on the
+// (|scale * s / c| <= 0.75), the capped scores come from that polynomial on the
 // FMA pipe (one MUFU operation per score, the exponential); otherwise from
 // tanh(u) = 1 - 2 / (e^(2u) + 1), which costs two more.
 //

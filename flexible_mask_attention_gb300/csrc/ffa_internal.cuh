@@ -175,19 +175,18 @@ ffa_status_t launch_bwd(ffa_plan_s* p, const void* q, const void* k, const void*
 // base-2 units the kernels use x2 = c log2(e) tanh(raw * scale / c).
 //
 // tanh(u) ~ u * sum_k kTanhPoly[k] * u^(2k) on |u| <= kTanhPolyRange: the odd
-// polynomial of degree 11 with the smallest largest error relative to tanh
-// (1.3e-6 in fp64, 1.4e-6 when evaluated by Horner in fp32), so a capped
+// polynomial of degree 9 with the smallest largest error relative to tanh
+// (1.26e-6 in fp64, 1.33e-6 when evaluated by Horner in fp32), so a capped
 // score c tanh(x / c) is off by at most 1.4e-6 |x| whatever the cap;
 // written by tanh_poly.py in this package.
-constexpr int kTanhPolyTerms = 6;
-constexpr double kTanhPolyRange = 1.0;
+constexpr int kTanhPolyTerms = 5;
+constexpr double kTanhPolyRange = 0.75;
 constexpr double kTanhPoly[kTanhPolyTerms] = {
-    9.99998715205285826e-01,
-    -3.33276316555438212e-01,
-    1.32733617778814705e-01,
-    -5.14167687820982905e-02,
-    1.65506712346618519e-02,
-    -2.99609548713972596e-03};
+    9.99998743192078265e-01,
+    -3.33262889929604456e-01,
+    1.32458877985800832e-01,
+    -4.97348543713007282e-02,
+    1.26672359966334969e-02};
 struct CapConsts {
   float a = 0.f;   // scale / c
   float c2 = 0.f;  // c * log2(e)

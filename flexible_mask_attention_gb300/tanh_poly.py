@@ -2,8 +2,8 @@
 
 The kernels cap a score x to c * tanh(x / c).  Where every argument
 u = x / c of a tile lies in [-U, U] they evaluate tanh(u) as
-u * Q(u^2) with Q(w) = q_0 + q_1 w + ... + q_5 w^5 (an odd polynomial of
-degree 11), on the FMA pipe; elsewhere they fall back to the exponential
+u * Q(u^2) with Q(w) = q_0 + q_1 w + ... + q_4 w^4 (an odd polynomial of
+degree 9), on the FMA pipe; elsewhere they fall back to the exponential
 identity tanh(u) = 1 - 2 / (exp(2u) + 1).
 
 Q is the minimax approximation of tanh on [-U, U] in relative error: the
@@ -13,7 +13,7 @@ Relative error keeps the capped score c * tanh(x / c) accurate relative to
 the score itself for every cap c (an absolute bound would be multiplied by
 c).  It is found here as a linear program over a dense grid (minimise t
 subject to |p(u_i) - tanh(u_i)| <= t * tanh(u_i)), with p written in the odd
-Chebyshev polynomials T_1, T_3, ..., T_11 of u / U so that the program is
+Chebyshev polynomials T_1, T_3, ..., T_9 of u / U so that the program is
 well conditioned, and then converted to the monomial coefficients q_k.
 
     python -m flexible_mask_attention_gb300.tanh_poly   # prints the C table
@@ -24,8 +24,8 @@ from __future__ import annotations
 
 import numpy as np
 
-U = 1.0        # range of the polynomial: |u| <= U
-N_TERMS = 6    # q_0 .. q_5 (degree 11)
+U = 0.75       # range of the polynomial: |u| <= U
+N_TERMS = 5    # q_0 .. q_4 (degree 9)
 
 
 def fit(U: float = U, n_terms: int = N_TERMS, n_grid: int = 20001):

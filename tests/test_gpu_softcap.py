@@ -72,7 +72,7 @@ def test_softcap_with_sink():
 
 
 # Scores of unit-scale inputs stay well inside the tanh polynomial's range
-# (|score / c| <= 1) for these caps, so every warp takes the polynomial path;
+# (|score / c| <= 0.75) for these caps, so the warps take the polynomial path;
 # in the mixed case a few query rows are scaled up so that the warps holding
 # them fall back to the exponential form inside the same launch.
 POLY_CASES = [
