@@ -21,7 +21,16 @@ the work-list specification of the planner:
   * order: cost octave floor(log2(cost + 1)) descending, then kv head, then
     cost descending, then item index;
   * backward: per k-tile one visit per q-tile seen, merged the same way, one
-    item per (kt, kv head), cost g * sum of visit costs.
+    item per (kt, kv head), cost g * sum of visit costs;
+  * gathered forward units: a unit whose q-tiles meet only FULL slices with
+    8-aligned key ranges (the end may be Tk), Tk <= 2^19, is instead listed
+    as gathered steps when that takes fewer steps: the 8-key blocks any of
+    its slices covers, ascending, 16 to a step; a step is (0, info0, info1,
+    r + 1) with record r = 16 block starts (key index, -8 for an unused
+    slot) then, per half, 16 x 4 words of row bits (bit r of word w: row
+    32w + r of the half's q-tile sees the slot's keys); info_h = 1 when the
+    half has a row bit set, else -1; cost 5 per busy half.  At most 2048
+    blocks per unit.
 """
 from __future__ import annotations
 
@@ -31,6 +40,11 @@ import numpy as np
 
 TILE = 128
 FULL_COST, PARTIAL_COST = 4, 5
+GATHER_KEYS = 8           # keys per gathered slot (one 8-row TMA box)
+GATHER_SLOTS = 16         # slots per gathered step (a 128-key tile)
+GATHER_MAX_BLOCKS = 2048  # blocks per gathered unit
+GATHER_MAX_TK = 1 << 19
+GATHER_WORDS = GATHER_SLOTS + 2 * GATHER_SLOTS * 4
 
 
 def row_intervals(qs, qe, ks, ke, t):
@@ -130,10 +144,20 @@ def plan(total_q, total_k, num_heads_q, num_heads_kv, q_ranges, k_ranges, mask_t
     # forward units and steps
     pair_mode = 0 if g >= 2 else 1
     n_units = n_qt if pair_mode == 0 else (n_qt + 1) // 2
+    gathered = gather_units(total_q, total_k, q_ranges, k_ranges, mask_types, pair_mode, fvis)
+    records = []
     steps, soff, scnt, cost_half = [], [], [], []
     for u in range(n_units):
         soff.append(len(steps))
-        if pair_mode == 0:
+        if u in gathered:
+            st, ca, cb = [], 0, 0
+            for rec, (i0, i1) in gathered[u]:
+                st.append((0, i0, i1, len(records) + 1))
+                records.append(rec)
+                ca += PARTIAL_COST if i0 >= 0 else 0
+                cb += PARTIAL_COST if i1 >= 0 else 0
+            cost_half.append((ca, cb))
+        elif pair_mode == 0:
             st = [(kt, i, i, 0) for kt, i in fvis[u]]
             c = sum(_cost(i) for _, i in fvis[u])
             cost_half.append((c, c))
@@ -220,9 +244,71 @@ def plan(total_q, total_k, num_heads_q, num_heads_kv, q_ranges, k_ranges, mask_t
         "bwd_order": order_of([it[4] for it in bitems], [it[1] for it in bitems]),
         "merges": np.array(merges, dtype=np.int32).reshape(-1, 8),
         "fwd_masks": np.array(fmasks, dtype=np.int32).reshape(-1, 1),
+        "gathers": np.array(records, dtype=np.int32).reshape(-1, GATHER_WORDS),
         "bwd_masks": np.array(bmasks, dtype=np.int32).reshape(-1, 1),
         "n_slots": n_slots,
         "grid_fwd": max(1, min(num_sms, len(items))),
         "grid_bwd": max(1, min(num_sms, len(bitems))),
         "area": visible_area(q_ranges, k_ranges, mask_types),
     }
+
+
+def _tile_slices(total_q, q_ranges, k_ranges, mask_types):
+    """Per q-tile: the non-empty slices whose q range meets its rows."""
+    n_qt = -(-total_q // TILE)
+    out = [[] for _ in range(n_qt)]
+    for s, ((qs, qe), (ks, ke), t) in enumerate(zip(np.asarray(q_ranges).reshape(-1, 2),
+                                                    np.asarray(k_ranges).reshape(-1, 2),
+                                                    np.asarray(mask_types).reshape(-1))):
+        qs, qe, ks, ke, t = int(qs), int(qe), int(ks), int(ke), int(t)
+        if qe <= qs or ke <= ks:
+            continue
+        for qt in range(qs // TILE, -(-qe // TILE)):
+            out[qt].append((qs, qe, ks, ke, t))
+    return out
+
+
+def gather_units(total_q, total_k, q_ranges, k_ranges, mask_types, pair_mode, fvis):
+    """{unit: [(record words, (info0, info1)), ...]} for the gathered units."""
+    n_qt = -(-total_q // TILE)
+    n_units = n_qt if pair_mode == 0 else (n_qt + 1) // 2
+    if total_k > GATHER_MAX_TK:
+        return {}
+    tiles = _tile_slices(total_q, q_ranges, k_ranges, mask_types)
+    out = {}
+    for u in range(n_units):
+        qts = [u] if pair_mode == 0 else [q for q in (2 * u, 2 * u + 1) if q < n_qt]
+        sl = [x for q in qts for x in tiles[q]]
+        if not sl or any(t != 0 or ks % GATHER_KEYS or (ke % GATHER_KEYS and ke != total_k)
+                         for _, _, ks, ke, t in sl):
+            continue
+        blocks = sorted({b for _, _, ks, ke, _ in sl
+                         for b in range(ks // GATHER_KEYS, -(-ke // GATHER_KEYS))})
+        if pair_mode == 0:
+            regular = len(fvis[u])
+        else:  # steps of the two q-tiles' visit lists merged on kt
+            regular = len({kt for q in qts for kt, _ in fvis[q]})
+        n_steps = -(-len(blocks) // GATHER_SLOTS)
+        if len(blocks) > GATHER_MAX_BLOCKS or n_steps >= regular:
+            continue
+        half_tiles = [u, u] if pair_mode == 0 else [2 * u, 2 * u + 1 if 2 * u + 1 < n_qt else -1]
+        res = []
+        for j in range(n_steps):
+            bs = blocks[GATHER_SLOTS * j: GATHER_SLOTS * (j + 1)]
+            rec = [GATHER_KEYS * b for b in bs] + [-GATHER_KEYS] * (GATHER_SLOTS - len(bs))
+            infos = []
+            for qt in half_tiles:
+                words = np.zeros((GATHER_SLOTS, 4), dtype=np.uint32)
+                if qt >= 0:
+                    for slot, b in enumerate(bs):
+                        k0, k1 = GATHER_KEYS * b, GATHER_KEYS * (b + 1)
+                        for qs, qe, ks, ke, _ in tiles[qt]:
+                            if ks < k1 and ke > k0:
+                                for r in range(max(qs, TILE * qt), min(qe, TILE * (qt + 1))):
+                                    rr = r - TILE * qt
+                                    words[slot, rr >> 5] |= np.uint32(1 << (rr & 31))
+                rec += [int(w) for w in words.view(np.int32).reshape(-1)]
+                infos.append(1 if words.any() else -1)
+            res.append((rec, (infos[0], infos[1])))
+        out[u] = res
+    return out

@@ -157,3 +157,59 @@ def test_plan_split_and_order_rules():
                      split_below=-1)
     assert q["fwd_items"].tolist() == [[0, 1, 0, 0, 0, 2, -1, 10]]
     assert q["bwd_items"].tolist() == [[0, 0, 0, 1, 5, 0, 0, 0], [1, 0, 1, 2, 5, 0, 0, 0]]
+
+
+@pytest.mark.parametrize("blocks,seed", [((64, 64), 1), ((64, 8), 2), ((16, 64), 3), ((8, 64), 4),
+                                         ((64, 16), 5), ((128, 128), 6)])
+@pytest.mark.parametrize("heads", [(4, 2), (2, 2)])
+def test_gathered_steps_cover_the_mask_exactly(blocks, seed, heads):
+    """Gathered forward steps (the planner specification for units of full,
+    8-key aligned slices): for every item half, the (row, key) pairs its
+    steps' slot row bits mark are exactly the visible pairs of its q-tile's
+    rows in the dense mask, each once; keys past Tk are never marked, unused
+    slots (start -8) carry no bits, slot starts ascend within a step."""
+    T = 1000  # not a multiple of the tile or of the block sizes
+    wl = W.block_sparse(total=T, hq=heads[0], hkv=heads[1], q_block=blocks[0], k_block=blocks[1],
+                        seed=seed)
+    m = dense.dense_mask(T, T, wl.q_ranges, wl.k_ranges, wl.mask_types).astype(bool)
+    p = planner.plan(T, T, heads[0], heads[1], wl.q_ranges, wl.k_ranges, wl.mask_types,
+                     num_sms=152)
+    steps, rec = p["fwd_steps"], p["gathers"]
+    if blocks == (128, 128):  # tile-aligned blocks: the tile lists are already exact
+        assert rec.shape[0] == 0
+        return
+    assert rec.shape[0] > 0
+    # a (q-tile, head) may be cut into several items (split): sum over them
+    marked_by = {}
+    for it in p["fwd_items"]:
+        for h in range(2):
+            qt, head = it[h], it[2 + h]
+            if qt < 0 or head < 0:
+                continue
+            marked, gathered = marked_by.setdefault((qt, head), [np.zeros((128, T), np.int64), False])
+            for st in steps[it[4]:it[5]]:
+                if st[3] <= 0:
+                    continue
+                r = rec[st[3] - 1]
+                starts = r[:16]
+                assert (np.diff(starts[starts >= 0]) > 0).all() and (starts[starts < 0] == -8).all()
+                words = r[16 + 64 * h: 16 + 64 * (h + 1)].view(np.uint32).reshape(16, 4)
+                assert (st[1 + h] >= 0) == bool(words.any())
+                for slot, y in enumerate(starts):
+                    if y < 0:
+                        assert not words[slot].any()
+                        continue
+                    bits = (words[slot][np.arange(128) >> 5] >> (np.arange(128) & 31)) & 1
+                    for rr in np.nonzero(bits)[0]:
+                        marked[rr, y:min(y + 8, T)] += 1
+                marked_by[(qt, head)][1] = True
+    n_halves = 0
+    for (qt, head), (marked, gathered) in marked_by.items():
+        if not gathered:
+            continue
+        n_halves += 1
+        ref = m[128 * qt: min(128 * qt + 128, T)]
+        got = marked[: ref.shape[0]]
+        assert (got[ref] == 1).all(), "a visible pair is missed or listed twice"
+        assert (got[~ref] == 0).all(), "an invisible pair is marked visible"
+    assert n_halves > 0
