@@ -600,7 +600,8 @@ struct DqParams {
   int n_items;
   const Slice* slices;
   const int* masks;  // slice lists of multi-slice visits
-  int Tq, Hq, g, qpad;
+  const int* gathers;  // gathered step records
+  int Tq, Tk, Hq, g, qpad;
   float scale, scale_log2;
   const float* nlse2;
   const float* ndelta;
@@ -652,7 +653,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     ffa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_do, const DqParams P) {
+                      const __grid_constant__ CUtensorMap tm_do,
+                      const __grid_constant__ CUtensorMap tm_k8,
+                      const __grid_constant__ CUtensorMap tm_v8, const DqParams P) {
   using C = DqCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
@@ -711,6 +714,25 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_do);
+      prefetch_tmap(&tm_k8);
+      prefetch_tmap(&tm_v8);
+      // One K or V tile: the k-tile's rows, or a gathered step's 16 blocks of
+      // 8 rows (8-row boxes at 1024-byte aligned slots; unused slots read zeros).
+      auto load_kv = [&](uint32_t dst, const CUtensorMap* m, const CUtensorMap* m8, uint32_t b,
+                         int hk, const int4& stp) {
+        if (stp.w > 0) {
+          const int* rec = P.gathers + (size_t)(stp.w - 1) * kGatherWords;
+#pragma unroll 1
+          for (int sl = 0; sl < kGatherSlots; ++sl) {
+            const int y = rec[sl];
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_2d(dst + c * 16384 + sl * 1024, m8, b, hk * D + c * 64, y);
+          }
+        } else {
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_2d(dst + c * 16384, m, b, hk * D + c * 64, stp.x * 128);
+        }
+      };
       uint32_t kv_cnt = 0, q_cnt = 0;
       bool ok = true, k_only = false;
       for (int r = 0; ok; ++r) {
@@ -741,16 +763,14 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
             const uint32_t kph = (kv_cnt / C::kKStages) & 1, vph = (kv_cnt / C::kVStages) & 1;
             if (!(ok = mbar_wait(bar(C::kBKEmpty + ks), kph ^ 1, ctl, 801))) break;
             mbar_arrive_expect_tx(bar(C::kBKFull + ks), C::kTileBytes);
-            for (int c = 0; c < C::kChunks; ++c)
-              tma_load_2d(sbase + C::kKOff + ks * C::kTileBytes + c * 16384, &tm_k,
-                          bar(C::kBKFull + ks), hk * D + c * 64, st.x * 128);
+            load_kv(sbase + C::kKOff + ks * C::kTileBytes, &tm_k, &tm_k8, bar(C::kBKFull + ks), hk,
+                    st);
             k_only = true;
             if (!(ok = mbar_wait(bar(C::kBVEmpty + vs), vph ^ 1, ctl, 802))) break;
             k_only = false;
             mbar_arrive_expect_tx(bar(C::kBVFull + vs), C::kTileBytes);
-            for (int c = 0; c < C::kChunks; ++c)
-              tma_load_2d(sbase + C::kVOff + vs * C::kTileBytes + c * 16384, &tm_v,
-                          bar(C::kBVFull + vs), hk * D + c * 64, st.x * 128);
+            load_kv(sbase + C::kVOff + vs * C::kTileBytes, &tm_v, &tm_v8, bar(C::kBVFull + vs), hk,
+                    st);
             ++kv_cnt;
           }
         }
@@ -901,7 +921,12 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           tc_fence_before();
           mbar_arrive(bar(C::kBDpFree));
           uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
-          if (info & 1) step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
+          if (info & 1) {
+            if (st.w > 0)
+              gather_mask(P.gathers + (size_t)(st.w - 1) * kGatherWords, h, t, P.Tk, vb);
+            else
+              step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
+          }
           const uint32_t m_lo = wg ? vb[2] : vb[0], m_hi = wg ? vb[3] : vb[1];
           const uint32_t tSb = tmem + lane_addr + C::kTS0 + 128 * (v & 1) + 64 * wg;
 #pragma unroll
@@ -1098,9 +1123,11 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
       if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
     }
   }
-  alignas(64) CUtensorMap tq, tk, tv, tdo;
+  alignas(64) CUtensorMap tq, tk, tv, tdo, tk8, tv8;
   if (!encode_tile_map(&tq, q, p->Tq, p->Hq * D) || !encode_tile_map(&tk, k, p->Tk, p->Hkv * D) ||
-      !encode_tile_map(&tv, v, p->Tk, p->Hkv * D) || !encode_tile_map(&tdo, dout, p->Tq, p->Hq * D))
+      !encode_tile_map(&tv, v, p->Tk, p->Hkv * D) || !encode_tile_map(&tdo, dout, p->Tq, p->Hq * D) ||
+      !encode_tile_map(&tk8, k, p->Tk, p->Hkv * D, kGatherKeys) ||
+      !encode_tile_map(&tv8, v, p->Tk, p->Hkv * D, kGatherKeys))
     return FFA_ERR_INVALID_ARG;
   const float scale_log2 = scale * kLog2e;
   {
@@ -1147,7 +1174,9 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     P.n_items = (int)p->n_dq_items;
     P.slices = p->slices;
     P.masks = p->fwd_masks;
+    P.gathers = p->gathers;
     P.Tq = p->Tq;
+    P.Tk = p->Tk;
     P.Hq = p->Hq;
     P.g = p->Hq / p->Hkv;
     P.qpad = qpad;
@@ -1165,7 +1194,8 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     if (!split_regs_ok<ffa_bwd_dq_kernel<D, kCap>>()) return FFA_ERR_UNSUPPORTED;
     if (cudaMemsetAsync(P.ticket, 0, sizeof(int), st) != cudaSuccess) return FFA_ERR_CUDA;
     record_phase(p, 4, st);
-    ffa_bwd_dq_kernel<D, kCap><<<p->grid_dq, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, P);
+    ffa_bwd_dq_kernel<D, kCap><<<p->grid_dq, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo,
+                                                                                tk8, tv8, P);
     note_launches(1);
     if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   }

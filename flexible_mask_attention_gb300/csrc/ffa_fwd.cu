@@ -83,7 +83,8 @@ struct FwdParams {
   int n_items;
   const Slice* slices;
   const int* masks;  // slice lists of multi-slice visits
-  int Tq, Hq, g;
+  const int* gathers;  // gathered step records
+  int Tq, Tk, Hq, g;
   float scale_log2;
   __nv_bfloat16* out;
   float* lse;
@@ -203,7 +204,8 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 template <int D, bool kCap>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     ffa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const FwdParams P) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_k8,
+                   const __grid_constant__ CUtensorMap tm_v8, const FwdParams P) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -257,6 +259,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_k8);
+      prefetch_tmap(&tm_v8);
+      // One K or V tile into `dst`: the k-tile's 128 rows, or for a gathered
+      // step 16 blocks of 8 rows (each an 8-row box filling one 1024-byte
+      // swizzle atom; unused slots start at row -8 and read zeros).
+      auto load_kv = [&](uint32_t dst, const CUtensorMap* m, const CUtensorMap* m8, uint32_t b,
+                         int hk, const int4& stp) {
+        if (stp.w > 0) {
+          const int* rec = P.gathers + (size_t)(stp.w - 1) * kGatherWords;
+#pragma unroll 1
+          for (int sl = 0; sl < kGatherSlots; ++sl) {
+            const int y = rec[sl];
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_2d(dst + c * 16384 + sl * 1024, m8, b, hk * D + c * 64, y);
+          }
+        } else {
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_2d(dst + c * 16384, m, b, hk * D + c * 64, stp.x * 128);
+        }
+      };
       uint32_t kv_cnt = 0, q_cnt = 0;
       bool ok = true, k_only = false;  // k_only: K of step kv_cnt issued, its V not yet
       for (int r = 0; ok; ++r) {
@@ -279,21 +301,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         it[kFiH1] * D + c * 64, it[kFiQt1] * 128);
         ++q_cnt;
         for (int j = sb; j < se; ++j) {
-          const int kt = P.steps[j].x;
+          const int4 stp = P.steps[j];
           const int stage = kv_cnt % C::kStages;
           const uint32_t ph = (kv_cnt / C::kStages) & 1;
           if (!(ok = mbar_wait(bar(C::kBKEmpty + stage), ph ^ 1, ctl, 101))) break;
           mbar_arrive_expect_tx(bar(C::kBKFull + stage), C::kTileBytes);
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_2d(sbase + C::kKOff + stage * C::kTileBytes + c * 16384, &tm_k,
-                        bar(C::kBKFull + stage), hk * D + c * 64, kt * 128);
+          load_kv(sbase + C::kKOff + stage * C::kTileBytes, &tm_k, &tm_k8, bar(C::kBKFull + stage),
+                  hk, stp);
           k_only = true;
           if (!(ok = mbar_wait(bar(C::kBVEmpty + stage), ph ^ 1, ctl, 102))) break;
           k_only = false;
           mbar_arrive_expect_tx(bar(C::kBVFull + stage), C::kTileBytes);
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_2d(sbase + C::kVOff + stage * C::kTileBytes + c * 16384, &tm_v,
-                        bar(C::kBVFull + stage), hk * D + c * 64, kt * 128);
+          load_kv(sbase + C::kVOff + stage * C::kTileBytes, &tm_v, &tm_v8, bar(C::kBVFull + stage),
+                  hk, stp);
           ++kv_cnt;
         }
       }
@@ -468,8 +488,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const bool lo_in_range = -mn <= P.cap.smax;
         uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
         if (info & 1) {
-          // PARTIAL step: keep the keys this row sees under the step's slice(s).
-          step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
+          // PARTIAL (or gathered) step: keep the keys this row sees.
+          if (st.w > 0)
+            gather_mask(P.gathers + (size_t)(st.w - 1) * kGatherWords, h, row_in, P.Tk, vb);
+          else
+            step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (!mask_bit(vb, c)) u[c] = 0xff800000u;  // -inf
@@ -654,9 +677,11 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
                           void* out, float* lse, void* ws, cudaStream_t st, const SinkArgs& sk,
                           float softcap) {
   using C = FwdCfg<D>;
-  alignas(64) CUtensorMap tq, tk, tv;
+  alignas(64) CUtensorMap tq, tk, tv, tk8, tv8;
   if (!encode_tile_map(&tq, q, p->Tq, p->Hq * D) || !encode_tile_map(&tk, k, p->Tk, p->Hkv * D) ||
-      !encode_tile_map(&tv, v, p->Tk, p->Hkv * D))
+      !encode_tile_map(&tv, v, p->Tk, p->Hkv * D) ||
+      !encode_tile_map(&tk8, k, p->Tk, p->Hkv * D, kGatherKeys) ||
+      !encode_tile_map(&tv8, v, p->Tk, p->Hkv * D, kGatherKeys))
     return FFA_ERR_INVALID_ARG;
   FwdParams P;
   P.steps = p->fwd_steps;
@@ -666,7 +691,9 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   P.n_items = (int)p->n_fwd_items;
   P.slices = p->slices;
   P.masks = p->fwd_masks;
+  P.gathers = p->gathers;
   P.Tq = p->Tq;
+  P.Tk = p->Tk;
   P.Hq = p->Hq;
   P.g = p->Hq / p->Hkv;
   P.scale_log2 = scale * kLog2e;
@@ -686,7 +713,8 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   if (!split_regs_ok<ffa_fwd_kernel<D, kCap>>()) return FFA_ERR_UNSUPPORTED;
   if (cudaMemsetAsync(P.ticket, 0, sizeof(int), st) != cudaSuccess) return FFA_ERR_CUDA;
   record_phase(p, 0, st);
-  ffa_fwd_kernel<D, kCap><<<p->grid_fwd, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, P);
+  ffa_fwd_kernel<D, kCap><<<p->grid_fwd, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, tk8, tv8,
+                                                                             P);
   note_launches(1);
   if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   if (p->n_merges > 0) {

@@ -25,6 +25,18 @@ __host__ __device__ constexpr int visit_info(int slice, bool partial) {
 }
 __host__ __device__ constexpr int visit_list_info(int m) { return (m << 2) | 3; }
 
+// Gathered forward steps (step.w = r + 1 > 0; x unused): for units whose
+// slices are all FULL with 8-key aligned key ranges, the 8-key blocks any of
+// their rows sees are packed 16 to a K/V tile.  Record r (kGatherWords
+// int32): kGatherSlots block start keys (-kGatherKeys for an unused slot,
+// loaded as zero-filled rows), then per half kGatherSlots x 4 words of row
+// bits (bit i of word w: row 32w + i of the half's q-tile sees the slot).
+constexpr int kGatherKeys = 8;
+constexpr int kGatherSlots = 16;
+constexpr int kGatherWords = kGatherSlots + 2 * kGatherSlots * 4;
+constexpr int kGatherMaxBlocks = 2048;  // 8-key blocks per gathered unit
+constexpr int kGatherMaxTk = 1 << 19;   // key count up to which units may gather
+
 #ifdef __CUDACC__
 // Adds [lo, hi) (tile-local, any range) to a 128-bit mask of tile columns.
 __device__ __forceinline__ void add_window(int lo, int hi, uint32_t (&b)[4]) {
@@ -82,6 +94,23 @@ __device__ __forceinline__ void step_mask(int info, const Slice* __restrict__ sl
   }
 }
 
+// Visible columns of a gathered step for query row `row_in` of half h: slot s
+// holds keys [start_s, start_s + 8) in columns [8s, 8s + 8); the columns of a
+// slot are set when the row's bit is set, keys at or past Tk never.
+__device__ __forceinline__ void gather_mask(const int* __restrict__ rec, int h, int row_in,
+                                            int Tk, uint32_t (&b)[4]) {
+  b[0] = b[1] = b[2] = b[3] = 0u;
+  const int* rows = rec + kGatherSlots + h * kGatherSlots * 4 + (row_in >> 5);
+#pragma unroll
+  for (int s = 0; s < kGatherSlots; ++s) {
+    const int y = rec[s];
+    if (y >= 0 && ((rows[4 * s] >> (row_in & 31)) & 1)) {
+      const int valid = min(kGatherKeys, Tk - y);
+      b[s >> 2] |= ((1u << valid) - 1u) << (kGatherKeys * (s & 3));
+    }
+  }
+}
+
 __device__ __forceinline__ bool mask_bit(const uint32_t (&b)[4], int c) {
   return (b[c >> 5] >> (c & 31)) & 1u;
 }
@@ -128,6 +157,8 @@ struct ffa_plan_s {
   int n_slots = 0;  // partial-result slots (split forward items)
   int* fwd_masks = nullptr;  // slice lists of multi-slice forward visits
   int64_t n_fwd_masks = 0;
+  int* gathers = nullptr;  // gathered step records [n_gathers][kGatherWords]
+  int64_t n_gathers = 0;
   int4* bwd_steps = nullptr;
   int64_t n_bwd_steps = 0;
   int* bwd_masks = nullptr;  // slice lists of multi-slice backward visits
@@ -225,7 +256,9 @@ inline CapConsts make_cap_consts(float scale, float c) {
 size_t bwd_workspace_bytes(const ffa_plan_s* p);
 // Implemented in ffa_plan.cu.
 bool on_plan_device(const ffa_plan_s* p);  // current device == the plan's device
-bool encode_tile_map(void* map128, const void* base, int rows, int cols_elems);
+// box_rows: 128 for whole tiles, kGatherKeys for the slots of gathered steps.
+bool encode_tile_map(void* map128, const void* base, int rows, int cols_elems,
+                     int box_rows = 128);
 void note_launches(int n);  // adds to the count reported by ffa_kernel_launch_count
 // Records phase event i of the plan on `st` when the caller asked for them.
 inline void record_phase(const ffa_plan_s* p, int i, cudaStream_t st) {

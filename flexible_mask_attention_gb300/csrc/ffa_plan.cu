@@ -336,9 +336,10 @@ __global__ void k_fwd_unit_count(const int2* __restrict__ visits, const int* __r
 
 __global__ void k_fwd_unit_fill(const int2* __restrict__ visits, const int* __restrict__ voff,
                                 const int* __restrict__ vcnt, int n_qt, int n_units,
-                                int pair_mode, const int* __restrict__ soff, int4* steps) {
+                                int pair_mode, const int* __restrict__ soff,
+                                const int* __restrict__ gcnt, int4* steps) {
   const int u = blockIdx.x * blockDim.x + threadIdx.x;
-  if (u >= n_units) return;
+  if (u >= n_units || gcnt[u] > 0) return;  // gathered units are filled by k_gather_fill
   int4* o = steps + soff[u];
   if (pair_mode == 0) {
     const int2* a = visits + voff[u];
@@ -482,6 +483,208 @@ __global__ void k_dq_counts(const int* __restrict__ items, int n_items,
   }
   counts[2 * i] = n0;
   counts[2 * i + 1] = n1;
+}
+
+// ---- gathered forward units -------------------------------------------------
+// One block per forward unit.  A unit gathers when every slice of its q-tiles'
+// lists is FULL with ks and ke multiples of kGatherKeys (ke may be Tk), it
+// covers 1 .. kGatherMaxBlocks blocks of kGatherKeys keys, and ceil(blocks /
+// kGatherSlots) gathered steps are fewer than its regular steps.  The blocks
+// are collected in a shared-memory bitmap (order-free, so deterministic).
+constexpr int kGatherThreads = 256;
+constexpr int kGatherBitmapWords = kGatherMaxTk / kGatherKeys / 32;
+
+struct GatherUnit {
+  int qt[2];  // q-tile of each half (-1: none)
+  int n_qt;   // distinct q-tiles (1 or 2)
+};
+
+__device__ __forceinline__ GatherUnit gather_unit(int u, int pair_mode, int n_qt) {
+  GatherUnit g;
+  if (pair_mode == 0) {
+    g.qt[0] = g.qt[1] = u;
+    g.n_qt = 1;
+  } else {
+    g.qt[0] = 2 * u;
+    g.qt[1] = 2 * u + 1 < n_qt ? 2 * u + 1 : -1;
+    g.n_qt = g.qt[1] >= 0 ? 2 : 1;
+  }
+  return g;
+}
+
+// Marks the unit's blocks in `bits` (cleared here); returns false (for the
+// whole block) if a slice is not eligible.
+__device__ bool gather_bitmap(const Slice* __restrict__ sl, const int* __restrict__ list,
+                              const int* __restrict__ loff, const int* __restrict__ lcnt,
+                              const GatherUnit& gu, int Tk, unsigned* bits) {
+  const int nwords = (((Tk + kGatherKeys - 1) / kGatherKeys) + 31) / 32;
+  for (int w = threadIdx.x; w < nwords; w += blockDim.x) bits[w] = 0u;
+  __syncthreads();
+  bool bad = false;
+  for (int t = 0; t < gu.n_qt; ++t) {
+    const int* L = list + loff[gu.qt[t]];
+    const int n = lcnt[gu.qt[t]];
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const Slice x = sl[L[i]];
+      if (x.t != 0 || x.ks % kGatherKeys != 0 || (x.ke % kGatherKeys != 0 && x.ke != Tk)) {
+        bad = true;
+        continue;
+      }
+      const int b0 = x.ks / kGatherKeys, b1 = (x.ke + kGatherKeys - 1) / kGatherKeys;
+      for (int w = b0 >> 5; w <= (b1 - 1) >> 5; ++w) {
+        const int lo = max(b0 - 32 * w, 0), hi = min(b1 - 32 * w, 32);
+        const unsigned m = (hi == 32 ? 0xffffffffu : ((1u << hi) - 1u)) & ~((1u << lo) - 1u);
+        atomicOr(&bits[w], m);
+      }
+    }
+  }
+  return !__syncthreads_or(bad);
+}
+
+// Number of set bits in bits[0, nwords) (block-wide; every thread gets it).
+__device__ int block_popc(const unsigned* bits, int nwords, int* red) {
+  int c = 0;
+  for (int w = threadIdx.x; w < nwords; w += blockDim.x) c += __popc(bits[w]);
+  for (int d = 16; d > 0; d >>= 1) c += __shfl_xor_sync(0xffffffffu, c, d);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = c;
+  __syncthreads();
+  int tot = 0;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += red[i];
+  __syncthreads();
+  return tot;
+}
+
+// gcnt[u] = gathered steps of unit u (0: regular); scnt[u] is replaced by
+// it for gathered units.  scnt holds the regular step counts on entry.
+__global__ void __launch_bounds__(kGatherThreads)
+    k_gather_count(const Slice* __restrict__ sl, const int* __restrict__ list,
+                   const int* __restrict__ loff, const int* __restrict__ lcnt, int n_qt,
+                   int pair_mode, int Tk, int* __restrict__ scnt, int* __restrict__ gcnt) {
+  __shared__ unsigned bits[kGatherBitmapWords];
+  __shared__ int red[kGatherThreads / 32];
+  const int u = blockIdx.x;
+  const GatherUnit gu = gather_unit(u, pair_mode, n_qt);
+  const bool ok = gather_bitmap(sl, list, loff, lcnt, gu, Tk, bits);
+  const int nwords = (((Tk + kGatherKeys - 1) / kGatherKeys) + 31) / 32;
+  const int n = ok ? block_popc(bits, nwords, red) : 0;
+  const int steps = (n + kGatherSlots - 1) / kGatherSlots;
+  const bool gather = ok && n > 0 && n <= kGatherMaxBlocks && steps < scnt[u];
+  if (threadIdx.x == 0) {
+    gcnt[u] = gather ? steps : 0;
+    if (gather) scnt[u] = steps;
+  }
+}
+
+// Steps, records and half costs of the gathered units.  Dynamic shared
+// memory: the bitmap, per-word bit offsets, block starts and per-half row
+// masks of up to kGatherMaxBlocks blocks.
+constexpr size_t kGatherFillSmem =
+    sizeof(unsigned) * kGatherBitmapWords + sizeof(int) * kGatherBitmapWords +
+    sizeof(int) * kGatherMaxBlocks + sizeof(unsigned) * 2 * kGatherMaxBlocks * 4;
+
+__global__ void __launch_bounds__(kGatherThreads)
+    k_gather_fill(const Slice* __restrict__ sl, const int* __restrict__ list,
+                  const int* __restrict__ loff, const int* __restrict__ lcnt, int n_qt,
+                  int pair_mode, int Tk, const int* __restrict__ gcnt,
+                  const int* __restrict__ goff, const int* __restrict__ soff, int4* steps,
+                  int* __restrict__ records, int* __restrict__ cost_half) {
+  extern __shared__ unsigned gsm[];
+  unsigned* bits = gsm;
+  int* woff = reinterpret_cast<int*>(bits + kGatherBitmapWords);
+  int* start = woff + kGatherBitmapWords;
+  unsigned* rmask = reinterpret_cast<unsigned*>(start + kGatherMaxBlocks);  // [2][blocks][4]
+  __shared__ int red[kGatherThreads / 32];
+  __shared__ int cost[2];
+  const int u = blockIdx.x;
+  const int n_steps = gcnt[u];
+  if (n_steps == 0) return;  // whole block
+  const GatherUnit gu = gather_unit(u, pair_mode, n_qt);
+  gather_bitmap(sl, list, loff, lcnt, gu, Tk, bits);
+  const int nwords = (((Tk + kGatherKeys - 1) / kGatherKeys) + 31) / 32;
+  // exclusive prefix of the words' bit counts (one thread per chunk of words)
+  {
+    const int per = (nwords + blockDim.x - 1) / blockDim.x;
+    const int w0 = threadIdx.x * per, w1 = min(nwords, w0 + per);
+    int c = 0;
+    for (int w = w0; w < w1; ++w) c += __popc(bits[w]);
+    int incl = c;  // inclusive scan over the block's threads, by warps
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += y;
+    }
+    if (lane == 31) red[wid] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int i = 0; i < wid; ++i) base += red[i];
+    int run = base + incl - c;
+    for (int w = w0; w < w1; ++w) {
+      woff[w] = run;
+      run += __popc(bits[w]);
+    }
+  }
+  const int n = n_steps * kGatherSlots;  // slots including unused ones
+  for (int i = threadIdx.x; i < n; i += blockDim.x) start[i] = -kGatherKeys;
+  for (int i = threadIdx.x; i < 2 * n * 4; i += blockDim.x) rmask[i] = 0u;
+  __syncthreads();
+  for (int w = threadIdx.x; w < nwords; w += blockDim.x) {
+    unsigned m = bits[w];
+    int pos = woff[w];
+    while (m) {
+      const int b = 32 * w + __ffs(m) - 1;
+      start[pos++] = b * kGatherKeys;
+      m &= m - 1u;
+    }
+  }
+  // row bits: each slice marks its rows of the half's q-tile on its blocks
+  for (int h = 0; h < 2; ++h) {
+    const int qt = gu.qt[h];
+    if (qt < 0 || (h == 1 && pair_mode == 0)) continue;
+    const int* L = list + loff[qt];
+    const int cnt = lcnt[qt];
+    for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
+      const Slice x = sl[L[i]];
+      uint32_t rb[4] = {0u, 0u, 0u, 0u};
+      add_window(max(x.qs, 128 * qt) - 128 * qt, min(x.qe, 128 * qt + 128) - 128 * qt, rb);
+      const int b0 = x.ks / kGatherKeys, b1 = (x.ke + kGatherKeys - 1) / kGatherKeys;
+      for (int b = b0; b < b1; ++b) {
+        const int w = b >> 5;
+        const int pos = woff[w] + __popc(bits[w] & ((1u << (b & 31)) - 1u));
+        for (int k = 0; k < 4; ++k)
+          if (rb[k]) atomicOr(&rmask[(h * n + pos) * 4 + k], rb[k]);
+      }
+    }
+  }
+  if (threadIdx.x < 2) cost[threadIdx.x] = 0;
+  __syncthreads();
+  if (pair_mode == 0)  // both halves are the same q-tile (two heads)
+    for (int i = threadIdx.x; i < n * 4; i += blockDim.x) rmask[n * 4 + i] = rmask[i];
+  __syncthreads();
+  const int r0 = goff[u], s0 = soff[u];
+  for (int i = threadIdx.x; i < n_steps * kGatherWords; i += blockDim.x) {
+    const int j = i / kGatherWords, o = i % kGatherWords;
+    int v;
+    if (o < kGatherSlots) {
+      v = start[j * kGatherSlots + o];
+    } else {
+      const int h = (o - kGatherSlots) / (kGatherSlots * 4);
+      const int rem = (o - kGatherSlots) % (kGatherSlots * 4);
+      v = (int)rmask[(h * n + j * kGatherSlots + rem / 4) * 4 + rem % 4];
+    }
+    records[(size_t)(r0 + j) * kGatherWords + o] = v;
+  }
+  for (int j = threadIdx.x; j < n_steps; j += blockDim.x) {
+    int info[2];
+    for (int h = 0; h < 2; ++h) {
+      unsigned any = 0u;
+      for (int k = 0; k < kGatherSlots * 4; ++k) any |= rmask[(h * n + j * kGatherSlots) * 4 + k];
+      info[h] = any ? 1 : -1;
+      if (any) atomicAdd(&cost[h], kPartialCost);
+    }
+    steps[s0 + j] = make_int4(0, info[0], info[1], r0 + j + 1);
+  }
+  __syncthreads();
+  if (threadIdx.x < 2) cost_half[2 * u + threadIdx.x] = cost[threadIdx.x];
 }
 
 // ---- ordering ---------------------------------------------------------------
@@ -663,7 +866,7 @@ void free_plan(ffa_plan_s* p) {
   if (!p) return;
   void* bufs[] = {p->slices, p->fwd_steps, p->fwd_items, p->fwd_order, p->merges,
                   p->bwd_steps, p->bwd_items, p->bwd_order, p->err, p->fwd_masks,
-                  p->bwd_masks, p->dq_counts, p->tickets};
+                  p->bwd_masks, p->dq_counts, p->tickets, p->gathers};
   for (void* b : bufs)
     if (b) cudaFree(b);
   if (!p->dq_alias) {
@@ -791,16 +994,46 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
                                                            cost_half.as<int>());
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
-  rc = scan(scnt.as<int>(), n_units, soff.as<int>(), dtot, &tot, st);
-  if (rc != FFA_OK) return rc;
+  // gathered units (full, 8-key aligned slices): their step counts replace
+  // the regular ones before the step offsets are scanned
+  DevBuf gcnt(st), goff(st);
+  FFA_CUDA(gcnt.alloc(sizeof(int) * n_units));
+  FFA_CUDA(goff.alloc(sizeof(int) * n_units));
+  FFA_CUDA(cudaMemsetAsync(gcnt.p, 0, sizeof(int) * n_units, st));
+  if (p->Tk <= kGatherMaxTk && n_units > 0) {
+    k_gather_count<<<n_units, kGatherThreads, 0, st>>>(p->slices, qlist.as<int>(), qloff.as<int>(),
+                                                       qlcnt.as<int>(), n_qt, pair_mode, p->Tk,
+                                                       scnt.as<int>(), gcnt.as<int>());
+    note_launches(1);
+    FFA_CUDA(cudaGetLastError());
+  }
+  long long sg[2];  // steps, gathered records
+  if ((rc = scan_launch(scnt.as<int>(), n_units, soff.as<int>(), dtot, st))) return rc;
+  if ((rc = scan_launch(gcnt.as<int>(), n_units, goff.as<int>(), dtot + 1, st))) return rc;
+  if ((rc = read_to_host(sg, dtot, sizeof sg, st))) return rc;
+  tot = sg[0];
+  if (tot > 0x7fffffffLL || sg[1] > (1LL << 24)) return FFA_ERR_UNSUPPORTED;
   p->n_fwd_steps = tot;
+  p->n_gathers = sg[1];
   FFA_CUDA(steps.alloc(sizeof(int4) * (size_t)tot));
+  FFA_CUDA(cudaMallocAsync(&p->gathers,
+                           sizeof(int) * kGatherWords * (size_t)std::max(1LL, sg[1]), st));
   k_fwd_unit_fill<<<grid_for(n_units, 128), 128, 0, st>>>(visits.as<int2>(), voff.as<int>(),
                                                           vcnt.as<int>(), n_qt, n_units,
                                                           pair_mode, soff.as<int>(),
-                                                          steps.as<int4>());
+                                                          gcnt.as<int>(), steps.as<int4>());
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
+  if (sg[1] > 0) {
+    FFA_CUDA(cudaFuncSetAttribute(k_gather_fill, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kGatherFillSmem));
+    k_gather_fill<<<n_units, kGatherThreads, kGatherFillSmem, st>>>(
+        p->slices, qlist.as<int>(), qloff.as<int>(), qlcnt.as<int>(), n_qt, pair_mode, p->Tk,
+        gcnt.as<int>(), goff.as<int>(), soff.as<int>(), steps.as<int4>(), p->gathers,
+        cost_half.as<int>());
+    note_launches(1);
+    FFA_CUDA(cudaGetLastError());
+  }
   // forward items
   const int pairs = (g + 1) / 2;
   const long long n_items = pair_mode == 0 ? (long long)n_units * p->Hkv * pairs
@@ -972,13 +1205,15 @@ void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_
 uint64_t g_launches_total() { return g_launches.load(std::memory_order_relaxed); }
 
 // 2-D tensor map over a row-major [rows][cols] bf16 matrix: boxes of
-// 128 rows x 64 columns (128 bytes), 128-byte swizzle, zero fill outside.
-bool encode_tile_map(void* map128, const void* base, int rows, int cols_elems) {
+// box_rows rows x 64 columns (128 bytes), 128-byte swizzle, zero fill outside.
+// An 8-row box fills exactly one 1024-byte swizzle atom, so boxes written at
+// 1024-byte aligned offsets of a tile lay out rows as one 128-row box would.
+bool encode_tile_map(void* map128, const void* base, int rows, int cols_elems, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols_elems, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)cols_elems * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(static_cast<CUtensorMap*>(map128), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                   const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1058,6 +1293,7 @@ ffa_status_t ffa_plan_info(ffa_plan_t p, ffa_plan_info_t* info) {
   info->area = p->area;
   info->fwd_masks = p->n_fwd_masks;
   info->bwd_masks = p->n_bwd_masks;
+  info->gathers = p->n_gathers;
   return FFA_OK;
 }
 
@@ -1077,6 +1313,7 @@ ffa_status_t ffa_plan_export(ffa_plan_t p, int32_t which, int32_t* dst, int64_t 
     case 6: src = p->merges; words = kMgWords * p->n_merges; break;
     case 7: src = p->fwd_masks; words = p->n_fwd_masks; break;
     case 8: src = p->bwd_masks; words = p->n_bwd_masks; break;
+    case 9: src = p->gathers; words = kGatherWords * p->n_gathers; break;
     default: return FFA_ERR_INVALID_ARG;
   }
   *written = words;

@@ -105,17 +105,26 @@ typedef struct {
   int64_t area;       /* visible (q, k) pairs per head: sum over rows of |keys seen| */
   int64_t fwd_masks;  /* words of the forward slice lists (multi-slice visits) */
   int64_t bwd_masks;  /* words of the backward slice lists */
+  int64_t gathers;    /* gathered forward step records, 144 words each */
 } ffa_plan_info_t;
 
 ffa_status_t ffa_plan_info(ffa_plan_t plan, ffa_plan_info_t* info);
 
 /* Copy one work list to HOST memory (used to check the planner bit for bit).
  *   which: 0 fwd steps, 1 fwd items, 2 fwd order, 3 bwd steps, 4 bwd items,
- *          5 bwd order, 6 merge groups, 7 fwd slice lists, 8 bwd slice lists.
+ *          5 bwd order, 6 merge groups, 7 fwd slice lists, 8 bwd slice lists,
+ *          9 gathered step records.
  *   A step's visit info is (s << 2) | partial when one slice s sees the tile
  *   pair, or (m << 2) | 3 when several do; then list[m] = n and list[m+1 ..
  *   m+n] are their slice indices, ascending (the tile is computed once and
  *   masked by the union of their windows).
+ *   Gathered forward steps (a forward unit whose slices are all FULL with key
+ *   ranges aligned to 8 keys, when that takes fewer steps than its tiles):
+ *   step (0, info0, info1, r + 1) computes 16 blocks of 8 keys packed into
+ *   one K/V tile; record r holds the 16 block start keys (-8: unused slot),
+ *   then for each half 16 x 4 words of row bits (bit i of word w: row
+ *   32 w + i of the half's q-tile sees that block); info_h is 1 when half h
+ *   has a row bit set, else -1.
  *   dst: host int32 buffer of `capacity` words; *written receives the count.
  * Synchronises the plan's stream. */
 ffa_status_t ffa_plan_export(ffa_plan_t plan, int32_t which, int32_t* dst, int64_t capacity,
