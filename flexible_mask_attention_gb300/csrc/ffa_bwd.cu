@@ -718,19 +718,28 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       prefetch_tmap(&tm_v8);
       // One K or V tile: the k-tile's rows, or a gathered step's 16 blocks of
       // 8 rows (8-row boxes at 1024-byte aligned slots; unused slots read zeros).
+      // ys: the step's 16 slot start rows, read once per step (4 x 16 bytes).
       auto load_kv = [&](uint32_t dst, const CUtensorMap* m, const CUtensorMap* m8, uint32_t b,
-                         int hk, const int4& stp) {
+                         int hk, const int4& stp, const int4 (&ys)[4]) {
         if (stp.w > 0) {
-          const int* rec = P.gathers + (size_t)(stp.w - 1) * kGatherWords;
-#pragma unroll 1
-          for (int sl = 0; sl < kGatherSlots; ++sl) {
-            const int y = rec[sl];
-            for (int c = 0; c < C::kChunks; ++c)
-              tma_load_2d(dst + c * 16384 + sl * 1024, m8, b, hk * D + c * 64, y);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int y4[4] = {ys[q4].x, ys[q4].y, ys[q4].z, ys[q4].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              for (int c = 0; c < C::kChunks; ++c)
+                tma_load_2d(dst + c * 16384 + (4 * q4 + e) * 1024, m8, b, hk * D + c * 64, y4[e]);
           }
         } else {
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_2d(dst + c * 16384, m, b, hk * D + c * 64, stp.x * 128);
+        }
+      };
+      auto slot_rows = [&](const int4& stp, int4 (&ys)[4]) {
+        if (stp.w > 0) {
+          const int4* r4 = reinterpret_cast<const int4*>(P.gathers + (size_t)(stp.w - 1) * kGatherWords);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) ys[q4] = r4[q4];
         }
       };
       uint32_t kv_cnt = 0, q_cnt = 0;
@@ -759,18 +768,20 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           for (int j = sb; j < se; ++j) {
             const int4 st = P.steps[j];
             if (half_info(st, h) < 0) continue;
+            int4 ys[4];
+            slot_rows(st, ys);  // in flight while the ring slots are awaited
             const int ks = kv_cnt % C::kKStages, vs = kv_cnt % C::kVStages;
             const uint32_t kph = (kv_cnt / C::kKStages) & 1, vph = (kv_cnt / C::kVStages) & 1;
             if (!(ok = mbar_wait(bar(C::kBKEmpty + ks), kph ^ 1, ctl, 801))) break;
             mbar_arrive_expect_tx(bar(C::kBKFull + ks), C::kTileBytes);
             load_kv(sbase + C::kKOff + ks * C::kTileBytes, &tm_k, &tm_k8, bar(C::kBKFull + ks), hk,
-                    st);
+                    st, ys);
             k_only = true;
             if (!(ok = mbar_wait(bar(C::kBVEmpty + vs), vph ^ 1, ctl, 802))) break;
             k_only = false;
             mbar_arrive_expect_tx(bar(C::kBVFull + vs), C::kTileBytes);
             load_kv(sbase + C::kVOff + vs * C::kTileBytes, &tm_v, &tm_v8, bar(C::kBVFull + vs), hk,
-                    st);
+                    st, ys);
             ++kv_cnt;
           }
         }

@@ -188,9 +188,13 @@ __global__ void k_scan(const int* __restrict__ in, int n, int* __restrict__ out,
 // list [n, s_0 .. s_n-1] in `masks`.  Warp scans of the per-position counts
 // place visits and list entries, so the output never depends on scheduling.
 // Count mode (kCount) only stores the tile's visit and list-word totals.
-// Tiles with more than kMaxLocalSegs runs re-read the slice list for every
-// position instead of shared memory.
+// Tiles with more than kMaxLocalSegs runs over at most kSweepPositions
+// positions are swept instead: one pass over the slice list counts each
+// position's runs in shared memory, a second places the slice lists.  Other
+// tiles with more than kMaxLocalSegs runs re-read the slice list for every
+// position.
 constexpr int kFillWarps = 4;
+constexpr int kSweepPositions = 256;
 
 template <bool kFwd, bool kCount>
 __global__ void __launch_bounds__(32 * kFillWarps)
@@ -201,6 +205,9 @@ __global__ void __launch_bounds__(32 * kFillWarps)
                  int* __restrict__ masks) {
   __shared__ TileRun seg[kFillWarps][kMaxLocalSegs];
   __shared__ int seg_s[kFillWarps][kMaxLocalSegs];
+  __shared__ int sweep_cnt[kFillWarps][kSweepPositions];
+  __shared__ int sweep_first[kFillWarps][kSweepPositions];
+  __shared__ int sweep_ptr[kFillWarps][kSweepPositions];
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x * kFillWarps + wib;
   if (tile >= n_tiles) return;  // whole warp leaves together
@@ -229,6 +236,100 @@ __global__ void __launch_bounds__(32 * kFillWarps)
   }
   __syncwarp();
   const bool overflow = nseg > kMaxLocalSegs;
+  if (overflow && hi - lo <= kSweepPositions) {
+    // Many runs over few positions (fine block-sparse tables): one pass over
+    // the list counts, per position, its runs and the first of them.
+    int* cnt = sweep_cnt[wib];
+    int* first = sweep_first[wib];
+    int* ptr = sweep_ptr[wib];
+    const int P = hi - lo;
+    for (int xi = lane; xi < P; xi += 32) {
+      cnt[xi] = 0;
+      first[xi] = 0x7fffffff;
+    }
+    __syncwarp();
+    for (int i = lane; i < S; i += 32) {
+      TileRun r;
+      if (kFwd ? fwd_tile_run(sl[L[i]], tile, r) : bwd_tile_run(sl[L[i]], tile, r)) {
+        for (int x = r.b; x < r.e; ++x) {
+          atomicAdd(&cnt[x - lo], 1);
+          atomicMin(&first[x - lo], i);
+        }
+      }
+    }
+    __syncwarp();
+    int vbase = kCount ? 0 : voff[tile], mbase = kCount ? 0 : moff[tile];
+    for (int x0 = 0; x0 < P; x0 += 32) {
+      const int xi = x0 + lane, x = lo + xi;
+      int c = 0, first_s = 0;
+      bool first_partial = false;
+      if (xi < P && (c = cnt[xi]) > 0) {
+        first_s = L[first[xi]];
+        TileRun r;
+        if (kFwd) fwd_tile_run(sl[first_s], tile, r);
+        else bwd_tile_run(sl[first_s], tile, r);
+        first_partial = !(x >= r.fb && x < r.fe);
+      }
+      const int vis = c > 0 ? 1 : 0, msz = c >= 2 ? c + 1 : 0;
+      int vi = vis, mi = msz;
+      for (int d = 1; d < 32; d <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, vi, d), b = __shfl_up_sync(0xffffffffu, mi, d);
+        if (lane >= d) {
+          vi += a;
+          mi += b;
+        }
+      }
+      if (!kCount && c > 0) {
+        int info = visit_info(first_s, first_partial);
+        if (c >= 2) {
+          const int m = mbase + mi - msz;
+          info = visit_list_info(m);
+          masks[m] = c;
+          ptr[xi] = m + 1;
+        }
+        visits[vbase + vi - vis] = make_int2(x, info);
+      }
+      vbase += __shfl_sync(0xffffffffu, vi, 31);
+      mbase += __shfl_sync(0xffffffffu, mi, 31);
+    }
+    if (kCount) {
+      if (lane == 0) {
+        vcnt[tile] = vbase;
+        mcnt[tile] = mbase;
+      }
+      return;
+    }
+    __syncwarp();
+    // Slice lists of the positions with several runs, in list order: the
+    // list is walked 32 entries at a time, and lanes whose runs meet at a
+    // position take consecutive places in lane order.
+    for (int i0 = 0; i0 < S; i0 += 32) {
+      const int i = i0 + lane;
+      TileRun r;
+      r.b = r.e = 0;
+      int s_i = -1;
+      if (i < S) {
+        s_i = L[i];
+        if (!(kFwd ? fwd_tile_run(sl[s_i], tile, r) : bwd_tile_run(sl[s_i], tile, r))) r.b = r.e = 0;
+      }
+      int len = r.e - r.b, maxlen = len;
+      for (int d = 16; d > 0; d >>= 1) maxlen = max(maxlen, __shfl_xor_sync(0xffffffffu, maxlen, d));
+      for (int j = 0; j < maxlen; ++j) {
+        const bool act = j < len && cnt[r.b + j - lo] >= 2;
+        const unsigned m = __match_any_sync(0xffffffffu, act ? r.b + j : -1 - lane);
+        const unsigned before = m & ((1u << lane) - 1u);
+        int base = 0;
+        if (act) base = ptr[r.b + j - lo];
+        __syncwarp();
+        if (act) {
+          masks[base + __popc(before)] = s_i;
+          if (before == 0u) ptr[r.b + j - lo] = base + __popc(m);
+        }
+        __syncwarp();
+      }
+    }
+    return;
+  }
   const int n_src = overflow ? S : nseg;
   // run i of this tile (slice index in *s); false when the slice has none
   auto run_of = [&](int i, TileRun& r, int& s) -> bool {
