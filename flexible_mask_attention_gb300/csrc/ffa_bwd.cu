@@ -654,7 +654,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_do,
-                      const __grid_constant__ GatherMaps tm_g, const DqParams P) {
+                      const __grid_constant__ CUtensorMap tm_k8,
+                      const __grid_constant__ CUtensorMap tm_v8, const DqParams P) {
   using C = DqCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
@@ -713,41 +714,21 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_do);
-      for (int i = 0; i < 4; ++i) {
-        prefetch_tmap(&tm_g.k[i]);
-        prefetch_tmap(&tm_g.v[i]);
-      }
+      prefetch_tmap(&tm_k8);
+      prefetch_tmap(&tm_v8);
       // One K or V tile: the k-tile's rows, or a gathered step's 16 blocks of
       // 8 rows (8-row boxes at 1024-byte aligned slots; unused slots read zeros).
       // ys: the step's 16 slot start rows, read once per step (4 x 16 bytes).
-      // A gathered tile is loaded run by run: consecutive slots holding
-      // consecutive keys (or unused slots, read as zero rows from row -8n)
-      // go as boxes of 16, 8, 4, 2 or 1 slots, each at its 1024-byte
-      // aligned slot offset.
-      auto load_kv = [&](uint32_t dst, const CUtensorMap* m, const CUtensorMap* mg, uint32_t b,
+      auto load_kv = [&](uint32_t dst, const CUtensorMap* m, const CUtensorMap* m8, uint32_t b,
                          int hk, const int4& stp, const int4 (&ys)[4]) {
         if (stp.w > 0) {
-          const int y[kGatherSlots] = {ys[0].x, ys[0].y, ys[0].z, ys[0].w, ys[1].x, ys[1].y,
-                                       ys[1].z, ys[1].w, ys[2].x, ys[2].y, ys[2].z, ys[2].w,
-                                       ys[3].x, ys[3].y, ys[3].z, ys[3].w};
-          int sl = 0;
-#pragma unroll 1
-          while (sl < kGatherSlots) {
-            const bool unused = y[sl] < 0;
-            int run = 1;
-            while (sl + run < kGatherSlots &&
-                   (unused ? y[sl + run] < 0 : y[sl + run] == y[sl] + kGatherKeys * run))
-              ++run;
-            while (run > 0) {
-              const int lg = run >= 16 ? 4 : run >= 8 ? 3 : run >= 4 ? 2 : run >= 2 ? 1 : 0;
-              const int n = 1 << lg;
-              const CUtensorMap* bm = lg == 4 ? m : mg + lg;
-              const int yy = unused ? -kGatherKeys * n : y[sl];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int y4[4] = {ys[q4].x, ys[q4].y, ys[q4].z, ys[q4].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
               for (int c = 0; c < C::kChunks; ++c)
-                tma_load_2d(dst + c * 16384 + sl * 1024, bm, b, hk * D + c * 64, yy);
-              sl += n;
-              run -= n;
-            }
+                tma_load_2d(dst + c * 16384 + (4 * q4 + e) * 1024, m8, b, hk * D + c * 64, y4[e]);
           }
         } else {
           for (int c = 0; c < C::kChunks; ++c)
@@ -793,13 +774,13 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
             const uint32_t kph = (kv_cnt / C::kKStages) & 1, vph = (kv_cnt / C::kVStages) & 1;
             if (!(ok = mbar_wait(bar(C::kBKEmpty + ks), kph ^ 1, ctl, 801))) break;
             mbar_arrive_expect_tx(bar(C::kBKFull + ks), C::kTileBytes);
-            load_kv(sbase + C::kKOff + ks * C::kTileBytes, &tm_k, tm_g.k, bar(C::kBKFull + ks), hk,
+            load_kv(sbase + C::kKOff + ks * C::kTileBytes, &tm_k, &tm_k8, bar(C::kBKFull + ks), hk,
                     st, ys);
             k_only = true;
             if (!(ok = mbar_wait(bar(C::kBVEmpty + vs), vph ^ 1, ctl, 802))) break;
             k_only = false;
             mbar_arrive_expect_tx(bar(C::kBVFull + vs), C::kTileBytes);
-            load_kv(sbase + C::kVOff + vs * C::kTileBytes, &tm_v, tm_g.v, bar(C::kBVFull + vs), hk,
+            load_kv(sbase + C::kVOff + vs * C::kTileBytes, &tm_v, &tm_v8, bar(C::kBVFull + vs), hk,
                     st, ys);
             ++kv_cnt;
           }
@@ -1153,11 +1134,11 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
       if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
     }
   }
-  alignas(64) CUtensorMap tq, tk, tv, tdo;
-  alignas(64) GatherMaps tg;
+  alignas(64) CUtensorMap tq, tk, tv, tdo, tk8, tv8;
   if (!encode_tile_map(&tq, q, p->Tq, p->Hq * D) || !encode_tile_map(&tk, k, p->Tk, p->Hkv * D) ||
       !encode_tile_map(&tv, v, p->Tk, p->Hkv * D) || !encode_tile_map(&tdo, dout, p->Tq, p->Hq * D) ||
-      !encode_gather_maps(&tg, k, v, p->Tk, p->Hkv * D))
+      !encode_tile_map(&tk8, k, p->Tk, p->Hkv * D, kGatherKeys) ||
+      !encode_tile_map(&tv8, v, p->Tk, p->Hkv * D, kGatherKeys))
     return FFA_ERR_INVALID_ARG;
   const float scale_log2 = scale * kLog2e;
   {
@@ -1225,7 +1206,7 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     if (cudaMemsetAsync(P.ticket, 0, sizeof(int), st) != cudaSuccess) return FFA_ERR_CUDA;
     record_phase(p, 4, st);
     ffa_bwd_dq_kernel<D, kCap><<<p->grid_dq, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo,
-                                                                                tg, P);
+                                                                                tk8, tv8, P);
     note_launches(1);
     if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   }

@@ -204,8 +204,8 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 template <int D, bool kCap>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     ffa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ GatherMaps tm_g,
-                   const FwdParams P) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_k8,
+                   const __grid_constant__ CUtensorMap tm_v8, const FwdParams P) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -259,42 +259,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      for (int i = 0; i < 4; ++i) {
-        prefetch_tmap(&tm_g.k[i]);
-        prefetch_tmap(&tm_g.v[i]);
-      }
+      prefetch_tmap(&tm_k8);
+      prefetch_tmap(&tm_v8);
       // One K or V tile into `dst`: the k-tile's 128 rows, or for a gathered
       // step 16 blocks of 8 rows (each an 8-row box filling one 1024-byte
       // swizzle atom; unused slots start at row -8 and read zeros).
       // ys: the step's 16 slot start rows, read once per step (4 x 16 bytes).
-      // A gathered tile is loaded run by run: consecutive slots holding
-      // consecutive keys (or unused slots, read as zero rows from row -8n)
-      // go as boxes of 16, 8, 4, 2 or 1 slots, each at its 1024-byte
-      // aligned slot offset.
-      auto load_kv = [&](uint32_t dst, const CUtensorMap* m, const CUtensorMap* mg, uint32_t b,
+      auto load_kv = [&](uint32_t dst, const CUtensorMap* m, const CUtensorMap* m8, uint32_t b,
                          int hk, const int4& stp, const int4 (&ys)[4]) {
         if (stp.w > 0) {
-          const int y[kGatherSlots] = {ys[0].x, ys[0].y, ys[0].z, ys[0].w, ys[1].x, ys[1].y,
-                                       ys[1].z, ys[1].w, ys[2].x, ys[2].y, ys[2].z, ys[2].w,
-                                       ys[3].x, ys[3].y, ys[3].z, ys[3].w};
-          int sl = 0;
-#pragma unroll 1
-          while (sl < kGatherSlots) {
-            const bool unused = y[sl] < 0;
-            int run = 1;
-            while (sl + run < kGatherSlots &&
-                   (unused ? y[sl + run] < 0 : y[sl + run] == y[sl] + kGatherKeys * run))
-              ++run;
-            while (run > 0) {
-              const int lg = run >= 16 ? 4 : run >= 8 ? 3 : run >= 4 ? 2 : run >= 2 ? 1 : 0;
-              const int n = 1 << lg;
-              const CUtensorMap* bm = lg == 4 ? m : mg + lg;
-              const int yy = unused ? -kGatherKeys * n : y[sl];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int y4[4] = {ys[q4].x, ys[q4].y, ys[q4].z, ys[q4].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
               for (int c = 0; c < C::kChunks; ++c)
-                tma_load_2d(dst + c * 16384 + sl * 1024, bm, b, hk * D + c * 64, yy);
-              sl += n;
-              run -= n;
-            }
+                tma_load_2d(dst + c * 16384 + (4 * q4 + e) * 1024, m8, b, hk * D + c * 64, y4[e]);
           }
         } else {
           for (int c = 0; c < C::kChunks; ++c)
@@ -337,13 +317,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const uint32_t ph = (kv_cnt / C::kStages) & 1;
           if (!(ok = mbar_wait(bar(C::kBKEmpty + stage), ph ^ 1, ctl, 101))) break;
           mbar_arrive_expect_tx(bar(C::kBKFull + stage), C::kTileBytes);
-          load_kv(sbase + C::kKOff + stage * C::kTileBytes, &tm_k, tm_g.k, bar(C::kBKFull + stage),
+          load_kv(sbase + C::kKOff + stage * C::kTileBytes, &tm_k, &tm_k8, bar(C::kBKFull + stage),
                   hk, stp, ys);
           k_only = true;
           if (!(ok = mbar_wait(bar(C::kBVEmpty + stage), ph ^ 1, ctl, 102))) break;
           k_only = false;
           mbar_arrive_expect_tx(bar(C::kBVFull + stage), C::kTileBytes);
-          load_kv(sbase + C::kVOff + stage * C::kTileBytes, &tm_v, tm_g.v, bar(C::kBVFull + stage),
+          load_kv(sbase + C::kVOff + stage * C::kTileBytes, &tm_v, &tm_v8, bar(C::kBVFull + stage),
                   hk, stp, ys);
           ++kv_cnt;
         }
@@ -708,10 +688,11 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
                           void* out, float* lse, void* ws, cudaStream_t st, const SinkArgs& sk,
                           float softcap) {
   using C = FwdCfg<D>;
-  alignas(64) CUtensorMap tq, tk, tv;
-  alignas(64) GatherMaps tg;
+  alignas(64) CUtensorMap tq, tk, tv, tk8, tv8;
   if (!encode_tile_map(&tq, q, p->Tq, p->Hq * D) || !encode_tile_map(&tk, k, p->Tk, p->Hkv * D) ||
-      !encode_tile_map(&tv, v, p->Tk, p->Hkv * D) || !encode_gather_maps(&tg, k, v, p->Tk, p->Hkv * D))
+      !encode_tile_map(&tv, v, p->Tk, p->Hkv * D) ||
+      !encode_tile_map(&tk8, k, p->Tk, p->Hkv * D, kGatherKeys) ||
+      !encode_tile_map(&tv8, v, p->Tk, p->Hkv * D, kGatherKeys))
     return FFA_ERR_INVALID_ARG;
   FwdParams P;
   P.steps = p->fwd_steps;
@@ -743,7 +724,8 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   if (!split_regs_ok<ffa_fwd_kernel<D, kCap>>()) return FFA_ERR_UNSUPPORTED;
   if (cudaMemsetAsync(P.ticket, 0, sizeof(int), st) != cudaSuccess) return FFA_ERR_CUDA;
   record_phase(p, 0, st);
-  ffa_fwd_kernel<D, kCap><<<p->grid_fwd, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, tg, P);
+  ffa_fwd_kernel<D, kCap><<<p->grid_fwd, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, tk8, tv8,
+                                                                             P);
   note_launches(1);
   if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   if (p->n_merges > 0) {

@@ -2,7 +2,6 @@
 // units of libffa.so.
 #pragma once
 
-#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -37,13 +36,6 @@ constexpr int kGatherSlots = 16;
 constexpr int kGatherWords = kGatherSlots + 2 * kGatherSlots * 4;
 constexpr int kGatherMaxBlocks = 2048;  // 8-key blocks per gathered unit
 constexpr int kGatherMaxTk = 1 << 19;   // key count up to which units may gather
-
-// Tensor maps for the boxes of gathered steps: runs of consecutive slots are
-// loaded as one box of 8, 16, 32 or 64 rows (16 slots: the tile's own map).
-struct GatherMaps {
-  CUtensorMap k[4];
-  CUtensorMap v[4];
-};
 
 #ifdef __CUDACC__
 // Adds [lo, hi) (tile-local, any range) to a 128-bit mask of tile columns.
@@ -267,15 +259,6 @@ bool on_plan_device(const ffa_plan_s* p);  // current device == the plan's devic
 // box_rows: 128 for whole tiles, kGatherKeys for the slots of gathered steps.
 bool encode_tile_map(void* map128, const void* base, int rows, int cols_elems,
                      int box_rows = 128);
-// The K and V maps of gathered steps: boxes of 8, 16, 32 and 64 rows.
-inline bool encode_gather_maps(GatherMaps* g, const void* k, const void* v, int rows,
-                               int cols_elems) {
-  for (int i = 0; i < 4; ++i)
-    if (!encode_tile_map(&g->k[i], k, rows, cols_elems, kGatherKeys << i) ||
-        !encode_tile_map(&g->v[i], v, rows, cols_elems, kGatherKeys << i))
-      return false;
-  return true;
-}
 void note_launches(int n);  // adds to the count reported by ffa_kernel_launch_count
 // Records phase event i of the plan on `st` when the caller asked for them.
 inline void record_phase(const ffa_plan_s* p, int i, cudaStream_t st) {
