@@ -923,6 +923,14 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           if (j + 1 < se) st_next = P.steps[j + 1];  // prefetch the next step descriptor
           const int info = half_info(st, h);
           if (info < 0) continue;
+          // The column mask depends on the plan only: its reads overlap the wait.
+          uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
+          if (info & 1) {
+            if (st.w > 0)
+              gather_mask(P.gathers + (size_t)(st.w - 1) * kGatherWords, h, t, P.Tk, vb);
+            else
+              step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
+          }
           const bool w = mbar_wait(bar(C::kBSdFull), sd_cnt & 1, ctl, 1000);
           if (!(ok = __all_sync(0xffffffffu, w))) break;
           ++sd_cnt;
@@ -931,13 +939,6 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           tmem_ld64(tmem + lane_addr + C::kTdP + 64 * wg, dp);
           tc_fence_before();
           mbar_arrive(bar(C::kBDpFree));
-          uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
-          if (info & 1) {
-            if (st.w > 0)
-              gather_mask(P.gathers + (size_t)(st.w - 1) * kGatherWords, h, t, P.Tk, vb);
-            else
-              step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
-          }
           const uint32_t m_lo = wg ? vb[2] : vb[0], m_hi = wg ? vb[3] : vb[1];
           const uint32_t tSb = tmem + lane_addr + C::kTS0 + 128 * (v & 1) + 64 * wg;
 #pragma unroll

@@ -476,6 +476,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (j + 1 < se) st_next = P.steps[j + 1];  // prefetch the next step descriptor
         const int info = h == 0 ? st.y : st.z;
         if (info < 0) continue;
+        // The column mask of a PARTIAL (or gathered) step depends on the plan
+        // only: its reads overlap the wait for S.
+        uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
+        if (info & 1) {
+          if (st.w > 0)
+            gather_mask(P.gathers + (size_t)(st.w - 1) * kGatherWords, h, row_in, P.Tk, vb);
+          else
+            step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
+        }
         const bool w = mbar_wait(bar(C::kBSFull + h), s_cnt & 1, ctl, 300 + h);
         if (!(ok = __all_sync(0xffffffffu, w))) break;
         ++s_cnt;
@@ -497,13 +506,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mn = fminf(fminf(mn0, mn1), fminf(mn2, mn3));
         }
         const bool lo_in_range = -mn <= P.cap.smax;
-        uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
         if (info & 1) {
           // PARTIAL (or gathered) step: keep the keys this row sees.
-          if (st.w > 0)
-            gather_mask(P.gathers + (size_t)(st.w - 1) * kGatherWords, h, row_in, P.Tk, vb);
-          else
-            step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (!mask_bit(vb, c)) u[c] = 0xff800000u;  // -inf
