@@ -709,6 +709,11 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   reg_dealloc<kSplitNarrowRegs>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer
+    // The whole warp runs the loop: lane 0 draws the items, waits on the
+    // rings and sets each barrier's byte count; the 16 slots of a gathered
+    // K/V tile (8 rows each, 1024-byte aligned, unused ones reading zero rows
+    // from row -8) are copied by lanes 0-15 in parallel after a __syncwarp
+    // that orders them behind the byte count.  Whole tiles are lane 0's.
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
@@ -716,85 +721,90 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       prefetch_tmap(&tm_do);
       prefetch_tmap(&tm_k8);
       prefetch_tmap(&tm_v8);
-      // One K or V tile: the k-tile's rows, or a gathered step's 16 blocks of
-      // 8 rows (8-row boxes at 1024-byte aligned slots; unused slots read zeros).
-      // ys: the step's 16 slot start rows, read once per step (4 x 16 bytes).
-      auto load_kv = [&](uint32_t dst, const CUtensorMap* m, const CUtensorMap* m8, uint32_t b,
-                         int hk, const int4& stp, const int4 (&ys)[4]) {
-        if (stp.w > 0) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int y4[4] = {ys[q4].x, ys[q4].y, ys[q4].z, ys[q4].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              for (int c = 0; c < C::kChunks; ++c)
-                tma_load_2d(dst + c * 16384 + (4 * q4 + e) * 1024, m8, b, hk * D + c * 64, y4[e]);
-          }
-        } else {
+    }
+    auto load_kv = [&](uint32_t dst, const CUtensorMap* m, const CUtensorMap* m8, uint32_t b,
+                       int hk, const int4& stp, int y) {
+      if (stp.w > 0) {
+        if (lane < kGatherSlots)
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_2d(dst + c * 16384, m, b, hk * D + c * 64, stp.x * 128);
-        }
-      };
-      auto slot_rows = [&](const int4& stp, int4 (&ys)[4]) {
-        if (stp.w > 0) {
-          const int4* r4 = reinterpret_cast<const int4*>(P.gathers + (size_t)(stp.w - 1) * kGatherWords);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) ys[q4] = r4[q4];
-        }
-      };
-      uint32_t kv_cnt = 0, q_cnt = 0;
-      bool ok = true, k_only = false;
-      for (int r = 0; ok; ++r) {
+            tma_load_2d(dst + c * 16384 + lane * 1024, m8, b, hk * D + c * 64, y);
+      } else if (lane == 0) {
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_2d(dst + c * 16384, m, b, hk * D + c * 64, stp.x * 128);
+      }
+    };
+    uint32_t kv_cnt = 0, q_cnt = 0;
+    bool ok = true, k_only = false;
+    for (int r = 0; ok; ++r) {
+      int idx = -1;
+      if (lane == 0) {
         const int pos = atomicAdd(P.ticket, 1);
-        const int idx = pos < P.n_items ? P.order[pos] : -1;
-        if (!(ok = queue_publish(queue, r, idx, ctl, 809)) || idx < 0) break;
-        const int* it = P.items + (size_t)idx * kFiWords;
-        const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
-        if (se <= sb) continue;
-        for (int h = 0; ok && h < 2; ++h) {
-          if (!half_active(it, h)) continue;
-          const int n = P.counts[2 * idx + h];
-          if (n == 0) continue;
-          const int qt = it[kFiQt0 + h], head = it[kFiH0 + h], hk = head / P.g;
-          if (!(ok = mbar_wait(bar(C::kBQEmpty), (q_cnt & 1) ^ 1, ctl, 800))) break;
-          mbar_arrive_expect_tx(bar(C::kBQFull), 2 * C::kTileBytes);
-          for (int c = 0; c < C::kChunks; ++c) {
-            tma_load_2d(sbase + C::kQOff + c * 16384, &tm_q, bar(C::kBQFull), head * D + c * 64,
-                        qt * 128);
-            tma_load_2d(sbase + C::kDOOff + c * 16384, &tm_do, bar(C::kBQFull),
-                        head * D + c * 64, qt * 128);
-          }
-          ++q_cnt;
-          for (int j = sb; j < se; ++j) {
-            const int4 st = P.steps[j];
-            if (half_info(st, h) < 0) continue;
-            int4 ys[4];
-            slot_rows(st, ys);  // in flight while the ring slots are awaited
-            const int ks = kv_cnt % C::kKStages, vs = kv_cnt % C::kVStages;
-            const uint32_t kph = (kv_cnt / C::kKStages) & 1, vph = (kv_cnt / C::kVStages) & 1;
-            if (!(ok = mbar_wait(bar(C::kBKEmpty + ks), kph ^ 1, ctl, 801))) break;
-            mbar_arrive_expect_tx(bar(C::kBKFull + ks), C::kTileBytes);
-            load_kv(sbase + C::kKOff + ks * C::kTileBytes, &tm_k, &tm_k8, bar(C::kBKFull + ks), hk,
-                    st, ys);
-            k_only = true;
-            if (!(ok = mbar_wait(bar(C::kBVEmpty + vs), vph ^ 1, ctl, 802))) break;
-            k_only = false;
-            mbar_arrive_expect_tx(bar(C::kBVFull + vs), C::kTileBytes);
-            load_kv(sbase + C::kVOff + vs * C::kTileBytes, &tm_v, &tm_v8, bar(C::kBVFull + vs), hk,
-                    st, ys);
-            ++kv_cnt;
+        idx = pos < P.n_items ? P.order[pos] : -1;
+        ok = queue_publish(queue, r, idx, ctl, 809);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      if (!ok || idx < 0) break;
+      const int* it = P.items + (size_t)idx * kFiWords;
+      const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
+      if (se <= sb) continue;
+      for (int h = 0; ok && h < 2; ++h) {
+        if (!half_active(it, h)) continue;
+        const int n = P.counts[2 * idx + h];
+        if (n == 0) continue;
+        const int qt = it[kFiQt0 + h], head = it[kFiH0 + h], hk = head / P.g;
+        if (lane == 0) {
+          ok = mbar_wait(bar(C::kBQEmpty), (q_cnt & 1) ^ 1, ctl, 800);
+          if (ok) {
+            mbar_arrive_expect_tx(bar(C::kBQFull), 2 * C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c) {
+              tma_load_2d(sbase + C::kQOff + c * 16384, &tm_q, bar(C::kBQFull), head * D + c * 64,
+                          qt * 128);
+              tma_load_2d(sbase + C::kDOOff + c * 16384, &tm_do, bar(C::kBQFull),
+                          head * D + c * 64, qt * 128);
+            }
           }
         }
+        if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+        ++q_cnt;
+        for (int j = sb; j < se; ++j) {
+          const int4 st = P.steps[j];
+          if (half_info(st, h) < 0) continue;
+          // this lane's slot start (read while the ring slots are awaited)
+          const int y = st.w > 0 && lane < kGatherSlots
+                            ? P.gathers[(size_t)(st.w - 1) * kGatherWords + lane] : 0;
+          const int ks = kv_cnt % C::kKStages, vs = kv_cnt % C::kVStages;
+          const uint32_t kph = (kv_cnt / C::kKStages) & 1, vph = (kv_cnt / C::kVStages) & 1;
+          if (lane == 0) {
+            ok = mbar_wait(bar(C::kBKEmpty + ks), kph ^ 1, ctl, 801);
+            if (ok) mbar_arrive_expect_tx(bar(C::kBKFull + ks), C::kTileBytes);
+          }
+          if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+          __syncwarp();
+          load_kv(sbase + C::kKOff + ks * C::kTileBytes, &tm_k, &tm_k8, bar(C::kBKFull + ks), hk,
+                  st, y);
+          k_only = true;
+          if (lane == 0) {
+            ok = mbar_wait(bar(C::kBVEmpty + vs), vph ^ 1, ctl, 802);
+            if (ok) mbar_arrive_expect_tx(bar(C::kBVFull + vs), C::kTileBytes);
+          }
+          if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+          __syncwarp();
+          k_only = false;
+          load_kv(sbase + C::kVOff + vs * C::kTileBytes, &tm_v, &tm_v8, bar(C::kBVFull + vs), hk,
+                  st, y);
+          ++kv_cnt;
+        }
       }
-      if (!ok) {
-        if (q_cnt > 0) drain_wait_b(bar(C::kBQFull), (q_cnt - 1) & 1, kDrainNs);
-        for (uint32_t i = kv_cnt > (uint32_t)C::kKStages ? kv_cnt - C::kKStages : 0; i < kv_cnt; ++i)
-          drain_wait_b(bar(C::kBKFull + i % C::kKStages), (i / C::kKStages) & 1, kDrainNs);
-        for (uint32_t i = kv_cnt > (uint32_t)C::kVStages ? kv_cnt - C::kVStages : 0; i < kv_cnt; ++i)
-          drain_wait_b(bar(C::kBVFull + i % C::kVStages), (i / C::kVStages) & 1, kDrainNs);
-        if (k_only)
-          drain_wait_b(bar(C::kBKFull + kv_cnt % C::kKStages), (kv_cnt / C::kKStages) & 1, kDrainNs);
-      }
+    }
+    if (!ok && lane == 0) {
+      if (q_cnt > 0) drain_wait_b(bar(C::kBQFull), (q_cnt - 1) & 1, kDrainNs);
+      for (uint32_t i = kv_cnt > (uint32_t)C::kKStages ? kv_cnt - C::kKStages : 0; i < kv_cnt; ++i)
+        drain_wait_b(bar(C::kBKFull + i % C::kKStages), (i / C::kKStages) & 1, kDrainNs);
+      for (uint32_t i = kv_cnt > (uint32_t)C::kVStages ? kv_cnt - C::kVStages : 0; i < kv_cnt; ++i)
+        drain_wait_b(bar(C::kBVFull + i % C::kVStages), (i / C::kVStages) & 1, kDrainNs);
+      if (k_only)
+        drain_wait_b(bar(C::kBKFull + kv_cnt % C::kKStages), (kv_cnt / C::kKStages) & 1, kDrainNs);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -923,14 +933,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           if (j + 1 < se) st_next = P.steps[j + 1];  // prefetch the next step descriptor
           const int info = half_info(st, h);
           if (info < 0) continue;
-          // The column mask depends on the plan only: its reads overlap the wait.
+          // A gathered step's column mask (every step of such a unit is one)
+          // is read while the scores are awaited; a PARTIAL tile's after.
           uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
-          if (info & 1) {
-            if (st.w > 0)
-              gather_mask(P.gathers + (size_t)(st.w - 1) * kGatherWords, h, t, P.Tk, vb);
-            else
-              step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
-          }
+          if (st.w > 0) gather_mask(P.gathers + (size_t)(st.w - 1) * kGatherWords, h, t, P.Tk, vb);
           const bool w = mbar_wait(bar(C::kBSdFull), sd_cnt & 1, ctl, 1000);
           if (!(ok = __all_sync(0xffffffffu, w))) break;
           ++sd_cnt;
@@ -939,6 +945,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           tmem_ld64(tmem + lane_addr + C::kTdP + 64 * wg, dp);
           tc_fence_before();
           mbar_arrive(bar(C::kBDpFree));
+          if ((info & 1) && st.w <= 0) step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
           const uint32_t m_lo = wg ? vb[2] : vb[0], m_hi = wg ? vb[3] : vb[1];
           const uint32_t tSb = tmem + lane_addr + C::kTS0 + 128 * (v & 1) + 64 * wg;
 #pragma unroll

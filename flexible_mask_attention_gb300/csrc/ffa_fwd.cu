@@ -255,89 +255,98 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   reg_dealloc<kSplitNarrowRegs>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer
+    // The whole warp runs the loop.  Lane 0 draws the items, waits on the
+    // rings and sets each barrier's byte count; the 16 slots of a gathered
+    // tile (8 rows each, 1024-byte aligned, unused ones reading zero rows
+    // from row -8) are copied by lanes 0-15 in parallel, after a __syncwarp
+    // that orders them behind the byte count.  Whole tiles are lane 0's.
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_k8);
       prefetch_tmap(&tm_v8);
-      // One K or V tile into `dst`: the k-tile's 128 rows, or for a gathered
-      // step 16 blocks of 8 rows (each an 8-row box filling one 1024-byte
-      // swizzle atom; unused slots start at row -8 and read zeros).
-      // ys: the step's 16 slot start rows, read once per step (4 x 16 bytes).
-      auto load_kv = [&](uint32_t dst, const CUtensorMap* m, const CUtensorMap* m8, uint32_t b,
-                         int hk, const int4& stp, const int4 (&ys)[4]) {
-        if (stp.w > 0) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int y4[4] = {ys[q4].x, ys[q4].y, ys[q4].z, ys[q4].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              for (int c = 0; c < C::kChunks; ++c)
-                tma_load_2d(dst + c * 16384 + (4 * q4 + e) * 1024, m8, b, hk * D + c * 64, y4[e]);
-          }
-        } else {
+    }
+    auto load_kv = [&](uint32_t dst, const CUtensorMap* m, const CUtensorMap* m8, uint32_t b,
+                       int hk, const int4& stp, int y) {
+      if (stp.w > 0) {
+        if (lane < kGatherSlots)
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_2d(dst + c * 16384, m, b, hk * D + c * 64, stp.x * 128);
-        }
-      };
-      auto slot_rows = [&](const int4& stp, int4 (&ys)[4]) {
-        if (stp.w > 0) {
-          const int4* r4 = reinterpret_cast<const int4*>(P.gathers + (size_t)(stp.w - 1) * kGatherWords);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) ys[q4] = r4[q4];
-        }
-      };
-      uint32_t kv_cnt = 0, q_cnt = 0;
-      bool ok = true, k_only = false;  // k_only: K of step kv_cnt issued, its V not yet
-      for (int r = 0; ok; ++r) {
-        const int pos = atomicAdd(P.ticket, 1);
-        const int idx = pos < P.n_items ? P.order[pos] : -1;
-        if (!(ok = queue_publish(queue, r, idx, ctl, 109)) || idx < 0) break;
-        const int* it = P.items + (size_t)idx * kFiWords;
-        const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
-        if (se <= sb) continue;
-        const bool act1 = it[kFiQt1] >= 0 && it[kFiH1] >= 0;
-        const int hk = it[kFiH0] / P.g;
-        if (!(ok = mbar_wait(bar(C::kBQEmpty), (q_cnt & 1) ^ 1, ctl, 100))) break;
-        mbar_arrive_expect_tx(bar(C::kBQFull), (act1 ? 2 : 1) * C::kTileBytes);
+            tma_load_2d(dst + c * 16384 + lane * 1024, m8, b, hk * D + c * 64, y);
+      } else if (lane == 0) {
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_2d(sbase + C::kQOff + c * 16384, &tm_q, bar(C::kBQFull),
-                      it[kFiH0] * D + c * 64, it[kFiQt0] * 128);
-        if (act1)
+          tma_load_2d(dst + c * 16384, m, b, hk * D + c * 64, stp.x * 128);
+      }
+    };
+    uint32_t kv_cnt = 0, q_cnt = 0;
+    bool ok = true, k_only = false;  // k_only: K of step kv_cnt issued, its V not yet
+    for (int r = 0; ok; ++r) {
+      int idx = -1;
+      if (lane == 0) {
+        const int pos = atomicAdd(P.ticket, 1);
+        idx = pos < P.n_items ? P.order[pos] : -1;
+        ok = queue_publish(queue, r, idx, ctl, 109);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      if (!ok || idx < 0) break;
+      const int* it = P.items + (size_t)idx * kFiWords;
+      const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
+      if (se <= sb) continue;
+      const bool act1 = it[kFiQt1] >= 0 && it[kFiH1] >= 0;
+      const int hk = it[kFiH0] / P.g;
+      if (lane == 0) {
+        ok = mbar_wait(bar(C::kBQEmpty), (q_cnt & 1) ^ 1, ctl, 100);
+        if (ok) {
+          mbar_arrive_expect_tx(bar(C::kBQFull), (act1 ? 2 : 1) * C::kTileBytes);
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_2d(sbase + C::kQOff + C::kTileBytes + c * 16384, &tm_q, bar(C::kBQFull),
-                        it[kFiH1] * D + c * 64, it[kFiQt1] * 128);
-        ++q_cnt;
-        for (int j = sb; j < se; ++j) {
-          const int4 stp = P.steps[j];
-          int4 ys[4];
-          slot_rows(stp, ys);  // in flight while the ring slot is awaited
-          const int stage = kv_cnt % C::kStages;
-          const uint32_t ph = (kv_cnt / C::kStages) & 1;
-          if (!(ok = mbar_wait(bar(C::kBKEmpty + stage), ph ^ 1, ctl, 101))) break;
-          mbar_arrive_expect_tx(bar(C::kBKFull + stage), C::kTileBytes);
-          load_kv(sbase + C::kKOff + stage * C::kTileBytes, &tm_k, &tm_k8, bar(C::kBKFull + stage),
-                  hk, stp, ys);
-          k_only = true;
-          if (!(ok = mbar_wait(bar(C::kBVEmpty + stage), ph ^ 1, ctl, 102))) break;
-          k_only = false;
-          mbar_arrive_expect_tx(bar(C::kBVFull + stage), C::kTileBytes);
-          load_kv(sbase + C::kVOff + stage * C::kTileBytes, &tm_v, &tm_v8, bar(C::kBVFull + stage),
-                  hk, stp, ys);
-          ++kv_cnt;
+            tma_load_2d(sbase + C::kQOff + c * 16384, &tm_q, bar(C::kBQFull),
+                        it[kFiH0] * D + c * 64, it[kFiQt0] * 128);
+          if (act1)
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_2d(sbase + C::kQOff + C::kTileBytes + c * 16384, &tm_q, bar(C::kBQFull),
+                          it[kFiH1] * D + c * 64, it[kFiQt1] * 128);
         }
       }
-      if (!ok) {
-        // Aborted: let the copies already issued land before the CTA exits.
-        if (q_cnt > 0) drain_wait(bar(C::kBQFull), (q_cnt - 1) & 1, kDrainNs);
-        for (uint32_t i = kv_cnt > (uint32_t)C::kStages ? kv_cnt - C::kStages : 0; i < kv_cnt; ++i) {
-          drain_wait(bar(C::kBKFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
-          drain_wait(bar(C::kBVFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
+      if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+      ++q_cnt;
+      for (int j = sb; j < se; ++j) {
+        const int4 stp = P.steps[j];
+        // this lane's slot start (read while the ring slot is awaited)
+        const int y = stp.w > 0 && lane < kGatherSlots
+                          ? P.gathers[(size_t)(stp.w - 1) * kGatherWords + lane] : 0;
+        const int stage = kv_cnt % C::kStages;
+        const uint32_t ph = (kv_cnt / C::kStages) & 1;
+        if (lane == 0) {
+          ok = mbar_wait(bar(C::kBKEmpty + stage), ph ^ 1, ctl, 101);
+          if (ok) mbar_arrive_expect_tx(bar(C::kBKFull + stage), C::kTileBytes);
         }
-        if (k_only)
-          drain_wait(bar(C::kBKFull + kv_cnt % C::kStages), (kv_cnt / C::kStages) & 1, kDrainNs);
+        if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+        __syncwarp();
+        load_kv(sbase + C::kKOff + stage * C::kTileBytes, &tm_k, &tm_k8, bar(C::kBKFull + stage),
+                hk, stp, y);
+        k_only = true;
+        if (lane == 0) {
+          ok = mbar_wait(bar(C::kBVEmpty + stage), ph ^ 1, ctl, 102);
+          if (ok) mbar_arrive_expect_tx(bar(C::kBVFull + stage), C::kTileBytes);
+        }
+        if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+        __syncwarp();
+        k_only = false;
+        load_kv(sbase + C::kVOff + stage * C::kTileBytes, &tm_v, &tm_v8, bar(C::kBVFull + stage),
+                hk, stp, y);
+        ++kv_cnt;
       }
+    }
+    if (!ok && lane == 0) {
+      // Aborted: let the copies already issued land before the CTA exits.
+      if (q_cnt > 0) drain_wait(bar(C::kBQFull), (q_cnt - 1) & 1, kDrainNs);
+      for (uint32_t i = kv_cnt > (uint32_t)C::kStages ? kv_cnt - C::kStages : 0; i < kv_cnt; ++i) {
+        drain_wait(bar(C::kBKFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
+        drain_wait(bar(C::kBVFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
+      }
+      if (k_only)
+        drain_wait(bar(C::kBKFull + kv_cnt % C::kStages), (kv_cnt / C::kStages) & 1, kDrainNs);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -477,14 +486,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int info = h == 0 ? st.y : st.z;
         if (info < 0) continue;
         // The column mask of a PARTIAL (or gathered) step depends on the plan
-        // only: its reads overlap the wait for S.
-        uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
-        if (info & 1) {
-          if (st.w > 0)
-            gather_mask(P.gathers + (size_t)(st.w - 1) * kGatherWords, h, row_in, P.Tk, vb);
-          else
-            step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
-        }
+        // only: its data is fetched into L1 while S is awaited.
+        if (info & 1) prefetch_step_mask(st, info, P.gathers, P.slices, P.masks, lane);
         const bool w = mbar_wait(bar(C::kBSFull + h), s_cnt & 1, ctl, 300 + h);
         if (!(ok = __all_sync(0xffffffffu, w))) break;
         ++s_cnt;
@@ -506,7 +509,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mn = fminf(fminf(mn0, mn1), fminf(mn2, mn3));
         }
         const bool lo_in_range = -mn <= P.cap.smax;
+        uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
         if (info & 1) {
+          if (st.w > 0)
+            gather_mask(P.gathers + (size_t)(st.w - 1) * kGatherWords, h, row_in, P.Tk, vb);
+          else
+            step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
           // PARTIAL (or gathered) step: keep the keys this row sees.
 #pragma unroll
           for (int c = 0; c < 128; ++c)

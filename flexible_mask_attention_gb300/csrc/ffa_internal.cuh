@@ -97,18 +97,50 @@ __device__ __forceinline__ void step_mask(int info, const Slice* __restrict__ sl
 // Visible columns of a gathered step for query row `row_in` of half h: slot s
 // holds keys [start_s, start_s + 8) in columns [8s, 8s + 8); the columns of a
 // slot are set when the row's bit is set, keys at or past Tk never.
+// All 32 words are loaded up front and independently (four 16-byte loads
+// for the starts), so the record costs one memory round trip.
 __device__ __forceinline__ void gather_mask(const int* __restrict__ rec, int h, int row_in,
                                             int Tk, uint32_t (&b)[4]) {
-  b[0] = b[1] = b[2] = b[3] = 0u;
+  int y[kGatherSlots];
+  uint32_t bits[kGatherSlots];
+  const int4* r4 = reinterpret_cast<const int4*>(rec);
+#pragma unroll
+  for (int q = 0; q < kGatherSlots / 4; ++q) {
+    const int4 v = r4[q];
+    y[4 * q] = v.x;
+    y[4 * q + 1] = v.y;
+    y[4 * q + 2] = v.z;
+    y[4 * q + 3] = v.w;
+  }
   const int* rows = rec + kGatherSlots + h * kGatherSlots * 4 + (row_in >> 5);
 #pragma unroll
+  for (int s = 0; s < kGatherSlots; ++s) bits[s] = (uint32_t)rows[4 * s];
+  b[0] = b[1] = b[2] = b[3] = 0u;
+#pragma unroll
   for (int s = 0; s < kGatherSlots; ++s) {
-    const int y = rec[s];
-    if (y >= 0 && ((rows[4 * s] >> (row_in & 31)) & 1)) {
-      const int valid = min(kGatherKeys, Tk - y);
-      b[s >> 2] |= ((1u << valid) - 1u) << (kGatherKeys * (s & 3));
-    }
+    const int valid = max(0, min(kGatherKeys, Tk - y[s]));  // 0 for unused slots too
+    const uint32_t on = (y[s] >= 0) && ((bits[s] >> (row_in & 31)) & 1u) ? 1u : 0u;
+    b[s >> 2] |= (((1u << valid) - 1u) & (0u - on)) << (kGatherKeys * (s & 3));
   }
+}
+
+// L1 prefetch of the plan data a masked step's column mask reads: the lines
+// of a gathered record (one per lane 0-4; a record is 576 bytes), or the
+// step's slice descriptor or slice list.  Costs no registers.
+__device__ __forceinline__ void prefetch_step_mask(const int4& st, int info,
+                                                   const int* __restrict__ gathers,
+                                                   const Slice* __restrict__ slices,
+                                                   const int* __restrict__ masks, int lane) {
+  const char* p;
+  if (st.w > 0) {
+    if (lane >= 5) return;
+    p = reinterpret_cast<const char*>(gathers + (size_t)(st.w - 1) * kGatherWords) + 128 * lane;
+  } else {
+    if (lane != 0) return;
+    p = (info & 3) == 3 ? reinterpret_cast<const char*>(masks + (info >> 2))
+                        : reinterpret_cast<const char*>(slices + (info >> 2));
+  }
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ bool mask_bit(const uint32_t (&b)[4], int c) {
