@@ -486,8 +486,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int info = h == 0 ? st.y : st.z;
         if (info < 0) continue;
         // The column mask of a PARTIAL (or gathered) step depends on the plan
-        // only: its data is fetched into L1 while S is awaited.
-        if (info & 1) prefetch_step_mask(st, info, P.gathers, P.slices, P.masks, lane);
+        // only: its reads overlap the wait for S.
+        uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
+        if (info & 1) {
+          if (st.w > 0)
+            gather_mask(P.gathers + (size_t)(st.w - 1) * kGatherWords, h, row_in, P.Tk, vb);
+          else
+            step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
+        }
         const bool w = mbar_wait(bar(C::kBSFull + h), s_cnt & 1, ctl, 300 + h);
         if (!(ok = __all_sync(0xffffffffu, w))) break;
         ++s_cnt;
@@ -509,12 +515,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mn = fminf(fminf(mn0, mn1), fminf(mn2, mn3));
         }
         const bool lo_in_range = -mn <= P.cap.smax;
-        uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
         if (info & 1) {
-          if (st.w > 0)
-            gather_mask(P.gathers + (size_t)(st.w - 1) * kGatherWords, h, row_in, P.Tk, vb);
-          else
-            step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
           // PARTIAL (or gathered) step: keep the keys this row sees.
 #pragma unroll
           for (int c = 0; c < 128; ++c)

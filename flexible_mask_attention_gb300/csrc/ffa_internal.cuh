@@ -124,25 +124,6 @@ __device__ __forceinline__ void gather_mask(const int* __restrict__ rec, int h, 
   }
 }
 
-// L1 prefetch of the plan data a masked step's column mask reads: the lines
-// of a gathered record (one per lane 0-4; a record is 576 bytes), or the
-// step's slice descriptor or slice list.  Costs no registers.
-__device__ __forceinline__ void prefetch_step_mask(const int4& st, int info,
-                                                   const int* __restrict__ gathers,
-                                                   const Slice* __restrict__ slices,
-                                                   const int* __restrict__ masks, int lane) {
-  const char* p;
-  if (st.w > 0) {
-    if (lane >= 5) return;
-    p = reinterpret_cast<const char*>(gathers + (size_t)(st.w - 1) * kGatherWords) + 128 * lane;
-  } else {
-    if (lane != 0) return;
-    p = (info & 3) == 3 ? reinterpret_cast<const char*>(masks + (info >> 2))
-                        : reinterpret_cast<const char*>(slices + (info >> 2));
-  }
-  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
-}
-
 __device__ __forceinline__ bool mask_bit(const uint32_t (&b)[4], int c) {
   return (b[c >> 5] >> (c & 31)) & 1u;
 }
