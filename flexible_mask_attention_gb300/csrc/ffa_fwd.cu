@@ -59,26 +59,20 @@ template <int D>
 struct FwdCfg {
   static constexpr int kChunks = D / 64;          // 128-byte column chunks per row
   static constexpr int kTileBytes = 128 * D * 2;  // one 128 x D bf16 tile
-  // V of step j may only be loaded once P V of step j - kVStages is done,
-  // while K of step j is free once S of step j - kKStages is: V gets the
-  // deeper ring (measured: with two V stages the MMA thread waited about 300
-  // cycles per step for V on the 64K mask).
-  static constexpr int kKStages = D == 128 ? 2 : 4;
-  static constexpr int kVStages = D == 128 ? 3 : 4;
+  static constexpr int kStages = D == 128 ? 2 : 4;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = 2 * kTileBytes;
-  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
   // barrier indices
-  static constexpr int kBQFull = 0, kBQEmpty = 1, kBKFull = 2, kBKEmpty = kBKFull + kKStages,
-                       kBVFull = kBKEmpty + kKStages, kBVEmpty = kBVFull + kVStages,
-                       kBSFull = kBVEmpty + kVStages, kBPFull = kBSFull + 2, kBOFull = kBPFull + 2,
+  static constexpr int kBQFull = 0, kBQEmpty = 1, kBKFull = 2, kBVFull = 2 + kStages,
+                       kBKEmpty = 2 + 2 * kStages, kBVEmpty = 2 + 3 * kStages,
+                       kBSFull = 2 + 4 * kStages, kBPFull = kBSFull + 2, kBOFull = kBPFull + 2,
                        kBOEmpty = kBOFull + 2, kBDrain = kBOEmpty + 2,
                        kBItemFull = kBDrain + 1, kBItemEmpty = kBItemFull + kItemRing,
                        kNumBars = kBItemEmpty + kItemRing;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag, queue slots
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + alignment slack
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
 struct FwdParams {
@@ -229,12 +223,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(C::kBQFull), 1);
     mbar_init(bar(C::kBQEmpty), 1);
-    for (int s = 0; s < C::kKStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar(C::kBKFull + s), 1);
-      mbar_init(bar(C::kBKEmpty + s), 1);
-    }
-    for (int s = 0; s < C::kVStages; ++s) {
       mbar_init(bar(C::kBVFull + s), 1);
+      mbar_init(bar(C::kBKEmpty + s), 1);
       mbar_init(bar(C::kBVEmpty + s), 1);
     }
     for (int h = 0; h < 2; ++h) {
@@ -323,25 +315,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // this lane's slot start (read while the ring slot is awaited)
         const int y = stp.w > 0 && lane < kGatherSlots
                           ? P.gathers[(size_t)(stp.w - 1) * kGatherWords + lane] : 0;
-        const int ks = kv_cnt % C::kKStages, vs = kv_cnt % C::kVStages;
-        const uint32_t kph = (kv_cnt / C::kKStages) & 1, vph = (kv_cnt / C::kVStages) & 1;
+        const int stage = kv_cnt % C::kStages;
+        const uint32_t ph = (kv_cnt / C::kStages) & 1;
         if (lane == 0) {
-          ok = mbar_wait(bar(C::kBKEmpty + ks), kph ^ 1, ctl, 101);
-          if (ok) mbar_arrive_expect_tx(bar(C::kBKFull + ks), C::kTileBytes);
+          ok = mbar_wait(bar(C::kBKEmpty + stage), ph ^ 1, ctl, 101);
+          if (ok) mbar_arrive_expect_tx(bar(C::kBKFull + stage), C::kTileBytes);
         }
         if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
         __syncwarp();
-        load_kv(sbase + C::kKOff + ks * C::kTileBytes, &tm_k, &tm_k8, bar(C::kBKFull + ks),
+        load_kv(sbase + C::kKOff + stage * C::kTileBytes, &tm_k, &tm_k8, bar(C::kBKFull + stage),
                 hk, stp, y);
         k_only = true;
         if (lane == 0) {
-          ok = mbar_wait(bar(C::kBVEmpty + vs), vph ^ 1, ctl, 102);
-          if (ok) mbar_arrive_expect_tx(bar(C::kBVFull + vs), C::kTileBytes);
+          ok = mbar_wait(bar(C::kBVEmpty + stage), ph ^ 1, ctl, 102);
+          if (ok) mbar_arrive_expect_tx(bar(C::kBVFull + stage), C::kTileBytes);
         }
         if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
         __syncwarp();
         k_only = false;
-        load_kv(sbase + C::kVOff + vs * C::kTileBytes, &tm_v, &tm_v8, bar(C::kBVFull + vs),
+        load_kv(sbase + C::kVOff + stage * C::kTileBytes, &tm_v, &tm_v8, bar(C::kBVFull + stage),
                 hk, stp, y);
         ++kv_cnt;
       }
@@ -349,12 +341,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (!ok && lane == 0) {
       // Aborted: let the copies already issued land before the CTA exits.
       if (q_cnt > 0) drain_wait(bar(C::kBQFull), (q_cnt - 1) & 1, kDrainNs);
-      for (uint32_t i = kv_cnt > (uint32_t)C::kKStages ? kv_cnt - C::kKStages : 0; i < kv_cnt; ++i)
-        drain_wait(bar(C::kBKFull + i % C::kKStages), (i / C::kKStages) & 1, kDrainNs);
-      for (uint32_t i = kv_cnt > (uint32_t)C::kVStages ? kv_cnt - C::kVStages : 0; i < kv_cnt; ++i)
-        drain_wait(bar(C::kBVFull + i % C::kVStages), (i / C::kVStages) & 1, kDrainNs);
+      for (uint32_t i = kv_cnt > (uint32_t)C::kStages ? kv_cnt - C::kStages : 0; i < kv_cnt; ++i) {
+        drain_wait(bar(C::kBKFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
+        drain_wait(bar(C::kBVFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
+      }
       if (k_only)
-        drain_wait(bar(C::kBKFull + kv_cnt % C::kKStages), (kv_cnt / C::kKStages) & 1, kDrainNs);
+        drain_wait(bar(C::kBKFull + kv_cnt % C::kStages), (kv_cnt / C::kStages) & 1, kDrainNs);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -395,8 +387,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         bool first_pv[2] = {true, true};
         int4 cur = P.steps[sb];
         {
-          const int stage = kv_cnt % C::kKStages;
-          if (!(ok = mbar_wait(bar(C::kBKFull + stage), (kv_cnt / C::kKStages) & 1, ctl, 201)))
+          const int stage = kv_cnt % C::kStages;
+          if (!(ok = mbar_wait(bar(C::kBKFull + stage), (kv_cnt / C::kStages) & 1, ctl, 201)))
             break;
           tc_fence_after();
           if (cur.y >= 0) {
@@ -411,10 +403,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         for (int j = sb; ok && j < se; ++j) {
           const uint32_t c = kv_cnt + (uint32_t)(j - sb);
-          const int stage = c % C::kVStages;  // V of this step
-          const uint32_t ph = (c / C::kVStages) & 1;
-          const int stage_n = (c + 1) % C::kKStages;  // K of the next step
-          const uint32_t ph_n = ((c + 1) / C::kKStages) & 1;
+          const int stage = c % C::kStages;
+          const uint32_t ph = (c / C::kStages) & 1;
+          const int stage_n = (c + 1) % C::kStages;
+          const uint32_t ph_n = ((c + 1) / C::kStages) & 1;
           const bool has_next = j + 1 < se;
           const int4 nxt = has_next ? P.steps[j + 1] : make_int4(0, -1, -1, 0);
           bool v_ready = false, k_next_ready = false;
