@@ -648,7 +648,8 @@ __device__ __forceinline__ bool half_active(const int* it, int h) {
 
 __device__ __forceinline__ int half_info(const int4& st, int h) { return h == 0 ? st.y : st.z; }
 
-template <int D, bool kCap>
+// kGather: the plan has gathered steps (instantiated apart, as in the forward).
+template <int D, bool kCap, bool kGather>
 __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     ffa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -724,7 +725,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     }
     auto load_kv = [&](uint32_t dst, const CUtensorMap* m, const CUtensorMap* m8, uint32_t b,
                        int hk, const int4& stp, int y) {
-      if (stp.w > 0) {
+      if (kGather && stp.w > 0) {
         if (lane < kGatherSlots)
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_2d(dst + c * 16384 + lane * 1024, m8, b, hk * D + c * 64, y);
@@ -771,7 +772,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           const int4 st = P.steps[j];
           if (half_info(st, h) < 0) continue;
           // this lane's slot start (read while the ring slots are awaited)
-          const int y = st.w > 0 && lane < kGatherSlots
+          const int y = kGather && st.w > 0 && lane < kGatherSlots
                             ? P.gathers[(size_t)(st.w - 1) * kGatherWords + lane] : 0;
           const int ks = kv_cnt % C::kKStages, vs = kv_cnt % C::kVStages;
           const uint32_t kph = (kv_cnt / C::kKStages) & 1, vph = (kv_cnt / C::kVStages) & 1;
@@ -936,7 +937,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           // A gathered step's column mask (every step of such a unit is one)
           // is read while the scores are awaited; a PARTIAL tile's after.
           uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
-          if (st.w > 0) gather_mask(P.gathers + (size_t)(st.w - 1) * kGatherWords, h, t, P.Tk, vb);
+          if (kGather && st.w > 0)
+            gather_mask(P.gathers + (size_t)(st.w - 1) * kGatherWords, h, t, P.Tk, vb);
           const bool w = mbar_wait(bar(C::kBSdFull), sd_cnt & 1, ctl, 1000);
           if (!(ok = __all_sync(0xffffffffu, w))) break;
           ++sd_cnt;
@@ -945,7 +947,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           tmem_ld64(tmem + lane_addr + C::kTdP + 64 * wg, dp);
           tc_fence_before();
           mbar_arrive(bar(C::kBDpFree));
-          if ((info & 1) && st.w <= 0) step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
+          if ((info & 1) && !(kGather && st.w > 0))
+            step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
           const uint32_t m_lo = wg ? vb[2] : vb[0], m_hi = wg ? vb[3] : vb[1];
           const uint32_t tSb = tmem + lane_addr + C::kTS0 + 128 * (v & 1) + 64 * wg;
 #pragma unroll
@@ -1112,7 +1115,7 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-template <int D, bool kCap>
+template <int D, bool kCap, bool kGather>
 ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const void* v,
                           const void* out, const void* dout, const float* lse, float scale,
                           void* dq, void* dk, void* dv, void* ws, cudaStream_t st,
@@ -1207,14 +1210,14 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     P.cap = cap;
     P.err = p->err;
     P.wait_ns = p->wait_ns;
-    if (cudaFuncSetAttribute(ffa_bwd_dq_kernel<D, kCap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(ffa_bwd_dq_kernel<D, kCap, kGather>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
       return FFA_ERR_CUDA;
-    if (!split_regs_ok<ffa_bwd_dq_kernel<D, kCap>>()) return FFA_ERR_UNSUPPORTED;
+    if (!split_regs_ok<ffa_bwd_dq_kernel<D, kCap, kGather>>()) return FFA_ERR_UNSUPPORTED;
     if (cudaMemsetAsync(P.ticket, 0, sizeof(int), st) != cudaSuccess) return FFA_ERR_CUDA;
     record_phase(p, 4, st);
-    ffa_bwd_dq_kernel<D, kCap><<<p->grid_dq, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo,
-                                                                                tk8, tv8, P);
+    ffa_bwd_dq_kernel<D, kCap, kGather><<<p->grid_dq, C::kThreads, C::kSmemBytes, st>>>(
+        tq, tk, tv, tdo, tk8, tv8, P);
     note_launches(1);
     if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   }
@@ -1233,17 +1236,17 @@ ffa_status_t launch_bwd(ffa_plan_s* p, const void* q, const void* k, const void*
                         const void* out, const void* dout, const float* lse, float scale,
                         void* dq, void* dk, void* dv, void* ws, size_t, cudaStream_t st,
                         const SinkArgs& sink, float* dsink, float softcap) {
-  const bool c = softcap > 0.f;
+  const bool c = softcap > 0.f, g = p->n_gathers > 0;
+#define FFA_BWD(DD, CC, GG)                                                                   \
+  launch_bwd_d<DD, CC, GG>(p, q, k, v, out, dout, lse, scale, dq, dk, dv, ws, st, sink, dsink, \
+                           softcap)
   if (p->D == 128)
-    return c ? launch_bwd_d<128, true>(p, q, k, v, out, dout, lse, scale, dq, dk, dv, ws, st, sink,
-                                       dsink, softcap)
-             : launch_bwd_d<128, false>(p, q, k, v, out, dout, lse, scale, dq, dk, dv, ws, st,
-                                        sink, dsink, softcap);
+    return c ? (g ? FFA_BWD(128, true, true) : FFA_BWD(128, true, false))
+             : (g ? FFA_BWD(128, false, true) : FFA_BWD(128, false, false));
   if (p->D == 64)
-    return c ? launch_bwd_d<64, true>(p, q, k, v, out, dout, lse, scale, dq, dk, dv, ws, st, sink,
-                                      dsink, softcap)
-             : launch_bwd_d<64, false>(p, q, k, v, out, dout, lse, scale, dq, dk, dv, ws, st, sink,
-                                       dsink, softcap);
+    return c ? (g ? FFA_BWD(64, true, true) : FFA_BWD(64, true, false))
+             : (g ? FFA_BWD(64, false, true) : FFA_BWD(64, false, false));
+#undef FFA_BWD
   return FFA_ERR_UNSUPPORTED;
 }
 

@@ -201,7 +201,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-template <int D, bool kCap>
+// kGather: the plan has gathered steps (instantiated apart, so that plans
+// without them run code with no trace of the gathered paths).
+template <int D, bool kCap, bool kGather>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     ffa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_k8,
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     auto load_kv = [&](uint32_t dst, const CUtensorMap* m, const CUtensorMap* m8, uint32_t b,
                        int hk, const int4& stp, int y) {
-      if (stp.w > 0) {
+      if (kGather && stp.w > 0) {
         if (lane < kGatherSlots)
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_2d(dst + c * 16384 + lane * 1024, m8, b, hk * D + c * 64, y);
@@ -313,7 +315,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int j = sb; j < se; ++j) {
         const int4 stp = P.steps[j];
         // this lane's slot start (read while the ring slot is awaited)
-        const int y = stp.w > 0 && lane < kGatherSlots
+        const int y = kGather && stp.w > 0 && lane < kGatherSlots
                           ? P.gathers[(size_t)(stp.w - 1) * kGatherWords + lane] : 0;
         const int stage = kv_cnt % C::kStages;
         const uint32_t ph = (kv_cnt / C::kStages) & 1;
@@ -489,7 +491,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // only: its reads overlap the wait for S.
         uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
         if (info & 1) {
-          if (st.w > 0)
+          if (kGather && st.w > 0)
             gather_mask(P.gathers + (size_t)(st.w - 1) * kGatherWords, h, row_in, P.Tk, vb);
           else
             step_mask<true>(info, P.slices, P.masks, row, st.x, vb);
@@ -696,7 +698,7 @@ __global__ void __launch_bounds__(128)
   lse[(size_t)head * Tq + row] = lse2 * kLn2;
 }
 
-template <int D, bool kCap>
+template <int D, bool kCap, bool kGather>
 ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const void* v, float scale,
                           void* out, float* lse, void* ws, cudaStream_t st, const SinkArgs& sk,
                           float softcap) {
@@ -731,14 +733,14 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   P.n_sink = sk.n;
   P.sink_layout = sk.layout;
   if (kCap) P.cap = make_cap_consts(scale, softcap);
-  if (cudaFuncSetAttribute(ffa_fwd_kernel<D, kCap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::kSmemBytes) != cudaSuccess)
+  if (cudaFuncSetAttribute(ffa_fwd_kernel<D, kCap, kGather>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
     return FFA_ERR_CUDA;
-  if (!split_regs_ok<ffa_fwd_kernel<D, kCap>>()) return FFA_ERR_UNSUPPORTED;
+  if (!split_regs_ok<ffa_fwd_kernel<D, kCap, kGather>>()) return FFA_ERR_UNSUPPORTED;
   if (cudaMemsetAsync(P.ticket, 0, sizeof(int), st) != cudaSuccess) return FFA_ERR_CUDA;
   record_phase(p, 0, st);
-  ffa_fwd_kernel<D, kCap><<<p->grid_fwd, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, tk8, tv8,
-                                                                             P);
+  ffa_fwd_kernel<D, kCap, kGather><<<p->grid_fwd, kFwdThreads, C::kSmemBytes, st>>>(
+      tq, tk, tv, tk8, tv8, P);
   note_launches(1);
   if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   if (p->n_merges > 0) {
@@ -760,13 +762,16 @@ size_t fwd_workspace_bytes(const ffa_plan_s* p) {
 ffa_status_t launch_fwd(ffa_plan_s* p, const void* q, const void* k, const void* v, float scale,
                         void* out, float* lse, void* ws, size_t, cudaStream_t st,
                         const SinkArgs& sink, float softcap) {
-  const bool cap = softcap > 0.f;
+  const bool cap = softcap > 0.f, g = p->n_gathers > 0;
+#define FFA_FWD(DD, CC, GG) \
+  launch_fwd_d<DD, CC, GG>(p, q, k, v, scale, out, lse, ws, st, sink, softcap)
   if (p->D == 128)
-    return cap ? launch_fwd_d<128, true>(p, q, k, v, scale, out, lse, ws, st, sink, softcap)
-               : launch_fwd_d<128, false>(p, q, k, v, scale, out, lse, ws, st, sink, softcap);
+    return cap ? (g ? FFA_FWD(128, true, true) : FFA_FWD(128, true, false))
+               : (g ? FFA_FWD(128, false, true) : FFA_FWD(128, false, false));
   if (p->D == 64)
-    return cap ? launch_fwd_d<64, true>(p, q, k, v, scale, out, lse, ws, st, sink, softcap)
-               : launch_fwd_d<64, false>(p, q, k, v, scale, out, lse, ws, st, sink, softcap);
+    return cap ? (g ? FFA_FWD(64, true, true) : FFA_FWD(64, true, false))
+               : (g ? FFA_FWD(64, false, true) : FFA_FWD(64, false, false));
+#undef FFA_FWD
   return FFA_ERR_UNSUPPORTED;
 }
 
