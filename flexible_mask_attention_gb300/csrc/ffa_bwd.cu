@@ -710,11 +710,12 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   reg_dealloc<kSplitNarrowRegs>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer
-    // The whole warp runs the loop: lane 0 draws the items, waits on the
-    // rings and sets each barrier's byte count; the 16 slots of a gathered
-    // K/V tile (8 rows each, 1024-byte aligned, unused ones reading zero rows
-    // from row -8) are copied by lanes 0-15 in parallel after a __syncwarp
-    // that orders them behind the byte count.  Whole tiles are lane 0's.
+    // Lane 0 draws the items, waits on the rings and sets each barrier's
+    // byte count.  With gathered steps the whole warp runs the loop and the
+    // 16 slots of a gathered K/V tile (8 rows each, 1024-byte aligned, unused
+    // ones reading zero rows from row -8) are copied by lanes 0-15 in
+    // parallel after a __syncwarp that orders them behind the byte count;
+    // without them lane 0 runs it alone (measured faster there).
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
@@ -736,6 +737,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     };
     uint32_t kv_cnt = 0, q_cnt = 0;
     bool ok = true, k_only = false;
+    // without gathered steps lane 0 runs the loop alone
+    const unsigned pm = kGather ? 0xffffffffu : 1u;
+    if (kGather || lane == 0)
     for (int r = 0; ok; ++r) {
       int idx = -1;
       if (lane == 0) {
@@ -743,8 +747,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         idx = pos < P.n_items ? P.order[pos] : -1;
         ok = queue_publish(queue, r, idx, ctl, 809);
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      idx = __shfl_sync(0xffffffffu, idx, 0);
+      ok = __shfl_sync(pm, ok, 0);
+      idx = __shfl_sync(pm, idx, 0);
       if (!ok || idx < 0) break;
       const int* it = P.items + (size_t)idx * kFiWords;
       const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
@@ -766,7 +770,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
             }
           }
         }
-        if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+        if (!(ok = __shfl_sync(pm, ok, 0))) break;
         ++q_cnt;
         for (int j = sb; j < se; ++j) {
           const int4 st = P.steps[j];
@@ -780,8 +784,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
             ok = mbar_wait(bar(C::kBKEmpty + ks), kph ^ 1, ctl, 801);
             if (ok) mbar_arrive_expect_tx(bar(C::kBKFull + ks), C::kTileBytes);
           }
-          if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
-          __syncwarp();
+          if (!(ok = __shfl_sync(pm, ok, 0))) break;
+          __syncwarp(pm);
           load_kv(sbase + C::kKOff + ks * C::kTileBytes, &tm_k, &tm_k8, bar(C::kBKFull + ks), hk,
                   st, y);
           k_only = true;
@@ -789,8 +793,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
             ok = mbar_wait(bar(C::kBVEmpty + vs), vph ^ 1, ctl, 802);
             if (ok) mbar_arrive_expect_tx(bar(C::kBVFull + vs), C::kTileBytes);
           }
-          if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
-          __syncwarp();
+          if (!(ok = __shfl_sync(pm, ok, 0))) break;
+          __syncwarp(pm);
           k_only = false;
           load_kv(sbase + C::kVOff + vs * C::kTileBytes, &tm_v, &tm_v8, bar(C::kBVFull + vs), hk,
                   st, y);

@@ -257,11 +257,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   reg_dealloc<kSplitNarrowRegs>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer
-    // The whole warp runs the loop.  Lane 0 draws the items, waits on the
-    // rings and sets each barrier's byte count; the 16 slots of a gathered
-    // tile (8 rows each, 1024-byte aligned, unused ones reading zero rows
-    // from row -8) are copied by lanes 0-15 in parallel, after a __syncwarp
-    // that orders them behind the byte count.  Whole tiles are lane 0's.
+    // Lane 0 draws the items, waits on the rings and sets each barrier's
+    // byte count.  With gathered steps the whole warp runs the loop and the
+    // 16 slots of a gathered tile (8 rows each, 1024-byte aligned, unused
+    // ones reading zero rows from row -8) are copied by lanes 0-15 in
+    // parallel after a __syncwarp that orders them behind the byte count;
+    // without them lane 0 runs it alone.
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
@@ -282,6 +283,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     };
     uint32_t kv_cnt = 0, q_cnt = 0;
     bool ok = true, k_only = false;  // k_only: K of step kv_cnt issued, its V not yet
+    const unsigned pm = kGather ? 0xffffffffu : 1u;  // lanes running the loop
+    if (kGather || lane == 0)
     for (int r = 0; ok; ++r) {
       int idx = -1;
       if (lane == 0) {
@@ -289,8 +292,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         idx = pos < P.n_items ? P.order[pos] : -1;
         ok = queue_publish(queue, r, idx, ctl, 109);
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      idx = __shfl_sync(0xffffffffu, idx, 0);
+      ok = __shfl_sync(pm, ok, 0);
+      idx = __shfl_sync(pm, idx, 0);
       if (!ok || idx < 0) break;
       const int* it = P.items + (size_t)idx * kFiWords;
       const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                           it[kFiH1] * D + c * 64, it[kFiQt1] * 128);
         }
       }
-      if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+      if (!(ok = __shfl_sync(pm, ok, 0))) break;
       ++q_cnt;
       for (int j = sb; j < se; ++j) {
         const int4 stp = P.steps[j];
@@ -323,8 +326,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           ok = mbar_wait(bar(C::kBKEmpty + stage), ph ^ 1, ctl, 101);
           if (ok) mbar_arrive_expect_tx(bar(C::kBKFull + stage), C::kTileBytes);
         }
-        if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
-        __syncwarp();
+        if (!(ok = __shfl_sync(pm, ok, 0))) break;
+        __syncwarp(pm);
         load_kv(sbase + C::kKOff + stage * C::kTileBytes, &tm_k, &tm_k8, bar(C::kBKFull + stage),
                 hk, stp, y);
         k_only = true;
@@ -332,8 +335,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           ok = mbar_wait(bar(C::kBVEmpty + stage), ph ^ 1, ctl, 102);
           if (ok) mbar_arrive_expect_tx(bar(C::kBVFull + stage), C::kTileBytes);
         }
-        if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
-        __syncwarp();
+        if (!(ok = __shfl_sync(pm, ok, 0))) break;
+        __syncwarp(pm);
         k_only = false;
         load_kv(sbase + C::kVOff + stage * C::kTileBytes, &tm_v, &tm_v8, bar(C::kBVFull + stage),
                 hk, stp, y);
