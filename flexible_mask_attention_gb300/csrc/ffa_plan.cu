@@ -590,7 +590,8 @@ __global__ void k_dq_counts(const int* __restrict__ items, int n_items,
 // One block per forward unit.  A unit gathers when every slice of its q-tiles'
 // lists is FULL with ks and ke multiples of kGatherKeys (ke may be Tk), it
 // covers 1 .. kGatherMaxBlocks blocks of kGatherKeys keys, and ceil(blocks /
-// kGatherSlots) gathered steps are fewer than its regular steps.  The blocks
+// kGatherSlots) gathered steps are at most 2/3 of its regular steps (a
+// gathered step, masked per element, costs about 1.5 tile steps).  The blocks
 // are collected in a shared-memory bitmap (order-free, so deterministic).
 constexpr int kGatherThreads = 256;
 constexpr int kGatherBitmapWords = kGatherMaxTk / kGatherKeys / 32;
@@ -669,7 +670,7 @@ __global__ void __launch_bounds__(kGatherThreads)
   const int nwords = (((Tk + kGatherKeys - 1) / kGatherKeys) + 31) / 32;
   const int n = ok ? block_popc(bits, nwords, red) : 0;
   const int steps = (n + kGatherSlots - 1) / kGatherSlots;
-  const bool gather = ok && n > 0 && n <= kGatherMaxBlocks && steps < scnt[u];
+  const bool gather = ok && n > 0 && n <= kGatherMaxBlocks && 3 * steps <= 2 * scnt[u];
   if (threadIdx.x == 0) {
     gcnt[u] = gather ? steps : 0;
     if (gather) scnt[u] = steps;

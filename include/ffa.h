@@ -119,7 +119,7 @@ ffa_status_t ffa_plan_info(ffa_plan_t plan, ffa_plan_info_t* info);
  *   m+n] are their slice indices, ascending (the tile is computed once and
  *   masked by the union of their windows).
  *   Gathered forward steps (a forward unit whose slices are all FULL with key
- *   ranges aligned to 8 keys, when that takes fewer steps than its tiles):
+ *   ranges aligned to 8 keys, when that takes at most 2/3 of its tile steps):
  *   step (0, info0, info1, r + 1) computes 16 blocks of 8 keys packed into
  *   one K/V tile; record r holds the 16 block start keys (-8: unused slot),
  *   then for each half 16 x 4 words of row bits (bit i of word w: row

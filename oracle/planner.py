@@ -24,13 +24,21 @@ the work-list specification of the planner:
     item per (kt, kv head), cost g * sum of visit costs;
   * gathered forward units: a unit whose q-tiles meet only FULL slices with
     8-aligned key ranges (the end may be Tk), Tk <= 2^19, is instead listed
-    as gathered steps when that takes fewer steps: the 8-key blocks any of
+    as gathered steps when that takes at most 2/3 of its steps (a gathered
+    step, masked per element, costs about 1.5 tile steps): the 8-key blocks any of
     its slices covers, ascending, 16 to a step; a step is (0, info0, info1,
     r + 1) with record r = 16 block starts (key index, -8 for an unused
     slot) then, per half, 16 x 4 words of row bits (bit r of word w: row
     32w + r of the half's q-tile sees the slot's keys); info_h = 1 when the
     half has a row bit set, else -1; cost 5 per busy half.  At most 2048
-    blocks per unit.
+    blocks per unit;
+  * gathered backward units, the transpose: a k-tile whose slices are all
+    FULL with 8-aligned query ranges (the end may be Tq), Tq <= 2^19, lists
+    the 8-row query blocks its slices cover, 16 to a step, when that takes
+    at most 2/3 of its visits; a step is (0, 1, 0, r + 1) with record r =
+    16 block start rows (-8: unused) then 16 x 4 words of key bits (bit i of
+    word w: key 32w + i of the k-tile is seen by the slot's rows); cost 5
+    per step (times g in the item).
 """
 from __future__ import annotations
 
@@ -45,6 +53,7 @@ GATHER_SLOTS = 16         # slots per gathered step (a 128-key tile)
 GATHER_MAX_BLOCKS = 2048  # blocks per gathered unit
 GATHER_MAX_TK = 1 << 19
 GATHER_WORDS = GATHER_SLOTS + 2 * GATHER_SLOTS * 4
+BGATHER_WORDS = GATHER_SLOTS + GATHER_SLOTS * 4
 
 
 def row_intervals(qs, qe, ks, ke, t):
@@ -225,15 +234,25 @@ def plan(total_q, total_k, num_heads_q, num_heads_kv, q_ranges, k_ranges, mask_t
     fwd_items = np.array(items, dtype=np.int32).reshape(-1, 8)
     fwd_order = order_of([it[7] for it in items], [max(it[2], 0) // g for it in items])
 
+    bgathered = gather_units_bwd(total_q, total_k, q_ranges, k_ranges, mask_types, bvis)
+    brecords = []
     bsteps, bitems = [], []
-    boff = []
+    boff, bn, bcost = [], [], []
     for kt in range(n_kt):
         boff.append(len(bsteps))
-        bsteps.extend((qt, i, 0, 0) for qt, i in bvis[kt])
+        if kt in bgathered:
+            for rec in bgathered[kt]:
+                bsteps.append((0, 1, 0, len(brecords) + 1))
+                brecords.append(rec)
+            bn.append(len(bgathered[kt]))
+            bcost.append(PARTIAL_COST * len(bgathered[kt]))
+        else:
+            bsteps.extend((qt, i, 0, 0) for qt, i in bvis[kt])
+            bn.append(len(bvis[kt]))
+            bcost.append(sum(_cost(i) for _, i in bvis[kt]))
     for kt in range(n_kt):
-        c = sum(_cost(i) for _, i in bvis[kt])
         for hk in range(num_heads_kv):
-            bitems.append([kt, hk, boff[kt], boff[kt] + len(bvis[kt]), c * g, 0, 0, 0])
+            bitems.append([kt, hk, boff[kt], boff[kt] + bn[kt], bcost[kt] * g, 0, 0, 0])
     bwd_items = np.array(bitems, dtype=np.int32).reshape(-1, 8)
     return {
         "fwd_steps": np.array(steps, dtype=np.int32).reshape(-1, 4),
@@ -245,6 +264,7 @@ def plan(total_q, total_k, num_heads_q, num_heads_kv, q_ranges, k_ranges, mask_t
         "merges": np.array(merges, dtype=np.int32).reshape(-1, 8),
         "fwd_masks": np.array(fmasks, dtype=np.int32).reshape(-1, 1),
         "gathers": np.array(records, dtype=np.int32).reshape(-1, GATHER_WORDS),
+        "bgathers": np.array(brecords, dtype=np.int32).reshape(-1, BGATHER_WORDS),
         "bwd_masks": np.array(bmasks, dtype=np.int32).reshape(-1, 1),
         "n_slots": n_slots,
         "grid_fwd": max(1, min(num_sms, len(items))),
@@ -289,7 +309,7 @@ def gather_units(total_q, total_k, q_ranges, k_ranges, mask_types, pair_mode, fv
         else:  # steps of the two q-tiles' visit lists merged on kt
             regular = len({kt for q in qts for kt, _ in fvis[q]})
         n_steps = -(-len(blocks) // GATHER_SLOTS)
-        if len(blocks) > GATHER_MAX_BLOCKS or n_steps >= regular:
+        if len(blocks) > GATHER_MAX_BLOCKS or 3 * n_steps > 2 * regular:
             continue
         half_tiles = [u, u] if pair_mode == 0 else [2 * u, 2 * u + 1 if 2 * u + 1 < n_qt else -1]
         res = []
@@ -311,4 +331,51 @@ def gather_units(total_q, total_k, q_ranges, k_ranges, mask_types, pair_mode, fv
                 infos.append(1 if words.any() else -1)
             res.append((rec, (infos[0], infos[1])))
         out[u] = res
+    return out
+
+
+def _ktile_slices(total_k, q_ranges, k_ranges, mask_types):
+    """Per k-tile: the non-empty slices whose k range meets its keys."""
+    n_kt = -(-total_k // TILE)
+    out = [[] for _ in range(n_kt)]
+    for s, ((qs, qe), (ks, ke), t) in enumerate(zip(np.asarray(q_ranges).reshape(-1, 2),
+                                                    np.asarray(k_ranges).reshape(-1, 2),
+                                                    np.asarray(mask_types).reshape(-1))):
+        qs, qe, ks, ke, t = int(qs), int(qe), int(ks), int(ke), int(t)
+        if qe <= qs or ke <= ks:
+            continue
+        for kt in range(ks // TILE, -(-ke // TILE)):
+            out[kt].append((qs, qe, ks, ke, t))
+    return out
+
+
+def gather_units_bwd(total_q, total_k, q_ranges, k_ranges, mask_types, bvis):
+    """{k-tile: [record words, ...]} for the gathered backward units."""
+    if total_q > GATHER_MAX_TK:
+        return {}
+    tiles = _ktile_slices(total_k, q_ranges, k_ranges, mask_types)
+    out = {}
+    for kt, sl in enumerate(tiles):
+        if not sl or any(t != 0 or qs % GATHER_KEYS or (qe % GATHER_KEYS and qe != total_q)
+                         for qs, qe, _, _, t in sl):
+            continue
+        blocks = sorted({b for qs, qe, _, _, _ in sl
+                         for b in range(qs // GATHER_KEYS, -(-qe // GATHER_KEYS))})
+        n_steps = -(-len(blocks) // GATHER_SLOTS)
+        if len(blocks) > GATHER_MAX_BLOCKS or 3 * n_steps > 2 * len(bvis[kt]):
+            continue
+        res = []
+        for j in range(n_steps):
+            bs = blocks[GATHER_SLOTS * j: GATHER_SLOTS * (j + 1)]
+            rec = [GATHER_KEYS * b for b in bs] + [-GATHER_KEYS] * (GATHER_SLOTS - len(bs))
+            words = np.zeros((GATHER_SLOTS, 4), dtype=np.uint32)
+            for slot, b in enumerate(bs):
+                r0, r1 = GATHER_KEYS * b, GATHER_KEYS * (b + 1)
+                for qs, qe, ks, ke, _ in sl:
+                    if qs < r1 and qe > r0:
+                        for key in range(max(ks, TILE * kt), min(ke, TILE * (kt + 1))):
+                            kk = key - TILE * kt
+                            words[slot, kk >> 5] |= np.uint32(1 << (kk & 31))
+            res.append(rec + [int(w) for w in words.view(np.int32).reshape(-1)])
+        out[kt] = res
     return out

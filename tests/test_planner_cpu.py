@@ -159,25 +159,39 @@ def test_plan_split_and_order_rules():
     assert q["bwd_items"].tolist() == [[0, 0, 0, 1, 5, 0, 0, 0], [1, 0, 1, 2, 5, 0, 0, 0]]
 
 
-@pytest.mark.parametrize("blocks,seed", [((64, 64), 1), ((64, 8), 2), ((16, 64), 3), ((8, 64), 4),
-                                         ((64, 16), 5), ((128, 128), 6)])
-@pytest.mark.parametrize("heads", [(4, 2), (2, 2)])
+# (q block, k block, seed, heads) of tables the planner gathers for
+FWD_GATHER_CASES = [((64, 64), 1, (4, 2)), ((64, 64), 1, (2, 2)), ((64, 8), 2, (4, 2)),
+                    ((64, 8), 2, (2, 2)), ((16, 64), 3, (4, 2)), ((64, 16), 5, (2, 2))]
+BWD_GATHER_CASES = [((64, 64), 1, (4, 2)), ((16, 64), 3, (2, 2)), ((8, 64), 4, (4, 2)),
+                    ((64, 16), 5, (2, 2))]
+
+
+def _block_sparse_plan(blocks, seed, heads, T=1000):
+    """A ragged block-sparse table (T not a multiple of the tile or of the
+    blocks), its dense mask and the CPU planner's lists."""
+    wl = W.block_sparse(total=T, hq=heads[0], hkv=heads[1], q_block=blocks[0],
+                        k_block=blocks[1], seed=seed)
+    m = dense.dense_mask(T, T, wl.q_ranges, wl.k_ranges, wl.mask_types).astype(bool)
+    p = planner.plan(T, T, heads[0], heads[1], wl.q_ranges, wl.k_ranges, wl.mask_types,
+                     num_sms=152)
+    return m, p
+
+
+def test_tile_aligned_blocks_do_not_gather():
+    m, p = _block_sparse_plan((128, 128), 6, (4, 2), T=1024)
+    assert p["gathers"].shape[0] == 0 and p["bgathers"].shape[0] == 0
+
+
+@pytest.mark.parametrize("blocks,seed,heads", FWD_GATHER_CASES)
 def test_gathered_steps_cover_the_mask_exactly(blocks, seed, heads):
     """Gathered forward steps (the planner specification for units of full,
     8-key aligned slices): for every item half, the (row, key) pairs its
     steps' slot row bits mark are exactly the visible pairs of its q-tile's
     rows in the dense mask, each once; keys past Tk are never marked, unused
     slots (start -8) carry no bits, slot starts ascend within a step."""
-    T = 1000  # not a multiple of the tile or of the block sizes
-    wl = W.block_sparse(total=T, hq=heads[0], hkv=heads[1], q_block=blocks[0], k_block=blocks[1],
-                        seed=seed)
-    m = dense.dense_mask(T, T, wl.q_ranges, wl.k_ranges, wl.mask_types).astype(bool)
-    p = planner.plan(T, T, heads[0], heads[1], wl.q_ranges, wl.k_ranges, wl.mask_types,
-                     num_sms=152)
+    m, p = _block_sparse_plan(blocks, seed, heads)
+    T = m.shape[1]
     steps, rec = p["fwd_steps"], p["gathers"]
-    if blocks == (128, 128):  # tile-aligned blocks: the tile lists are already exact
-        assert rec.shape[0] == 0
-        return
     assert rec.shape[0] > 0
     # a (q-tile, head) may be cut into several items (split): sum over them
     marked_by = {}
@@ -213,3 +227,42 @@ def test_gathered_steps_cover_the_mask_exactly(blocks, seed, heads):
         assert (got[ref] == 1).all(), "a visible pair is missed or listed twice"
         assert (got[~ref] == 0).all(), "an invisible pair is marked visible"
     assert n_halves > 0
+
+
+@pytest.mark.parametrize("blocks,seed,heads", BWD_GATHER_CASES)
+def test_gathered_backward_steps_cover_the_mask_exactly(blocks, seed, heads):
+    """Gathered backward steps (the transpose: k-tiles of full slices with
+    8-row aligned query ranges): over a k-tile's steps, the (row, key) pairs
+    the slots' key bits mark are exactly the visible pairs of its keys in the
+    dense mask, each once; rows past Tq are never marked; every kv head's
+    item of the k-tile has the same steps."""
+    m, p = _block_sparse_plan(blocks, seed, heads)
+    Tq, Tk = m.shape
+    steps, rec = p["bwd_steps"], p["bgathers"]
+    assert rec.shape[0] > 0
+    seen_tiles = 0
+    for it in p["bwd_items"]:
+        kt = it[0]
+        st = steps[it[2]:it[3]]
+        if not (st[:, 3] > 0).any():
+            continue
+        assert (st[:, 3] > 0).all() and (st[:, 1] == 1).all()
+        seen_tiles += 1
+        marked = np.zeros((Tq, 128), dtype=np.int64)
+        for s_ in st:
+            r = rec[s_[3] - 1]
+            starts = r[:16]
+            assert (np.diff(starts[starts >= 0]) > 0).all() and (starts[starts < 0] == -8).all()
+            words = r[16:].view(np.uint32).reshape(16, 4)
+            for slot, y in enumerate(starts):
+                if y < 0:
+                    assert not words[slot].any()
+                    continue
+                bits = (words[slot][np.arange(128) >> 5] >> (np.arange(128) & 31)) & 1
+                for kk in np.nonzero(bits)[0]:
+                    marked[y:min(y + 8, Tq), kk] += 1
+        ref = m[:, 128 * kt: min(128 * kt + 128, Tk)]
+        got = marked[:, : ref.shape[1]]
+        assert (got[ref] == 1).all(), "a visible pair is missed or listed twice"
+        assert (got[~ref] == 0).all(), "an invisible pair is marked visible"
+    assert seen_tiles > 0
