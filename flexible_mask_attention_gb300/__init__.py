@@ -54,7 +54,7 @@ class _PlanInfo(ctypes.Structure):
                 ("merges", ctypes.c_int64), ("grid_fwd", ctypes.c_int32),
                 ("grid_bwd", ctypes.c_int32), ("area", ctypes.c_int64),
                 ("fwd_masks", ctypes.c_int64), ("bwd_masks", ctypes.c_int64),
-                ("gathers", ctypes.c_int64)]
+                ("gathers", ctypes.c_int64), ("bgathers", ctypes.c_int64)]
 
 
 _lib = None
@@ -190,7 +190,7 @@ def ffa_plan_info(plan: Plan) -> dict:
     return {f: getattr(info, f) for f, _ in _PlanInfo._fields_}
 
 
-_EXPORT_WORDS = {0: 4, 1: 8, 2: 1, 3: 4, 4: 8, 5: 1, 6: 8, 7: 1, 8: 1, 9: 144}
+_EXPORT_WORDS = {0: 4, 1: 8, 2: 1, 3: 4, 4: 8, 5: 1, 6: 8, 7: 1, 8: 1, 9: 144, 10: 80}
 
 
 def ffa_plan_export(plan: Plan, which: int):

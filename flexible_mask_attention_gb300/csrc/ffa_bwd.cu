@@ -93,7 +93,8 @@ struct KvParams {
   int n_items;
   const Slice* slices;
   const int* masks;  // slice lists of multi-slice visits
-  int Tk, Hkv, g, qpad;
+  const int* bgathers;  // gathered backward step records
+  int Tq, Tk, Hkv, g, qpad;
   float scale, scale_log2;
   const float* nlse2;   // [Hq][qpad] -lse * log2(e)
   const float* ndelta;  // [Hq][qpad] -rowsum(dO * O)
@@ -186,12 +187,15 @@ __device__ __forceinline__ void pds_chunk(const uint32_t (&s)[64], uint32_t tP, 
   }
 }
 
-template <int D, bool kCap>
+// kGather: the plan has gathered backward steps (instantiated apart).
+template <int D, bool kCap, bool kGather>
 __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
     ffa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
-                        const __grid_constant__ CUtensorMap tm_do, const KvParams P) {
+                        const __grid_constant__ CUtensorMap tm_do,
+                        const __grid_constant__ CUtensorMap tm_q8,
+                        const __grid_constant__ CUtensorMap tm_do8, const KvParams P) {
   using C = KvCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
@@ -248,65 +252,115 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
   reg_dealloc<kSplitNarrowRegs>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer
+    // Lane 0 draws the items, waits on the rings and sets each barrier's
+    // byte count.  With gathered steps the whole warp runs the loop, and the
+    // 16 query blocks of a gathered Q / dO tile (8 rows each at 1024-byte
+    // aligned slots; unused ones read zero rows from row -8) and their
+    // 32-byte pieces of -lse2 and -delta (unused ones copy row 0's, finite
+    // values that their masked columns never use) are copied by lanes 0-15
+    // after a __syncwarp that orders them behind the byte count.
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_do);
-      uint32_t kv_cnt = 0, q_cnt = 0, do_cnt = 0;  // tiles issued
-      bool ok = true;
-      for (int r = 0; ok; ++r) {
+      prefetch_tmap(&tm_q8);
+      prefetch_tmap(&tm_do8);
+    }
+    uint32_t kv_cnt = 0, q_cnt = 0, do_cnt = 0;  // tiles issued
+    bool ok = true;
+    const unsigned pm = kGather ? 0xffffffffu : 1u;  // lanes running the loop
+    if (kGather || lane == 0)
+    for (int r = 0; ok; ++r) {
+      int idx = -1;
+      if (lane == 0) {
         const int pos = atomicAdd(P.ticket, 1);
-        const int idx = pos < P.n_items ? P.order[pos] : -1;
-        if (!(ok = queue_publish(queue, r, idx, ctl, 409)) || idx < 0) break;
-        const int* it = P.items + (size_t)idx * kBiWords;
-        const int sb = it[kBiStepBeg], se = it[kBiStepEnd];
-        if (se <= sb) continue;
-        const int kt = it[kBiKt], hk = it[kBiHkv];
-        if (!(ok = mbar_wait(bar(C::kBKVEmpty), (kv_cnt & 1) ^ 1, ctl, 400))) break;
-        mbar_arrive_expect_tx(bar(C::kBKVFull), 2 * C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_2d(sbase + C::kKOff + c * 16384, &tm_k, bar(C::kBKVFull), hk * D + c * 64,
-                      kt * 128);
-          tma_load_2d(sbase + C::kVOff + c * 16384, &tm_v, bar(C::kBKVFull), hk * D + c * 64,
-                      kt * 128);
+        idx = pos < P.n_items ? P.order[pos] : -1;
+        ok = queue_publish(queue, r, idx, ctl, 409);
+      }
+      ok = __shfl_sync(pm, ok, 0);
+      idx = __shfl_sync(pm, idx, 0);
+      if (!ok || idx < 0) break;
+      const int* it = P.items + (size_t)idx * kBiWords;
+      const int sb = it[kBiStepBeg], se = it[kBiStepEnd];
+      if (se <= sb) continue;
+      const int kt = it[kBiKt], hk = it[kBiHkv];
+      if (lane == 0) {
+        ok = mbar_wait(bar(C::kBKVEmpty), (kv_cnt & 1) ^ 1, ctl, 400);
+        if (ok) {
+          mbar_arrive_expect_tx(bar(C::kBKVFull), 2 * C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c) {
+            tma_load_2d(sbase + C::kKOff + c * 16384, &tm_k, bar(C::kBKVFull), hk * D + c * 64,
+                        kt * 128);
+            tma_load_2d(sbase + C::kVOff + c * 16384, &tm_v, bar(C::kBKVFull), hk * D + c * 64,
+                        kt * 128);
+          }
         }
-        ++kv_cnt;
-        const int n_it = (se - sb) * g;
-        for (int i = 0; i < n_it; ++i) {
-          const int qt = P.steps[sb + i / g].x;
-          const int h = hk * g + i % g;
-          const int qs = q_cnt % C::kQStages;
-          if (!(ok = mbar_wait(bar(C::kBQEmpty + qs), ((q_cnt / C::kQStages) & 1) ^ 1, ctl, 401)))
-            break;
-          mbar_arrive_expect_tx(bar(C::kBQFull + qs), C::kTileBytes);
+      }
+      if (!(ok = __shfl_sync(pm, ok, 0))) break;
+      ++kv_cnt;
+      const int n_it = (se - sb) * g;
+      for (int i = 0; i < n_it; ++i) {
+        const int4 stp = P.steps[sb + i / g];
+        const int qt = stp.x;
+        const int h = hk * g + i % g;
+        const bool gat = kGather && stp.w > 0;
+        // this lane's query block (read while the ring slots are awaited)
+        const int y = gat && lane < kGatherSlots
+                          ? P.bgathers[(size_t)(stp.w - 1) * kBGatherWords + lane] : 0;
+        const int qs = q_cnt % C::kQStages;
+        if (lane == 0) {
+          ok = mbar_wait(bar(C::kBQEmpty + qs), ((q_cnt / C::kQStages) & 1) ^ 1, ctl, 401);
+          if (ok) mbar_arrive_expect_tx(bar(C::kBQFull + qs), C::kTileBytes);
+        }
+        if (!(ok = __shfl_sync(pm, ok, 0))) break;
+        __syncwarp(pm);
+        if (gat) {
+          if (lane < kGatherSlots)
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_2d(sbase + C::kQOff + qs * C::kTileBytes + c * 16384 + lane * 1024, &tm_q8,
+                          bar(C::kBQFull + qs), h * D + c * 64, y);
+        } else if (lane == 0) {
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_2d(sbase + C::kQOff + qs * C::kTileBytes + c * 16384, &tm_q,
                         bar(C::kBQFull + qs), h * D + c * 64, qt * 128);
-          ++q_cnt;
-          const int ds = do_cnt % C::kDOStages;
-          if (!(ok = mbar_wait(bar(C::kBDOEmpty + ds), ((do_cnt / C::kDOStages) & 1) ^ 1, ctl,
-                               402)))
-            break;
-          mbar_arrive_expect_tx(bar(C::kBDOFull + ds), C::kTileBytes + C::kLseStageBytes);
+        }
+        ++q_cnt;
+        const int ds = do_cnt % C::kDOStages;
+        if (lane == 0) {
+          ok = mbar_wait(bar(C::kBDOEmpty + ds), ((do_cnt / C::kDOStages) & 1) ^ 1, ctl, 402);
+          if (ok) mbar_arrive_expect_tx(bar(C::kBDOFull + ds), C::kTileBytes + C::kLseStageBytes);
+        }
+        if (!(ok = __shfl_sync(pm, ok, 0))) break;
+        __syncwarp(pm);
+        const uint32_t ls = sbase + C::kLseOff + ds * C::kLseStageBytes;
+        if (gat) {
+          if (lane < kGatherSlots) {
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_2d(sbase + C::kDOOff + ds * C::kTileBytes + c * 16384 + lane * 1024,
+                          &tm_do8, bar(C::kBDOFull + ds), h * D + c * 64, y);
+            const size_t row = (size_t)h * P.qpad + (y > 0 ? y : 0);
+            bulk_load(ls + lane * 32, P.nlse2 + row, 32, bar(C::kBDOFull + ds));
+            bulk_load(ls + 512 + lane * 32, P.ndelta + row, 32, bar(C::kBDOFull + ds));
+          }
+        } else if (lane == 0) {
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_2d(sbase + C::kDOOff + ds * C::kTileBytes + c * 16384, &tm_do,
                         bar(C::kBDOFull + ds), h * D + c * 64, qt * 128);
-          const uint32_t ls = sbase + C::kLseOff + ds * C::kLseStageBytes;
           bulk_load(ls, P.nlse2 + (size_t)h * P.qpad + qt * 128, 512, bar(C::kBDOFull + ds));
           bulk_load(ls + 512, P.ndelta + (size_t)h * P.qpad + qt * 128, 512,
                     bar(C::kBDOFull + ds));
-          ++do_cnt;
         }
+        ++do_cnt;
       }
-      if (!ok) {
-        if (kv_cnt > 0) drain_wait_b(bar(C::kBKVFull), (kv_cnt - 1) & 1, kDrainNs);
-        for (uint32_t i = q_cnt > (uint32_t)C::kQStages ? q_cnt - C::kQStages : 0; i < q_cnt; ++i)
-          drain_wait_b(bar(C::kBQFull + i % C::kQStages), (i / C::kQStages) & 1, kDrainNs);
-        for (uint32_t i = do_cnt > (uint32_t)C::kDOStages ? do_cnt - C::kDOStages : 0; i < do_cnt;
-             ++i)
-          drain_wait_b(bar(C::kBDOFull + i % C::kDOStages), (i / C::kDOStages) & 1, kDrainNs);
-      }
+    }
+    if (!ok && lane == 0) {
+      if (kv_cnt > 0) drain_wait_b(bar(C::kBKVFull), (kv_cnt - 1) & 1, kDrainNs);
+      for (uint32_t i = q_cnt > (uint32_t)C::kQStages ? q_cnt - C::kQStages : 0; i < q_cnt; ++i)
+        drain_wait_b(bar(C::kBQFull + i % C::kQStages), (i / C::kQStages) & 1, kDrainNs);
+      for (uint32_t i = do_cnt > (uint32_t)C::kDOStages ? do_cnt - C::kDOStages : 0; i < do_cnt;
+           ++i)
+        drain_wait_b(bar(C::kBDOFull + i % C::kDOStages), (i / C::kDOStages) & 1, kDrainNs);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -447,7 +501,12 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
         if (i + 1 < n_it) st_next = P.steps[sb + (i + 1) / g];  // prefetch the next descriptor
         const int qt = st.x, info = st.y;
         uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
-        if (info & 1) step_mask<false>(info, P.slices, P.masks, key, qt, vb);
+        if (info & 1) {
+          if (kGather && st.w > 0)
+            gather_key_mask(P.bgathers + (size_t)(st.w - 1) * kBGatherWords, j, P.Tq, vb);
+          else
+            step_mask<false>(info, P.slices, P.masks, key, qt, vb);
+        }
         const float* nl = reinterpret_cast<const float*>(
             smem + C::kLseOff + (sdp_cnt % C::kDOStages) * C::kLseStageBytes);
         const float* nd = nl + 128;
@@ -1149,11 +1208,13 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
       if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
     }
   }
-  alignas(64) CUtensorMap tq, tk, tv, tdo, tk8, tv8;
+  alignas(64) CUtensorMap tq, tk, tv, tdo, tk8, tv8, tq8, tdo8;
   if (!encode_tile_map(&tq, q, p->Tq, p->Hq * D) || !encode_tile_map(&tk, k, p->Tk, p->Hkv * D) ||
       !encode_tile_map(&tv, v, p->Tk, p->Hkv * D) || !encode_tile_map(&tdo, dout, p->Tq, p->Hq * D) ||
       !encode_tile_map(&tk8, k, p->Tk, p->Hkv * D, kGatherKeys) ||
-      !encode_tile_map(&tv8, v, p->Tk, p->Hkv * D, kGatherKeys))
+      !encode_tile_map(&tv8, v, p->Tk, p->Hkv * D, kGatherKeys) ||
+      !encode_tile_map(&tq8, q, p->Tq, p->Hq * D, kGatherKeys) ||
+      !encode_tile_map(&tdo8, dout, p->Tq, p->Hq * D, kGatherKeys))
     return FFA_ERR_INVALID_ARG;
   const float scale_log2 = scale * kLog2e;
   {
@@ -1166,6 +1227,8 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     P.n_items = (int)p->n_bwd_items;
     P.slices = p->slices;
     P.masks = p->bwd_masks;
+    P.bgathers = p->bgathers;
+    P.Tq = p->Tq;
     P.Tk = p->Tk;
     P.Hkv = p->Hkv;
     P.g = p->Hq / p->Hkv;
@@ -1179,13 +1242,18 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     P.dv = static_cast<__nv_bfloat16*>(dv);
     P.err = p->err;
     P.wait_ns = p->wait_ns;
-    if (cudaFuncSetAttribute(ffa_bwd_dkdv_kernel<D, kCap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes) != cudaSuccess)
+    // the dK/dV pass gathers when the backward lists have gathered steps
+    const bool bg = p->n_bgathers > 0;
+    auto kern = bg ? ffa_bwd_dkdv_kernel<D, kCap, true> : ffa_bwd_dkdv_kernel<D, kCap, false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
       return FFA_ERR_CUDA;
-    if (!split_regs_ok<ffa_bwd_dkdv_kernel<D, kCap>>()) return FFA_ERR_UNSUPPORTED;
+    if (!(bg ? split_regs_ok<ffa_bwd_dkdv_kernel<D, kCap, true>>()
+             : split_regs_ok<ffa_bwd_dkdv_kernel<D, kCap, false>>()))
+      return FFA_ERR_UNSUPPORTED;
     if (cudaMemsetAsync(P.ticket, 0, sizeof(int), st) != cudaSuccess) return FFA_ERR_CUDA;
     record_phase(p, 3, st);
-    ffa_bwd_dkdv_kernel<D, kCap><<<p->grid_bwd, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, P);
+    kern<<<p->grid_bwd, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tq8, tdo8, P);
     note_launches(1);
     if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   }

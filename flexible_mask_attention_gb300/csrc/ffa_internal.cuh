@@ -34,6 +34,12 @@ __host__ __device__ constexpr int visit_list_info(int m) { return (m << 2) | 3; 
 constexpr int kGatherKeys = 8;
 constexpr int kGatherSlots = 16;
 constexpr int kGatherWords = kGatherSlots + 2 * kGatherSlots * 4;
+// Gathered backward steps (step.w = r + 1 > 0 in the k-tile's list): the
+// transpose, for k-tiles whose slices are all FULL with 8-row aligned query
+// ranges.  Record r (kBGatherWords int32): kGatherSlots query-block start
+// rows (-kGatherKeys: unused), then kGatherSlots x 4 words of key bits (bit i
+// of word w: key 32w + i of the k-tile is seen by the slot's rows).
+constexpr int kBGatherWords = kGatherSlots + kGatherSlots * 4;
 constexpr int kGatherMaxBlocks = 2048;  // 8-key blocks per gathered unit
 constexpr int kGatherMaxTk = 1 << 19;   // key count up to which units may gather
 
@@ -124,6 +130,34 @@ __device__ __forceinline__ void gather_mask(const int* __restrict__ rec, int h, 
   }
 }
 
+// Visible columns of a gathered backward step for key `key_in` of the
+// k-tile: slot s holds query rows [start_s, start_s + 8) in columns
+// [8s, 8s + 8); set when the key's bit is set, rows at or past Tq never.
+__device__ __forceinline__ void gather_key_mask(const int* __restrict__ rec, int key_in, int Tq,
+                                                uint32_t (&b)[4]) {
+  int y[kGatherSlots];
+  uint32_t bits[kGatherSlots];
+  const int4* r4 = reinterpret_cast<const int4*>(rec);
+#pragma unroll
+  for (int q = 0; q < kGatherSlots / 4; ++q) {
+    const int4 v = r4[q];
+    y[4 * q] = v.x;
+    y[4 * q + 1] = v.y;
+    y[4 * q + 2] = v.z;
+    y[4 * q + 3] = v.w;
+  }
+  const int* keys = rec + kGatherSlots + (key_in >> 5);
+#pragma unroll
+  for (int s = 0; s < kGatherSlots; ++s) bits[s] = (uint32_t)keys[4 * s];
+  b[0] = b[1] = b[2] = b[3] = 0u;
+#pragma unroll
+  for (int s = 0; s < kGatherSlots; ++s) {
+    const int valid = max(0, min(kGatherKeys, Tq - y[s]));
+    const uint32_t on = (y[s] >= 0) && ((bits[s] >> (key_in & 31)) & 1u) ? 1u : 0u;
+    b[s >> 2] |= (((1u << valid) - 1u) & (0u - on)) << (kGatherKeys * (s & 3));
+  }
+}
+
 __device__ __forceinline__ bool mask_bit(const uint32_t (&b)[4], int c) {
   return (b[c >> 5] >> (c & 31)) & 1u;
 }
@@ -172,6 +206,8 @@ struct ffa_plan_s {
   int64_t n_fwd_masks = 0;
   int* gathers = nullptr;  // gathered step records [n_gathers][kGatherWords]
   int64_t n_gathers = 0;
+  int* bgathers = nullptr;  // gathered backward records [n_bgathers][kBGatherWords]
+  int64_t n_bgathers = 0;
   int4* bwd_steps = nullptr;
   int64_t n_bwd_steps = 0;
   int* bwd_masks = nullptr;  // slice lists of multi-slice backward visits

@@ -548,17 +548,23 @@ __global__ void k_split_fill(const int* __restrict__ items, int n_items,
 
 // ---- backward items ---------------------------------------------------------
 __global__ void k_bwd_items(int n_kt, int Hkv, int g, const int2* __restrict__ visits,
-                            const int* __restrict__ off, const int* __restrict__ cnt,
+                            const int* __restrict__ voff, const int* __restrict__ vcnt,
+                            const int* __restrict__ soff, const int* __restrict__ gcnt,
                             int4* steps, int* items) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= n_kt * Hkv) return;
   const int kt = idx / Hkv, hk = idx % Hkv;
-  const int b = off[kt], n = cnt[kt];
-  int c = 0;
-  for (int i = 0; i < n; ++i) {
-    const int2 v = visits[b + i];
-    c += visit_cost(v.y);
-    if (hk == 0) steps[b + i] = make_int4(v.x, v.y, 0, 0);
+  const int b = soff[kt], ng = gcnt[kt];
+  int c = 0, n = ng;
+  if (ng > 0) {  // gathered k-tile: its steps are k_bgather_fill's
+    c = kPartialCost * ng;
+  } else {
+    n = vcnt[kt];
+    for (int i = 0; i < n; ++i) {
+      const int2 v = visits[voff[kt] + i];
+      c += visit_cost(v.y);
+      if (hk == 0) steps[b + i] = make_int4(v.x, v.y, 0, 0);
+    }
   }
   int* it = items + (size_t)idx * kBiWords;
   it[kBiKt] = kt;
@@ -616,10 +622,13 @@ __device__ __forceinline__ GatherUnit gather_unit(int u, int pair_mode, int n_qt
 
 // Marks the unit's blocks in `bits` (cleared here); returns false (for the
 // whole block) if a slice is not eligible.
+// kBwd: the backward's transpose (the unit is a k-tile, the blocks are 8-row
+// query blocks of the slices' q ranges, T is Tq).
+template <bool kBwd = false>
 __device__ bool gather_bitmap(const Slice* __restrict__ sl, const int* __restrict__ list,
                               const int* __restrict__ loff, const int* __restrict__ lcnt,
-                              const GatherUnit& gu, int Tk, unsigned* bits) {
-  const int nwords = (((Tk + kGatherKeys - 1) / kGatherKeys) + 31) / 32;
+                              const GatherUnit& gu, int T, unsigned* bits) {
+  const int nwords = (((T + kGatherKeys - 1) / kGatherKeys) + 31) / 32;
   for (int w = threadIdx.x; w < nwords; w += blockDim.x) bits[w] = 0u;
   __syncthreads();
   bool bad = false;
@@ -628,11 +637,12 @@ __device__ bool gather_bitmap(const Slice* __restrict__ sl, const int* __restric
     const int n = lcnt[gu.qt[t]];
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
       const Slice x = sl[L[i]];
-      if (x.t != 0 || x.ks % kGatherKeys != 0 || (x.ke % kGatherKeys != 0 && x.ke != Tk)) {
+      const int lo = kBwd ? x.qs : x.ks, hi = kBwd ? x.qe : x.ke;
+      if (x.t != 0 || lo % kGatherKeys != 0 || (hi % kGatherKeys != 0 && hi != T)) {
         bad = true;
         continue;
       }
-      const int b0 = x.ks / kGatherKeys, b1 = (x.ke + kGatherKeys - 1) / kGatherKeys;
+      const int b0 = lo / kGatherKeys, b1 = (hi + kGatherKeys - 1) / kGatherKeys;
       for (int w = b0 >> 5; w <= (b1 - 1) >> 5; ++w) {
         const int lo = max(b0 - 32 * w, 0), hi = min(b1 - 32 * w, 32);
         const unsigned m = (hi == 32 ? 0xffffffffu : ((1u << hi) - 1u)) & ~((1u << lo) - 1u);
@@ -787,6 +797,122 @@ __global__ void __launch_bounds__(kGatherThreads)
   }
   __syncthreads();
   if (threadIdx.x < 2) cost_half[2 * u + threadIdx.x] = cost[threadIdx.x];
+}
+
+// Gathered backward units (one block per k-tile): the transpose of the
+// forward's.  A k-tile gathers when every slice of its list is FULL with qs
+// and qe multiples of kGatherKeys (qe may be Tq), it covers 1 ..
+// kGatherMaxBlocks query blocks and ceil(blocks / kGatherSlots) steps are at
+// most 2/3 of its visits.  bgcnt[kt] = gathered steps (0: regular);
+// bscnt[kt] = the k-tile's step count either way.
+__global__ void __launch_bounds__(kGatherThreads)
+    k_bgather_count(const Slice* __restrict__ sl, const int* __restrict__ list,
+                    const int* __restrict__ loff, const int* __restrict__ lcnt, int Tq,
+                    const int* __restrict__ vcnt, int* __restrict__ bgcnt,
+                    int* __restrict__ bscnt) {
+  __shared__ unsigned bits[kGatherBitmapWords];
+  __shared__ int red[kGatherThreads / 32];
+  const int kt = blockIdx.x;
+  GatherUnit gu;
+  gu.qt[0] = kt;
+  gu.qt[1] = -1;
+  gu.n_qt = 1;
+  const bool ok = gather_bitmap<true>(sl, list, loff, lcnt, gu, Tq, bits);
+  const int nwords = (((Tq + kGatherKeys - 1) / kGatherKeys) + 31) / 32;
+  const int n = ok ? block_popc(bits, nwords, red) : 0;
+  const int steps = (n + kGatherSlots - 1) / kGatherSlots;
+  const bool gather = ok && n > 0 && n <= kGatherMaxBlocks && 3 * steps <= 2 * vcnt[kt];
+  if (threadIdx.x == 0) {
+    bgcnt[kt] = gather ? steps : 0;
+    bscnt[kt] = gather ? steps : vcnt[kt];
+  }
+}
+
+// Steps and records of the gathered k-tiles: 16 query-block start rows, then
+// 16 x 4 words of key bits (the keys of the k-tile each slot's rows see).
+constexpr size_t kBGatherFillSmem =
+    sizeof(unsigned) * kGatherBitmapWords + sizeof(int) * kGatherBitmapWords +
+    sizeof(int) * kGatherMaxBlocks + sizeof(unsigned) * kGatherMaxBlocks * 4;
+
+__global__ void __launch_bounds__(kGatherThreads)
+    k_bgather_fill(const Slice* __restrict__ sl, const int* __restrict__ list,
+                   const int* __restrict__ loff, const int* __restrict__ lcnt, int Tq,
+                   const int* __restrict__ bgcnt, const int* __restrict__ bgoff,
+                   const int* __restrict__ bsoff, int4* steps, int* __restrict__ records) {
+  extern __shared__ unsigned gsm[];
+  unsigned* bits = gsm;
+  int* woff = reinterpret_cast<int*>(bits + kGatherBitmapWords);
+  int* start = woff + kGatherBitmapWords;
+  unsigned* kmask = reinterpret_cast<unsigned*>(start + kGatherMaxBlocks);  // [blocks][4]
+  __shared__ int red[kGatherThreads / 32];
+  const int kt = blockIdx.x;
+  const int n_steps = bgcnt[kt];
+  if (n_steps == 0) return;  // whole block
+  GatherUnit gu;
+  gu.qt[0] = kt;
+  gu.qt[1] = -1;
+  gu.n_qt = 1;
+  gather_bitmap<true>(sl, list, loff, lcnt, gu, Tq, bits);
+  const int nwords = (((Tq + kGatherKeys - 1) / kGatherKeys) + 31) / 32;
+  {  // exclusive prefix of the words' bit counts
+    const int per = (nwords + blockDim.x - 1) / blockDim.x;
+    const int w0 = threadIdx.x * per, w1 = min(nwords, w0 + per);
+    int c = 0;
+    for (int w = w0; w < w1; ++w) c += __popc(bits[w]);
+    int incl = c;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += y;
+    }
+    if (lane == 31) red[wid] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int i = 0; i < wid; ++i) base += red[i];
+    int run = base + incl - c;
+    for (int w = w0; w < w1; ++w) {
+      woff[w] = run;
+      run += __popc(bits[w]);
+    }
+  }
+  const int n = n_steps * kGatherSlots;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) start[i] = -kGatherKeys;
+  for (int i = threadIdx.x; i < n * 4; i += blockDim.x) kmask[i] = 0u;
+  __syncthreads();
+  for (int w = threadIdx.x; w < nwords; w += blockDim.x) {
+    unsigned m = bits[w];
+    int pos = woff[w];
+    while (m) {
+      start[pos++] = (32 * w + __ffs(m) - 1) * kGatherKeys;
+      m &= m - 1u;
+    }
+  }
+  {
+    const int* L = list + loff[kt];
+    const int cnt = lcnt[kt];
+    for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
+      const Slice x = sl[L[i]];
+      uint32_t kb[4] = {0u, 0u, 0u, 0u};
+      add_window(max(x.ks, 128 * kt) - 128 * kt, min(x.ke, 128 * kt + 128) - 128 * kt, kb);
+      const int b0 = x.qs / kGatherKeys, b1 = (x.qe + kGatherKeys - 1) / kGatherKeys;
+      for (int b = b0; b < b1; ++b) {
+        const int w = b >> 5;
+        const int pos = woff[w] + __popc(bits[w] & ((1u << (b & 31)) - 1u));
+        for (int k = 0; k < 4; ++k)
+          if (kb[k]) atomicOr(&kmask[pos * 4 + k], kb[k]);
+      }
+    }
+  }
+  __syncthreads();
+  const int r0 = bgoff[kt], s0 = bsoff[kt];
+  for (int i = threadIdx.x; i < n_steps * kBGatherWords; i += blockDim.x) {
+    const int j = i / kBGatherWords, o = i % kBGatherWords;
+    const int v = o < kGatherSlots ? start[j * kGatherSlots + o]
+                                   : (int)kmask[(j * kGatherSlots) * 4 + (o - kGatherSlots)];
+    records[(size_t)(r0 + j) * kBGatherWords + o] = v;
+  }
+  for (int j = threadIdx.x; j < n_steps; j += blockDim.x)
+    steps[s0 + j] = make_int4(0, 1, 0, r0 + j + 1);
 }
 
 // ---- ordering ---------------------------------------------------------------
@@ -968,7 +1094,7 @@ void free_plan(ffa_plan_s* p) {
   if (!p) return;
   void* bufs[] = {p->slices, p->fwd_steps, p->fwd_items, p->fwd_order, p->merges,
                   p->bwd_steps, p->bwd_items, p->bwd_order, p->err, p->fwd_masks,
-                  p->bwd_masks, p->dq_counts, p->tickets, p->gathers};
+                  p->bwd_masks, p->dq_counts, p->tickets, p->gathers, p->bgathers};
   for (void* b : bufs)
     if (b) cudaFree(b);
   if (!p->dq_alias) {
@@ -1241,9 +1367,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   if ((rc = read_to_host(bm, dtot, sizeof bm, st))) return rc;
   tot = bm[0];
   if (tot > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
-  p->n_bwd_steps = tot;
   FFA_CUDA(bvis.alloc(sizeof(int2) * (size_t)tot));
-  FFA_CUDA(cudaMallocAsync(&p->bwd_steps, sizeof(int4) * (size_t)std::max(1LL, tot), st));
   const long long bmtot = bm[1];
   if (bmtot > (1LL << 29)) return FFA_ERR_UNSUPPORTED;
   p->n_bwd_masks = bmtot;
@@ -1252,15 +1376,52 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
       p->slices, klist.as<int>(), kloff.as<int>(), klcnt.as<int>(), n_kt, nullptr, nullptr,
       boff.as<int>(), bmoff.as<int>(), bvis.as<int2>(), p->bwd_masks);
   note_launches(1);
+  // gathered k-tiles (full slices, 8-row aligned query ranges): their step
+  // counts replace the visit counts before the step offsets are scanned
+  DevBuf bgcnt(st), bgoff(st), bscnt(st), bsoff(st);
+  FFA_CUDA(bgcnt.alloc(sizeof(int) * n_kt));
+  FFA_CUDA(bgoff.alloc(sizeof(int) * n_kt));
+  FFA_CUDA(bscnt.alloc(sizeof(int) * n_kt));
+  FFA_CUDA(bsoff.alloc(sizeof(int) * n_kt));
+  if (p->Tq <= kGatherMaxTk && n_kt > 0) {
+    k_bgather_count<<<n_kt, kGatherThreads, 0, st>>>(p->slices, klist.as<int>(), kloff.as<int>(),
+                                                     klcnt.as<int>(), p->Tq, bcnt.as<int>(),
+                                                     bgcnt.as<int>(), bscnt.as<int>());
+    note_launches(1);
+    FFA_CUDA(cudaGetLastError());
+  } else {
+    FFA_CUDA(cudaMemsetAsync(bgcnt.p, 0, sizeof(int) * n_kt, st));
+    FFA_CUDA(cudaMemcpyAsync(bscnt.p, bcnt.p, sizeof(int) * n_kt, cudaMemcpyDeviceToDevice, st));
+  }
+  long long bs[2];  // steps, gathered records
+  if ((rc = scan_launch(bscnt.as<int>(), n_kt, bsoff.as<int>(), dtot, st))) return rc;
+  if ((rc = scan_launch(bgcnt.as<int>(), n_kt, bgoff.as<int>(), dtot + 1, st))) return rc;
+  if ((rc = read_to_host(bs, dtot, sizeof bs, st))) return rc;
+  if (bs[0] > 0x7fffffffLL || bs[1] > (1LL << 24)) return FFA_ERR_UNSUPPORTED;
+  p->n_bwd_steps = bs[0];
+  p->n_bgathers = bs[1];
+  FFA_CUDA(cudaMallocAsync(&p->bwd_steps, sizeof(int4) * (size_t)std::max(1LL, bs[0]), st));
+  FFA_CUDA(cudaMallocAsync(&p->bgathers,
+                           sizeof(int) * kBGatherWords * (size_t)std::max(1LL, bs[1]), st));
   const long long nb_items = (long long)n_kt * p->Hkv;
   p->n_bwd_items = nb_items;
   FFA_CUDA(cudaMallocAsync(&p->bwd_items, sizeof(int) * kBiWords * (size_t)std::max(1LL, nb_items), st));
   FFA_CUDA(cudaMallocAsync(&p->bwd_order, sizeof(int) * (size_t)std::max(1LL, nb_items), st));
   k_bwd_items<<<grid_for(nb_items, 128), 128, 0, st>>>(n_kt, p->Hkv, g, bvis.as<int2>(),
                                                        boff.as<int>(), bcnt.as<int>(),
+                                                       bsoff.as<int>(), bgcnt.as<int>(),
                                                        p->bwd_steps, p->bwd_items);
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
+  if (bs[1] > 0) {
+    FFA_CUDA(cudaFuncSetAttribute(k_bgather_fill, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kBGatherFillSmem));
+    k_bgather_fill<<<n_kt, kGatherThreads, kBGatherFillSmem, st>>>(
+        p->slices, klist.as<int>(), kloff.as<int>(), klcnt.as<int>(), p->Tq, bgcnt.as<int>(),
+        bgoff.as<int>(), bsoff.as<int>(), p->bwd_steps, p->bgathers);
+    note_launches(1);
+    FFA_CUDA(cudaGetLastError());
+  }
   rc = sort_items(p->bwd_items, kBiWords, kBiCost, kBiHkv, 1, (int)nb_items, p->bwd_order, st);
   if (rc != FFA_OK) return rc;
   p->grid_fwd = (int)std::max(1LL, std::min<long long>(p->num_sms, final_items));
@@ -1396,6 +1557,7 @@ ffa_status_t ffa_plan_info(ffa_plan_t p, ffa_plan_info_t* info) {
   info->fwd_masks = p->n_fwd_masks;
   info->bwd_masks = p->n_bwd_masks;
   info->gathers = p->n_gathers;
+  info->bgathers = p->n_bgathers;
   return FFA_OK;
 }
 
@@ -1416,6 +1578,7 @@ ffa_status_t ffa_plan_export(ffa_plan_t p, int32_t which, int32_t* dst, int64_t 
     case 7: src = p->fwd_masks; words = p->n_fwd_masks; break;
     case 8: src = p->bwd_masks; words = p->n_bwd_masks; break;
     case 9: src = p->gathers; words = kGatherWords * p->n_gathers; break;
+    case 10: src = p->bgathers; words = kBGatherWords * p->n_bgathers; break;
     default: return FFA_ERR_INVALID_ARG;
   }
   *written = words;

@@ -106,6 +106,7 @@ typedef struct {
   int64_t fwd_masks;  /* words of the forward slice lists (multi-slice visits) */
   int64_t bwd_masks;  /* words of the backward slice lists */
   int64_t gathers;    /* gathered forward step records, 144 words each */
+  int64_t bgathers;   /* gathered backward step records, 80 words each */
 } ffa_plan_info_t;
 
 ffa_status_t ffa_plan_info(ffa_plan_t plan, ffa_plan_info_t* info);
@@ -113,7 +114,7 @@ ffa_status_t ffa_plan_info(ffa_plan_t plan, ffa_plan_info_t* info);
 /* Copy one work list to HOST memory (used to check the planner bit for bit).
  *   which: 0 fwd steps, 1 fwd items, 2 fwd order, 3 bwd steps, 4 bwd items,
  *          5 bwd order, 6 merge groups, 7 fwd slice lists, 8 bwd slice lists,
- *          9 gathered step records.
+ *          9 gathered forward step records, 10 gathered backward step records.
  *   A step's visit info is (s << 2) | partial when one slice s sees the tile
  *   pair, or (m << 2) | 3 when several do; then list[m] = n and list[m+1 ..
  *   m+n] are their slice indices, ascending (the tile is computed once and
@@ -125,6 +126,12 @@ ffa_status_t ffa_plan_info(ffa_plan_t plan, ffa_plan_info_t* info);
  *   then for each half 16 x 4 words of row bits (bit i of word w: row
  *   32 w + i of the half's q-tile sees that block); info_h is 1 when half h
  *   has a row bit set, else -1.
+ *   Gathered backward steps, the transpose (a k-tile whose slices are all FULL
+ *   with query ranges aligned to 8 rows, when that takes at most 2/3 of its
+ *   visits): step (0, 1, 0, r + 1) computes 16 blocks of 8 query rows packed
+ *   into one Q / dO tile; record r holds the 16 block start rows (-8: unused)
+ *   then 16 x 4 words of key bits (bit i of word w: key 32 w + i of the
+ *   k-tile is seen by that block's rows).
  *   dst: host int32 buffer of `capacity` words; *written receives the count.
  * Synchronises the plan's stream. */
 ffa_status_t ffa_plan_export(ffa_plan_t plan, int32_t which, int32_t* dst, int64_t capacity,

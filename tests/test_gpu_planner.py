@@ -10,7 +10,7 @@ from oracle import planner
 pytestmark = pytest.mark.gpu
 
 NAMES = ["fwd_steps", "fwd_items", "fwd_order", "bwd_steps", "bwd_items", "bwd_order", "merges",
-         "fwd_masks", "bwd_masks", "gathers"]
+         "fwd_masks", "bwd_masks", "gathers", "bgathers"]
 
 
 def compare(qr, kr, ty, Tq, Tk, Hq, Hkv, D, split_below=0):
