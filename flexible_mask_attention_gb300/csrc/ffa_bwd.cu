@@ -48,7 +48,8 @@ __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity, uint
 // Warp roles (384 threads): warps 0-7 P/dS in two warpgroups (thread = key =
 // TMEM lane; warpgroup w owns query columns [64w, 64w+64)) and the dK/dV
 // epilogue, warp 8 TMA producer, warp 9 MMA issuer (TMEM owner), warps 10-11
-// idle; registers split 200 / 104 between them (ffa_ptx.cuh).
+// loaders of dO and of -lse2 / -delta for plans with gathered steps (idle
+// otherwise); registers split 200 / 104 between them (ffa_ptx.cuh).
 // TMEM columns: dV [0,D), dK [D,2D), S^T [2D,2D+128), dP^T [2D+128,2D+256).
 // Warpgroup w owns dP^T columns [64w, 64w+64) of that range and, once it has
 // read a 32-column chunk, overwrites the chunk with bf16 pairs: dS^T in its
@@ -228,7 +229,8 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
     mbar_init(bar(C::kBSFull), 1);
     for (int s = 0; s < kItemRing; ++s) {
       mbar_init(bar(C::kBItemFull + s), 1);
-      mbar_init(bar(C::kBItemEmpty + s), 1 + 256);  // MMA thread + elementwise threads
+      // MMA thread + elementwise threads (+ lane 0 of the dO and -lse2 / -delta warps)
+      mbar_init(bar(C::kBItemEmpty + s), 1 + 256 + (kGather ? 2 : 0));
     }
     mbar_init(bar(C::kBSFree), 256);
     mbar_init(bar(C::kBPFull), 256);
@@ -250,22 +252,39 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
 
   if (warp >= 8) {
   reg_dealloc<kSplitNarrowRegs>();
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    // Lane 0 draws the items, waits on the rings and sets each barrier's
-    // byte count.  With gathered steps the whole warp runs the loop, and the
-    // 16 query blocks of a gathered Q / dO tile (8 rows each at 1024-byte
-    // aligned slots; unused ones read zero rows from row -8) and their
-    // 32-byte pieces of -lse2 and -delta (unused ones copy row 0's, finite
-    // values that their masked columns never use) are copied by lanes 0-15
-    // after a __syncwarp that orders them behind the byte count.
+  if (warp == 8 || (kGather && warp >= 10)) {
+    // ------------------------------------------------------------ producers
+    // Warp 8 draws the items and loads K / V and Q; it loads dO, -lse2 and
+    // -delta too unless the plan has gathered steps.  Each lane-issued copy
+    // costs the issuing warp some 60 cycles, so with gathered steps (16
+    // query blocks of 8 rows per tile: 2 x 16 boxes per tile with D = 128)
+    // the dO tiles go to warp 10 and their -lse2 / -delta pieces to warp 11,
+    // which take the items from the work queue like the consumers and wait
+    // on the dO ring themselves.  Lane 0 of the loading warp waits on the
+    // rings and sets each barrier's byte count (warp 10 for the dO ring: a
+    // barrier may see warp 11's bytes before that, its phase cannot complete
+    // without the arrival).  Without gathered steps lane 0 alone runs the
+    // loop; with them the whole warp does, and the 16 query blocks of a
+    // gathered tile (8 rows each at 1024-byte aligned slots; unused ones read
+    // zero rows from row -8) and their 32-byte pieces of -lse2 and -delta
+    // (unused ones copy row 0's, finite values that their masked columns
+    // never use) are copied by lanes 0-15 after a __syncwarp that orders
+    // them behind the waits.
+    const int role = warp == 8 ? 0 : warp - 9;  // 0: items, K/V, Q; 1: dO; 2: -lse2, -delta
+    const bool load_q = role == 0;
+    const bool load_do = kGather ? role == 1 : true;
+    const bool load_lse = kGather ? role == 2 : true;
     if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      prefetch_tmap(&tm_do);
-      prefetch_tmap(&tm_q8);
-      prefetch_tmap(&tm_do8);
+      if (role == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_q8);
+      }
+      if (load_do) {
+        prefetch_tmap(&tm_do);
+        prefetch_tmap(&tm_do8);
+      }
     }
     uint32_t kv_cnt = 0, q_cnt = 0, do_cnt = 0;  // tiles issued
     bool ok = true;
@@ -274,9 +293,13 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
     for (int r = 0; ok; ++r) {
       int idx = -1;
       if (lane == 0) {
-        const int pos = atomicAdd(P.ticket, 1);
-        idx = pos < P.n_items ? P.order[pos] : -1;
-        ok = queue_publish(queue, r, idx, ctl, 409);
+        if (role == 0) {
+          const int pos = atomicAdd(P.ticket, 1);
+          idx = pos < P.n_items ? P.order[pos] : -1;
+          ok = queue_publish(queue, r, idx, ctl, 409);
+        } else {
+          ok = queue_take(queue, r, idx, ctl, 409 + role);
+        }
       }
       ok = __shfl_sync(pm, ok, 0);
       idx = __shfl_sync(pm, idx, 0);
@@ -285,20 +308,22 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
       const int sb = it[kBiStepBeg], se = it[kBiStepEnd];
       if (se <= sb) continue;
       const int kt = it[kBiKt], hk = it[kBiHkv];
-      if (lane == 0) {
-        ok = mbar_wait(bar(C::kBKVEmpty), (kv_cnt & 1) ^ 1, ctl, 400);
-        if (ok) {
-          mbar_arrive_expect_tx(bar(C::kBKVFull), 2 * C::kTileBytes);
-          for (int c = 0; c < C::kChunks; ++c) {
-            tma_load_2d(sbase + C::kKOff + c * 16384, &tm_k, bar(C::kBKVFull), hk * D + c * 64,
-                        kt * 128);
-            tma_load_2d(sbase + C::kVOff + c * 16384, &tm_v, bar(C::kBKVFull), hk * D + c * 64,
-                        kt * 128);
+      if (role == 0) {
+        if (lane == 0) {
+          ok = mbar_wait(bar(C::kBKVEmpty), (kv_cnt & 1) ^ 1, ctl, 400);
+          if (ok) {
+            mbar_arrive_expect_tx(bar(C::kBKVFull), 2 * C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c) {
+              tma_load_2d(sbase + C::kKOff + c * 16384, &tm_k, bar(C::kBKVFull), hk * D + c * 64,
+                          kt * 128);
+              tma_load_2d(sbase + C::kVOff + c * 16384, &tm_v, bar(C::kBKVFull), hk * D + c * 64,
+                          kt * 128);
+            }
           }
         }
+        if (!(ok = __shfl_sync(pm, ok, 0))) break;
+        ++kv_cnt;
       }
-      if (!(ok = __shfl_sync(pm, ok, 0))) break;
-      ++kv_cnt;
       const int n_it = (se - sb) * g;
       for (int i = 0; i < n_it; ++i) {
         const int4 stp = P.steps[sb + i / g];
@@ -308,53 +333,67 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
         // this lane's query block (read while the ring slots are awaited)
         const int y = gat && lane < kGatherSlots
                           ? P.bgathers[(size_t)(stp.w - 1) * kBGatherWords + lane] : 0;
-        const int qs = q_cnt % C::kQStages;
-        if (lane == 0) {
-          ok = mbar_wait(bar(C::kBQEmpty + qs), ((q_cnt / C::kQStages) & 1) ^ 1, ctl, 401);
-          if (ok) mbar_arrive_expect_tx(bar(C::kBQFull + qs), C::kTileBytes);
-        }
-        if (!(ok = __shfl_sync(pm, ok, 0))) break;
-        __syncwarp(pm);
-        if (gat) {
-          if (lane < kGatherSlots)
-            for (int c = 0; c < C::kChunks; ++c)
-              tma_load_2d(sbase + C::kQOff + qs * C::kTileBytes + c * 16384 + lane * 1024, &tm_q8,
-                          bar(C::kBQFull + qs), h * D + c * 64, y);
-        } else if (lane == 0) {
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_2d(sbase + C::kQOff + qs * C::kTileBytes + c * 16384, &tm_q,
-                        bar(C::kBQFull + qs), h * D + c * 64, qt * 128);
-        }
-        ++q_cnt;
-        const int ds = do_cnt % C::kDOStages;
-        if (lane == 0) {
-          ok = mbar_wait(bar(C::kBDOEmpty + ds), ((do_cnt / C::kDOStages) & 1) ^ 1, ctl, 402);
-          if (ok) mbar_arrive_expect_tx(bar(C::kBDOFull + ds), C::kTileBytes + C::kLseStageBytes);
-        }
-        if (!(ok = __shfl_sync(pm, ok, 0))) break;
-        __syncwarp(pm);
-        const uint32_t ls = sbase + C::kLseOff + ds * C::kLseStageBytes;
-        if (gat) {
-          if (lane < kGatherSlots) {
-            for (int c = 0; c < C::kChunks; ++c)
-              tma_load_2d(sbase + C::kDOOff + ds * C::kTileBytes + c * 16384 + lane * 1024,
-                          &tm_do8, bar(C::kBDOFull + ds), h * D + c * 64, y);
-            const size_t row = (size_t)h * P.qpad + (y > 0 ? y : 0);
-            bulk_load(ls + lane * 32, P.nlse2 + row, 32, bar(C::kBDOFull + ds));
-            bulk_load(ls + 512 + lane * 32, P.ndelta + row, 32, bar(C::kBDOFull + ds));
+        if (load_q) {
+          const int qs = q_cnt % C::kQStages;
+          if (lane == 0) {
+            ok = mbar_wait(bar(C::kBQEmpty + qs), ((q_cnt / C::kQStages) & 1) ^ 1, ctl, 401);
+            if (ok) mbar_arrive_expect_tx(bar(C::kBQFull + qs), C::kTileBytes);
           }
-        } else if (lane == 0) {
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_2d(sbase + C::kDOOff + ds * C::kTileBytes + c * 16384, &tm_do,
-                        bar(C::kBDOFull + ds), h * D + c * 64, qt * 128);
-          bulk_load(ls, P.nlse2 + (size_t)h * P.qpad + qt * 128, 512, bar(C::kBDOFull + ds));
-          bulk_load(ls + 512, P.ndelta + (size_t)h * P.qpad + qt * 128, 512,
-                    bar(C::kBDOFull + ds));
+          if (!(ok = __shfl_sync(pm, ok, 0))) break;
+          __syncwarp(pm);
+          if (gat) {
+            if (lane < kGatherSlots)
+              for (int c = 0; c < C::kChunks; ++c)
+                tma_load_2d(sbase + C::kQOff + qs * C::kTileBytes + c * 16384 + lane * 1024,
+                            &tm_q8, bar(C::kBQFull + qs), h * D + c * 64, y);
+          } else if (lane == 0) {
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_2d(sbase + C::kQOff + qs * C::kTileBytes + c * 16384, &tm_q,
+                          bar(C::kBQFull + qs), h * D + c * 64, qt * 128);
+          }
+          ++q_cnt;
         }
-        ++do_cnt;
+        if (load_do || load_lse) {
+          const int ds = do_cnt % C::kDOStages;
+          if (lane == 0) {
+            ok = mbar_wait(bar(C::kBDOEmpty + ds), ((do_cnt / C::kDOStages) & 1) ^ 1, ctl, 402);
+            if (ok && load_do)
+              mbar_arrive_expect_tx(bar(C::kBDOFull + ds), C::kTileBytes + C::kLseStageBytes);
+          }
+          if (!(ok = __shfl_sync(pm, ok, 0))) break;
+          __syncwarp(pm);
+          if (load_do) {
+            if (gat) {
+              if (lane < kGatherSlots)
+                for (int c = 0; c < C::kChunks; ++c)
+                  tma_load_2d(sbase + C::kDOOff + ds * C::kTileBytes + c * 16384 + lane * 1024,
+                              &tm_do8, bar(C::kBDOFull + ds), h * D + c * 64, y);
+            } else if (lane == 0) {
+              for (int c = 0; c < C::kChunks; ++c)
+                tma_load_2d(sbase + C::kDOOff + ds * C::kTileBytes + c * 16384, &tm_do,
+                            bar(C::kBDOFull + ds), h * D + c * 64, qt * 128);
+            }
+          }
+          if (load_lse) {
+            const uint32_t ls = sbase + C::kLseOff + ds * C::kLseStageBytes;
+            if (gat) {
+              if (lane < kGatherSlots) {
+                const size_t row = (size_t)h * P.qpad + (y > 0 ? y : 0);
+                bulk_load(ls + lane * 32, P.nlse2 + row, 32, bar(C::kBDOFull + ds));
+                bulk_load(ls + 512 + lane * 32, P.ndelta + row, 32, bar(C::kBDOFull + ds));
+              }
+            } else if (lane == 0) {
+              bulk_load(ls, P.nlse2 + (size_t)h * P.qpad + qt * 128, 512, bar(C::kBDOFull + ds));
+              bulk_load(ls + 512, P.ndelta + (size_t)h * P.qpad + qt * 128, 512,
+                        bar(C::kBDOFull + ds));
+            }
+          }
+          ++do_cnt;
+        }
       }
     }
     if (!ok && lane == 0) {
+      // let this warp's copies in flight land before the CTA exits
       if (kv_cnt > 0) drain_wait_b(bar(C::kBKVFull), (kv_cnt - 1) & 1, kDrainNs);
       for (uint32_t i = q_cnt > (uint32_t)C::kQStages ? q_cnt - C::kQStages : 0; i < q_cnt; ++i)
         drain_wait_b(bar(C::kBQFull + i % C::kQStages), (i / C::kQStages) & 1, kDrainNs);
@@ -616,8 +655,9 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
 // (q-tile, query head) with its visits in k-tile order.
 // Warp roles (384 threads): warps 0-7 dS warps in two warpgroups (thread =
 // query row = TMEM lane; warpgroup w owns key columns [64w, 64w+64)) and the
-// dQ epilogue, warp 8 TMA producer, warp 9 MMA issuer, warps 10-11 idle;
-// registers split 200 / 104 as in the dK/dV pass.
+// dQ epilogue, warp 8 TMA producer, warp 9 MMA issuer, warp 10 V loader for
+// plans with gathered steps, idle otherwise as warp 11 is; registers split
+// 200 / 104 as in the dK/dV pass.
 // TMEM columns: S of even steps [0,128), of odd steps [128,256), dP
 // [256,384), dQ [384,384+D).  Warpgroup w writes its dS pairs over columns
 // [64w, 64w+32) of its step's S buffer (read by itself first); the dQ MMA
@@ -752,7 +792,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     mbar_init(bar(C::kBDrain), 1);
     for (int s = 0; s < kItemRing; ++s) {
       mbar_init(bar(C::kBItemFull + s), 1);
-      mbar_init(bar(C::kBItemEmpty + s), 1 + 256);  // MMA thread + dS threads
+      // MMA thread + dS threads (+ lane 0 of the V warp)
+      mbar_init(bar(C::kBItemEmpty + s), 1 + 256 + (kGather ? 1 : 0));
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -767,21 +808,32 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
 
   if (warp >= 8) {
   reg_dealloc<kSplitNarrowRegs>();
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    // Lane 0 draws the items, waits on the rings and sets each barrier's
-    // byte count.  With gathered steps the whole warp runs the loop and the
-    // 16 slots of a gathered K/V tile (8 rows each, 1024-byte aligned, unused
-    // ones reading zero rows from row -8) are copied by lanes 0-15 in
-    // parallel after a __syncwarp that orders them behind the byte count;
-    // without them lane 0 runs it alone (measured faster there).
+  if (warp == 8 || (kGather && warp == 10)) {
+    // ------------------------------------------------------------ producers
+    // Warp 8 draws the items and loads Q / dO and K, and V too unless the
+    // plan has gathered steps; then warp 10 loads V (a gathered tile is 16
+    // slots x D / 64 boxes per tensor, and each lane-issued copy costs the
+    // issuing warp some 60 cycles), taking the items from the work queue like
+    // the consumers and waiting on the V ring itself.  Lane 0 of the loading
+    // warp waits on the rings and sets each barrier's byte count.  With
+    // gathered steps the whole warp runs the loop and the 16 slots of a
+    // gathered K/V tile (8 rows each, 1024-byte aligned, unused ones reading
+    // zero rows from row -8) are copied by lanes 0-15 in parallel after a
+    // __syncwarp that orders them behind the byte count; without them lane 0
+    // runs it alone (measured faster there).
+    const bool role0 = warp == 8;
+    const bool load_k = role0, load_v = !kGather || !role0;
     if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      prefetch_tmap(&tm_do);
-      prefetch_tmap(&tm_k8);
-      prefetch_tmap(&tm_v8);
+      if (role0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_do);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_k8);
+      }
+      if (load_v) {
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_v8);
+      }
     }
     auto load_kv = [&](uint32_t dst, const CUtensorMap* m, const CUtensorMap* m8, uint32_t b,
                        int hk, const int4& stp, int y) {
@@ -794,17 +846,21 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           tma_load_2d(dst + c * 16384, m, b, hk * D + c * 64, stp.x * 128);
       }
     };
-    uint32_t kv_cnt = 0, q_cnt = 0;
-    bool ok = true, k_only = false;
+    uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0;
+    bool ok = true;
     // without gathered steps lane 0 runs the loop alone
     const unsigned pm = kGather ? 0xffffffffu : 1u;
     if (kGather || lane == 0)
     for (int r = 0; ok; ++r) {
       int idx = -1;
       if (lane == 0) {
-        const int pos = atomicAdd(P.ticket, 1);
-        idx = pos < P.n_items ? P.order[pos] : -1;
-        ok = queue_publish(queue, r, idx, ctl, 809);
+        if (role0) {
+          const int pos = atomicAdd(P.ticket, 1);
+          idx = pos < P.n_items ? P.order[pos] : -1;
+          ok = queue_publish(queue, r, idx, ctl, 809);
+        } else {
+          ok = queue_take(queue, r, idx, ctl, 810);
+        }
       }
       ok = __shfl_sync(pm, ok, 0);
       idx = __shfl_sync(pm, idx, 0);
@@ -817,58 +873,62 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         const int n = P.counts[2 * idx + h];
         if (n == 0) continue;
         const int qt = it[kFiQt0 + h], head = it[kFiH0 + h], hk = head / P.g;
-        if (lane == 0) {
-          ok = mbar_wait(bar(C::kBQEmpty), (q_cnt & 1) ^ 1, ctl, 800);
-          if (ok) {
-            mbar_arrive_expect_tx(bar(C::kBQFull), 2 * C::kTileBytes);
-            for (int c = 0; c < C::kChunks; ++c) {
-              tma_load_2d(sbase + C::kQOff + c * 16384, &tm_q, bar(C::kBQFull), head * D + c * 64,
-                          qt * 128);
-              tma_load_2d(sbase + C::kDOOff + c * 16384, &tm_do, bar(C::kBQFull),
-                          head * D + c * 64, qt * 128);
+        if (role0) {
+          if (lane == 0) {
+            ok = mbar_wait(bar(C::kBQEmpty), (q_cnt & 1) ^ 1, ctl, 800);
+            if (ok) {
+              mbar_arrive_expect_tx(bar(C::kBQFull), 2 * C::kTileBytes);
+              for (int c = 0; c < C::kChunks; ++c) {
+                tma_load_2d(sbase + C::kQOff + c * 16384, &tm_q, bar(C::kBQFull),
+                            head * D + c * 64, qt * 128);
+                tma_load_2d(sbase + C::kDOOff + c * 16384, &tm_do, bar(C::kBQFull),
+                            head * D + c * 64, qt * 128);
+              }
             }
           }
+          if (!(ok = __shfl_sync(pm, ok, 0))) break;
+          ++q_cnt;
         }
-        if (!(ok = __shfl_sync(pm, ok, 0))) break;
-        ++q_cnt;
         for (int j = sb; j < se; ++j) {
           const int4 st = P.steps[j];
           if (half_info(st, h) < 0) continue;
           // this lane's slot start (read while the ring slots are awaited)
           const int y = kGather && st.w > 0 && lane < kGatherSlots
                             ? P.gathers[(size_t)(st.w - 1) * kGatherWords + lane] : 0;
-          const int ks = kv_cnt % C::kKStages, vs = kv_cnt % C::kVStages;
-          const uint32_t kph = (kv_cnt / C::kKStages) & 1, vph = (kv_cnt / C::kVStages) & 1;
-          if (lane == 0) {
-            ok = mbar_wait(bar(C::kBKEmpty + ks), kph ^ 1, ctl, 801);
-            if (ok) mbar_arrive_expect_tx(bar(C::kBKFull + ks), C::kTileBytes);
+          if (load_k) {
+            const int ks = k_cnt % C::kKStages;
+            if (lane == 0) {
+              ok = mbar_wait(bar(C::kBKEmpty + ks), ((k_cnt / C::kKStages) & 1) ^ 1, ctl, 801);
+              if (ok) mbar_arrive_expect_tx(bar(C::kBKFull + ks), C::kTileBytes);
+            }
+            if (!(ok = __shfl_sync(pm, ok, 0))) break;
+            __syncwarp(pm);
+            load_kv(sbase + C::kKOff + ks * C::kTileBytes, &tm_k, &tm_k8, bar(C::kBKFull + ks),
+                    hk, st, y);
+            ++k_cnt;
           }
-          if (!(ok = __shfl_sync(pm, ok, 0))) break;
-          __syncwarp(pm);
-          load_kv(sbase + C::kKOff + ks * C::kTileBytes, &tm_k, &tm_k8, bar(C::kBKFull + ks), hk,
-                  st, y);
-          k_only = true;
-          if (lane == 0) {
-            ok = mbar_wait(bar(C::kBVEmpty + vs), vph ^ 1, ctl, 802);
-            if (ok) mbar_arrive_expect_tx(bar(C::kBVFull + vs), C::kTileBytes);
+          if (load_v) {
+            const int vs = v_cnt % C::kVStages;
+            if (lane == 0) {
+              ok = mbar_wait(bar(C::kBVEmpty + vs), ((v_cnt / C::kVStages) & 1) ^ 1, ctl, 802);
+              if (ok) mbar_arrive_expect_tx(bar(C::kBVFull + vs), C::kTileBytes);
+            }
+            if (!(ok = __shfl_sync(pm, ok, 0))) break;
+            __syncwarp(pm);
+            load_kv(sbase + C::kVOff + vs * C::kTileBytes, &tm_v, &tm_v8, bar(C::kBVFull + vs),
+                    hk, st, y);
+            ++v_cnt;
           }
-          if (!(ok = __shfl_sync(pm, ok, 0))) break;
-          __syncwarp(pm);
-          k_only = false;
-          load_kv(sbase + C::kVOff + vs * C::kTileBytes, &tm_v, &tm_v8, bar(C::kBVFull + vs), hk,
-                  st, y);
-          ++kv_cnt;
         }
       }
     }
     if (!ok && lane == 0) {
+      // let this warp's copies in flight land before the CTA exits
       if (q_cnt > 0) drain_wait_b(bar(C::kBQFull), (q_cnt - 1) & 1, kDrainNs);
-      for (uint32_t i = kv_cnt > (uint32_t)C::kKStages ? kv_cnt - C::kKStages : 0; i < kv_cnt; ++i)
+      for (uint32_t i = k_cnt > (uint32_t)C::kKStages ? k_cnt - C::kKStages : 0; i < k_cnt; ++i)
         drain_wait_b(bar(C::kBKFull + i % C::kKStages), (i / C::kKStages) & 1, kDrainNs);
-      for (uint32_t i = kv_cnt > (uint32_t)C::kVStages ? kv_cnt - C::kVStages : 0; i < kv_cnt; ++i)
+      for (uint32_t i = v_cnt > (uint32_t)C::kVStages ? v_cnt - C::kVStages : 0; i < v_cnt; ++i)
         drain_wait_b(bar(C::kBVFull + i % C::kVStages), (i / C::kVStages) & 1, kDrainNs);
-      if (k_only)
-        drain_wait_b(bar(C::kBKFull + kv_cnt % C::kKStages), (kv_cnt / C::kKStages) & 1, kDrainNs);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer

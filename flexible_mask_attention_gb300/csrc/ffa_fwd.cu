@@ -10,7 +10,8 @@
 //   warps 4-7  softmax for half 1
 //   warp  8    TMA producer: Q tiles, then a ring of K/V stages
 //   warp  9    tcgen05 MMA issuer (and TMEM owner)
-//   warps 10-11 idle
+//   warp  10   V loader for plans with gathered steps (idle otherwise)
+//   warp  11   idle
 // Registers: the control warpgroup (warps 8-11) shrinks to 104 per thread
 // and the softmax warpgroups grow to 200 (the split in ffa_ptx.cuh).
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
@@ -240,7 +241,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     mbar_init(bar(C::kBDrain), 1);
     for (int s = 0; s < kItemRing; ++s) {
       mbar_init(bar(C::kBItemFull + s), 1);
-      mbar_init(bar(C::kBItemEmpty + s), 1 + 256);  // MMA thread + softmax threads
+      // MMA thread + softmax threads (+ lane 0 of the V warp)
+      mbar_init(bar(C::kBItemEmpty + s), 1 + 256 + (kGather ? 1 : 0));
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -255,20 +257,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   if (warp >= 8) {
   reg_dealloc<kSplitNarrowRegs>();
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    // Lane 0 draws the items, waits on the rings and sets each barrier's
-    // byte count.  With gathered steps the whole warp runs the loop and the
-    // 16 slots of a gathered tile (8 rows each, 1024-byte aligned, unused
-    // ones reading zero rows from row -8) are copied by lanes 0-15 in
-    // parallel after a __syncwarp that orders them behind the byte count;
-    // without them lane 0 runs it alone.
+  if (warp == 8 || (kGather && warp == 10)) {
+    // ------------------------------------------------------------ producers
+    // Warp 8 draws the items and loads Q and K, and V too unless the plan
+    // has gathered steps; then warp 10 loads V (a gathered tile is 16 slots x
+    // D / 64 boxes per tensor, and each lane-issued copy costs the issuing
+    // warp some 60 cycles), taking the items from the work queue like the
+    // consumers and waiting on the V stages itself.  Lane 0 of the loading
+    // warp waits on the rings and sets each barrier's byte count.  With
+    // gathered steps the whole warp runs the loop and the 16 slots of a
+    // gathered tile (8 rows each, 1024-byte aligned, unused ones reading
+    // zero rows from row -8) are copied by lanes 0-15 in parallel after a
+    // __syncwarp that orders them behind the byte count; without them lane 0
+    // runs it alone.
+    const bool role0 = warp == 8;
+    const bool load_v = !kGather || !role0;
     if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      prefetch_tmap(&tm_k8);
-      prefetch_tmap(&tm_v8);
+      if (role0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_k8);
+      }
+      if (load_v) {
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_v8);
+      }
     }
     auto load_kv = [&](uint32_t dst, const CUtensorMap* m, const CUtensorMap* m8, uint32_t b,
                        int hk, const int4& stp, int y) {
@@ -281,16 +294,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tma_load_2d(dst + c * 16384, m, b, hk * D + c * 64, stp.x * 128);
       }
     };
-    uint32_t kv_cnt = 0, q_cnt = 0;
-    bool ok = true, k_only = false;  // k_only: K of step kv_cnt issued, its V not yet
+    uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0;  // K / V tiles issued (same stage sequence)
+    bool ok = true;
     const unsigned pm = kGather ? 0xffffffffu : 1u;  // lanes running the loop
     if (kGather || lane == 0)
     for (int r = 0; ok; ++r) {
       int idx = -1;
       if (lane == 0) {
-        const int pos = atomicAdd(P.ticket, 1);
-        idx = pos < P.n_items ? P.order[pos] : -1;
-        ok = queue_publish(queue, r, idx, ctl, 109);
+        if (role0) {
+          const int pos = atomicAdd(P.ticket, 1);
+          idx = pos < P.n_items ? P.order[pos] : -1;
+          ok = queue_publish(queue, r, idx, ctl, 109);
+        } else {
+          ok = queue_take(queue, r, idx, ctl, 110);
+        }
       }
       ok = __shfl_sync(pm, ok, 0);
       idx = __shfl_sync(pm, idx, 0);
@@ -300,58 +317,61 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (se <= sb) continue;
       const bool act1 = it[kFiQt1] >= 0 && it[kFiH1] >= 0;
       const int hk = it[kFiH0] / P.g;
-      if (lane == 0) {
-        ok = mbar_wait(bar(C::kBQEmpty), (q_cnt & 1) ^ 1, ctl, 100);
-        if (ok) {
-          mbar_arrive_expect_tx(bar(C::kBQFull), (act1 ? 2 : 1) * C::kTileBytes);
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_2d(sbase + C::kQOff + c * 16384, &tm_q, bar(C::kBQFull),
-                        it[kFiH0] * D + c * 64, it[kFiQt0] * 128);
-          if (act1)
+      if (role0) {
+        if (lane == 0) {
+          ok = mbar_wait(bar(C::kBQEmpty), (q_cnt & 1) ^ 1, ctl, 100);
+          if (ok) {
+            mbar_arrive_expect_tx(bar(C::kBQFull), (act1 ? 2 : 1) * C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c)
-              tma_load_2d(sbase + C::kQOff + C::kTileBytes + c * 16384, &tm_q, bar(C::kBQFull),
-                          it[kFiH1] * D + c * 64, it[kFiQt1] * 128);
+              tma_load_2d(sbase + C::kQOff + c * 16384, &tm_q, bar(C::kBQFull),
+                          it[kFiH0] * D + c * 64, it[kFiQt0] * 128);
+            if (act1)
+              for (int c = 0; c < C::kChunks; ++c)
+                tma_load_2d(sbase + C::kQOff + C::kTileBytes + c * 16384, &tm_q,
+                            bar(C::kBQFull), it[kFiH1] * D + c * 64, it[kFiQt1] * 128);
+          }
         }
+        if (!(ok = __shfl_sync(pm, ok, 0))) break;
+        ++q_cnt;
       }
-      if (!(ok = __shfl_sync(pm, ok, 0))) break;
-      ++q_cnt;
       for (int j = sb; j < se; ++j) {
         const int4 stp = P.steps[j];
         // this lane's slot start (read while the ring slot is awaited)
         const int y = kGather && stp.w > 0 && lane < kGatherSlots
                           ? P.gathers[(size_t)(stp.w - 1) * kGatherWords + lane] : 0;
-        const int stage = kv_cnt % C::kStages;
-        const uint32_t ph = (kv_cnt / C::kStages) & 1;
-        if (lane == 0) {
-          ok = mbar_wait(bar(C::kBKEmpty + stage), ph ^ 1, ctl, 101);
-          if (ok) mbar_arrive_expect_tx(bar(C::kBKFull + stage), C::kTileBytes);
+        if (role0) {
+          const int stage = k_cnt % C::kStages;
+          if (lane == 0) {
+            ok = mbar_wait(bar(C::kBKEmpty + stage), ((k_cnt / C::kStages) & 1) ^ 1, ctl, 101);
+            if (ok) mbar_arrive_expect_tx(bar(C::kBKFull + stage), C::kTileBytes);
+          }
+          if (!(ok = __shfl_sync(pm, ok, 0))) break;
+          __syncwarp(pm);
+          load_kv(sbase + C::kKOff + stage * C::kTileBytes, &tm_k, &tm_k8,
+                  bar(C::kBKFull + stage), hk, stp, y);
+          ++k_cnt;
         }
-        if (!(ok = __shfl_sync(pm, ok, 0))) break;
-        __syncwarp(pm);
-        load_kv(sbase + C::kKOff + stage * C::kTileBytes, &tm_k, &tm_k8, bar(C::kBKFull + stage),
-                hk, stp, y);
-        k_only = true;
-        if (lane == 0) {
-          ok = mbar_wait(bar(C::kBVEmpty + stage), ph ^ 1, ctl, 102);
-          if (ok) mbar_arrive_expect_tx(bar(C::kBVFull + stage), C::kTileBytes);
+        if (load_v) {
+          const int stage = v_cnt % C::kStages;
+          if (lane == 0) {
+            ok = mbar_wait(bar(C::kBVEmpty + stage), ((v_cnt / C::kStages) & 1) ^ 1, ctl, 102);
+            if (ok) mbar_arrive_expect_tx(bar(C::kBVFull + stage), C::kTileBytes);
+          }
+          if (!(ok = __shfl_sync(pm, ok, 0))) break;
+          __syncwarp(pm);
+          load_kv(sbase + C::kVOff + stage * C::kTileBytes, &tm_v, &tm_v8,
+                  bar(C::kBVFull + stage), hk, stp, y);
+          ++v_cnt;
         }
-        if (!(ok = __shfl_sync(pm, ok, 0))) break;
-        __syncwarp(pm);
-        k_only = false;
-        load_kv(sbase + C::kVOff + stage * C::kTileBytes, &tm_v, &tm_v8, bar(C::kBVFull + stage),
-                hk, stp, y);
-        ++kv_cnt;
       }
     }
     if (!ok && lane == 0) {
-      // Aborted: let the copies already issued land before the CTA exits.
+      // Aborted: let this warp's copies already issued land before the CTA exits.
       if (q_cnt > 0) drain_wait(bar(C::kBQFull), (q_cnt - 1) & 1, kDrainNs);
-      for (uint32_t i = kv_cnt > (uint32_t)C::kStages ? kv_cnt - C::kStages : 0; i < kv_cnt; ++i) {
+      for (uint32_t i = k_cnt > (uint32_t)C::kStages ? k_cnt - C::kStages : 0; i < k_cnt; ++i)
         drain_wait(bar(C::kBKFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
+      for (uint32_t i = v_cnt > (uint32_t)C::kStages ? v_cnt - C::kStages : 0; i < v_cnt; ++i)
         drain_wait(bar(C::kBVFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
-      }
-      if (k_only)
-        drain_wait(bar(C::kBKFull + kv_cnt % C::kStages), (kv_cnt / C::kStages) & 1, kDrainNs);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
