@@ -596,8 +596,8 @@ __global__ void k_dq_counts(const int* __restrict__ items, int n_items,
 // One block per forward unit.  A unit gathers when every slice of its q-tiles'
 // lists is FULL with ks and ke multiples of kGatherKeys (ke may be Tk), it
 // covers 1 .. kGatherMaxBlocks blocks of kGatherKeys keys, and ceil(blocks /
-// kGatherSlots) gathered steps are at most 2/3 of its regular steps (a
-// gathered step, masked per element, costs about 1.5 tile steps).  The blocks
+// kGatherSlots) gathered steps are at most 9/10 of its regular steps (a
+// gathered step costs about as much as a masked tile step).  The blocks
 // are collected in a shared-memory bitmap (order-free, so deterministic).
 constexpr int kGatherThreads = 256;
 constexpr int kGatherBitmapWords = kGatherMaxTk / kGatherKeys / 32;
@@ -680,7 +680,7 @@ __global__ void __launch_bounds__(kGatherThreads)
   const int nwords = (((Tk + kGatherKeys - 1) / kGatherKeys) + 31) / 32;
   const int n = ok ? block_popc(bits, nwords, red) : 0;
   const int steps = (n + kGatherSlots - 1) / kGatherSlots;
-  const bool gather = ok && n > 0 && n <= kGatherMaxBlocks && 3 * steps <= 2 * scnt[u];
+  const bool gather = ok && n > 0 && n <= kGatherMaxBlocks && 10 * steps <= 9 * scnt[u];
   if (threadIdx.x == 0) {
     gcnt[u] = gather ? steps : 0;
     if (gather) scnt[u] = steps;
@@ -803,7 +803,7 @@ __global__ void __launch_bounds__(kGatherThreads)
 // forward's.  A k-tile gathers when every slice of its list is FULL with qs
 // and qe multiples of kGatherKeys (qe may be Tq), it covers 1 ..
 // kGatherMaxBlocks query blocks and ceil(blocks / kGatherSlots) steps are at
-// most 2/3 of its visits.  bgcnt[kt] = gathered steps (0: regular);
+// most 9/10 of its visits.  bgcnt[kt] = gathered steps (0: regular);
 // bscnt[kt] = the k-tile's step count either way.
 __global__ void __launch_bounds__(kGatherThreads)
     k_bgather_count(const Slice* __restrict__ sl, const int* __restrict__ list,
@@ -821,7 +821,7 @@ __global__ void __launch_bounds__(kGatherThreads)
   const int nwords = (((Tq + kGatherKeys - 1) / kGatherKeys) + 31) / 32;
   const int n = ok ? block_popc(bits, nwords, red) : 0;
   const int steps = (n + kGatherSlots - 1) / kGatherSlots;
-  const bool gather = ok && n > 0 && n <= kGatherMaxBlocks && 3 * steps <= 2 * vcnt[kt];
+  const bool gather = ok && n > 0 && n <= kGatherMaxBlocks && 10 * steps <= 9 * vcnt[kt];
   if (threadIdx.x == 0) {
     bgcnt[kt] = gather ? steps : 0;
     bscnt[kt] = gather ? steps : vcnt[kt];

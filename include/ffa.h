@@ -120,14 +120,14 @@ ffa_status_t ffa_plan_info(ffa_plan_t plan, ffa_plan_info_t* info);
  *   m+n] are their slice indices, ascending (the tile is computed once and
  *   masked by the union of their windows).
  *   Gathered forward steps (a forward unit whose slices are all FULL with key
- *   ranges aligned to 8 keys, when that takes at most 2/3 of its tile steps):
+ *   ranges aligned to 8 keys, when that takes at most 9/10 of its tile steps):
  *   step (0, info0, info1, r + 1) computes 16 blocks of 8 keys packed into
  *   one K/V tile; record r holds the 16 block start keys (-8: unused slot),
  *   then for each half 16 x 4 words of row bits (bit i of word w: row
  *   32 w + i of the half's q-tile sees that block); info_h is 1 when half h
  *   has a row bit set, else -1.
  *   Gathered backward steps, the transpose (a k-tile whose slices are all FULL
- *   with query ranges aligned to 8 rows, when that takes at most 2/3 of its
+ *   with query ranges aligned to 8 rows, when that takes at most 9/10 of its
  *   visits): step (0, 1, 0, r + 1) computes 16 blocks of 8 query rows packed
  *   into one Q / dO tile; record r holds the 16 block start rows (-8: unused)
  *   then 16 x 4 words of key bits (bit i of word w: key 32 w + i of the

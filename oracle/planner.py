@@ -24,8 +24,8 @@ the work-list specification of the planner:
     item per (kt, kv head), cost g * sum of visit costs;
   * gathered forward units: a unit whose q-tiles meet only FULL slices with
     8-aligned key ranges (the end may be Tk), Tk <= 2^19, is instead listed
-    as gathered steps when that takes at most 2/3 of its steps (a gathered
-    step, masked per element, costs about 1.5 tile steps): the 8-key blocks any of
+    as gathered steps when that takes at most 9/10 of its steps (a gathered
+    step costs about as much as a masked tile step): the 8-key blocks any of
     its slices covers, ascending, 16 to a step; a step is (0, info0, info1,
     r + 1) with record r = 16 block starts (key index, -8 for an unused
     slot) then, per half, 16 x 4 words of row bits (bit r of word w: row
@@ -35,7 +35,7 @@ the work-list specification of the planner:
   * gathered backward units, the transpose: a k-tile whose slices are all
     FULL with 8-aligned query ranges (the end may be Tq), Tq <= 2^19, lists
     the 8-row query blocks its slices cover, 16 to a step, when that takes
-    at most 2/3 of its visits; a step is (0, 1, 0, r + 1) with record r =
+    at most 9/10 of its visits; a step is (0, 1, 0, r + 1) with record r =
     16 block start rows (-8: unused) then 16 x 4 words of key bits (bit i of
     word w: key 32w + i of the k-tile is seen by the slot's rows); cost 5
     per step (times g in the item).
@@ -309,7 +309,7 @@ def gather_units(total_q, total_k, q_ranges, k_ranges, mask_types, pair_mode, fv
         else:  # steps of the two q-tiles' visit lists merged on kt
             regular = len({kt for q in qts for kt, _ in fvis[q]})
         n_steps = -(-len(blocks) // GATHER_SLOTS)
-        if len(blocks) > GATHER_MAX_BLOCKS or 3 * n_steps > 2 * regular:
+        if len(blocks) > GATHER_MAX_BLOCKS or 10 * n_steps > 9 * regular:
             continue
         half_tiles = [u, u] if pair_mode == 0 else [2 * u, 2 * u + 1 if 2 * u + 1 < n_qt else -1]
         res = []
@@ -362,7 +362,7 @@ def gather_units_bwd(total_q, total_k, q_ranges, k_ranges, mask_types, bvis):
         blocks = sorted({b for qs, qe, _, _, _ in sl
                          for b in range(qs // GATHER_KEYS, -(-qe // GATHER_KEYS))})
         n_steps = -(-len(blocks) // GATHER_SLOTS)
-        if len(blocks) > GATHER_MAX_BLOCKS or 3 * n_steps > 2 * len(bvis[kt]):
+        if len(blocks) > GATHER_MAX_BLOCKS or 10 * n_steps > 9 * len(bvis[kt]):
             continue
         res = []
         for j in range(n_steps):
