@@ -259,6 +259,9 @@ CONFIGS = {
     # documents of all four types), small enough for a full oracle backward
     "heterogeneous_mid": lambda: heterogeneous_prefix_docs(total=16384, h=2, n_docs=11, seed=13,
                                                            dout_seed=17),
+    # the 64K mask with 2 heads (inputs 134 MB, larger than L2): the
+    # single-kernel profiling case
+    "heterogeneous_h2": lambda: heterogeneous_prefix_docs(h=2),
     "long_context": long_context_docs,
     "short_docs": short_causal_docs,
     "block_sparse_64x64": lambda: block_sparse(q_block=64, k_block=64),
