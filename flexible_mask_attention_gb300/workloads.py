@@ -262,6 +262,8 @@ CONFIGS = {
     # the 64K mask with 2 heads (inputs 134 MB, larger than L2): the
     # single-kernel profiling case
     "heterogeneous_h2": lambda: heterogeneous_prefix_docs(h=2),
+    # packed causal documents with 8 query / 2 kv heads (inputs 168 MB)
+    "packed_causal_h8": lambda: packed_causal_docs(hq=8, hkv=2),
     "long_context": long_context_docs,
     "short_docs": short_causal_docs,
     "block_sparse_64x64": lambda: block_sparse(q_block=64, k_block=64),

@@ -70,3 +70,45 @@ def test_block_sparse_full_size_sampled(name, with_dkv):
     check_grad(dq[rows[:12]], rq, "dq")
     if with_dkv:
         check_grad(dk[keys], rk, "dk"); check_grad(dv[keys], rv, "dv")
+
+
+# Gathered steps in the capped kernels and with sink logits: the tables gather
+# in both directions (every forward unit and every k-tile; the T = 1500 one
+# with a ragged last query block, GQA g = 3, D = 64).  Scale 2.5 and cap 5
+# push scores outside the tanh polynomial's range (exponential form); scale 1
+# and cap 30 keep them inside it.
+GATHERED_EXT = [
+    # (total, hq, hkv, d, q_block, k_block, seed, input scale, cap)
+    (2048, 4, 2, 128, 32, 64, 31, 2.5, 5.0),
+    (2048, 4, 2, 128, 64, 64, 32, 1.0, 30.0),
+    (1500, 6, 2, 64, 64, 16, 33, 2.5, 5.0),
+]
+
+
+@pytest.mark.parametrize("case", GATHERED_EXT,
+                         ids=[f"T{c[0]}_D{c[3]}_q{c[4]}_k{c[5]}_cap{c[8]:g}" for c in GATHERED_EXT])
+def test_block_sparse_gathered_softcap_sink(case):
+    total, hq, hkv, d, qb, kb, seed, scale, cap = case
+    wl = W.block_sparse(total=total, hq=hq, hkv=hkv, d=d, q_block=qb, k_block=kb, seed=seed)
+    q, k, v, do = W.make_tensors(wl, with_dout=True)
+    q = (q.float() * scale).to(torch.bfloat16)
+    k = (k.float() * scale).to(torch.bfloat16)
+    sink = (2.0 * torch.randn(2, hq, generator=torch.Generator().manual_seed(seed))).float()
+    plan = ffa.ffa_plan_create(wl.q_ranges, wl.k_ranges, wl.mask_types, wl.total_q, wl.total_k,
+                               hq, hkv, d)
+    info = ffa.ffa_plan_info(plan)
+    assert info["gathers"] > 0 and info["bgathers"] > 0
+    qd, kd, vd, dod, sd = (t.to(DEV) for t in (q, k, v, do, sink))
+    out, lse = ffa.ffa_fwd_ex(plan, qd, kd, vd, sink=sd, softcap=cap)
+    dq, dk, dv, ds = ffa.ffa_bwd_ex(plan, qd, kd, vd, out, dod, lse, sink=sd, softcap=cap)
+    torch.cuda.synchronize()
+    assert ffa.ffa_get_last_device_error(plan) == (0, 0)
+    a = (wl.q_ranges, wl.k_ranges, wl.mask_types)
+    ro, rl = oracle.fwd(q, k, v, *a, sink=sink, softcap=cap)
+    check_fwd(out.float().cpu().numpy(), lse.cpu().numpy(), ro, rl)
+    rq, rk, rv = oracle.bwd(q, k, v, do, *a, sink=sink, softcap=cap)
+    check_grad(dq.float().cpu().numpy(), rq, "dq")
+    check_grad(dk.float().cpu().numpy(), rk, "dk")
+    check_grad(dv.float().cpu().numpy(), rv, "dv")
+    rs = oracle.dsink(q, k, v, do, *a, sink, "sh", softcap=cap)
+    check_grad(ds.cpu().numpy(), rs, "dsink")
