@@ -264,6 +264,9 @@ CONFIGS = {
     "heterogeneous_h2": lambda: heterogeneous_prefix_docs(h=2),
     # packed causal documents with 8 query / 2 kv heads (inputs 168 MB)
     "packed_causal_h8": lambda: packed_causal_docs(hq=8, hkv=2),
+    # the same documents with one kv head of 4 query heads (the GQA ratio of
+    # the 32 / 8 head table), small enough for a full oracle backward
+    "packed_causal_h4": lambda: packed_causal_docs(hq=4, hkv=1),
     "long_context": long_context_docs,
     "short_docs": short_causal_docs,
     "block_sparse_64x64": lambda: block_sparse(q_block=64, k_block=64),

@@ -10,6 +10,8 @@ gradients with the fp64 oracle:
   * the 16K-token version of the benchmark mask (4096-token prefix, 11
     documents of all four mask types, 2 heads) in full: every element of
     out, lse, dq, dk and dv;
+  * the 32K-token packed-causal mask (its documents, one kv head of 4 query
+    heads) in full;
   * the 64K-token benchmark mask and the packed-causal mask at full size, in
     the launch configuration the benchmark times, on the keys seen by the
     most rows (prefix keys, the first keys of the longest causal documents,
@@ -85,3 +87,21 @@ def test_full_size_heaviest_keys(name):
     gv = dv.float().cpu().numpy()[keys][:, kv_heads]
     check_grad(gk, rk, "dk")
     check_grad(gv, rv, "dv")
+
+
+def test_packed_causal_every_element():
+    """The packed-document causal mask (32768 tokens, lognormal document
+    lengths up to 16K, the backward workload of the benchmark tables) with
+    one kv head of 4 query heads: every element of out, lse, dq, dk and dv
+    against the oracle.  Its longest document (12386 tokens) gives dK/dV
+    items of up to 97 q-tile steps per head."""
+    wl = W.CONFIGS["packed_causal_h4"]()
+    assert wl.total_q == 32768 and wl.num_heads_q == 4 * wl.num_heads_kv
+    (q, k, v, do), out, lse, (dq, dk, dv) = run_path(wl)
+    a = (wl.q_ranges, wl.k_ranges, wl.mask_types)
+    ro, rl = oracle.fwd(q, k, v, *a)
+    check_fwd(out.float().cpu().numpy(), lse.cpu().numpy(), ro, rl)
+    rq, rk, rv = oracle.bwd(q, k, v, do, *a)
+    check_grad(dq.float().cpu().numpy(), rq, "dq")
+    check_grad(dk.float().cpu().numpy(), rk, "dk")
+    check_grad(dv.float().cpu().numpy(), rv, "dv")
