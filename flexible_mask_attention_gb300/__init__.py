@@ -54,7 +54,8 @@ class _PlanInfo(ctypes.Structure):
                 ("merges", ctypes.c_int64), ("grid_fwd", ctypes.c_int32),
                 ("grid_bwd", ctypes.c_int32), ("area", ctypes.c_int64),
                 ("fwd_masks", ctypes.c_int64), ("bwd_masks", ctypes.c_int64),
-                ("gathers", ctypes.c_int64), ("bgathers", ctypes.c_int64)]
+                ("gathers", ctypes.c_int64), ("bgathers", ctypes.c_int64),
+                ("stacked", ctypes.c_int64)]
 
 
 _lib = None

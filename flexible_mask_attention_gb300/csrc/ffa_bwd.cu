@@ -701,6 +701,7 @@ struct DqParams {
   const int* masks;  // slice lists of multi-slice visits
   const int* gathers;  // gathered step records
   int Tq, Tk, Hq, g, qpad;
+  int stack;  // head-stacked units: a half is a 64-row slab of two heads
   float scale, scale_log2;
   const float* nlse2;
   const float* ndelta;
@@ -755,7 +756,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_do,
                       const __grid_constant__ CUtensorMap tm_k8,
-                      const __grid_constant__ CUtensorMap tm_v8, const DqParams P) {
+                      const __grid_constant__ CUtensorMap tm_v8,
+                      const __grid_constant__ CUtensorMap tm_q64,
+                      const __grid_constant__ CUtensorMap tm_do64, const DqParams P) {
   using C = DqCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
@@ -878,11 +881,22 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
             ok = mbar_wait(bar(C::kBQEmpty), (q_cnt & 1) ^ 1, ctl, 800);
             if (ok) {
               mbar_arrive_expect_tx(bar(C::kBQFull), 2 * C::kTileBytes);
-              for (int c = 0; c < C::kChunks; ++c) {
-                tma_load_2d(sbase + C::kQOff + c * 16384, &tm_q, bar(C::kBQFull),
-                            head * D + c * 64, qt * 128);
-                tma_load_2d(sbase + C::kDOOff + c * 16384, &tm_do, bar(C::kBQFull),
-                            head * D + c * 64, qt * 128);
+              if (kGather && P.stack) {  // heads head, head + 1 of the 64-row slab qt
+                for (int j = 0; j < 2; ++j)
+                  for (int c = 0; c < C::kChunks; ++c) {
+                    const uint32_t o = c * 16384 + j * (kSlabRows * 128);
+                    tma_load_2d(sbase + C::kQOff + o, &tm_q64, bar(C::kBQFull),
+                                (head + j) * D + c * 64, qt * kSlabRows);
+                    tma_load_2d(sbase + C::kDOOff + o, &tm_do64, bar(C::kBQFull),
+                                (head + j) * D + c * 64, qt * kSlabRows);
+                  }
+              } else {
+                for (int c = 0; c < C::kChunks; ++c) {
+                  tma_load_2d(sbase + C::kQOff + c * 16384, &tm_q, bar(C::kBQFull),
+                              head * D + c * 64, qt * 128);
+                  tma_load_2d(sbase + C::kDOOff + c * 16384, &tm_do, bar(C::kBQFull),
+                              head * D + c * 64, qt * 128);
+                }
               }
             }
           }
@@ -1045,8 +1059,11 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
       for (int h = 0; ok && h < 2; ++h) {
         if (!half_active(it, h)) continue;
-        const int qt = it[kFiQt0 + h], head = it[kFiH0 + h];
-        const int row = qt * 128 + t;
+        const int qt = it[kFiQt0 + h];
+        // tile row -> query row and head (head-stacked: 64-row slab, two heads)
+        const bool stk = kGather && P.stack;
+        const int row = stk ? qt * kSlabRows + (t & (kSlabRows - 1)) : qt * 128 + t;
+        const int head = it[kFiH0 + h] + (stk ? t / kSlabRows : 0);
         const float nl = P.nlse2[(size_t)head * P.qpad + row];
         const float nd = P.ndelta[(size_t)head * P.qpad + row];
         const float2 nl2 = make_float2(nl, nl);
@@ -1268,13 +1285,15 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
       if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
     }
   }
-  alignas(64) CUtensorMap tq, tk, tv, tdo, tk8, tv8, tq8, tdo8;
+  alignas(64) CUtensorMap tq, tk, tv, tdo, tk8, tv8, tq8, tdo8, tq64, tdo64;
   if (!encode_tile_map(&tq, q, p->Tq, p->Hq * D) || !encode_tile_map(&tk, k, p->Tk, p->Hkv * D) ||
       !encode_tile_map(&tv, v, p->Tk, p->Hkv * D) || !encode_tile_map(&tdo, dout, p->Tq, p->Hq * D) ||
       !encode_tile_map(&tk8, k, p->Tk, p->Hkv * D, kGatherKeys) ||
       !encode_tile_map(&tv8, v, p->Tk, p->Hkv * D, kGatherKeys) ||
       !encode_tile_map(&tq8, q, p->Tq, p->Hq * D, kGatherKeys) ||
-      !encode_tile_map(&tdo8, dout, p->Tq, p->Hq * D, kGatherKeys))
+      !encode_tile_map(&tdo8, dout, p->Tq, p->Hq * D, kGatherKeys) ||
+      !encode_tile_map(&tq64, q, p->Tq, p->Hq * D, kSlabRows) ||
+      !encode_tile_map(&tdo64, dout, p->Tq, p->Hq * D, kSlabRows))
     return FFA_ERR_INVALID_ARG;
   const float scale_log2 = scale * kLog2e;
   {
@@ -1334,6 +1353,7 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     P.Hq = p->Hq;
     P.g = p->Hq / p->Hkv;
     P.qpad = qpad;
+    P.stack = p->stacked;
     P.scale = scale;
     P.scale_log2 = scale_log2;
     P.nlse2 = nlse2;
@@ -1349,7 +1369,7 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     if (cudaMemsetAsync(P.ticket, 0, sizeof(int), st) != cudaSuccess) return FFA_ERR_CUDA;
     record_phase(p, 4, st);
     ffa_bwd_dq_kernel<D, kCap, kGather><<<p->grid_dq, C::kThreads, C::kSmemBytes, st>>>(
-        tq, tk, tv, tdo, tk8, tv8, P);
+        tq, tk, tv, tdo, tk8, tv8, tq64, tdo64, P);
     note_launches(1);
     if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   }

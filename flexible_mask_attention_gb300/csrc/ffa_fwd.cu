@@ -86,6 +86,7 @@ struct FwdParams {
   const int* masks;  // slice lists of multi-slice visits
   const int* gathers;  // gathered step records
   int Tq, Tk, Hq, g;
+  int stack;  // head-stacked units: a half is a 64-row slab of two heads
   float scale_log2;
   __nv_bfloat16* out;
   float* lse;
@@ -208,7 +209,8 @@ template <int D, bool kCap, bool kGather>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     ffa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_k8,
-                   const __grid_constant__ CUtensorMap tm_v8, const FwdParams P) {
+                   const __grid_constant__ CUtensorMap tm_v8,
+                   const __grid_constant__ CUtensorMap tm_q64, const FwdParams P) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -322,13 +324,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           ok = mbar_wait(bar(C::kBQEmpty), (q_cnt & 1) ^ 1, ctl, 100);
           if (ok) {
             mbar_arrive_expect_tx(bar(C::kBQFull), (act1 ? 2 : 1) * C::kTileBytes);
-            for (int c = 0; c < C::kChunks; ++c)
-              tma_load_2d(sbase + C::kQOff + c * 16384, &tm_q, bar(C::kBQFull),
-                          it[kFiH0] * D + c * 64, it[kFiQt0] * 128);
-            if (act1)
+            if (kGather && P.stack) {
+              // a half: the slab's 64 rows of heads h and h + 1, tile rows
+              // 0-63 and 64-127 (8 KB apart in each 128-byte column chunk)
+              for (int hh = 0; hh < (act1 ? 2 : 1); ++hh)
+                for (int j = 0; j < 2; ++j)
+                  for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_2d(sbase + C::kQOff + hh * C::kTileBytes + c * 16384 +
+                                    j * (kSlabRows * 128),
+                                &tm_q64, bar(C::kBQFull), (it[kFiH0 + hh] + j) * D + c * 64,
+                                it[kFiQt0 + hh] * kSlabRows);
+            } else {
               for (int c = 0; c < C::kChunks; ++c)
-                tma_load_2d(sbase + C::kQOff + C::kTileBytes + c * 16384, &tm_q,
-                            bar(C::kBQFull), it[kFiH1] * D + c * 64, it[kFiQt1] * 128);
+                tma_load_2d(sbase + C::kQOff + c * 16384, &tm_q, bar(C::kBQFull),
+                            it[kFiH0] * D + c * 64, it[kFiQt0] * 128);
+              if (act1)
+                for (int c = 0; c < C::kChunks; ++c)
+                  tma_load_2d(sbase + C::kQOff + C::kTileBytes + c * 16384, &tm_q,
+                              bar(C::kBQFull), it[kFiH1] * D + c * 64, it[kFiQt1] * 128);
+            }
           }
         }
         if (!(ok = __shfl_sync(pm, ok, 0))) break;
@@ -500,8 +514,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
       const bool act1 = it[kFiQt1] >= 0 && it[kFiH1] >= 0;
       if (h == 1 && !act1) continue;
-      const int qt = it[kFiQt0 + h], head = it[kFiH0 + h], slot = it[kFiSlot];
-      const int row = qt * 128 + row_in;
+      const int qt = it[kFiQt0 + h], slot = it[kFiSlot];
+      // tile row -> query row and head (head-stacked: 64-row slab, two heads)
+      const bool stk = kGather && P.stack;
+      const int row = stk ? qt * kSlabRows + (row_in & (kSlabRows - 1)) : qt * 128 + row_in;
+      const int head = it[kFiH0 + h] + (stk ? row_in / kSlabRows : 0);
       float m = -INFINITY, l = 0.f;
       bool visited = false;
       int4 st_next = sb < se ? P.steps[sb] : make_int4(0, -1, -1, 0);
@@ -726,11 +743,12 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
                           void* out, float* lse, void* ws, cudaStream_t st, const SinkArgs& sk,
                           float softcap) {
   using C = FwdCfg<D>;
-  alignas(64) CUtensorMap tq, tk, tv, tk8, tv8;
+  alignas(64) CUtensorMap tq, tk, tv, tk8, tv8, tq64;
   if (!encode_tile_map(&tq, q, p->Tq, p->Hq * D) || !encode_tile_map(&tk, k, p->Tk, p->Hkv * D) ||
       !encode_tile_map(&tv, v, p->Tk, p->Hkv * D) ||
       !encode_tile_map(&tk8, k, p->Tk, p->Hkv * D, kGatherKeys) ||
-      !encode_tile_map(&tv8, v, p->Tk, p->Hkv * D, kGatherKeys))
+      !encode_tile_map(&tv8, v, p->Tk, p->Hkv * D, kGatherKeys) ||
+      !encode_tile_map(&tq64, q, p->Tq, p->Hq * D, kSlabRows))
     return FFA_ERR_INVALID_ARG;
   FwdParams P;
   P.steps = p->fwd_steps;
@@ -745,6 +763,7 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   P.Tk = p->Tk;
   P.Hq = p->Hq;
   P.g = p->Hq / p->Hkv;
+  P.stack = p->stacked;
   P.scale_log2 = scale * kLog2e;
   P.out = static_cast<__nv_bfloat16*>(out);
   P.lse = lse;
@@ -763,7 +782,7 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   if (cudaMemsetAsync(P.ticket, 0, sizeof(int), st) != cudaSuccess) return FFA_ERR_CUDA;
   record_phase(p, 0, st);
   ffa_fwd_kernel<D, kCap, kGather><<<p->grid_fwd, kFwdThreads, C::kSmemBytes, st>>>(
-      tq, tk, tv, tk8, tv8, P);
+      tq, tk, tv, tk8, tv8, tq64, P);
   note_launches(1);
   if (cudaGetLastError() != cudaSuccess) return FFA_ERR_CUDA;
   if (p->n_merges > 0) {

@@ -42,6 +42,12 @@ constexpr int kGatherWords = kGatherSlots + 2 * kGatherSlots * 4;
 constexpr int kBGatherWords = kGatherSlots + kGatherSlots * 4;
 constexpr int kGatherMaxBlocks = 2048;  // 8-key blocks per gathered unit
 constexpr int kGatherMaxTk = 1 << 19;   // key count up to which units may gather
+// Head-stacked forward units (plan.stacked): a unit is a slab of kSlabRows
+// query rows, and a half of an item is that slab for two consecutive query
+// heads h, h + 1 stacked in one 128-row tile (tile row r: query row
+// kSlabRows * slab + r % kSlabRows of head h + r / kSlabRows).  Every step of
+// such a plan is gathered, with the same row bits for r and r + kSlabRows.
+constexpr int kSlabRows = 64;
 
 #ifdef __CUDACC__
 // Adds [lo, hi) (tile-local, any range) to a 128-bit mask of tile columns.
@@ -202,6 +208,7 @@ struct ffa_plan_s {
   int* merges = nullptr;
   int64_t n_merges = 0;
   int n_slots = 0;  // partial-result slots (split forward items)
+  int stacked = 0;  // forward units are head-stacked 64-row slabs (kSlabRows)
   int* fwd_masks = nullptr;  // slice lists of multi-slice forward visits
   int64_t n_fwd_masks = 0;
   int* gathers = nullptr;  // gathered step records [n_gathers][kGatherWords]

@@ -474,7 +474,15 @@ __global__ void k_fwd_items(int n_items, int pair_mode, int g, int Hkv, int Hq, 
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= n_items) return;
   int u, qt0, qt1, h0, h1;
-  if (pair_mode == 0) {
+  if (pair_mode == 2) {  // `pairs` holds the groups of four heads
+    u = idx / (Hkv * pairs);
+    const int rem = idx % (Hkv * pairs);
+    const int hk = rem / pairs, p = rem % pairs;
+    qt0 = qt1 = u;
+    h0 = hk * g + 4 * p;
+    h1 = (4 * p + 2 < g) ? h0 + 2 : -1;
+    if (h1 < 0) qt1 = -1;
+  } else if (pair_mode == 0) {
     u = idx / (Hkv * pairs);
     const int rem = idx % (Hkv * pairs);
     const int hk = rem / pairs, p = rem % pairs;
@@ -603,13 +611,23 @@ constexpr int kGatherThreads = 256;
 constexpr int kGatherBitmapWords = kGatherMaxTk / kGatherKeys / 32;
 
 struct GatherUnit {
-  int qt[2];  // q-tile of each half (-1: none)
-  int n_qt;   // distinct q-tiles (1 or 2)
+  int qt[2];   // q-tile of each half (-1: none)
+  int n_qt;    // distinct q-tiles (1 or 2)
+  int p0, p1;  // query rows of the unit: slices outside [p0, p1) are skipped
 };
 
+// pair_mode 0: q-tile u (two heads); 1: q-tiles 2u, 2u+1; 2: the 64-row
+// slab u of q-tile u / 2 (head-stacked units).
 __device__ __forceinline__ GatherUnit gather_unit(int u, int pair_mode, int n_qt) {
   GatherUnit g;
-  if (pair_mode == 0) {
+  g.p0 = -1;
+  g.p1 = 0x7fffffff;
+  if (pair_mode == 2) {
+    g.qt[0] = g.qt[1] = u >> 1;
+    g.n_qt = 1;
+    g.p0 = kSlabRows * u;
+    g.p1 = g.p0 + kSlabRows;
+  } else if (pair_mode == 0) {
     g.qt[0] = g.qt[1] = u;
     g.n_qt = 1;
   } else {
@@ -637,6 +655,7 @@ __device__ bool gather_bitmap(const Slice* __restrict__ sl, const int* __restric
     const int n = lcnt[gu.qt[t]];
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
       const Slice x = sl[L[i]];
+      if (!kBwd && (x.qe <= gu.p0 || x.qs >= gu.p1)) continue;  // outside the unit's rows
       const int lo = kBwd ? x.qs : x.ks, hi = kBwd ? x.qe : x.ke;
       if (x.t != 0 || lo % kGatherKeys != 0 || (hi % kGatherKeys != 0 && hi != T)) {
         bad = true;
@@ -684,6 +703,28 @@ __global__ void __launch_bounds__(kGatherThreads)
   if (threadIdx.x == 0) {
     gcnt[u] = gather ? steps : 0;
     if (gather) scnt[u] = steps;
+  }
+}
+
+// Head-stacked units: slab_steps[u] = gathered steps of the 64-row slab u,
+// or -1 when one of its slices is not eligible or it has too many blocks;
+// tot[0] += the steps, tot[1] += the ineligible slabs.
+__global__ void __launch_bounds__(kGatherThreads)
+    k_slab_count(const Slice* __restrict__ sl, const int* __restrict__ list,
+                 const int* __restrict__ loff, const int* __restrict__ lcnt, int n_qt, int Tk,
+                 int* __restrict__ slab_steps, long long* tot) {
+  __shared__ unsigned bits[kGatherBitmapWords];
+  __shared__ int red[kGatherThreads / 32];
+  const int u = blockIdx.x;
+  const GatherUnit gu = gather_unit(u, 2, n_qt);
+  const bool ok = gather_bitmap(sl, list, loff, lcnt, gu, Tk, bits);
+  const int nwords = (((Tk + kGatherKeys - 1) / kGatherKeys) + 31) / 32;
+  const int n = ok ? block_popc(bits, nwords, red) : 0;
+  const int steps = ok && n <= kGatherMaxBlocks ? (n + kGatherSlots - 1) / kGatherSlots : -1;
+  if (threadIdx.x == 0) {
+    slab_steps[u] = max(steps, 0);
+    if (steps >= 0) atomicAdd(reinterpret_cast<unsigned long long*>(tot), (unsigned long long)steps);
+    else atomicAdd(reinterpret_cast<unsigned long long*>(tot + 1), 1ull);
   }
 }
 
@@ -751,13 +792,20 @@ __global__ void __launch_bounds__(kGatherThreads)
   // row bits: each slice marks its rows of the half's q-tile on its blocks
   for (int h = 0; h < 2; ++h) {
     const int qt = gu.qt[h];
-    if (qt < 0 || (h == 1 && pair_mode == 0)) continue;
+    if (qt < 0 || (h == 1 && pair_mode != 1)) continue;
     const int* L = list + loff[qt];
     const int cnt = lcnt[qt];
     for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
       const Slice x = sl[L[i]];
       uint32_t rb[4] = {0u, 0u, 0u, 0u};
-      add_window(max(x.qs, 128 * qt) - 128 * qt, min(x.qe, 128 * qt + 128) - 128 * qt, rb);
+      if (pair_mode == 2) {  // tile rows r and r + 64 are both slab row r
+        if (x.qe <= gu.p0 || x.qs >= gu.p1) continue;
+        const int a = max(x.qs, gu.p0) - gu.p0, b = min(x.qe, gu.p1) - gu.p0;
+        add_window(a, b, rb);
+        add_window(a + kSlabRows, b + kSlabRows, rb);
+      } else {
+        add_window(max(x.qs, 128 * qt) - 128 * qt, min(x.qe, 128 * qt + 128) - 128 * qt, rb);
+      }
       const int b0 = x.ks / kGatherKeys, b1 = (x.ke + kGatherKeys - 1) / kGatherKeys;
       for (int b = b0; b < b1; ++b) {
         const int w = b >> 5;
@@ -769,7 +817,7 @@ __global__ void __launch_bounds__(kGatherThreads)
   }
   if (threadIdx.x < 2) cost[threadIdx.x] = 0;
   __syncthreads();
-  if (pair_mode == 0)  // both halves are the same q-tile (two heads)
+  if (pair_mode != 1)  // both halves are the same rows (two heads, or two head pairs)
     for (int i = threadIdx.x; i < n * 4; i += blockDim.x) rmask[n * 4 + i] = rmask[i];
   __syncthreads();
   const int r0 = goff[u], s0 = soff[u];
@@ -1210,8 +1258,8 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
   // forward units -> steps
-  const int pair_mode = g >= 2 ? 0 : 1;
-  const int n_units = pair_mode == 0 ? n_qt : (n_qt + 1) / 2;
+  int pair_mode = g >= 2 ? 0 : 1;
+  int n_units = pair_mode == 0 ? n_qt : (n_qt + 1) / 2;
   DevBuf scnt(st), soff(st), cost_half(st), steps(st);
   FFA_CUDA(scnt.alloc(sizeof(int) * n_units));
   FFA_CUDA(soff.alloc(sizeof(int) * n_units));
@@ -1235,10 +1283,46 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
     note_launches(1);
     FFA_CUDA(cudaGetLastError());
   }
-  long long sg[2];  // steps, gathered records
+  // head-stacked units (64-row slabs, heads stacked in pairs): counted beside
+  // the q-tile units and chosen after the read below when every slab gathers
+  // and they take at most 9/10 of the tile steps (per group of four heads)
+  const bool try_stack = pair_mode == 0 && g >= 4 && g % 2 == 0 && p->Tk <= kGatherMaxTk &&
+                         n_qt > 0;
+  const int n_slabs = (p->Tq + kSlabRows - 1) / kSlabRows;
+  DevBuf slab_steps(st), slab_off(st), slab_cost(st);
+  if (try_stack) {
+    FFA_CUDA(slab_steps.alloc(sizeof(int) * n_slabs));
+    FFA_CUDA(cudaMemsetAsync(dtot + 2, 0, 2 * sizeof(long long), st));
+    k_slab_count<<<n_slabs, kGatherThreads, 0, st>>>(p->slices, qlist.as<int>(), qloff.as<int>(),
+                                                     qlcnt.as<int>(), n_qt, p->Tk,
+                                                     slab_steps.as<int>(), dtot + 2);
+    note_launches(1);
+    FFA_CUDA(cudaGetLastError());
+  }
+  long long sg[4] = {0, 0, 0, 1};  // steps, gathered records; slab steps, ineligible slabs
   if ((rc = scan_launch(scnt.as<int>(), n_units, soff.as<int>(), dtot, st))) return rc;
   if ((rc = scan_launch(gcnt.as<int>(), n_units, goff.as<int>(), dtot + 1, st))) return rc;
-  if ((rc = read_to_host(sg, dtot, sizeof sg, st))) return rc;
+  if ((rc = read_to_host(sg, dtot, (try_stack ? 4 : 2) * sizeof(long long), st))) return rc;
+  const bool stacked = try_stack && sg[3] == 0 && sg[2] > 0 &&
+                       10LL * ((g + 3) / 4) * sg[2] <= 9LL * (g / 2) * sg[0];
+  int* u_scnt = scnt.as<int>();
+  int* u_soff = soff.as<int>();
+  int* u_gcnt = gcnt.as<int>();
+  int* u_goff = goff.as<int>();
+  int* u_cost = cost_half.as<int>();
+  if (stacked) {  // every step gathered: record r is step r, offsets shared
+    pair_mode = 2;
+    n_units = n_slabs;
+    FFA_CUDA(slab_off.alloc(sizeof(int) * n_slabs));
+    FFA_CUDA(slab_cost.alloc(sizeof(int) * 2 * n_slabs));
+    FFA_CUDA(cudaMemsetAsync(slab_cost.p, 0, sizeof(int) * 2 * n_slabs, st));
+    if ((rc = scan_launch(slab_steps.as<int>(), n_slabs, slab_off.as<int>(), dtot, st))) return rc;
+    u_scnt = u_gcnt = slab_steps.as<int>();
+    u_soff = u_goff = slab_off.as<int>();
+    u_cost = slab_cost.as<int>();
+    sg[0] = sg[1] = sg[2];
+    p->stacked = 1;
+  }
   tot = sg[0];
   if (tot > 0x7fffffffLL || sg[1] > (1LL << 24)) return FFA_ERR_UNSUPPORTED;
   p->n_fwd_steps = tot;
@@ -1246,25 +1330,27 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   FFA_CUDA(steps.alloc(sizeof(int4) * (size_t)tot));
   FFA_CUDA(cudaMallocAsync(&p->gathers,
                            sizeof(int) * kGatherWords * (size_t)std::max(1LL, sg[1]), st));
-  k_fwd_unit_fill<<<grid_for(n_units, 128), 128, 0, st>>>(visits.as<int2>(), voff.as<int>(),
-                                                          vcnt.as<int>(), n_qt, n_units,
-                                                          pair_mode, soff.as<int>(),
-                                                          gcnt.as<int>(), steps.as<int4>());
-  note_launches(1);
-  FFA_CUDA(cudaGetLastError());
+  if (!stacked) {
+    k_fwd_unit_fill<<<grid_for(n_units, 128), 128, 0, st>>>(visits.as<int2>(), voff.as<int>(),
+                                                            vcnt.as<int>(), n_qt, n_units,
+                                                            pair_mode, soff.as<int>(),
+                                                            gcnt.as<int>(), steps.as<int4>());
+    note_launches(1);
+    FFA_CUDA(cudaGetLastError());
+  }
   if (sg[1] > 0) {
     FFA_CUDA(cudaFuncSetAttribute(k_gather_fill, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kGatherFillSmem));
     k_gather_fill<<<n_units, kGatherThreads, kGatherFillSmem, st>>>(
         p->slices, qlist.as<int>(), qloff.as<int>(), qlcnt.as<int>(), n_qt, pair_mode, p->Tk,
-        gcnt.as<int>(), goff.as<int>(), soff.as<int>(), steps.as<int4>(), p->gathers,
-        cost_half.as<int>());
+        u_gcnt, u_goff, u_soff, steps.as<int4>(), p->gathers, u_cost);
     note_launches(1);
     FFA_CUDA(cudaGetLastError());
   }
   // forward items
-  const int pairs = (g + 1) / 2;
-  const long long n_items = pair_mode == 0 ? (long long)n_units * p->Hkv * pairs
+  // head pairs per kv head (groups of four heads for stacked units)
+  const int pairs = pair_mode == 2 ? (g + 3) / 4 : (g + 1) / 2;
+  const long long n_items = pair_mode != 1 ? (long long)n_units * p->Hkv * pairs
                                            : (long long)n_units * p->Hq;
   if (n_items > 0x7fffffffLL / kFiWords) return FFA_ERR_UNSUPPORTED;
   DevBuf items(st), live(st);
@@ -1272,9 +1358,8 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   FFA_CUDA(live.alloc(sizeof(int)));
   FFA_CUDA(cudaMemsetAsync(live.p, 0, sizeof(int), st));
   k_fwd_items<<<grid_for(n_items, 128), 128, 0, st>>>((int)n_items, pair_mode, g, p->Hkv, p->Hq,
-                                                      pairs, n_qt, soff.as<int>(), scnt.as<int>(),
-                                                      cost_half.as<int>(), items.as<int>(),
-                                                      live.as<int>());
+                                                      pairs, n_qt, u_soff, u_scnt, u_cost,
+                                                      items.as<int>(), live.as<int>());
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
   int hlive = 0;
@@ -1284,7 +1369,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   }
   const int threshold = split_below == 0 ? 2 * p->num_sms : split_below;
   long long final_items = n_items;
-  if (split_below >= 0 && hlive > 0 && hlive < threshold) {
+  if (split_below >= 0 && hlive > 0 && hlive < threshold && !stacked) {
     const int nsplit = std::min(16, (threshold + hlive - 1) / hlive);
     DevBuf chunks(st), coff(st), slots(st), sloff(st), groups(st), goff(st), nitems(st),
         merges(st);
@@ -1558,6 +1643,7 @@ ffa_status_t ffa_plan_info(ffa_plan_t p, ffa_plan_info_t* info) {
   info->bwd_masks = p->n_bwd_masks;
   info->gathers = p->n_gathers;
   info->bgathers = p->n_bgathers;
+  info->stacked = p->stacked;
   return FFA_OK;
 }
 

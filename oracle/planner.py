@@ -38,7 +38,19 @@ the work-list specification of the planner:
     at most 9/10 of its visits; a step is (0, 1, 0, r + 1) with record r =
     16 block start rows (-8: unused) then 16 x 4 words of key bits (bit i of
     word w: key 32w + i of the k-tile is seen by the slot's rows); cost 5
-    per step (times g in the item).
+    per step (times g in the item);
+  * head-stacked forward units: with g even and >= 4, Tk <= 2^19, when
+    every 64-row slab of the queries meets only FULL slices with 8-aligned
+    key ranges (at most 2048 blocks per slab), and ceil(g / 4) times the
+    slabs' gathered steps is at most 9/10 of g / 2 times the steps chosen
+    above, the forward units become the slabs instead: slab s (rows 64s ..
+    64s + 63) lists the 8-key blocks its slices cover, 16 to a step, as
+    above, with row bits for tile rows r and r + 64 both meaning row
+    64s + r (the same bits in both halves); items are (s, s, h, h + 2) for
+    the first query head h = hk * g + 4p of each group of four (half 1 idle,
+    s and head -1, when 4p + 2 >= g): a half is the slab's 64 rows of heads
+    h and h + 1 (h + 2 and h + 3), stacked in one 128-row tile.  Such plans
+    are never split.
 """
 from __future__ import annotations
 
@@ -53,6 +65,7 @@ GATHER_SLOTS = 16         # slots per gathered step (a 128-key tile)
 GATHER_MAX_BLOCKS = 2048  # blocks per gathered unit
 GATHER_MAX_TK = 1 << 19
 GATHER_WORDS = GATHER_SLOTS + 2 * GATHER_SLOTS * 4
+SLAB = 64                 # query rows per head-stacked unit
 BGATHER_WORDS = GATHER_SLOTS + GATHER_SLOTS * 4
 
 
@@ -186,8 +199,39 @@ def plan(total_q, total_k, num_heads_q, num_heads_kv, q_ranges, k_ranges, mask_t
         steps.extend(st)
         scnt.append(len(st))
 
+    stacked = False
+    if pair_mode == 0 and g >= 4 and g % 2 == 0:
+        slabs = gather_slabs(total_q, total_k, q_ranges, k_ranges, mask_types)
+        if slabs is not None:
+            n_slab_steps = sum(len(v) for v in slabs.values())
+            if n_slab_steps > 0 and 10 * (-(-g // 4)) * n_slab_steps <= 9 * (g // 2) * len(steps):
+                stacked = True
+    if stacked:
+        n_units = -(-total_q // SLAB)
+        records, steps, soff, scnt, cost_half = [], [], [], [], []
+        for u in range(n_units):
+            soff.append(len(steps))
+            ca = cb = 0
+            for rec, (i0, i1) in slabs.get(u, []):
+                steps.append((0, i0, i1, len(records) + 1))
+                records.append(rec)
+                ca += PARTIAL_COST if i0 >= 0 else 0
+                cb += PARTIAL_COST if i1 >= 0 else 0
+            cost_half.append((ca, cb))
+            scnt.append(len(steps) - soff[-1])
+
     items = []
-    if pair_mode == 0:
+    if stacked:
+        quads = -(-g // 4)
+        for u in range(n_units):
+            for hk in range(num_heads_kv):
+                for p in range(quads):
+                    h0 = hk * g + 4 * p
+                    h1 = h0 + 2 if 4 * p + 2 < g else -1
+                    qt1 = u if h1 >= 0 else -1
+                    cost = cost_half[u][0] + (cost_half[u][1] if h1 >= 0 else 0)
+                    items.append([u, qt1, h0, h1, soff[u], soff[u] + scnt[u], -1, cost])
+    elif pair_mode == 0:
         pairs = (g + 1) // 2
         for u in range(n_units):
             for hk in range(num_heads_kv):
@@ -208,7 +252,7 @@ def plan(total_q, total_k, num_heads_q, num_heads_kv, q_ranges, k_ranges, mask_t
     live = sum(1 for it in items if it[5] > it[4])
     threshold = 2 * num_sms if split_below == 0 else split_below
     merges, n_slots = [], 0
-    if split_below >= 0 and 0 < live < threshold:
+    if split_below >= 0 and 0 < live < threshold and not stacked:
         nsplit = min(16, -(-threshold // live))
         new = []
         for it in items:
@@ -267,6 +311,7 @@ def plan(total_q, total_k, num_heads_q, num_heads_kv, q_ranges, k_ranges, mask_t
         "bgathers": np.array(brecords, dtype=np.int32).reshape(-1, BGATHER_WORDS),
         "bwd_masks": np.array(bmasks, dtype=np.int32).reshape(-1, 1),
         "n_slots": n_slots,
+        "stacked": stacked,
         "grid_fwd": max(1, min(num_sms, len(items))),
         "grid_bwd": max(1, min(num_sms, len(bitems))),
         "area": visible_area(q_ranges, k_ranges, mask_types),
@@ -331,6 +376,50 @@ def gather_units(total_q, total_k, q_ranges, k_ranges, mask_types, pair_mode, fv
                 infos.append(1 if words.any() else -1)
             res.append((rec, (infos[0], infos[1])))
         out[u] = res
+    return out
+
+
+def gather_slabs(total_q, total_k, q_ranges, k_ranges, mask_types):
+    """{slab: [(record words, (info0, info1)), ...]} of the head-stacked
+    units, or None when some slab is not eligible."""
+    if total_k > GATHER_MAX_TK:
+        return None
+    n_slabs = -(-total_q // SLAB)
+    lists = [[] for _ in range(n_slabs)]
+    for (qs, qe), (ks, ke), t in zip(np.asarray(q_ranges).reshape(-1, 2),
+                                     np.asarray(k_ranges).reshape(-1, 2),
+                                     np.asarray(mask_types).reshape(-1)):
+        qs, qe, ks, ke, t = int(qs), int(qe), int(ks), int(ke), int(t)
+        if qe <= qs or ke <= ks:
+            continue
+        for u in range(qs // SLAB, -(-qe // SLAB)):
+            lists[u].append((qs, qe, ks, ke, t))
+    out = {}
+    for u, sl in enumerate(lists):
+        if any(t != 0 or ks % GATHER_KEYS or (ke % GATHER_KEYS and ke != total_k)
+               for _, _, ks, ke, t in sl):
+            return None
+        blocks = sorted({b for _, _, ks, ke, _ in sl
+                         for b in range(ks // GATHER_KEYS, -(-ke // GATHER_KEYS))})
+        if len(blocks) > GATHER_MAX_BLOCKS:
+            return None
+        res = []
+        for j in range(-(-len(blocks) // GATHER_SLOTS)):
+            bs = blocks[GATHER_SLOTS * j: GATHER_SLOTS * (j + 1)]
+            rec = [GATHER_KEYS * b for b in bs] + [-GATHER_KEYS] * (GATHER_SLOTS - len(bs))
+            words = np.zeros((GATHER_SLOTS, 4), dtype=np.uint32)
+            for slot, b in enumerate(bs):
+                k0, k1 = GATHER_KEYS * b, GATHER_KEYS * (b + 1)
+                for qs, qe, ks, ke, _ in sl:
+                    if ks < k1 and ke > k0:
+                        for r in range(max(qs, SLAB * u), min(qe, SLAB * (u + 1))):
+                            for rr in (r - SLAB * u, r - SLAB * u + SLAB):
+                                words[slot, rr >> 5] |= np.uint32(1 << (rr & 31))
+            half = [int(w) for w in words.view(np.int32).reshape(-1)]
+            info = 1 if words.any() else -1
+            res.append((rec + half + half, (info, info)))
+        if res:
+            out[u] = res
     return out
 
 

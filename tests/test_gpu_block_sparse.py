@@ -112,3 +112,48 @@ def test_block_sparse_gathered_softcap_sink(case):
     check_grad(dv.float().cpu().numpy(), rv, "dv")
     rs = oracle.dsink(q, k, v, do, *a, sink, "sh", softcap=cap)
     check_grad(ds.cpu().numpy(), rs, "dsink")
+
+
+
+# Head-stacked forward units (a 128-row tile holds one 64-row slab of two
+# query heads): Hq / Hkv = 4 or 6, ragged T, D = 128 and 64, with and without
+# sink logits and softcap.
+STACKED = [
+    # (total, hq, hkv, d, q_block, k_block, seed, sink, cap)
+    (2000, 8, 2, 128, 64, 64, 51, False, 0.0),
+    (2000, 8, 2, 128, 16, 64, 52, True, 0.0),
+    (1500, 12, 2, 64, 32, 64, 53, False, 0.0),
+    (1000, 4, 1, 128, 64, 8, 54, True, 5.0),
+]
+
+
+@pytest.mark.parametrize("case", STACKED,
+                         ids=[f"T{c[0]}_H{c[1]}x{c[2]}_D{c[3]}_q{c[4]}_k{c[5]}" for c in STACKED])
+def test_block_sparse_stacked(case):
+    total, hq, hkv, d, qb, kb, seed, with_sink, cap = case
+    wl = W.block_sparse(total=total, hq=hq, hkv=hkv, d=d, q_block=qb, k_block=kb, seed=seed)
+    q, k, v, do = W.make_tensors(wl, with_dout=True)
+    if cap > 0:
+        q = (q.float() * 2.5).to(torch.bfloat16)
+        k = (k.float() * 2.5).to(torch.bfloat16)
+    sink = (2.0 * torch.randn(2, hq, generator=torch.Generator().manual_seed(seed))).float() \
+        if with_sink else None
+    plan = ffa.ffa_plan_create(wl.q_ranges, wl.k_ranges, wl.mask_types, wl.total_q, wl.total_k,
+                               hq, hkv, d)
+    assert ffa.ffa_plan_info(plan)["stacked"] == 1
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    sd = sink.to(DEV) if sink is not None else None
+    out, lse = ffa.ffa_fwd_ex(plan, qd, kd, vd, sink=sd, softcap=cap)
+    dq, dk, dv, ds = ffa.ffa_bwd_ex(plan, qd, kd, vd, out, dod, lse, sink=sd, softcap=cap)
+    torch.cuda.synchronize()
+    assert ffa.ffa_get_last_device_error(plan) == (0, 0)
+    a = (wl.q_ranges, wl.k_ranges, wl.mask_types)
+    ro, rl = oracle.fwd(q, k, v, *a, sink=sink, softcap=cap)
+    check_fwd(out.float().cpu().numpy(), lse.cpu().numpy(), ro, rl)
+    rq, rk, rv = oracle.bwd(q, k, v, do, *a, sink=sink, softcap=cap)
+    check_grad(dq.float().cpu().numpy(), rq, "dq")
+    check_grad(dk.float().cpu().numpy(), rk, "dk")
+    check_grad(dv.float().cpu().numpy(), rv, "dv")
+    if sink is not None:
+        rs = oracle.dsink(q, k, v, do, *a, sink, "sh", softcap=cap)
+        check_grad(ds.cpu().numpy(), rs, "dsink")

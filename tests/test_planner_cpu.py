@@ -266,3 +266,68 @@ def test_gathered_backward_steps_cover_the_mask_exactly(blocks, seed, heads):
         assert (got[ref] == 1).all(), "a visible pair is missed or listed twice"
         assert (got[~ref] == 0).all(), "an invisible pair is marked visible"
     assert seen_tiles > 0
+
+
+# (q block, k block, seed, heads) of tables whose forward units are stacked:
+# Hq / Hkv = 4 or 6, T = 1000 (the last 64-row slab is ragged)
+STACK_CASES = [((64, 64), 1, (8, 2)), ((16, 64), 3, (8, 2)), ((64, 8), 2, (4, 1)),
+               ((32, 64), 7, (12, 2))]
+
+
+@pytest.mark.parametrize("blocks,seed,heads", STACK_CASES)
+def test_stacked_units_cover_the_mask_exactly(blocks, seed, heads):
+    """Head-stacked forward units (the planner specification for g even and
+    >= 4): every (64-row slab, query head) is one half's tile rows 0-63 or
+    64-127 of exactly one item; the (row, key) pairs its steps' row bits mark
+    are exactly the visible pairs of the slab's rows, each once; tile rows r
+    and r + 64 carry the same bits; the plan is not split."""
+    m, p = _block_sparse_plan(blocks, seed, heads)
+    assert p["stacked"] and p["merges"].shape[0] == 0
+    T, Hq, g = m.shape[1], heads[0], heads[0] // heads[1]
+    n_slabs = -(-T // 64)
+    steps, rec = p["fwd_steps"], p["gathers"]
+    assert (steps[:, 3] > 0).all(), "every step of a stacked plan is gathered"
+    marked, seen = {}, {}
+    for it in p["fwd_items"]:
+        assert it[6] == -1
+        for h in range(2):
+            u, h0 = it[h], it[2 + h]
+            if u < 0 or h0 < 0:
+                continue
+            assert h0 % 2 == 0 and h0 // g == (h0 + 1) // g
+            for j in range(2):
+                seen[(u, h0 + j)] = seen.get((u, h0 + j), 0) + 1
+                marked.setdefault((u, h0 + j), np.zeros((64, T), np.int64))
+            for st in steps[it[4]:it[5]]:
+                r = rec[st[3] - 1]
+                starts = r[:16]
+                words = r[16 + 64 * h: 16 + 64 * (h + 1)].view(np.uint32).reshape(16, 4)
+                assert (st[1 + h] >= 0) == bool(words.any())
+                for slot, y in enumerate(starts):
+                    if y < 0:
+                        assert not words[slot].any()
+                        continue
+                    bits = (words[slot][np.arange(128) >> 5] >> (np.arange(128) & 31)) & 1
+                    assert (bits[:64] == bits[64:]).all()
+                    for j in range(2):
+                        for rr in np.nonzero(bits[64 * j: 64 * j + 64])[0]:
+                            marked[(u, h0 + j)][rr, y:min(y + 8, T)] += 1
+    assert set(seen) == {(u, hq) for u in range(n_slabs) for hq in range(Hq)}
+    assert all(c == 1 for c in seen.values())
+    for (u, _), got in marked.items():
+        ref = m[64 * u: min(64 * u + 64, T)]
+        got = got[: ref.shape[0]]
+        assert (got[ref] == 1).all(), "a visible pair is missed or listed twice"
+        assert (got[~ref] == 0).all(), "an invisible pair is marked visible"
+
+
+def test_stacking_needs_four_heads_and_every_slab_eligible():
+    """Two heads per kv head do not stack; one causal slice among the blocks
+    keeps the tile units."""
+    _, p = _block_sparse_plan((64, 64), 1, (4, 2))
+    assert not p["stacked"]
+    wl = W.block_sparse(total=1000, hq=8, hkv=2, q_block=64, k_block=64, seed=1)
+    ty = wl.mask_types.copy()
+    ty[0] = 1
+    p = planner.plan(1000, 1000, 8, 2, wl.q_ranges, wl.k_ranges, ty, num_sms=152)
+    assert not p["stacked"]
