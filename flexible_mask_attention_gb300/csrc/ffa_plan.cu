@@ -468,6 +468,136 @@ __global__ void k_fwd_unit_fill(const int2* __restrict__ visits, const int* __re
   }
 }
 
+// Warp-parallel forms of k_fwd_unit_count / k_fill (one warp per unit; the
+// serial ones above stay for key ranges longer than kUnitWarpTiles tiles).
+// A unit of two q-tiles merges their visit lists on kt: the k-tiles either
+// list holds are marked in shared-memory bitmaps, and a visit's place in the
+// merged list is the count of marked k-tiles below it.
+constexpr int kUnitWarpTiles = 8192;
+constexpr int kUnitWarpWords = kUnitWarpTiles / 32;
+constexpr int kUnitWarps = 2;  // warps per block
+
+__device__ __forceinline__ int warp_sum(int v) {
+  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+  return v;
+}
+
+// Bitmaps of the k-tiles of lists a and b, their union, and exclusive
+// prefix counts of the union's and b's words.
+struct UnitBits {
+  unsigned a[kUnitWarpWords], b[kUnitWarpWords];
+  int pre_u[kUnitWarpWords], pre_b[kUnitWarpWords];
+};
+
+__device__ void unit_bits(const int2* a, int na, const int2* b, int nb, int words, UnitBits& m) {
+  const int lane = threadIdx.x & 31;
+  for (int w = lane; w < words; w += 32) m.a[w] = m.b[w] = 0u;
+  __syncwarp();
+  for (int i = lane; i < na; i += 32) atomicOr(&m.a[a[i].x >> 5], 1u << (a[i].x & 31));
+  for (int i = lane; i < nb; i += 32) atomicOr(&m.b[b[i].x >> 5], 1u << (b[i].x & 31));
+  __syncwarp();
+  int carry_u = 0, carry_b = 0;
+  for (int w0 = 0; w0 < words; w0 += 32) {
+    const int w = w0 + lane;
+    const int cu = w < words ? __popc(m.a[w] | m.b[w]) : 0, cb = w < words ? __popc(m.b[w]) : 0;
+    int iu = cu, ib = cb;  // inclusive warp scans
+    for (int d = 1; d < 32; d <<= 1) {
+      const int yu = __shfl_up_sync(0xffffffffu, iu, d), yb = __shfl_up_sync(0xffffffffu, ib, d);
+      if (lane >= d) {
+        iu += yu;
+        ib += yb;
+      }
+    }
+    if (w < words) {
+      m.pre_u[w] = carry_u + iu - cu;
+      m.pre_b[w] = carry_b + ib - cb;
+    }
+    carry_u += __shfl_sync(0xffffffffu, iu, 31);
+    carry_b += __shfl_sync(0xffffffffu, ib, 31);
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ int rank_below(const unsigned* bits, const int* pre, int x) {
+  return pre[x >> 5] + __popc(bits[x >> 5] & ((1u << (x & 31)) - 1u));
+}
+
+__global__ void __launch_bounds__(32 * kUnitWarps)
+    k_fwd_unit_count_w(const int2* __restrict__ visits, const int* __restrict__ voff,
+                       const int* __restrict__ vcnt, int n_qt, int n_units, int pair_mode,
+                       int n_kt, int* scnt, int* cost_half) {
+  __shared__ UnitBits sm[kUnitWarps];
+  const int u = blockIdx.x * kUnitWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (u >= n_units) return;  // whole warp
+  if (pair_mode == 0) {
+    const int2* a = visits + voff[u];
+    int c = 0;
+    for (int i = lane; i < vcnt[u]; i += 32) c += visit_cost(a[i].y);
+    c = warp_sum(c);
+    if (lane == 0) {
+      scnt[u] = vcnt[u];
+      cost_half[2 * u] = cost_half[2 * u + 1] = c;
+    }
+    return;
+  }
+  const int qa = 2 * u, qb = 2 * u + 1;
+  const int na = vcnt[qa], nb = qb < n_qt ? vcnt[qb] : 0;
+  const int2* a = visits + voff[qa];
+  const int2* b = qb < n_qt ? visits + voff[qb] : visits;
+  UnitBits& m = sm[threadIdx.x >> 5];
+  const int words = (n_kt + 31) / 32;
+  unit_bits(a, na, b, nb, words, m);
+  int ca = 0, cb = 0, common = 0;
+  for (int i = lane; i < na; i += 32) {
+    ca += visit_cost(a[i].y);
+    common += (m.b[a[i].x >> 5] >> (a[i].x & 31)) & 1u;
+  }
+  for (int i = lane; i < nb; i += 32) cb += visit_cost(b[i].y);
+  ca = warp_sum(ca);
+  cb = warp_sum(cb);
+  common = warp_sum(common);
+  if (lane == 0) {
+    scnt[u] = na + nb - common;
+    cost_half[2 * u] = ca;
+    cost_half[2 * u + 1] = cb;
+  }
+}
+
+__global__ void __launch_bounds__(32 * kUnitWarps)
+    k_fwd_unit_fill_w(const int2* __restrict__ visits, const int* __restrict__ voff,
+                      const int* __restrict__ vcnt, int n_qt, int n_units, int pair_mode,
+                      int n_kt, const int* __restrict__ soff, const int* __restrict__ gcnt,
+                      int4* steps) {
+  __shared__ UnitBits sm[kUnitWarps];
+  const int u = blockIdx.x * kUnitWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (u >= n_units || gcnt[u] > 0) return;  // whole warp; gathered units: k_gather_fill
+  int4* o = steps + soff[u];
+  if (pair_mode == 0) {
+    const int2* a = visits + voff[u];
+    for (int i = lane; i < vcnt[u]; i += 32) o[i] = make_int4(a[i].x, a[i].y, a[i].y, 0);
+    return;
+  }
+  const int qa = 2 * u, qb = 2 * u + 1;
+  const int na = vcnt[qa], nb = qb < n_qt ? vcnt[qb] : 0;
+  const int2* a = visits + voff[qa];
+  const int2* b = qb < n_qt ? visits + voff[qb] : visits;
+  UnitBits& m = sm[threadIdx.x >> 5];
+  const int words = (n_kt + 31) / 32;
+  unit_bits(a, na, b, nb, words, m);
+  for (int i = lane; i < na; i += 32) {
+    const int x = a[i].x;
+    const bool in_b = (m.b[x >> 5] >> (x & 31)) & 1u;
+    const int pos = m.pre_u[x >> 5] + __popc((m.a[x >> 5] | m.b[x >> 5]) & ((1u << (x & 31)) - 1u));
+    o[pos] = make_int4(x, a[i].y, in_b ? b[rank_below(m.b, m.pre_b, x)].y : -1, 0);
+  }
+  for (int j = lane; j < nb; j += 32) {
+    const int x = b[j].x;
+    if ((m.a[x >> 5] >> (x & 31)) & 1u) continue;  // merged with a's visit above
+    const int pos = m.pre_u[x >> 5] + __popc((m.a[x >> 5] | m.b[x >> 5]) & ((1u << (x & 31)) - 1u));
+    o[pos] = make_int4(x, -1, b[j].y, 0);
+  }
+}
+
 __global__ void k_fwd_items(int n_items, int pair_mode, int g, int Hkv, int Hq, int pairs,
                             int n_qt, const int* __restrict__ soff, const int* __restrict__ scnt,
                             const int* __restrict__ cost_half, int* items, int* live) {
@@ -555,32 +685,37 @@ __global__ void k_split_fill(const int* __restrict__ items, int n_items,
 }
 
 // ---- backward items ---------------------------------------------------------
+// One warp per k-tile: its steps (the visits, unless gathered) and the
+// items of every kv head.
 __global__ void k_bwd_items(int n_kt, int Hkv, int g, const int2* __restrict__ visits,
                             const int* __restrict__ voff, const int* __restrict__ vcnt,
                             const int* __restrict__ soff, const int* __restrict__ gcnt,
                             int4* steps, int* items) {
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= n_kt * Hkv) return;
-  const int kt = idx / Hkv, hk = idx % Hkv;
+  const int kt = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (kt >= n_kt) return;  // whole warp
   const int b = soff[kt], ng = gcnt[kt];
   int c = 0, n = ng;
   if (ng > 0) {  // gathered k-tile: its steps are k_bgather_fill's
     c = kPartialCost * ng;
   } else {
     n = vcnt[kt];
-    for (int i = 0; i < n; ++i) {
-      const int2 v = visits[voff[kt] + i];
-      c += visit_cost(v.y);
-      if (hk == 0) steps[b + i] = make_int4(v.x, v.y, 0, 0);
+    const int2* v = visits + voff[kt];
+    for (int i = lane; i < n; i += 32) {
+      const int2 x = v[i];
+      c += visit_cost(x.y);
+      steps[b + i] = make_int4(x.x, x.y, 0, 0);
     }
+    c = warp_sum(c);
   }
-  int* it = items + (size_t)idx * kBiWords;
-  it[kBiKt] = kt;
-  it[kBiHkv] = hk;
-  it[kBiStepBeg] = b;
-  it[kBiStepEnd] = b + n;
-  it[kBiCost] = c * g;
-  it[5] = it[6] = it[7] = 0;
+  for (int hk = lane; hk < Hkv; hk += 32) {
+    int* it = items + ((size_t)kt * Hkv + hk) * kBiWords;
+    it[kBiKt] = kt;
+    it[kBiHkv] = hk;
+    it[kBiStepBeg] = b;
+    it[kBiStepEnd] = b + n;
+    it[kBiCost] = c * g;
+    it[5] = it[6] = it[7] = 0;
+  }
 }
 
 // Visits of each half of the (unsplit) forward items the dQ pass walks: a
@@ -977,21 +1112,24 @@ __global__ void __launch_bounds__(kGatherThreads)
 // than L2-memory latency each.
 constexpr int kSortSmemKeys = 16384;
 
+__device__ __forceinline__ unsigned long long sort_key(const int* __restrict__ items, int words,
+                                                       int cost_word, int n, int head_word,
+                                                       int head_div, int i) {
+  if (i >= n) return ~0ull;
+  const int* it = items + (size_t)i * words;
+  const unsigned long long c = (unsigned int)it[cost_word] & 0x3ffffffu;
+  const unsigned long long hk = (unsigned int)(max(it[head_word], 0) / head_div) & 0xffu;
+  const unsigned long long oct = 63u - min(63u, (unsigned int)(63 - __clzll((long long)c + 1)));
+  return (oct << 58) | (hk << 50) | ((0x3ffffffull - c) << 24) | (unsigned long long)i;
+}
+
 __global__ void k_sort_order(const int* __restrict__ items, int words, int cost_word, int n,
                              int n2, unsigned long long* scratch, int* order, int head_word,
                              int head_div) {
   extern __shared__ unsigned long long sort_keys[];
   unsigned long long* keys = n2 <= kSortSmemKeys ? sort_keys : scratch;
   for (int i = threadIdx.x; i < n2; i += blockDim.x) {
-    unsigned long long key = ~0ull;
-    if (i < n) {
-      const int* it = items + (size_t)i * words;
-      const unsigned long long c = (unsigned int)it[cost_word] & 0x3ffffffu;
-      const unsigned long long hk = (unsigned int)(max(it[head_word], 0) / head_div) & 0xffu;
-      const unsigned long long oct = 63u - min(63u, (unsigned int)(63 - __clzll((long long)c + 1)));
-      key = (oct << 58) | (hk << 50) | ((0x3ffffffull - c) << 24) | (unsigned long long)i;
-    }
-    keys[i] = key;
+    keys[i] = sort_key(items, words, cost_word, n, head_word, head_div, i);
   }
   __syncthreads();
   for (int k = 2; k <= n2; k <<= 1) {
@@ -1011,6 +1149,89 @@ __global__ void k_sort_order(const int* __restrict__ items, int words, int cost_
     }
   }
   for (int i = threadIdx.x; i < n; i += blockDim.x) order[i] = (int)(keys[i] & 0xffffffu);
+}
+
+// The same network with each thread holding E consecutive keys in registers
+// (n2 = 1024 E, 2 <= E <= 16): compare-exchange partners within a thread are
+// swapped in registers, partners up to 32 E apart through warp shuffles, and
+// only the passes with wider strides go through shared memory with a block
+// barrier (15 of the 91 passes for n2 = 8192, instead of all of them).
+template <int E>
+__device__ __forceinline__ void cmpx(unsigned long long& lo, unsigned long long& hi, bool up) {
+  if ((lo > hi) == up) {
+    const unsigned long long t = lo;
+    lo = hi;
+    hi = t;
+  }
+}
+
+template <int E>
+__global__ void __launch_bounds__(1024)
+    k_sort_order_blocked(const int* __restrict__ items, int words, int cost_word, int n,
+                         int* order, int head_word, int head_div) {
+  extern __shared__ unsigned long long sort_keys[];  // n2 = 1024 E keys
+  unsigned long long* keys = sort_keys;
+  constexpr int n2 = 1024 * E;
+  const int t = threadIdx.x, lane = t & 31;
+  unsigned long long v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = sort_key(items, words, cost_word, n, head_word, head_div, t * E + e);
+  bool in_smem = false;
+  for (int k = 2; k <= n2; k <<= 1) {
+    int j = k >> 1;
+    for (; j >= E; j >>= 1) {
+      if (j >= 32 * E) {  // partners in other warps: through shared memory
+        if (!in_smem) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) keys[t * E + e] = v[e];
+          in_smem = true;
+        }
+        __syncthreads();
+        for (int p = t; p < n2 / 2; p += 1024) {
+          const int i = (p / j) * 2 * j + (p % j), l = i + j;
+          unsigned long long a = keys[i], b = keys[l];
+          cmpx<E>(a, b, (i & k) == 0);
+          keys[i] = a;
+          keys[l] = b;
+        }
+        continue;
+      }
+      if (in_smem) {
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[e] = keys[t * E + e];
+        in_smem = false;
+      }
+      // partner: lane ^ (j / E), same slot
+      const int m = j / E;
+      const bool lower = (lane & m) == 0;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[e], m);
+        const bool up = (((t * E + e) & k) == 0);
+        const unsigned long long mn = v[e] < o ? v[e] : o, mx = v[e] < o ? o : v[e];
+        v[e] = (lower == up) ? mn : mx;
+      }
+    }
+    if (in_smem) {
+      __syncthreads();
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = keys[t * E + e];
+      in_smem = false;
+    }
+    // strides below E: partners in this thread's registers
+#pragma unroll
+    for (int jj = E / 2; jj > 0; jj >>= 1) {
+      if (jj <= (k >> 1)) {
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          if ((e & jj) == 0) cmpx<E>(v[e], v[e | jj], (((t * E + e) & k) == 0));
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if (t * E + e < n) order[t * E + e] = (int)(v[e] & 0xffffffu);
 }
 
 // ---- host helpers -----------------------------------------------------------
@@ -1126,6 +1347,24 @@ ffa_status_t sort_items(const int* items, int words, int cost_word, int head_wor
   if (n >= (1 << 24)) return FFA_ERR_UNSUPPORTED;
   int n2 = 1;
   while (n2 < n) n2 <<= 1;
+  if (n2 >= 2048 && n2 <= kSortSmemKeys) {
+    const int sm = (int)(sizeof(unsigned long long) * (size_t)n2);
+#define FFA_SORT_BLOCKED(E)                                                                    \
+  do {                                                                                         \
+    FFA_CUDA(cudaFuncSetAttribute(k_sort_order_blocked<E>,                                     \
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, sm));           \
+    k_sort_order_blocked<E><<<1, 1024, sm, st>>>(items, words, cost_word, n, order, head_word, \
+                                                 head_div);                                    \
+  } while (0)
+    if (n2 == 2048) FFA_SORT_BLOCKED(2);
+    else if (n2 == 4096) FFA_SORT_BLOCKED(4);
+    else if (n2 == 8192) FFA_SORT_BLOCKED(8);
+    else FFA_SORT_BLOCKED(16);
+#undef FFA_SORT_BLOCKED
+    note_launches(1);
+    FFA_CUDA(cudaGetLastError());
+    return FFA_OK;
+  }
   DevBuf scratch(st);
   if (n2 > kSortSmemKeys) FFA_CUDA(scratch.alloc(sizeof(unsigned long long) * (size_t)n2));
   const size_t smem = n2 <= kSortSmemKeys ? sizeof(unsigned long long) * (size_t)n2 : 0;
@@ -1264,10 +1503,16 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   FFA_CUDA(scnt.alloc(sizeof(int) * n_units));
   FFA_CUDA(soff.alloc(sizeof(int) * n_units));
   FFA_CUDA(cost_half.alloc(sizeof(int) * 2 * n_units));
-  k_fwd_unit_count<<<grid_for(n_units, 128), 128, 0, st>>>(visits.as<int2>(), voff.as<int>(),
-                                                           vcnt.as<int>(), n_qt, n_units,
-                                                           pair_mode, scnt.as<int>(),
-                                                           cost_half.as<int>());
+  const bool unit_warps = n_kt <= kUnitWarpTiles;
+  if (unit_warps)
+    k_fwd_unit_count_w<<<grid_for(n_units, kUnitWarps), 32 * kUnitWarps, 0, st>>>(
+        visits.as<int2>(), voff.as<int>(), vcnt.as<int>(), n_qt, n_units, pair_mode, n_kt,
+        scnt.as<int>(), cost_half.as<int>());
+  else
+    k_fwd_unit_count<<<grid_for(n_units, 128), 128, 0, st>>>(visits.as<int2>(), voff.as<int>(),
+                                                             vcnt.as<int>(), n_qt, n_units,
+                                                             pair_mode, scnt.as<int>(),
+                                                             cost_half.as<int>());
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
   // gathered units (full, 8-key aligned slices): their step counts replace
@@ -1331,10 +1576,15 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   FFA_CUDA(cudaMallocAsync(&p->gathers,
                            sizeof(int) * kGatherWords * (size_t)std::max(1LL, sg[1]), st));
   if (!stacked) {
-    k_fwd_unit_fill<<<grid_for(n_units, 128), 128, 0, st>>>(visits.as<int2>(), voff.as<int>(),
-                                                            vcnt.as<int>(), n_qt, n_units,
-                                                            pair_mode, soff.as<int>(),
-                                                            gcnt.as<int>(), steps.as<int4>());
+    if (unit_warps)
+      k_fwd_unit_fill_w<<<grid_for(n_units, kUnitWarps), 32 * kUnitWarps, 0, st>>>(
+          visits.as<int2>(), voff.as<int>(), vcnt.as<int>(), n_qt, n_units, pair_mode, n_kt,
+          soff.as<int>(), gcnt.as<int>(), steps.as<int4>());
+    else
+      k_fwd_unit_fill<<<grid_for(n_units, 128), 128, 0, st>>>(visits.as<int2>(), voff.as<int>(),
+                                                              vcnt.as<int>(), n_qt, n_units,
+                                                              pair_mode, soff.as<int>(),
+                                                              gcnt.as<int>(), steps.as<int4>());
     note_launches(1);
     FFA_CUDA(cudaGetLastError());
   }
@@ -1492,7 +1742,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   p->n_bwd_items = nb_items;
   FFA_CUDA(cudaMallocAsync(&p->bwd_items, sizeof(int) * kBiWords * (size_t)std::max(1LL, nb_items), st));
   FFA_CUDA(cudaMallocAsync(&p->bwd_order, sizeof(int) * (size_t)std::max(1LL, nb_items), st));
-  k_bwd_items<<<grid_for(nb_items, 128), 128, 0, st>>>(n_kt, p->Hkv, g, bvis.as<int2>(),
+  k_bwd_items<<<grid_for(n_kt, 4), 128, 0, st>>>(n_kt, p->Hkv, g, bvis.as<int2>(),
                                                        boff.as<int>(), bcnt.as<int>(),
                                                        bsoff.as<int>(), bgcnt.as<int>(),
                                                        p->bwd_steps, p->bwd_items);
