@@ -156,13 +156,27 @@ __global__ void __launch_bounds__(kListThreads)
 }
 
 // Single-block exclusive scan of n int32 counts; total in *total.
-__global__ void k_scan(const int* __restrict__ in, int n, int* __restrict__ out, long long* total) {
+__device__ __forceinline__ int warp_sum(int v) {
+  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+  return v;
+}
+
+__global__ void k_scan(const int* __restrict__ in, int n, int* __restrict__ out, long long* total,
+                       long long* nonzero) {
   __shared__ long long part[1024];
   const int T = blockDim.x, t = threadIdx.x;
   const int per = (n + T - 1) / T;
   const int b = t * per, e = min(n, b + per);
   long long s = 0;
-  for (int i = b; i < e; ++i) s += in[i];
+  int nz = 0;
+  for (int i = b; i < e; ++i) {
+    s += in[i];
+    nz += in[i] != 0;
+  }
+  if (nonzero) {  // entries that are not zero
+    nz = warp_sum(nz);
+    if ((t & 31) == 0 && nz) atomicAdd(reinterpret_cast<unsigned long long*>(nonzero), (unsigned long long)nz);
+  }
   part[t] = s;
   __syncthreads();
   for (int off = 1; off < T; off <<= 1) {
@@ -477,11 +491,6 @@ constexpr int kUnitWarpTiles = 8192;
 constexpr int kUnitWarpWords = kUnitWarpTiles / 32;
 constexpr int kUnitWarps = 2;  // warps per block
 
-__device__ __forceinline__ int warp_sum(int v) {
-  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
-  return v;
-}
-
 // Bitmaps of the k-tiles of lists a and b, their union, and exclusive
 // prefix counts of the union's and b's words.
 struct UnitBits {
@@ -600,7 +609,7 @@ __global__ void __launch_bounds__(32 * kUnitWarps)
 
 __global__ void k_fwd_items(int n_items, int pair_mode, int g, int Hkv, int Hq, int pairs,
                             int n_qt, const int* __restrict__ soff, const int* __restrict__ scnt,
-                            const int* __restrict__ cost_half, int* items, int* live) {
+                            const int* __restrict__ cost_half, int* items) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= n_items) return;
   int u, qt0, qt1, h0, h1;
@@ -636,7 +645,6 @@ __global__ void k_fwd_items(int n_items, int pair_mode, int g, int Hkv, int Hq, 
   it[kFiStepEnd] = soff[u] + scnt[u];
   it[kFiSlot] = -1;
   it[kFiCost] = cost_half[2 * u] + (h1 >= 0 ? cost_half[2 * u + 1] : 0);
-  if (scnt[u] > 0) atomicAdd(live, 1);
 }
 
 // Split: chunk counts per item, then the chunked item list and merge groups.
@@ -841,9 +849,10 @@ __global__ void __launch_bounds__(kGatherThreads)
   }
 }
 
-// Head-stacked units: slab_steps[u] = gathered steps of the 64-row slab u,
-// or -1 when one of its slices is not eligible or it has too many blocks;
-// tot[0] += the steps, tot[1] += the ineligible slabs.
+// Head-stacked units: slab_steps[u] = gathered steps of the 64-row slab u
+// (0 when one of its slices is not eligible or it has too many blocks);
+// tot[0] += the steps, tot[1] += the ineligible slabs, tot[5] += the slabs
+// with steps.
 __global__ void __launch_bounds__(kGatherThreads)
     k_slab_count(const Slice* __restrict__ sl, const int* __restrict__ list,
                  const int* __restrict__ loff, const int* __restrict__ lcnt, int n_qt, int Tk,
@@ -860,6 +869,7 @@ __global__ void __launch_bounds__(kGatherThreads)
     slab_steps[u] = max(steps, 0);
     if (steps >= 0) atomicAdd(reinterpret_cast<unsigned long long*>(tot), (unsigned long long)steps);
     else atomicAdd(reinterpret_cast<unsigned long long*>(tot + 1), 1ull);
+    if (steps > 0) atomicAdd(reinterpret_cast<unsigned long long*>(tot + 5), 1ull);
   }
 }
 
@@ -1324,9 +1334,11 @@ ffa_status_t read_to_host(void* dst, const void* src, size_t bytes, cudaStream_t
 
 // Exclusive scan of in[0, n) into out, total into *dtot (device), no read back:
 // independent scans are launched back to back and their totals read at once.
-ffa_status_t scan_launch(const int* in, int n, int* out, long long* dtot, cudaStream_t st) {
+// nonzero (optional, zeroed by the caller): += the count of nonzero entries.
+ffa_status_t scan_launch(const int* in, int n, int* out, long long* dtot, cudaStream_t st,
+                         long long* nonzero = nullptr) {
   if (n > 0) {
-    k_scan<<<1, 1024, 0, st>>>(in, n, out, dtot);
+    k_scan<<<1, 1024, 0, st>>>(in, n, out, dtot, nonzero);
     note_launches(1);
   } else FFA_CUDA(cudaMemsetAsync(dtot, 0, sizeof(long long), st));
   FFA_CUDA(cudaGetLastError());
@@ -1403,11 +1415,11 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   FFA_CUDA(cudaMallocAsync(&p->tickets, 4 * sizeof(int), st));
   FFA_CUDA(cudaMemsetAsync(p->err, 0, 2 * sizeof(int), st));
   DevBuf flags_area(st);
-  FFA_CUDA(flags_area.alloc(64));
+  FFA_CUDA(flags_area.alloc(128));
   int* flags = flags_area.as<int>();
   unsigned long long* area = reinterpret_cast<unsigned long long*>(flags + 4);
   long long* dtot = reinterpret_cast<long long*>(flags + 8);
-  FFA_CUDA(cudaMemsetAsync(flags, 0, 64, st));
+  FFA_CUDA(cudaMemsetAsync(flags, 0, 128, st));
   if (S > 0) {
     k_pack_slices<<<grid_for(S, 256), 256, 0, st>>>(qr, kr, ty, S, p->slices);
     note_launches(1);
@@ -1480,9 +1492,23 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
       fmcnt.as<int>(), nullptr, nullptr, nullptr, nullptr);
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
-  long long vm[2];  // visits, slice-list words
+  // backward visits (transposed lists), counted now so that one read returns
+  // both directions' totals
+  DevBuf bcnt(st), boff(st), bvis(st), bmcnt(st), bmoff(st);
+  FFA_CUDA(bcnt.alloc(sizeof(int) * n_kt));
+  FFA_CUDA(boff.alloc(sizeof(int) * n_kt));
+  FFA_CUDA(bmcnt.alloc(sizeof(int) * n_kt));
+  FFA_CUDA(bmoff.alloc(sizeof(int) * n_kt));
+  k_visit_warp<false, true><<<grid_for(n_kt, kFillWarps), 32 * kFillWarps, 0, st>>>(
+      p->slices, klist.as<int>(), kloff.as<int>(), klcnt.as<int>(), n_kt, bcnt.as<int>(),
+      bmcnt.as<int>(), nullptr, nullptr, nullptr, nullptr);
+  note_launches(1);
+  FFA_CUDA(cudaGetLastError());
+  long long vm[4];  // forward visits, slice-list words; backward visits, slice-list words
   if ((rc = scan_launch(vcnt.as<int>(), n_qt, voff.as<int>(), dtot, st))) return rc;
   if ((rc = scan_launch(fmcnt.as<int>(), n_qt, fmoff.as<int>(), dtot + 1, st))) return rc;
+  if ((rc = scan_launch(bcnt.as<int>(), n_kt, boff.as<int>(), dtot + 2, st))) return rc;
+  if ((rc = scan_launch(bmcnt.as<int>(), n_kt, bmoff.as<int>(), dtot + 3, st))) return rc;
   if ((rc = read_to_host(vm, dtot, sizeof vm, st))) return rc;
   tot = vm[0];
   if (tot > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
@@ -1496,6 +1522,34 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
       voff.as<int>(), fmoff.as<int>(), visits.as<int2>(), p->fwd_masks);
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
+  if (vm[2] > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
+  FFA_CUDA(bvis.alloc(sizeof(int2) * (size_t)vm[2]));
+  const long long bmtot = vm[3];
+  if (bmtot > (1LL << 29)) return FFA_ERR_UNSUPPORTED;
+  p->n_bwd_masks = bmtot;
+  FFA_CUDA(cudaMallocAsync(&p->bwd_masks, sizeof(int) * (size_t)std::max(1LL, bmtot), st));
+  k_visit_warp<false, false><<<grid_for(n_kt, kFillWarps), 32 * kFillWarps, 0, st>>>(
+      p->slices, klist.as<int>(), kloff.as<int>(), klcnt.as<int>(), n_kt, nullptr, nullptr,
+      boff.as<int>(), bmoff.as<int>(), bvis.as<int2>(), p->bwd_masks);
+  note_launches(1);
+  FFA_CUDA(cudaGetLastError());
+  // gathered k-tiles (full slices, 8-row aligned query ranges): their step
+  // counts replace the visit counts; scanned with the forward's below
+  DevBuf bgcnt(st), bgoff(st), bscnt(st), bsoff(st);
+  FFA_CUDA(bgcnt.alloc(sizeof(int) * n_kt));
+  FFA_CUDA(bgoff.alloc(sizeof(int) * n_kt));
+  FFA_CUDA(bscnt.alloc(sizeof(int) * n_kt));
+  FFA_CUDA(bsoff.alloc(sizeof(int) * n_kt));
+  if (p->Tq <= kGatherMaxTk && n_kt > 0) {
+    k_bgather_count<<<n_kt, kGatherThreads, 0, st>>>(p->slices, klist.as<int>(), kloff.as<int>(),
+                                                     klcnt.as<int>(), p->Tq, bcnt.as<int>(),
+                                                     bgcnt.as<int>(), bscnt.as<int>());
+    note_launches(1);
+    FFA_CUDA(cudaGetLastError());
+  } else {
+    FFA_CUDA(cudaMemsetAsync(bgcnt.p, 0, sizeof(int) * n_kt, st));
+    FFA_CUDA(cudaMemcpyAsync(bscnt.p, bcnt.p, sizeof(int) * n_kt, cudaMemcpyDeviceToDevice, st));
+  }
   // forward units -> steps
   int pair_mode = g >= 2 ? 0 : 1;
   int n_units = pair_mode == 0 ? n_qt : (n_qt + 1) / 2;
@@ -1537,17 +1591,26 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   DevBuf slab_steps(st), slab_off(st), slab_cost(st);
   if (try_stack) {
     FFA_CUDA(slab_steps.alloc(sizeof(int) * n_slabs));
-    FFA_CUDA(cudaMemsetAsync(dtot + 2, 0, 2 * sizeof(long long), st));
+  }
+  // one read: forward steps and gathered records, slab steps and ineligible
+  // slabs, backward steps and gathered records, units and slabs with steps
+  FFA_CUDA(cudaMemsetAsync(dtot + 4, 0, 8 * sizeof(long long), st));
+  if (try_stack) {
     k_slab_count<<<n_slabs, kGatherThreads, 0, st>>>(p->slices, qlist.as<int>(), qloff.as<int>(),
                                                      qlcnt.as<int>(), n_qt, p->Tk,
-                                                     slab_steps.as<int>(), dtot + 2);
+                                                     slab_steps.as<int>(), dtot + 6);
     note_launches(1);
     FFA_CUDA(cudaGetLastError());
   }
-  long long sg[4] = {0, 0, 0, 1};  // steps, gathered records; slab steps, ineligible slabs
-  if ((rc = scan_launch(scnt.as<int>(), n_units, soff.as<int>(), dtot, st))) return rc;
-  if ((rc = scan_launch(gcnt.as<int>(), n_units, goff.as<int>(), dtot + 1, st))) return rc;
-  if ((rc = read_to_host(sg, dtot, (try_stack ? 4 : 2) * sizeof(long long), st))) return rc;
+  long long sg[8];
+  if ((rc = scan_launch(scnt.as<int>(), n_units, soff.as<int>(), dtot + 4, st, dtot + 10)))
+    return rc;
+  if ((rc = scan_launch(gcnt.as<int>(), n_units, goff.as<int>(), dtot + 5, st))) return rc;
+  if ((rc = scan_launch(bscnt.as<int>(), n_kt, bsoff.as<int>(), dtot + 8, st))) return rc;
+  if ((rc = scan_launch(bgcnt.as<int>(), n_kt, bgoff.as<int>(), dtot + 9, st))) return rc;
+  if ((rc = read_to_host(sg, dtot + 4, sizeof sg, st))) return rc;
+  const long long bs[2] = {sg[4], sg[5]};  // backward steps, gathered records
+  long long nz_units = sg[6];             // forward units with steps
   const bool stacked = try_stack && sg[3] == 0 && sg[2] > 0 &&
                        10LL * ((g + 3) / 4) * sg[2] <= 9LL * (g / 2) * sg[0];
   int* u_scnt = scnt.as<int>();
@@ -1566,6 +1629,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
     u_soff = u_goff = slab_off.as<int>();
     u_cost = slab_cost.as<int>();
     sg[0] = sg[1] = sg[2];
+    nz_units = sg[7];
     p->stacked = 1;
   }
   tot = sg[0];
@@ -1603,24 +1667,19 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   const long long n_items = pair_mode != 1 ? (long long)n_units * p->Hkv * pairs
                                            : (long long)n_units * p->Hq;
   if (n_items > 0x7fffffffLL / kFiWords) return FFA_ERR_UNSUPPORTED;
-  DevBuf items(st), live(st);
+  DevBuf items(st);
   FFA_CUDA(items.alloc(sizeof(int) * kFiWords * (size_t)n_items));
-  FFA_CUDA(live.alloc(sizeof(int)));
-  FFA_CUDA(cudaMemsetAsync(live.p, 0, sizeof(int), st));
   k_fwd_items<<<grid_for(n_items, 128), 128, 0, st>>>((int)n_items, pair_mode, g, p->Hkv, p->Hq,
                                                       pairs, n_qt, u_soff, u_scnt, u_cost,
-                                                      items.as<int>(), live.as<int>());
+                                                      items.as<int>());
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
-  int hlive = 0;
-  {
-    const ffa_status_t rc_live = read_to_host(&hlive, live.p, sizeof(int), st);
-    if (rc_live != FFA_OK) return rc_live;
-  }
+  // items with steps: every item of a unit with steps
+  const long long hlive = nz_units * (n_units > 0 ? n_items / n_units : 0);
   const int threshold = split_below == 0 ? 2 * p->num_sms : split_below;
   long long final_items = n_items;
   if (split_below >= 0 && hlive > 0 && hlive < threshold && !stacked) {
-    const int nsplit = std::min(16, (threshold + hlive - 1) / hlive);
+    const int nsplit = (int)std::min<long long>(16, (threshold + hlive - 1) / hlive);
     DevBuf chunks(st), coff(st), slots(st), sloff(st), groups(st), goff(st), nitems(st),
         merges(st);
     const size_t nb = sizeof(int) * (size_t)n_items;
@@ -1685,53 +1744,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
     FFA_CUDA(cudaGetLastError());
   }
 
-  // backward
-  DevBuf bcnt(st), boff(st), bvis(st), bmcnt(st), bmoff(st);
-  FFA_CUDA(bcnt.alloc(sizeof(int) * n_kt));
-  FFA_CUDA(boff.alloc(sizeof(int) * n_kt));
-  FFA_CUDA(bmcnt.alloc(sizeof(int) * n_kt));
-  FFA_CUDA(bmoff.alloc(sizeof(int) * n_kt));
-  k_visit_warp<false, true><<<grid_for(n_kt, kFillWarps), 32 * kFillWarps, 0, st>>>(
-      p->slices, klist.as<int>(), kloff.as<int>(), klcnt.as<int>(), n_kt, bcnt.as<int>(),
-      bmcnt.as<int>(), nullptr, nullptr, nullptr, nullptr);
-  note_launches(1);
-  FFA_CUDA(cudaGetLastError());
-  long long bm[2];  // visits, slice-list words
-  if ((rc = scan_launch(bcnt.as<int>(), n_kt, boff.as<int>(), dtot, st))) return rc;
-  if ((rc = scan_launch(bmcnt.as<int>(), n_kt, bmoff.as<int>(), dtot + 1, st))) return rc;
-  if ((rc = read_to_host(bm, dtot, sizeof bm, st))) return rc;
-  tot = bm[0];
-  if (tot > 0x7fffffffLL) return FFA_ERR_UNSUPPORTED;
-  FFA_CUDA(bvis.alloc(sizeof(int2) * (size_t)tot));
-  const long long bmtot = bm[1];
-  if (bmtot > (1LL << 29)) return FFA_ERR_UNSUPPORTED;
-  p->n_bwd_masks = bmtot;
-  FFA_CUDA(cudaMallocAsync(&p->bwd_masks, sizeof(int) * (size_t)std::max(1LL, bmtot), st));
-  k_visit_warp<false, false><<<grid_for(n_kt, kFillWarps), 32 * kFillWarps, 0, st>>>(
-      p->slices, klist.as<int>(), kloff.as<int>(), klcnt.as<int>(), n_kt, nullptr, nullptr,
-      boff.as<int>(), bmoff.as<int>(), bvis.as<int2>(), p->bwd_masks);
-  note_launches(1);
-  // gathered k-tiles (full slices, 8-row aligned query ranges): their step
-  // counts replace the visit counts before the step offsets are scanned
-  DevBuf bgcnt(st), bgoff(st), bscnt(st), bsoff(st);
-  FFA_CUDA(bgcnt.alloc(sizeof(int) * n_kt));
-  FFA_CUDA(bgoff.alloc(sizeof(int) * n_kt));
-  FFA_CUDA(bscnt.alloc(sizeof(int) * n_kt));
-  FFA_CUDA(bsoff.alloc(sizeof(int) * n_kt));
-  if (p->Tq <= kGatherMaxTk && n_kt > 0) {
-    k_bgather_count<<<n_kt, kGatherThreads, 0, st>>>(p->slices, klist.as<int>(), kloff.as<int>(),
-                                                     klcnt.as<int>(), p->Tq, bcnt.as<int>(),
-                                                     bgcnt.as<int>(), bscnt.as<int>());
-    note_launches(1);
-    FFA_CUDA(cudaGetLastError());
-  } else {
-    FFA_CUDA(cudaMemsetAsync(bgcnt.p, 0, sizeof(int) * n_kt, st));
-    FFA_CUDA(cudaMemcpyAsync(bscnt.p, bcnt.p, sizeof(int) * n_kt, cudaMemcpyDeviceToDevice, st));
-  }
-  long long bs[2];  // steps, gathered records
-  if ((rc = scan_launch(bscnt.as<int>(), n_kt, bsoff.as<int>(), dtot, st))) return rc;
-  if ((rc = scan_launch(bgcnt.as<int>(), n_kt, bgoff.as<int>(), dtot + 1, st))) return rc;
-  if ((rc = read_to_host(bs, dtot, sizeof bs, st))) return rc;
+  // backward (visits and step counts were made with the forward's)
   if (bs[0] > 0x7fffffffLL || bs[1] > (1LL << 24)) return FFA_ERR_UNSUPPORTED;
   p->n_bwd_steps = bs[0];
   p->n_bgathers = bs[1];
