@@ -1249,9 +1249,10 @@ __global__ void __launch_bounds__(1024)
 struct DevBuf {
   void* p = nullptr;
   cudaStream_t st = nullptr;
+  bool own = true;  // false: a view into another buffer (see Arena)
   explicit DevBuf(cudaStream_t s = nullptr) : st(s) {}
   ~DevBuf() {
-    if (p) cudaFreeAsync(p, st);
+    if (p && own) cudaFreeAsync(p, st);
   }
   template <class T>
   T* as() {
@@ -1268,6 +1269,45 @@ struct DevBuf {
 };
 
 inline int grid_for(long long n, int block) { return (int)std::max(1LL, (n + block - 1) / block); }
+
+// Dynamic shared-memory limits of the planner's kernels, raised once per
+// kernel and device (a bit per device in one word per kernel).
+enum AttrSlot : int { kAttrSortGlobal, kAttrSort2, kAttrSort4, kAttrSort8, kAttrSort16,
+                      kAttrGatherFill, kAttrBGatherFill, kAttrSlots };
+std::atomic<unsigned long long> g_attr_done[kAttrSlots];
+
+cudaError_t smem_limit_once(int slot, const void* func, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (g_attr_done[slot].load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) g_attr_done[slot].fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+// The planner's per-tile and per-unit int arrays, carved from one allocation
+// (each a 128-byte aligned run) instead of one allocation apiece: the host
+// calls between the planner's reads are what the GPU waits for.
+struct Arena {
+  DevBuf buf;
+  size_t cap = 0, used = 0;  // in ints
+  explicit Arena(cudaStream_t s) : buf(s) {}
+  static size_t run(long long n) { return (size_t)((std::max(1LL, n) + 31) / 32 * 32); }
+  cudaError_t reserve(size_t ints) {
+    cap = ints;
+    return buf.alloc(sizeof(int) * ints);
+  }
+  bool take(DevBuf& d, long long n) {  // d views n ints
+    const size_t r = run(n);
+    if (used + r > cap) return false;
+    d.p = buf.as<int>() + used;
+    d.own = false;
+    used += r;
+    return true;
+  }
+};
 
 #define FFA_CUDA(x)                                      \
   do {                                                   \
@@ -1363,8 +1403,7 @@ ffa_status_t sort_items(const int* items, int words, int cost_word, int head_wor
     const int sm = (int)(sizeof(unsigned long long) * (size_t)n2);
 #define FFA_SORT_BLOCKED(E)                                                                    \
   do {                                                                                         \
-    FFA_CUDA(cudaFuncSetAttribute(k_sort_order_blocked<E>,                                     \
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, sm));           \
+    FFA_CUDA(smem_limit_once(kAttrSort##E, (const void*)k_sort_order_blocked<E>, sm));          \
     k_sort_order_blocked<E><<<1, 1024, sm, st>>>(items, words, cost_word, n, order, head_word, \
                                                  head_div);                                    \
   } while (0)
@@ -1380,8 +1419,8 @@ ffa_status_t sort_items(const int* items, int words, int cost_word, int head_wor
   DevBuf scratch(st);
   if (n2 > kSortSmemKeys) FFA_CUDA(scratch.alloc(sizeof(unsigned long long) * (size_t)n2));
   const size_t smem = n2 <= kSortSmemKeys ? sizeof(unsigned long long) * (size_t)n2 : 0;
-  FFA_CUDA(cudaFuncSetAttribute(k_sort_order, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)(sizeof(unsigned long long) * kSortSmemKeys)));
+  FFA_CUDA(smem_limit_once(kAttrSortGlobal, (const void*)k_sort_order,
+                           (int)(sizeof(unsigned long long) * kSortSmemKeys)));
   k_sort_order<<<1, 1024, smem, st>>>(items, words, cost_word, n, n2,
                                       scratch.as<unsigned long long>(), order, head_word, head_div);
   note_launches(1);
@@ -1432,11 +1471,21 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   const int n_qt = p->n_qt, n_kt = p->n_kt, g = p->Hq / p->Hkv;
   long long tot = 0;
   ffa_status_t rc = FFA_OK;
+  // per-tile / per-unit arrays: 12 over q-tiles (lists, visits, units,
+  // costs), 10 over k-tiles, 4 over 64-row slabs
+  const long long n_slabs_max = ((long long)p->Tq + kSlabRows - 1) / kSlabRows;
+  Arena arena(st);
+  FFA_CUDA(arena.reserve(12 * Arena::run(n_qt) + 10 * Arena::run(n_kt) +
+                         2 * Arena::run(n_slabs_max) + 2 * Arena::run(2 * n_slabs_max)));
+#define FFA_TAKE(d, n) \
+  do {                 \
+    if (!arena.take(d, n)) return FFA_ERR_CUDA; \
+  } while (0)
   DevBuf qlcnt(st), qloff(st), qlist(st), klcnt(st), kloff(st), klist(st);
-  FFA_CUDA(qlcnt.alloc(sizeof(int) * n_qt));
-  FFA_CUDA(qloff.alloc(sizeof(int) * n_qt));
-  FFA_CUDA(klcnt.alloc(sizeof(int) * n_kt));
-  FFA_CUDA(kloff.alloc(sizeof(int) * n_kt));
+  FFA_TAKE(qlcnt, n_qt);
+  FFA_TAKE(qloff, n_qt);
+  FFA_TAKE(klcnt, n_kt);
+  FFA_TAKE(kloff, n_kt);
   if (n_qt > 0) {
     k_tile_slices<true><<<n_qt, kListThreads, 0, st>>>(p->slices, S, nullptr, qlcnt.as<int>(),
                                                        nullptr);
@@ -1483,10 +1532,10 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
 
   // forward visits
   DevBuf vcnt(st), voff(st), visits(st), fmcnt(st), fmoff(st);
-  FFA_CUDA(vcnt.alloc(sizeof(int) * n_qt));
-  FFA_CUDA(voff.alloc(sizeof(int) * n_qt));
-  FFA_CUDA(fmcnt.alloc(sizeof(int) * n_qt));
-  FFA_CUDA(fmoff.alloc(sizeof(int) * n_qt));
+  FFA_TAKE(vcnt, n_qt);
+  FFA_TAKE(voff, n_qt);
+  FFA_TAKE(fmcnt, n_qt);
+  FFA_TAKE(fmoff, n_qt);
   k_visit_warp<true, true><<<grid_for(n_qt, kFillWarps), 32 * kFillWarps, 0, st>>>(
       p->slices, qlist.as<int>(), qloff.as<int>(), qlcnt.as<int>(), n_qt, vcnt.as<int>(),
       fmcnt.as<int>(), nullptr, nullptr, nullptr, nullptr);
@@ -1495,10 +1544,10 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   // backward visits (transposed lists), counted now so that one read returns
   // both directions' totals
   DevBuf bcnt(st), boff(st), bvis(st), bmcnt(st), bmoff(st);
-  FFA_CUDA(bcnt.alloc(sizeof(int) * n_kt));
-  FFA_CUDA(boff.alloc(sizeof(int) * n_kt));
-  FFA_CUDA(bmcnt.alloc(sizeof(int) * n_kt));
-  FFA_CUDA(bmoff.alloc(sizeof(int) * n_kt));
+  FFA_TAKE(bcnt, n_kt);
+  FFA_TAKE(boff, n_kt);
+  FFA_TAKE(bmcnt, n_kt);
+  FFA_TAKE(bmoff, n_kt);
   k_visit_warp<false, true><<<grid_for(n_kt, kFillWarps), 32 * kFillWarps, 0, st>>>(
       p->slices, klist.as<int>(), kloff.as<int>(), klcnt.as<int>(), n_kt, bcnt.as<int>(),
       bmcnt.as<int>(), nullptr, nullptr, nullptr, nullptr);
@@ -1536,10 +1585,10 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   // gathered k-tiles (full slices, 8-row aligned query ranges): their step
   // counts replace the visit counts; scanned with the forward's below
   DevBuf bgcnt(st), bgoff(st), bscnt(st), bsoff(st);
-  FFA_CUDA(bgcnt.alloc(sizeof(int) * n_kt));
-  FFA_CUDA(bgoff.alloc(sizeof(int) * n_kt));
-  FFA_CUDA(bscnt.alloc(sizeof(int) * n_kt));
-  FFA_CUDA(bsoff.alloc(sizeof(int) * n_kt));
+  FFA_TAKE(bgcnt, n_kt);
+  FFA_TAKE(bgoff, n_kt);
+  FFA_TAKE(bscnt, n_kt);
+  FFA_TAKE(bsoff, n_kt);
   if (p->Tq <= kGatherMaxTk && n_kt > 0) {
     k_bgather_count<<<n_kt, kGatherThreads, 0, st>>>(p->slices, klist.as<int>(), kloff.as<int>(),
                                                      klcnt.as<int>(), p->Tq, bcnt.as<int>(),
@@ -1554,9 +1603,9 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   int pair_mode = g >= 2 ? 0 : 1;
   int n_units = pair_mode == 0 ? n_qt : (n_qt + 1) / 2;
   DevBuf scnt(st), soff(st), cost_half(st), steps(st);
-  FFA_CUDA(scnt.alloc(sizeof(int) * n_units));
-  FFA_CUDA(soff.alloc(sizeof(int) * n_units));
-  FFA_CUDA(cost_half.alloc(sizeof(int) * 2 * n_units));
+  FFA_TAKE(scnt, n_units);
+  FFA_TAKE(soff, n_units);
+  FFA_TAKE(cost_half, 2LL * n_units);
   const bool unit_warps = n_kt <= kUnitWarpTiles;
   if (unit_warps)
     k_fwd_unit_count_w<<<grid_for(n_units, kUnitWarps), 32 * kUnitWarps, 0, st>>>(
@@ -1572,8 +1621,8 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   // gathered units (full, 8-key aligned slices): their step counts replace
   // the regular ones before the step offsets are scanned
   DevBuf gcnt(st), goff(st);
-  FFA_CUDA(gcnt.alloc(sizeof(int) * n_units));
-  FFA_CUDA(goff.alloc(sizeof(int) * n_units));
+  FFA_TAKE(gcnt, n_units);
+  FFA_TAKE(goff, n_units);
   FFA_CUDA(cudaMemsetAsync(gcnt.p, 0, sizeof(int) * n_units, st));
   if (p->Tk <= kGatherMaxTk && n_units > 0) {
     k_gather_count<<<n_units, kGatherThreads, 0, st>>>(p->slices, qlist.as<int>(), qloff.as<int>(),
@@ -1590,7 +1639,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   const int n_slabs = (p->Tq + kSlabRows - 1) / kSlabRows;
   DevBuf slab_steps(st), slab_off(st), slab_cost(st);
   if (try_stack) {
-    FFA_CUDA(slab_steps.alloc(sizeof(int) * n_slabs));
+    FFA_TAKE(slab_steps, n_slabs);
   }
   // one read: forward steps and gathered records, slab steps and ineligible
   // slabs, backward steps and gathered records, units and slabs with steps
@@ -1621,8 +1670,8 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   if (stacked) {  // every step gathered: record r is step r, offsets shared
     pair_mode = 2;
     n_units = n_slabs;
-    FFA_CUDA(slab_off.alloc(sizeof(int) * n_slabs));
-    FFA_CUDA(slab_cost.alloc(sizeof(int) * 2 * n_slabs));
+    FFA_TAKE(slab_off, n_slabs);
+    FFA_TAKE(slab_cost, 2LL * n_slabs);
     FFA_CUDA(cudaMemsetAsync(slab_cost.p, 0, sizeof(int) * 2 * n_slabs, st));
     if ((rc = scan_launch(slab_steps.as<int>(), n_slabs, slab_off.as<int>(), dtot, st))) return rc;
     u_scnt = u_gcnt = slab_steps.as<int>();
@@ -1653,8 +1702,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
     FFA_CUDA(cudaGetLastError());
   }
   if (sg[1] > 0) {
-    FFA_CUDA(cudaFuncSetAttribute(k_gather_fill, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)kGatherFillSmem));
+    FFA_CUDA(smem_limit_once(kAttrGatherFill, (const void*)k_gather_fill, (int)kGatherFillSmem));
     k_gather_fill<<<n_units, kGatherThreads, kGatherFillSmem, st>>>(
         p->slices, qlist.as<int>(), qloff.as<int>(), qlcnt.as<int>(), n_qt, pair_mode, p->Tk,
         u_gcnt, u_goff, u_soff, steps.as<int4>(), p->gathers, u_cost);
@@ -1762,8 +1810,8 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   note_launches(1);
   FFA_CUDA(cudaGetLastError());
   if (bs[1] > 0) {
-    FFA_CUDA(cudaFuncSetAttribute(k_bgather_fill, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)kBGatherFillSmem));
+    FFA_CUDA(smem_limit_once(kAttrBGatherFill, (const void*)k_bgather_fill,
+                             (int)kBGatherFillSmem));
     k_bgather_fill<<<n_kt, kGatherThreads, kBGatherFillSmem, st>>>(
         p->slices, klist.as<int>(), kloff.as<int>(), klcnt.as<int>(), p->Tq, bgcnt.as<int>(),
         bgoff.as<int>(), bsoff.as<int>(), p->bwd_steps, p->bgathers);
@@ -1777,6 +1825,7 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   FFA_CUDA(cudaStreamSynchronize(st));
   return FFA_OK;
 }
+#undef FFA_TAKE
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
