@@ -652,7 +652,8 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
 // ============================================================================
 // dQ pass
 // Work units: the halves of the planner's unsplit forward items, i.e. one
-// (q-tile, query head) with its visits in k-tile order.
+// (q-tile, query head) with its visits in k-tile order (in head-stacked
+// plans a 64-row slab of two query heads, tile rows 0-63 and 64-127).
 // Warp roles (384 threads): warps 0-7 dS warps in two warpgroups (thread =
 // query row = TMEM lane; warpgroup w owns key columns [64w, 64w+64)) and the
 // dQ epilogue, warp 8 TMA producer, warp 9 MMA issuer, warp 10 V loader for

@@ -3,7 +3,8 @@
 //
 // One persistent CTA per SM walks its share of the planner's work items.  An
 // item holds two 128-row halves (two query heads of one kv head, or two
-// consecutive q-tiles of one head) that share every K/V tile load.
+// consecutive q-tiles of one head; in head-stacked plans each half is one
+// 64-row slab of two query heads) that share every K/V tile load.
 //
 // Warp roles (384 threads, three warpgroups):
 //   warps 0-3  softmax for half 0 (thread = query row = TMEM lane)
