@@ -138,11 +138,18 @@ class ClockSampler:
 
 
 def kernel_source_hash() -> str:
+    """Hash of the CUDA sources with comments and blank lines removed, so
+    that a capture stays matched to its kernels across comment edits."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "flexible_mask_attention_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(f.encode() + code.encode())
     return h.hexdigest()[:16]
 
 
