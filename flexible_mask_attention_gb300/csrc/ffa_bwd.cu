@@ -1075,10 +1075,11 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           if (j + 1 < se) st_next = P.steps[j + 1];  // prefetch the next step descriptor
           const int info = half_info(st, h);
           if (info < 0) continue;
-          // A gathered step's column mask (every step of such a unit is one)
-          // is read while the scores are awaited; a PARTIAL tile's after.
+          // A gathered step's column mask (every step of such a unit is one;
+          // none for a step whose rows all see all its keys) is read while
+          // the scores are awaited; a PARTIAL tile's after.
           uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
-          if (kGather && st.w > 0)
+          if (kGather && st.w > 0 && (info & 1))
             gather_mask(P.gathers + (size_t)(st.w - 1) * kGatherWords, h, t, P.Tk, vb);
           const bool w = mbar_wait(bar(C::kBSdFull), sd_cnt & 1, ctl, 1000);
           if (!(ok = __all_sync(0xffffffffu, w))) break;

@@ -980,10 +980,16 @@ __global__ void __launch_bounds__(kGatherThreads)
   }
   for (int j = threadIdx.x; j < n_steps; j += blockDim.x) {
     int info[2];
+    bool slots_used = true;
+    for (int k = 0; k < kGatherSlots; ++k) slots_used &= start[j * kGatherSlots + k] >= 0;
     for (int h = 0; h < 2; ++h) {
-      unsigned any = 0u;
-      for (int k = 0; k < kGatherSlots * 4; ++k) any |= rmask[(h * n + j * kGatherSlots) * 4 + k];
-      info[h] = any ? 1 : -1;
+      unsigned any = 0u, all = ~0u;
+      for (int k = 0; k < kGatherSlots * 4; ++k) {
+        any |= rmask[(h * n + j * kGatherSlots) * 4 + k];
+        all &= rmask[(h * n + j * kGatherSlots) * 4 + k];
+      }
+      // 0: every slot holds keys and every row sees them all (no mask)
+      info[h] = !any ? -1 : (slots_used && all == ~0u ? 0 : 1);
       if (any) atomicAdd(&cost[h], kPartialCost);
     }
     steps[s0 + j] = make_int4(0, info[0], info[1], r0 + j + 1);

@@ -125,8 +125,9 @@ ffa_status_t ffa_plan_info(ffa_plan_t plan, ffa_plan_info_t* info);
  *   step (0, info0, info1, r + 1) computes 16 blocks of 8 keys packed into
  *   one K/V tile; record r holds the 16 block start keys (-8: unused slot),
  *   then for each half 16 x 4 words of row bits (bit i of word w: row
- *   32 w + i of the half's q-tile sees that block); info_h is 1 when half h
- *   has a row bit set, else -1.
+ *   32 w + i of the half's q-tile sees that block); info_h is 0 when all 16
+ *   slots hold keys and every row of half h sees them all (no mask), else 1
+ *   when half h has a row bit set, else -1.
  *   Gathered backward steps, the transpose (a k-tile whose slices are all FULL
  *   with query ranges aligned to 8 rows, when that takes at most 9/10 of its
  *   visits): step (0, 1, 0, r + 1) computes 16 blocks of 8 query rows packed

@@ -29,8 +29,10 @@ the work-list specification of the planner:
     its slices covers, ascending, 16 to a step; a step is (0, info0, info1,
     r + 1) with record r = 16 block starts (key index, -8 for an unused
     slot) then, per half, 16 x 4 words of row bits (bit r of word w: row
-    32w + r of the half's q-tile sees the slot's keys); info_h = 1 when the
-    half has a row bit set, else -1; cost 5 per busy half.  At most 2048
+    32w + r of the half's q-tile sees the slot's keys); info_h = 0 when all
+    16 slots hold keys and every row bit of the half is set (the step needs
+    no mask), else 1 when the half has a row bit set, else -1; cost 5 per
+    busy half.  At most 2048
     blocks per unit;
   * gathered backward units, the transpose: a k-tile whose slices are all
     FULL with 8-aligned query ranges (the end may be Tq), Tq <= 2^19, lists
@@ -373,10 +375,19 @@ def gather_units(total_q, total_k, q_ranges, k_ranges, mask_types, pair_mode, fv
                                     rr = r - TILE * qt
                                     words[slot, rr >> 5] |= np.uint32(1 << (rr & 31))
                 rec += [int(w) for w in words.view(np.int32).reshape(-1)]
-                infos.append(1 if words.any() else -1)
+                infos.append(_half_info(words, rec[:GATHER_SLOTS]))
             res.append((rec, (infos[0], infos[1])))
         out[u] = res
     return out
+
+
+def _half_info(words, starts):
+    """Step info of a gathered half: -1 idle, 0 when all 16 slots hold keys
+    and every row of the half sees all of them (no mask), else 1."""
+    if not words.any():
+        return -1
+    full = all(y >= 0 for y in starts[:GATHER_SLOTS]) and bool((words == 0xFFFFFFFF).all())
+    return 0 if full else 1
 
 
 def gather_slabs(total_q, total_k, q_ranges, k_ranges, mask_types):
@@ -416,7 +427,7 @@ def gather_slabs(total_q, total_k, q_ranges, k_ranges, mask_types):
                             for rr in (r - SLAB * u, r - SLAB * u + SLAB):
                                 words[slot, rr >> 5] |= np.uint32(1 << (rr & 31))
             half = [int(w) for w in words.view(np.int32).reshape(-1)]
-            info = 1 if words.any() else -1
+            info = _half_info(words, rec)
             res.append((rec + half + half, (info, info)))
         if res:
             out[u] = res
