@@ -99,6 +99,14 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.skip = 0  # samples taken before the timed region
+
+    def _lines(self) -> int:
+        try:
+            with open(self.path) as fh:
+                return sum(1 for _ in fh)
+        except OSError:
+            return 0
 
     def start(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -106,10 +114,18 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        # nvidia-smi takes a while to start: wait for its first sample, then
+        # count only the samples taken from here on (the timed region)
+        import time
+        t0 = time.monotonic()
+        while self._lines() == 0 and time.monotonic() - t0 < 3.0 and self.proc.poll() is None:
+            time.sleep(0.01)
+        self.skip = self._lines()
 
     def stop(self):
         if self.proc is None:
@@ -120,7 +136,10 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         rows = []
-        for line in open(self.path):
+        lines = open(self.path).read().splitlines()
+        if len(lines) > self.skip:  # else keep the last sample before the region
+            lines = lines[self.skip:]
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
