@@ -702,7 +702,8 @@ struct DqParams {
   const int* masks;  // slice lists of multi-slice visits
   const int* gathers;  // gathered step records
   int Tq, Tk, Hq, g, qpad;
-  int stack;  // head-stacked units: a half is a 64-row slab of two heads
+  int stack;  // head-stacked units: slab rows R (a half: R rows of 128 / R heads), or 0
+  int alternate;  // an item's halves are the same rows, taking its steps in turn
   float scale, scale_log2;
   const float* nlse2;
   const float* ndelta;
@@ -748,6 +749,12 @@ __device__ __forceinline__ bool half_active(const int* it, int h) {
 }
 
 __device__ __forceinline__ int half_info(const int4& st, int h) { return h == 0 ? st.y : st.z; }
+
+// The dQ pass's view of a step: items whose two halves are the same rows
+// taking the steps in turn (alternate) are walked as half 0 over all steps.
+__device__ __forceinline__ int dq_info(const int4& st, int h, bool alternate) {
+  return alternate ? (h == 0 ? max(st.y, st.z) : -1) : half_info(st, h);
+}
 
 // kGather: the plan has gathered steps (instantiated apart, as in the forward).
 template <int D, bool kCap, bool kGather>
@@ -882,14 +889,15 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
             ok = mbar_wait(bar(C::kBQEmpty), (q_cnt & 1) ^ 1, ctl, 800);
             if (ok) {
               mbar_arrive_expect_tx(bar(C::kBQFull), 2 * C::kTileBytes);
-              if (kGather && P.stack) {  // heads head, head + 1 of the 64-row slab qt
-                for (int j = 0; j < 2; ++j)
+              if (kGather && P.stack) {  // heads head, head + 1, ... of the R-row slab qt
+                const int R = P.stack;
+                for (int j = 0; j < 128 / R; ++j)
                   for (int c = 0; c < C::kChunks; ++c) {
-                    const uint32_t o = c * 16384 + j * (kSlabRows * 128);
+                    const uint32_t o = c * 16384 + j * (R * 128);
                     tma_load_2d(sbase + C::kQOff + o, &tm_q64, bar(C::kBQFull),
-                                (head + j) * D + c * 64, qt * kSlabRows);
+                                (head + j) * D + c * 64, qt * R);
                     tma_load_2d(sbase + C::kDOOff + o, &tm_do64, bar(C::kBQFull),
-                                (head + j) * D + c * 64, qt * kSlabRows);
+                                (head + j) * D + c * 64, qt * R);
                   }
               } else {
                 for (int c = 0; c < C::kChunks; ++c) {
@@ -906,7 +914,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         }
         for (int j = sb; j < se; ++j) {
           const int4 st = P.steps[j];
-          if (half_info(st, h) < 0) continue;
+          if (dq_info(st, h, kGather && P.alternate) < 0) continue;
           // this lane's slot start (read while the ring slots are awaited)
           const int y = kGather && st.w > 0 && lane < kGatherSlots
                             ? P.gathers[(size_t)(st.w - 1) * kGatherWords + lane] : 0;
@@ -1059,12 +1067,12 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       const int* it = P.items + (size_t)idx * kFiWords;
       const int sb = it[kFiStepBeg], se = it[kFiStepEnd];
       for (int h = 0; ok && h < 2; ++h) {
-        if (!half_active(it, h)) continue;
+        if (!half_active(it, h) || (kGather && P.alternate && h == 1)) continue;
         const int qt = it[kFiQt0 + h];
-        // tile row -> query row and head (head-stacked: 64-row slab, two heads)
+        // tile row -> query row and head (head-stacked: R-row slab of 128 / R heads)
         const bool stk = kGather && P.stack;
-        const int row = stk ? qt * kSlabRows + (t & (kSlabRows - 1)) : qt * 128 + t;
-        const int head = it[kFiH0 + h] + (stk ? t / kSlabRows : 0);
+        const int row = stk ? qt * P.stack + (t & (P.stack - 1)) : qt * 128 + t;
+        const int head = it[kFiH0 + h] + (stk ? t / P.stack : 0);
         const float nl = P.nlse2[(size_t)head * P.qpad + row];
         const float nd = P.ndelta[(size_t)head * P.qpad + row];
         const float2 nl2 = make_float2(nl, nl);
@@ -1073,7 +1081,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         for (int j = sb; j < se; ++j) {
           const int4 st = st_next;
           if (j + 1 < se) st_next = P.steps[j + 1];  // prefetch the next step descriptor
-          const int info = half_info(st, h);
+          const int info = dq_info(st, h, kGather && P.alternate);
           if (info < 0) continue;
           // A gathered step's column mask (every step of such a unit is one;
           // none for a step whose rows all see all its keys) is read while
@@ -1294,8 +1302,8 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
       !encode_tile_map(&tv8, v, p->Tk, p->Hkv * D, kGatherKeys) ||
       !encode_tile_map(&tq8, q, p->Tq, p->Hq * D, kGatherKeys) ||
       !encode_tile_map(&tdo8, dout, p->Tq, p->Hq * D, kGatherKeys) ||
-      !encode_tile_map(&tq64, q, p->Tq, p->Hq * D, kSlabRows) ||
-      !encode_tile_map(&tdo64, dout, p->Tq, p->Hq * D, kSlabRows))
+      !encode_tile_map(&tq64, q, p->Tq, p->Hq * D, p->stacked ? p->stacked : kSlabRows) ||
+      !encode_tile_map(&tdo64, dout, p->Tq, p->Hq * D, p->stacked ? p->stacked : kSlabRows))
     return FFA_ERR_INVALID_ARG;
   const float scale_log2 = scale * kLog2e;
   {
@@ -1356,6 +1364,7 @@ ffa_status_t launch_bwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
     P.g = p->Hq / p->Hkv;
     P.qpad = qpad;
     P.stack = p->stacked;
+    P.alternate = p->alternate;
     P.scale = scale;
     P.scale_log2 = scale_log2;
     P.nlse2 = nlse2;

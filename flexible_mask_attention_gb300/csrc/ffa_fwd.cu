@@ -72,9 +72,12 @@ struct FwdCfg {
                        kBSFull = 2 + 4 * kStages, kBPFull = kBSFull + 2, kBOFull = kBPFull + 2,
                        kBOEmpty = kBOFull + 2, kBDrain = kBOEmpty + 2,
                        kBItemFull = kBDrain + 1, kBItemEmpty = kBItemFull + kItemRing,
-                       kNumBars = kBItemEmpty + kItemRing;
+                       kBHandFull = kBItemEmpty + kItemRing, kBHandEmpty = kBHandFull + 1,
+                       kNumBars = kBHandEmpty + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag, queue slots
-  static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + alignment slack
+  // alternating items: half 1's row state (m, l) handed to half 0
+  static constexpr int kHandOff = kMiscOff + 64;
+  static constexpr int kSmemBytes = kHandOff + 128 * 8 + 1024;  // + alignment slack
 };
 
 struct FwdParams {
@@ -87,7 +90,8 @@ struct FwdParams {
   const int* masks;  // slice lists of multi-slice visits
   const int* gathers;  // gathered step records
   int Tq, Tk, Hq, g;
-  int stack;  // head-stacked units: a half is a 64-row slab of two heads
+  int stack;  // head-stacked units: slab rows R (a half: R rows of 128 / R heads), or 0
+  int alternate;  // an item's halves are the same rows, taking its steps in turn
   float scale_log2;
   __nv_bfloat16* out;
   float* lse;
@@ -242,6 +246,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(bar(C::kBOEmpty + h), 128);
     }
     mbar_init(bar(C::kBDrain), 1);
+    mbar_init(bar(C::kBHandFull), 128);   // half 1's threads
+    mbar_init(bar(C::kBHandEmpty), 128);  // half 0's threads
     for (int s = 0; s < kItemRing; ++s) {
       mbar_init(bar(C::kBItemFull + s), 1);
       // MMA thread + softmax threads (+ lane 0 of the V warp)
@@ -326,15 +332,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (ok) {
             mbar_arrive_expect_tx(bar(C::kBQFull), (act1 ? 2 : 1) * C::kTileBytes);
             if (kGather && P.stack) {
-              // a half: the slab's 64 rows of heads h and h + 1, tile rows
-              // 0-63 and 64-127 (8 KB apart in each 128-byte column chunk)
+              // a half: the slab's R rows of heads h, h + 1, ..., tile rows
+              // [R j, R j + R) for head h + j (128 R bytes apart in each
+              // 128-byte column chunk); tm_q64's box is R rows
+              const int R = P.stack;
               for (int hh = 0; hh < (act1 ? 2 : 1); ++hh)
-                for (int j = 0; j < 2; ++j)
+                for (int j = 0; j < 128 / R; ++j)
                   for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_2d(sbase + C::kQOff + hh * C::kTileBytes + c * 16384 +
-                                    j * (kSlabRows * 128),
+                    tma_load_2d(sbase + C::kQOff + hh * C::kTileBytes + c * 16384 + j * (R * 128),
                                 &tm_q64, bar(C::kBQFull), (it[kFiH0 + hh] + j) * D + c * 64,
-                                it[kFiQt0 + hh] * kSlabRows);
+                                it[kFiQt0 + hh] * R);
             } else {
               for (int c = 0; c < C::kChunks; ++c)
                 tma_load_2d(sbase + C::kQOff + c * 16384, &tm_q, bar(C::kBQFull),
@@ -413,6 +420,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     (acc || kk > 0) ? 1u : 0u);
       };
       uint32_t kv_cnt = 0, q_cnt = 0, p_cnt[2] = {0, 0}, oe_cnt[2] = {0, 0};
+      const bool alt_items = kGather && P.alternate;
       bool ok = true;
       for (int r = 0; ok; ++r) {
         int idx;
@@ -426,6 +434,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_after();
         bool first_pv[2] = {true, true};
         int4 cur = P.steps[sb];
+        int4 nxt = sb + 1 < se ? P.steps[sb + 1] : make_int4(0, -1, -1, 0);
         {
           const int stage = kv_cnt % C::kStages;
           if (!(ok = mbar_wait(bar(C::kBKFull + stage), (kv_cnt / C::kStages) & 1, ctl, 201)))
@@ -448,8 +457,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const int stage_n = (c + 1) % C::kStages;
           const uint32_t ph_n = ((c + 1) / C::kStages) & 1;
           const bool has_next = j + 1 < se;
-          const int4 nxt = has_next ? P.steps[j + 1] : make_int4(0, -1, -1, 0);
+          // step descriptors are read two steps ahead: the load of step j + 2
+          // has a whole step to land
+          const int4 nxt2 = j + 2 < se ? P.steps[j + 2] : make_int4(0, -1, -1, 0);
           bool v_ready = false, k_next_ready = false;
+          if (alt_items && has_next && (nxt.y >= 0 || nxt.z >= 0)) {
+            // halves that take the steps in turn: the next step's S (the other
+            // half's buffer, whose P went to PV a step ago) goes before this
+            // step's PV, so one half's softmax runs while the other's does
+            const int hn = nxt.y >= 0 ? 0 : 1;
+            if (!(ok = mbar_wait(bar(C::kBKFull + stage_n), ph_n, ctl, 215))) break;
+            k_next_ready = true;
+            tc_fence_after();
+            issue_s(hn, stage_n);
+            mma_commit(bar(C::kBSFull + hn));
+          }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int info = h == 0 ? cur.y : (act1 ? cur.z : -1);
@@ -470,7 +492,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               first_pv[h] = false;
             }
             const int ninfo = h == 0 ? nxt.y : (act1 ? nxt.z : -1);
-            if (has_next && ninfo >= 0) {
+            if (!alt_items && has_next && ninfo >= 0) {
               if (!k_next_ready) {
                 if (!(ok = mbar_wait(bar(C::kBKFull + stage_n), ph_n, ctl, 215))) break;
                 k_next_ready = true;
@@ -484,6 +506,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mma_commit(bar(C::kBVEmpty + stage));
           if (has_next) mma_commit(bar(C::kBKEmpty + stage_n));  // S of step j+1 issued
           cur = nxt;
+          nxt = nxt2;
         }
         if (!ok) break;
 #pragma unroll
@@ -505,7 +528,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_addr + h * 128;
     const uint32_t tO = tmem + lane_addr + 256 + h * 128;
-    uint32_t s_cnt = 0, o_cnt = 0;
+    const uint32_t tO1 = tmem + lane_addr + 256 + 128;  // half 1's O (alternating items)
+    float2* hand = reinterpret_cast<float2*>(smem + C::kHandOff);
+    const bool alt = kGather && P.alternate;
+    uint32_t s_cnt = 0, o_cnt = 0, o1_cnt = 0, hand_cnt = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
       int idx = -1;
@@ -516,17 +542,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const bool act1 = it[kFiQt1] >= 0 && it[kFiH1] >= 0;
       if (h == 1 && !act1) continue;
       const int qt = it[kFiQt0 + h], slot = it[kFiSlot];
-      // tile row -> query row and head (head-stacked: 64-row slab, two heads)
+      // tile row -> query row and head (head-stacked: R-row slab of 128 / R heads)
       const bool stk = kGather && P.stack;
-      const int row = stk ? qt * kSlabRows + (row_in & (kSlabRows - 1)) : qt * 128 + row_in;
-      const int head = it[kFiH0 + h] + (stk ? row_in / kSlabRows : 0);
+      const int row = stk ? qt * P.stack + (row_in & (P.stack - 1)) : qt * 128 + row_in;
+      const int head = it[kFiH0 + h] + (stk ? row_in / P.stack : 0);
       float m = -INFINITY, l = 0.f;
-      bool visited = false;
+      bool visited = false, vis1 = false;  // vis1: half 1 had a step (alternating items)
       int4 st_next = sb < se ? P.steps[sb] : make_int4(0, -1, -1, 0);
       for (int j = sb; j < se; ++j) {
         const int4 st = st_next;
         if (j + 1 < se) st_next = P.steps[j + 1];  // prefetch the next step descriptor
         const int info = h == 0 ? st.y : st.z;
+        vis1 |= st.z >= 0;
         if (info < 0) continue;
         // The column mask of a PARTIAL (or gathered) step depends on the plan
         // only: its reads overlap the wait for S.
@@ -615,6 +642,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         visited = true;
       }
       if (!ok) break;
+      // ---- alternating item: half 1 hands its (m, l) to half 0, which merges
+      // the two halves' states by logsumexp and writes the rows
+      float a0 = 1.f, a1 = 0.f;
+      if (alt) {
+        if (h == 1) {
+          const bool w = mbar_wait(bar(C::kBHandEmpty), (hand_cnt & 1) ^ 1, ctl, 320);
+          if (!(ok = __all_sync(0xffffffffu, w))) break;
+          ++hand_cnt;
+          hand[row_in] = make_float2(m, l);
+          mbar_arrive(bar(C::kBHandFull));
+          continue;
+        }
+        const bool w = mbar_wait(bar(C::kBHandFull), hand_cnt & 1, ctl, 321);
+        if (!(ok = __all_sync(0xffffffffu, w))) break;
+        ++hand_cnt;
+        const float2 st1 = hand[row_in];
+        mbar_arrive(bar(C::kBHandEmpty));
+        const float mm = fmaxf(visited ? m : -INFINITY, vis1 ? st1.x : -INFINITY);
+        a0 = visited && mm > -INFINITY ? exp2f(m - mm) : 0.f;
+        a1 = vis1 && mm > -INFINITY ? exp2f(st1.x - mm) : 0.f;
+        l = a0 * l + a1 * st1.y;
+        m = mm;
+      }
       // ---- epilogue: O / l -> out (bf16) or a partial slot (fp32), 32 columns at a time
       const bool nonempty = l > 0.f;
       float inv_l = nonempty ? 1.f / l : 0.f;
@@ -636,18 +686,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ++o_cnt;
         tc_fence_after();
       }
+      const bool read1 = alt && vis1;  // half 0 merges half 1's O
+      if (read1) {
+        const bool w = mbar_wait(bar(C::kBOFull + 1), o1_cnt & 1, ctl, 312);
+        if (!(ok = __all_sync(0xffffffffu, w))) break;
+        ++o1_cnt;
+        tc_fence_after();
+      }
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t u[32];
         if (visited) {
           tmem_ld32(tO + 32 * c, u);
-          if (c == D / 32 - 1) {
-            tc_fence_before();
-            mbar_arrive(bar(C::kBOEmpty + h));
-          }
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) u[i] = 0u;
+        }
+        if (read1) {
+          uint32_t u1[32];
+          tmem_ld32(tO1 + 32 * c, u1);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            u[i] = __float_as_uint(
+                fmaf(a1, __uint_as_float(u1[i]), visited ? a0 * __uint_as_float(u[i]) : 0.f));
+        }
+        if (c == D / 32 - 1) {
+          tc_fence_before();
+          if (visited) mbar_arrive(bar(C::kBOEmpty + h));
+          if (read1) mbar_arrive(bar(C::kBOEmpty + 1));
         }
         if (!store) continue;
         if (slot < 0) {
@@ -749,7 +815,7 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
       !encode_tile_map(&tv, v, p->Tk, p->Hkv * D) ||
       !encode_tile_map(&tk8, k, p->Tk, p->Hkv * D, kGatherKeys) ||
       !encode_tile_map(&tv8, v, p->Tk, p->Hkv * D, kGatherKeys) ||
-      !encode_tile_map(&tq64, q, p->Tq, p->Hq * D, kSlabRows))
+      !encode_tile_map(&tq64, q, p->Tq, p->Hq * D, p->stacked ? p->stacked : kSlabRows))
     return FFA_ERR_INVALID_ARG;
   FwdParams P;
   P.steps = p->fwd_steps;
@@ -765,6 +831,7 @@ ffa_status_t launch_fwd_d(ffa_plan_s* p, const void* q, const void* k, const voi
   P.Hq = p->Hq;
   P.g = p->Hq / p->Hkv;
   P.stack = p->stacked;
+  P.alternate = p->alternate;
   P.scale_log2 = scale * kLog2e;
   P.out = static_cast<__nv_bfloat16*>(out);
   P.lse = lse;

@@ -42,11 +42,11 @@ constexpr int kGatherWords = kGatherSlots + 2 * kGatherSlots * 4;
 constexpr int kBGatherWords = kGatherSlots + kGatherSlots * 4;
 constexpr int kGatherMaxBlocks = 2048;  // 8-key blocks per gathered unit
 constexpr int kGatherMaxTk = 1 << 19;   // key count up to which units may gather
-// Head-stacked forward units (plan.stacked): a unit is a slab of kSlabRows
-// query rows, and a half of an item is that slab for two consecutive query
-// heads h, h + 1 stacked in one 128-row tile (tile row r: query row
-// kSlabRows * slab + r % kSlabRows of head h + r / kSlabRows).  Every step of
-// such a plan is gathered, with the same row bits for r and r + kSlabRows.
+// Head-stacked forward units (plan.stacked = R, 64 or 32): a unit is a slab
+// of R query rows, and a half of an item is that slab for 128 / R
+// consecutive query heads h, h + 1, ... stacked in one 128-row tile (tile row
+// r: query row R * slab + r % R of head h + r / R).  Every step of such a plan
+// is gathered, with the same row bits for r, r + R, ...
 constexpr int kSlabRows = 64;
 
 #ifdef __CUDACC__
@@ -208,7 +208,8 @@ struct ffa_plan_s {
   int* merges = nullptr;
   int64_t n_merges = 0;
   int n_slots = 0;  // partial-result slots (split forward items)
-  int stacked = 0;  // forward units are head-stacked 64-row slabs (kSlabRows)
+  int stacked = 0;  // slab rows of head-stacked forward units (64 or 32), 0: q-tile units
+  int alternate = 0;  // items' halves are the same rows, taking the steps in turn (merged)
   int* fwd_masks = nullptr;  // slice lists of multi-slice forward visits
   int64_t n_fwd_masks = 0;
   int* gathers = nullptr;  // gathered step records [n_gathers][kGatherWords]

@@ -607,19 +607,20 @@ __global__ void __launch_bounds__(32 * kUnitWarps)
   }
 }
 
-__global__ void k_fwd_items(int n_items, int pair_mode, int g, int Hkv, int Hq, int pairs,
+__global__ void k_fwd_items(int n_items, int pair_mode, int m, int alternate, int g, int Hkv,
+                            int Hq, int pairs,
                             int n_qt, const int* __restrict__ soff, const int* __restrict__ scnt,
                             const int* __restrict__ cost_half, int* items) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= n_items) return;
   int u, qt0, qt1, h0, h1;
-  if (pair_mode == 2) {  // `pairs` holds the groups of four heads
+  if (pair_mode == 2) {  // `pairs`: groups of 2m heads, m heads per half
     u = idx / (Hkv * pairs);
     const int rem = idx % (Hkv * pairs);
     const int hk = rem / pairs, p = rem % pairs;
     qt0 = qt1 = u;
-    h0 = hk * g + 4 * p;
-    h1 = (4 * p + 2 < g) ? h0 + 2 : -1;
+    h0 = hk * g + 2 * m * p;
+    h1 = alternate ? h0 : (2 * m * p + m < g) ? h0 + m : -1;
     if (h1 < 0) qt1 = -1;
   } else if (pair_mode == 0) {
     u = idx / (Hkv * pairs);
@@ -728,16 +729,19 @@ __global__ void k_bwd_items(int n_kt, int Hkv, int g, const int2* __restrict__ v
 
 // Visits of each half of the (unsplit) forward items the dQ pass walks: a
 // half skips the steps whose info for it is -1.
+// alternate: the halves of every item are the same rows, taking the steps in
+// turn; the dQ pass walks them as one half over all the steps.
 __global__ void k_dq_counts(const int* __restrict__ items, int n_items,
-                            const int4* __restrict__ steps, int* __restrict__ counts) {
+                            const int4* __restrict__ steps, int alternate,
+                            int* __restrict__ counts) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n_items) return;
   const int* it = items + (size_t)i * kFiWords;
   int n0 = 0, n1 = 0;
   for (int j = it[kFiStepBeg]; j < it[kFiStepEnd]; ++j) {
     const int4 s = steps[j];
-    n0 += s.y >= 0 ? 1 : 0;
-    n1 += s.z >= 0 ? 1 : 0;
+    n0 += (s.y >= 0 || (alternate && s.z >= 0)) ? 1 : 0;
+    n1 += (!alternate && s.z >= 0) ? 1 : 0;
   }
   counts[2 * i] = n0;
   counts[2 * i + 1] = n1;
@@ -759,17 +763,18 @@ struct GatherUnit {
   int p0, p1;  // query rows of the unit: slices outside [p0, p1) are skipped
 };
 
-// pair_mode 0: q-tile u (two heads); 1: q-tiles 2u, 2u+1; 2: the 64-row
-// slab u of q-tile u / 2 (head-stacked units).
-__device__ __forceinline__ GatherUnit gather_unit(int u, int pair_mode, int n_qt) {
+// pair_mode 0: q-tile u (two heads); 1: q-tiles 2u, 2u+1; 2: the slab u of
+// `rows` (64 or 32) query rows (head-stacked units).
+__device__ __forceinline__ GatherUnit gather_unit(int u, int pair_mode, int n_qt,
+                                                  int rows = kSlabRows) {
   GatherUnit g;
   g.p0 = -1;
   g.p1 = 0x7fffffff;
   if (pair_mode == 2) {
-    g.qt[0] = g.qt[1] = u >> 1;
+    g.qt[0] = g.qt[1] = (rows * u) >> 7;
     g.n_qt = 1;
-    g.p0 = kSlabRows * u;
-    g.p1 = g.p0 + kSlabRows;
+    g.p0 = rows * u;
+    g.p1 = g.p0 + rows;
   } else if (pair_mode == 0) {
     g.qt[0] = g.qt[1] = u;
     g.n_qt = 1;
@@ -849,27 +854,29 @@ __global__ void __launch_bounds__(kGatherThreads)
   }
 }
 
-// Head-stacked units: slab_steps[u] = gathered steps of the 64-row slab u
-// (0 when one of its slices is not eligible or it has too many blocks);
-// tot[0] += the steps, tot[1] += the ineligible slabs, tot[5] += the slabs
-// with steps.
+// Head-stacked units: slab_steps[u] = gathered steps of the slab u of `rows`
+// query rows (0 when one of its slices is not eligible or it has too many
+// blocks); tot_steps += the steps, tot_bad += the ineligible slabs, tot_nz
+// += the slabs with steps.
 __global__ void __launch_bounds__(kGatherThreads)
     k_slab_count(const Slice* __restrict__ sl, const int* __restrict__ list,
                  const int* __restrict__ loff, const int* __restrict__ lcnt, int n_qt, int Tk,
-                 int* __restrict__ slab_steps, long long* tot) {
+                 int rows, int* __restrict__ slab_steps, long long* tot_steps,
+                 long long* tot_bad, long long* tot_nz) {
   __shared__ unsigned bits[kGatherBitmapWords];
   __shared__ int red[kGatherThreads / 32];
   const int u = blockIdx.x;
-  const GatherUnit gu = gather_unit(u, 2, n_qt);
+  const GatherUnit gu = gather_unit(u, 2, n_qt, rows);
   const bool ok = gather_bitmap(sl, list, loff, lcnt, gu, Tk, bits);
   const int nwords = (((Tk + kGatherKeys - 1) / kGatherKeys) + 31) / 32;
   const int n = ok ? block_popc(bits, nwords, red) : 0;
   const int steps = ok && n <= kGatherMaxBlocks ? (n + kGatherSlots - 1) / kGatherSlots : -1;
   if (threadIdx.x == 0) {
     slab_steps[u] = max(steps, 0);
-    if (steps >= 0) atomicAdd(reinterpret_cast<unsigned long long*>(tot), (unsigned long long)steps);
-    else atomicAdd(reinterpret_cast<unsigned long long*>(tot + 1), 1ull);
-    if (steps > 0) atomicAdd(reinterpret_cast<unsigned long long*>(tot + 5), 1ull);
+    if (steps >= 0)
+      atomicAdd(reinterpret_cast<unsigned long long*>(tot_steps), (unsigned long long)steps);
+    else atomicAdd(reinterpret_cast<unsigned long long*>(tot_bad), 1ull);
+    if (steps > 0) atomicAdd(reinterpret_cast<unsigned long long*>(tot_nz), 1ull);
   }
 }
 
@@ -883,7 +890,8 @@ constexpr size_t kGatherFillSmem =
 __global__ void __launch_bounds__(kGatherThreads)
     k_gather_fill(const Slice* __restrict__ sl, const int* __restrict__ list,
                   const int* __restrict__ loff, const int* __restrict__ lcnt, int n_qt,
-                  int pair_mode, int Tk, const int* __restrict__ gcnt,
+                  int pair_mode, int rows, int alternate, int Tk,
+                  const int* __restrict__ gcnt,
                   const int* __restrict__ goff, const int* __restrict__ soff, int4* steps,
                   int* __restrict__ records, int* __restrict__ cost_half) {
   extern __shared__ unsigned gsm[];
@@ -896,7 +904,7 @@ __global__ void __launch_bounds__(kGatherThreads)
   const int u = blockIdx.x;
   const int n_steps = gcnt[u];
   if (n_steps == 0) return;  // whole block
-  const GatherUnit gu = gather_unit(u, pair_mode, n_qt);
+  const GatherUnit gu = gather_unit(u, pair_mode, n_qt, rows);
   gather_bitmap(sl, list, loff, lcnt, gu, Tk, bits);
   const int nwords = (((Tk + kGatherKeys - 1) / kGatherKeys) + 31) / 32;
   // exclusive prefix of the words' bit counts (one thread per chunk of words)
@@ -943,11 +951,10 @@ __global__ void __launch_bounds__(kGatherThreads)
     for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
       const Slice x = sl[L[i]];
       uint32_t rb[4] = {0u, 0u, 0u, 0u};
-      if (pair_mode == 2) {  // tile rows r and r + 64 are both slab row r
+      if (pair_mode == 2) {  // tile rows r, r + rows, ... are all slab row r
         if (x.qe <= gu.p0 || x.qs >= gu.p1) continue;
         const int a = max(x.qs, gu.p0) - gu.p0, b = min(x.qe, gu.p1) - gu.p0;
-        add_window(a, b, rb);
-        add_window(a + kSlabRows, b + kSlabRows, rb);
+        for (int o = 0; o < 128; o += rows) add_window(a + o, b + o, rb);
       } else {
         add_window(max(x.qs, 128 * qt) - 128 * qt, min(x.qe, 128 * qt + 128) - 128 * qt, rb);
       }
@@ -990,8 +997,13 @@ __global__ void __launch_bounds__(kGatherThreads)
       }
       // 0: every slot holds keys and every row sees them all (no mask)
       info[h] = !any ? -1 : (slots_used && all == ~0u ? 0 : 1);
-      if (any) atomicAdd(&cost[h], kPartialCost);
     }
+    if (alternate) {  // the halves take the unit's steps in turn
+      info[1] = (j & 1) ? info[0] : -1;
+      if (j & 1) info[0] = -1;
+    }
+    for (int h = 0; h < 2; ++h)
+      if (info[h] >= 0) atomicAdd(&cost[h], kPartialCost);
     steps[s0 + j] = make_int4(0, info[0], info[1], r0 + j + 1);
   }
   __syncthreads();
@@ -1460,11 +1472,11 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   FFA_CUDA(cudaMallocAsync(&p->tickets, 4 * sizeof(int), st));
   FFA_CUDA(cudaMemsetAsync(p->err, 0, 2 * sizeof(int), st));
   DevBuf flags_area(st);
-  FFA_CUDA(flags_area.alloc(128));
+  FFA_CUDA(flags_area.alloc(192));
   int* flags = flags_area.as<int>();
   unsigned long long* area = reinterpret_cast<unsigned long long*>(flags + 4);
   long long* dtot = reinterpret_cast<long long*>(flags + 8);
-  FFA_CUDA(cudaMemsetAsync(flags, 0, 128, st));
+  FFA_CUDA(cudaMemsetAsync(flags, 0, 192, st));
   if (S > 0) {
     k_pack_slices<<<grid_for(S, 256), 256, 0, st>>>(qr, kr, ty, S, p->slices);
     note_launches(1);
@@ -1479,10 +1491,10 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   ffa_status_t rc = FFA_OK;
   // per-tile / per-unit arrays: 12 over q-tiles (lists, visits, units,
   // costs), 10 over k-tiles, 4 over 64-row slabs
-  const long long n_slabs_max = ((long long)p->Tq + kSlabRows - 1) / kSlabRows;
+  const long long n_slabs_max = ((long long)p->Tq + kSlabRows / 2 - 1) / (kSlabRows / 2);
   Arena arena(st);
   FFA_CUDA(arena.reserve(12 * Arena::run(n_qt) + 10 * Arena::run(n_kt) +
-                         2 * Arena::run(n_slabs_max) + 2 * Arena::run(2 * n_slabs_max)));
+                         3 * Arena::run(n_slabs_max) + Arena::run(2 * n_slabs_max)));
 #define FFA_TAKE(d, n) \
   do {                 \
     if (!arena.take(d, n)) return FFA_ERR_CUDA; \
@@ -1637,27 +1649,37 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
     note_launches(1);
     FFA_CUDA(cudaGetLastError());
   }
-  // head-stacked units (64-row slabs, heads stacked in pairs): counted beside
-  // the q-tile units and chosen after the read below when every slab gathers
-  // and they take at most 9/10 of the tile steps (per group of four heads)
+  // head-stacked units (slabs of 64 rows with heads stacked in pairs, or of
+  // 32 rows with heads in fours): counted beside the q-tile units and chosen
+  // after the read below when every slab gathers and they take at most 9/10
+  // of the chosen units' work (the planner specification gives the counts)
   const bool try_stack = pair_mode == 0 && g >= 4 && g % 2 == 0 && p->Tk <= kGatherMaxTk &&
                          n_qt > 0;
+  const bool try_stack4 = try_stack && g % 4 == 0;
   const int n_slabs = (p->Tq + kSlabRows - 1) / kSlabRows;
-  DevBuf slab_steps(st), slab_off(st), slab_cost(st);
+  const int n_slabs4 = (p->Tq + kSlabRows / 2 - 1) / (kSlabRows / 2);
+  DevBuf slab_steps(st), slab_steps4(st), slab_off(st), slab_cost(st);
+  if (try_stack) FFA_TAKE(slab_steps, n_slabs);
+  if (try_stack4) FFA_TAKE(slab_steps4, n_slabs4);
+  // one read: forward steps and gathered records, 64-row slab steps and
+  // ineligible slabs, backward steps and gathered records, units and 64-row
+  // slabs with steps, 32-row slab steps, ineligible and nonzero slabs
+  FFA_CUDA(cudaMemsetAsync(dtot + 4, 0, 12 * sizeof(long long), st));
   if (try_stack) {
-    FFA_TAKE(slab_steps, n_slabs);
-  }
-  // one read: forward steps and gathered records, slab steps and ineligible
-  // slabs, backward steps and gathered records, units and slabs with steps
-  FFA_CUDA(cudaMemsetAsync(dtot + 4, 0, 8 * sizeof(long long), st));
-  if (try_stack) {
-    k_slab_count<<<n_slabs, kGatherThreads, 0, st>>>(p->slices, qlist.as<int>(), qloff.as<int>(),
-                                                     qlcnt.as<int>(), n_qt, p->Tk,
-                                                     slab_steps.as<int>(), dtot + 6);
+    k_slab_count<<<n_slabs, kGatherThreads, 0, st>>>(
+        p->slices, qlist.as<int>(), qloff.as<int>(), qlcnt.as<int>(), n_qt, p->Tk, kSlabRows,
+        slab_steps.as<int>(), dtot + 6, dtot + 7, dtot + 11);
     note_launches(1);
     FFA_CUDA(cudaGetLastError());
   }
-  long long sg[8];
+  if (try_stack4) {
+    k_slab_count<<<n_slabs4, kGatherThreads, 0, st>>>(
+        p->slices, qlist.as<int>(), qloff.as<int>(), qlcnt.as<int>(), n_qt, p->Tk,
+        kSlabRows / 2, slab_steps4.as<int>(), dtot + 12, dtot + 13, dtot + 14);
+    note_launches(1);
+    FFA_CUDA(cudaGetLastError());
+  }
+  long long sg[12];
   if ((rc = scan_launch(scnt.as<int>(), n_units, soff.as<int>(), dtot + 4, st, dtot + 10)))
     return rc;
   if ((rc = scan_launch(gcnt.as<int>(), n_units, goff.as<int>(), dtot + 5, st))) return rc;
@@ -1666,26 +1688,39 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   if ((rc = read_to_host(sg, dtot + 4, sizeof sg, st))) return rc;
   const long long bs[2] = {sg[4], sg[5]};  // backward steps, gathered records
   long long nz_units = sg[6];             // forward units with steps
-  const bool stacked = try_stack && sg[3] == 0 && sg[2] > 0 &&
-                       10LL * ((g + 3) / 4) * sg[2] <= 9LL * (g / 2) * sg[0];
+  int stack_rows = 0;
+  long long half_steps = (long long)g * sg[0];  // work of the units chosen so far
+  if (try_stack && sg[3] == 0 && sg[2] > 0 &&
+      10LL * ((g + 3) / 4) * sg[2] <= 9LL * (g / 2) * sg[0]) {
+    stack_rows = kSlabRows;
+    half_steps = (long long)(g / 2) * sg[2];
+  }
+  if (try_stack4 && sg[9] == 0 && sg[8] > 0 && 10LL * (g / 4) * sg[8] <= 9LL * half_steps)
+    stack_rows = kSlabRows / 2;
+  const bool stacked = stack_rows > 0;
   int* u_scnt = scnt.as<int>();
   int* u_soff = soff.as<int>();
   int* u_gcnt = gcnt.as<int>();
   int* u_goff = goff.as<int>();
   int* u_cost = cost_half.as<int>();
   if (stacked) {  // every step gathered: record r is step r, offsets shared
+    const bool four = stack_rows != kSlabRows;
     pair_mode = 2;
-    n_units = n_slabs;
-    FFA_TAKE(slab_off, n_slabs);
-    FFA_TAKE(slab_cost, 2LL * n_slabs);
-    FFA_CUDA(cudaMemsetAsync(slab_cost.p, 0, sizeof(int) * 2 * n_slabs, st));
-    if ((rc = scan_launch(slab_steps.as<int>(), n_slabs, slab_off.as<int>(), dtot, st))) return rc;
-    u_scnt = u_gcnt = slab_steps.as<int>();
+    n_units = four ? n_slabs4 : n_slabs;
+    FFA_TAKE(slab_off, n_units);
+    FFA_TAKE(slab_cost, 2LL * n_units);
+    FFA_CUDA(cudaMemsetAsync(slab_cost.p, 0, sizeof(int) * 2 * n_units, st));
+    int* ss = four ? slab_steps4.as<int>() : slab_steps.as<int>();
+    if ((rc = scan_launch(ss, n_units, slab_off.as<int>(), dtot, st))) return rc;
+    u_scnt = u_gcnt = ss;
     u_soff = u_goff = slab_off.as<int>();
     u_cost = slab_cost.as<int>();
-    sg[0] = sg[1] = sg[2];
-    nz_units = sg[7];
-    p->stacked = 1;
+    sg[0] = sg[1] = four ? sg[8] : sg[2];
+    nz_units = four ? sg[10] : sg[7];
+    p->stacked = stack_rows;
+    // one half of an item holds all four heads: the two halves take the
+    // slab's steps in turn instead (merged at the end of the item)
+    p->alternate = four && g == 4;
   }
   tot = sg[0];
   if (tot > 0x7fffffffLL || sg[1] > (1LL << 24)) return FFA_ERR_UNSUPPORTED;
@@ -1710,20 +1745,23 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   if (sg[1] > 0) {
     FFA_CUDA(smem_limit_once(kAttrGatherFill, (const void*)k_gather_fill, (int)kGatherFillSmem));
     k_gather_fill<<<n_units, kGatherThreads, kGatherFillSmem, st>>>(
-        p->slices, qlist.as<int>(), qloff.as<int>(), qlcnt.as<int>(), n_qt, pair_mode, p->Tk,
-        u_gcnt, u_goff, u_soff, steps.as<int4>(), p->gathers, u_cost);
+        p->slices, qlist.as<int>(), qloff.as<int>(), qlcnt.as<int>(), n_qt, pair_mode,
+        stacked ? stack_rows : kSlabRows, p->alternate, p->Tk, u_gcnt, u_goff, u_soff,
+        steps.as<int4>(), p->gathers, u_cost);
     note_launches(1);
     FFA_CUDA(cudaGetLastError());
   }
   // forward items
-  // head pairs per kv head (groups of four heads for stacked units)
-  const int pairs = pair_mode == 2 ? (g + 3) / 4 : (g + 1) / 2;
+  // head pairs per kv head (groups of 2m heads for stacked units, m heads a half)
+  const int m_heads = stacked ? 128 / stack_rows : 1;
+  const int pairs = pair_mode == 2 ? (g + 2 * m_heads - 1) / (2 * m_heads) : (g + 1) / 2;
   const long long n_items = pair_mode != 1 ? (long long)n_units * p->Hkv * pairs
                                            : (long long)n_units * p->Hq;
   if (n_items > 0x7fffffffLL / kFiWords) return FFA_ERR_UNSUPPORTED;
   DevBuf items(st);
   FFA_CUDA(items.alloc(sizeof(int) * kFiWords * (size_t)n_items));
-  k_fwd_items<<<grid_for(n_items, 128), 128, 0, st>>>((int)n_items, pair_mode, g, p->Hkv, p->Hq,
+  k_fwd_items<<<grid_for(n_items, 128), 128, 0, st>>>((int)n_items, pair_mode, m_heads,
+                                                      p->alternate, g, p->Hkv, p->Hq,
                                                       pairs, n_qt, u_soff, u_scnt, u_cost,
                                                       items.as<int>());
   note_launches(1);
@@ -1793,7 +1831,8 @@ ffa_status_t build_plan(ffa_plan_s* p, const int32_t* qr, const int32_t* kr, con
   FFA_CUDA(cudaMallocAsync(&p->dq_counts, sizeof(int) * 2 * (size_t)std::max<int64_t>(1, p->n_dq_items), st));
   if (p->n_dq_items > 0) {
     k_dq_counts<<<grid_for(p->n_dq_items, 128), 128, 0, st>>>(p->dq_items, (int)p->n_dq_items,
-                                                             p->fwd_steps, p->dq_counts);
+                                                             p->fwd_steps, p->alternate,
+                                                             p->dq_counts);
     note_launches(1);
     FFA_CUDA(cudaGetLastError());
   }

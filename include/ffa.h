@@ -107,7 +107,7 @@ typedef struct {
   int64_t bwd_masks;  /* words of the backward slice lists */
   int64_t gathers;    /* gathered forward step records, 144 words each */
   int64_t bgathers;   /* gathered backward step records, 80 words each */
-  int64_t stacked;    /* 1: the forward units are head-stacked 64-row slabs (below) */
+  int64_t stacked;    /* slab rows (64 or 32) of head-stacked forward units, 0: none (below) */
 } ffa_plan_info_t;
 
 ffa_status_t ffa_plan_info(ffa_plan_t plan, ffa_plan_info_t* info);
@@ -134,15 +134,15 @@ ffa_status_t ffa_plan_info(ffa_plan_t plan, ffa_plan_info_t* info);
  *   into one Q / dO tile; record r holds the 16 block start rows (-8: unused)
  *   then 16 x 4 words of key bits (bit i of word w: key 32 w + i of the
  *   k-tile is seen by that block's rows).
- *   Head-stacked forward units (info.stacked = 1; with Hq / Hkv even and at
- *   least 4, when every 64-row slab of the queries meets only FULL slices
- *   with 8-aligned key ranges and slab units take at most 9/10 of the tile
- *   steps per four heads): the units are 64-row slabs, every step is
- *   gathered, and an item (s, s, h, h + 2) holds in half 0 the slab's rows
- *   of heads h and h + 1 stacked as tile rows 0-63 and 64-127 (half 1:
- *   heads h + 2, h + 3; idle, slab and head -1, past the group); a record's
- *   row bits r and r + 64 both stand for slab row r.  Such plans are not
- *   split.
+ *   Head-stacked forward units (info.stacked = R; with Hq / Hkv even and at
+ *   least 4, when every R-row slab of the queries meets only FULL slices
+ *   with 8-aligned key ranges and slab units take at most 9/10 of the work
+ *   otherwise chosen; R = 32 needs Hq / Hkv a multiple of 4): the units are
+ *   R-row slabs, every step is gathered, and an item (s, s, h, h + m), with
+ *   m = 128 / R, holds in half 0 the slab's rows of heads h .. h + m - 1
+ *   stacked as tile rows [R j, R j + R) for head h + j (half 1: heads
+ *   h + m ..; idle, slab and head -1, past the group); a record's row bits
+ *   r, r + R, ... all stand for slab row r.  Such plans are not split.
  *   dst: host int32 buffer of `capacity` words; *written receives the count.
  * Synchronises the plan's stream. */
 ffa_status_t ffa_plan_export(ffa_plan_t plan, int32_t which, int32_t* dst, int64_t capacity,

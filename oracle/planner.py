@@ -51,8 +51,17 @@ the work-list specification of the planner:
     64s + r (the same bits in both halves); items are (s, s, h, h + 2) for
     the first query head h = hk * g + 4p of each group of four (half 1 idle,
     s and head -1, when 4p + 2 >= g): a half is the slab's 64 rows of heads
-    h and h + 1 (h + 2 and h + 3), stacked in one 128-row tile.  Such plans
-    are never split.
+    h and h + 1 (h + 2 and h + 3), stacked in one 128-row tile.  With g a
+    multiple of 4, 32-row slabs of four heads per half (tile rows r, r + 32,
+    r + 64, r + 96 all mean slab row r; items (s, s, h, h + 4) for h =
+    hk * g + 8p, half 1 idle when 8p + 4 >= g) replace the choice above when
+    g / 4 times their steps is at most 9/10 of its half-steps (g times the
+    tile steps, or g / 2 times the 64-row slab steps).  With 32-row slabs and
+    g = 4 (`alternate`) an item is (s, s, h, h): both halves hold the same
+    rows and heads, take the slab's steps in turn (step j of the slab is
+    (0, i, -1, r + 1) for even j, (0, -1, i, r + 1) for odd j) and are merged
+    by logsumexp at the end of the item.  `stacked` is the slab height (64
+    or 32), 0 for q-tile units.  Such plans are never split.
 """
 from __future__ import annotations
 
@@ -201,20 +210,33 @@ def plan(total_q, total_k, num_heads_q, num_heads_kv, q_ranges, k_ranges, mask_t
         steps.extend(st)
         scnt.append(len(st))
 
-    stacked = False
+    stacked = 0  # slab rows of head-stacked units, 0: q-tile units
+    half_steps = g * len(steps)  # of the units chosen so far
     if pair_mode == 0 and g >= 4 and g % 2 == 0:
         slabs = gather_slabs(total_q, total_k, q_ranges, k_ranges, mask_types)
         if slabs is not None:
             n_slab_steps = sum(len(v) for v in slabs.values())
             if n_slab_steps > 0 and 10 * (-(-g // 4)) * n_slab_steps <= 9 * (g // 2) * len(steps):
-                stacked = True
+                stacked, half_steps = SLAB, (g // 2) * n_slab_steps
+    if pair_mode == 0 and g >= 4 and g % 4 == 0:
+        slabs4 = gather_slabs(total_q, total_k, q_ranges, k_ranges, mask_types, SLAB // 2)
+        if slabs4 is not None:
+            n4 = sum(len(v) for v in slabs4.values())
+            if n4 > 0 and 10 * (g // 4) * n4 <= 9 * half_steps:
+                stacked, slabs = SLAB // 2, slabs4
+    # 32-row slabs with 4 query heads per kv head fill one half of an item;
+    # its two halves then take the slab's steps in turn (even steps half 0,
+    # odd ones half 1) and are merged by logsumexp at the end of the item
+    alternate = stacked == SLAB // 2 and g == 4
     if stacked:
-        n_units = -(-total_q // SLAB)
+        n_units = -(-total_q // stacked)
         records, steps, soff, scnt, cost_half = [], [], [], [], []
         for u in range(n_units):
             soff.append(len(steps))
             ca = cb = 0
-            for rec, (i0, i1) in slabs.get(u, []):
+            for j, (rec, (i0, i1)) in enumerate(slabs.get(u, [])):
+                if alternate:
+                    i0, i1 = (i0, -1) if j % 2 == 0 else (-1, i0)
                 steps.append((0, i0, i1, len(records) + 1))
                 records.append(rec)
                 ca += PARTIAL_COST if i0 >= 0 else 0
@@ -224,12 +246,15 @@ def plan(total_q, total_k, num_heads_q, num_heads_kv, q_ranges, k_ranges, mask_t
 
     items = []
     if stacked:
-        quads = -(-g // 4)
+        m = TILE // stacked  # query heads per half
+        groups = -(-g // (2 * m))
         for u in range(n_units):
             for hk in range(num_heads_kv):
-                for p in range(quads):
-                    h0 = hk * g + 4 * p
-                    h1 = h0 + 2 if 4 * p + 2 < g else -1
+                for p in range(groups):
+                    h0 = hk * g + 2 * m * p
+                    h1 = h0 + m if 2 * m * p + m < g else -1
+                    if alternate:
+                        h1 = h0
                     qt1 = u if h1 >= 0 else -1
                     cost = cost_half[u][0] + (cost_half[u][1] if h1 >= 0 else 0)
                     items.append([u, qt1, h0, h1, soff[u], soff[u] + scnt[u], -1, cost])
@@ -314,6 +339,7 @@ def plan(total_q, total_k, num_heads_q, num_heads_kv, q_ranges, k_ranges, mask_t
         "bwd_masks": np.array(bmasks, dtype=np.int32).reshape(-1, 1),
         "n_slots": n_slots,
         "stacked": stacked,
+        "alternate": alternate,
         "grid_fwd": max(1, min(num_sms, len(items))),
         "grid_bwd": max(1, min(num_sms, len(bitems))),
         "area": visible_area(q_ranges, k_ranges, mask_types),
@@ -390,11 +416,12 @@ def _half_info(words, starts):
     return 0 if full else 1
 
 
-def gather_slabs(total_q, total_k, q_ranges, k_ranges, mask_types):
+def gather_slabs(total_q, total_k, q_ranges, k_ranges, mask_types, rows=SLAB):
     """{slab: [(record words, (info0, info1)), ...]} of the head-stacked
-    units, or None when some slab is not eligible."""
+    units of `rows` query rows, or None when some slab is not eligible."""
     if total_k > GATHER_MAX_TK:
         return None
+    SLAB = rows
     n_slabs = -(-total_q // SLAB)
     lists = [[] for _ in range(n_slabs)]
     for (qs, qe), (ks, ke), t in zip(np.asarray(q_ranges).reshape(-1, 2),
@@ -424,7 +451,7 @@ def gather_slabs(total_q, total_k, q_ranges, k_ranges, mask_types):
                 for qs, qe, ks, ke, _ in sl:
                     if ks < k1 and ke > k0:
                         for r in range(max(qs, SLAB * u), min(qe, SLAB * (u + 1))):
-                            for rr in (r - SLAB * u, r - SLAB * u + SLAB):
+                            for rr in range(r - SLAB * u, TILE, SLAB):
                                 words[slot, rr >> 5] |= np.uint32(1 << (rr & 31))
             half = [int(w) for w in words.view(np.int32).reshape(-1)]
             info = _half_info(words, rec)

@@ -116,14 +116,16 @@ def test_block_sparse_gathered_softcap_sink(case):
 
 
 # Head-stacked forward units (a 128-row tile holds one 64-row slab of two
-# query heads): Hq / Hkv = 4 or 6, ragged T, D = 128 and 64, with and without
-# sink logits and softcap.
+# query heads, or one 32-row slab of four): Hq / Hkv = 4, 6 or 8, ragged T,
+# D = 128 and 64, with and without sink logits and softcap.
 STACKED = [
     # (total, hq, hkv, d, q_block, k_block, seed, sink, cap)
     (2000, 8, 2, 128, 64, 64, 51, False, 0.0),
     (2000, 8, 2, 128, 16, 64, 52, True, 0.0),
     (1500, 12, 2, 64, 32, 64, 53, False, 0.0),
     (1000, 4, 1, 128, 64, 8, 54, True, 5.0),
+    (2000, 8, 2, 128, 16, 64, 55, False, 30.0),   # 32-row slabs of four heads
+    (1000, 16, 2, 64, 16, 64, 56, True, 0.0),     # 32-row slabs, both halves busy
 ]
 
 
@@ -140,7 +142,7 @@ def test_block_sparse_stacked(case):
         if with_sink else None
     plan = ffa.ffa_plan_create(wl.q_ranges, wl.k_ranges, wl.mask_types, wl.total_q, wl.total_k,
                                hq, hkv, d)
-    assert ffa.ffa_plan_info(plan)["stacked"] == 1
+    assert ffa.ffa_plan_info(plan)["stacked"] in (32, 64)
     qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
     sd = sink.to(DEV) if sink is not None else None
     out, lse = ffa.ffa_fwd_ex(plan, qd, kd, vd, sink=sd, softcap=cap)

@@ -24,7 +24,7 @@ def compare(qr, kr, ty, Tq, Tk, Hq, Hkv, D, split_below=0):
     info = ffa.ffa_plan_info(plan)
     assert info["area"] == ref["area"]
     assert info["grid_fwd"] == ref["grid_fwd"] and info["grid_bwd"] == ref["grid_bwd"]
-    assert bool(info["stacked"]) == ref["stacked"]
+    assert info["stacked"] == ref["stacked"]
     plan.destroy()
     return ref
 
@@ -80,10 +80,11 @@ def test_overlap_found_between_tiny_slices():
 
 
 @pytest.mark.parametrize("blocks,heads,T", [((64, 64), (8, 2), 4096), ((16, 64), (8, 2), 4096),
-                                            ((64, 8), (4, 1), 4096), ((32, 64), (12, 2), 1000)])
+                                            ((64, 8), (4, 1), 4096), ((32, 64), (12, 2), 1000),
+                                            ((16, 64), (16, 2), 1000)])
 def test_block_sparse_stacked(blocks, heads, T):
-    """Head-stacked forward units (4 or 6 query heads per kv head): the same
-    lists and the same choice as the CPU derivation."""
+    """Head-stacked forward units (4, 6 or 8 query heads per kv head; 64- and
+    32-row slabs): the same lists and the same choice as the CPU derivation."""
     wl = W.block_sparse(total=T, hq=heads[0], hkv=heads[1], q_block=blocks[0],
                         k_block=blocks[1], seed=11)
     ref = compare(wl.q_ranges, wl.k_ranges, wl.mask_types, T, T, heads[0], heads[1],

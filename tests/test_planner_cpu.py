@@ -271,51 +271,61 @@ def test_gathered_backward_steps_cover_the_mask_exactly(blocks, seed, heads):
 # (q block, k block, seed, heads) of tables whose forward units are stacked:
 # Hq / Hkv = 4 or 6, T = 1000 (the last 64-row slab is ragged)
 STACK_CASES = [((64, 64), 1, (8, 2)), ((16, 64), 3, (8, 2)), ((64, 8), 2, (4, 1)),
-               ((32, 64), 7, (12, 2))]
+               ((32, 64), 7, (12, 2)), ((16, 64), 5, (16, 2)), ((16, 32), 8, (12, 2))]
 
 
 @pytest.mark.parametrize("blocks,seed,heads", STACK_CASES)
 def test_stacked_units_cover_the_mask_exactly(blocks, seed, heads):
     """Head-stacked forward units (the planner specification for g even and
-    >= 4): every (64-row slab, query head) is one half's tile rows 0-63 or
-    64-127 of exactly one item; the (row, key) pairs its steps' row bits mark
-    are exactly the visible pairs of the slab's rows, each once; tile rows r
-    and r + 64 carry the same bits; the plan is not split."""
-    m, p = _block_sparse_plan(blocks, seed, heads)
-    assert p["stacked"] and p["merges"].shape[0] == 0
-    T, Hq, g = m.shape[1], heads[0], heads[0] // heads[1]
-    n_slabs = -(-T // 64)
+    >= 4): with slabs of R rows and m = 128 / R heads per half, every (slab,
+    query head) is tile rows [R j, R j + R) of one half of exactly one item;
+    the (row, key) pairs its steps' row bits mark are exactly the visible
+    pairs of the slab's rows, each once; the m row groups of a half carry
+    the same bits; the plan is not split."""
+    m_, p = _block_sparse_plan(blocks, seed, heads)
+    R = p["stacked"]
+    assert R in (32, 64) and p["merges"].shape[0] == 0
+    T, Hq, g = m_.shape[1], heads[0], heads[0] // heads[1]
+    m = 128 // R
+    n_slabs = -(-T // R)
     steps, rec = p["fwd_steps"], p["gathers"]
     assert (steps[:, 3] > 0).all(), "every step of a stacked plan is gathered"
     marked, seen = {}, {}
     for it in p["fwd_items"]:
         assert it[6] == -1
+        # with alternating halves both halves are the same (slab, heads): the
+        # item covers them once, each half with its own steps
+        covers = {(it[h], it[2 + h]) for h in range(2) if it[h] >= 0 and it[2 + h] >= 0}
+        assert p["alternate"] == (len(covers) == 1 and it[1] >= 0)
+        for u, h0 in covers:
+            for j in range(m):
+                seen[(u, h0 + j)] = seen.get((u, h0 + j), 0) + 1
+                marked.setdefault((u, h0 + j), np.zeros((R, T), np.int64))
         for h in range(2):
             u, h0 = it[h], it[2 + h]
             if u < 0 or h0 < 0:
                 continue
-            assert h0 % 2 == 0 and h0 // g == (h0 + 1) // g
-            for j in range(2):
-                seen[(u, h0 + j)] = seen.get((u, h0 + j), 0) + 1
-                marked.setdefault((u, h0 + j), np.zeros((64, T), np.int64))
+            assert h0 % m == 0 and h0 // g == (h0 + m - 1) // g
             for st in steps[it[4]:it[5]]:
                 r = rec[st[3] - 1]
                 starts = r[:16]
                 words = r[16 + 64 * h: 16 + 64 * (h + 1)].view(np.uint32).reshape(16, 4)
+                if p["alternate"] and st[1 + h] < 0:
+                    continue  # the other half's step
                 assert (st[1 + h] >= 0) == bool(words.any())
                 for slot, y in enumerate(starts):
                     if y < 0:
                         assert not words[slot].any()
                         continue
                     bits = (words[slot][np.arange(128) >> 5] >> (np.arange(128) & 31)) & 1
-                    assert (bits[:64] == bits[64:]).all()
-                    for j in range(2):
-                        for rr in np.nonzero(bits[64 * j: 64 * j + 64])[0]:
+                    for j in range(m):
+                        assert (bits[R * j: R * j + R] == bits[:R]).all()
+                        for rr in np.nonzero(bits[R * j: R * j + R])[0]:
                             marked[(u, h0 + j)][rr, y:min(y + 8, T)] += 1
     assert set(seen) == {(u, hq) for u in range(n_slabs) for hq in range(Hq)}
     assert all(c == 1 for c in seen.values())
     for (u, _), got in marked.items():
-        ref = m[64 * u: min(64 * u + 64, T)]
+        ref = m_[R * u: min(R * u + R, T)]
         got = got[: ref.shape[0]]
         assert (got[ref] == 1).all(), "a visible pair is missed or listed twice"
         assert (got[~ref] == 0).all(), "an invisible pair is marked visible"
