@@ -142,7 +142,10 @@ ffa_status_t ffa_plan_info(ffa_plan_t plan, ffa_plan_info_t* info);
  *   m = 128 / R, holds in half 0 the slab's rows of heads h .. h + m - 1
  *   stacked as tile rows [R j, R j + R) for head h + j (half 1: heads
  *   h + m ..; idle, slab and head -1, past the group); a record's row bits
- *   r, r + R, ... all stand for slab row r.  Such plans are not split.
+ *   r, r + R, ... all stand for slab row r.  With R = 32 and Hq / Hkv = 4
+ *   an item is (s, s, h, h): both halves hold the same rows and take the
+ *   slab's steps in turn (even steps half 0, odd ones half 1), merged by
+ *   logsumexp in the kernel.  Such plans are not split.
  *   dst: host int32 buffer of `capacity` words; *written receives the count.
  * Synchronises the plan's stream. */
 ffa_status_t ffa_plan_export(ffa_plan_t plan, int32_t which, int32_t* dst, int64_t capacity,
