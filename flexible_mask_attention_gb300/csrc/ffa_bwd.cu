@@ -430,14 +430,16 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
         const int* it = P.items + (size_t)idx * kBiWords;
         const int sb = it[kBiStepBeg], se = it[kBiStepEnd];
         if (se <= sb) continue;
+        // Waits on TMA barriers need no tcgen05 fence (the copies and the MMAs
+        // are async-proxy operations ordered by the barrier); the waits on the
+        // elementwise warps' arrivals are followed by one, and every MMA that
+        // rewrites TMEM they read is issued after such a fence.
         if (!(ok = mbar_wait(bar(C::kBKVFull), kv_cnt & 1, ctl, 500))) break;
         ++kv_cnt;
-        tc_fence_after();
         const int n_it = (se - sb) * g;
         {  // S^T of the first iteration
           const int qs = q_cnt % C::kQStages;
           if (!(ok = mbar_wait(bar(C::kBQFull + qs), (q_cnt / C::kQStages) & 1, ctl, 501))) break;
-          tc_fence_after();
           issue_st(qs);
           mma_commit(bar(C::kBSFull));
         }
@@ -445,7 +447,6 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
           const uint32_t c = q_cnt + (uint32_t)i;
           const int qs = c % C::kQStages, ds = c % C::kDOStages;
           if (!(ok = mbar_wait(bar(C::kBDOFull + ds), (c / C::kDOStages) & 1, ctl, 502))) break;
-          tc_fence_after();
           // dP^T = V dO^T; its columns were last read by the previous dV / dK MMAs.
           {
             const uint64_t dod = dDOk + ds * kTile16;
@@ -507,6 +508,7 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
         // a pending S-free arrival of the last iteration is consumed here
         if (!(ok = mbar_wait(bar(C::kBSFree), sf_cnt & 1, ctl, 507))) break;
         ++sf_cnt;
+        tc_fence_after();  // the next item's first S^T rewrites those columns
         q_cnt += (uint32_t)n_it;
         mma_commit(bar(C::kBDkvFull));
         mma_commit(bar(C::kBKVEmpty));

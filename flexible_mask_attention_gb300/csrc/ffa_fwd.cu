@@ -431,7 +431,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const bool act1 = it[kFiQt1] >= 0 && it[kFiH1] >= 0;
         if (!(ok = mbar_wait(bar(C::kBQFull), q_cnt & 1, ctl, 200))) break;
         ++q_cnt;
-        tc_fence_after();
         bool first_pv[2] = {true, true};
         int4 cur = P.steps[sb];
         int4 nxt = sb + 1 < se ? P.steps[sb + 1] : make_int4(0, -1, -1, 0);
@@ -439,7 +438,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const int stage = kv_cnt % C::kStages;
           if (!(ok = mbar_wait(bar(C::kBKFull + stage), (kv_cnt / C::kStages) & 1, ctl, 201)))
             break;
-          tc_fence_after();
           if (cur.y >= 0) {
             issue_s(0, stage);
             mma_commit(bar(C::kBSFull + 0));
@@ -468,7 +466,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const int hn = nxt.y >= 0 ? 0 : 1;
             if (!(ok = mbar_wait(bar(C::kBKFull + stage_n), ph_n, ctl, 215))) break;
             k_next_ready = true;
-            tc_fence_after();
             issue_s(hn, stage_n);
             mma_commit(bar(C::kBSFull + hn));
           }
@@ -496,7 +493,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               if (!k_next_ready) {
                 if (!(ok = mbar_wait(bar(C::kBKFull + stage_n), ph_n, ctl, 215))) break;
                 k_next_ready = true;
-                tc_fence_after();
               }
               issue_s(h, stage_n);
               mma_commit(bar(C::kBSFull + h));
