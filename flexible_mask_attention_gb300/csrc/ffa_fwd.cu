@@ -1022,12 +1022,14 @@ ffa_status_t launch_fwd(ffa_plan_s* p, const void* q, const void* k, const void*
                         void* out, float* lse, void* ws, size_t, cudaStream_t st,
                         const SinkArgs& sink, float softcap) {
   const bool cap = softcap > 0.f, g = p->n_gathers > 0;
-  // Staged output where the items average at most 16 steps: the epilogue is
-  // then a large share of an item (GB300: forward 3-5% faster on short
-  // documents and 64 x 64 blocks), while on longer items the 32 KB of
-  // staging taken from the L1 cache costs about as much as it saves.
+  // Staged output where the items average at most 16 steps of 128 x 128
+  // visible pairs (visible pairs x query heads over items x two halves of
+  // 128 x 128; this follows the steps the items run within 5% on long
+  // items): the epilogue is then a large share of an item (GB300: forward
+  // 2-5% faster on short documents and small blocks), while on longer items
+  // the 32 KB of staging taken from the L1 cache costs more than it saves.
   // Capped plans keep the direct stores (no staged instantiation).
-  const bool stage = !cap && p->n_fwd_steps <= 16 * p->n_fwd_items;
+  const bool stage = !cap && p->area * p->Hq <= 16LL * 2 * 128 * 128 * p->n_fwd_items;
 #define FFA_FWD(DD, CC, GG, SS) \
   launch_fwd_d<DD, CC, GG, SS>(p, q, k, v, scale, out, lse, ws, st, sink, softcap)
   if (p->D == 128) {
