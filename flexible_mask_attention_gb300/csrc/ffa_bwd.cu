@@ -72,8 +72,8 @@ struct KvCfg {
   static constexpr int kLseStageBytes = 2 * 128 * 4;
   static constexpr int kBarOff = kLseOff + kDOStages * kLseStageBytes;
   static constexpr int kBKVFull = 0, kBKVEmpty = 1, kBQFull = 2, kBQEmpty = 2 + kQStages,
-                       kBDOFull = 2 + 2 * kQStages, kBDOEmpty = kBDOFull + kDOStages,
-                       kBSdpFull = kBDOEmpty + kDOStages, kBSFree = kBSdpFull + 1,
+                       kBDOFull = 2 + 2 * kQStages, kBSdpFull = kBDOFull + kDOStages,
+                       kBSFree = kBSdpFull + 1,
                        kBPFull = kBSFree + 1, kBDkvFull = kBPFull + 2,
                        kBDkvEmpty = kBDkvFull + 1, kBDrain = kBDkvEmpty + 1,
                        kBSFull = kBDrain + 1, kBItemFull = kBSFull + 1,
@@ -221,10 +221,7 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
       mbar_init(bar(C::kBQFull + s), 1);
       mbar_init(bar(C::kBQEmpty + s), 1);
     }
-    for (int s = 0; s < C::kDOStages; ++s) {
-      mbar_init(bar(C::kBDOFull + s), 1);
-      mbar_init(bar(C::kBDOEmpty + s), 1);
-    }
+    for (int s = 0; s < C::kDOStages; ++s) mbar_init(bar(C::kBDOFull + s), 1);
     mbar_init(bar(C::kBSdpFull), 1);
     mbar_init(bar(C::kBSFull), 1);
     for (int s = 0; s < kItemRing; ++s) {
@@ -356,7 +353,15 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
         if (load_do || load_lse) {
           const int ds = do_cnt % C::kDOStages;
           if (lane == 0) {
-            ok = mbar_wait(bar(C::kBDOEmpty + ds), ((do_cnt / C::kDOStages) & 1) ^ 1, ctl, 402);
+            // The dO stage (and its -lse2 / -delta) of iteration do_cnt - kDOStages
+            // is free once that iteration's dV / dK MMAs are done, the moment
+            // its Q stage is handed back: wait on that Q-empty phase, so the
+            // MMA thread commits one barrier per iteration instead of two.
+            if (do_cnt >= (uint32_t)C::kDOStages) {
+              const uint32_t c0 = do_cnt - C::kDOStages;
+              ok = mbar_wait(bar(C::kBQEmpty + c0 % C::kQStages), (c0 / C::kQStages) & 1, ctl,
+                             402);
+            }
             if (ok && load_do)
               mbar_arrive_expect_tx(bar(C::kBDOFull + ds), C::kTileBytes + C::kLseStageBytes);
           }
@@ -501,8 +506,7 @@ __global__ void __launch_bounds__(KvCfg<D>::kThreads, 1)
           }
           if (!ok) break;
           ++p_cnt;
-          mma_commit(bar(C::kBDOEmpty + ds));
-          mma_commit(bar(C::kBQEmpty + qs));
+          mma_commit(bar(C::kBQEmpty + qs));  // also frees the iteration's dO stage
         }
         if (!ok) break;
         // a pending S-free arrival of the last iteration is consumed here
