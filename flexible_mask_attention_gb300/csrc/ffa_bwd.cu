@@ -686,7 +686,7 @@ struct DqCfg {
   static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
   static constexpr int kBQFull = 0, kBQEmpty = 1, kBKFull = 2, kBKEmpty = kBKFull + kKStages,
                        kBVFull = kBKEmpty + kKStages, kBVEmpty = kBVFull + kVStages,
-                       kBSdFull = kBVEmpty + kVStages, kBDpFree = kBSdFull + 1,
+                       kBDpFree = kBVEmpty + kVStages,
                        kBDsFull = kBDpFree + 1, kBDqFull = kBDsFull + 1,
                        kBDqEmpty = kBDqFull + 1, kBDrain = kBDqEmpty + 1,
                        kBItemFull = kBDrain + 1, kBItemEmpty = kBItemFull + kItemRing,
@@ -801,7 +801,6 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       mbar_init(bar(C::kBVFull + s), 1);
       mbar_init(bar(C::kBVEmpty + s), 1);
     }
-    mbar_init(bar(C::kBSdFull), 1);
     mbar_init(bar(C::kBDpFree), 256);
     mbar_init(bar(C::kBDsFull), 256);
     mbar_init(bar(C::kBDqFull), 1);
@@ -1009,8 +1008,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
             if (!(ok = mbar_wait(bar(C::kBVFull + vs), (kv_cnt / C::kVStages) & 1, ctl, 902))) break;
             tc_fence_after();
             issue_dp(vs);
-            mma_commit(bar(C::kBSdFull));
-            mma_commit(bar(C::kBVEmpty + vs));  // V is read by the dP MMA only
+            // V is read by the dP MMA only; the same arrival tells the dS
+            // warps that this step's S and dP are in TMEM
+            mma_commit(bar(C::kBVEmpty + vs));
           }
           for (int v = 0; v < n; ++v) {
             const uint32_t c = kv_cnt + (uint32_t)v;
@@ -1026,8 +1026,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
               if (!(ok = mbar_wait(bar(C::kBVFull + v1), (c1 / C::kVStages) & 1, ctl, 905))) break;
               tc_fence_after();
               issue_dp(v1);
-              mma_commit(bar(C::kBSdFull));
-              mma_commit(bar(C::kBVEmpty + v1));
+              mma_commit(bar(C::kBVEmpty + v1));  // V free; S and dP of step v + 1 ready
             }
             if (!(ok = mbar_wait(bar(C::kBDsFull), ds_cnt & 1, ctl, 906))) break;
             ++ds_cnt;
@@ -1095,7 +1094,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
           if (kGather && st.w > 0 && (info & 1))
             gather_mask(P.gathers + (size_t)(st.w - 1) * kGatherWords, h, t, P.Tk, vb);
-          const bool w = mbar_wait(bar(C::kBSdFull), sd_cnt & 1, ctl, 1000);
+          // S and dP of the step are in TMEM once its V stage is handed back
+          // (one arrival per step on the V ring serves both)
+          const bool w = mbar_wait(bar(C::kBVEmpty + sd_cnt % C::kVStages),
+                                   (sd_cnt / C::kVStages) & 1, ctl, 1000);
           if (!(ok = __all_sync(0xffffffffu, w))) break;
           ++sd_cnt;
           tc_fence_after();
