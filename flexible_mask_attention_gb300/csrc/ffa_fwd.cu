@@ -9,7 +9,8 @@
 // Warp roles (384 threads, three warpgroups):
 //   warps 0-3  softmax for half 0 (thread = query row = TMEM lane)
 //   warps 4-7  softmax for half 1
-//   warp  8    TMA producer: Q tiles, then a ring of K/V stages
+//   warp  8    TMA producer: Q tiles, then a ring of K/V stages (stage u
+//              of an item: V of step u - 1 with K of step u)
 //   warp  9    tcgen05 MMA issuer (and TMEM owner)
 //   warp  10   V loader for plans with gathered steps (idle otherwise)
 //   warp  11   idle
@@ -69,9 +70,10 @@ struct FwdCfg {
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
   // barrier indices
-  static constexpr int kBQFull = 0, kBQEmpty = 1, kBKFull = 2, kBVFull = 2 + kStages,
-                       kBKEmpty = 2 + 2 * kStages, kBVEmpty = 2 + 3 * kStages,
-                       kBSFull = 2 + 4 * kStages, kBPFull = kBSFull + 2, kBOFull = kBPFull + 2,
+  // K/V ring: stage u of an item holds V of step u - 1 and K of step u (the
+  // first only K, the last only V; see the producer)
+  static constexpr int kBQFull = 0, kBQEmpty = 1, kBStFull = 2, kBStEmpty = 2 + kStages,
+                       kBSFull = 2 + 2 * kStages, kBPFull = kBSFull + 2, kBOFull = kBPFull + 2,
                        kBOEmpty = kBOFull + 2, kBDrain = kBOEmpty + 2,
                        kBItemFull = kBDrain + 1, kBItemEmpty = kBItemFull + kItemRing,
                        kBHandFull = kBItemEmpty + kItemRing, kBHandEmpty = kBHandFull + 1,
@@ -263,10 +265,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     mbar_init(bar(C::kBQFull), 1);
     mbar_init(bar(C::kBQEmpty), 1);
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar(C::kBKFull + s), 1);
-      mbar_init(bar(C::kBVFull + s), 1);
-      mbar_init(bar(C::kBKEmpty + s), 1);
-      mbar_init(bar(C::kBVEmpty + s), 1);
+      mbar_init(bar(C::kBStFull + s), 1);   // warp 8's arrival with the stage's bytes
+      mbar_init(bar(C::kBStEmpty + s), 1);  // the MMA thread's commit
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(bar(C::kBSFull + h), 1);
@@ -306,13 +306,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // has gathered steps; then warp 10 loads V (a gathered tile is 16 slots x
     // D / 64 boxes per tensor, and each lane-issued copy costs the issuing
     // warp some 60 cycles), taking the items from the work queue like the
-    // consumers and waiting on the V stages itself.  Lane 0 of the loading
-    // warp waits on the rings and sets each barrier's byte count.  With
-    // gathered steps the whole warp runs the loop and the 16 slots of a
-    // gathered tile (8 rows each, 1024-byte aligned, unused ones reading
-    // zero rows from row -8) are copied by lanes 0-15 in parallel after a
-    // __syncwarp that orders them behind the byte count; without them lane 0
-    // runs it alone.
+    // consumers and waiting on the ring itself.  The ring's stage u of an
+    // item (n steps, stages 0..n) holds V of step u - 1 and K of step u: the
+    // two tiles the MMA thread needs next once step u - 1's P is ready, so
+    // one wait and one release per step cover both.  Lane 0 of warp 8 waits
+    // on the ring and sets each stage's byte count (both tiles'); warp 10's
+    // V copies may land on the stage's barrier before that arrival, whose
+    // phase cannot complete without it.  With gathered steps the whole warp
+    // runs the loop and the 16 slots of a gathered tile (8 rows each,
+    // 1024-byte aligned, unused ones reading zero rows from row -8) are
+    // copied by lanes 0-15 in parallel after a __syncwarp that orders them
+    // behind the wait; without them lane 0 runs it alone.
     const bool role0 = warp == 8;
     const bool load_v = !kGather || !role0;
     if (lane == 0) {
@@ -337,7 +341,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tma_load_2d(dst + c * 16384, m, b, hk * D + c * 64, stp.x * 128);
       }
     };
-    uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0;  // K / V tiles issued (same stage sequence)
+    uint32_t u_cnt = 0, q_cnt = 0;  // ring stages and Q tiles issued
     bool ok = true;
     const unsigned pm = kGather ? 0xffffffffu : 1u;  // lanes running the loop
     if (kGather || lane == 0)
@@ -390,44 +394,40 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (!(ok = __shfl_sync(pm, ok, 0))) break;
         ++q_cnt;
       }
-      for (int j = sb; j < se; ++j) {
-        const int4 stp = P.steps[j];
-        // this lane's slot start (read while the ring slot is awaited)
-        const int y = kGather && stp.w > 0 && lane < kGatherSlots
+      const int n = se - sb;
+      for (int u = 0; u <= n; ++u) {
+        const bool has_k = u < n, has_v = u > 0;
+        const bool mine = role0 ? has_k : has_v;  // this warp copies a tile into the stage
+        const int4 stp = mine ? P.steps[sb + (role0 ? u : u - 1)] : make_int4(0, -1, -1, 0);
+        // this lane's slot start of that tile (read while the stage is awaited)
+        const int y = kGather && mine && stp.w > 0 && lane < kGatherSlots
                           ? P.gathers[(size_t)(stp.w - 1) * kGatherWords + lane] : 0;
-        if (role0) {
-          const int stage = k_cnt % C::kStages;
-          if (lane == 0) {
-            ok = mbar_wait(bar(C::kBKEmpty + stage), ((k_cnt / C::kStages) & 1) ^ 1, ctl, 101);
-            if (ok) mbar_arrive_expect_tx(bar(C::kBKFull + stage), C::kTileBytes);
-          }
-          if (!(ok = __shfl_sync(pm, ok, 0))) break;
-          __syncwarp(pm);
+        const int stage = u_cnt % C::kStages;
+        if (lane == 0) {
+          ok = mbar_wait(bar(C::kBStEmpty + stage), ((u_cnt / C::kStages) & 1) ^ 1, ctl,
+                         role0 ? 101 : 102);
+          if (ok && role0)
+            mbar_arrive_expect_tx(bar(C::kBStFull + stage),
+                                  ((has_k ? 1 : 0) + (has_v ? 1 : 0)) * C::kTileBytes);
+        }
+        if (!(ok = __shfl_sync(pm, ok, 0))) break;
+        __syncwarp(pm);
+        if (role0 && has_k)
           load_kv(sbase + C::kKOff + stage * C::kTileBytes, &tm_k, &tm_k8,
-                  bar(C::kBKFull + stage), hk, stp, y);
-          ++k_cnt;
-        }
-        if (load_v) {
-          const int stage = v_cnt % C::kStages;
-          if (lane == 0) {
-            ok = mbar_wait(bar(C::kBVEmpty + stage), ((v_cnt / C::kStages) & 1) ^ 1, ctl, 102);
-            if (ok) mbar_arrive_expect_tx(bar(C::kBVFull + stage), C::kTileBytes);
-          }
-          if (!(ok = __shfl_sync(pm, ok, 0))) break;
-          __syncwarp(pm);
+                  bar(C::kBStFull + stage), hk, stp, y);
+        if (load_v && has_v) {
+          const int4 stv = role0 ? P.steps[sb + u - 1] : stp;  // warp 8 alone: no gathered steps
           load_kv(sbase + C::kVOff + stage * C::kTileBytes, &tm_v, &tm_v8,
-                  bar(C::kBVFull + stage), hk, stp, y);
-          ++v_cnt;
+                  bar(C::kBStFull + stage), hk, stv, y);
         }
+        ++u_cnt;
       }
     }
     if (!ok && lane == 0) {
       // Aborted: let this warp's copies already issued land before the CTA exits.
       if (q_cnt > 0) drain_wait(bar(C::kBQFull), (q_cnt - 1) & 1, kDrainNs);
-      for (uint32_t i = k_cnt > (uint32_t)C::kStages ? k_cnt - C::kStages : 0; i < k_cnt; ++i)
-        drain_wait(bar(C::kBKFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
-      for (uint32_t i = v_cnt > (uint32_t)C::kStages ? v_cnt - C::kStages : 0; i < v_cnt; ++i)
-        drain_wait(bar(C::kBVFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
+      for (uint32_t i = u_cnt > (uint32_t)C::kStages ? u_cnt - C::kStages : 0; i < u_cnt; ++i)
+        drain_wait(bar(C::kBStFull + i % C::kStages), (i / C::kStages) & 1, kDrainNs);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mma_ts_at(tmem + 256 + h * 128, tmem + h * 128 + kk * 8, vd, kk * 128, kIdPV,
                     (acc || kk > 0) ? 1u : 0u);
       };
-      uint32_t kv_cnt = 0, q_cnt = 0, p_cnt[2] = {0, 0}, oe_cnt[2] = {0, 0};
+      uint32_t u_cnt = 0, q_cnt = 0, p_cnt[2] = {0, 0}, oe_cnt[2] = {0, 0};  // u: ring stages
       const bool alt_items = kGather && P.alternate;
       bool ok = true;
       for (int r = 0; ok; ++r) {
@@ -473,9 +473,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         bool first_pv[2] = {true, true};
         int4 cur = P.steps[sb];
         int4 nxt = sb + 1 < se ? P.steps[sb + 1] : make_int4(0, -1, -1, 0);
-        {
-          const int stage = kv_cnt % C::kStages;
-          if (!(ok = mbar_wait(bar(C::kBKFull + stage), (kv_cnt / C::kStages) & 1, ctl, 201)))
+        {  // the item's first stage: K of its first step
+          const int stage = u_cnt % C::kStages;
+          if (!(ok = mbar_wait(bar(C::kBStFull + stage), (u_cnt / C::kStages) & 1, ctl, 201)))
             break;
           if (cur.y >= 0) {
             issue_s(0, stage);
@@ -485,27 +485,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             issue_s(1, stage);
             mma_commit(bar(C::kBSFull + 1));
           }
-          mma_commit(bar(C::kBKEmpty + stage));  // every S of this step is issued
+          mma_commit(bar(C::kBStEmpty + stage));  // every S of this step is issued
+          ++u_cnt;
         }
         for (int j = sb; ok && j < se; ++j) {
-          const uint32_t c = kv_cnt + (uint32_t)(j - sb);
-          const int stage = c % C::kStages;
-          const uint32_t ph = (c / C::kStages) & 1;
-          const int stage_n = (c + 1) % C::kStages;
-          const uint32_t ph_n = ((c + 1) / C::kStages) & 1;
+          // the stage of V(j) and K(j + 1): one wait for both, released once
+          // this step's P V and the next step's S are issued
+          const int stage = u_cnt % C::kStages;
           const bool has_next = j + 1 < se;
           // step descriptors are read two steps ahead: the load of step j + 2
           // has a whole step to land
           const int4 nxt2 = j + 2 < se ? P.steps[j + 2] : make_int4(0, -1, -1, 0);
-          bool v_ready = false, k_next_ready = false;
+          if (!(ok = mbar_wait(bar(C::kBStFull + stage), (u_cnt / C::kStages) & 1, ctl, 214)))
+            break;
           if (alt_items && has_next && (nxt.y >= 0 || nxt.z >= 0)) {
             // halves that take the steps in turn: the next step's S (the other
             // half's buffer, whose P went to PV a step ago) goes before this
             // step's PV, so one half's softmax runs while the other's does
             const int hn = nxt.y >= 0 ? 0 : 1;
-            if (!(ok = mbar_wait(bar(C::kBKFull + stage_n), ph_n, ctl, 215))) break;
-            k_next_ready = true;
-            issue_s(hn, stage_n);
+            issue_s(hn, stage);
             mma_commit(bar(C::kBSFull + hn));
           }
 #pragma unroll
@@ -519,27 +517,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                   break;
                 ++oe_cnt[h];
               }
-              if (!v_ready) {
-                if (!(ok = mbar_wait(bar(C::kBVFull + stage), ph, ctl, 214))) break;
-                v_ready = true;
-              }
               tc_fence_after();
               issue_pv(h, stage, !first_pv[h]);
               first_pv[h] = false;
             }
             const int ninfo = h == 0 ? nxt.y : (act1 ? nxt.z : -1);
             if (!alt_items && has_next && ninfo >= 0) {
-              if (!k_next_ready) {
-                if (!(ok = mbar_wait(bar(C::kBKFull + stage_n), ph_n, ctl, 215))) break;
-                k_next_ready = true;
-              }
-              issue_s(h, stage_n);
+              issue_s(h, stage);
               mma_commit(bar(C::kBSFull + h));
             }
           }
           if (!ok) break;
-          mma_commit(bar(C::kBVEmpty + stage));
-          if (has_next) mma_commit(bar(C::kBKEmpty + stage_n));  // S of step j+1 issued
+          mma_commit(bar(C::kBStEmpty + stage));  // V(j) and K(j + 1) read
+          ++u_cnt;
           cur = nxt;
           nxt = nxt2;
         }
@@ -548,7 +538,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int h = 0; h < 2; ++h)
           if (!first_pv[h]) mma_commit(bar(C::kBOFull + h));
         mma_commit(bar(C::kBQEmpty));
-        kv_cnt += (uint32_t)(se - sb);
       }
       // Every MMA issued so far must finish before TMEM is released.
       mma_commit(bar(C::kBDrain));
