@@ -684,8 +684,14 @@ struct DqCfg {
   static constexpr int kKOff = 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kKStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-  static constexpr int kBQFull = 0, kBQEmpty = 1, kBKFull = 2, kBKEmpty = kBKFull + kKStages,
-                       kBVFull = kBKEmpty + kKStages, kBVEmpty = kBVFull + kVStages,
+  // K and V of step c both land on step barrier c % kStepBars (warp 8 sets
+  // the byte count of both): one wait per step covers the two tiles that the
+  // S and dP MMAs of the step read back to back.  Each ring keeps its own
+  // release barriers; kStepBars is the deeper ring's depth, so a tile is
+  // only copied once the step barrier's previous phase has completed.
+  static constexpr int kStepBars = kKStages > kVStages ? kKStages : kVStages;
+  static constexpr int kBQFull = 0, kBQEmpty = 1, kBStepFull = 2,
+                       kBKEmpty = kBStepFull + kStepBars, kBVEmpty = kBKEmpty + kKStages,
                        kBDpFree = kBVEmpty + kVStages,
                        kBDsFull = kBDpFree + 1, kBDqFull = kBDsFull + 1,
                        kBDqEmpty = kBDqFull + 1, kBDrain = kBDqEmpty + 1,
@@ -793,14 +799,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(C::kBQFull), 1);
     mbar_init(bar(C::kBQEmpty), 1);
-    for (int s = 0; s < C::kKStages; ++s) {
-      mbar_init(bar(C::kBKFull + s), 1);
-      mbar_init(bar(C::kBKEmpty + s), 1);
-    }
-    for (int s = 0; s < C::kVStages; ++s) {
-      mbar_init(bar(C::kBVFull + s), 1);
-      mbar_init(bar(C::kBVEmpty + s), 1);
-    }
+    for (int s = 0; s < C::kStepBars; ++s) mbar_init(bar(C::kBStepFull + s), 1);
+    for (int s = 0; s < C::kKStages; ++s) mbar_init(bar(C::kBKEmpty + s), 1);
+    for (int s = 0; s < C::kVStages; ++s) mbar_init(bar(C::kBVEmpty + s), 1);
     mbar_init(bar(C::kBDpFree), 256);
     mbar_init(bar(C::kBDsFull), 256);
     mbar_init(bar(C::kBDqFull), 1);
@@ -927,24 +928,24 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
             const int ks = k_cnt % C::kKStages;
             if (lane == 0) {
               ok = mbar_wait(bar(C::kBKEmpty + ks), ((k_cnt / C::kKStages) & 1) ^ 1, ctl, 801);
-              if (ok) mbar_arrive_expect_tx(bar(C::kBKFull + ks), C::kTileBytes);
+              if (ok)  // the step's K and V (V's copies may land first)
+                mbar_arrive_expect_tx(bar(C::kBStepFull + k_cnt % C::kStepBars), 2 * C::kTileBytes);
             }
             if (!(ok = __shfl_sync(pm, ok, 0))) break;
             __syncwarp(pm);
-            load_kv(sbase + C::kKOff + ks * C::kTileBytes, &tm_k, &tm_k8, bar(C::kBKFull + ks),
-                    hk, st, y);
+            load_kv(sbase + C::kKOff + ks * C::kTileBytes, &tm_k, &tm_k8,
+                    bar(C::kBStepFull + k_cnt % C::kStepBars), hk, st, y);
             ++k_cnt;
           }
           if (load_v) {
             const int vs = v_cnt % C::kVStages;
             if (lane == 0) {
               ok = mbar_wait(bar(C::kBVEmpty + vs), ((v_cnt / C::kVStages) & 1) ^ 1, ctl, 802);
-              if (ok) mbar_arrive_expect_tx(bar(C::kBVFull + vs), C::kTileBytes);
             }
             if (!(ok = __shfl_sync(pm, ok, 0))) break;
             __syncwarp(pm);
-            load_kv(sbase + C::kVOff + vs * C::kTileBytes, &tm_v, &tm_v8, bar(C::kBVFull + vs),
-                    hk, st, y);
+            load_kv(sbase + C::kVOff + vs * C::kTileBytes, &tm_v, &tm_v8,
+                    bar(C::kBStepFull + v_cnt % C::kStepBars), hk, st, y);
             ++v_cnt;
           }
         }
@@ -953,10 +954,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     if (!ok && lane == 0) {
       // let this warp's copies in flight land before the CTA exits
       if (q_cnt > 0) drain_wait_b(bar(C::kBQFull), (q_cnt - 1) & 1, kDrainNs);
-      for (uint32_t i = k_cnt > (uint32_t)C::kKStages ? k_cnt - C::kKStages : 0; i < k_cnt; ++i)
-        drain_wait_b(bar(C::kBKFull + i % C::kKStages), (i / C::kKStages) & 1, kDrainNs);
-      for (uint32_t i = v_cnt > (uint32_t)C::kVStages ? v_cnt - C::kVStages : 0; i < v_cnt; ++i)
-        drain_wait_b(bar(C::kBVFull + i % C::kVStages), (i / C::kVStages) & 1, kDrainNs);
+      const uint32_t n_cp = k_cnt > v_cnt ? k_cnt : v_cnt;  // steps this warp copied into
+      for (uint32_t i = n_cp > (uint32_t)C::kStepBars ? n_cp - C::kStepBars : 0; i < n_cp; ++i)
+        drain_wait_b(bar(C::kBStepFull + i % C::kStepBars), (i / C::kStepBars) & 1, kDrainNs);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -1002,11 +1002,11 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           tc_fence_after();
           {  // step 0: S and dP
             const int ks = kv_cnt % C::kKStages, vs = kv_cnt % C::kVStages;
-            if (!(ok = mbar_wait(bar(C::kBKFull + ks), (kv_cnt / C::kKStages) & 1, ctl, 901))) break;
+            if (!(ok = mbar_wait(bar(C::kBStepFull + kv_cnt % C::kStepBars),
+                                 (kv_cnt / C::kStepBars) & 1, ctl, 901)))
+              break;  // K and V of the step
             tc_fence_after();
             issue_s(0, ks);
-            if (!(ok = mbar_wait(bar(C::kBVFull + vs), (kv_cnt / C::kVStages) & 1, ctl, 902))) break;
-            tc_fence_after();
             issue_dp(vs);
             // V is read by the dP MMA only; the same arrival tells the dS
             // warps that this step's S and dP are in TMEM
@@ -1018,12 +1018,13 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
             if (v + 1 < n) {
               const uint32_t c1 = c + 1;
               const int k1 = c1 % C::kKStages, v1 = c1 % C::kVStages;
-              if (!(ok = mbar_wait(bar(C::kBKFull + k1), (c1 / C::kKStages) & 1, ctl, 903))) break;
+              if (!(ok = mbar_wait(bar(C::kBStepFull + c1 % C::kStepBars), (c1 / C::kStepBars) & 1,
+                                   ctl, 903)))
+                break;  // K and V of step v + 1
               tc_fence_after();
               issue_s((v + 1) & 1, k1);
               if (!(ok = mbar_wait(bar(C::kBDpFree), dpf_cnt & 1, ctl, 904))) break;
               ++dpf_cnt;
-              if (!(ok = mbar_wait(bar(C::kBVFull + v1), (c1 / C::kVStages) & 1, ctl, 905))) break;
               tc_fence_after();
               issue_dp(v1);
               mma_commit(bar(C::kBVEmpty + v1));  // V free; S and dP of step v + 1 ready
