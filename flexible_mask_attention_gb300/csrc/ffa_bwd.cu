@@ -831,13 +831,15 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     // plan has gathered steps; then warp 10 loads V (a gathered tile is 16
     // slots x D / 64 boxes per tensor, and each lane-issued copy costs the
     // issuing warp some 60 cycles), taking the items from the work queue like
-    // the consumers and waiting on the V ring itself.  Lane 0 of the loading
-    // warp waits on the rings and sets each barrier's byte count.  With
-    // gathered steps the whole warp runs the loop and the 16 slots of a
-    // gathered K/V tile (8 rows each, 1024-byte aligned, unused ones reading
-    // zero rows from row -8) are copied by lanes 0-15 in parallel after a
-    // __syncwarp that orders them behind the byte count; without them lane 0
-    // runs it alone (measured faster there).
+    // the consumers and waiting on the V ring itself.  Lane 0 of each loading
+    // warp waits on its ring's release; warp 8's sets the step barrier's byte
+    // count for the step's K and V (warp 10's V copies may land on it first:
+    // its phase cannot complete without that arrival).  With gathered steps
+    // the whole warp runs the loop and the 16 slots of a gathered K/V tile
+    // (8 rows each, 1024-byte aligned, unused ones reading zero rows from row
+    // -8) are copied by lanes 0-15 in parallel after a __syncwarp that orders
+    // them behind the wait; without them lane 0 runs it alone (measured
+    // faster there).
     const bool role0 = warp == 8;
     const bool load_k = role0, load_v = !kGather || !role0;
     if (lane == 0) {
